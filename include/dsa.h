@@ -1,0 +1,247 @@
+/*
+ * dsa.h — C ABI of libdsa: query-aware dynamic block-sparse decode attention over a paged bf16
+ * KV cache, for NVIDIA GB300 (sm_103a).
+ *
+ * Sources restated (cited by title and section):
+ *   [PSA]    "PSA: Progressive Sparse Attention — Algorithm and System Co-design for Efficient
+ *             Attention in LLM Serving"
+ *   [LServe] "LServe: Efficient Long-sequence LLM Serving with Unified Sparse Attention"
+ *   [PRR]    "Predict, Reuse, and Repair: Accelerating Dynamic Sparse Attention for Long-Context
+ *             LLM Decoding"
+ *
+ * Conventions shared by every entry point
+ * ---------------------------------------
+ *  - Every pointer argument is a DEVICE pointer owned by the caller unless marked "host".  The
+ *    library keeps no state between calls, allocates no memory, never synchronises the device and
+ *    enqueues all work on `stream` (a cudaStream_t passed as void*; NULL = legacy default stream).
+ *  - Return value: DSA_OK (0) once the kernels are enqueued, or a negative DSA_ERR_* code when a
+ *    host-side check fails, in which case nothing was enqueued; dsa_last_error() then returns a
+ *    message for the calling thread.  Launch failures return DSA_ERR_CUDA.
+ *  - Shapes: B = batch (requests), Hq = query heads, Hkv = KV heads, G = Hq / Hkv (query heads per
+ *    KV head, 1..16), D = head_dim (128), p = page_size (multiple of 16, 16..256).
+ *  - Softmax: logits s_t = scale * (q . k_t); m = max_t s_t (natural-log units); l = sum_t
+ *    exp(s_t - m); O = sum_t exp(s_t - m) v_t / l.  An empty token set gives O = 0, m = -inf, l = 0.
+ *  - Page ids read from the page table are checked against num_phys_pages; a bad id is skipped
+ *    (its tokens contribute nothing) and DSA_STATUS_BAD_PAGE is OR-ed into *status when
+ *    kv->status is non-NULL.
+ *  - Scores use -inf for "no page here"; selection only ever picks pages with a score > -inf.
+ */
+#ifndef DSA_H_
+#define DSA_H_
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+typedef void* dsa_stream_t; /* cudaStream_t */
+
+enum {
+  DSA_OK = 0,
+  DSA_ERR_INVALID_ARG = -1, /* null pointer, negative size, inconsistent shapes */
+  DSA_ERR_ALIGNMENT = -2,   /* pointer not aligned as documented (16 B for bf16 pools) */
+  DSA_ERR_UNSUPPORTED = -3, /* shape outside what the kernels implement (D != 128, G > 16, ...) */
+  DSA_ERR_CUDA = -4,        /* a CUDA runtime / driver call failed */
+  DSA_ERR_WORKSPACE = -5    /* workspace missing or smaller than the size query returned */
+};
+
+/* Bits a kernel may OR into kv->status (device int32).  Never set by a correct call. */
+enum { DSA_STATUS_BAD_PAGE = 1, DSA_STATUS_OVERFLOW = 2 };
+
+enum { DSA_META_MINMAX = 0, DSA_META_MEAN = 1 };
+enum { DSA_EMA_INIT = 0, DSA_EMA_UPDATE = 1 };
+enum { DSA_PSA_NLEFT = 1 };
+
+/*
+ * The paged KV cache (the block/page KV cache of [PSA] §3.1 and [LServe] §3.2.1).
+ *   k_pages, v_pages : bf16 [num_phys_pages][Hkv][p][D], 16-byte aligned, contiguous.  Token t of
+ *                      request b is slot t % p of physical page page_table[b][t / p].
+ *   page_table       : int32 [B][max_pages_per_seq].
+ *   seq_lens         : int32 [B], tokens in the cache for each request (0 <= L_b <= p * max_pages).
+ *   head_is_streaming: uint8 [Hkv] or NULL.  Non-zero marks a streaming (Lambda-mask) KV head
+ *                      ([LServe] §4.1, dual cache §3.2.1): the dense-path calls (scoring,
+ *                      selection, sparse attention, repair) skip those heads and leave their
+ *                      outputs untouched; dsa_streaming_head_attn serves only those heads.
+ *   status           : int32 [1] or NULL; device-detected problems are OR-ed into it.
+ * The struct itself is read on the host during the call and not retained.
+ */
+typedef struct dsa_paged_kv {
+  const void* k_pages;
+  const void* v_pages;
+  const int32_t* page_table;
+  const int32_t* seq_lens;
+  const uint8_t* head_is_streaming;
+  int32_t* status;
+  int32_t batch;
+  int32_t num_q_heads;
+  int32_t num_kv_heads;
+  int32_t head_dim;
+  int32_t page_size;
+  int32_t max_pages_per_seq;
+  int32_t num_phys_pages;
+} dsa_paged_kv;
+
+/* Message for the last failed call on this host thread ("" if none). Host string, not owned. */
+const char* dsa_last_error(void);
+/* Library version string (host, static). */
+const char* dsa_version(void);
+
+/*
+ * Per-page key metadata ([LServe] §4.2 and Figure 7: k_max / k_min kept with each page;
+ * [PSA] §5: cuboid-mean block metadata).
+ *   meta_kind    : DSA_META_MINMAX or DSA_META_MEAN.
+ *   logical_page : tokens per logical page; divides p (g = p / logical_page sub-pages per page).
+ *   meta (out)   : MINMAX -> bf16 [num_phys_pages][Hkv][g][D][2], pairs (max, min) per dimension;
+ *                  MEAN   -> fp32 [num_phys_pages][Hkv][g][D].  16-byte aligned.
+ * Every (request, page position j < ceil(L_b / p)) is processed: the physical page it maps to
+ * gets the max/min (exact in bf16) or the fp32 mean of its valid tokens per logical sub-page.  A
+ * sub-page with no valid token is written as zeros.  Physical pages no request reaches are left
+ * untouched.  Streaming heads are processed too (the data is per page, not per head kind).
+ */
+int dsa_build_page_meta(const dsa_paged_kv* kv, int32_t meta_kind, int32_t logical_page,
+                        void* meta, dsa_stream_t stream);
+
+/*
+ * Page criticality ([LServe] §4.2: S^j = sum_i max(q_i kmax^j_i, q_i kmin^j_i); [PSA] §3.2:
+ * CS = q . meta; [PRR] §5: one representative query per KV head for GQA).
+ *   q            : bf16 [B][Hq][D].  The representative query of KV head h is the fp32 mean of
+ *                  its G query heads h*G .. h*G+G-1.
+ *   meta         : as written by dsa_build_page_meta with the same meta_kind / logical_page.
+ *   scores (out) : fp32 [B][Hkv][score_stride]; score_stride >= max_pages_per_seq * g.  Logical
+ *                  page j < ceil(L_b / logical_page) gets its score; slots beyond get -inf; the
+ *                  whole row of a streaming head gets -inf.
+ */
+int dsa_score_pages(const dsa_paged_kv* kv, const void* q, const void* meta, int32_t meta_kind,
+                    int32_t logical_page, float* scores, int32_t score_stride,
+                    dsa_stream_t stream);
+
+/*
+ * Fixed-budget top-K page selection (the baseline selection of [PSA] §2.2 and [PRR] §2).
+ *   scores      : fp32 [rows][stride]; entries 0..n-1 of each row are candidates; an entry
+ *                 counts as valid when > -inf (NaN is invalid).
+ *   k           : budget (>= 0).
+ *   idx (out)   : int32 [rows][idx_stride], idx_stride >= k.  The min(k, #valid) highest-scoring
+ *                 valid entries, ties to the lower index, written in ASCENDING index order;
+ *                 slots past the count are set to -1.
+ *   count (out) : int32 [rows].
+ * n <= 65536.  One CTA per row.
+ */
+int dsa_select_topk(const float* scores, int32_t rows, int32_t n, int32_t stride, int32_t k,
+                    int32_t* idx, int32_t idx_stride, int32_t* count, dsa_stream_t stream);
+
+/*
+ * Hierarchical paging selection ([LServe] §4.2): the score of physical page P is the max of the
+ * logical scores P*g .. P*g+g-1 (restricted to < n_logical); then top-k_phys physical pages as in
+ * dsa_select_topk (valid = > -inf, ties to the lower index, ascending output).  g = 1 is flat
+ * top-K.  idx holds physical page POSITIONS within the request (units of p tokens).
+ */
+int dsa_select_hier(const float* logical_scores, int32_t rows, int32_t n_logical, int32_t stride,
+                    int32_t g, int32_t k_phys, int32_t* idx, int32_t idx_stride, int32_t* count,
+                    dsa_stream_t stream);
+
+/*
+ * PSA progressive threshold selection with fused attention ([PSA] §3.2, with the on-device
+ * verification of §3.3: the stop decision never leaves the GPU).
+ * For each dense (request b, KV head h): rank pages (block = one page of p tokens) by scores
+ * (descending, ties to the lower index), visit them in rank order and stop after the first block
+ * where, for every query head of the group, AS_acc / (AS_acc + AS_min) >= tau (AS = unnormalised
+ * softmax mass of a block, AS_acc their running sum, AS_min the smallest seen), or after `cap`
+ * blocks, or when the valid blocks run out.  With flags & DSA_PSA_NLEFT the rule reads
+ * AS_acc / (AS_acc + N_left * AS_min), N_left = valid blocks not yet visited.
+ *   scores       : fp32 [B][Hkv][score_stride] (one score per page, e.g. DSA_META_MEAN with
+ *                  logical_page == p).
+ *   tau          : 0 < tau <= 1.  cap >= 1.
+ *   idx (out)    : int32 [B][Hkv][idx_stride], idx_stride >= cap: visited page positions in
+ *                  visiting (rank) order; count (out) int32 [B][Hkv].
+ *   out/m/l (out): fp32 [B][Hq][D], [B][Hq], [B][Hq]: attention over the visited blocks.
+ * ranks n_valid <= 65536 pages per row.
+ */
+int dsa_select_threshold(const dsa_paged_kv* kv, const void* q, const float* scores,
+                         int32_t score_stride, float tau, int32_t cap, int32_t flags, float scale,
+                         int32_t* idx, int32_t idx_stride, int32_t* count, float* out, float* m,
+                         float* l, dsa_stream_t stream);
+
+/*
+ * Exact attention over the selected pages, split over pages (split-K) with a log-sum-exp merge
+ * ([LServe] §3.3: iterate only the selected KV pages; [PRR] §3.3: the instrumented forward that
+ * also writes m and l).
+ *   idx, count   : int32 [B][Hkv][idx_stride], int32 [B][Hkv]: page positions (units of p) of
+ *                  each dense row; order is free; positions >= ceil(L_b / p) or < 0 are skipped.
+ *   out/m/l      : fp32 [B][Hq][D], [B][Hq], [B][Hq]; may be NULL when page_partials is given.
+ *   page_partials: NULL, or fp32 [B][Hkv][idx_stride][G][D + 4]: for selected slot i the partial
+ *                  record (O_0..O_{D-1}, m, l, 0, 0) of attention over that page alone (the
+ *                  per-page partials PRR's exact repair merges).  Slots >= count are not written.
+ *   num_splits   : pages of a row are spread over this many CTAs (0 = choose automatically).
+ *   workspace    : device scratch of at least dsa_sparse_decode_attn_workspace_size() bytes,
+ *                  16-byte aligned (may be NULL when that size is 0).
+ */
+int dsa_sparse_decode_attn(const dsa_paged_kv* kv, const void* q, const int32_t* idx,
+                           int32_t idx_stride, const int32_t* count, float scale, float* out,
+                           float* m, float* l, float* page_partials, int32_t num_splits,
+                           void* workspace, size_t workspace_bytes, dsa_stream_t stream);
+size_t dsa_sparse_decode_attn_workspace_size(const dsa_paged_kv* kv, int32_t idx_stride,
+                                             int32_t num_splits);
+
+/*
+ * PRR repair and merge ([PRR] §3.3 repair kernel and recurrence).  Given the speculative set P
+ * (spec_idx/spec_count, ASCENDING and unique) whose per-page partials a previous
+ * dsa_sparse_decode_attn wrote to page_partials (same idx_stride = spec_stride), and the true set
+ * A (true_idx/true_count, ASCENDING and unique): attention is computed only for the missed pages
+ * M = A \ P, and merged with the partials of
+ *     superset == 0: P ∩ A          -> out = attention over A exactly,
+ *     superset != 0: all of P       -> out = attention over P ∪ A.
+ *   out/m/l (out): fp32 [B][Hq][D], [B][Hq], [B][Hq].
+ *   workspace    : at least dsa_repair_merge_workspace_size() bytes.
+ */
+int dsa_repair_merge(const dsa_paged_kv* kv, const void* q, const int32_t* spec_idx,
+                     int32_t spec_stride, const int32_t* spec_count, const float* page_partials,
+                     const int32_t* true_idx, int32_t true_stride, const int32_t* true_count,
+                     int32_t superset, float scale, float* out, float* m, float* l,
+                     void* workspace, size_t workspace_bytes, dsa_stream_t stream);
+size_t dsa_repair_merge_workspace_size(const dsa_paged_kv* kv, int32_t true_stride);
+
+/*
+ * Streaming heads ([LServe] §4.1, Lambda-shaped mask): for every KV head marked in
+ * kv->head_is_streaming, exact attention of its G query heads over tokens
+ * [0, min(sink, L_b)) ∪ [max(0, L_b - local), L_b).  Writes out/m/l rows of those heads only.
+ */
+int dsa_streaming_head_attn(const dsa_paged_kv* kv, const void* q, int32_t sink_tokens,
+                            int32_t local_tokens, float scale, float* out, float* m, float* l,
+                            dsa_stream_t stream);
+
+/*
+ * PRR EMA predictor ([PRR] §3.1) fused with the speculative-set selection ([PRR] §3.4 with a fixed
+ * budget |P| = k_pred).
+ *   IS           : fp32 [rows][stride], the true scores of this step (entries 0..n-1; -inf =
+ *                  no page).
+ *   ell, v       : fp32 [rows][stride] level and trend, updated in place:
+ *                  DSA_EMA_INIT  : ell = IS, v = 0;
+ *                  DSA_EMA_UPDATE: v = beta (IS - ell) + (1 - beta) v, ell = alpha IS + (1 - alpha)
+ *                                  ell (both read the previous ell).
+ *                  Entries with IS = -inf get ell = -inf, v = 0.
+ *   pred (out)   : fp32 [rows][stride] or NULL: the next step's prediction ell + gamma v (-inf
+ *                  where ell = -inf).
+ *   pred_idx/pred_count (out): top-k_pred of the prediction, as dsa_select_topk (may be NULL
+ *                  when k_pred == 0).
+ */
+int dsa_ema_predict_update(const float* IS, int32_t rows, int32_t n, int32_t stride, float* ell,
+                           float* v, int32_t mode, float alpha, float beta, float gamma,
+                           float* pred, int32_t k_pred, int32_t* pred_idx,
+                           int32_t pred_idx_stride, int32_t* pred_count, dsa_stream_t stream);
+
+/*
+ * Log-sum-exp merge of partial records ([PRR] §3.3 recurrence, applied to all parts at once).
+ *   partials : fp32 [rows][num_parts][G][D + 4] records (O, m, l, 0, 0); a record with l == 0 is
+ *              the identity.
+ *   out/m/l  : fp32 [rows * G][D], [rows * G], [rows * G].
+ */
+int dsa_merge_partials(const float* partials, int32_t rows, int32_t num_parts, int32_t group,
+                       int32_t head_dim, float* out, float* m, float* l, dsa_stream_t stream);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* DSA_H_ */

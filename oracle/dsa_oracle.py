@@ -1,0 +1,409 @@
+"""Plain float64 CPU oracle of the dynamic block-sparse decode step.
+
+TEST INFRASTRUCTURE ONLY: imported by ``tests/``, ``__graft_entry__.smoke()`` and the CPU arm of
+``bench.py``; never by the product path.  Nothing here is shared with, or imported from, the CUDA
+library.  Every routine works on one (request, KV head) row at a time in float64 with plain numpy,
+and states the passage it restates:
+
+* *PSA*   = "PSA: Progressive Sparse Attention — Algorithm and System Co-design for Efficient
+  Attention in LLM Serving",
+* *LServe* = "LServe: Efficient Long-sequence LLM Serving with Unified Sparse Attention",
+* *PRR*   = "Predict, Reuse, and Repair: Accelerating Dynamic Sparse Attention for Long-Context LLM
+  Decoding".
+
+Readings taken where the pages are silent or garbled (each also listed in the design notes):
+
+* softmax logits are ``scale * q.k`` with ``m`` the natural-log running max; ``l = sum exp(s - m)``
+  and ``O`` is normalised (``O = sum exp(s - m) v / l``);
+* the GQA representative query is the arithmetic mean of the group's query heads;
+* pages past the request length score ``-inf`` and are never selected; tokens past the length are
+  masked out of attention;
+* top-K ties go to the lower page index; selections are returned in ascending page order, except
+  the PSA ranking, which is returned in rank order;
+* the PSA stop rule is the literal ``AS_acc / (AS_acc + AS_min) >= tau`` (the ``N_left`` counter
+  the listing maintains is unused there; ``use_nleft`` switches to
+  ``AS_acc / (AS_acc + N_left * AS_min)``); with a GQA group the rule must hold for every query head
+  of the group;
+* the EMA update uses the previous level in both equations, exactly as printed;
+* PRR's exact mode drops speculative pages outside the true set (output equals attention over the
+  true set); its superset mode keeps them (output equals attention over the union).
+"""
+
+from __future__ import annotations
+
+import itertools
+import math
+
+import numpy as np
+
+NEG_INF = -math.inf
+
+__all__ = [
+    "to_f64", "request_tokens",
+    "page_meta_minmax", "page_meta_mean",
+    "representative_query", "score_pages_minmax", "score_pages_mean", "pad_scores",
+    "rank_pages", "select_topk", "physical_scores", "select_hier",
+    "page_token_ids", "streaming_token_ids", "attend", "merge_partials", "page_partials",
+    "psa_progressive",
+    "ema_init", "ema_update", "ema_predict",
+    "spec_repair", "hit_rate", "score_weighted_hit", "calibration_grid", "calibrate_ema",
+]
+
+
+# --------------------------------------------------------------------------------------------
+# inputs
+# --------------------------------------------------------------------------------------------
+
+def to_f64(x) -> np.ndarray:
+    """Exact float64 copy of a numpy array or a CPU/GPU torch tensor (bf16 widens exactly)."""
+    if hasattr(x, "detach"):
+        return x.detach().to("cpu").double().numpy()
+    return np.asarray(x, dtype=np.float64)
+
+
+def _to_int(x) -> np.ndarray:
+    if hasattr(x, "detach"):
+        return x.detach().to("cpu").long().numpy()
+    return np.asarray(x, dtype=np.int64)
+
+
+def request_tokens(pool, page_table, seq_len: int, b: int, h: int) -> np.ndarray:
+    """Rows ``[seq_len][D]`` of one request and KV head, read through the page table.
+
+    Token ``t`` of request ``b`` lives in physical page ``page_table[b][t // page]`` at slot
+    ``t % page`` of a pool laid out ``[phys_page][kv_head][slot][D]`` (the block/page KV cache of
+    *PSA* §3.1 and *LServe* §3.2.1).
+    """
+    page = int(pool.shape[2])
+    table = _to_int(page_table[b])
+    rows = []
+    for start in range(0, seq_len, page):
+        phys = int(table[start // page])
+        n = min(page, seq_len - start)
+        rows.append(to_f64(pool[phys, h, :n]))
+    if not rows:
+        return np.zeros((0, int(pool.shape[3])))
+    return np.concatenate(rows, axis=0)
+
+
+# --------------------------------------------------------------------------------------------
+# per-page key metadata (LServe §4.2 / Figure 7; PSA §5 cuboid-mean metadata)
+# --------------------------------------------------------------------------------------------
+
+def page_meta_minmax(keys: np.ndarray, logical_page: int):
+    """Element-wise max and min key of every logical page, over its valid tokens only.
+
+    Returns ``kmax, kmin`` of shape ``[ceil(L / logical_page)][D]`` (LServe §4.2: the k_max and
+    k_min vectors attached to every page).
+    """
+    L, D = keys.shape
+    n = -(-L // logical_page)
+    kmax = np.empty((n, D))
+    kmin = np.empty((n, D))
+    for j in range(n):
+        seg = keys[j * logical_page:(j + 1) * logical_page]
+        kmax[j] = seg.max(axis=0)
+        kmin[j] = seg.min(axis=0)
+    return kmax, kmin
+
+
+def page_meta_mean(keys: np.ndarray, block: int) -> np.ndarray:
+    """Mean key of every block over its valid tokens (PSA §5: cuboid-mean block metadata)."""
+    L, D = keys.shape
+    n = -(-L // block)
+    out = np.empty((n, D))
+    for j in range(n):
+        seg = keys[j * block:(j + 1) * block]
+        out[j] = seg.sum(axis=0) / seg.shape[0]
+    return out
+
+
+# --------------------------------------------------------------------------------------------
+# page criticality (LServe §4.2 importance formula; PSA §3.2 CS = q . B_meta; PRR §5 GQA query)
+# --------------------------------------------------------------------------------------------
+
+def representative_query(q_group) -> np.ndarray:
+    """One query per KV head: the mean of the group's query heads (PRR §5, Quest GQA extension)."""
+    q = to_f64(q_group)
+    return q.mean(axis=0)
+
+
+def score_pages_minmax(qbar: np.ndarray, kmax: np.ndarray, kmin: np.ndarray) -> np.ndarray:
+    """``S^j = sum_i max(q_i * kmax_i^j, q_i * kmin_i^j)`` for every logical page j (LServe §4.2)."""
+    return np.maximum(qbar[None, :] * kmax, qbar[None, :] * kmin).sum(axis=1)
+
+
+def score_pages_mean(qbar: np.ndarray, kmean: np.ndarray) -> np.ndarray:
+    """Criticality ``CS_j = q . mean_j`` of every block (PSA §3.2, first step of PSAttention)."""
+    return kmean @ qbar
+
+
+def pad_scores(scores: np.ndarray, stride: int) -> np.ndarray:
+    """Scores laid out over ``stride`` slots; slots past the last valid page hold ``-inf``."""
+    out = np.full(stride, NEG_INF)
+    out[:len(scores)] = scores
+    return out
+
+
+# --------------------------------------------------------------------------------------------
+# selection
+# --------------------------------------------------------------------------------------------
+
+def rank_pages(scores) -> list[int]:
+    """Valid pages (score > -inf) ordered by score descending, ties to the lower page index."""
+    s = np.asarray(scores, dtype=np.float64)
+    valid = [j for j in range(len(s)) if s[j] > NEG_INF]
+    return sorted(valid, key=lambda j: (-s[j], j))
+
+
+def select_topk(scores, k: int) -> list[int]:
+    """Fixed-budget selection: the k most critical valid pages, ascending page order.
+
+    The baseline dynamic sparse attention every page discusses (PSA §2.2; PRR §2 selection stage).
+    A budget at or above the number of valid pages selects all of them.
+    """
+    return sorted(rank_pages(scores)[:k])
+
+
+def physical_scores(logical_scores, g: int) -> np.ndarray:
+    """Importance of a physical page = max over its g logical pages (LServe §4.2)."""
+    s = np.asarray(logical_scores, dtype=np.float64)
+    n_phys = -(-len(s) // g)
+    return np.array([s[p * g:(p + 1) * g].max() for p in range(n_phys)])
+
+
+def select_hier(logical_scores, g: int, k_phys: int) -> list[int]:
+    """Hierarchical paging: max-reduce logical scores per physical page, then top-k physical."""
+    return select_topk(physical_scores(logical_scores, g), k_phys)
+
+
+# --------------------------------------------------------------------------------------------
+# exact attention over a token set and the online-softmax merge (PRR §3.3)
+# --------------------------------------------------------------------------------------------
+
+def page_token_ids(pages, page_size: int, seq_len: int) -> np.ndarray:
+    """Token positions covered by the listed pages, clipped to the request length."""
+    ids = []
+    for j in pages:
+        lo = int(j) * page_size
+        ids.extend(range(lo, min(lo + page_size, seq_len)))
+    return np.asarray(ids, dtype=np.int64)
+
+
+def streaming_token_ids(seq_len: int, sink: int, local: int) -> np.ndarray:
+    """Lambda-shaped window of a streaming head: the first ``sink`` and last ``local`` tokens
+    (LServe §4.1).  Overlapping windows count each token once."""
+    keep = set(range(min(sink, seq_len))) | set(range(max(0, seq_len - local), seq_len))
+    return np.asarray(sorted(keep), dtype=np.int64)
+
+
+def attend(q, keys: np.ndarray, values: np.ndarray, token_ids, scale: float):
+    """Softmax attention of every query row over the listed tokens.
+
+    ``q`` is ``[G][D]``.  Returns ``(O [G][D], m [G], l [G])`` with logits ``s = scale * q . k``,
+    ``m = max s``, ``l = sum exp(s - m)`` and ``O = sum exp(s - m) v / l``.  An empty token set gives
+    ``O = 0, m = -inf, l = 0``.
+    """
+    q = to_f64(q)
+    G, D = q.shape
+    ids = np.asarray(token_ids, dtype=np.int64)
+    if ids.size == 0:
+        return np.zeros((G, D)), np.full(G, NEG_INF), np.zeros(G)
+    s = scale * (q @ keys[ids].T)
+    m = s.max(axis=1)
+    e = np.exp(s - m[:, None])
+    l = e.sum(axis=1)
+    O = (e @ values[ids]) / l[:, None]
+    return O, m, l
+
+
+def merge_partials(parts):
+    """Fold partial results ``(O, m, l)`` over disjoint token sets into one.
+
+    Applies the PRR §3.3 repair recurrence once per part: the running max is raised to the new
+    max, both denominators are rescaled to it, and the normalised outputs are re-weighted by their
+    share of the merged denominator.  Parts with ``l == 0`` (empty sets) are the identity.
+    """
+    parts = list(parts)
+    G, D = parts[0][0].shape
+    O = np.zeros((G, D))
+    m = np.full(G, NEG_INF)
+    l = np.zeros(G)
+    for (Op, mp, lp) in parts:
+        for g in range(G):
+            if lp[g] == 0.0:
+                continue
+            if l[g] == 0.0:
+                O[g], m[g], l[g] = Op[g], mp[g], lp[g]
+                continue
+            m_new = max(m[g], mp[g])
+            a = math.exp(m[g] - m_new) * l[g]
+            b = math.exp(mp[g] - m_new) * lp[g]
+            O[g] = (a * O[g] + b * Op[g]) / (a + b)
+            m[g] = m_new
+            l[g] = a + b
+    return O, m, l
+
+
+def page_partials(q, keys, values, pages, page_size: int, seq_len: int, scale: float):
+    """One ``(O, m, l)`` partial per listed page (the instrumented speculative pass of PRR §3.3,
+    kept per page so partials of pages outside the true set can be dropped)."""
+    return {int(j): attend(q, keys, values, page_token_ids([j], page_size, seq_len), scale)
+            for j in pages}
+
+
+# --------------------------------------------------------------------------------------------
+# PSA progressive threshold selection (PSA §3.2)
+# --------------------------------------------------------------------------------------------
+
+def psa_progressive(q, keys, values, block_scores, block: int, seq_len: int, tau: float,
+                    cap: int, scale: float, use_nleft: bool = False):
+    """Threshold-driven block selection with fused outputs, as PSA §3.2 describes.
+
+    Blocks are visited in criticality order (score descending, ties to the lower index).  For each
+    visited block the unnormalised attention mass ``AS`` (sum of ``exp(s - M)`` over its tokens, with
+    one reference ``M`` shared by every block so that ratios are exact) and its normalised output
+    are folded into the accumulated output by mass weighting; the accumulated mass and the smallest
+    block mass seen so far are tracked, and the walk ends at the first block after which
+    ``AS_acc / (AS_acc + AS_min) >= tau`` holds for every query row, or when ``cap`` blocks were
+    visited, or when the blocks run out.
+
+    Returns a dict with ``ranked`` (the visited blocks in visiting order), ``O_fused`` (the
+    mass-weighted fusion, ``[G][D]``), ``m`` and ``l`` (the natural-log max and denominator over the
+    visited tokens) and ``ratios`` (the stop-rule ratio after each visited block, per row).
+    """
+    q = to_f64(q)
+    G, D = q.shape
+    order = rank_pages(block_scores)
+    if not order:
+        return dict(ranked=[], O_fused=np.zeros((G, D)), m=np.full(G, NEG_INF), l=np.zeros(G),
+                    ratios=[])
+    all_ids = page_token_ids(order, block, seq_len)
+    M = (scale * (q @ keys[all_ids].T)).max(axis=1)   # common reference for the masses
+    O_acc = np.zeros((G, D))
+    AS_acc = np.zeros(G)
+    AS_min = np.full(G, np.inf)
+    remaining = len(order)
+    visited, ratios = [], []
+    for b in order:
+        if len(visited) == cap:
+            break
+        ids = page_token_ids([b], block, seq_len)
+        w = np.exp(scale * (q @ keys[ids].T) - M[:, None])     # [G][T]
+        AS = w.sum(axis=1)
+        O_b = (w @ values[ids]) / AS[:, None]
+        O_acc = (AS_acc[:, None] * O_acc + AS[:, None] * O_b) / (AS_acc + AS)[:, None]
+        AS_acc = AS_acc + AS
+        AS_min = np.minimum(AS_min, AS)
+        remaining -= 1
+        visited.append(b)
+        denom_min = remaining * AS_min if use_nleft else AS_min
+        ratio = AS_acc / (AS_acc + denom_min)
+        ratios.append(ratio)
+        if np.all(ratio >= tau):
+            break
+    ids = page_token_ids(visited, block, seq_len)
+    s = scale * (q @ keys[ids].T)
+    m = s.max(axis=1)
+    l = np.exp(s - m[:, None]).sum(axis=1)
+    return dict(ranked=visited, O_fused=O_acc, m=m, l=l, ratios=ratios)
+
+
+# --------------------------------------------------------------------------------------------
+# PRR: EMA predictor (§3.1), calibration (§3.2), speculate + repair (§3.3), budget (§3.4)
+# --------------------------------------------------------------------------------------------
+
+def ema_init(IS):
+    """State after the first observed score vector: level = IS, trend = 0 (invalid pages keep a
+    -inf level and a zero trend)."""
+    IS = np.asarray(IS, dtype=np.float64)
+    return IS.copy(), np.zeros_like(IS)
+
+
+def ema_update(IS, ell, v, alpha: float, beta: float):
+    """PRR §3.1 update with the true scores of step t; both equations read the level of step t-1:
+    ``v_t = beta (IS_t - l_{t-1}) + (1 - beta) v_{t-1}`` and ``l_t = alpha IS_t + (1 - alpha) l_{t-1}``.
+    Pages whose score is -inf keep level -inf and trend 0."""
+    IS = np.asarray(IS, dtype=np.float64)
+    valid = IS > NEG_INF
+    v_new = np.zeros_like(IS)
+    l_new = np.full_like(IS, NEG_INF)
+    v_new[valid] = beta * (IS[valid] - ell[valid]) + (1.0 - beta) * v[valid]
+    l_new[valid] = alpha * IS[valid] + (1.0 - alpha) * ell[valid]
+    return l_new, v_new
+
+
+def ema_predict(ell, v, gamma: float):
+    """PRR §3.1 prediction before selection: ``IS_hat_t = l_{t-1} + gamma v_{t-1}``."""
+    ell = np.asarray(ell, dtype=np.float64)
+    out = np.full_like(ell, NEG_INF)
+    ok = ell > NEG_INF
+    out[ok] = ell[ok] + gamma * np.asarray(v)[ok]
+    return out
+
+
+def spec_repair(q, keys, values, page_size: int, seq_len: int, spec_pages, true_pages,
+                scale: float, superset: bool = False):
+    """Speculate over P, then repair with the missed pages M = A \\ P (PRR §3.3).
+
+    The speculative pass yields one partial per page of P.  Exact mode merges the partials of
+    P ∩ A with fresh partials of A \\ P, which is attention over A.  Superset mode merges every
+    partial of P with those of A \\ P (the recurrence applied to the whole speculative result),
+    which is attention over P ∪ A.
+    """
+    P = sorted(set(int(j) for j in spec_pages))
+    A = sorted(set(int(j) for j in true_pages))
+    spec = page_partials(q, keys, values, P, page_size, seq_len, scale)
+    missed = [j for j in A if j not in spec]
+    repair = page_partials(q, keys, values, missed, page_size, seq_len, scale)
+    keep = P if superset else [j for j in P if j in set(A)]
+    parts = [spec[j] for j in keep] + [repair[j] for j in missed]
+    if not parts:
+        G, D = to_f64(q).shape
+        return np.zeros((G, D)), np.full(G, NEG_INF), np.zeros(G)
+    return merge_partials(parts)
+
+
+def hit_rate(spec_pages, true_pages) -> float:
+    """|P ∩ A| / |A|."""
+    A = set(int(j) for j in true_pages)
+    if not A:
+        return 1.0
+    return len(A & set(int(j) for j in spec_pages)) / len(A)
+
+
+def score_weighted_hit(spec_pages, true_pages, IS) -> float:
+    """One term of PRR §3.2's objective H: true-set score mass covered by the prediction."""
+    A = [int(j) for j in true_pages]
+    P = set(int(j) for j in spec_pages)
+    den = sum(IS[j] for j in A)
+    num = sum(IS[j] for j in A if j in P)
+    return num / den if den != 0 else 1.0
+
+
+def calibration_grid():
+    """PRR §3.2 search space: alpha 0.2..0.8 step 0.2, beta 0.1..0.5 step 0.1, gamma 0..0.75 step
+    0.25, as (alpha, beta, gamma) triples in that nesting order."""
+    alphas = [0.2 * i for i in range(1, 5)]
+    betas = [0.1 * i for i in range(1, 6)]
+    gammas = [0.25 * i for i in range(0, 4)]
+    return list(itertools.product(alphas, betas, gammas))
+
+
+def calibrate_ema(IS_traj, k: int, k_pred: int):
+    """PRR §3.2: choose (alpha, beta, gamma) maximising the mean score-weighted hit rate H over a
+    score trajectory ``IS_traj`` ``[T][n]``.  The first step initialises the state; steps 1..T-1
+    are scored.  Ties go to the first candidate in grid order.  Returns (best triple, H values)."""
+    traj = [np.asarray(x, dtype=np.float64) for x in IS_traj]
+    Hs = []
+    for (a, b, c) in calibration_grid():
+        ell, v = ema_init(traj[0])
+        total = 0.0
+        for t in range(1, len(traj)):
+            P = select_topk(ema_predict(ell, v, c), k_pred)
+            A = select_topk(traj[t], k)
+            total += score_weighted_hit(P, A, traj[t])
+            ell, v = ema_update(traj[t], ell, v, a, b)
+        Hs.append(total / max(1, len(traj) - 1))
+    best = int(np.argmax(Hs))
+    return calibration_grid()[best], Hs
