@@ -1,0 +1,511 @@
+#!/usr/bin/env python3
+"""Decode-step benchmark of the dynamic block-sparse attention path on GB300.
+
+Default workload: PRR speculate-and-repair decode at 512K tokens (1 request, 32 query heads on 2
+KV heads, head_dim 128, block 64, top-64 true blocks, |P| = 76 predicted blocks, EMA predictor
+alpha 0.6 / beta 0.3 / gamma 0.5, query random walk N(0, 0.05)).  One bench step is one decode
+step of the whole path: page scoring over the kmax/kmin metadata, top-K selection, speculative
+attention over P (on a second stream, concurrently with scoring/selection), repair of A \\ P
+with the log-sum-exp merge, and the EMA update that predicts the next P.  The step is captured
+once as a CUDA graph and replayed; L2 is flushed (a 256 MiB write) before every timed step and
+the flush is outside the timed window.
+
+value = algorithmic bytes of the step / device time of the step (GB/s): metadata read by scoring
++ K/V of every page attended (P and A \\ P) + auxiliary state (query, scores, EMA level/trend,
+predictions, index lists, partial records).  ms_per_step is the same step's device time.
+
+--impl reference times the float64 oracle (the CPU definition the CUDA path is checked against)
+on the same workload, metric and unit, on this host's cores.
+"""
+
+from __future__ import annotations
+
+import argparse
+import json
+import math
+import os
+import statistics
+import subprocess
+import sys
+import threading
+import time
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+METRIC = "selected-KV GB/s and decode attn µs/step at 1 GB300; fraction of HBM roofline"
+FALLBACK_HBM_GBS = 6800.0
+L2_FLUSH_BYTES = 256 << 20
+
+
+def parse_args(argv=None):
+    p = argparse.ArgumentParser()
+    p.add_argument("--gpus", type=int, default=1)
+    p.add_argument("--steps", type=int, default=2000)
+    p.add_argument("--warmup", type=int, default=20)
+    p.add_argument("--impl", choices=["ours", "reference"], default="ours")
+    p.add_argument("--workload", default="prr_512k")
+    p.add_argument("--no-e2e", action="store_true")
+    p.add_argument("--cpu-seconds", type=float, default=12.0)
+    p.add_argument("--no-cpu-baseline", action="store_true")
+    p.add_argument("--oracle-child", action="store_true", help=argparse.SUPPRESS)
+    return p.parse_args(argv)
+
+
+# ------------------------------------------------------------------------------------ helpers
+
+def load_peaks():
+    path = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    try:
+        with open(path) as f:
+            d = json.load(f)
+        return float(d["hbm_gbs"]), "measured (MEASURED_PEAKS.json hbm_gbs)"
+    except Exception:
+        return FALLBACK_HBM_GBS, "fallback"
+
+
+class ClockSampler:
+    """nvidia-smi clock / throttle sampling in the background while the timed loop runs."""
+
+    FIELDS = ("clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.hw_slowdown,"
+              "clocks_event_reasons.hw_thermal_slowdown,clocks_event_reasons.sw_thermal_slowdown,"
+              "clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, gpu_id: str):
+        self.gpu_id = gpu_id
+        self.lines = []
+        self.proc = None
+
+    def start(self):
+        try:
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", f"--query-gpu={self.FIELDS}", "--format=csv,noheader,nounits",
+                 "-lms", "100", "-i", self.gpu_id],
+                stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
+            threading.Thread(target=self._read, daemon=True).start()
+        except Exception:
+            self.proc = None
+
+    def _read(self):
+        for line in self.proc.stdout:
+            self.lines.append(line.strip())
+
+    def stop(self):
+        if self.proc is None:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["unavailable"]}
+        self.proc.terminate()
+        try:
+            self.proc.wait(timeout=5)
+        except Exception:
+            self.proc.kill()
+        sm, smax, reasons = [], [], set()
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        for ln in self.lines:
+            parts = [x.strip() for x in ln.split(",")]
+            if len(parts) < 7:
+                continue
+            try:
+                sm.append(float(parts[0]))
+                smax.append(float(parts[1]))
+            except ValueError:
+                continue
+            for n, v in zip(names, parts[3:7]):
+                if v.lower().startswith("active"):
+                    reasons.add(n)
+        return {"sm_mhz": statistics.median(sm) if sm else None,
+                "sm_max_mhz": max(smax) if smax else None,
+                "reasons": sorted(reasons), "samples": len(sm)}
+
+
+def gpu_selector(dev) -> str:
+    """nvidia-smi -i argument naming the GPU torch uses (its UUID when torch exposes it)."""
+    import torch
+
+    props = torch.cuda.get_device_properties(dev)
+    uuid = getattr(props, "uuid", None)
+    if uuid:
+        u = str(uuid)
+        return u if u.startswith("GPU-") else "GPU-" + u
+    return str(dev.index or 0)
+
+
+def max_over_ranks(value: float, device=None) -> float:
+    """Largest per-rank value (the step time every rank must wait for); identity on one rank."""
+    import torch
+    import torch.distributed as dist
+
+    if not (dist.is_available() and dist.is_initialized()) or dist.get_world_size() == 1:
+        return value
+    t = torch.tensor([value], dtype=torch.float64, device=device)
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
+def dist_env():
+    return (int(os.environ.get("RANK", "0")), int(os.environ.get("WORLD_SIZE", "1")),
+            int(os.environ.get("LOCAL_RANK", "0")))
+
+
+# ------------------------------------------------------------------------------------ bytes
+
+def prr_bytes(w, n_valid_pages, P_counts, missed_counts):
+    """Algorithmic bytes of one PRR decode step (see module docstring), and the spec form
+    (metadata + K/V of the true set A only)."""
+    rows = w.batch * w.num_kv_heads
+    G, D = w.group, w.head_dim
+    page_kv = w.page_size * D * 2 * 2
+    meta = rows * n_valid_pages * 2 * D * 2
+    q = w.batch * w.num_q_heads * D * 2
+    kv = (sum(P_counts) + sum(missed_counts)) * page_kv
+    records = (sum(P_counts) + sum(missed_counts)) * G * 132 * 4
+    scores = rows * n_valid_pages * 4 * 3            # written, read by select and by the EMA
+    ema = rows * n_valid_pages * 4 * 5               # level, trend read+write, prediction write
+    idx = rows * (w.k + w.k_pred) * 4 * 3
+    out = w.batch * w.num_q_heads * (D + 2) * 4
+    total = meta + q + kv + records + scores + ema + idx + out
+    north = meta + rows * w.k * page_kv
+    return total, north, dict(meta=meta, kv=kv, records=records, aux=q + scores + ema + idx + out)
+
+
+# ------------------------------------------------------------------------------------ ours
+
+def bench_prr(args, w, dev, rank):
+    import torch
+
+    from dynamic_block_sparse_gb300.pipeline import Cache, PRRDecoder
+    from dynamic_block_sparse_gb300.workloads import make_inputs
+
+    inputs = make_inputs(w, device=dev, shuffle_pages=False)
+    cache = Cache.from_inputs(inputs, dev)
+    dec = PRRDecoder(cache, w.k, w.k_pred, w.alpha, w.beta, w.gamma)
+    qs = inputs["q"]
+    nq = qs.shape[0]
+    n_valid = -(-w.seq_len // w.page_size)
+    flush = torch.empty(L2_FLUSH_BYTES, dtype=torch.uint8, device=dev)
+    stream = torch.cuda.current_stream()
+
+    # metadata build (context stage): timed on its own
+    ev = [torch.cuda.Event(enable_timing=True) for _ in range(2)]
+    meta_ms = []
+    for i in range(4):
+        flush.fill_(i)
+        ev[0].record()
+        dec.build_meta()
+        ev[1].record()
+        torch.cuda.synchronize()
+        meta_ms.append(ev[0].elapsed_time(ev[1]))
+    meta_build_ms = statistics.median(meta_ms[1:])
+
+    static_q = qs[0].clone()
+    dec.step(static_q)                                   # step 0: EMA init
+    for i in range(1, 4):                                # eager steady-state steps
+        static_q.copy_(qs[i % nq])
+        dec.step(static_q)
+    torch.cuda.synchronize()
+
+    graph = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(graph):
+        dec.step(static_q)
+    stage_graphs = {}
+    for name, fn in (("score_pages", lambda: dec.stage_score(static_q)),
+                     ("select_topk", lambda: dec.stage_select()),
+                     ("spec_attn", lambda: dec.stage_spec(static_q)),
+                     ("repair_merge", lambda: dec.stage_repair(static_q)),
+                     ("ema_predict", lambda: dec.stage_ema())):
+        g = torch.cuda.CUDAGraph()
+        with torch.cuda.graph(g):
+            fn()
+        stage_graphs[name] = g
+    torch.cuda.synchronize()
+
+    def timed_replay(g, n, qi0=0, collect=None):
+        starts = [torch.cuda.Event(enable_timing=True) for _ in range(n)]
+        ends = [torch.cuda.Event(enable_timing=True) for _ in range(n)]
+        for i in range(n):
+            static_q.copy_(qs[(qi0 + i) % nq])
+            if collect is not None:
+                collect[0].append((dec.spec_idx.clone(), dec.spec_count.clone()))
+            flush.fill_(i & 0xFF)
+            starts[i].record(stream)
+            g.replay()
+            ends[i].record(stream)
+            if collect is not None:
+                collect[1].append((dec.idx.clone(), dec.count.clone()))
+        torch.cuda.synchronize()
+        return [s.elapsed_time(e) for s, e in zip(starts, ends)]
+
+    timed_replay(graph, args.warmup, qi0=4)
+    sampler = ClockSampler(gpu_selector(dev))
+    sampler.start()
+    time.sleep(0.3)
+    collect = ([], [])
+    if hasattr(torch.distributed, "is_initialized") and torch.distributed.is_initialized():
+        torch.distributed.barrier()
+    torch.cuda.synchronize()
+    step_ms = timed_replay(graph, args.steps, qi0=4 + args.warmup, collect=collect)
+    torch.cuda.synchronize()
+    stage_ms = {name: statistics.mean(timed_replay(g, max(50, min(400, args.steps))))
+                for name, g in stage_graphs.items()}
+    clocks = sampler.stop()
+
+    # pages attended per timed step
+    P_counts, missed = [], []
+    for (pi, pc), (ai, ac) in zip(*collect):
+        pi, pc, ai, ac = pi.cpu(), pc.cpu(), ai.cpu(), ac.cpu()
+        pcount, mcount = 0, 0
+        for b in range(w.batch):
+            for h in range(w.num_kv_heads):
+                P = set(pi[b, h, :int(pc[b, h])].tolist())
+                A = ai[b, h, :int(ac[b, h])].tolist()
+                pcount += len(P)
+                mcount += sum(1 for a in A if a not in P)
+        P_counts.append(pcount)
+        missed.append(mcount)
+    n = len(step_ms)
+    bytes_step, north_step, parts = prr_bytes(w, n_valid, P_counts, missed)
+    bytes_step /= n
+    north_step /= n
+    mean_ms = statistics.mean(step_ms)
+
+    rows = w.batch * w.num_kv_heads
+    page_kv = w.page_size * w.head_dim * 4
+    q_bytes = w.batch * w.num_q_heads * w.head_dim * 2
+    stage_bytes = {
+        "score_pages": rows * n_valid * 512 + q_bytes + rows * n_valid * 4,
+        "select_topk": rows * n_valid * 4 + rows * w.k * 4,
+        "spec_attn": (sum(P_counts) / n) * (page_kv + w.group * 528) + q_bytes,
+        "ema_predict": rows * n_valid * 4 * 6 + rows * w.k_pred * 4,
+    }
+    dominant = max(stage_bytes, key=lambda k: stage_ms[k])
+    e2e = None
+    if not args.no_e2e:
+        e2e = e2e_prr(args, w, dec, qs, flush, bytes_step)
+    extra = dict(meta_build_ms=meta_build_ms,
+                 meta_build_gbs=(rows * n_valid * w.page_size * w.head_dim * 2
+                                 + rows * n_valid * 512) / (meta_build_ms * 1e6),
+                 stage_ms=stage_ms, stage_bytes=stage_bytes,
+                 mean_P=sum(P_counts) / n / rows, mean_missed=sum(missed) / n / rows,
+                 bytes_per_step=bytes_step, north_star_bytes_per_step=north_step,
+                 north_star_gbs=north_step / (mean_ms * 1e6),
+                 byte_parts={k: v / n for k, v in parts.items()},
+                 step_ms_p50=statistics.median(step_ms), step_ms_min=min(step_ms))
+    return dict(mean_ms=mean_ms, bytes_step=bytes_step, clocks=clocks, dominant=dominant,
+                dominant_ms=stage_ms[dominant], dominant_bytes=stage_bytes[dominant], e2e=e2e,
+                launches_per_step=6, extra=extra)
+
+
+def e2e_prr(args, w, dec, qs, flush, bytes_step):
+    """Same step through the public Python API with host buffers: pinned host query -> device,
+    decode step (eager library calls), output/m/l -> pinned host, every step."""
+    import torch
+
+    nq = qs.shape[0]
+    host_q = torch.empty((nq,) + tuple(qs.shape[1:]), dtype=qs.dtype, pin_memory=True)
+    host_q.copy_(qs.cpu())
+    dev_q = torch.empty_like(qs[0])
+    out_h = torch.empty(dec.out.shape, dtype=torch.float32, pin_memory=True)
+    m_h = torch.empty(dec.m.shape, dtype=torch.float32, pin_memory=True)
+    l_h = torch.empty(dec.l.shape, dtype=torch.float32, pin_memory=True)
+    n = max(20, min(300, args.steps))
+    stream = torch.cuda.current_stream()
+    times = []
+    for i in range(n + 5):
+        flush.fill_(i & 0xFF)
+        s, e = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        s.record(stream)
+        dev_q.copy_(host_q[i % nq], non_blocking=True)
+        dec.step(dev_q)
+        out_h.copy_(dec.out, non_blocking=True)
+        m_h.copy_(dec.m, non_blocking=True)
+        l_h.copy_(dec.l, non_blocking=True)
+        e.record(stream)
+        e.synchronize()
+        if i >= 5:
+            times.append(s.elapsed_time(e))
+    ms = statistics.mean(times)
+    h2d = dev_q.numel() * dev_q.element_size()
+    d2h = (dec.out.numel() + dec.m.numel() + dec.l.numel()) * 4
+    return {"value": bytes_step / (ms * 1e6), "unit": "GB/s", "ms_per_step": ms,
+            "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h}
+
+
+# ------------------------------------------------------------------------------------ oracle
+
+def oracle_prr(w, seconds: float | None, steps: int | None, warmup: int = 0):
+    """Times the float64 oracle's PRR decode step (both KV heads, metadata precomputed) on the
+    host.  Returns (seconds per step, steps timed, bytes per step)."""
+    import numpy as np
+
+    import oracle as O
+    from dynamic_block_sparse_gb300.workloads import make_inputs
+
+    inp = make_inputs(w, "cpu", shuffle_pages=False)
+    G = w.group
+    rows = []
+    for b in range(w.batch):
+        L = int(inp["seq_lens"][b])
+        for h in range(w.num_kv_heads):
+            K = O.request_tokens(inp["k_pages"], inp["page_table"], L, b, h)
+            V = O.request_tokens(inp["v_pages"], inp["page_table"], L, b, h)
+            kmax, kmin = O.page_meta_minmax(K, w.page_size)
+            rows.append(dict(b=b, h=h, L=L, K=K, V=V, kmax=kmax, kmin=kmin, ell=None, v=None))
+    qs = inp["q"]
+    P_counts, missed = [], []
+
+    def one_step(t):
+        q = qs[t % qs.shape[0]]
+        pc = mc = 0
+        for r in rows:
+            qg = q[r["b"], r["h"] * G:(r["h"] + 1) * G]
+            IS = O.score_pages_minmax(O.representative_query(qg), r["kmax"], r["kmin"])
+            A = O.select_topk(IS, w.k)
+            if r["ell"] is None:
+                O.attend(qg, r["K"], r["V"], O.page_token_ids(A, w.page_size, r["L"]), w.scale)
+                r["ell"], r["v"] = O.ema_init(IS)
+            else:
+                P = O.select_topk(O.ema_predict(r["ell"], r["v"], w.gamma), w.k_pred)
+                O.spec_repair(qg, r["K"], r["V"], w.page_size, r["L"], P, A, w.scale)
+                r["ell"], r["v"] = O.ema_update(IS, r["ell"], r["v"], w.alpha, w.beta)
+                pc += len(P)
+                mc += len(set(A) - set(P))
+        return pc, mc
+
+    one_step(0)
+    t = 1
+    for _ in range(warmup):
+        one_step(t)
+        t += 1
+    t0 = time.perf_counter()
+    done = 0
+    while True:
+        pc, mc = one_step(t)
+        P_counts.append(pc)
+        missed.append(mc)
+        t += 1
+        done += 1
+        el = time.perf_counter() - t0
+        if (steps is not None and done >= steps) or (steps is None and el >= seconds):
+            break
+    el = time.perf_counter() - t0
+    n_valid = -(-w.seq_len // w.page_size)
+    total, _, _ = prr_bytes(w, n_valid, P_counts, missed)
+    return el / done, done, total / done
+
+
+def cpu_baseline(args, w):
+    """Runs the oracle in a child process pinned to one BLAS thread for ~cpu_seconds."""
+    env = dict(os.environ)
+    for k in ("OMP_NUM_THREADS", "OPENBLAS_NUM_THREADS", "MKL_NUM_THREADS"):
+        env[k] = "1"
+    env["CUDA_VISIBLE_DEVICES"] = ""
+    cmd = [sys.executable, os.path.abspath(__file__), "--oracle-child", "--workload", w.name,
+           "--cpu-seconds", str(args.cpu_seconds)]
+    r = subprocess.run(cmd, capture_output=True, text=True, env=env, timeout=900)
+    if r.returncode != 0:
+        return {"value": None, "error": r.stderr[-400:]}
+    return json.loads(r.stdout.strip().splitlines()[-1])
+
+
+def oracle_child(args):
+    from dynamic_block_sparse_gb300.workloads import BY_NAME
+
+    w = BY_NAME[args.workload]
+    sec, n, bytes_step = oracle_prr(w, args.cpu_seconds, None)
+    print(json.dumps({"value": bytes_step / sec / 1e9, "unit": "GB/s", "cores": 1,
+                      "kind": "oracle", "ms_per_step": sec * 1e3,
+                      "sample": f"{n} consecutive decode steps of {w.name} (both KV heads, "
+                                f"metadata precomputed), float64 numpy, 1 BLAS thread"}))
+
+
+# ------------------------------------------------------------------------------------ main
+
+def main():
+    args = parse_args()
+    if args.oracle_child:
+        oracle_child(args)
+        return
+    from dynamic_block_sparse_gb300.workloads import BY_NAME
+
+    w = BY_NAME[args.workload]
+    if w.mode != "prr":
+        raise SystemExit("bench.py times the PRR speculate-and-repair workload (prr_512k)")
+    rank, world, local_rank = dist_env()
+    config = {"workload": f"{w.name}: B{w.batch}, {w.num_q_heads}q/{w.num_kv_heads}kv heads, "
+                          f"D{w.head_dim}, {w.seq_len} tokens, block {w.page_size}, top-{w.k}, "
+                          f"|P|={w.k_pred}, EMA a{w.alpha} b{w.beta} g{w.gamma}",
+              "seq_len": w.seq_len, "batch_per_gpu": w.batch, "l2": "flushed (256 MiB write) "
+              "before every timed step, outside the timed window",
+              "timing": "CUDA graph of one decode step, CUDA events on the launching stream"}
+
+    if args.impl == "reference":
+        if rank != 0:
+            return
+        sec, n, bytes_step = oracle_prr(w, None, max(1, args.steps), warmup=args.warmup)
+        value = bytes_step / sec / 1e9
+        line = {"impl": "reference", "metric": METRIC, "value": value, "unit": "GB/s",
+                "n_gpus": args.gpus, "steps": n, "warmup": args.warmup,
+                "ms_per_step": sec * 1e3, "higher_is_better": True, "scaling": "weak",
+                "vs_baseline": None, "dtype": "f64", "data": "synthetic", "config": config,
+                "cpu_baseline": {"kind": "oracle", "cores": 1, "value": value, "unit": "GB/s",
+                                 "sample": f"{n} decode steps of {w.name}, float64 numpy"},
+                "e2e": {"value": value, "unit": "GB/s", "h2d_bytes_per_step": 0,
+                        "d2h_bytes_per_step": 0}}
+        print(json.dumps(line))
+        return
+
+    import torch
+
+    if world > 1:
+        torch.cuda.set_device(local_rank)
+        torch.distributed.init_process_group("nccl")
+    dev = torch.device("cuda", torch.cuda.current_device())
+    res = bench_prr(args, w, dev, rank)
+
+    mean_ms = max_over_ranks(res["mean_ms"], dev)
+    value = res["bytes_step"] * world / (mean_ms * 1e6)
+    peak, peak_src = load_peaks()
+    achieved = res["dominant_bytes"] / (res["dominant_ms"] * 1e6)
+    traffic = None
+    tfile = os.path.join(ROOT, "profiles", "traffic.json")
+    if os.path.exists(tfile):
+        try:
+            tj = json.load(open(tfile))
+            ent = tj.get(res["dominant"])
+            if ent and ent.get("source_hash") == source_hash():
+                traffic = ent["bytes_per_launch"]
+        except Exception:
+            traffic = None
+    line = {
+        "metric": METRIC, "value": value, "unit": "GB/s", "n_gpus": world, "steps": args.steps,
+        "warmup": args.warmup, "ms_per_step": mean_ms, "us_per_step": mean_ms * 1e3,
+        "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "bf16",
+        "data": "synthetic", "config": config,
+        "roofline": {"bound": "hbm", "kernel": res["dominant"], "achieved": achieved,
+                     "peak": peak, "unit": "GB/s", "frac": achieved / peak, "traffic": traffic,
+                     "peak_source": peak_src, "step_frac": value / world / peak},
+        "clocks": res["clocks"], "gpu_launches": res["launches_per_step"] * args.steps,
+    }
+    if res["e2e"] is not None:
+        line["e2e"] = res["e2e"]
+    line.update(res["extra"])
+    if rank == 0 and world == 1 and not args.no_cpu_baseline:
+        line["cpu_baseline"] = cpu_baseline(args, w)
+    if rank == 0:
+        print(json.dumps(line))
+    if world > 1:
+        torch.distributed.destroy_process_group()
+
+
+def source_hash() -> str:
+    import hashlib
+
+    h = hashlib.sha256()
+    csrc = os.path.join(ROOT, "dynamic_block_sparse_gb300", "csrc")
+    for f in sorted(os.listdir(csrc)):
+        with open(os.path.join(csrc, f), "rb") as fh:
+            h.update(f.encode() + fh.read())
+    return h.hexdigest()[:16]
+
+
+if __name__ == "__main__":
+    main()

@@ -1,0 +1,229 @@
+"""ctypes binding of libdsa: the C-ABI entry points under the same names, taking torch tensors.
+
+Argument marshalling only: every function passes device pointers, sizes and the current CUDA
+stream to the library and raises :class:`DsaError` on a non-zero return code.  There is no
+fallback: if ``libdsa.so`` is missing or cannot be loaded, every call raises.
+"""
+
+from __future__ import annotations
+
+import ctypes
+import os
+import re
+from ctypes import c_float, c_int32, c_size_t, c_void_p
+
+import torch
+
+from . import build as _build
+
+DSA_META_MINMAX, DSA_META_MEAN = 0, 1
+DSA_EMA_INIT, DSA_EMA_UPDATE = 0, 1
+DSA_PSA_NLEFT = 1
+DSA_STATUS_BAD_PAGE, DSA_STATUS_OVERFLOW, DSA_STATUS_TIMEOUT = 1, 2, 4
+RECORD_FLOATS = 132  # partial record: O[128], m, l, 0, 0
+
+HEADER = os.path.join(_build.ROOT, "include", "dsa.h")
+
+
+class DsaError(RuntimeError):
+    def __init__(self, fn: str, rc: int, msg: str):
+        super().__init__(f"{fn} failed with code {rc}: {msg}")
+        self.rc = rc
+
+
+class PagedKV(ctypes.Structure):
+    _fields_ = [
+        ("k_pages", c_void_p), ("v_pages", c_void_p), ("page_table", c_void_p),
+        ("seq_lens", c_void_p), ("head_is_streaming", c_void_p), ("status", c_void_p),
+        ("batch", c_int32), ("num_q_heads", c_int32), ("num_kv_heads", c_int32),
+        ("head_dim", c_int32), ("page_size", c_int32), ("max_pages_per_seq", c_int32),
+        ("num_phys_pages", c_int32),
+    ]
+
+
+_P = c_void_p
+_I = c_int32
+_SIGNATURES = {
+    "dsa_last_error": ([], ctypes.c_char_p),
+    "dsa_version": ([], ctypes.c_char_p),
+    "dsa_build_page_meta": ([_P, _I, _I, _P, _P], _I),
+    "dsa_score_pages": ([_P, _P, _P, _I, _I, _P, _I, _P], _I),
+    "dsa_select_topk": ([_P, _I, _I, _I, _I, _P, _I, _P, _P], _I),
+    "dsa_select_hier": ([_P, _I, _I, _I, _I, _I, _P, _I, _P, _P], _I),
+    "dsa_select_threshold": ([_P, _P, _P, _I, c_float, _I, _I, c_float, _P, _I, _P, _P, _P, _P,
+                              _P], _I),
+    "dsa_sparse_decode_attn": ([_P, _P, _P, _I, _P, c_float, _P, _P, _P, _P, _I, _P, c_size_t,
+                                _P], _I),
+    "dsa_sparse_decode_attn_workspace_size": ([_P, _I, _I], c_size_t),
+    "dsa_repair_merge": ([_P, _P, _P, _I, _P, _P, _P, _I, _P, _I, c_float, _P, _P, _P, _P,
+                          c_size_t, _P], _I),
+    "dsa_repair_merge_workspace_size": ([_P, _I], c_size_t),
+    "dsa_streaming_head_attn": ([_P, _P, _I, _I, c_float, _P, _P, _P, _P], _I),
+    "dsa_ema_predict_update": ([_P, _I, _I, _I, _P, _P, _I, c_float, c_float, c_float, _P, _I,
+                                _P, _I, _P, _P], _I),
+    "dsa_merge_partials": ([_P, _I, _I, _I, _I, _P, _P, _P, _P], _I),
+}
+
+_lib = None
+
+
+def header_functions(path: str = HEADER) -> list[str]:
+    """Names of the functions ``include/dsa.h`` declares."""
+    text = open(path).read()
+    text = re.sub(r"/\*.*?\*/", "", text, flags=re.S)
+    return sorted(set(re.findall(r"\b(dsa_[a-z_0-9]+)\s*\(", text)))
+
+
+def load(path: str | None = None) -> ctypes.CDLL:
+    """Loads libdsa.so (built in-tree by ``build()``) and declares every signature."""
+    global _lib
+    if _lib is not None:
+        return _lib
+    path = path or _build.LIB_PATH
+    if not os.path.exists(path):
+        raise RuntimeError(f"{path} is missing: build the CUDA library first "
+                           "(python -c 'import __graft_entry__ as g; g.build()')")
+    lib = ctypes.CDLL(path)
+    for name, (args, res) in _SIGNATURES.items():
+        fn = getattr(lib, name)
+        fn.argtypes = args
+        fn.restype = res
+    _lib = lib
+    return lib
+
+
+def _ptr(t) -> int | None:
+    if t is None:
+        return None
+    if not t.is_cuda:
+        raise ValueError("tensor must live on a CUDA device")
+    return t.data_ptr()
+
+
+def _stream(stream) -> int | None:
+    if stream is None:
+        stream = torch.cuda.current_stream()
+    return stream.cuda_stream
+
+
+def _check(name: str, rc: int) -> None:
+    if rc != 0:
+        raise DsaError(name, rc, load().dsa_last_error().decode())
+
+
+def last_error() -> str:
+    return load().dsa_last_error().decode()
+
+
+def version() -> str:
+    return load().dsa_version().decode()
+
+
+def paged_kv(k_pages, v_pages, page_table, seq_lens, num_q_heads: int,
+             head_is_streaming=None, status=None) -> PagedKV:
+    """Descriptor of a paged cache; ``k_pages``/``v_pages`` are bf16 ``[P][Hkv][page][D]``."""
+    P, Hkv, page, D = k_pages.shape
+    assert k_pages.dtype == torch.bfloat16 and v_pages.shape == k_pages.shape
+    assert page_table.dtype == torch.int32 and seq_lens.dtype == torch.int32
+    kv = PagedKV()
+    kv.k_pages = _ptr(k_pages)
+    kv.v_pages = _ptr(v_pages)
+    kv.page_table = _ptr(page_table)
+    kv.seq_lens = _ptr(seq_lens)
+    kv.head_is_streaming = _ptr(head_is_streaming)
+    kv.status = _ptr(status)
+    kv.batch = page_table.shape[0]
+    kv.num_q_heads = num_q_heads
+    kv.num_kv_heads = Hkv
+    kv.head_dim = D
+    kv.page_size = page
+    kv.max_pages_per_seq = page_table.shape[1]
+    kv.num_phys_pages = P
+    return kv
+
+
+def dsa_build_page_meta(kv: PagedKV, meta_kind: int, logical_page: int, meta, stream=None):
+    _check("dsa_build_page_meta", load().dsa_build_page_meta(
+        ctypes.byref(kv), meta_kind, logical_page, _ptr(meta), _stream(stream)))
+
+
+def dsa_score_pages(kv: PagedKV, q, meta, meta_kind: int, logical_page: int, scores,
+                    stream=None):
+    _check("dsa_score_pages", load().dsa_score_pages(
+        ctypes.byref(kv), _ptr(q), _ptr(meta), meta_kind, logical_page, _ptr(scores),
+        scores.shape[-1], _stream(stream)))
+
+
+def dsa_select_topk(scores, n: int, k: int, idx, count, stream=None):
+    rows = scores.numel() // scores.shape[-1]
+    _check("dsa_select_topk", load().dsa_select_topk(
+        _ptr(scores), rows, n, scores.shape[-1], k, _ptr(idx), idx.shape[-1], _ptr(count),
+        _stream(stream)))
+
+
+def dsa_select_hier(logical_scores, n_logical: int, g: int, k_phys: int, idx, count,
+                    stream=None):
+    rows = logical_scores.numel() // logical_scores.shape[-1]
+    _check("dsa_select_hier", load().dsa_select_hier(
+        _ptr(logical_scores), rows, n_logical, logical_scores.shape[-1], g, k_phys, _ptr(idx),
+        idx.shape[-1], _ptr(count), _stream(stream)))
+
+
+def dsa_select_threshold(kv: PagedKV, q, scores, tau: float, cap: int, scale: float, idx, count,
+                         out, m, l, flags: int = 0, stream=None):
+    _check("dsa_select_threshold", load().dsa_select_threshold(
+        ctypes.byref(kv), _ptr(q), _ptr(scores), scores.shape[-1], tau, cap, flags, scale,
+        _ptr(idx), idx.shape[-1], _ptr(count), _ptr(out), _ptr(m), _ptr(l), _stream(stream)))
+
+
+def dsa_sparse_decode_attn_workspace_size(kv: PagedKV, idx_stride: int, num_splits: int = 0) -> int:
+    return int(load().dsa_sparse_decode_attn_workspace_size(ctypes.byref(kv), idx_stride,
+                                                            num_splits))
+
+
+def dsa_sparse_decode_attn(kv: PagedKV, q, idx, count, scale: float, out=None, m=None, l=None,
+                           page_partials=None, num_splits: int = 0, workspace=None, stream=None):
+    ws_bytes = 0 if workspace is None else workspace.numel() * workspace.element_size()
+    _check("dsa_sparse_decode_attn", load().dsa_sparse_decode_attn(
+        ctypes.byref(kv), _ptr(q), _ptr(idx), idx.shape[-1], _ptr(count), scale, _ptr(out),
+        _ptr(m), _ptr(l), _ptr(page_partials), num_splits, _ptr(workspace), ws_bytes,
+        _stream(stream)))
+
+
+def dsa_repair_merge_workspace_size(kv: PagedKV, true_stride: int) -> int:
+    return int(load().dsa_repair_merge_workspace_size(ctypes.byref(kv), true_stride))
+
+
+def dsa_repair_merge(kv: PagedKV, q, spec_idx, spec_count, page_partials, true_idx, true_count,
+                     scale: float, out, m, l, workspace, superset: bool = False, stream=None):
+    ws_bytes = workspace.numel() * workspace.element_size()
+    _check("dsa_repair_merge", load().dsa_repair_merge(
+        ctypes.byref(kv), _ptr(q), _ptr(spec_idx), spec_idx.shape[-1], _ptr(spec_count),
+        _ptr(page_partials), _ptr(true_idx), true_idx.shape[-1], _ptr(true_count),
+        1 if superset else 0, scale, _ptr(out), _ptr(m), _ptr(l), _ptr(workspace), ws_bytes,
+        _stream(stream)))
+
+
+def dsa_streaming_head_attn(kv: PagedKV, q, sink: int, local: int, scale: float, out, m, l,
+                            stream=None):
+    _check("dsa_streaming_head_attn", load().dsa_streaming_head_attn(
+        ctypes.byref(kv), _ptr(q), sink, local, scale, _ptr(out), _ptr(m), _ptr(l),
+        _stream(stream)))
+
+
+def dsa_ema_predict_update(IS, n: int, ell, v, mode: int, alpha: float, beta: float,
+                           gamma: float, pred=None, k_pred: int = 0, pred_idx=None,
+                           pred_count=None, stream=None):
+    rows = IS.numel() // IS.shape[-1]
+    _check("dsa_ema_predict_update", load().dsa_ema_predict_update(
+        _ptr(IS), rows, n, IS.shape[-1], _ptr(ell), _ptr(v), mode, alpha, beta, gamma,
+        _ptr(pred), k_pred, _ptr(pred_idx), 0 if pred_idx is None else pred_idx.shape[-1],
+        _ptr(pred_count), _stream(stream)))
+
+
+def dsa_merge_partials(partials, out, m, l, stream=None):
+    """``partials`` fp32 ``[rows][parts][G][132]`` -> ``out [rows*G][128]``, ``m``, ``l``."""
+    rows, parts, G, rec = partials.shape
+    assert rec == RECORD_FLOATS
+    _check("dsa_merge_partials", load().dsa_merge_partials(
+        _ptr(partials), rows, parts, G, 128, _ptr(out), _ptr(m), _ptr(l), _stream(stream)))

@@ -1,0 +1,500 @@
+// C ABI of libdsa: validates arguments on the host, encodes TMA descriptors for the KV pools,
+// chooses split counts and launches the kernels on the caller's stream.  Allocates nothing.
+#include <cudaTypedefs.h>
+
+#include <cstdarg>
+#include <cstdio>
+#include <mutex>
+#include <string>
+
+#include "internal.h"
+
+namespace dsa {
+size_t threshold_smem_bytes(int page, int max_pages);
+}
+
+namespace {
+
+using namespace dsa;
+
+constexpr int kTargetCtas = 2 * 152;  // two CTAs per SM of a GB300
+
+thread_local std::string g_err;
+
+int fail(int code, const char* fmt, ...) {
+  char buf[512];
+  va_list ap;
+  va_start(ap, fmt);
+  vsnprintf(buf, sizeof(buf), fmt, ap);
+  va_end(ap);
+  g_err = buf;
+  return code;
+}
+
+int cuda_fail(cudaError_t e, const char* what) {
+  return fail(DSA_ERR_CUDA, "%s: %s", what, cudaGetErrorString(e));
+}
+
+int ok() {
+  g_err.clear();
+  return DSA_OK;
+}
+
+bool aligned(const void* p, size_t a) { return (reinterpret_cast<uintptr_t>(p) % a) == 0; }
+
+PFN_cuTensorMapEncodeTiled_v12000 encode_fn() {
+  static PFN_cuTensorMapEncodeTiled_v12000 fn = nullptr;
+  static std::once_flag once;
+  std::call_once(once, [] {
+    void* p = nullptr;
+    cudaDriverEntryPointQueryResult q;
+    if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &p, 12000, cudaEnableDefault,
+                                         &q) == cudaSuccess &&
+        q == cudaDriverEntryPointSuccess)
+      fn = reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(p);
+  });
+  return fn;
+}
+
+// 2-D view of a pool: rows = (phys_page, kv_head, slot), 128 bf16 per row; box = 64 dims x page
+// rows with 128-byte swizzle (one half of the head dimension of one page).
+int pool_map(const void* base, const dsa_paged_kv* kv, CUtensorMap* map) {
+  auto fn = encode_fn();
+  if (!fn) return fail(DSA_ERR_CUDA, "cuTensorMapEncodeTiled is not available from the driver");
+  cuuint64_t dims[2] = {static_cast<cuuint64_t>(kHeadDim),
+                        static_cast<cuuint64_t>(kv->num_phys_pages) * kv->num_kv_heads *
+                            kv->page_size};
+  cuuint64_t strides[1] = {static_cast<cuuint64_t>(kHeadDim) * 2};
+  cuuint32_t box[2] = {64, static_cast<cuuint32_t>(kv->page_size)};
+  cuuint32_t estr[2] = {1, 1};
+  CUresult r = fn(map, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, const_cast<void*>(base), dims, strides,
+                  box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+                  CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+  if (r != CUDA_SUCCESS) return fail(DSA_ERR_CUDA, "cuTensorMapEncodeTiled failed (%d)", int(r));
+  return DSA_OK;
+}
+
+// Checks the cache descriptor.  pools: whether k/v pools are needed (0 none, 1 K only, 2 both).
+int check_kv(const dsa_paged_kv* kv, int pools, KvView* view) {
+  if (!kv) return fail(DSA_ERR_INVALID_ARG, "kv descriptor is NULL");
+  if (!kv->page_table || !kv->seq_lens) return fail(DSA_ERR_INVALID_ARG, "page_table/seq_lens NULL");
+  if (pools >= 1 && !kv->k_pages) return fail(DSA_ERR_INVALID_ARG, "k_pages is NULL");
+  if (pools >= 2 && !kv->v_pages) return fail(DSA_ERR_INVALID_ARG, "v_pages is NULL");
+  if (kv->batch <= 0 || kv->num_q_heads <= 0 || kv->num_kv_heads <= 0 || kv->page_size <= 0 ||
+      kv->max_pages_per_seq <= 0 || kv->num_phys_pages <= 0)
+    return fail(DSA_ERR_INVALID_ARG, "kv shape fields must be positive");
+  if (kv->head_dim != kHeadDim)
+    return fail(DSA_ERR_UNSUPPORTED, "head_dim %d unsupported (only 128)", kv->head_dim);
+  if (kv->num_q_heads % kv->num_kv_heads != 0)
+    return fail(DSA_ERR_INVALID_ARG, "num_q_heads must be a multiple of num_kv_heads");
+  const int G = kv->num_q_heads / kv->num_kv_heads;
+  if (G > kMaxGroup) return fail(DSA_ERR_UNSUPPORTED, "group size %d > %d", G, kMaxGroup);
+  if (kv->page_size % 16 != 0 || kv->page_size > 256)
+    return fail(DSA_ERR_UNSUPPORTED, "page_size %d must be a multiple of 16 in [16, 256]",
+                kv->page_size);
+  const long long rows =
+      static_cast<long long>(kv->num_phys_pages) * kv->num_kv_heads * kv->page_size;
+  if (rows >= (1LL << 31))
+    return fail(DSA_ERR_UNSUPPORTED, "pool of %lld token rows exceeds 2^31", rows);
+  if ((pools >= 1 && !aligned(kv->k_pages, 16)) || (pools >= 2 && !aligned(kv->v_pages, 16)))
+    return fail(DSA_ERR_ALIGNMENT, "k_pages/v_pages must be 16-byte aligned");
+  view->page_table = kv->page_table;
+  view->seq_lens = kv->seq_lens;
+  view->streaming = kv->head_is_streaming;
+  view->status = kv->status;
+  view->B = kv->batch;
+  view->Hq = kv->num_q_heads;
+  view->Hkv = kv->num_kv_heads;
+  view->G = G;
+  view->D = kv->head_dim;
+  view->p = kv->page_size;
+  view->max_pages = kv->max_pages_per_seq;
+  view->num_phys = kv->num_phys_pages;
+  return DSA_OK;
+}
+
+int attn_stages(int page, int pages_per_cta) {
+  int s = 131072 / (512 * page);
+  if (s < 1) s = 1;
+  if (s > 8) s = 8;
+  if (pages_per_cta >= 1 && s > pages_per_cta) s = pages_per_cta;
+  return s;
+}
+
+int auto_splits(int rows, int stride, int requested) {
+  int min_splits = (stride + kMaxListPages - 1) / kMaxListPages;
+  if (min_splits < 1) min_splits = 1;
+  int s = requested;
+  if (s <= 0) {
+    s = (kTargetCtas + rows - 1) / rows;
+    const int cap = (stride + 1) / 2;  // at least two pages per CTA on average
+    if (s > cap) s = cap;
+  }
+  if (s < min_splits) s = min_splits;
+  if (s > stride && stride > 0) s = stride;
+  if (s < 1) s = 1;
+  return s;
+}
+
+int repair_splits(int stride) {
+  int s = (stride + 3) / 4;
+  const int min_splits = (stride + kMaxListPages - 1) / kMaxListPages;
+  if (s < min_splits) s = min_splits;
+  return s < 1 ? 1 : s;
+}
+
+size_t record_bytes(int rows, int slots, int G) {
+  return static_cast<size_t>(rows) * slots * G * kRecordFloats * sizeof(float);
+}
+
+float scale_log2(float scale) { return scale * kLog2e; }
+
+}  // namespace
+
+extern "C" {
+
+const char* dsa_last_error(void) { return g_err.c_str(); }
+
+const char* dsa_version(void) { return "libdsa 0.1 (sm_103a)"; }
+
+int dsa_build_page_meta(const dsa_paged_kv* kv, int32_t meta_kind, int32_t logical_page,
+                        void* meta, dsa_stream_t stream) {
+  KvView v;
+  int rc = check_kv(kv, 1, &v);
+  if (rc) return rc;
+  if (meta_kind != DSA_META_MINMAX && meta_kind != DSA_META_MEAN)
+    return fail(DSA_ERR_INVALID_ARG, "unknown meta_kind %d", meta_kind);
+  if (logical_page <= 0 || v.p % logical_page != 0)
+    return fail(DSA_ERR_INVALID_ARG, "logical_page %d must divide page_size %d", logical_page, v.p);
+  if (!meta) return fail(DSA_ERR_INVALID_ARG, "meta is NULL");
+  if (!aligned(meta, 16)) return fail(DSA_ERR_ALIGNMENT, "meta must be 16-byte aligned");
+  cudaError_t e = launch_build_meta(v, static_cast<const __nv_bfloat16*>(kv->k_pages), meta_kind,
+                                    logical_page, meta, static_cast<cudaStream_t>(stream));
+  return e == cudaSuccess ? ok() : cuda_fail(e, "dsa_build_page_meta launch");
+}
+
+int dsa_score_pages(const dsa_paged_kv* kv, const void* q, const void* meta, int32_t meta_kind,
+                    int32_t logical_page, float* scores, int32_t score_stride,
+                    dsa_stream_t stream) {
+  KvView v;
+  int rc = check_kv(kv, 0, &v);
+  if (rc) return rc;
+  if (!q || !meta || !scores) return fail(DSA_ERR_INVALID_ARG, "q/meta/scores is NULL");
+  if (meta_kind != DSA_META_MINMAX && meta_kind != DSA_META_MEAN)
+    return fail(DSA_ERR_INVALID_ARG, "unknown meta_kind %d", meta_kind);
+  if (logical_page <= 0 || v.p % logical_page != 0)
+    return fail(DSA_ERR_INVALID_ARG, "logical_page %d must divide page_size %d", logical_page, v.p);
+  if (!aligned(meta, 16)) return fail(DSA_ERR_ALIGNMENT, "meta must be 16-byte aligned");
+  const long long need = static_cast<long long>(v.max_pages) * (v.p / logical_page);
+  if (score_stride < need)
+    return fail(DSA_ERR_INVALID_ARG, "score_stride %d < max_pages * g = %lld", score_stride, need);
+  cudaError_t e = launch_score(v, static_cast<const __nv_bfloat16*>(q), meta, meta_kind,
+                               logical_page, scores, score_stride,
+                               static_cast<cudaStream_t>(stream));
+  return e == cudaSuccess ? ok() : cuda_fail(e, "dsa_score_pages launch");
+}
+
+static int select_common(const float* scores, int32_t rows, int32_t n_logical, int32_t stride,
+                         int32_t g, int32_t k, int32_t* idx, int32_t idx_stride, int32_t* count,
+                         dsa_stream_t stream, const char* name) {
+  if (rows < 0 || n_logical < 0 || k < 0 || g < 1)
+    return fail(DSA_ERR_INVALID_ARG, "%s: negative size or g < 1", name);
+  if (rows == 0) return ok();
+  if (!scores || !idx || !count) return fail(DSA_ERR_INVALID_ARG, "%s: NULL pointer", name);
+  if (n_logical > stride) return fail(DSA_ERR_INVALID_ARG, "%s: n > stride", name);
+  if (idx_stride < k) return fail(DSA_ERR_INVALID_ARG, "%s: idx_stride < k", name);
+  const int n = (n_logical + g - 1) / g;
+  if (n > kMaxSelectN)
+    return fail(DSA_ERR_UNSUPPORTED, "%s: %d candidates per row > %d", name, n, kMaxSelectN);
+  cudaError_t e = launch_select(scores, rows, n_logical, stride, g, k, idx, idx_stride, count,
+                                static_cast<cudaStream_t>(stream));
+  return e == cudaSuccess ? ok() : cuda_fail(e, name);
+}
+
+int dsa_select_topk(const float* scores, int32_t rows, int32_t n, int32_t stride, int32_t k,
+                    int32_t* idx, int32_t idx_stride, int32_t* count, dsa_stream_t stream) {
+  return select_common(scores, rows, n, stride, 1, k, idx, idx_stride, count, stream,
+                       "dsa_select_topk");
+}
+
+int dsa_select_hier(const float* logical_scores, int32_t rows, int32_t n_logical, int32_t stride,
+                    int32_t g, int32_t k_phys, int32_t* idx, int32_t idx_stride, int32_t* count,
+                    dsa_stream_t stream) {
+  return select_common(logical_scores, rows, n_logical, stride, g, k_phys, idx, idx_stride, count,
+                       stream, "dsa_select_hier");
+}
+
+int dsa_select_threshold(const dsa_paged_kv* kv, const void* q, const float* scores,
+                         int32_t score_stride, float tau, int32_t cap, int32_t flags, float scale,
+                         int32_t* idx, int32_t idx_stride, int32_t* count, float* out, float* m,
+                         float* l, dsa_stream_t stream) {
+  KvView v;
+  int rc = check_kv(kv, 2, &v);
+  if (rc) return rc;
+  if (!q || !scores || !idx || !count || !out || !m || !l)
+    return fail(DSA_ERR_INVALID_ARG, "dsa_select_threshold: NULL pointer");
+  if (!(tau > 0.f && tau <= 1.f)) return fail(DSA_ERR_INVALID_ARG, "tau must be in (0, 1]");
+  if (cap < 1 || idx_stride < cap) return fail(DSA_ERR_INVALID_ARG, "need 1 <= cap <= idx_stride");
+  if (score_stride < 1) return fail(DSA_ERR_INVALID_ARG, "score_stride < 1");
+  if (v.max_pages > kMaxThresholdN)
+    return fail(DSA_ERR_UNSUPPORTED, "max_pages_per_seq %d > %d for threshold selection",
+                v.max_pages, kMaxThresholdN);
+  if (threshold_smem_bytes(v.p, v.max_pages) > 227 * 1024)
+    return fail(DSA_ERR_UNSUPPORTED, "threshold selection shared memory too large");
+  CUtensorMap tk, tv;
+  if ((rc = pool_map(kv->k_pages, kv, &tk)) || (rc = pool_map(kv->v_pages, kv, &tv))) return rc;
+  ThresholdArgs a;
+  a.kv = v;
+  a.q = static_cast<const __nv_bfloat16*>(q);
+  a.scores = scores;
+  a.score_stride = score_stride;
+  a.tau = tau;
+  a.cap = cap;
+  a.flags = flags;
+  a.scale_log2 = scale_log2(scale);
+  a.idx = idx;
+  a.idx_stride = idx_stride;
+  a.count = count;
+  a.out = out;
+  a.m = m;
+  a.l = l;
+  cudaError_t e = launch_threshold(tk, tv, a, static_cast<cudaStream_t>(stream));
+  return e == cudaSuccess ? ok() : cuda_fail(e, "dsa_select_threshold launch");
+}
+
+size_t dsa_sparse_decode_attn_workspace_size(const dsa_paged_kv* kv, int32_t idx_stride,
+                                             int32_t num_splits) {
+  if (!kv || kv->num_kv_heads <= 0 || kv->batch <= 0 || idx_stride <= 0) return 0;
+  const int rows = kv->batch * kv->num_kv_heads;
+  const int G = kv->num_q_heads / kv->num_kv_heads;
+  const int s = auto_splits(rows, idx_stride, num_splits);
+  return s > 1 ? record_bytes(rows, s, G) : 0;
+}
+
+int dsa_sparse_decode_attn(const dsa_paged_kv* kv, const void* q, const int32_t* idx,
+                           int32_t idx_stride, const int32_t* count, float scale, float* out,
+                           float* m, float* l, float* page_partials, int32_t num_splits,
+                           void* workspace, size_t workspace_bytes, dsa_stream_t stream) {
+  KvView v;
+  int rc = check_kv(kv, 2, &v);
+  if (rc) return rc;
+  if (!q || !idx || !count) return fail(DSA_ERR_INVALID_ARG, "q/idx/count is NULL");
+  if (idx_stride < 1) return fail(DSA_ERR_INVALID_ARG, "idx_stride < 1");
+  const bool want_out = out != nullptr;
+  if (want_out && (!m || !l)) return fail(DSA_ERR_INVALID_ARG, "out given without m/l");
+  if (!want_out && !page_partials)
+    return fail(DSA_ERR_INVALID_ARG, "neither out nor page_partials given");
+  CUtensorMap tk, tv;
+  if ((rc = pool_map(kv->k_pages, kv, &tk)) || (rc = pool_map(kv->v_pages, kv, &tv))) return rc;
+  cudaStream_t s = static_cast<cudaStream_t>(stream);
+  const int rows = v.B * v.Hkv;
+  AttnArgs a = {};
+  a.kv = v;
+  a.q = static_cast<const __nv_bfloat16*>(q);
+  a.scale_log2 = scale_log2(scale);
+  a.idx = idx;
+  a.idx_stride = idx_stride;
+  a.count = count;
+  cudaError_t e;
+  if (page_partials) {
+    a.num_splits = idx_stride;
+    a.part = page_partials;
+    a.part_slots = idx_stride;
+    a.stages = 1;
+    e = launch_attn(LIST_ONE_PAGE, tk, tv, a, idx_stride, s);
+    if (e != cudaSuccess) return cuda_fail(e, "dsa_sparse_decode_attn launch");
+    if (want_out) {
+      MergeArgs mg = {};
+      mg.part = page_partials;
+      mg.slots = idx_stride;
+      mg.count = count;
+      mg.rows = rows;
+      mg.G = v.G;
+      mg.Hkv = v.Hkv;
+      mg.Hq = v.Hq;
+      mg.streaming = v.streaming;
+      mg.out = out;
+      mg.m = m;
+      mg.l = l;
+      mg.out_rows_are_heads = 1;
+      e = launch_merge(mg, s);
+      if (e != cudaSuccess) return cuda_fail(e, "dsa_sparse_decode_attn merge");
+    }
+    return ok();
+  }
+  const int splits = auto_splits(rows, idx_stride, num_splits);
+  const int per_cta = (idx_stride + splits - 1) / splits;
+  a.num_splits = splits;
+  a.stages = attn_stages(v.p, per_cta);
+  a.out = out;
+  a.m = m;
+  a.l = l;
+  if (splits > 1) {
+    const size_t need = record_bytes(rows, splits, v.G);
+    if (!workspace || workspace_bytes < need)
+      return fail(DSA_ERR_WORKSPACE, "workspace of %zu bytes needed", need);
+    if (!aligned(workspace, 16)) return fail(DSA_ERR_ALIGNMENT, "workspace must be 16-byte aligned");
+    a.part = static_cast<float*>(workspace);
+    a.part_slots = splits;
+  }
+  e = launch_attn(LIST_SELECTED, tk, tv, a, splits, s);
+  if (e != cudaSuccess) return cuda_fail(e, "dsa_sparse_decode_attn launch");
+  if (splits > 1) {
+    MergeArgs mg = {};
+    mg.part = static_cast<const float*>(workspace);
+    mg.slots = splits;
+    mg.rows = rows;
+    mg.G = v.G;
+    mg.Hkv = v.Hkv;
+    mg.Hq = v.Hq;
+    mg.streaming = v.streaming;
+    mg.out = out;
+    mg.m = m;
+    mg.l = l;
+    mg.out_rows_are_heads = 1;
+    e = launch_merge(mg, s);
+    if (e != cudaSuccess) return cuda_fail(e, "dsa_sparse_decode_attn merge");
+  }
+  return ok();
+}
+
+size_t dsa_repair_merge_workspace_size(const dsa_paged_kv* kv, int32_t true_stride) {
+  if (!kv || kv->num_kv_heads <= 0 || kv->batch <= 0 || true_stride <= 0) return 0;
+  const int rows = kv->batch * kv->num_kv_heads;
+  const int G = kv->num_q_heads / kv->num_kv_heads;
+  return record_bytes(rows, repair_splits(true_stride), G);
+}
+
+int dsa_repair_merge(const dsa_paged_kv* kv, const void* q, const int32_t* spec_idx,
+                     int32_t spec_stride, const int32_t* spec_count, const float* page_partials,
+                     const int32_t* true_idx, int32_t true_stride, const int32_t* true_count,
+                     int32_t superset, float scale, float* out, float* m, float* l,
+                     void* workspace, size_t workspace_bytes, dsa_stream_t stream) {
+  KvView v;
+  int rc = check_kv(kv, 2, &v);
+  if (rc) return rc;
+  if (!q || !spec_idx || !spec_count || !page_partials || !true_idx || !true_count || !out || !m ||
+      !l)
+    return fail(DSA_ERR_INVALID_ARG, "dsa_repair_merge: NULL pointer");
+  if (spec_stride < 1 || true_stride < 1) return fail(DSA_ERR_INVALID_ARG, "stride < 1");
+  const int rows = v.B * v.Hkv;
+  const int splits = repair_splits(true_stride);
+  const size_t need = record_bytes(rows, splits, v.G);
+  if (!workspace || workspace_bytes < need)
+    return fail(DSA_ERR_WORKSPACE, "workspace of %zu bytes needed", need);
+  if (!aligned(workspace, 16)) return fail(DSA_ERR_ALIGNMENT, "workspace must be 16-byte aligned");
+  CUtensorMap tk, tv;
+  if ((rc = pool_map(kv->k_pages, kv, &tk)) || (rc = pool_map(kv->v_pages, kv, &tv))) return rc;
+  cudaStream_t s = static_cast<cudaStream_t>(stream);
+  AttnArgs a = {};
+  a.kv = v;
+  a.q = static_cast<const __nv_bfloat16*>(q);
+  a.scale_log2 = scale_log2(scale);
+  a.idx = true_idx;
+  a.idx_stride = true_stride;
+  a.count = true_count;
+  a.spec_idx = spec_idx;
+  a.spec_stride = spec_stride;
+  a.spec_count = spec_count;
+  a.num_splits = splits;
+  a.part = static_cast<float*>(workspace);
+  a.part_slots = splits;
+  a.stages = attn_stages(v.p, (true_stride + splits - 1) / splits);
+  cudaError_t e = launch_attn(LIST_REPAIR, tk, tv, a, splits, s);
+  if (e != cudaSuccess) return cuda_fail(e, "dsa_repair_merge launch");
+  MergeArgs mg = {};
+  mg.part = static_cast<const float*>(workspace);
+  mg.slots = splits;
+  mg.spec_part = page_partials;
+  mg.spec_stride = spec_stride;
+  mg.spec_idx = spec_idx;
+  mg.spec_count = spec_count;
+  mg.true_idx = true_idx;
+  mg.true_stride = true_stride;
+  mg.true_count = true_count;
+  mg.superset = superset != 0;
+  mg.rows = rows;
+  mg.G = v.G;
+  mg.Hkv = v.Hkv;
+  mg.Hq = v.Hq;
+  mg.streaming = v.streaming;
+  mg.out = out;
+  mg.m = m;
+  mg.l = l;
+  mg.out_rows_are_heads = 1;
+  e = launch_merge(mg, s);
+  return e == cudaSuccess ? ok() : cuda_fail(e, "dsa_repair_merge merge");
+}
+
+int dsa_streaming_head_attn(const dsa_paged_kv* kv, const void* q, int32_t sink_tokens,
+                            int32_t local_tokens, float scale, float* out, float* m, float* l,
+                            dsa_stream_t stream) {
+  KvView v;
+  int rc = check_kv(kv, 2, &v);
+  if (rc) return rc;
+  if (!q || !out || !m || !l) return fail(DSA_ERR_INVALID_ARG, "q/out/m/l is NULL");
+  if (sink_tokens < 0 || local_tokens < 0) return fail(DSA_ERR_INVALID_ARG, "negative window");
+  if (!kv->head_is_streaming) return ok();  // no streaming heads: nothing to do
+  const long long pages = (static_cast<long long>(sink_tokens) + v.p - 1) / v.p +
+                          (static_cast<long long>(local_tokens) + v.p - 1) / v.p + 1;
+  if (pages > kMaxListPages)
+    return fail(DSA_ERR_UNSUPPORTED, "sink + local spans more than %d pages", kMaxListPages);
+  CUtensorMap tk, tv;
+  if ((rc = pool_map(kv->k_pages, kv, &tk)) || (rc = pool_map(kv->v_pages, kv, &tv))) return rc;
+  AttnArgs a = {};
+  a.kv = v;
+  a.q = static_cast<const __nv_bfloat16*>(q);
+  a.scale_log2 = scale_log2(scale);
+  a.num_splits = 1;
+  a.sink = sink_tokens;
+  a.local = local_tokens;
+  a.out = out;
+  a.m = m;
+  a.l = l;
+  a.stages = attn_stages(v.p, static_cast<int>(pages));
+  cudaError_t e = launch_attn(LIST_STREAMING, tk, tv, a, 1, static_cast<cudaStream_t>(stream));
+  return e == cudaSuccess ? ok() : cuda_fail(e, "dsa_streaming_head_attn launch");
+}
+
+int dsa_ema_predict_update(const float* IS, int32_t rows, int32_t n, int32_t stride, float* ell,
+                           float* v, int32_t mode, float alpha, float beta, float gamma,
+                           float* pred, int32_t k_pred, int32_t* pred_idx,
+                           int32_t pred_idx_stride, int32_t* pred_count, dsa_stream_t stream) {
+  if (rows < 0 || n < 0 || k_pred < 0) return fail(DSA_ERR_INVALID_ARG, "negative size");
+  if (rows == 0) return ok();
+  if (!IS || !ell || !v) return fail(DSA_ERR_INVALID_ARG, "IS/ell/v is NULL");
+  if (mode != DSA_EMA_INIT && mode != DSA_EMA_UPDATE)
+    return fail(DSA_ERR_INVALID_ARG, "unknown EMA mode %d", mode);
+  if (n > stride) return fail(DSA_ERR_INVALID_ARG, "n > stride");
+  if (n > kMaxSelectN) return fail(DSA_ERR_UNSUPPORTED, "n %d > %d", n, kMaxSelectN);
+  if (k_pred > 0 && (!pred_idx || !pred_count || pred_idx_stride < k_pred))
+    return fail(DSA_ERR_INVALID_ARG, "pred_idx/pred_count NULL or pred_idx_stride < k_pred");
+  cudaError_t e = launch_ema(IS, rows, n, stride, ell, v, mode, alpha, beta, gamma, pred, k_pred,
+                             pred_idx, pred_idx_stride, pred_count,
+                             static_cast<cudaStream_t>(stream));
+  return e == cudaSuccess ? ok() : cuda_fail(e, "dsa_ema_predict_update launch");
+}
+
+int dsa_merge_partials(const float* partials, int32_t rows, int32_t num_parts, int32_t group,
+                       int32_t head_dim, float* out, float* m, float* l, dsa_stream_t stream) {
+  if (rows < 0 || num_parts < 0) return fail(DSA_ERR_INVALID_ARG, "negative size");
+  if (rows == 0) return ok();
+  if (!partials || !out || !m || !l) return fail(DSA_ERR_INVALID_ARG, "NULL pointer");
+  if (head_dim != kHeadDim) return fail(DSA_ERR_UNSUPPORTED, "head_dim must be 128");
+  if (group < 1 || group > 65535) return fail(DSA_ERR_INVALID_ARG, "bad group");
+  MergeArgs mg = {};
+  mg.part = partials;
+  mg.slots = num_parts;
+  mg.rows = rows;
+  mg.G = group;
+  mg.Hkv = 1;
+  mg.Hq = group;
+  mg.out = out;
+  mg.m = m;
+  mg.l = l;
+  mg.out_rows_are_heads = 0;
+  cudaError_t e = launch_merge(mg, static_cast<cudaStream_t>(stream));
+  return e == cudaSuccess ? ok() : cuda_fail(e, "dsa_merge_partials launch");
+}
+
+}  // extern "C"

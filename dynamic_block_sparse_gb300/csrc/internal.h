@@ -1,0 +1,132 @@
+// Internal launch interface between the C-ABI layer (api.cu) and the kernel files.
+#pragma once
+
+#include <cuda.h>
+#include <cuda_bf16.h>
+#include <cuda_runtime.h>
+#include <stdint.h>
+
+#include <mutex>
+#include <unordered_map>
+
+#include "dsa.h"
+
+namespace dsa {
+
+constexpr int kHeadDim = 128;
+constexpr int kMaxGroup = 16;          // query heads per KV head served by one m16 tile
+constexpr float kLog2e = 1.4426950408889634f;
+constexpr float kLn2 = 0.6931471805599453f;
+constexpr int kMaxListPages = 256;     // pages one attention CTA may be handed
+constexpr int kRecordFloats = 132;     // partial record: O[128], m, l, pad, pad
+constexpr int kMaxSelectN = 32768;     // candidates per row held in shared memory by selection
+constexpr int kMaxThresholdN = 16384;  // candidates per row for the PSA kernel
+
+struct KvView {
+  const int32_t* page_table;
+  const int32_t* seq_lens;
+  const uint8_t* streaming;  // may be null
+  int32_t* status;           // may be null
+  int B, Hq, Hkv, G, D, p, max_pages, num_phys;
+};
+
+enum AttnList { LIST_SELECTED = 0, LIST_ONE_PAGE = 1, LIST_STREAMING = 2, LIST_REPAIR = 3 };
+
+struct AttnArgs {
+  KvView kv;
+  const __nv_bfloat16* q;
+  float scale_log2;
+  const int32_t* idx;  // SELECTED / ONE_PAGE: selected positions; REPAIR: true set A
+  int idx_stride;
+  const int32_t* count;
+  const int32_t* spec_idx;  // REPAIR: speculative set P
+  int spec_stride;
+  const int32_t* spec_count;
+  int num_splits;
+  int sink, local;  // STREAMING window
+  float* out;
+  float* m;
+  float* l;
+  float* part;  // partial records [rows][part_slots][G][kRecordFloats]
+  int part_slots;
+  int stages;
+};
+
+// Raises a kernel's dynamic shared-memory limit once per (kernel, device); later calls with the
+// same or a smaller size do nothing, so steady-state launches (and stream capture) skip it.
+inline cudaError_t ensure_dynamic_smem(const void* fn, size_t bytes) {
+  static std::mutex mu;
+  static std::unordered_map<const void*, size_t> done[64];
+  int dev = 0;
+  cudaError_t e = cudaGetDevice(&dev);
+  if (e != cudaSuccess) return e;
+  if (dev < 0 || dev >= 64) dev = 0;
+  std::lock_guard<std::mutex> lock(mu);
+  auto it = done[dev].find(fn);
+  if (it != done[dev].end() && it->second >= bytes) return cudaSuccess;
+  e = cudaFuncSetAttribute(fn, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                           static_cast<int>(bytes));
+  if (e == cudaSuccess) done[dev][fn] = bytes;
+  return e;
+}
+
+size_t attn_smem_bytes(int page, int stages);
+cudaError_t launch_attn(int list, const CUtensorMap& tmK, const CUtensorMap& tmV,
+                        const AttnArgs& a, int grid_x, cudaStream_t s);
+
+struct MergeArgs {
+  const float* part;  // [rows][slots][G][kRecordFloats]
+  int slots;
+  const int32_t* count;  // parts per row (null = slots)
+  // repair: extra parts from page partials of hits
+  const float* spec_part;
+  int spec_stride;
+  const int32_t* spec_idx;
+  const int32_t* spec_count;
+  const int32_t* true_idx;
+  int true_stride;
+  const int32_t* true_count;
+  int superset;
+  int rows, G, Hkv, Hq;
+  const uint8_t* streaming;  // rows of streaming heads are skipped when non-null
+  float* out;
+  float* m;
+  float* l;
+  int out_rows_are_heads;  // 1: out index = (b*Hq + h*G + g); 0: out index = row*G + g
+};
+cudaError_t launch_merge(const MergeArgs& a, cudaStream_t s);
+
+// metadata and scoring
+cudaError_t launch_build_meta(const KvView& kv, const __nv_bfloat16* k_pages, int kind, int lp,
+                              void* meta, cudaStream_t s);
+cudaError_t launch_score(const KvView& kv, const __nv_bfloat16* q, const void* meta, int kind,
+                         int lp, float* scores, int stride, cudaStream_t s);
+
+// selection
+cudaError_t launch_select(const float* scores, int rows, int n_logical, int stride, int g, int k,
+                          int32_t* idx, int idx_stride, int32_t* count, cudaStream_t s);
+cudaError_t launch_ema(const float* IS, int rows, int n, int stride, float* ell, float* v,
+                       int mode, float alpha, float beta, float gamma, float* pred, int k_pred,
+                       int32_t* pred_idx, int pred_idx_stride, int32_t* pred_count,
+                       cudaStream_t s);
+
+struct ThresholdArgs {
+  KvView kv;
+  const __nv_bfloat16* q;
+  const float* scores;
+  int score_stride;
+  float tau;
+  int cap;
+  int flags;
+  float scale_log2;
+  int32_t* idx;
+  int idx_stride;
+  int32_t* count;
+  float* out;
+  float* m;
+  float* l;
+};
+cudaError_t launch_threshold(const CUtensorMap& tmK, const CUtensorMap& tmV,
+                             const ThresholdArgs& a, cudaStream_t s);
+
+}  // namespace dsa

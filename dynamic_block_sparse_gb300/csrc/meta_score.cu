@@ -1,0 +1,253 @@
+// Per-page key metadata and page criticality scoring.  Both are streaming HBM scans: 16-byte
+// vector loads, several independent loads in flight per thread, no shared-memory staging needed.
+#include "common.cuh"
+#include "internal.h"
+
+namespace dsa {
+namespace {
+
+// ------------------------------------------------------------------------------------ metadata
+// One warp per (request, page position, KV head).  Lane l reads 16-byte chunk (l & 15) of token
+// rows of parity (l >> 4); the two half-warps are combined at the end of every logical page.
+template <int KIND>
+__global__ void __launch_bounds__(256)
+    build_meta_kernel(const KvView kv, const __nv_bfloat16* __restrict__ k_pages, int lp,
+                      void* __restrict__ meta) {
+  const int lane = threadIdx.x & 31;
+  const long long item = static_cast<long long>(blockIdx.x) * 8 + (threadIdx.x >> 5);
+  const int h = static_cast<int>(item % kv.Hkv);
+  const long long bj = item / kv.Hkv;
+  const int b = static_cast<int>(bj / kv.max_pages), j = static_cast<int>(bj % kv.max_pages);
+  if (b >= kv.B) return;
+  const int page = kv.p;
+  const int L = request_len(kv, b);
+  const int npos = (L + page - 1) / page;
+  if (j >= npos) return;
+  const int phys = kv.page_table[static_cast<size_t>(b) * kv.max_pages + j];
+  if (phys < 0 || phys >= kv.num_phys) {
+    if (lane == 0) raise_status(kv.status, DSA_STATUS_BAD_PAGE);
+    return;
+  }
+  const int valid = min(page, L - j * page);
+  const int g = page / lp;
+  const int half = lane >> 4, c = lane & 15;
+  const __nv_bfloat16* base =
+      k_pages + (static_cast<size_t>(phys) * kv.Hkv + h) * page * kHeadDim + c * 8;
+
+  for (int sub = 0; sub < g; ++sub) {
+    const int t_lo = sub * lp, t_hi = min((sub + 1) * lp, valid);
+    float a[8], bmin[8];
+#pragma unroll
+    for (int e = 0; e < 8; ++e) {
+      a[e] = (KIND == DSA_META_MINMAX) ? -INFINITY : 0.f;
+      bmin[e] = INFINITY;
+    }
+    int t = t_lo + half;
+#pragma unroll 1
+    for (; t + 6 < t_hi; t += 8) {
+      uint4 raw[4];
+#pragma unroll
+      for (int u = 0; u < 4; ++u)
+        raw[u] = __ldg(reinterpret_cast<const uint4*>(base + static_cast<size_t>(t + 2 * u) * kHeadDim));
+#pragma unroll
+      for (int u = 0; u < 4; ++u) {
+        const __nv_bfloat16* v = reinterpret_cast<const __nv_bfloat16*>(&raw[u]);
+#pragma unroll
+        for (int e = 0; e < 8; ++e) {
+          const float x = __bfloat162float(v[e]);
+          if (KIND == DSA_META_MINMAX) {
+            a[e] = fmaxf(a[e], x);
+            bmin[e] = fminf(bmin[e], x);
+          } else {
+            a[e] += x;
+          }
+        }
+      }
+    }
+    for (; t < t_hi; t += 2) {
+      const uint4 raw = __ldg(reinterpret_cast<const uint4*>(base + static_cast<size_t>(t) * kHeadDim));
+      const __nv_bfloat16* v = reinterpret_cast<const __nv_bfloat16*>(&raw);
+#pragma unroll
+      for (int e = 0; e < 8; ++e) {
+        const float x = __bfloat162float(v[e]);
+        if (KIND == DSA_META_MINMAX) {
+          a[e] = fmaxf(a[e], x);
+          bmin[e] = fminf(bmin[e], x);
+        } else {
+          a[e] += x;
+        }
+      }
+    }
+#pragma unroll
+    for (int e = 0; e < 8; ++e) {
+      const float oa = __shfl_xor_sync(0xffffffffu, a[e], 16);
+      const float ob = __shfl_xor_sync(0xffffffffu, bmin[e], 16);
+      if (KIND == DSA_META_MINMAX) {
+        a[e] = fmaxf(a[e], oa);
+        bmin[e] = fminf(bmin[e], ob);
+      } else {
+        a[e] += oa;
+      }
+    }
+    const bool empty = t_hi <= t_lo;
+    const size_t rec = (static_cast<size_t>(phys) * kv.Hkv + h) * g + sub;
+    // lanes < 16 write dims 8c..8c+3, lanes >= 16 dims 8c+4..8c+7
+    const int e0 = half * 4;
+    if (KIND == DSA_META_MINMAX) {
+      uint4 o;
+      uint32_t* w = reinterpret_cast<uint32_t*>(&o);
+#pragma unroll
+      for (int e = 0; e < 4; ++e) {
+        const float hi = half ? a[4 + e] : a[e];
+        const float lo = half ? bmin[4 + e] : bmin[e];
+        __nv_bfloat162 pr = __floats2bfloat162_rn(empty ? 0.f : hi, empty ? 0.f : lo);
+        w[e] = *reinterpret_cast<uint32_t*>(&pr);
+      }
+      __nv_bfloat16* dst = reinterpret_cast<__nv_bfloat16*>(meta) + rec * (2 * kHeadDim) +
+                           (c * 8 + e0) * 2;
+      *reinterpret_cast<uint4*>(dst) = o;
+    } else {
+      const float cnt = static_cast<float>(max(t_hi - t_lo, 1));
+      float4 o;
+      o.x = empty ? 0.f : (half ? a[4] : a[0]) / cnt;
+      o.y = empty ? 0.f : (half ? a[5] : a[1]) / cnt;
+      o.z = empty ? 0.f : (half ? a[6] : a[2]) / cnt;
+      o.w = empty ? 0.f : (half ? a[7] : a[3]) / cnt;
+      float* dst = reinterpret_cast<float*>(meta) + rec * kHeadDim + c * 8 + e0;
+      *reinterpret_cast<float4*>(dst) = o;
+    }
+  }
+}
+
+// ------------------------------------------------------------------------------------ scoring
+// Each 512-byte metadata record (MINMAX: 128 x (max, min) bf16; MEAN: 128 fp32) is read by a
+// group of 8 lanes, 4 x 16 bytes each; chunk c covers dims 4c..4c+3 in both formats, so lane
+// (l & 7) always needs the same 16 query dims and keeps them in registers.
+constexpr int kScoreThreads = 256;
+constexpr int kScoreGroups = kScoreThreads / 8;
+
+template <int KIND>
+DSA_DEV float record_partial(const uint4 (&raw)[4], const float (&qv)[16]) {
+  float s = 0.f;
+#pragma unroll
+  for (int i = 0; i < 4; ++i) {
+    if (KIND == DSA_META_MINMAX) {
+      const __nv_bfloat16* v = reinterpret_cast<const __nv_bfloat16*>(&raw[i]);
+#pragma unroll
+      for (int e = 0; e < 4; ++e) {
+        const float q = qv[i * 4 + e];
+        const float hi = q * __bfloat162float(v[2 * e]);
+        const float lo = q * __bfloat162float(v[2 * e + 1]);
+        s += fmaxf(hi, lo);
+      }
+    } else {
+      const float* v = reinterpret_cast<const float*>(&raw[i]);
+#pragma unroll
+      for (int e = 0; e < 4; ++e) s = fmaf(qv[i * 4 + e], v[e], s);
+    }
+  }
+  return s;
+}
+
+template <int KIND>
+__global__ void __launch_bounds__(kScoreThreads)
+    score_kernel(const KvView kv, const __nv_bfloat16* __restrict__ q,
+                 const uint8_t* __restrict__ meta, int lp, int pages_per_cta,
+                 float* __restrict__ scores, int stride) {
+  __shared__ float sQbar[kHeadDim];
+  const int row = blockIdx.y;
+  const int b = row / kv.Hkv, h = row % kv.Hkv;
+  const int j0 = blockIdx.x * pages_per_cta;
+  const int j1 = min(j0 + pages_per_cta, stride);
+  float* out = scores + static_cast<size_t>(row) * stride;
+  if (kv.streaming != nullptr && kv.streaming[h] != 0) {
+    for (int j = j0 + threadIdx.x; j < j1; j += kScoreThreads) out[j] = -INFINITY;
+    return;
+  }
+  const int g = kv.p / lp;
+  const int L = request_len(kv, b);
+  const int nl = (L + lp - 1) / lp;
+  if (threadIdx.x < kHeadDim) {
+    const __nv_bfloat16* qg = q + (static_cast<size_t>(b) * kv.Hq + h * kv.G) * kHeadDim;
+    float s = 0.f;
+    for (int r = 0; r < kv.G; ++r) s += __bfloat162float(qg[r * kHeadDim + threadIdx.x]);
+    sQbar[threadIdx.x] = s / static_cast<float>(kv.G);
+  }
+  __syncthreads();
+  const int lane = threadIdx.x & 31;
+  const int gl = lane & 7;
+  float qv[16];
+#pragma unroll
+  for (int i = 0; i < 4; ++i)
+#pragma unroll
+    for (int e = 0; e < 4; ++e) qv[i * 4 + e] = sQbar[(gl + 8 * i) * 4 + e];
+
+  const int32_t* table = kv.page_table + static_cast<size_t>(b) * kv.max_pages;
+  // warp-uniform loop: warp w, group gi of its 4 groups, handles records jA and jA + 32
+  for (int jbase = j0 + (threadIdx.x >> 5) * 4; jbase < j1; jbase += 2 * kScoreGroups) {
+    const int jA = jbase + (lane >> 3);
+    const int jB = jA + kScoreGroups;
+    const bool inA = jA < j1 && jA < nl, inB = jB < j1 && jB < nl;
+    const int physA = inA ? table[jA / g] : 0;
+    const int physB = inB ? table[jB / g] : 0;
+    const bool okA = inA && physA >= 0 && physA < kv.num_phys;
+    const bool okB = inB && physB >= 0 && physB < kv.num_phys;
+    if (gl == 0 && ((inA && !okA) || (inB && !okB))) raise_status(kv.status, DSA_STATUS_BAD_PAGE);
+    uint4 ra[4], rb[4];
+    if (okA) {
+      const uint4* rec = reinterpret_cast<const uint4*>(
+          meta + ((static_cast<size_t>(physA) * kv.Hkv + h) * g + jA % g) * 512);
+#pragma unroll
+      for (int i = 0; i < 4; ++i) ra[i] = __ldg(rec + gl + 8 * i);
+    }
+    if (okB) {
+      const uint4* rec = reinterpret_cast<const uint4*>(
+          meta + ((static_cast<size_t>(physB) * kv.Hkv + h) * g + jB % g) * 512);
+#pragma unroll
+      for (int i = 0; i < 4; ++i) rb[i] = __ldg(rec + gl + 8 * i);
+    }
+    float sA = okA ? record_partial<KIND>(ra, qv) : 0.f;
+    float sB = okB ? record_partial<KIND>(rb, qv) : 0.f;
+#pragma unroll
+    for (int o = 1; o < 8; o <<= 1) {
+      sA += __shfl_xor_sync(0xffffffffu, sA, o);
+      sB += __shfl_xor_sync(0xffffffffu, sB, o);
+    }
+    if (gl == 0) {
+      if (jA < j1) out[jA] = okA ? sA : -INFINITY;
+      if (jB < j1) out[jB] = okB ? sB : -INFINITY;
+    }
+  }
+}
+
+}  // namespace
+
+cudaError_t launch_build_meta(const KvView& kv, const __nv_bfloat16* k_pages, int kind, int lp,
+                              void* meta, cudaStream_t s) {
+  const long long items = static_cast<long long>(kv.B) * kv.max_pages * kv.Hkv;
+  const long long blocks = (items + 7) / 8;
+  if (blocks > 0x7fffffffLL) return cudaErrorInvalidValue;
+  if (kind == DSA_META_MINMAX)
+    build_meta_kernel<DSA_META_MINMAX><<<static_cast<unsigned>(blocks), 256, 0, s>>>(kv, k_pages, lp, meta);
+  else
+    build_meta_kernel<DSA_META_MEAN><<<static_cast<unsigned>(blocks), 256, 0, s>>>(kv, k_pages, lp, meta);
+  return cudaGetLastError();
+}
+
+cudaError_t launch_score(const KvView& kv, const __nv_bfloat16* q, const void* meta, int kind,
+                         int lp, float* scores, int stride, cudaStream_t s) {
+  const int rows = kv.B * kv.Hkv;
+  // Enough CTAs to cover every SM a few times; each group handles 2 records per round.
+  int ppc = 2 * kScoreGroups;
+  while (ppc > 2 * kScoreGroups / 2 && static_cast<long long>(rows) * ((stride + ppc - 1) / ppc) < 4 * 152)
+    ppc /= 2;
+  dim3 grid((stride + ppc - 1) / ppc, rows);
+  const uint8_t* m = static_cast<const uint8_t*>(meta);
+  if (kind == DSA_META_MINMAX)
+    score_kernel<DSA_META_MINMAX><<<grid, kScoreThreads, 0, s>>>(kv, q, m, lp, ppc, scores, stride);
+  else
+    score_kernel<DSA_META_MEAN><<<grid, kScoreThreads, 0, s>>>(kv, q, m, lp, ppc, scores, stride);
+  return cudaGetLastError();
+}
+
+}  // namespace dsa

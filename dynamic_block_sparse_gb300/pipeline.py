@@ -1,0 +1,263 @@
+"""Decode-step pipelines over libdsa: host-side sequencing of the C-ABI calls, nothing else.
+
+Every buffer a step needs is allocated once, when a decoder is built; a step only enqueues
+library kernels on the current CUDA stream (and, for PRR, on a second stream).
+
+* :class:`TopKDecoder`      — kmax/kmin page scores, fixed top-K, sparse attention.
+* :class:`HierDecoder`      — LServe: logical pages scored, max-reduced to physical pages,
+                              top-K physical pages reused for ``reuse`` steps; streaming heads
+                              attend to their sink + local window.
+* :class:`ThresholdDecoder` — PSA: mean-key block scores, progressive threshold selection with
+                              fused attention.
+* :class:`PRRDecoder`       — PRR: speculative attention over the EMA-predicted set P runs on a
+                              second stream while scoring and top-K selection produce the true
+                              set A; the repair pass adds A \\ P and drops P \\ A.
+"""
+
+from __future__ import annotations
+
+import math
+
+import torch
+
+from . import binding as B
+
+
+class Cache:
+    """A paged bf16 KV cache on the GPU plus its descriptor."""
+
+    def __init__(self, k_pages, v_pages, page_table, seq_lens, num_q_heads: int,
+                 head_is_streaming=None):
+        self.k_pages, self.v_pages = k_pages, v_pages
+        self.page_table, self.seq_lens = page_table, seq_lens
+        self.head_is_streaming = head_is_streaming
+        self.num_q_heads = num_q_heads
+        self.device = k_pages.device
+        self.status = torch.zeros(1, dtype=torch.int32, device=self.device)
+        self.kv = B.paged_kv(k_pages, v_pages, page_table, seq_lens, num_q_heads,
+                             head_is_streaming, self.status)
+        P, self.num_kv_heads, self.page_size, self.head_dim = k_pages.shape
+        self.num_phys_pages = P
+        self.batch, self.max_pages = page_table.shape
+        self.group = num_q_heads // self.num_kv_heads
+        self.rows = self.batch * self.num_kv_heads
+
+    @classmethod
+    def from_inputs(cls, inputs: dict, device="cuda") -> "Cache":
+        w = inputs["workload"]
+        t = {k: inputs[k].to(device) for k in ("k_pages", "v_pages", "page_table", "seq_lens",
+                                                "head_is_streaming")}
+        hs = t["head_is_streaming"] if w.streaming_kv_heads else None
+        return cls(t["k_pages"], t["v_pages"], t["page_table"], t["seq_lens"], w.num_q_heads, hs)
+
+    def meta_buffer(self, kind: int, logical_page: int) -> torch.Tensor:
+        g = self.page_size // logical_page
+        if kind == B.DSA_META_MINMAX:
+            return torch.zeros((self.num_phys_pages, self.num_kv_heads, g, self.head_dim, 2),
+                               dtype=torch.bfloat16, device=self.device)
+        return torch.zeros((self.num_phys_pages, self.num_kv_heads, g, self.head_dim),
+                           dtype=torch.float32, device=self.device)
+
+    def outputs(self):
+        o = torch.zeros((self.batch, self.num_q_heads, self.head_dim), dtype=torch.float32,
+                        device=self.device)
+        m = torch.zeros((self.batch, self.num_q_heads), dtype=torch.float32, device=self.device)
+        l = torch.zeros_like(m)
+        return o, m, l
+
+
+class TopKDecoder:
+    def __init__(self, cache: Cache, k: int, logical_page: int | None = None,
+                 meta_kind: int = B.DSA_META_MINMAX, scale: float | None = None):
+        c = cache
+        self.cache, self.k = c, k
+        self.lp = logical_page or c.page_size
+        self.kind = meta_kind
+        self.scale = scale if scale is not None else 1.0 / math.sqrt(c.head_dim)
+        self.meta = c.meta_buffer(meta_kind, self.lp)
+        self.stride = c.max_pages * (c.page_size // self.lp)
+        self.scores = torch.empty((c.batch, c.num_kv_heads, self.stride), dtype=torch.float32,
+                                  device=c.device)
+        self.idx = torch.empty((c.batch, c.num_kv_heads, max(1, k)), dtype=torch.int32,
+                               device=c.device)
+        self.count = torch.empty((c.batch, c.num_kv_heads), dtype=torch.int32, device=c.device)
+        self.out, self.m, self.l = c.outputs()
+        ws = B.dsa_sparse_decode_attn_workspace_size(c.kv, self.idx.shape[-1])
+        self.workspace = torch.empty(max(16, ws), dtype=torch.uint8, device=c.device)
+
+    def build_meta(self, stream=None):
+        B.dsa_build_page_meta(self.cache.kv, self.kind, self.lp, self.meta, stream)
+
+    def select(self, q, stream=None):
+        c = self.cache
+        B.dsa_score_pages(c.kv, q, self.meta, self.kind, self.lp, self.scores, stream)
+        B.dsa_select_topk(self.scores, self.stride, self.k, self.idx, self.count, stream)
+
+    def attend(self, q, stream=None):
+        B.dsa_sparse_decode_attn(self.cache.kv, q, self.idx, self.count, self.scale, self.out,
+                                 self.m, self.l, workspace=self.workspace, stream=stream)
+
+    def step(self, q, stream=None):
+        self.select(q, stream)
+        self.attend(q, stream)
+        return self.out, self.m, self.l
+
+
+class HierDecoder:
+    def __init__(self, cache: Cache, k_phys: int, logical_page: int, sink: int, local: int,
+                 reuse: int = 4, scale: float | None = None):
+        c = cache
+        self.cache, self.k, self.lp = c, k_phys, logical_page
+        self.g = c.page_size // logical_page
+        self.sink, self.local, self.reuse = sink, local, reuse
+        self.scale = scale if scale is not None else 1.0 / math.sqrt(c.head_dim)
+        self.meta = c.meta_buffer(B.DSA_META_MINMAX, logical_page)
+        self.stride = c.max_pages * self.g
+        self.scores = torch.empty((c.batch, c.num_kv_heads, self.stride), dtype=torch.float32,
+                                  device=c.device)
+        self.idx = torch.empty((c.batch, c.num_kv_heads, max(1, k_phys)), dtype=torch.int32,
+                               device=c.device)
+        self.count = torch.empty((c.batch, c.num_kv_heads), dtype=torch.int32, device=c.device)
+        self.out, self.m, self.l = c.outputs()
+        ws = B.dsa_sparse_decode_attn_workspace_size(c.kv, self.idx.shape[-1])
+        self.workspace = torch.empty(max(16, ws), dtype=torch.uint8, device=c.device)
+
+    def build_meta(self, stream=None):
+        B.dsa_build_page_meta(self.cache.kv, B.DSA_META_MINMAX, self.lp, self.meta, stream)
+
+    def select(self, q, stream=None):
+        c = self.cache
+        B.dsa_score_pages(c.kv, q, self.meta, B.DSA_META_MINMAX, self.lp, self.scores, stream)
+        B.dsa_select_hier(self.scores, self.stride, self.g, self.k, self.idx, self.count, stream)
+
+    def step(self, q, t: int, stream=None):
+        """Decode step t: selection runs when t is a multiple of the reuse interval (LServe §4.3),
+        otherwise the previous selection is reused with this step's query."""
+        c = self.cache
+        if t % self.reuse == 0:
+            self.select(q, stream)
+        B.dsa_sparse_decode_attn(c.kv, q, self.idx, self.count, self.scale, self.out, self.m,
+                                 self.l, workspace=self.workspace, stream=stream)
+        if c.head_is_streaming is not None:
+            B.dsa_streaming_head_attn(c.kv, q, self.sink, self.local, self.scale, self.out,
+                                      self.m, self.l, stream)
+        return self.out, self.m, self.l
+
+
+class ThresholdDecoder:
+    def __init__(self, cache: Cache, tau: float, cap: int, use_nleft: bool = False,
+                 scale: float | None = None):
+        c = cache
+        self.cache, self.tau, self.cap = c, tau, cap
+        self.flags = B.DSA_PSA_NLEFT if use_nleft else 0
+        self.scale = scale if scale is not None else 1.0 / math.sqrt(c.head_dim)
+        self.meta = c.meta_buffer(B.DSA_META_MEAN, c.page_size)
+        self.stride = c.max_pages
+        self.scores = torch.empty((c.batch, c.num_kv_heads, self.stride), dtype=torch.float32,
+                                  device=c.device)
+        self.idx = torch.empty((c.batch, c.num_kv_heads, cap), dtype=torch.int32, device=c.device)
+        self.count = torch.empty((c.batch, c.num_kv_heads), dtype=torch.int32, device=c.device)
+        self.out, self.m, self.l = c.outputs()
+
+    def build_meta(self, stream=None):
+        B.dsa_build_page_meta(self.cache.kv, B.DSA_META_MEAN, self.cache.page_size, self.meta,
+                              stream)
+
+    def step(self, q, stream=None):
+        c = self.cache
+        B.dsa_score_pages(c.kv, q, self.meta, B.DSA_META_MEAN, c.page_size, self.scores, stream)
+        B.dsa_select_threshold(c.kv, q, self.scores, self.tau, self.cap, self.scale, self.idx,
+                               self.count, self.out, self.m, self.l, self.flags, stream)
+        return self.out, self.m, self.l
+
+
+class PRRDecoder:
+    """Predict, reuse and repair over top-K block selection (PRR §3.1-§3.4, fixed budget)."""
+
+    def __init__(self, cache: Cache, k: int, k_pred: int, alpha: float, beta: float,
+                 gamma: float, superset: bool = False, scale: float | None = None,
+                 two_streams: bool = True):
+        c = cache
+        self.cache, self.k, self.k_pred = c, k, k_pred
+        self.alpha, self.beta, self.gamma = alpha, beta, gamma
+        self.superset = superset
+        self.scale = scale if scale is not None else 1.0 / math.sqrt(c.head_dim)
+        self.meta = c.meta_buffer(B.DSA_META_MINMAX, c.page_size)
+        self.stride = c.max_pages
+        dev = c.device
+        self.scores = torch.empty((c.batch, c.num_kv_heads, self.stride), dtype=torch.float32,
+                                  device=dev)
+        self.ell = torch.zeros_like(self.scores)
+        self.trend = torch.zeros_like(self.scores)
+        self.pred = torch.empty_like(self.scores)
+        self.idx = torch.empty((c.batch, c.num_kv_heads, k), dtype=torch.int32, device=dev)
+        self.count = torch.empty((c.batch, c.num_kv_heads), dtype=torch.int32, device=dev)
+        self.spec_idx = torch.empty((c.batch, c.num_kv_heads, k_pred), dtype=torch.int32,
+                                    device=dev)
+        self.spec_count = torch.empty((c.batch, c.num_kv_heads), dtype=torch.int32, device=dev)
+        self.partials = torch.empty((c.batch, c.num_kv_heads, k_pred, c.group, B.RECORD_FLOATS),
+                                    dtype=torch.float32, device=dev)
+        self.out, self.m, self.l = c.outputs()
+        ws = max(B.dsa_repair_merge_workspace_size(c.kv, k),
+                 B.dsa_sparse_decode_attn_workspace_size(c.kv, k))
+        self.workspace = torch.empty(max(16, ws), dtype=torch.uint8, device=dev)
+        self.side = torch.cuda.Stream(device=dev) if two_streams else None
+        self.t = 0
+
+    def build_meta(self, stream=None):
+        B.dsa_build_page_meta(self.cache.kv, B.DSA_META_MINMAX, self.cache.page_size, self.meta,
+                              stream)
+
+    def _score_select(self, q, stream):
+        c = self.cache
+        B.dsa_score_pages(c.kv, q, self.meta, B.DSA_META_MINMAX, c.page_size, self.scores, stream)
+        B.dsa_select_topk(self.scores, self.stride, self.k, self.idx, self.count, stream)
+
+    def _ema(self, mode, stream):
+        B.dsa_ema_predict_update(self.scores, self.stride, self.ell, self.trend, mode, self.alpha,
+                                 self.beta, self.gamma, self.pred, self.k_pred, self.spec_idx,
+                                 self.spec_count, stream)
+
+    # ---- stages (one or two library calls each), exposed so a caller can time them one by one
+    def stage_score(self, q, stream=None):
+        c = self.cache
+        B.dsa_score_pages(c.kv, q, self.meta, B.DSA_META_MINMAX, c.page_size, self.scores, stream)
+
+    def stage_select(self, stream=None):
+        B.dsa_select_topk(self.scores, self.stride, self.k, self.idx, self.count, stream)
+
+    def stage_spec(self, q, stream=None):
+        B.dsa_sparse_decode_attn(self.cache.kv, q, self.spec_idx, self.spec_count, self.scale,
+                                 page_partials=self.partials, stream=stream)
+
+    def stage_repair(self, q, stream=None):
+        B.dsa_repair_merge(self.cache.kv, q, self.spec_idx, self.spec_count, self.partials,
+                           self.idx, self.count, self.scale, self.out, self.m, self.l,
+                           self.workspace, superset=self.superset, stream=stream)
+
+    def stage_ema(self, mode=B.DSA_EMA_UPDATE, stream=None):
+        self._ema(mode, stream)
+
+    def step(self, q):
+        """One decode step with query q (bf16 [B][Hq][D]); returns (out, m, l)."""
+        c = self.cache
+        main = torch.cuda.current_stream(c.device)
+        if self.t == 0:
+            self._score_select(q, main)
+            B.dsa_sparse_decode_attn(c.kv, q, self.idx, self.count, self.scale, self.out, self.m,
+                                     self.l, workspace=self.workspace, stream=main)
+            self._ema(B.DSA_EMA_INIT, main)
+        else:
+            spec_stream = self.side if self.side is not None else main
+            if self.side is not None:
+                self.side.wait_stream(main)
+            # speculative attention over P (predicted at the end of the previous step) ...
+            self.stage_spec(q, spec_stream)
+            # ... while the true scores and the true set A are computed
+            self._score_select(q, main)
+            if self.side is not None:
+                main.wait_stream(self.side)
+            self.stage_repair(q, main)
+            self._ema(B.DSA_EMA_UPDATE, main)
+        self.t += 1
+        return self.out, self.m, self.l

@@ -48,7 +48,11 @@ enum {
 };
 
 /* Bits a kernel may OR into kv->status (device int32).  Never set by a correct call. */
-enum { DSA_STATUS_BAD_PAGE = 1, DSA_STATUS_OVERFLOW = 2 };
+enum {
+  DSA_STATUS_BAD_PAGE = 1, /* a page-table entry outside [0, num_phys_pages) was skipped */
+  DSA_STATUS_OVERFLOW = 2, /* a list exceeded an internal capacity and was truncated */
+  DSA_STATUS_TIMEOUT = 4   /* a bounded on-device wait gave up (the kernel returned early) */
+};
 
 enum { DSA_META_MINMAX = 0, DSA_META_MEAN = 1 };
 enum { DSA_EMA_INIT = 0, DSA_EMA_UPDATE = 1 };
@@ -126,7 +130,7 @@ int dsa_score_pages(const dsa_paged_kv* kv, const void* q, const void* meta, int
  *                 valid entries, ties to the lower index, written in ASCENDING index order;
  *                 slots past the count are set to -1.
  *   count (out) : int32 [rows].
- * n <= 65536.  One CTA per row.
+ * n <= 32768.  One CTA per row.
  */
 int dsa_select_topk(const float* scores, int32_t rows, int32_t n, int32_t stride, int32_t k,
                     int32_t* idx, int32_t idx_stride, int32_t* count, dsa_stream_t stream);
@@ -156,7 +160,7 @@ int dsa_select_hier(const float* logical_scores, int32_t rows, int32_t n_logical
  *   idx (out)    : int32 [B][Hkv][idx_stride], idx_stride >= cap: visited page positions in
  *                  visiting (rank) order; count (out) int32 [B][Hkv].
  *   out/m/l (out): fp32 [B][Hq][D], [B][Hq], [B][Hq]: attention over the visited blocks.
- * ranks n_valid <= 65536 pages per row.
+ * max_pages_per_seq <= 16384.
  */
 int dsa_select_threshold(const dsa_paged_kv* kv, const void* q, const float* scores,
                          int32_t score_stride, float tau, int32_t cap, int32_t flags, float scale,

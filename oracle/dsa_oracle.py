@@ -24,7 +24,8 @@ Readings taken where the pages are silent or garbled (each also listed in the de
   the listing maintains is unused there; ``use_nleft`` switches to
   ``AS_acc / (AS_acc + N_left * AS_min)``); with a GQA group the rule must hold for every query head
   of the group;
-* the EMA update uses the previous level in both equations, exactly as printed;
+* the EMA update uses the previous level in both equations, exactly as printed; a page without
+  a level yet starts at its score with zero trend;
 * PRR's exact mode drops speculative pages outside the true set (output equals attention over the
   true set); its superset mode keeps them (output equals attention over the union).
 """
@@ -323,13 +324,19 @@ def ema_init(IS):
 def ema_update(IS, ell, v, alpha: float, beta: float):
     """PRR §3.1 update with the true scores of step t; both equations read the level of step t-1:
     ``v_t = beta (IS_t - l_{t-1}) + (1 - beta) v_{t-1}`` and ``l_t = alpha IS_t + (1 - alpha) l_{t-1}``.
-    Pages whose score is -inf keep level -inf and trend 0."""
+    Pages whose score is -inf keep level -inf and trend 0; a page that has a score but no level
+    yet (it just became valid) starts the way ``ema_init`` does: level = IS, trend = 0."""
     IS = np.asarray(IS, dtype=np.float64)
+    ell = np.asarray(ell, dtype=np.float64)
+    v = np.asarray(v, dtype=np.float64)
     valid = IS > NEG_INF
+    fresh = valid & ~(ell > NEG_INF)
+    upd = valid & ~fresh
     v_new = np.zeros_like(IS)
     l_new = np.full_like(IS, NEG_INF)
-    v_new[valid] = beta * (IS[valid] - ell[valid]) + (1.0 - beta) * v[valid]
-    l_new[valid] = alpha * IS[valid] + (1.0 - alpha) * ell[valid]
+    v_new[upd] = beta * (IS[upd] - ell[upd]) + (1.0 - beta) * v[upd]
+    l_new[upd] = alpha * IS[upd] + (1.0 - alpha) * ell[upd]
+    l_new[fresh] = IS[fresh]
     return l_new, v_new
 
 

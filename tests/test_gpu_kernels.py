@@ -1,0 +1,445 @@
+"""Kernel-by-kernel parity of libdsa against the float64 oracle (one C-ABI call per test)."""
+
+import math
+
+import numpy as np
+import pytest
+import torch
+
+import oracle as O
+from dynamic_block_sparse_gb300 import binding as B
+from dynamic_block_sparse_gb300.pipeline import Cache
+from dynamic_block_sparse_gb300.workloads import Workload, make_inputs
+from support import (assert_outputs, check_topk, f64, oracle_mean_scores, oracle_minmax_scores,
+                     row_tokens, to_cuda)
+
+pytestmark = pytest.mark.gpu
+
+
+def small(B_=2, Hq=8, Hkv=2, L=700, page=16, lp=None, kind="minmax", extra=5, seed=7, hot=0,
+          streaming=()):
+    w = Workload("unit", B_, Hq, Hkv, 128, L, page, lp or page, kind, "topk", k=8, hot_pages=hot,
+                 hot_scale=0.5, seed=seed, ragged=True, extra_phys_pages=extra,
+                 streaming_kv_heads=streaming)
+    inp = to_cuda(make_inputs(w, "cpu"))
+    cache = Cache(inp["k_pages"], inp["v_pages"], inp["page_table"], inp["seq_lens"], Hq,
+                  inp["head_is_streaming"] if streaming else None)
+    return w, inp, cache
+
+
+def keys_values(inp, cache, b, h):
+    L = int(inp["seq_lens"][b])
+    return (row_tokens(inp["k_pages"], inp["page_table"], L, b, h),
+            row_tokens(inp["v_pages"], inp["page_table"], L, b, h), L)
+
+
+# ---------------------------------------------------------------------------------- metadata
+
+@pytest.mark.parametrize("page,lp", [(16, 16), (64, 16), (64, 64), (32, 8)])
+@pytest.mark.parametrize("kind", ["minmax", "mean"])
+def test_build_page_meta(page, lp, kind):
+    w, inp, cache = small(page=page, lp=lp, kind=kind, L=page * 9 + 5)
+    code = B.DSA_META_MINMAX if kind == "minmax" else B.DSA_META_MEAN
+    meta = cache.meta_buffer(code, lp)
+    B.dsa_build_page_meta(cache.kv, code, lp, meta)
+    torch.cuda.synchronize()
+    g = page // lp
+    table = inp["page_table"].cpu().numpy()
+    mcpu = meta.float().cpu().numpy()
+    for b in range(w.batch):
+        for h in range(w.num_kv_heads):
+            K, _, L = keys_values(inp, cache, b, h)
+            if kind == "minmax":
+                kmax, kmin = O.page_meta_minmax(K, lp)
+                for j in range(len(kmax)):
+                    rec = mcpu[table[b, j // g], h, j % g]
+                    np.testing.assert_array_equal(rec[:, 0], kmax[j])
+                    np.testing.assert_array_equal(rec[:, 1], kmin[j])
+            else:
+                mean = O.page_meta_mean(K, lp)
+                for j in range(len(mean)):
+                    rec = mcpu[table[b, j // g], h, j % g]
+                    np.testing.assert_allclose(rec, mean[j], rtol=1e-6, atol=1e-6)
+    assert int(cache.status.item()) == 0
+
+
+# ---------------------------------------------------------------------------------- scoring
+
+@pytest.mark.parametrize("page,lp,Hq,Hkv", [(16, 16, 8, 2), (64, 16, 16, 4), (64, 64, 32, 2),
+                                           (16, 16, 4, 4)])
+@pytest.mark.parametrize("kind", ["minmax", "mean"])
+def test_score_pages(page, lp, Hq, Hkv, kind):
+    w, inp, cache = small(Hq=Hq, Hkv=Hkv, page=page, lp=lp, kind=kind, L=page * 23 + 3,
+                          streaming=(1,) if Hkv > 2 else ())
+    code = B.DSA_META_MINMAX if kind == "minmax" else B.DSA_META_MEAN
+    meta = cache.meta_buffer(code, lp)
+    B.dsa_build_page_meta(cache.kv, code, lp, meta)
+    stride = cache.max_pages * (page // lp) + 3
+    scores = torch.full((w.batch, Hkv, stride), 7.0, device="cuda")
+    q = inp["q"][0]
+    B.dsa_score_pages(cache.kv, q, meta, code, lp, scores)
+    s = scores.double().cpu().numpy()
+    G = Hq // Hkv
+    for b in range(w.batch):
+        for h in range(Hkv):
+            if h in w.streaming_kv_heads:
+                assert np.all(np.isneginf(s[b, h]))
+                continue
+            K, _, L = keys_values(inp, cache, b, h)
+            qg = q[b, h * G:(h + 1) * G]
+            ref = (oracle_minmax_scores if kind == "minmax" else oracle_mean_scores)(K, qg, lp, stride)
+            nl = -(-L // lp)
+            assert np.all(np.isneginf(s[b, h, nl:]))
+            scale = np.abs(ref[:nl]).max()
+            np.testing.assert_allclose(s[b, h, :nl], ref[:nl], rtol=1e-5, atol=1e-6 * scale)
+
+
+# ---------------------------------------------------------------------------------- selection
+
+def _tied_scores(rows, n, seed, neg_inf_frac=0.1):
+    g = torch.Generator().manual_seed(seed)
+    s = torch.round(torch.randn(rows, n, generator=g) * 4) / 4       # many exact ties
+    s[torch.rand(rows, n, generator=g) < neg_inf_frac] = -math.inf
+    s[0, : min(n, 3)] = torch.tensor([0.0, -0.0, 0.0])[: min(n, 3)]   # signed zeros tie
+    if rows > 1:
+        s[1] = -math.inf                                               # a row with nothing valid
+    return s
+
+
+@pytest.mark.parametrize("n,k", [(1, 1), (37, 5), (37, 0), (2048, 256), (8192, 64), (8192, 76),
+                                 (32768, 1000), (300, 400)])
+def test_select_topk_exact(n, k):
+    s = _tied_scores(5, n, seed=n + k)
+    stride = n + 3
+    sd = torch.full((5, stride), -math.inf)
+    sd[:, :n] = s
+    sd = sd.cuda()
+    idx = torch.full((5, max(k, 1)), -7, dtype=torch.int32, device="cuda")
+    cnt = torch.empty(5, dtype=torch.int32, device="cuda")
+    B.dsa_select_topk(sd, n, k, idx, cnt)
+    idx, cnt = idx.cpu().numpy(), cnt.cpu().numpy()
+    for r in range(5):
+        ref = O.select_topk(s[r].double().numpy(), k)
+        assert cnt[r] == len(ref)
+        assert list(idx[r, :cnt[r]]) == ref
+        assert np.all(idx[r, cnt[r]:k] == -1)
+
+
+@pytest.mark.parametrize("n_logical,g,k", [(8192, 4, 64), (1001, 4, 12), (64, 1, 8), (999, 3, 50)])
+def test_select_hier_exact(n_logical, g, k):
+    s = _tied_scores(4, n_logical, seed=g * 100 + k)
+    sd = s.cuda()
+    idx = torch.empty((4, k), dtype=torch.int32, device="cuda")
+    cnt = torch.empty(4, dtype=torch.int32, device="cuda")
+    B.dsa_select_hier(sd, n_logical, g, k, idx, cnt)
+    idx, cnt = idx.cpu().numpy(), cnt.cpu().numpy()
+    for r in range(4):
+        ref = O.select_hier(s[r].double().numpy(), g, k)
+        assert list(idx[r, :cnt[r]]) == ref
+
+
+# ---------------------------------------------------------------------------------- attention
+
+def _random_selection(w, inp, k, seed, allow_bad=True):
+    g = np.random.default_rng(seed)
+    rows = w.batch * w.num_kv_heads
+    idx = np.full((rows, k), -1, dtype=np.int32)
+    cnt = np.zeros(rows, dtype=np.int32)
+    for r in range(rows):
+        b = r // w.num_kv_heads
+        npos = -(-int(inp["seq_lens"][b]) // w.page_size)
+        c = int(g.integers(0, min(k, npos) + 1)) if r % 3 else min(k, npos)
+        sel = sorted(g.choice(npos, c, replace=False).tolist())
+        if allow_bad and r == 1 and c > 0:
+            sel[-1] = npos + 3                                  # out of range: skipped
+        idx[r, :c] = sel
+        cnt[r] = c
+    return idx, cnt
+
+
+def _oracle_sparse(w, inp, cache, q, idx, cnt, scale):
+    G = w.group
+    O_ref = np.zeros((w.batch, w.num_q_heads, 128))
+    m_ref = np.full((w.batch, w.num_q_heads), -np.inf)
+    l_ref = np.zeros((w.batch, w.num_q_heads))
+    for r in range(idx.shape[0]):
+        b, h = divmod(r, w.num_kv_heads)
+        K, V, L = keys_values(inp, cache, b, h)
+        npos = -(-L // w.page_size)
+        pages = [int(j) for j in idx[r, :cnt[r]] if 0 <= j < npos]
+        res = O.attend(q[b, h * G:(h + 1) * G], K, V, O.page_token_ids(pages, w.page_size, L), scale)
+        O_ref[b, h * G:(h + 1) * G], m_ref[b, h * G:(h + 1) * G], l_ref[b, h * G:(h + 1) * G] = res
+    return O_ref, m_ref, l_ref
+
+
+@pytest.mark.parametrize("Hq,Hkv,page", [(8, 2, 16), (4, 4, 16), (32, 2, 64), (16, 2, 32),
+                                         (24, 2, 16)])
+@pytest.mark.parametrize("splits", [0, 1, 3])
+def test_sparse_decode_attn(Hq, Hkv, page, splits):
+    w, inp, cache = small(Hq=Hq, Hkv=Hkv, page=page, L=page * 40 + 9, seed=Hq + page)
+    k = 24
+    idx, cnt = _random_selection(w, inp, k, seed=splits + Hq)
+    scale = 1 / math.sqrt(128)
+    q = inp["q"][0]
+    ws = B.dsa_sparse_decode_attn_workspace_size(cache.kv, k, splits)
+    wsb = torch.empty(max(ws, 16), dtype=torch.uint8, device="cuda")
+    out, m, l = cache.outputs()
+    B.dsa_sparse_decode_attn(cache.kv, q, torch.from_numpy(idx).cuda(), torch.from_numpy(cnt).cuda(),
+                             scale, out, m, l, num_splits=splits, workspace=wsb)
+    torch.cuda.synchronize()
+    ref = _oracle_sparse(w, inp, cache, q, idx, cnt, scale)
+    assert_outputs(out.cpu().numpy(), m.cpu().numpy(), l.cpu().numpy(), ref, "sparse attn")
+    assert int(cache.status.item()) == 0
+
+
+@pytest.mark.parametrize("Hq,Hkv,page", [(32, 2, 64), (8, 2, 16)])
+def test_page_partials_and_merge(Hq, Hkv, page):
+    w, inp, cache = small(Hq=Hq, Hkv=Hkv, page=page, L=page * 30 + 1, seed=3)
+    k = 12
+    idx, cnt = _random_selection(w, inp, k, seed=5, allow_bad=False)
+    scale = 1 / math.sqrt(128)
+    q = inp["q"][0]
+    G = w.group
+    part = torch.full((w.batch, Hkv, k, G, B.RECORD_FLOATS), 9.0, device="cuda")
+    out, m, l = cache.outputs()
+    B.dsa_sparse_decode_attn(cache.kv, q, torch.from_numpy(idx).cuda(), torch.from_numpy(cnt).cuda(),
+                             scale, out, m, l, page_partials=part)
+    torch.cuda.synchronize()
+    pc = part.cpu().numpy()
+    for r in range(w.batch * Hkv):
+        b, h = divmod(r, Hkv)
+        K, V, L = keys_values(inp, cache, b, h)
+        for i in range(cnt[r]):
+            ref = O.attend(q[b, h * G:(h + 1) * G], K, V,
+                           O.page_token_ids([idx[r, i]], page, L), scale)
+            rec = pc[b, h, i]
+            assert_outputs(rec[:, :128], rec[:, 128], rec[:, 129], ref, f"record {r},{i}")
+    ref = _oracle_sparse(w, inp, cache, q, idx, cnt, scale)
+    assert_outputs(out.cpu().numpy(), m.cpu().numpy(), l.cpu().numpy(), ref, "merged partials")
+
+
+def test_merge_partials_generic():
+    g = np.random.default_rng(4)
+    rows, parts, G = 3, 5, 4
+    rec = np.zeros((rows, parts, G, B.RECORD_FLOATS), dtype=np.float32)
+    rec[..., :128] = g.normal(size=(rows, parts, G, 128))
+    rec[..., 128] = g.normal(size=(rows, parts, G)) * 3
+    rec[..., 129] = g.uniform(0.5, 20, size=(rows, parts, G))
+    rec[1, 2, :, 129] = 0.0                  # empty part: identity
+    rec[1, 2, :, 128] = -np.inf
+    t = torch.from_numpy(rec).cuda()
+    out = torch.empty((rows * G, 128), device="cuda")
+    m = torch.empty(rows * G, device="cuda")
+    l = torch.empty_like(m)
+    B.dsa_merge_partials(t, out, m, l)
+    for r in range(rows):
+        ref = O.merge_partials([(rec[r, p, :, :128].astype(np.float64), rec[r, p, :, 128].astype(np.float64),
+                                 rec[r, p, :, 129].astype(np.float64)) for p in range(parts)])
+        assert_outputs(out[r * G:(r + 1) * G].cpu().numpy(), m[r * G:(r + 1) * G].cpu().numpy(),
+                       l[r * G:(r + 1) * G].cpu().numpy(), ref, f"merge row {r}")
+
+
+@pytest.mark.parametrize("L,sink,local,page", [(5000, 64, 256, 64), (300, 64, 256, 64),
+                                               (200, 64, 256, 16), (1000, 0, 100, 16),
+                                               (1000, 50, 0, 16), (4100, 64, 256, 16)])
+def test_streaming_head_attn(L, sink, local, page):
+    w, inp, cache = small(Hq=16, Hkv=4, page=page, L=L, streaming=(2, 3), seed=L)
+    scale = 1 / math.sqrt(128)
+    q = inp["q"][0]
+    out, m, l = cache.outputs()
+    out.fill_(5.0)
+    B.dsa_streaming_head_attn(cache.kv, q, sink, local, scale, out, m, l)
+    torch.cuda.synchronize()
+    G = w.group
+    oc, mc, lc = out.cpu().numpy(), m.cpu().numpy(), l.cpu().numpy()
+    for b in range(w.batch):
+        for h in range(4):
+            sl = slice(h * G, (h + 1) * G)
+            if h not in (2, 3):
+                assert np.all(oc[b, sl] == 5.0)          # dense heads untouched
+                continue
+            K, V, Lb = keys_values(inp, cache, b, h)
+            ref = O.attend(q[b, sl], K, V, O.streaming_token_ids(Lb, sink, local), scale)
+            assert_outputs(oc[b, sl], mc[b, sl], lc[b, sl], ref, f"stream b{b} h{h}")
+
+
+@pytest.mark.parametrize("case", ["random", "disjoint", "p_superset", "equal", "empty_p"])
+@pytest.mark.parametrize("superset", [False, True])
+def test_repair_merge(case, superset):
+    w, inp, cache = small(Hq=32, Hkv=2, page=64, L=64 * 50 + 17, seed=11)
+    G = w.group
+    kA, kP = 10, 12
+    g = np.random.default_rng(hash(case) % 997)
+    rows = w.batch * 2
+    A = np.full((rows, kA), -1, np.int32)
+    P = np.full((rows, kP), -1, np.int32)
+    cA = np.zeros(rows, np.int32)
+    cP = np.zeros(rows, np.int32)
+    for r in range(rows):
+        b = r // 2
+        npos = -(-int(inp["seq_lens"][b]) // 64)
+        a = sorted(g.choice(npos, kA, replace=False).tolist())
+        rest = [j for j in range(npos) if j not in a]
+        if case == "random":
+            p = sorted(g.choice(npos, kP, replace=False).tolist())
+        elif case == "disjoint":
+            p = sorted(g.choice(rest, kP, replace=False).tolist())
+        elif case == "p_superset":
+            p = sorted(a + g.choice(rest, 2, replace=False).tolist())
+        elif case == "equal":
+            p = list(a)
+        else:
+            p = []
+        A[r, :len(a)], cA[r] = a, len(a)
+        P[r, :len(p)], cP[r] = p, len(p)
+    scale = 1 / math.sqrt(128)
+    q = inp["q"][0]
+    dA, dP = torch.from_numpy(A).cuda(), torch.from_numpy(P).cuda()
+    dcA, dcP = torch.from_numpy(cA).cuda(), torch.from_numpy(cP).cuda()
+    part = torch.zeros((w.batch, 2, kP, G, B.RECORD_FLOATS), device="cuda")
+    B.dsa_sparse_decode_attn(cache.kv, q, dP, dcP, scale, page_partials=part)
+    ws = torch.empty(B.dsa_repair_merge_workspace_size(cache.kv, kA), dtype=torch.uint8, device="cuda")
+    out, m, l = cache.outputs()
+    B.dsa_repair_merge(cache.kv, q, dP, dcP, part, dA, dcA, scale, out, m, l, ws, superset=superset)
+    torch.cuda.synchronize()
+    for r in range(rows):
+        b, h = divmod(r, 2)
+        K, V, L = keys_values(inp, cache, b, h)
+        sl = slice(h * G, (h + 1) * G)
+        pages = sorted(set(A[r, :cA[r]]) | (set(P[r, :cP[r]]) if superset else set()))
+        ref = O.attend(q[b, sl], K, V, O.page_token_ids(pages, 64, L), scale)
+        orc = O.spec_repair(q[b, sl], K, V, 64, L, P[r, :cP[r]], A[r, :cA[r]], scale, superset)
+        for x, y in zip(ref, orc):
+            np.testing.assert_allclose(x, y, rtol=1e-12, atol=1e-12)
+        assert_outputs(out[b, sl].cpu().numpy(), m[b, sl].cpu().numpy(), l[b, sl].cpu().numpy(),
+                       ref, f"repair {case} row {r}")
+
+
+# ---------------------------------------------------------------------------------- EMA
+
+def test_ema_predict_update_sequence():
+    rows, n, k_pred = 3, 5000, 76
+    gen = torch.Generator().manual_seed(5)
+    base = torch.randn(rows, n, generator=gen) * 3 + 240
+    traj = [base + 0.3 * t * torch.randn(rows, n, generator=gen) for t in range(5)]
+    for t in traj:
+        t[:, n - 100:] = -math.inf                      # pages beyond the request
+    traj[3][0, 10:20] = -math.inf                       # temporarily invalid, then fresh again
+    stride = n + 8
+    IS = torch.full((rows, stride), -math.inf, device="cuda")
+    ell = torch.zeros((rows, stride), device="cuda")
+    v = torch.zeros_like(ell)
+    pred = torch.empty_like(ell)
+    pidx = torch.empty((rows, k_pred), dtype=torch.int32, device="cuda")
+    pcnt = torch.empty(rows, dtype=torch.int32, device="cuda")
+    ell64 = v64 = None
+    for t, s in enumerate(traj):
+        IS[:, :n] = s.cuda()
+        mode = B.DSA_EMA_INIT if t == 0 else B.DSA_EMA_UPDATE
+        B.dsa_ema_predict_update(IS, n, ell, v, mode, 0.6, 0.3, 0.5, pred, k_pred, pidx, pcnt)
+        torch.cuda.synchronize()
+        s64 = s.double().numpy()
+        if t == 0:
+            ell64, v64 = zip(*[O.ema_init(s64[r]) for r in range(rows)])
+        else:
+            ell64, v64 = zip(*[O.ema_update(s64[r], ell64[r], v64[r], 0.6, 0.3) for r in range(rows)])
+        for r in range(rows):
+            lg = ell[r, :n].double().cpu().numpy()
+            vg = v[r, :n].double().cpu().numpy()
+            fin = np.isfinite(ell64[r])
+            assert np.array_equal(np.isneginf(lg), ~fin)
+            np.testing.assert_allclose(lg[fin], ell64[r][fin], rtol=1e-6, atol=1e-5)
+            np.testing.assert_allclose(vg, v64[r], rtol=1e-5, atol=1e-4)
+            p64 = O.ema_predict(ell64[r], v64[r], 0.5)
+            check_topk(pidx[r, :pcnt[r]].cpu().numpy(), p64, k_pred, f"P t{t} r{r}")
+
+
+# ---------------------------------------------------------------------------------- PSA
+
+@pytest.mark.parametrize("tau,cap,nleft,G", [(0.95, 64, False, 1), (0.99, 12, False, 1),
+                                             (0.95, 64, True, 1), (1.0, 20, False, 1),
+                                             (0.9, 64, False, 4)])
+def test_select_threshold(tau, cap, nleft, G):
+    w = Workload("psa_unit", 2, 4 * G, 4, 128, 16 * 200 + 3, 16, 16, "mean", "threshold", cap=cap,
+                 tau=tau, zipf_s=1.1, seed=21, ragged=True, extra_phys_pages=3)
+    inp = to_cuda(make_inputs(w, "cpu"))
+    cache = Cache(inp["k_pages"], inp["v_pages"], inp["page_table"], inp["seq_lens"], w.num_q_heads)
+    meta = cache.meta_buffer(B.DSA_META_MEAN, 16)
+    B.dsa_build_page_meta(cache.kv, B.DSA_META_MEAN, 16, meta)
+    stride = cache.max_pages
+    scores = torch.empty((w.batch, 4, stride), device="cuda")
+    q = inp["q"][0]
+    B.dsa_score_pages(cache.kv, q, meta, B.DSA_META_MEAN, 16, scores)
+    idx = torch.full((w.batch, 4, cap), -1, dtype=torch.int32, device="cuda")
+    cnt = torch.empty((w.batch, 4), dtype=torch.int32, device="cuda")
+    out, m, l = cache.outputs()
+    scale = 1 / math.sqrt(128)
+    B.dsa_select_threshold(cache.kv, q, scores, tau, cap, scale, idx, cnt, out, m, l,
+                           B.DSA_PSA_NLEFT if nleft else 0)
+    torch.cuda.synchronize()
+    for b in range(w.batch):
+        for h in range(4):
+            K, V, L = keys_values(inp, cache, b, h)
+            qg = q[b, h * G:(h + 1) * G]
+            s64 = oracle_mean_scores(K, qg, 16, stride)
+            res = O.psa_progressive(qg, K, V, s64, 16, L, tau, cap, scale, use_nleft=nleft)
+            n_gpu = int(cnt[b, h])
+            got = idx[b, h, :n_gpu].cpu().numpy().tolist()
+            if got != res["ranked"]:
+                # allowed only when the decisive ratio sits on the threshold
+                r_last = res["ratios"][min(n_gpu, len(res["ratios"])) - 1]
+                assert got[:len(res["ranked"])] == res["ranked"][:len(got)], (b, h, got, res["ranked"])
+                assert np.min(np.abs(np.asarray(r_last) - tau)) <= 1e-5 * tau, (b, h, n_gpu, len(res["ranked"]))
+            ref = O.attend(qg, K, V, O.page_token_ids(got, 16, L), scale)
+            sl = slice(h * G, (h + 1) * G)
+            assert_outputs(out[b, sl].cpu().numpy(), m[b, sl].cpu().numpy(), l[b, sl].cpu().numpy(),
+                           ref, f"psa b{b} h{h}")
+
+
+# ---------------------------------------------------------------------------------- robustness
+
+def test_bad_page_ids_raise_status_without_fault():
+    w, inp, cache = small(Hq=8, Hkv=2, page=16, L=16 * 20)
+    table = inp["page_table"].clone()
+    table[0, 3] = cache.num_phys_pages + 11
+    table[1, 0] = -4
+    kv = B.paged_kv(inp["k_pages"], inp["v_pages"], table, inp["seq_lens"], 8, None, cache.status)
+    meta = cache.meta_buffer(B.DSA_META_MINMAX, 16)
+    B.dsa_build_page_meta(kv, B.DSA_META_MINMAX, 16, meta)
+    idx = torch.tensor([[[3, 4]] * 2] * 2, dtype=torch.int32, device="cuda")
+    idx[1, :, 0] = 0
+    cnt = torch.full((2, 2), 2, dtype=torch.int32, device="cuda")
+    out, m, l = cache.outputs()
+    ws = torch.empty(max(16, B.dsa_sparse_decode_attn_workspace_size(kv, 2)), dtype=torch.uint8,
+                     device="cuda")
+    B.dsa_sparse_decode_attn(kv, inp["q"][0], idx, cnt, 0.1, out, m, l, workspace=ws)
+    torch.cuda.synchronize()
+    assert int(cache.status.item()) & B.DSA_STATUS_BAD_PAGE
+    assert torch.isfinite(out).all()
+
+
+def test_host_errors_are_reported():
+    w, inp, cache = small()
+    kv = B.paged_kv(inp["k_pages"], inp["v_pages"], inp["page_table"], inp["seq_lens"], 8)
+    kv.head_dim = 64
+    with pytest.raises(B.DsaError, match="head_dim"):
+        B.dsa_build_page_meta(kv, 0, 16, cache.meta_buffer(0, 16))
+    scores = torch.zeros((2, 10), device="cuda")
+    with pytest.raises(B.DsaError, match="idx_stride"):
+        B.dsa_select_topk(scores, 10, 5, torch.zeros((2, 3), dtype=torch.int32, device="cuda"),
+                          torch.zeros(2, dtype=torch.int32, device="cuda"))
+
+
+def test_kernels_are_deterministic():
+    w, inp, cache = small(Hq=32, Hkv=2, page=64, L=64 * 60, seed=1)
+    idx, cnt = _random_selection(w, inp, 40, seed=2, allow_bad=False)
+    dI, dC = torch.from_numpy(idx).cuda(), torch.from_numpy(cnt).cuda()
+    ws = torch.empty(B.dsa_sparse_decode_attn_workspace_size(cache.kv, 40) + 16,
+                     dtype=torch.uint8, device="cuda")
+    outs = []
+    for _ in range(2):
+        out, m, l = cache.outputs()
+        B.dsa_sparse_decode_attn(cache.kv, inp["q"][0], dI, dC, 0.08, out, m, l, workspace=ws)
+        outs.append((out.clone(), m.clone(), l.clone()))
+    for a, b in zip(*outs):
+        assert torch.equal(a, b)

@@ -1,0 +1,158 @@
+"""CPU-only checks of the host side: the C-ABI library builds, loads and exports every symbol the
+header declares; host-side argument validation answers without touching a GPU; the input
+generator is deterministic and plants what it says; the replica timing reduction works across
+processes (gloo)."""
+
+import ctypes
+import json
+import math
+import os
+import subprocess
+import sys
+
+import numpy as np
+import pytest
+import torch
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+
+
+@pytest.fixture(scope="module")
+def lib():
+    from dynamic_block_sparse_gb300 import binding, build
+    build.build()
+    return binding.load()
+
+
+def test_library_exports_every_header_function(lib):
+    from dynamic_block_sparse_gb300 import binding, build
+    names = binding.header_functions()
+    assert len(names) >= 14
+    nm = subprocess.run(["nm", "-D", "--defined-only", build.LIB_PATH], capture_output=True,
+                        text=True, check=True).stdout
+    exported = {ln.split()[-1] for ln in nm.splitlines() if ln.strip()}
+    for n in names:
+        assert n in exported, f"{n} declared in include/dsa.h but not exported"
+        assert hasattr(lib, n)
+    assert set(binding._SIGNATURES) == set(names), "binding signatures out of sync with the header"
+
+
+def test_header_struct_layout_matches_binding():
+    from dynamic_block_sparse_gb300 import binding
+    assert ctypes.sizeof(binding.PagedKV) == 6 * 8 + 7 * 4 + 4  # 6 pointers, 7 int32, padding
+
+
+def test_version_and_empty_error(lib):
+    assert b"sm_103a" in lib.dsa_version()
+    assert lib.dsa_last_error() == b""
+
+
+def test_host_validation_without_gpu(lib):
+    from dynamic_block_sparse_gb300 import binding as B
+    rc = lib.dsa_build_page_meta(None, 0, 16, None, None)
+    assert rc == -1 and b"kv descriptor" in lib.dsa_last_error()
+    kv = B.PagedKV()
+    kv.k_pages = kv.v_pages = kv.page_table = kv.seq_lens = 4096
+    kv.batch, kv.num_q_heads, kv.num_kv_heads = 1, 32, 2
+    kv.head_dim, kv.page_size, kv.max_pages_per_seq, kv.num_phys_pages = 64, 64, 8, 8
+    assert lib.dsa_build_page_meta(ctypes.byref(kv), 0, 64, 4096, None) == -3
+    assert b"head_dim" in lib.dsa_last_error()
+    kv.head_dim = 128
+    kv.page_size = 24
+    assert lib.dsa_build_page_meta(ctypes.byref(kv), 0, 24, 4096, None) == -3
+    kv.page_size = 64
+    kv.num_q_heads = 40
+    assert lib.dsa_build_page_meta(ctypes.byref(kv), 0, 64, 4096, None) == -3    # G = 20 > 16
+    kv.num_q_heads = 32
+    assert lib.dsa_build_page_meta(ctypes.byref(kv), 0, 48, 4096, None) == -1    # lp does not divide
+    assert lib.dsa_build_page_meta(ctypes.byref(kv), 0, 64, 4100, None) == -2    # misaligned meta
+    kv.k_pages = 4104
+    assert lib.dsa_build_page_meta(ctypes.byref(kv), 0, 64, 4096, None) == -2    # misaligned pool
+    assert lib.dsa_select_topk(None, 2, 10, 10, 5, None, 5, None, None) == -1
+    assert lib.dsa_select_topk(None, 0, 10, 10, 5, None, 5, None, None) == 0     # nothing to do
+    assert lib.dsa_select_topk(4096, 1, 40000, 40000, 5, 4096, 5, 4096, None) == -3
+    assert lib.dsa_ema_predict_update(4096, 1, 10, 10, 4096, 4096, 7, 0.6, 0.3, 0.5, None, 0,
+                                      None, 0, None, None) == -1
+    kv.k_pages = 4096
+    assert lib.dsa_select_threshold(ctypes.byref(kv), 4096, 4096, 8, 1.5, 4, 0, 0.1, 4096, 4,
+                                    4096, 4096, 4096, 4096, None) == -1          # tau > 1
+    assert lib.dsa_sparse_decode_attn_workspace_size(ctypes.byref(kv), 64, 1) == 0
+    assert lib.dsa_sparse_decode_attn_workspace_size(ctypes.byref(kv), 64, 4) == 2 * 4 * 16 * 132 * 4
+    assert lib.dsa_repair_merge_workspace_size(ctypes.byref(kv), 64) == 2 * 16 * 16 * 132 * 4
+
+
+def test_binding_refuses_cpu_tensors(lib):
+    from dynamic_block_sparse_gb300 import binding as B
+    with pytest.raises(ValueError, match="CUDA"):
+        B.dsa_select_topk(torch.zeros(2, 8), 8, 2, torch.zeros((2, 2), dtype=torch.int32),
+                          torch.zeros(2, dtype=torch.int32))
+
+
+def test_generator_is_deterministic_and_plants_hot_pages():
+    from dynamic_block_sparse_gb300.workloads import oracle_scale, BY_NAME, make_inputs
+    w = oracle_scale(BY_NAME["llama3_8b_layer"])
+    a, b = make_inputs(w), make_inputs(w)
+    for k in ("k_pages", "v_pages", "page_table", "seq_lens", "q"):
+        assert torch.equal(a[k], b[k])
+    assert a["k_pages"].dtype == torch.bfloat16
+    assert sorted(a["page_table"].flatten().tolist()) == sorted(set(a["page_table"].flatten().tolist()))
+    # hot pages: mean key projection on the query direction is ~hot_scale above the rest
+    G = w.group
+    q = a["q"][0, 0, :G].float().sum(0)
+    u = q / q.norm()
+    L = int(a["seq_lens"][0])
+    proj = []
+    for j in range(-(-L // w.page_size)):
+        proj.append(float(a["k_pages"][int(a["page_table"][0, j]), 0].float().mean(0) @ u))
+    proj = np.sort(np.array(proj))[::-1]
+    assert proj[: w.hot_pages].mean() > proj[w.hot_pages:].mean() + 0.3
+
+
+def test_zipf_workload_masses_follow_rank():
+    from dynamic_block_sparse_gb300.workloads import oracle_scale, BY_NAME, make_inputs
+    w = oracle_scale(BY_NAME["psa_threshold"]).replace(batch=1, num_q_heads=1, num_kv_heads=1)
+    a = make_inputs(w)
+    q = a["q"][0, 0, 0].float()
+    L = int(a["seq_lens"][0])
+    logits = []
+    for j in range(-(-L // 16)):
+        k = a["k_pages"][int(a["page_table"][0, j]), 0].float()
+        logits.append(float((k @ q).mean() / math.sqrt(128)))
+    logits = np.sort(np.array(logits))[::-1]
+    r = np.arange(1, len(logits) + 1)
+    slope = np.polyfit(np.log(r[:200]), logits[:200], 1)[0]
+    assert -1.4 < slope < -0.8           # mean logit of rank r falls like -1.1 ln r
+
+
+def test_bench_byte_accounting():
+    sys.path.insert(0, ROOT)
+    import bench
+    from dynamic_block_sparse_gb300.workloads import BY_NAME
+    w = BY_NAME["prr_512k"]
+    total, north, parts = bench.prr_bytes(w, 8192, [152], [4])
+    assert parts["meta"] == 2 * 8192 * 512
+    assert parts["kv"] == 156 * 64 * 512
+    assert north == 2 * 8192 * 512 + 2 * 64 * 64 * 512
+    assert total > parts["meta"] + parts["kv"]
+
+
+def _replica_worker(rank, world, port, out):
+    import torch.distributed as dist
+    os.environ.update(MASTER_ADDR="127.0.0.1", MASTER_PORT=str(port))
+    dist.init_process_group("gloo", rank=rank, world_size=world)
+    sys.path.insert(0, ROOT)
+    import bench
+    dist.barrier()
+    v = bench.max_over_ranks(1.0 + rank * 2.5)
+    with open(out + f".{rank}", "w") as f:
+        json.dump(v, f)
+    dist.destroy_process_group()
+
+
+def test_replica_timing_takes_max_over_ranks_gloo(tmp_path):
+    import torch.multiprocessing as mp
+    port = 29500 + (os.getpid() % 1000)
+    out = str(tmp_path / "r")
+    mp.spawn(_replica_worker, args=(2, port, out), nprocs=2, join=True)
+    vals = [json.load(open(out + f".{r}")) for r in range(2)]
+    assert vals == [3.5, 3.5]

@@ -350,6 +350,14 @@ def test_ema_constant_scores_are_a_fixed_point_and_init_predicts_last_scores():
     np.testing.assert_array_equal(v, [0, 0, 0, 0])
 
 
+def test_ema_page_without_history_starts_like_init():
+    ell = np.array([1.0, -np.inf, -np.inf])
+    v = np.array([0.5, 0.0, 0.0])
+    l2, v2 = O.ema_update(np.array([2.0, 4.0, -np.inf]), ell, v, 0.6, 0.3)
+    np.testing.assert_allclose(l2, [0.6 * 2 + 0.4 * 1, 4.0, -np.inf])
+    np.testing.assert_allclose(v2, [0.3 * (2 - 1) + 0.7 * 0.5, 0.0, 0.0])
+
+
 def test_ema_prediction_ranking_invariant_under_positive_affine_scores():
     r = rng(41)
     traj = [r.normal(size=50) for _ in range(6)]
