@@ -148,16 +148,17 @@ def dist_env():
 
 # ------------------------------------------------------------------------------------ bytes
 
-def prr_bytes(w, n_valid_pages, P_counts, missed_counts):
-    """Algorithmic bytes of one PRR decode step (see module docstring), and the spec form
-    (metadata + K/V of the true set A only)."""
+def prr_bytes(w, n_valid_pages, P_pages, missed_pages):
+    """Algorithmic bytes of one PRR decode step (see module docstring) for a step that attends
+    ``P_pages`` speculative and ``missed_pages`` repaired (page, KV head) units summed over rows
+    (averages are fine); also the spec form (metadata + K/V of the true set A only)."""
     rows = w.batch * w.num_kv_heads
     G, D = w.group, w.head_dim
     page_kv = w.page_size * D * 2 * 2
     meta = rows * n_valid_pages * 2 * D * 2
     q = w.batch * w.num_q_heads * D * 2
-    kv = (sum(P_counts) + sum(missed_counts)) * page_kv
-    records = (sum(P_counts) + sum(missed_counts)) * G * 132 * 4
+    kv = (P_pages + missed_pages) * page_kv
+    records = (P_pages + missed_pages) * G * 132 * 4
     scores = rows * n_valid_pages * 4 * 3            # written, read by select and by the EMA
     ema = rows * n_valid_pages * 4 * 5               # level, trend read+write, prediction write
     idx = rows * (w.k + w.k_pred) * 4 * 3
@@ -203,38 +204,48 @@ def bench_prr(args, w, dev, rank):
         dec.step(static_q)
     torch.cuda.synchronize()
 
-    graph = torch.cuda.CUDAGraph()
-    with torch.cuda.graph(graph):
-        dec.step(static_q)
+    # one graph per parity of the step index (the speculative-set buffers alternate)
+    parity0 = dec.t % 2
+    graphs = []
+    for _ in range(2):
+        g = torch.cuda.CUDAGraph()
+        with torch.cuda.graph(g):
+            dec.step(static_q)
+        graphs.append(g)
     stage_graphs = {}
     for name, fn in (("score_pages", lambda: dec.stage_score(static_q)),
                      ("select_topk", lambda: dec.stage_select()),
-                     ("spec_attn", lambda: dec.stage_spec(static_q)),
-                     ("repair_merge", lambda: dec.stage_repair(static_q)),
-                     ("ema_predict", lambda: dec.stage_ema())):
+                     ("spec_attn", lambda: dec.stage_spec(static_q, 0)),
+                     ("repair_merge", lambda: dec.stage_repair(static_q, 0)),
+                     ("ema_predict", lambda: dec.stage_ema(buf=1))):
         g = torch.cuda.CUDAGraph()
         with torch.cuda.graph(g):
             fn()
-        stage_graphs[name] = g
+        stage_graphs[name] = [g]
     torch.cuda.synchronize()
+    state = {"i": 0}
 
-    def timed_replay(g, n, qi0=0, collect=None):
+    def timed_replay(glist, n, qi0=0, collect=None):
+        """Replays the graphs in turn (L2 flushed before each, outside the timed window)."""
         starts = [torch.cuda.Event(enable_timing=True) for _ in range(n)]
         ends = [torch.cuda.Event(enable_timing=True) for _ in range(n)]
         for i in range(n):
+            gi = state["i"] % len(glist)
             static_q.copy_(qs[(qi0 + i) % nq])
             if collect is not None:
-                collect[0].append((dec.spec_idx.clone(), dec.spec_count.clone()))
+                buf = (parity0 + gi) % 2
+                collect[0].append((dec.spec_bufs[buf].clone(), dec.spec_counts[buf].clone()))
             flush.fill_(i & 0xFF)
             starts[i].record(stream)
-            g.replay()
+            glist[gi].replay()
             ends[i].record(stream)
+            state["i"] += 1
             if collect is not None:
                 collect[1].append((dec.idx.clone(), dec.count.clone()))
         torch.cuda.synchronize()
         return [s.elapsed_time(e) for s, e in zip(starts, ends)]
 
-    timed_replay(graph, args.warmup, qi0=4)
+    timed_replay(graphs, args.warmup, qi0=4)
     sampler = ClockSampler(gpu_selector(dev))
     sampler.start()
     time.sleep(0.3)
@@ -242,10 +253,12 @@ def bench_prr(args, w, dev, rank):
     if hasattr(torch.distributed, "is_initialized") and torch.distributed.is_initialized():
         torch.distributed.barrier()
     torch.cuda.synchronize()
-    step_ms = timed_replay(graph, args.steps, qi0=4 + args.warmup, collect=collect)
+    step_ms = timed_replay(graphs, args.steps, qi0=4 + args.warmup, collect=collect)
     torch.cuda.synchronize()
-    stage_ms = {name: statistics.mean(timed_replay(g, max(50, min(400, args.steps))))
-                for name, g in stage_graphs.items()}
+    stage_ms = {}
+    for name, g in stage_graphs.items():
+        state["i"] = 0
+        stage_ms[name] = statistics.mean(timed_replay(g, max(50, min(400, args.steps))))
     clocks = sampler.stop()
 
     # pages attended per timed step
@@ -262,9 +275,7 @@ def bench_prr(args, w, dev, rank):
         P_counts.append(pcount)
         missed.append(mcount)
     n = len(step_ms)
-    bytes_step, north_step, parts = prr_bytes(w, n_valid, P_counts, missed)
-    bytes_step /= n
-    north_step /= n
+    bytes_step, north_step, parts = prr_bytes(w, n_valid, sum(P_counts) / n, sum(missed) / n)
     mean_ms = statistics.mean(step_ms)
 
     rows = w.batch * w.num_kv_heads
@@ -287,7 +298,7 @@ def bench_prr(args, w, dev, rank):
                  mean_P=sum(P_counts) / n / rows, mean_missed=sum(missed) / n / rows,
                  bytes_per_step=bytes_step, north_star_bytes_per_step=north_step,
                  north_star_gbs=north_step / (mean_ms * 1e6),
-                 byte_parts={k: v / n for k, v in parts.items()},
+                 byte_parts=parts,
                  step_ms_p50=statistics.median(step_ms), step_ms_min=min(step_ms))
     return dict(mean_ms=mean_ms, bytes_step=bytes_step, clocks=clocks, dominant=dominant,
                 dominant_ms=stage_ms[dominant], dominant_bytes=stage_bytes[dominant], e2e=e2e,
@@ -388,8 +399,8 @@ def oracle_prr(w, seconds: float | None, steps: int | None, warmup: int = 0):
             break
     el = time.perf_counter() - t0
     n_valid = -(-w.seq_len // w.page_size)
-    total, _, _ = prr_bytes(w, n_valid, P_counts, missed)
-    return el / done, done, total / done
+    total, _, _ = prr_bytes(w, n_valid, sum(P_counts) / done, sum(missed) / done)
+    return el / done, done, total
 
 
 def cpu_baseline(args, w):

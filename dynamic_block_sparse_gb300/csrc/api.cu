@@ -234,6 +234,7 @@ int dsa_select_threshold(const dsa_paged_kv* kv, const void* q, const float* sco
   if (!q || !scores || !idx || !count || !out || !m || !l)
     return fail(DSA_ERR_INVALID_ARG, "dsa_select_threshold: NULL pointer");
   if (!(tau > 0.f && tau <= 1.f)) return fail(DSA_ERR_INVALID_ARG, "tau must be in (0, 1]");
+  if (!aligned(q, 16)) return fail(DSA_ERR_ALIGNMENT, "q must be 16-byte aligned");
   if (cap < 1 || idx_stride < cap) return fail(DSA_ERR_INVALID_ARG, "need 1 <= cap <= idx_stride");
   if (score_stride < 1) return fail(DSA_ERR_INVALID_ARG, "score_stride < 1");
   if (v.max_pages > kMaxThresholdN)
@@ -280,6 +281,9 @@ int dsa_sparse_decode_attn(const dsa_paged_kv* kv, const void* q, const int32_t*
   if (rc) return rc;
   if (!q || !idx || !count) return fail(DSA_ERR_INVALID_ARG, "q/idx/count is NULL");
   if (idx_stride < 1) return fail(DSA_ERR_INVALID_ARG, "idx_stride < 1");
+  if (!aligned(q, 16)) return fail(DSA_ERR_ALIGNMENT, "q must be 16-byte aligned");
+  if (page_partials && !aligned(page_partials, 16))
+    return fail(DSA_ERR_ALIGNMENT, "page_partials must be 16-byte aligned");
   const bool want_out = out != nullptr;
   if (want_out && (!m || !l)) return fail(DSA_ERR_INVALID_ARG, "out given without m/l");
   if (!want_out && !page_partials)
@@ -377,6 +381,10 @@ int dsa_repair_merge(const dsa_paged_kv* kv, const void* q, const int32_t* spec_
       !l)
     return fail(DSA_ERR_INVALID_ARG, "dsa_repair_merge: NULL pointer");
   if (spec_stride < 1 || true_stride < 1) return fail(DSA_ERR_INVALID_ARG, "stride < 1");
+  if (!aligned(q, 16) || !aligned(page_partials, 16))
+    return fail(DSA_ERR_ALIGNMENT, "q and page_partials must be 16-byte aligned");
+  if (spec_stride > 8192 || true_stride > 8192)
+    return fail(DSA_ERR_UNSUPPORTED, "repair lists longer than 8192 pages");
   const int rows = v.B * v.Hkv;
   const int splits = repair_splits(true_stride);
   const size_t need = record_bytes(rows, splits, v.G);
@@ -434,6 +442,7 @@ int dsa_streaming_head_attn(const dsa_paged_kv* kv, const void* q, int32_t sink_
   if (rc) return rc;
   if (!q || !out || !m || !l) return fail(DSA_ERR_INVALID_ARG, "q/out/m/l is NULL");
   if (sink_tokens < 0 || local_tokens < 0) return fail(DSA_ERR_INVALID_ARG, "negative window");
+  if (!aligned(q, 16)) return fail(DSA_ERR_ALIGNMENT, "q must be 16-byte aligned");
   if (!kv->head_is_streaming) return ok();  // no streaming heads: nothing to do
   const long long pages = (static_cast<long long>(sink_tokens) + v.p - 1) / v.p +
                           (static_cast<long long>(local_tokens) + v.p - 1) / v.p + 1;

@@ -16,10 +16,11 @@ constexpr int kAttnThreads = (kConsumers + 1) * 32;
 constexpr uint32_t kMergeBytes = kConsumers * (16 * 128 + 32) * 4;
 
 struct Layout {
-  uint32_t q_off, list_off, bar_off, misc_off, total;
+  uint32_t q_off, list_off, bar_off, misc_off, scratch_off, total;
 };
 
-__host__ __device__ inline Layout make_layout(int page, int stages) {
+// scratch_ints: extra int32 slots (the speculative list of a repair, staged for binary search).
+__host__ __device__ inline Layout make_layout(int page, int stages, int scratch_ints) {
   Layout L;
   uint32_t area = 512u * static_cast<uint32_t>(page) * static_cast<uint32_t>(stages);
   if (area < kMergeBytes) area = kMergeBytes;
@@ -28,7 +29,8 @@ __host__ __device__ inline Layout make_layout(int page, int stages) {
   L.list_off = L.q_off + 16u * kQStride * 2u;
   L.bar_off = L.list_off + kMaxListPages * 8u;
   L.misc_off = L.bar_off + 16u * static_cast<uint32_t>(stages);
-  L.total = L.misc_off + 64u + 1024u;  // + slack to align the dynamic base to 1024 bytes
+  L.scratch_off = L.misc_off + 64u;
+  L.total = L.scratch_off + 4u * static_cast<uint32_t>(scratch_ints) + 1024u;  // + align slack
   return L;
 }
 
@@ -85,7 +87,7 @@ __global__ void __launch_bounds__(kAttnThreads)
   const KvView& kv = a.kv;
   const int page = kv.p;
   const int S = a.stages;
-  const Layout lay = make_layout(page, S);
+  const Layout lay = make_layout(page, S, LIST == LIST_REPAIR ? a.spec_stride : 0);
   __nv_bfloat16* sQ = reinterpret_cast<__nv_bfloat16*>(smem + lay.q_off);
   int2* list = reinterpret_cast<int2*>(smem + lay.list_off);
   uint64_t* bars = reinterpret_cast<uint64_t*>(smem + lay.bar_off);
@@ -106,25 +108,33 @@ __global__ void __launch_bounds__(kAttnThreads)
   win.local_begin = 0;
   int out_slot = blockIdx.x;
 
+  int one_pos = -1;
   if (LIST == LIST_ONE_PAGE) {
+    // the slot's position and the row's count are independent loads: issue both, then test
+    one_pos = a.idx[static_cast<size_t>(row) * a.idx_stride + blockIdx.x];
     const int cnt = min(max(a.count[row], 0), a.idx_stride);
     if (static_cast<int>(blockIdx.x) >= cnt) return;
+  }
+  int32_t* sP = reinterpret_cast<int32_t*>(smem + lay.scratch_off);
+  if (LIST == LIST_REPAIR) {
+    const int cntP = min(max(a.spec_count[row], 0), a.spec_stride);
+    const int32_t* P = a.spec_idx + static_cast<size_t>(row) * a.spec_stride;
+    for (int i = tid; i < cntP; i += kAttnThreads) sP[i] = P[i];
+    __syncthreads();
   }
 
   // ---- page list (warp 0)
   if (warp == 0) {
     int n = 0;
-    if (LIST == LIST_SELECTED || LIST == LIST_ONE_PAGE) {
+    if (LIST == LIST_ONE_PAGE) {
+      int phys = 0;
+      const bool ok = lane == 0 && lookup_page(kv, b, one_pos, npos, &phys);
+      n = append_round(ok, phys, one_pos, list, n);
+    } else if (LIST == LIST_SELECTED) {
       const int cnt = min(max(a.count[row], 0), a.idx_stride);
-      int beg, end;
-      if (LIST == LIST_ONE_PAGE) {
-        beg = blockIdx.x;
-        end = beg + 1;
-      } else {
-        const int chunk = (cnt + a.num_splits - 1) / a.num_splits;
-        beg = min(cnt, static_cast<int>(blockIdx.x) * chunk);
-        end = min(cnt, beg + chunk);
-      }
+      const int chunk = (cnt + a.num_splits - 1) / a.num_splits;
+      const int beg = min(cnt, static_cast<int>(blockIdx.x) * chunk);
+      const int end = min(cnt, beg + chunk);
       const int32_t* sel = a.idx + static_cast<size_t>(row) * a.idx_stride;
       for (int base = beg; base < end; base += 32) {
         const int i = base + lane;
@@ -157,7 +167,7 @@ __global__ void __launch_bounds__(kAttnThreads)
       const int cntA = min(max(a.count[row], 0), a.idx_stride);
       const int cntP = min(max(a.spec_count[row], 0), a.spec_stride);
       const int32_t* A = a.idx + static_cast<size_t>(row) * a.idx_stride;
-      const int32_t* P = a.spec_idx + static_cast<size_t>(row) * a.spec_stride;
+      const int32_t* P = sP;
       int missed_total = 0;
       for (int base = 0; base < cntA; base += 32) {
         const int i = base + lane;
@@ -281,6 +291,14 @@ __global__ void __launch_bounds__(kAttnThreads)
 
   const bool final_out =
       (LIST == LIST_STREAMING) || (LIST == LIST_SELECTED && a.num_splits == 1);
+  if (!final_out && n_items == 0) {  // an empty part: the merge reads only its (m, l)
+    for (int g = tid; g < kv.G; g += kAttnThreads) {
+      float* rec = a.part +
+                   ((static_cast<size_t>(row) * a.part_slots + out_slot) * kv.G + g) * kRecordFloats;
+      *reinterpret_cast<float4*>(rec + 128) = make_float4(-INFINITY, 0.f, 0.f, 0.f);
+    }
+    return;
+  }
   for (int e = tid; e < kv.G * kHeadDim; e += kAttnThreads) {
     const int g = e >> 7, d = e & 127;
     float M = -INFINITY;
@@ -320,43 +338,138 @@ __global__ void __launch_bounds__(kAttnThreads)
   }
 }
 
-// Merges partial records (O, m, l) of one (row, query head) per CTA; thread d owns dim d.
-__global__ void __launch_bounds__(128) merge_records_kernel(const MergeArgs a) {
-  const int row = blockIdx.x, g = blockIdx.y, d = threadIdx.x;
+// Merges partial records (O, m, l) of one (row, query head) per CTA.  The parts (split records,
+// plus the speculative records of hit pages for a repair) are listed in shared memory, their
+// weights l * exp(m - M) computed in parallel, and the weighted sum of the O vectors is split
+// over 8 warps (each lane owns 4 dimensions) so that many independent loads are in flight.
+constexpr int kMergeThreads = 256;
+constexpr int kMergeWarps = kMergeThreads / 32;
+
+struct MergeLayout {
+  size_t w_off, a_off, acc_off, total;
+};
+
+// Shared-memory layout of the merge: record pointers, weights, the true set, per-warp partial
+// sums; every region starts on a 16-byte boundary (the partial sums are written as float4).
+__host__ __device__ inline MergeLayout merge_layout(int max_parts, int a_ints) {
+  auto up16 = [](size_t x) { return (x + 15) & ~static_cast<size_t>(15); };
+  MergeLayout L;
+  L.w_off = up16(static_cast<size_t>(max_parts) * sizeof(const float*));
+  L.a_off = up16(L.w_off + static_cast<size_t>(max_parts) * sizeof(float));
+  L.acc_off = up16(L.a_off + static_cast<size_t>(a_ints) * sizeof(int32_t));
+  L.total = L.acc_off + static_cast<size_t>(kMergeWarps) * 128 * sizeof(float);
+  return L;
+}
+
+__global__ void __launch_bounds__(kMergeThreads) merge_records_kernel(const MergeArgs a) {
+  extern __shared__ __align__(16) uint8_t msm[];
+  const int row = blockIdx.x, g = blockIdx.y;
   const int b = row / a.Hkv, h = row % a.Hkv;
   if (a.streaming != nullptr && a.streaming[h] != 0) return;
-  float M = -INFINITY, Lsum = 0.f, acc = 0.f;
-  auto fold = [&](const float* rec) {
-    const float lp = rec[129];
-    if (!(lp > 0.f)) return;
-    const float mp = rec[128];
-    const float Mn = fmaxf(M, mp);
-    const float sa = (M == -INFINITY) ? 0.f : fast_exp2((M - Mn) * kLog2e);
-    const float sb = fast_exp2((mp - Mn) * kLog2e) * lp;
-    acc = acc * sa + sb * rec[d];
-    Lsum = Lsum * sa + sb;
-    M = Mn;
-  };
-  const int nparts = a.count ? min(max(a.count[row], 0), a.slots) : a.slots;
-  for (int s = 0; s < nparts; ++s)
-    fold(a.part + ((static_cast<size_t>(row) * a.slots + s) * a.G + g) * kRecordFloats);
+  const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+  const int max_parts = a.slots + (a.spec_part != nullptr ? a.spec_stride : 0);
+  const MergeLayout lay = merge_layout(max_parts, a.spec_part != nullptr ? a.true_stride : 0);
+  const float** s_rec = reinterpret_cast<const float**>(msm);
+  float* s_w = reinterpret_cast<float*>(msm + lay.w_off);
+  int32_t* s_A = reinterpret_cast<int32_t*>(msm + lay.a_off);
+  float* s_acc = reinterpret_cast<float*>(msm + lay.acc_off);
+  __shared__ int s_red[33];
+  __shared__ float s_f[33];
+
+  const int nsplit = a.count ? min(max(a.count[row], 0), a.slots) : a.slots;
+  for (int s = tid; s < nsplit; s += kMergeThreads)
+    s_rec[s] = a.part + ((static_cast<size_t>(row) * a.slots + s) * a.G + g) * kRecordFloats;
+  int nparts = nsplit;
   if (a.spec_part != nullptr) {
     const int cntP = min(max(a.spec_count[row], 0), a.spec_stride);
     const int cntA = min(max(a.true_count[row], 0), a.true_stride);
     const int32_t* P = a.spec_idx + static_cast<size_t>(row) * a.spec_stride;
     const int32_t* A = a.true_idx + static_cast<size_t>(row) * a.true_stride;
-    for (int i = 0; i < cntP; ++i) {
-      if (!a.superset && !contains_sorted(A, cntA, P[i])) continue;
-      fold(a.spec_part + ((static_cast<size_t>(row) * a.spec_stride + i) * a.G + g) *
-                             kRecordFloats);
+    for (int i = tid; i < cntA; i += kMergeThreads) s_A[i] = A[i];
+    __syncthreads();
+    // hits in index order, one block-wide round per kMergeThreads entries of P
+    for (int base = 0; base < cntP; base += kMergeThreads) {
+      const int i = base + tid;
+      const bool hit = i < cntP && (a.superset || contains_sorted(s_A, cntA, P[i]));
+      int total;
+      const int at = block_exclusive_scan(hit ? 1 : 0, s_red, &total);
+      if (hit)
+        s_rec[nparts + at] = a.spec_part +
+                             ((static_cast<size_t>(row) * a.spec_stride + i) * a.G + g) * kRecordFloats;
+      nparts += total;
     }
   }
+  __syncthreads();
+  // weights: M = max m over non-empty parts, w = l exp(m - M), L = sum w
+  float mloc = -INFINITY;
+  for (int k = tid; k < nparts; k += kMergeThreads) {
+    const float* r = s_rec[k];
+    const float lp = r[129], mp = r[128];
+    s_w[k] = lp;
+    if (lp > 0.f) mloc = fmaxf(mloc, mp);
+  }
+  mloc = warp_max(mloc);
+  if (lane == 0) s_f[warp] = mloc;
+  __syncthreads();
+  float M = -INFINITY;
+#pragma unroll
+  for (int w = 0; w < kMergeWarps; ++w) M = fmaxf(M, s_f[w]);
+  __syncthreads();
+  float lsum = 0.f;
+  for (int k = tid; k < nparts; k += kMergeThreads) {
+    const float lp = s_w[k];
+    const float wk = lp > 0.f ? lp * fast_exp2((s_rec[k][128] - M) * kLog2e) : 0.f;
+    s_w[k] = wk;
+    lsum += wk;
+  }
+  lsum = warp_sum(lsum);
+  if (lane == 0) s_f[warp] = lsum;
+  __syncthreads();
+  float Lsum = 0.f;
+#pragma unroll
+  for (int w = 0; w < kMergeWarps; ++w) Lsum += s_f[w];
+  // weighted sum of O: warp w takes parts w, w + 8, ...; lane owns dims 4*lane .. 4*lane + 3
+  float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
+  int k = warp;
+  for (; k + 3 * kMergeWarps < nparts; k += 4 * kMergeWarps) {
+    float4 v[4];
+    float wv[4];
+#pragma unroll
+    for (int u = 0; u < 4; ++u) {
+      wv[u] = s_w[k + u * kMergeWarps];  // empty parts (weight 0) are never read
+      v[u] = wv[u] > 0.f ? *reinterpret_cast<const float4*>(s_rec[k + u * kMergeWarps] + lane * 4)
+                         : make_float4(0.f, 0.f, 0.f, 0.f);
+    }
+#pragma unroll
+    for (int u = 0; u < 4; ++u) {
+      acc.x += wv[u] * v[u].x;
+      acc.y += wv[u] * v[u].y;
+      acc.z += wv[u] * v[u].z;
+      acc.w += wv[u] * v[u].w;
+    }
+  }
+  for (; k < nparts; k += kMergeWarps) {
+    const float wk = s_w[k];
+    if (!(wk > 0.f)) continue;
+    const float4 v = *reinterpret_cast<const float4*>(s_rec[k] + lane * 4);
+    acc.x += wk * v.x;
+    acc.y += wk * v.y;
+    acc.z += wk * v.z;
+    acc.w += wk * v.w;
+  }
+  *reinterpret_cast<float4*>(s_acc + warp * 128 + lane * 4) = acc;
+  __syncthreads();
   const size_t oi = a.out_rows_are_heads
                         ? static_cast<size_t>(b) * a.Hq + static_cast<size_t>(h) * a.G + g
                         : static_cast<size_t>(row) * a.G + g;
-  a.out[oi * kHeadDim + d] = Lsum > 0.f ? acc / Lsum : 0.f;
-  if (d == 0) {
-    a.m[oi] = M;
+  if (tid < kHeadDim) {
+    float o = 0.f;
+#pragma unroll
+    for (int w = 0; w < kMergeWarps; ++w) o += s_acc[w * 128 + tid];
+    a.out[oi * kHeadDim + tid] = Lsum > 0.f ? o / Lsum : 0.f;
+  }
+  if (tid == 0) {
+    a.m[oi] = Lsum > 0.f ? M : -INFINITY;
     a.l[oi] = Lsum;
   }
 }
@@ -364,7 +477,8 @@ __global__ void __launch_bounds__(128) merge_records_kernel(const MergeArgs a) {
 template <int LIST>
 cudaError_t launch_list(const CUtensorMap& tmK, const CUtensorMap& tmV, const AttnArgs& a,
                         int grid_x, cudaStream_t s) {
-  const Layout lay = make_layout(a.kv.p, a.stages);
+  constexpr int list = LIST;
+  const Layout lay = make_layout(a.kv.p, a.stages, list == LIST_REPAIR ? a.spec_stride : 0);
   const size_t bytes = lay.total;
   cudaError_t e =
       ensure_dynamic_smem(reinterpret_cast<const void*>(attn_pages_kernel<LIST>), bytes);
@@ -376,7 +490,9 @@ cudaError_t launch_list(const CUtensorMap& tmK, const CUtensorMap& tmV, const At
 
 }  // namespace
 
-size_t attn_smem_bytes(int page, int stages) { return make_layout(page, stages).total; }
+size_t attn_smem_bytes(int page, int stages, int scratch_ints) {
+  return make_layout(page, stages, scratch_ints).total;
+}
 
 cudaError_t launch_attn(int list, const CUtensorMap& tmK, const CUtensorMap& tmV,
                         const AttnArgs& a, int grid_x, cudaStream_t s) {
@@ -390,8 +506,14 @@ cudaError_t launch_attn(int list, const CUtensorMap& tmK, const CUtensorMap& tmV
 }
 
 cudaError_t launch_merge(const MergeArgs& a, cudaStream_t s) {
+  const size_t bytes =
+      merge_layout(a.slots + (a.spec_part ? a.spec_stride : 0), a.spec_part ? a.true_stride : 0)
+          .total;
+  if (bytes > 200 * 1024) return cudaErrorInvalidValue;
+  cudaError_t e = ensure_dynamic_smem(reinterpret_cast<const void*>(merge_records_kernel), bytes);
+  if (e != cudaSuccess) return e;
   dim3 grid(a.rows, a.G);
-  merge_records_kernel<<<grid, 128, 0, s>>>(a);
+  merge_records_kernel<<<grid, kMergeThreads, bytes, s>>>(a);
   return cudaGetLastError();
 }
 

@@ -70,7 +70,7 @@ inline cudaError_t ensure_dynamic_smem(const void* fn, size_t bytes) {
   return e;
 }
 
-size_t attn_smem_bytes(int page, int stages);
+size_t attn_smem_bytes(int page, int stages, int scratch_ints);
 cudaError_t launch_attn(int list, const CUtensorMap& tmK, const CUtensorMap& tmV,
                         const AttnArgs& a, int grid_x, cudaStream_t s);
 

@@ -8,21 +8,43 @@ namespace {
 
 constexpr int kSelectThreads = 512;
 
+// Loads n fp32 values of a row as 16-byte vectors when the row allows it.
+template <typename F>
+DSA_DEV void for_each_row_value(const float* __restrict__ src, int n, bool vec4, F&& f) {
+  if (vec4) {
+    for (int j4 = threadIdx.x; j4 * 4 < n; j4 += kSelectThreads) {
+      const float4 v = __ldg(reinterpret_cast<const float4*>(src) + j4);
+      const int j = j4 * 4;
+      f(j, v.x);
+      if (j + 1 < n) f(j + 1, v.y);
+      if (j + 2 < n) f(j + 2, v.z);
+      if (j + 3 < n) f(j + 3, v.w);
+    }
+  } else {
+    for (int j = threadIdx.x; j < n; j += kSelectThreads) f(j, __ldg(src + j));
+  }
+}
+
 __global__ void __launch_bounds__(kSelectThreads)
     select_kernel(const float* __restrict__ scores, int n_logical, int stride, int g, int k,
                   int32_t* __restrict__ idx, int idx_stride, int32_t* __restrict__ count) {
   extern __shared__ uint32_t keys[];
-  __shared__ SelectScratch sh;
+  __shared__ SelectScratch<kSelectThreads> sh;
   const int row = blockIdx.x;
   const int n = (n_logical + g - 1) / g;
   const float* s = scores + static_cast<size_t>(row) * stride;
-  for (int j = threadIdx.x; j < n; j += kSelectThreads) {
-    float best = -INFINITY;
-    for (int e = 0; e < g; ++e) {
-      const int jj = j * g + e;
-      if (jj < n_logical) best = fmaxf(best, s[jj]);  // fmaxf drops NaN
+  if (g == 1) {
+    const bool vec4 = (stride & 3) == 0 && (reinterpret_cast<uintptr_t>(scores) & 15) == 0;
+    for_each_row_value(s, n, vec4, [&](int j, float x) { keys[j] = score_key(x); });
+  } else {
+    for (int j = threadIdx.x; j < n; j += kSelectThreads) {
+      float best = -INFINITY;
+      for (int e = 0; e < g; ++e) {
+        const int jj = j * g + e;
+        if (jj < n_logical) best = fmaxf(best, s[jj]);  // fmaxf drops NaN
+      }
+      keys[j] = score_key(best);
     }
-    keys[j] = score_key(best);
   }
   __syncthreads();
   const Selection sel = radix_select<kSelectThreads>(keys, n, k, sh);
@@ -38,26 +60,62 @@ __global__ void __launch_bounds__(kSelectThreads)
                float* __restrict__ pred, int k_pred, int32_t* __restrict__ pred_idx,
                int pred_idx_stride, int32_t* __restrict__ pred_count) {
   extern __shared__ uint32_t keys[];
-  __shared__ SelectScratch sh;
+  __shared__ SelectScratch<kSelectThreads> sh;
   const int row = blockIdx.x;
   const size_t base = static_cast<size_t>(row) * stride;
-  for (int j = threadIdx.x; j < n; j += kSelectThreads) {
-    const float is = IS[base + j];
-    float l_new = -INFINITY, v_new = 0.f;
+  auto update = [&](float is, float l_old, float v_old, float& l_new, float& v_new) {
+    l_new = -INFINITY;
+    v_new = 0.f;
     if (is > -INFINITY) {
-      const float l_old = ell[base + j];
       if (mode == DSA_EMA_INIT || !(l_old > -INFINITY)) {
         l_new = is;  // no history yet: start from the observed score with zero trend
       } else {
-        v_new = beta * (is - l_old) + (1.f - beta) * v[base + j];
+        v_new = beta * (is - l_old) + (1.f - beta) * v_old;
         l_new = alpha * is + (1.f - alpha) * l_old;
       }
     }
-    ell[base + j] = l_new;
-    v[base + j] = v_new;
-    const float p = l_new > -INFINITY ? l_new + gamma * v_new : -INFINITY;
-    if (pred) pred[base + j] = p;
-    keys[j] = score_key(p);
+  };
+  const bool vec4 = (stride & 3) == 0 && (n & 3) == 0 &&
+                    ((reinterpret_cast<uintptr_t>(IS) | reinterpret_cast<uintptr_t>(ell) |
+                      reinterpret_cast<uintptr_t>(v) | reinterpret_cast<uintptr_t>(pred)) & 15) == 0;
+  if (vec4) {
+    for (int j4 = threadIdx.x; j4 * 4 < n; j4 += kSelectThreads) {
+      const size_t o = base + static_cast<size_t>(j4) * 4;
+      const float4 is = __ldg(reinterpret_cast<const float4*>(IS + o));
+      float4 lo = make_float4(0.f, 0.f, 0.f, 0.f), vo = lo;
+      if (mode != DSA_EMA_INIT) {
+        lo = *reinterpret_cast<const float4*>(ell + o);
+        vo = *reinterpret_cast<const float4*>(v + o);
+      }
+      float4 ln, vn, pr;
+      update(is.x, lo.x, vo.x, ln.x, vn.x);
+      update(is.y, lo.y, vo.y, ln.y, vn.y);
+      update(is.z, lo.z, vo.z, ln.z, vn.z);
+      update(is.w, lo.w, vo.w, ln.w, vn.w);
+      pr.x = ln.x > -INFINITY ? ln.x + gamma * vn.x : -INFINITY;
+      pr.y = ln.y > -INFINITY ? ln.y + gamma * vn.y : -INFINITY;
+      pr.z = ln.z > -INFINITY ? ln.z + gamma * vn.z : -INFINITY;
+      pr.w = ln.w > -INFINITY ? ln.w + gamma * vn.w : -INFINITY;
+      *reinterpret_cast<float4*>(ell + o) = ln;
+      *reinterpret_cast<float4*>(v + o) = vn;
+      if (pred) *reinterpret_cast<float4*>(pred + o) = pr;
+      keys[j4 * 4 + 0] = score_key(pr.x);
+      keys[j4 * 4 + 1] = score_key(pr.y);
+      keys[j4 * 4 + 2] = score_key(pr.z);
+      keys[j4 * 4 + 3] = score_key(pr.w);
+    }
+  } else {
+    for (int j = threadIdx.x; j < n; j += kSelectThreads) {
+      float l_new, v_new;
+      const float l_old = mode == DSA_EMA_INIT ? 0.f : ell[base + j];
+      const float v_old = mode == DSA_EMA_INIT ? 0.f : v[base + j];
+      update(IS[base + j], l_old, v_old, l_new, v_new);
+      ell[base + j] = l_new;
+      v[base + j] = v_new;
+      const float p = l_new > -INFINITY ? l_new + gamma * v_new : -INFINITY;
+      if (pred) pred[base + j] = p;
+      keys[j] = score_key(p);
+    }
   }
   if (k_pred <= 0 || pred_idx == nullptr) return;
   __syncthreads();

@@ -56,7 +56,7 @@ __global__ void __launch_bounds__(kThrThreads)
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>(
       (reinterpret_cast<uintptr_t>(smem_raw) + 1023u) & ~static_cast<uintptr_t>(1023u));
-  __shared__ SelectScratch sh;
+  __shared__ SelectScratch<kThrThreads> sh;
   const KvView& kv = a.kv;
   const int page = kv.p;
   const int row = blockIdx.x;

@@ -172,7 +172,14 @@ class ThresholdDecoder:
 
 
 class PRRDecoder:
-    """Predict, reuse and repair over top-K block selection (PRR §3.1-§3.4, fixed budget)."""
+    """Predict, reuse and repair over top-K block selection (PRR §3.1-§3.4, fixed budget).
+
+    Step t (t >= 1) runs on three streams: the speculative pass over P_t on ``side``; scoring,
+    top-K selection of the true set A_t and the repair/merge on the caller's stream; and the EMA
+    update (which needs only this step's scores) on ``ema_stream``, writing P_{t+1} into the other
+    half of a double-buffered list so that it never races the readers of P_t.  The step ends with
+    every stream joined back to the caller's stream.
+    """
 
     def __init__(self, cache: Cache, k: int, k_pred: int, alpha: float, beta: float,
                  gamma: float, superset: bool = False, scale: float | None = None,
@@ -192,9 +199,10 @@ class PRRDecoder:
         self.pred = torch.empty_like(self.scores)
         self.idx = torch.empty((c.batch, c.num_kv_heads, k), dtype=torch.int32, device=dev)
         self.count = torch.empty((c.batch, c.num_kv_heads), dtype=torch.int32, device=dev)
-        self.spec_idx = torch.empty((c.batch, c.num_kv_heads, k_pred), dtype=torch.int32,
-                                    device=dev)
-        self.spec_count = torch.empty((c.batch, c.num_kv_heads), dtype=torch.int32, device=dev)
+        self.spec_bufs = [torch.full((c.batch, c.num_kv_heads, k_pred), -1, dtype=torch.int32,
+                                     device=dev) for _ in range(2)]
+        self.spec_counts = [torch.zeros((c.batch, c.num_kv_heads), dtype=torch.int32, device=dev)
+                            for _ in range(2)]
         self.partials = torch.empty((c.batch, c.num_kv_heads, k_pred, c.group, B.RECORD_FLOATS),
                                     dtype=torch.float32, device=dev)
         self.out, self.m, self.l = c.outputs()
@@ -202,21 +210,21 @@ class PRRDecoder:
                  B.dsa_sparse_decode_attn_workspace_size(c.kv, k))
         self.workspace = torch.empty(max(16, ws), dtype=torch.uint8, device=dev)
         self.side = torch.cuda.Stream(device=dev) if two_streams else None
+        self.ema_stream = torch.cuda.Stream(device=dev) if two_streams else None
         self.t = 0
+
+    @property
+    def spec_idx(self):
+        """The speculative set P the next step will use."""
+        return self.spec_bufs[self.t % 2]
+
+    @property
+    def spec_count(self):
+        return self.spec_counts[self.t % 2]
 
     def build_meta(self, stream=None):
         B.dsa_build_page_meta(self.cache.kv, B.DSA_META_MINMAX, self.cache.page_size, self.meta,
                               stream)
-
-    def _score_select(self, q, stream):
-        c = self.cache
-        B.dsa_score_pages(c.kv, q, self.meta, B.DSA_META_MINMAX, c.page_size, self.scores, stream)
-        B.dsa_select_topk(self.scores, self.stride, self.k, self.idx, self.count, stream)
-
-    def _ema(self, mode, stream):
-        B.dsa_ema_predict_update(self.scores, self.stride, self.ell, self.trend, mode, self.alpha,
-                                 self.beta, self.gamma, self.pred, self.k_pred, self.spec_idx,
-                                 self.spec_count, stream)
 
     # ---- stages (one or two library calls each), exposed so a caller can time them one by one
     def stage_score(self, q, stream=None):
@@ -226,38 +234,48 @@ class PRRDecoder:
     def stage_select(self, stream=None):
         B.dsa_select_topk(self.scores, self.stride, self.k, self.idx, self.count, stream)
 
-    def stage_spec(self, q, stream=None):
-        B.dsa_sparse_decode_attn(self.cache.kv, q, self.spec_idx, self.spec_count, self.scale,
-                                 page_partials=self.partials, stream=stream)
+    def stage_spec(self, q, buf: int = 0, stream=None):
+        B.dsa_sparse_decode_attn(self.cache.kv, q, self.spec_bufs[buf], self.spec_counts[buf],
+                                 self.scale, page_partials=self.partials, stream=stream)
 
-    def stage_repair(self, q, stream=None):
-        B.dsa_repair_merge(self.cache.kv, q, self.spec_idx, self.spec_count, self.partials,
-                           self.idx, self.count, self.scale, self.out, self.m, self.l,
-                           self.workspace, superset=self.superset, stream=stream)
+    def stage_repair(self, q, buf: int = 0, stream=None):
+        B.dsa_repair_merge(self.cache.kv, q, self.spec_bufs[buf], self.spec_counts[buf],
+                           self.partials, self.idx, self.count, self.scale, self.out, self.m,
+                           self.l, self.workspace, superset=self.superset, stream=stream)
 
-    def stage_ema(self, mode=B.DSA_EMA_UPDATE, stream=None):
-        self._ema(mode, stream)
+    def stage_ema(self, mode=B.DSA_EMA_UPDATE, buf: int = 1, stream=None):
+        B.dsa_ema_predict_update(self.scores, self.stride, self.ell, self.trend, mode, self.alpha,
+                                 self.beta, self.gamma, self.pred, self.k_pred,
+                                 self.spec_bufs[buf], self.spec_counts[buf], stream)
 
     def step(self, q):
         """One decode step with query q (bf16 [B][Hq][D]); returns (out, m, l)."""
         c = self.cache
         main = torch.cuda.current_stream(c.device)
+        cur, nxt = self.t % 2, (self.t + 1) % 2
         if self.t == 0:
-            self._score_select(q, main)
+            self.stage_score(q, main)
+            self.stage_select(main)
             B.dsa_sparse_decode_attn(c.kv, q, self.idx, self.count, self.scale, self.out, self.m,
                                      self.l, workspace=self.workspace, stream=main)
-            self._ema(B.DSA_EMA_INIT, main)
+            self.stage_ema(B.DSA_EMA_INIT, nxt, main)
+        elif self.side is None:
+            self.stage_score(q, main)
+            self.stage_select(main)
+            self.stage_ema(B.DSA_EMA_UPDATE, nxt, main)
+            self.stage_spec(q, cur, main)
+            self.stage_repair(q, cur, main)
         else:
-            spec_stream = self.side if self.side is not None else main
-            if self.side is not None:
-                self.side.wait_stream(main)
-            # speculative attention over P (predicted at the end of the previous step) ...
-            self.stage_spec(q, spec_stream)
-            # ... while the true scores and the true set A are computed
-            self._score_select(q, main)
-            if self.side is not None:
-                main.wait_stream(self.side)
-            self.stage_repair(q, main)
-            self._ema(B.DSA_EMA_UPDATE, main)
+            # speculative attention over P_t, concurrent with scoring and selection
+            self.side.wait_stream(main)
+            self.stage_spec(q, cur, self.side)
+            self.stage_score(q, main)
+            # the EMA needs only this step's scores: it runs beside selection and repair
+            self.ema_stream.wait_stream(main)
+            self.stage_ema(B.DSA_EMA_UPDATE, nxt, self.ema_stream)
+            self.stage_select(main)
+            main.wait_stream(self.side)
+            self.stage_repair(q, cur, main)
+            main.wait_stream(self.ema_stream)
         self.t += 1
         return self.out, self.m, self.l

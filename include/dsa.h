@@ -25,6 +25,8 @@
  *    (its tokens contribute nothing) and DSA_STATUS_BAD_PAGE is OR-ed into *status when
  *    kv->status is non-NULL.
  *  - Scores use -inf for "no page here"; selection only ever picks pages with a score > -inf.
+ *  - Alignment: the K/V pools, q (for the attention calls), metadata, partial records and
+ *    workspaces must be 16-byte aligned; a misaligned pointer returns DSA_ERR_ALIGNMENT.
  */
 #ifndef DSA_H_
 #define DSA_H_
