@@ -31,17 +31,15 @@ def _rows(w, sample):
     return [rows[i] for i in pick]
 
 
-_META_CACHE = {}
+_META_CACHE = {}   # oracle kmax/kmin per row of the workload being run; cleared per run
 
 
 def _minmax_scores(inp, b, h, lp, stride, q_group):
     """Oracle page scores of one row; the row's kmax/kmin (fixed across decode steps) is computed
     once per input set."""
     L = int(inp["seq_lens"][b])
-    key = (id(inp["k_pages"]), b, h, lp)
+    key = (b, h, lp)
     if key not in _META_CACHE:
-        if len(_META_CACHE) > 64:
-            _META_CACHE.clear()
         _META_CACHE[key] = row_meta_minmax(inp["k_pages"], inp["page_table"], L, b, h, lp)
     kmax, kmin = _META_CACHE[key]
     s = O.score_pages_minmax(O.representative_query(q_group), kmax, kmin)
@@ -49,6 +47,7 @@ def _minmax_scores(inp, b, h, lp, stride, q_group):
 
 
 def run_topk(w, inp, sample):
+    _META_CACHE.clear()
     cache = Cache.from_inputs(inp)
     dec = TopKDecoder(cache, w.k, w.logical_page)
     dec.build_meta()
@@ -76,6 +75,7 @@ def run_topk(w, inp, sample):
 
 
 def run_hier(w, inp, sample):
+    _META_CACHE.clear()
     cache = Cache.from_inputs(inp)
     dec = HierDecoder(cache, w.k, w.logical_page, w.sink, w.local, w.reuse)
     dec.build_meta()
@@ -109,6 +109,7 @@ def run_hier(w, inp, sample):
 
 
 def run_threshold(w, inp, sample):
+    _META_CACHE.clear()
     cache = Cache.from_inputs(inp)
     dec = ThresholdDecoder(cache, w.tau, w.cap)
     dec.build_meta()
@@ -144,6 +145,7 @@ def run_threshold(w, inp, sample):
 
 
 def run_prr(w, inp, sample, superset=False):
+    _META_CACHE.clear()
     cache = Cache.from_inputs(inp)
     dec = PRRDecoder(cache, w.k, w.k_pred, w.alpha, w.beta, w.gamma, superset=superset)
     dec.build_meta()
