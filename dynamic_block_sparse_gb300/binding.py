@@ -55,6 +55,8 @@ _SIGNATURES = {
     "dsa_sparse_decode_attn": ([_P, _P, _P, _I, _P, c_float, _P, _P, _P, _P, _I, _P, c_size_t,
                                 _P], _I),
     "dsa_sparse_decode_attn_workspace_size": ([_P, _I, _I], c_size_t),
+    "dsa_sparse_decode_attn_noalloc": ([_P, _P, _P, _I, _P, c_float, _P, _P, _P, _I, _P], _I),
+    "dsa_sparse_decode_attn_noalloc_max_bytes": ([], c_size_t),
     "dsa_repair_merge": ([_P, _P, _P, _I, _P, _P, _P, _I, _P, _I, c_float, _P, _P, _P, _P,
                           c_size_t, _P], _I),
     "dsa_repair_merge_workspace_size": ([_P, _I], c_size_t),
@@ -188,6 +190,19 @@ def dsa_sparse_decode_attn(kv: PagedKV, q, idx, count, scale: float, out=None, m
         ctypes.byref(kv), _ptr(q), _ptr(idx), idx.shape[-1], _ptr(count), scale, _ptr(out),
         _ptr(m), _ptr(l), _ptr(page_partials), num_splits, _ptr(workspace), ws_bytes,
         _stream(stream)))
+
+
+def dsa_sparse_decode_attn_noalloc(kv: PagedKV, q, idx, count, scale: float, out, m, l,
+                                   num_splits: int = 0, stream=None):
+    """dsa_sparse_decode_attn with the split records in the library's fixed device scratch (for
+    callers that must not allocate); calls must not overlap on the GPU."""
+    _check("dsa_sparse_decode_attn_noalloc", load().dsa_sparse_decode_attn_noalloc(
+        ctypes.byref(kv), _ptr(q), _ptr(idx), idx.shape[-1], _ptr(count), scale, _ptr(out),
+        _ptr(m), _ptr(l), num_splits, _stream(stream)))
+
+
+def dsa_sparse_decode_attn_noalloc_max_bytes() -> int:
+    return int(load().dsa_sparse_decode_attn_noalloc_max_bytes())
 
 
 def dsa_repair_merge_workspace_size(kv: PagedKV, true_stride: int) -> int:

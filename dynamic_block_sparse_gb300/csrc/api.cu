@@ -151,6 +151,40 @@ float scale_log2(float scale) { return scale * kLog2e; }
 
 }  // namespace
 
+// ---------------------------------------------------------------------------------------------
+// Fixed scratch for dsa_sparse_decode_attn_noalloc.  Some callers cannot call cudaMalloc: code
+// that runs inside a host framework which owns all device memory through its own allocator, and
+// latency-critical loops where the implicit device synchronisation of cudaMalloc/cudaFree is not
+// acceptable.  For them the split-K partial records live in this array, which every GPU that
+// loads the library holds until the process exits.
+constexpr size_t kNoAllocScratchBytes = size_t(4) << 20;  // 4 MiB
+static __device__ __align__(256) unsigned char g_noalloc_scratch[kNoAllocScratchBytes];
+
+namespace {
+
+// Device address of g_noalloc_scratch on the current device.  In host code the array's name is
+// only a host-side stand-in, so the address is looked up once per device (with that device
+// current) and cached.
+int noalloc_scratch(void** out) {
+  static std::mutex mu;
+  static void* addr[64] = {};
+  int dev = 0;
+  cudaError_t e = cudaGetDevice(&dev);
+  if (e != cudaSuccess) return cuda_fail(e, "cudaGetDevice");
+  if (dev < 0 || dev >= 64) return fail(DSA_ERR_UNSUPPORTED, "device ordinal %d >= 64", dev);
+  std::lock_guard<std::mutex> lock(mu);
+  if (!addr[dev]) {
+    void* p = nullptr;
+    e = cudaGetSymbolAddress(&p, g_noalloc_scratch);
+    if (e != cudaSuccess) return cuda_fail(e, "cudaGetSymbolAddress(scratch)");
+    addr[dev] = p;
+  }
+  *out = addr[dev];
+  return DSA_OK;
+}
+
+}  // namespace
+
 extern "C" {
 
 const char* dsa_last_error(void) { return g_err.c_str(); }
@@ -504,6 +538,72 @@ int dsa_merge_partials(const float* partials, int32_t rows, int32_t num_parts, i
   mg.out_rows_are_heads = 0;
   cudaError_t e = launch_merge(mg, static_cast<cudaStream_t>(stream));
   return e == cudaSuccess ? ok() : cuda_fail(e, "dsa_merge_partials launch");
+}
+
+size_t dsa_sparse_decode_attn_noalloc_max_bytes(void) { return kNoAllocScratchBytes; }
+
+int dsa_sparse_decode_attn_noalloc(const dsa_paged_kv* kv, const void* q, const int32_t* idx,
+                                   int32_t idx_stride, const int32_t* count, float scale,
+                                   float* out, float* m, float* l, int32_t num_splits,
+                                   dsa_stream_t stream) {
+  KvView v;
+  int rc = check_kv(kv, 2, &v);
+  if (rc) return rc;
+  if (!q || !idx || !count || !out || !m || !l)
+    return fail(DSA_ERR_INVALID_ARG, "q/idx/count/out/m/l is NULL");
+  if (idx_stride < 1) return fail(DSA_ERR_INVALID_ARG, "idx_stride < 1");
+  if (!aligned(q, 16)) return fail(DSA_ERR_ALIGNMENT, "q must be 16-byte aligned");
+  const int rows = v.B * v.Hkv;
+  const int splits = auto_splits(rows, idx_stride, num_splits);
+  const size_t need = splits > 1 ? record_bytes(rows, splits, v.G) : 0;
+  if (need > kNoAllocScratchBytes)
+    return fail(DSA_ERR_UNSUPPORTED,
+                "dsa_sparse_decode_attn_noalloc: %d rows x %d splits x %d heads need %zu bytes of "
+                "split records, more than its fixed %zu-byte scratch; pass fewer splits or use "
+                "dsa_sparse_decode_attn with a workspace",
+                rows, splits, v.G, need, kNoAllocScratchBytes);
+  void* scratch = nullptr;
+  if (need > 0 && (rc = noalloc_scratch(&scratch))) return rc;
+  CUtensorMap tk, tv;
+  if ((rc = pool_map(kv->k_pages, kv, &tk)) || (rc = pool_map(kv->v_pages, kv, &tv))) return rc;
+  cudaStream_t s = static_cast<cudaStream_t>(stream);
+  AttnArgs a = {};
+  a.kv = v;
+  a.q = static_cast<const __nv_bfloat16*>(q);
+  a.scale_log2 = scale_log2(scale);
+  a.idx = idx;
+  a.idx_stride = idx_stride;
+  a.count = count;
+  a.num_splits = splits;
+  a.stages = attn_stages(v.p, (idx_stride + splits - 1) / splits);
+  a.out = out;
+  a.m = m;
+  a.l = l;
+  // every split slot of every row is written before the merge reads it, so the scratch needs
+  // no clearing between calls
+  if (splits > 1) {
+    a.part = static_cast<float*>(scratch);
+    a.part_slots = splits;
+  }
+  cudaError_t e = launch_attn(LIST_SELECTED, tk, tv, a, splits, s);
+  if (e != cudaSuccess) return cuda_fail(e, "dsa_sparse_decode_attn_noalloc launch");
+  if (splits > 1) {
+    MergeArgs mg = {};
+    mg.part = static_cast<const float*>(scratch);
+    mg.slots = splits;
+    mg.rows = rows;
+    mg.G = v.G;
+    mg.Hkv = v.Hkv;
+    mg.Hq = v.Hq;
+    mg.streaming = v.streaming;
+    mg.out = out;
+    mg.m = m;
+    mg.l = l;
+    mg.out_rows_are_heads = 1;
+    e = launch_merge(mg, s);
+    if (e != cudaSuccess) return cuda_fail(e, "dsa_sparse_decode_attn_noalloc merge");
+  }
+  return ok();
 }
 
 }  // extern "C"

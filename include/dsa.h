@@ -191,6 +191,30 @@ size_t dsa_sparse_decode_attn_workspace_size(const dsa_paged_kv* kv, int32_t idx
                                              int32_t num_splits);
 
 /*
+ * dsa_sparse_decode_attn without a caller-provided workspace (none of the three source pages has
+ * a counterpart: this is a deployment convenience).  Some callers cannot call cudaMalloc: code
+ * running inside a host framework that owns all device memory through its own allocator, and
+ * latency-critical loops that cannot accept the device synchronisation cudaMalloc/cudaFree may
+ * imply.  This variant computes exactly what dsa_sparse_decode_attn computes (same kernels, same
+ * split choice for the same num_splits) but keeps the split-K partial records in a fixed 4 MiB
+ * device array inside the library, which every GPU that loads the library holds until exit.
+ *   - Allocates nothing; calls no cudaMalloc/cudaFree or allocating library routine.
+ *   - The first call on each device looks up the array's device address (cudaGetSymbolAddress,
+ *     with that device current) and caches it; make that first call before any stream capture.
+ *   - All calls share the one array: calls whose work overlaps on the GPU (e.g. on two streams)
+ *     race and corrupt each other's results; serialise them.  The array needs no clearing: every
+ *     record a call reads is written earlier in the same call.
+ *   - When rows * splits * G * 528 bytes exceeds the array (dsa_sparse_decode_attn_noalloc_
+ *     max_bytes()), the call returns DSA_ERR_UNSUPPORTED and enqueues nothing.
+ *   - out/m/l are required (no page_partials mode).
+ */
+int dsa_sparse_decode_attn_noalloc(const dsa_paged_kv* kv, const void* q, const int32_t* idx,
+                                   int32_t idx_stride, const int32_t* count, float scale,
+                                   float* out, float* m, float* l, int32_t num_splits,
+                                   dsa_stream_t stream);
+size_t dsa_sparse_decode_attn_noalloc_max_bytes(void);
+
+/*
  * PRR repair and merge ([PRR] §3.3 repair kernel and recurrence).  Given the speculative set P
  * (spec_idx/spec_count, ASCENDING and unique) whose per-page partials a previous
  * dsa_sparse_decode_attn wrote to page_partials (same idx_stride = spec_stride), and the true set
