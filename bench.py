@@ -48,6 +48,7 @@ def parse_args(argv=None):
     p.add_argument("--no-e2e", action="store_true")
     p.add_argument("--cpu-seconds", type=float, default=12.0)
     p.add_argument("--no-cpu-baseline", action="store_true")
+    p.add_argument("--no-rows", action="store_true", help="skip the per-row table")
     p.add_argument("--oracle-child", action="store_true", help=argparse.SUPPRESS)
     return p.parse_args(argv)
 
@@ -300,7 +301,25 @@ def bench_prr(args, w, dev, rank):
                  north_star_gbs=north_step / (mean_ms * 1e6),
                  byte_parts=parts,
                  step_ms_p50=statistics.median(step_ms), step_ms_min=min(step_ms))
-    return dict(mean_ms=mean_ms, bytes_step=bytes_step, clocks=clocks, dominant=dominant,
+    peak, _ = load_peaks()
+    hits = rows * w.k - sum(missed) / n
+    rep_bytes = (sum(missed) / n) * page_kv + hits * w.group * 528 + q_bytes
+    prr_rows = [
+        _entry("A2", w.name, "dsa_score_pages MINMAX", stage_ms["score_pages"],
+               stage_bytes["score_pages"], peak),
+        _entry("A3", w.name, "dsa_select_topk k=64 of 8192", stage_ms["select_topk"],
+               stage_bytes["select_topk"], peak),
+        _entry("A6", w.name, "dsa_sparse_decode_attn per-page records over P (speculative)",
+               stage_ms["spec_attn"], stage_bytes["spec_attn"], peak),
+        _entry("A9", w.name, "dsa_ema_predict_update + top-76", stage_ms["ema_predict"],
+               stage_bytes["ema_predict"], peak),
+        _entry("A10", w.name, "dsa_repair_merge (attention over A minus P, merge with the hits)",
+               stage_ms["repair_merge"], rep_bytes, peak),
+        _entry("step", w.name, "PRR decode step (graph, three streams)", mean_ms, bytes_step,
+               peak),
+    ]
+    return dict(rows=prr_rows, mean_ms=mean_ms, bytes_step=bytes_step, clocks=clocks,
+                dominant=dominant,
                 dominant_ms=stage_ms[dominant], dominant_bytes=stage_bytes[dominant], e2e=e2e,
                 launches_per_step=6, extra=extra)
 
@@ -338,6 +357,174 @@ def e2e_prr(args, w, dec, qs, flush, bytes_step):
     d2h = (dec.out.numel() + dec.m.numel() + dec.l.numel()) * 4
     return {"value": bytes_step / (ms * 1e6), "unit": "GB/s", "ms_per_step": ms,
             "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h}
+
+
+# ------------------------------------------------------------------------------------ rows
+
+def _graph(fn):
+    import torch
+
+    g = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(g):
+        fn()
+    return g
+
+
+def _time_graph(g, flush, n=30, warm=3):
+    """Mean device time (ms) of one replay, L2 flushed before each (outside the window)."""
+    import torch
+
+    stream = torch.cuda.current_stream()
+    for _ in range(warm):
+        g.replay()
+    torch.cuda.synchronize()
+    ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
+          for _ in range(n)]
+    for i, (s, e) in enumerate(ev):
+        flush.fill_(i & 0xFF)
+        s.record(stream)
+        g.replay()
+        e.record(stream)
+    torch.cuda.synchronize()
+    return statistics.mean(s.elapsed_time(e) for s, e in ev)
+
+
+def _entry(row, workload, op, ms, nbytes, peak, **kw):
+    gbs = nbytes / (ms * 1e6)
+    d = {"row": row, "workload": workload, "op": op, "us": round(ms * 1e3, 3),
+         "bytes": int(nbytes), "gbs": round(gbs, 1), "frac": round(gbs / peak, 4)}
+    d.update(kw)
+    return d
+
+
+def bench_rows(dev, flush, peak):
+    """Every hot-path row on the workload it belongs to: one library call captured as a graph and
+    replayed with L2 flushed before each replay.  Bytes are algorithmic (what the call must read
+    and write), from the counts the call actually produced."""
+    import torch
+
+    from dynamic_block_sparse_gb300 import binding as B
+    from dynamic_block_sparse_gb300.pipeline import (Cache, HierDecoder, ThresholdDecoder,
+                                                     TopKDecoder)
+    from dynamic_block_sparse_gb300.workloads import BY_NAME, make_inputs
+
+    out = []
+    KVP = 512  # K + V bytes per token per KV head
+
+    # ---- Llama-3-8B layer: kmax/kmin metadata, scores, top-256, sparse attention
+    w = BY_NAME["llama3_8b_layer"]
+    inp = make_inputs(w, dev, shuffle_pages=False)
+    cache = Cache.from_inputs(inp, dev)
+    dec = TopKDecoder(cache, w.k, w.logical_page)
+    q = inp["q"][0].clone()
+    rows, npg = w.batch * w.num_kv_heads, w.pages_per_seq
+    ms = _time_graph(_graph(dec.build_meta), flush)
+    out.append(_entry("A1", w.name, "dsa_build_page_meta MINMAX", ms,
+                      rows * npg * w.page_size * 256 + rows * npg * 512, peak))
+    dec.step(q)
+    torch.cuda.synchronize()
+    sel = int(dec.count.sum())
+    ms = _time_graph(_graph(lambda: B.dsa_score_pages(cache.kv, q, dec.meta, B.DSA_META_MINMAX,
+                                                      w.logical_page, dec.scores)), flush)
+    out.append(_entry("A2", w.name, "dsa_score_pages MINMAX", ms,
+                      rows * npg * 512 + q.numel() * 2 + rows * dec.stride * 4, peak))
+    ms = _time_graph(_graph(lambda: B.dsa_select_topk(dec.scores, dec.stride, w.k, dec.idx,
+                                                      dec.count)), flush)
+    out.append(_entry("A3", w.name, "dsa_select_topk k=256 of 2048", ms,
+                      rows * dec.stride * 4 + rows * w.k * 4, peak))
+    ms = _time_graph(_graph(lambda: dec.attend(q)), flush)
+    out.append(_entry("A6", w.name, "dsa_sparse_decode_attn (persistent split-K)", ms,
+                      sel * w.page_size * KVP + q.numel() * 2 + q.numel() * 4, peak, pages=sel))
+    ms = _time_graph(_graph(lambda: dec.step(q)), flush)
+    out.append(_entry("step", w.name, "score + top-K + attention", ms,
+                      rows * npg * 512 + sel * w.page_size * KVP + rows * dec.stride * 8, peak))
+    del dec, cache, inp
+    torch.cuda.empty_cache()
+
+    # ---- LServe hierarchical paging + streaming heads
+    w = BY_NAME["lserve_hier"]
+    inp = make_inputs(w, dev, shuffle_pages=False)
+    cache = Cache.from_inputs(inp, dev)
+    dec = HierDecoder(cache, w.k, w.logical_page, w.sink, w.local, w.reuse)
+    q = inp["q"][0].clone()
+    rows, npg = w.batch * w.num_kv_heads, w.pages_per_seq
+    dense = w.batch * (w.num_kv_heads - len(w.streaming_kv_heads))
+    stream_rows = rows - dense
+    ms = _time_graph(_graph(dec.build_meta), flush)
+    out.append(_entry("A1", w.name, "dsa_build_page_meta MINMAX (logical 16 in physical 64)", ms,
+                      rows * npg * w.page_size * 256 + rows * npg * w.g * 512, peak))
+    dec.step(q, 0)
+    torch.cuda.synchronize()
+    sel = int(dec.count.sum())
+    ms = _time_graph(_graph(lambda: B.dsa_score_pages(cache.kv, q, dec.meta, B.DSA_META_MINMAX,
+                                                      w.logical_page, dec.scores)), flush)
+    out.append(_entry("A2", w.name, "dsa_score_pages MINMAX logical pages (dense heads)", ms,
+                      dense * npg * w.g * 512 + q.numel() * 2 + rows * dec.stride * 4, peak))
+    ms = _time_graph(_graph(lambda: B.dsa_select_hier(dec.scores, dec.stride, w.g, w.k, dec.idx,
+                                                      dec.count)), flush)
+    out.append(_entry("A4", w.name, "dsa_select_hier g=4 k=64 of 2048", ms,
+                      rows * dec.stride * 4 + rows * w.k * 4, peak))
+    ms = _time_graph(_graph(lambda: B.dsa_sparse_decode_attn(
+        cache.kv, q, dec.idx, dec.count, dec.scale, dec.out, dec.m, dec.l,
+        workspace=dec.workspace)), flush)
+    out.append(_entry("A6", w.name, "dsa_sparse_decode_attn dense heads (persistent split-K)",
+                      ms, sel * w.page_size * KVP + q.numel() * 2, peak, pages=sel))
+    ms = _time_graph(_graph(lambda: B.dsa_streaming_head_attn(
+        cache.kv, q, w.sink, w.local, dec.scale, dec.out, dec.m, dec.l)), flush)
+    out.append(_entry("A7", w.name, "dsa_streaming_head_attn 64 sink + 256 local", ms,
+                      stream_rows * (w.sink + w.local) * KVP + q.numel(), peak))
+    ms0 = _time_graph(_graph(lambda: dec.step(q, 0)), flush)
+    out.append(_entry("step", w.name, "selection step (score + hier select + attention)", ms0,
+                      dense * npg * w.g * 512 + sel * w.page_size * KVP
+                      + stream_rows * (w.sink + w.local) * KVP, peak))
+    ms1 = _time_graph(_graph(lambda: dec.step(q, 1)), flush)
+    out.append(_entry("A8", w.name, "reuse step (attention with the reused selection)", ms1,
+                      sel * w.page_size * KVP + stream_rows * (w.sink + w.local) * KVP, peak))
+    del dec, cache, inp
+    torch.cuda.empty_cache()
+
+    # ---- PSA progressive threshold
+    w = BY_NAME["psa_threshold"]
+    inp = make_inputs(w, dev, shuffle_pages=False)
+    cache = Cache.from_inputs(inp, dev)
+    dec = ThresholdDecoder(cache, w.tau, w.cap)
+    q = inp["q"][0].clone()
+    rows, npg = w.batch * w.num_kv_heads, w.pages_per_seq
+    ms = _time_graph(_graph(dec.build_meta), flush)
+    out.append(_entry("A1", w.name, "dsa_build_page_meta MEAN", ms,
+                      rows * npg * w.page_size * 256 + rows * npg * 512, peak))
+    dec.step(q)
+    torch.cuda.synchronize()
+    visited = int(dec.count.sum())
+    ms = _time_graph(_graph(lambda: B.dsa_score_pages(cache.kv, q, dec.meta, B.DSA_META_MEAN,
+                                                      w.page_size, dec.scores)), flush)
+    out.append(_entry("A2", w.name, "dsa_score_pages MEAN", ms,
+                      rows * npg * 512 + q.numel() * 2 + rows * dec.stride * 4, peak))
+    ms = _time_graph(_graph(lambda: B.dsa_select_threshold(
+        cache.kv, q, dec.scores, w.tau, w.cap, dec.scale, dec.idx, dec.count, dec.out, dec.m,
+        dec.l)), flush)
+    out.append(_entry("A5", w.name, "dsa_select_threshold tau=0.95 (rank, attend, stop)", ms,
+                      rows * npg * 4 + visited * w.page_size * KVP + q.numel() * 6, peak,
+                      mean_blocks=round(visited / rows, 2)))
+    ms = _time_graph(_graph(lambda: dec.step(q)), flush)
+    out.append(_entry("step", w.name, "score + threshold selection", ms,
+                      rows * npg * 516 + visited * w.page_size * KVP, peak))
+    del dec, cache, inp
+    torch.cuda.empty_cache()
+
+    # ---- tiny top-K (the oracle-scale case)
+    w = BY_NAME["tiny_topk"]
+    inp = make_inputs(w, dev, shuffle_pages=False)
+    cache = Cache.from_inputs(inp, dev)
+    dec = TopKDecoder(cache, w.k, w.logical_page)
+    dec.build_meta()
+    q = inp["q"][0].clone()
+    ms = _time_graph(_graph(lambda: dec.step(q)), flush)
+    out.append(_entry("step", w.name, "score + top-32 + attention", ms,
+                      w.pages_per_seq * 512 + w.k * w.page_size * KVP, peak))
+    del dec, cache, inp
+    torch.cuda.empty_cache()
+    return out
 
 
 # ------------------------------------------------------------------------------------ oracle
@@ -499,6 +686,9 @@ def main():
     if res["e2e"] is not None:
         line["e2e"] = res["e2e"]
     line.update(res["extra"])
+    if not args.no_rows and world == 1:
+        flush = torch.empty(L2_FLUSH_BYTES, dtype=torch.uint8, device=dev)
+        line["rows"] = res["rows"] + bench_rows(dev, flush, peak)
     if rank == 0 and world == 1 and not args.no_cpu_baseline:
         line["cpu_baseline"] = cpu_baseline(args, w)
     if rank == 0:

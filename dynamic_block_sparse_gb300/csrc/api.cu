@@ -143,6 +143,25 @@ int repair_splits(int stride) {
   return s < 1 ? 1 : s;
 }
 
+// Upper bound on the chunks per row of the persistent split-K path (the kernel picks the count
+// from its grid and the number of dense rows): at least four pages per chunk, and few enough that
+// the row merge keeps [G][chunks] weights in shared memory.
+int stream_chunks(int stride) {
+  int c = (stride + 3) / 4;
+  if (c > 255) c = 255;
+  return c < 1 ? 1 : c;
+}
+
+size_t stream_records_bytes(int rows, int stride, int G) {
+  const size_t rec =
+      static_cast<size_t>(rows) * stream_chunks(stride) * G * kRecordFloats * sizeof(float);
+  return (rec + 255) & ~static_cast<size_t>(255);
+}
+
+size_t stream_workspace_bytes(int rows, int stride, int G) {
+  return stream_records_bytes(rows, stride, G) + static_cast<size_t>(rows) * sizeof(int32_t);
+}
+
 size_t record_bytes(int rows, int slots, int G) {
   return static_cast<size_t>(rows) * slots * G * kRecordFloats * sizeof(float);
 }
@@ -303,7 +322,10 @@ size_t dsa_sparse_decode_attn_workspace_size(const dsa_paged_kv* kv, int32_t idx
   const int rows = kv->batch * kv->num_kv_heads;
   const int G = kv->num_q_heads / kv->num_kv_heads;
   const int s = auto_splits(rows, idx_stride, num_splits);
-  return s > 1 ? record_bytes(rows, s, G) : 0;
+  const size_t classic = s > 1 ? record_bytes(rows, s, G) : 0;
+  if (num_splits > 0) return classic;
+  const size_t streamed = stream_workspace_bytes(rows, idx_stride, G);
+  return classic > streamed ? classic : streamed;
 }
 
 int dsa_sparse_decode_attn(const dsa_paged_kv* kv, const void* q, const int32_t* idx,
@@ -359,6 +381,36 @@ int dsa_sparse_decode_attn(const dsa_paged_kv* kv, const void* q, const int32_t*
       if (e != cudaSuccess) return cuda_fail(e, "dsa_sparse_decode_attn merge");
     }
     return ok();
+  }
+  // default: one persistent launch; the last unit of each row merges it
+  if (num_splits <= 0 && want_out && v.Hkv <= 1024) {
+    if (!aligned(out, 16)) return fail(DSA_ERR_ALIGNMENT, "out must be 16-byte aligned");
+    const size_t rec = stream_records_bytes(rows, idx_stride, v.G);
+    const size_t need = stream_workspace_bytes(rows, idx_stride, v.G);
+    if (!workspace || workspace_bytes < need)
+      return fail(DSA_ERR_WORKSPACE, "workspace of %zu bytes needed", need);
+    if (!aligned(workspace, 16)) return fail(DSA_ERR_ALIGNMENT, "workspace must be 16-byte aligned");
+    int stages = 131072 / (512 * v.p);
+    if (stages < 1) stages = 1;
+    if (stages > kStreamMaxStages) stages = kStreamMaxStages;
+    StreamAttnArgs sa = {};
+    sa.kv = v;
+    sa.q = a.q;
+    sa.scale_log2 = a.scale_log2;
+    sa.idx = idx;
+    sa.idx_stride = idx_stride;
+    sa.count = count;
+    sa.chunks = stream_chunks(idx_stride);
+    sa.stages = stages;
+    sa.part = static_cast<float*>(workspace);
+    sa.counters = reinterpret_cast<int32_t*>(static_cast<char*>(workspace) + rec);
+    sa.out = out;
+    sa.m = m;
+    sa.l = l;
+    e = cudaMemsetAsync(sa.counters, 0, static_cast<size_t>(rows) * sizeof(int32_t), s);
+    if (e != cudaSuccess) return cuda_fail(e, "dsa_sparse_decode_attn counter reset");
+    e = launch_stream_attn(tk, tv, sa, s);
+    return e == cudaSuccess ? ok() : cuda_fail(e, "dsa_sparse_decode_attn launch");
   }
   const int splits = auto_splits(rows, idx_stride, num_splits);
   const int per_cta = (idx_stride + splits - 1) / splits;

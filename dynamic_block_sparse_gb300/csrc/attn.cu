@@ -42,41 +42,6 @@ DSA_DEV bool token_in(const Window& w, int t) {
   return t < w.L && (t < w.sink_end || t >= w.local_begin);
 }
 
-DSA_DEV bool contains_sorted(const int32_t* a, int n, int x) {
-  int lo = 0, hi = n;
-  while (lo < hi) {
-    const int mid = (lo + hi) >> 1;
-    const int v = a[mid];
-    if (v == x) return true;
-    if (v < x) lo = mid + 1;
-    else hi = mid;
-  }
-  return false;
-}
-
-// Appends the valid candidates of one warp-wide round to the list, preserving order.
-DSA_DEV int append_round(bool ok, int phys, int pos, int2* list, int n) {
-  const int lane = threadIdx.x & 31;
-  const unsigned bal = __ballot_sync(0xffffffffu, ok);
-  if (ok) {
-    const int at = n + __popc(bal & ((1u << lane) - 1u));
-    if (at < kMaxListPages) list[at] = make_int2(phys, pos);
-  }
-  return n + __popc(bal);
-}
-
-// Page table lookup of position `pos` of request b, with range checks.
-DSA_DEV bool lookup_page(const KvView& kv, int b, int pos, int npos, int* phys) {
-  if (pos < 0 || pos >= npos) return false;
-  const int ph = kv.page_table[static_cast<size_t>(b) * kv.max_pages + pos];
-  if (ph < 0 || ph >= kv.num_phys) {
-    raise_status(kv.status, DSA_STATUS_BAD_PAGE);
-    return false;
-  }
-  *phys = ph;
-  return true;
-}
-
 template <int LIST>
 __global__ void __launch_bounds__(kAttnThreads)
     attn_pages_kernel(const __grid_constant__ CUtensorMap tmK,

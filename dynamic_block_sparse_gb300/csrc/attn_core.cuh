@@ -52,20 +52,28 @@ DSA_DEV void tile_scores(const uint32_t (&qa)[8][4], uint32_t kbase, int page, i
   const int lane = threadIdx.x & 31;
   const int mi = lane >> 3;
   const uint32_t tok = static_cast<uint32_t>(row0 + (mi >> 1) * 8 + (lane & 7));
+  // two independent accumulation chains per n-tile (even / odd k-steps) halve the mma latency
+  float acc[2][2][4];
 #pragma unroll
-  for (int nt = 0; nt < 2; ++nt)
+  for (int c = 0; c < 2; ++c)
 #pragma unroll
-    for (int e = 0; e < 4; ++e) sc[nt][e] = 0.f;
+    for (int nt = 0; nt < 2; ++nt)
+#pragma unroll
+      for (int e = 0; e < 4; ++e) acc[c][nt][e] = 0.f;
+  const uint32_t half_stride = static_cast<uint32_t>(page * 128);
 #pragma unroll
   for (int ks = 0; ks < 8; ++ks) {
     const uint32_t chunk = static_cast<uint32_t>(ks * 2 + (mi & 1));
-    const uint32_t addr = kbase + (chunk >> 3) * static_cast<uint32_t>(page * 128) +
-                          sw128(tok, chunk & 7u);
+    const uint32_t addr = kbase + (chunk >> 3) * half_stride + sw128(tok, chunk & 7u);
     uint32_t b0, b1, b2, b3;
     ldsm_x4(addr, b0, b1, b2, b3);
-    mma_bf16(sc[0], qa[ks], b0, b1);
-    mma_bf16(sc[1], qa[ks], b2, b3);
+    mma_bf16(acc[ks & 1][0], qa[ks], b0, b1);
+    mma_bf16(acc[ks & 1][1], qa[ks], b2, b3);
   }
+#pragma unroll
+  for (int nt = 0; nt < 2; ++nt)
+#pragma unroll
+    for (int e = 0; e < 4; ++e) sc[nt][e] = acc[0][nt][e] + acc[1][nt][e];
 }
 
 // Online-softmax update with the tile's logits (raw q.k in sc), then O += P . V_tile.
@@ -108,12 +116,15 @@ DSA_DEV void tile_softmax_pv(WarpSoftmaxState& st, float (&sc)[2][4], float scal
   st.l[1] = st.l[1] * alpha[1] + (p[0][2] + p[0][3] + p[1][2] + p[1][3]);
   st.m[0] = mnew[0];
   st.m[1] = mnew[1];
+  // once the running maxima settle the rescale is a no-op for the whole warp: skip it
+  if (!__all_sync(0xffffffffu, alpha[0] == 1.f && alpha[1] == 1.f)) {
 #pragma unroll
-  for (int j = 0; j < 16; ++j) {
-    st.o[j][0] *= alpha[0];
-    st.o[j][1] *= alpha[0];
-    st.o[j][2] *= alpha[1];
-    st.o[j][3] *= alpha[1];
+    for (int j = 0; j < 16; ++j) {
+      st.o[j][0] *= alpha[0];
+      st.o[j][1] *= alpha[0];
+      st.o[j][2] *= alpha[1];
+      st.o[j][3] *= alpha[1];
+    }
   }
   uint32_t pa[4];
   pa[0] = pack_bf16(p[0][0], p[0][1]);
@@ -179,6 +190,43 @@ DSA_DEV void state_store(const WarpSoftmaxState& st, float* sO, float* sM, float
     sL[r0] = st.l[0];
     sL[r0 + 8] = st.l[1];
   }
+}
+
+// ------------------------------------------------------------------------------- page lists
+
+DSA_DEV bool contains_sorted(const int32_t* a, int n, int x) {
+  int lo = 0, hi = n;
+  while (lo < hi) {
+    const int mid = (lo + hi) >> 1;
+    const int v = a[mid];
+    if (v == x) return true;
+    if (v < x) lo = mid + 1;
+    else hi = mid;
+  }
+  return false;
+}
+
+// Appends the valid candidates of one warp-wide round to the list, preserving order.
+DSA_DEV int append_round(bool ok, int phys, int pos, int2* list, int n) {
+  const int lane = threadIdx.x & 31;
+  const unsigned bal = __ballot_sync(0xffffffffu, ok);
+  if (ok) {
+    const int at = n + __popc(bal & ((1u << lane) - 1u));
+    if (at < kMaxListPages) list[at] = make_int2(phys, pos);
+  }
+  return n + __popc(bal);
+}
+
+// Page table lookup of position `pos` of request b, with range checks.
+DSA_DEV bool lookup_page(const KvView& kv, int b, int pos, int npos, int* phys) {
+  if (pos < 0 || pos >= npos) return false;
+  const int ph = kv.page_table[static_cast<size_t>(b) * kv.max_pages + pos];
+  if (ph < 0 || ph >= kv.num_phys) {
+    raise_status(kv.status, DSA_STATUS_BAD_PAGE);
+    return false;
+  }
+  *phys = ph;
+  return true;
 }
 
 }  // namespace dsa

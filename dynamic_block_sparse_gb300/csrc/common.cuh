@@ -97,6 +97,21 @@ DSA_DEV void tma_load_2d(uint32_t dst, const CUtensorMap* map, int c0, int c1, u
       : "memory");
 }
 
+// 1-D bulk copy global -> shared (both 16-byte aligned, bytes a multiple of 16), completing on
+// an mbarrier.
+DSA_DEV void bulk_load(uint32_t dst, const void* src, uint32_t bytes, uint32_t bar) {
+  asm volatile(
+      "cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1], %2, [%3];" ::"r"(
+          dst),
+      "l"(reinterpret_cast<uint64_t>(src)), "r"(bytes), "r"(bar)
+      : "memory");
+}
+
+// Named barrier over `count` threads (a multiple of 32) of the CTA.
+DSA_DEV void named_barrier(int id, int count) {
+  asm volatile("bar.sync %0, %1;" ::"r"(id), "r"(count) : "memory");
+}
+
 DSA_DEV void prefetch_tensormap(const CUtensorMap* map) {
   asm volatile("prefetch.tensormap [%0];" ::"l"(reinterpret_cast<uint64_t>(map)) : "memory");
 }

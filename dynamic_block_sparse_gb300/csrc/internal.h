@@ -96,6 +96,27 @@ struct MergeArgs {
 };
 cudaError_t launch_merge(const MergeArgs& a, cudaStream_t s);
 
+// Persistent split-K attention over (row, chunk) units with a last-ticket merge per row.
+struct StreamAttnArgs {
+  KvView kv;
+  const __nv_bfloat16* q;
+  float scale_log2;
+  const int32_t* idx;
+  int idx_stride;
+  const int32_t* count;
+  int chunks;         // upper bound on chunks per row (record stride); the kernel picks <= this
+  int stages;
+  float* part;        // [rows][chunks][G][kRecordFloats]
+  int32_t* counters;  // [rows], zero on entry
+  float* out;
+  float* m;
+  float* l;
+};
+constexpr int kStreamMaxStages = 16;
+size_t stream_attn_smem_bytes(int page, int stages);
+cudaError_t launch_stream_attn(const CUtensorMap& tmK, const CUtensorMap& tmV,
+                               const StreamAttnArgs& a, cudaStream_t s);
+
 // metadata and scoring
 cudaError_t launch_build_meta(const KvView& kv, const __nv_bfloat16* k_pages, int kind, int lp,
                               void* meta, cudaStream_t s);

@@ -25,8 +25,8 @@
  *    (its tokens contribute nothing) and DSA_STATUS_BAD_PAGE is OR-ed into *status when
  *    kv->status is non-NULL.
  *  - Scores use -inf for "no page here"; selection only ever picks pages with a score > -inf.
- *  - Alignment: the K/V pools, q (for the attention calls), metadata, partial records and
- *    workspaces must be 16-byte aligned; a misaligned pointer returns DSA_ERR_ALIGNMENT.
+ *  - Alignment: the K/V pools, q and out (for the attention calls), metadata, partial records
+ *    and workspaces must be 16-byte aligned; a misaligned pointer returns DSA_ERR_ALIGNMENT.
  */
 #ifndef DSA_H_
 #define DSA_H_
@@ -179,7 +179,10 @@ int dsa_select_threshold(const dsa_paged_kv* kv, const void* q, const float* sco
  *   page_partials: NULL, or fp32 [B][Hkv][idx_stride][G][D + 4]: for selected slot i the partial
  *                  record (O_0..O_{D-1}, m, l, 0, 0) of attention over that page alone (the
  *                  per-page partials PRR's exact repair merges).  Slots >= count are not written.
- *   num_splits   : pages of a row are spread over this many CTAs (0 = choose automatically).
+ *   num_splits   : 0 (default) = one persistent launch: every row's pages are cut into chunks,
+ *                  one per resident CTA, and the CTA finishing a row's last chunk merges the row;
+ *                  > 0 = the pages of a row are spread over exactly this many CTAs and merged
+ *                  by a second kernel.
  *   workspace    : device scratch of at least dsa_sparse_decode_attn_workspace_size() bytes,
  *                  16-byte aligned (may be NULL when that size is 0).
  */
