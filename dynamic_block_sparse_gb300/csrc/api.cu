@@ -56,18 +56,20 @@ PFN_cuTensorMapEncodeTiled_v12000 encode_fn() {
   return fn;
 }
 
-// 2-D view of a pool: rows = (phys_page, kv_head, slot), 128 bf16 per row; box = 64 dims x page
-// rows with 128-byte swizzle (one half of the head dimension of one page).
+// 3-D view of a pool: (64 dims, token rows, 2 halves) with strides 256 B per token row and 128 B
+// per half, so one box of (64, page, 2) with 128-byte swizzle stages a whole page of one KV head:
+// dims 0..63 of its rows, then dims 64..127 of its rows.
 int pool_map(const void* base, const dsa_paged_kv* kv, CUtensorMap* map) {
   auto fn = encode_fn();
   if (!fn) return fail(DSA_ERR_CUDA, "cuTensorMapEncodeTiled is not available from the driver");
-  cuuint64_t dims[2] = {static_cast<cuuint64_t>(kHeadDim),
+  cuuint64_t dims[3] = {64,
                         static_cast<cuuint64_t>(kv->num_phys_pages) * kv->num_kv_heads *
-                            kv->page_size};
-  cuuint64_t strides[1] = {static_cast<cuuint64_t>(kHeadDim) * 2};
-  cuuint32_t box[2] = {64, static_cast<cuuint32_t>(kv->page_size)};
-  cuuint32_t estr[2] = {1, 1};
-  CUresult r = fn(map, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, const_cast<void*>(base), dims, strides,
+                            kv->page_size,
+                        2};
+  cuuint64_t strides[2] = {static_cast<cuuint64_t>(kHeadDim) * 2, 128};
+  cuuint32_t box[3] = {64, static_cast<cuuint32_t>(kv->page_size), 2};
+  cuuint32_t estr[3] = {1, 1, 1};
+  CUresult r = fn(map, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, const_cast<void*>(base), dims, strides,
                   box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
                   CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
   if (r != CUDA_SUCCESS) return fail(DSA_ERR_CUDA, "cuTensorMapEncodeTiled failed (%d)", int(r));
@@ -143,23 +145,15 @@ int repair_splits(int stride) {
   return s < 1 ? 1 : s;
 }
 
-// Upper bound on the chunks per row of the persistent split-K path (the kernel picks the count
-// from its grid and the number of dense rows): at least four pages per chunk, and few enough that
-// the row merge keeps [G][chunks] weights in shared memory.
-int stream_chunks(int stride) {
-  int c = (stride + 3) / 4;
-  if (c > 255) c = 255;
-  return c < 1 ? 1 : c;
-}
-
-size_t stream_records_bytes(int rows, int stride, int G) {
-  const size_t rec =
-      static_cast<size_t>(rows) * stream_chunks(stride) * G * kRecordFloats * sizeof(float);
+// Workspace of the persistent split-K path: two partial records per CTA of its grid, then one
+// ticket counter per row.
+size_t stream_records_bytes(int grid, int G) {
+  const size_t rec = static_cast<size_t>(grid) * 2 * G * kRecordFloats * sizeof(float);
   return (rec + 255) & ~static_cast<size_t>(255);
 }
 
-size_t stream_workspace_bytes(int rows, int stride, int G) {
-  return stream_records_bytes(rows, stride, G) + static_cast<size_t>(rows) * sizeof(int32_t);
+size_t stream_workspace_bytes(int rows, int grid, int G) {
+  return stream_records_bytes(grid, G) + static_cast<size_t>(rows) * sizeof(int32_t);
 }
 
 size_t record_bytes(int rows, int slots, int G) {
@@ -324,7 +318,7 @@ size_t dsa_sparse_decode_attn_workspace_size(const dsa_paged_kv* kv, int32_t idx
   const int s = auto_splits(rows, idx_stride, num_splits);
   const size_t classic = s > 1 ? record_bytes(rows, s, G) : 0;
   if (num_splits > 0) return classic;
-  const size_t streamed = stream_workspace_bytes(rows, idx_stride, G);
+  const size_t streamed = stream_workspace_bytes(rows, stream_attn_grid(), G);
   return classic > streamed ? classic : streamed;
 }
 
@@ -385,8 +379,9 @@ int dsa_sparse_decode_attn(const dsa_paged_kv* kv, const void* q, const int32_t*
   // default: one persistent launch; the last unit of each row merges it
   if (num_splits <= 0 && want_out && v.Hkv <= 1024) {
     if (!aligned(out, 16)) return fail(DSA_ERR_ALIGNMENT, "out must be 16-byte aligned");
-    const size_t rec = stream_records_bytes(rows, idx_stride, v.G);
-    const size_t need = stream_workspace_bytes(rows, idx_stride, v.G);
+    const int grid = stream_attn_grid();
+    const size_t rec = stream_records_bytes(grid, v.G);
+    const size_t need = stream_workspace_bytes(rows, grid, v.G);
     if (!workspace || workspace_bytes < need)
       return fail(DSA_ERR_WORKSPACE, "workspace of %zu bytes needed", need);
     if (!aligned(workspace, 16)) return fail(DSA_ERR_ALIGNMENT, "workspace must be 16-byte aligned");
@@ -400,7 +395,6 @@ int dsa_sparse_decode_attn(const dsa_paged_kv* kv, const void* q, const int32_t*
     sa.idx = idx;
     sa.idx_stride = idx_stride;
     sa.count = count;
-    sa.chunks = stream_chunks(idx_stride);
     sa.stages = stages;
     sa.part = static_cast<float*>(workspace);
     sa.counters = reinterpret_cast<int32_t*>(static_cast<char*>(workspace) + rec);
@@ -409,7 +403,7 @@ int dsa_sparse_decode_attn(const dsa_paged_kv* kv, const void* q, const int32_t*
     sa.l = l;
     e = cudaMemsetAsync(sa.counters, 0, static_cast<size_t>(rows) * sizeof(int32_t), s);
     if (e != cudaSuccess) return cuda_fail(e, "dsa_sparse_decode_attn counter reset");
-    e = launch_stream_attn(tk, tv, sa, s);
+    e = launch_stream_attn(tk, tv, sa, grid, s);
     return e == cudaSuccess ? ok() : cuda_fail(e, "dsa_sparse_decode_attn launch");
   }
   const int splits = auto_splits(rows, idx_stride, num_splits);

@@ -31,17 +31,17 @@ DSA_DEV void state_init(WarpSoftmaxState& st) {
   st.l[0] = st.l[1] = 0.f;
 }
 
-// A-operand fragments of the staged query tile (sQ: 16 rows x kQStride bf16).
-DSA_DEV void load_q_frags(const __nv_bfloat16* sQ, uint32_t (&qa)[8][4]) {
+// A-operand fragments of the staged query tile (sQ: 16 rows of `stride` bf16).
+DSA_DEV void load_q_frags(const __nv_bfloat16* sQ, uint32_t (&qa)[8][4], int stride = kQStride) {
   const int lane = threadIdx.x & 31;
   const int r0 = lane >> 2, c0 = (lane & 3) * 2;
 #pragma unroll
   for (int ks = 0; ks < 8; ++ks) {
     const int c = ks * 16 + c0;
-    qa[ks][0] = *reinterpret_cast<const uint32_t*>(sQ + r0 * kQStride + c);
-    qa[ks][1] = *reinterpret_cast<const uint32_t*>(sQ + (r0 + 8) * kQStride + c);
-    qa[ks][2] = *reinterpret_cast<const uint32_t*>(sQ + r0 * kQStride + c + 8);
-    qa[ks][3] = *reinterpret_cast<const uint32_t*>(sQ + (r0 + 8) * kQStride + c + 8);
+    qa[ks][0] = *reinterpret_cast<const uint32_t*>(sQ + r0 * stride + c);
+    qa[ks][1] = *reinterpret_cast<const uint32_t*>(sQ + (r0 + 8) * stride + c);
+    qa[ks][2] = *reinterpret_cast<const uint32_t*>(sQ + r0 * stride + c + 8);
+    qa[ks][3] = *reinterpret_cast<const uint32_t*>(sQ + (r0 + 8) * stride + c + 8);
   }
 }
 

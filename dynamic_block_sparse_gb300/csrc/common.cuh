@@ -87,13 +87,15 @@ DSA_DEV bool mbar_wait(uint32_t bar, uint32_t parity, volatile int* abort, int32
 
 // ------------------------------------------------------------------------------- TMA
 
-// 2-D tiled bulk tensor load global -> shared, completing on an mbarrier (complete_tx::bytes).
-// c0 is the innermost coordinate in elements (must be a multiple of 16 bytes), c1 the row.
-DSA_DEV void tma_load_2d(uint32_t dst, const CUtensorMap* map, int c0, int c1, uint32_t bar) {
+// One KV page (both 64-dim halves of `page` token rows) global -> shared with one 3-D tiled
+// bulk tensor load completing on an mbarrier (complete_tx::bytes).  The pool's tensor map views it
+// as (64 dims, token rows, 2 halves) with box (64, page, 2) and 128-byte swizzle, so the page
+// lands as dims 0..63 of every row followed by dims 64..127 of every row, each line 128 bytes.
+DSA_DEV void tma_load_page(uint32_t dst, const CUtensorMap* map, int row0, uint32_t bar) {
   asm volatile(
-      "cp.async.bulk.tensor.2d.shared::cluster.global.tile.mbarrier::complete_tx::bytes"
-      " [%0], [%1, {%2, %3}], [%4];" ::"r"(dst),
-      "l"(reinterpret_cast<uint64_t>(map)), "r"(c0), "r"(c1), "r"(bar)
+      "cp.async.bulk.tensor.3d.shared::cluster.global.tile.mbarrier::complete_tx::bytes"
+      " [%0], [%1, {%2, %3, %4}], [%5];" ::"r"(dst),
+      "l"(reinterpret_cast<uint64_t>(map)), "r"(0), "r"(row0), "r"(0), "r"(bar)
       : "memory");
 }
 

@@ -96,7 +96,8 @@ struct MergeArgs {
 };
 cudaError_t launch_merge(const MergeArgs& a, cudaStream_t s);
 
-// Persistent split-K attention over (row, chunk) units with a last-ticket merge per row.
+// Persistent split-K attention: CTAs take equal ranges of the global page-slot space; rows cut
+// across CTAs are merged by the CTA that takes the row's last ticket.
 struct StreamAttnArgs {
   KvView kv;
   const __nv_bfloat16* q;
@@ -104,18 +105,19 @@ struct StreamAttnArgs {
   const int32_t* idx;
   int idx_stride;
   const int32_t* count;
-  int chunks;         // upper bound on chunks per row (record stride); the kernel picks <= this
   int stages;
-  float* part;        // [rows][chunks][G][kRecordFloats]
-  int32_t* counters;  // [rows], zero on entry
+  float* part;        // [grid][2][G][kRecordFloats]: each CTA's first-row and last-row records
+  int32_t* counters;  // [rows], zero on entry; left zero
   float* out;
   float* m;
   float* l;
 };
 constexpr int kStreamMaxStages = 16;
-size_t stream_attn_smem_bytes(int page, int stages);
+constexpr int kStreamMaxGrid = 512;  // bounds the row merge's [G][parts] weights in shared memory
+size_t stream_attn_smem_bytes(int page, int stages, int G);
+int stream_attn_grid();  // CTAs of one launch: one per SM
 cudaError_t launch_stream_attn(const CUtensorMap& tmK, const CUtensorMap& tmV,
-                               const StreamAttnArgs& a, cudaStream_t s);
+                               const StreamAttnArgs& a, int grid, cudaStream_t s);
 
 // metadata and scoring
 cudaError_t launch_build_meta(const KvView& kv, const __nv_bfloat16* k_pages, int kind, int lp,

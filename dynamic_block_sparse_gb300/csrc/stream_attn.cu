@@ -1,14 +1,21 @@
 // Persistent split-K sparse attention over many rows: one launch, one CTA per SM.
 //
-// Every dense (request, KV head) row's selected pages are cut into the same number of chunks, as
-// many as keep one (row, chunk) unit per CTA of the grid.  In each CTA warp 8 is a TMA producer:
-// it resolves the unit's page-table entries 32 at a time and streams the K/V pages through a
-// 128 KB ring, publishing each stage's page position in shared memory; warps 0..7 attend with the
-// mma core (eight consumer warps per SM keep enough 16-token tiles in flight to cover the mma
-// latency).  At the end of a unit the consumers merge their states, write the unit's partial
-// record (O, m, l per query head) to the workspace and take a ticket on the row's counter; the CTA
-// that takes the last ticket merges the row's records in chunk order (deterministic) and writes
-// the final rows.
+// Work partition (stream-K over page slots): every dense (request, KV head) row owns idx_stride
+// consecutive slots of one global slot space; CTA c of the n active CTAs takes the slots
+// [floor(c T / n), floor((c + 1) T / n)) of the T slots, so every CTA streams the same number of
+// selected pages whatever the number of rows.  The slots of one row inside one CTA form a unit.
+// A row that lies inside one CTA is finished by that CTA directly; a row cut across CTAs leaves
+// one partial record per CTA (at most two per CTA: its first and its last row), and the CTA that
+// takes the row's last ticket merges them in CTA order.  No CTA ever waits for another.
+//
+// Inside a CTA, warp 8 is a TMA producer: it resolves 32 page-table entries at a time and streams
+// whole K/V pages (one 3-D tensor load per pool) through a ring of about 128 KB, several lanes
+// issuing at once.  Warps 0..7 attend with the mma core.  Every (stage, 16-token tile) slot of the
+// ring belongs to one consumer warp for the whole launch, so a warp waits only for the pages it
+// computes on and each stage is released by exactly the warps that read it.  The producer also
+// publishes each unit (its row, selected slots and request length, and the row's G query vectors
+// by a 1-D bulk copy) through a two-slot mailbox, so the consumers never touch global memory
+// before their epilogues.
 #include "attn_core.cuh"
 #include "internal.h"
 
@@ -18,21 +25,49 @@ namespace {
 constexpr int kSW = 8;                     // consumer warps
 constexpr int kSThreads = (kSW + 1) * 32;  // + one TMA producer warp
 constexpr int kSConsumers = kSW * 32;
-constexpr uint32_t kSMergeBytes = kSW * (16 * 128 + 32) * 4;
 constexpr int kSMaxHeads = 1024;           // KV heads the dense-head table can hold
+constexpr int kIssueLanes = 4;             // producer lanes issuing page loads at once
 
 struct SLayout {
   uint32_t merge_off, q_off, bar_off, misc_off, total;
 };
 
-__host__ __device__ inline SLayout slayout(int page, int stages) {
+// merge area: per warp G rows of O (fp32) and G (m, l) pairs; later the row merge's weights.
+// q: two unpadded [16][128] bf16 query tiles (mailbox slots).  bars: [S] full, [S] empty, then the
+// mailbox's [2] full and [2] empty.
+__host__ __device__ inline SLayout slayout(int page, int stages, int G) {
   SLayout L;
   L.merge_off = ((512u * page * stages) + 1023u) & ~1023u;
-  L.q_off = L.merge_off + kSMergeBytes;
-  L.bar_off = L.q_off + 16u * kQStride * 2u;
-  L.misc_off = L.bar_off + 16u * static_cast<uint32_t>(stages);
+  L.q_off = L.merge_off + static_cast<uint32_t>(kSW * G * (kHeadDim + 2) * 4 + 127) / 128 * 128;
+  L.bar_off = L.q_off + 2u * 16u * kHeadDim * 2u;
+  L.misc_off = L.bar_off + 16u * static_cast<uint32_t>(stages) + 32u;
   L.total = L.misc_off + 256u + 4u * kSMaxHeads + 1024u;
   return L;
+}
+
+// Slot range [beg, end) of the active CTA c among n over T slots.
+__device__ __forceinline__ long long slot_start(long long c, long long T, long long n) {
+  return c * T / n;
+}
+
+// Index of the active CTA whose slot range holds slot x.
+__device__ __forceinline__ int slot_owner(long long x, long long T, long long n) {
+  return static_cast<int>(((x + 1) * n - 1) / T);
+}
+
+DSA_DEV bool mbar_wait_drain(uint32_t bar, uint32_t parity) {
+  const unsigned long long t0 = global_timer_ns();
+  while (!mbar_try_wait(bar, parity))
+    if (global_timer_ns() - t0 > 50000000ull) return false;
+  return true;
+}
+
+// acq_rel fetch-add at GPU scope: publishes this CTA's records (ordered before it by the CTA
+// barrier) and, for the last arrival, makes the other CTAs' records visible.
+DSA_DEV int ticket_add(int32_t* p) {
+  int old;
+  asm volatile("atom.acq_rel.gpu.global.add.s32 %0, [%1], 1;" : "=r"(old) : "l"(p) : "memory");
+  return old;
 }
 
 __global__ void __launch_bounds__(kSThreads, 1)
@@ -45,15 +80,21 @@ __global__ void __launch_bounds__(kSThreads, 1)
   const int page = kv.p;
   const int S = a.stages;
   const int G = kv.G;
-  const SLayout lay = slayout(page, S);
-  float* sO = reinterpret_cast<float*>(smem + lay.merge_off);
-  float* sM = sO + kSW * 2048;
-  float* sL = sM + kSW * 16;
-  __nv_bfloat16* sQ = reinterpret_cast<__nv_bfloat16*>(smem + lay.q_off);
-  uint64_t* bars = reinterpret_cast<uint64_t*>(smem + lay.bar_off);  // [S] full, [S] empty
+  const int tiles = page / 16;
+  const SLayout lay = slayout(page, S, G);
+  float* sO = reinterpret_cast<float*>(smem + lay.merge_off);  // [kSW][G][128]
+  float* sM = sO + kSW * G * kHeadDim;                          // [kSW][G]
+  float* sL = sM + kSW * G;                                     // [kSW][G]
+  __nv_bfloat16* sQ = reinterpret_cast<__nv_bfloat16*>(smem + lay.q_off);  // [2][16][128]
+  uint64_t* bars = reinterpret_cast<uint64_t*>(smem + lay.bar_off);
+  uint64_t* qbars = bars + 2 * S;  // mailbox: [2] full, [2] empty
   int* misc = reinterpret_cast<int*>(smem + lay.misc_off);
   volatile int* abort_flag = misc;          // [0]
-  volatile int* last_flag = misc + 1;       // [1]
+  volatile int* last_flag = misc + 1;       // [1], [2]: ticket outcomes of the cut rows
+  volatile int* issued = misc + 3;          // [3] ring positions the producer has issued
+  volatile int* producer_done = misc + 4;   // [4]
+  int* n_dense_heads = misc + 5;            // [5]
+  int* desc = misc + 8;                     // [8, 16): mailbox [2][row, beg, end, len]
   volatile int* stage_ok = misc + 16;       // [16, 32): did the producer load this stage
   volatile int* stage_pos = misc + 32;      // [32, 48): page position held by this stage
   int* dense_heads = misc + 64;             // [64, 64 + Hkv)
@@ -61,73 +102,196 @@ __global__ void __launch_bounds__(kSThreads, 1)
   const uint32_t stage_bytes = 512u * page;
   const uint32_t smem_base = smem_u32(smem);
 
-  if (tid == 0) {
-    for (int s = 0; s < S; ++s) {
-      mbar_init(smem_u32(&bars[s]), 1);
-      mbar_init(smem_u32(&bars[S + s]), kSW);
+  if (warp == 0) {
+    if (lane == 0) {
+      for (int s = 0; s < S; ++s) {
+        mbar_init(smem_u32(&bars[s]), 1);
+        mbar_init(smem_u32(&bars[S + s]), tiles);  // one arrival per 16-token tile of the page
+      }
+      for (int k = 0; k < 2; ++k) {
+        mbar_init(smem_u32(&qbars[k]), 1);
+        mbar_init(smem_u32(&qbars[2 + k]), kSW);
+      }
+      fence_mbar_init();
+      misc[0] = 0;
+      misc[3] = 0;
+      misc[4] = 0;
     }
-    fence_mbar_init();
-    misc[0] = 0;
+    // dense (non-streaming) KV heads in ascending order, 32 heads per ballot
     int nd = 0;
-    for (int hh = 0; hh < kv.Hkv; ++hh)
-      if (kv.streaming == nullptr || kv.streaming[hh] == 0) dense_heads[nd++] = hh;
-    misc[2] = nd;
+    for (int h0 = 0; h0 < kv.Hkv; h0 += 32) {
+      const int hh = h0 + lane;
+      const bool dense = hh < kv.Hkv && (kv.streaming == nullptr || kv.streaming[hh] == 0);
+      const unsigned bal = __ballot_sync(0xffffffffu, dense);
+      if (dense) dense_heads[nd + __popc(bal & ((1u << lane) - 1u))] = hh;
+      nd += __popc(bal);
+    }
+    if (lane == 0) *n_dense_heads = nd;
+  } else if (warp < kSW) {
+    // query rows G..15 of both mailbox tiles stay zero (the bulk copies write rows < G only)
+    for (int e = tid - 32; e < 2 * 16 * 16; e += kSConsumers - 32) {
+      const int r = (e >> 4) & 15;
+      if (r >= G) reinterpret_cast<uint4*>(sQ)[e] = make_uint4(0, 0, 0, 0);
+    }
   }
   __syncthreads();
-  const int nd_heads = misc[2];
-  const int n_dense = kv.B * nd_heads;
-  int chunks = n_dense > 0 ? static_cast<int>(gridDim.x) / n_dense : 1;
-  chunks = max(1, min(chunks, a.chunks));
-  const int chunk_pages = (a.idx_stride + chunks - 1) / chunks;
-  const int units_total = n_dense * chunks;
-
-  // unit u -> (row, selected slots [beg, end))
-  auto unit_range = [&](int u, int* row, int* beg, int* end) {
-    const int di = u / chunks;
-    const int c = u - di * chunks;
-    *row = (di / nd_heads) * kv.Hkv + dense_heads[di % nd_heads];
-    const int cnt = min(max(a.count[*row], 0), a.idx_stride);
-    *beg = min(cnt, c * chunk_pages);
-    *end = min(cnt, *beg + chunk_pages);
-  };
+  const int nd_heads = *n_dense_heads;
+  const int stride = a.idx_stride;
+  const long long T = static_cast<long long>(kv.B) * nd_heads * stride;
+  // active CTAs: at most one per slot, so that every active CTA holds at least one slot
+  const long long n_act = T < static_cast<long long>(gridDim.x) ? T : gridDim.x;
+  if (static_cast<long long>(blockIdx.x) >= n_act) return;
+  const long long my_beg = slot_start(blockIdx.x, T, n_act);
+  const long long my_end = slot_start(blockIdx.x + 1, T, n_act);
+  const int d_first = static_cast<int>(my_beg / stride);
+  const int n_units = static_cast<int>((my_end - 1) / stride) - d_first + 1;
 
   if (warp == kSW) {
-    // ---- producer
+    // ---- producer.  Unit u of this CTA is dense row d_first + u; lane l holds the descriptor of
+    // unit ub + l of the current batch of 32.  Chunks of up to 32 selected slots of one unit are
+    // software-pipelined: while chunk A's pages are issued, the page-table entries of chunk B and
+    // the selections of chunk C are already in flight.
     if (lane == 0) {
       prefetch_tensormap(&tmK);
       prefetch_tensormap(&tmV);
     }
-    int i = 0;  // ring position
-    for (int u = blockIdx.x; u < units_total && !*abort_flag; u += gridDim.x) {
-      int row, beg, end;
-      unit_range(u, &row, &beg, &end);
-      const int b = row / kv.Hkv, h = row % kv.Hkv;
-      const int npos = (request_len(kv, b) + page - 1) / page;
-      const int32_t* sel = a.idx + static_cast<size_t>(row) * a.idx_stride;
-      bool stopped = false;
-      for (int base = beg; base < end && !stopped; base += 32) {
-        const int j = base + lane;
-        int pos = -1, phys = 0;
-        bool ok = false;
-        if (j < end) {
-          pos = sel[j];
-          ok = lookup_page(kv, b, pos, npos, &phys);
+    const int NL = min(kIssueLanes, S);  // a group of NL pages uses NL distinct stages
+    int i = 0;                           // ring position
+    bool stopped = false;
+    // Selections of the first unit's first two chunks, loaded before its count is known (any slot
+    // below idx_stride is a valid address): they are used if the count leaves them selected.
+    const int spec_base = static_cast<int>(my_beg - static_cast<long long>(d_first) * stride);
+    int spec_a = -1, spec_b = -1;
+    {
+      const int row0 = (d_first / nd_heads) * kv.Hkv + dense_heads[d_first % nd_heads];
+      const int cap_end = static_cast<int>(
+          (my_end < static_cast<long long>(d_first + 1) * stride ? my_end
+                                                                 : static_cast<long long>(d_first + 1) * stride) -
+          static_cast<long long>(d_first) * stride);
+      const int32_t* sel0 = a.idx + static_cast<size_t>(row0) * stride;
+      if (spec_base + lane < cap_end) spec_a = sel0[spec_base + lane];
+      if (spec_base + 32 + lane < cap_end) spec_b = sel0[spec_base + 32 + lane];
+    }
+    for (int ub = 0; ub < n_units && !stopped; ub += 32) {
+      int t_row = 0, t_beg = 0, t_end = 0, t_len = 0;
+      {
+        const int u = ub + lane;
+        if (u < n_units) {
+          const int di = d_first + u;
+          t_row = (di / nd_heads) * kv.Hkv + dense_heads[di % nd_heads];
+          const long long r0 = static_cast<long long>(di) * stride;
+          const int pb = static_cast<int>((my_beg > r0 ? my_beg : r0) - r0);
+          const int pe = static_cast<int>((my_end < r0 + stride ? my_end : r0 + stride) - r0);
+          const int cnt = min(max(a.count[t_row], 0), stride);
+          t_beg = min(pb, cnt);
+          t_end = min(pe, cnt);
+          t_len = request_len(kv, t_row / kv.Hkv);
         }
-        const int nb = min(32, end - base);
-        for (int k = 0; k < nb; ++k, ++i) {
-          const int pk = __shfl_sync(0xffffffffu, pos, k);
-          const int phk = __shfl_sync(0xffffffffu, phys, k);
-          const int okk = __shfl_sync(0xffffffffu, ok ? 1 : 0, k);
-          const int s = i % S, uu = i / S;
+      }
+      const int ue = min(n_units, ub + 32);
+      int uq = ub;  // next unit to publish
+      // publishes unit u: waits for its mailbox slot, writes the descriptor, copies the queries
+      auto publish = [&](int u) -> bool {
+        const int slot = u & 1;
+        int stop = 0;
+        if (lane == 0 && u >= 2 &&
+            !mbar_wait(smem_u32(&qbars[2 + slot]), ((u >> 1) - 1) & 1, abort_flag, kv.status))
+          stop = 1;
+        const int row = __shfl_sync(0xffffffffu, t_row, u - ub);
+        const int beg = __shfl_sync(0xffffffffu, t_beg, u - ub);
+        const int end = __shfl_sync(0xffffffffu, t_end, u - ub);
+        const int len = __shfl_sync(0xffffffffu, t_len, u - ub);
+        if (__shfl_sync(0xffffffffu, stop, 0)) return false;
+        if (lane == 0) {
+          desc[slot * 4 + 0] = row;
+          desc[slot * 4 + 1] = beg;
+          desc[slot * 4 + 2] = end;
+          desc[slot * 4 + 3] = len;
+          const uint32_t full = smem_u32(&qbars[slot]);
+          const int b = row / kv.Hkv, h = row % kv.Hkv;
+          mbar_arrive_expect_tx(full, static_cast<uint32_t>(G) * kHeadDim * 2);
+          bulk_load(smem_u32(sQ + slot * 16 * kHeadDim),
+                    a.q + (static_cast<size_t>(b) * kv.Hq + static_cast<size_t>(h) * G) * kHeadDim,
+                    static_cast<uint32_t>(G) * kHeadDim * 2, full);
+        }
+        return true;
+      };
+      // first chunk at or after slot `base` of unit u (u == ue: none left in this batch)
+      auto seek = [&](int u, int base, int* cu, int* cb) {
+        while (u < ue) {
+          const int e = __shfl_sync(0xffffffffu, t_end, u - ub);
+          if (base < e) break;
+          ++u;
+          if (u < ue) base = __shfl_sync(0xffffffffu, t_beg, u - ub);
+        }
+        *cu = u;
+        *cb = base;
+      };
+      // lane's selected position in chunk (u, base), -1 past the unit's end
+      auto load_sel = [&](int u, int base) -> int {
+        if (u >= ue) return -1;
+        const int row = __shfl_sync(0xffffffffu, t_row, u - ub);
+        const int e = __shfl_sync(0xffffffffu, t_end, u - ub);
+        const int j = base + lane;
+        return j < e ? a.idx[static_cast<size_t>(row) * stride + j] : -1;
+      };
+      // raw page-table entry of a position inside the request, -1 outside
+      auto load_phys = [&](int u, int pos) -> int {
+        if (u >= ue) return -1;
+        const int row = __shfl_sync(0xffffffffu, t_row, u - ub);
+        const int len = __shfl_sync(0xffffffffu, t_len, u - ub);
+        const int b = row / kv.Hkv;
+        const int npos = (len + page - 1) / page;
+        return pos >= 0 && pos < npos ? kv.page_table[static_cast<size_t>(b) * kv.max_pages + pos]
+                                      : -1;
+      };
+      int ua, ba, ubb, bb, uc, bc;
+      seek(ub, __shfl_sync(0xffffffffu, t_beg, 0), &ua, &ba);
+      seek(ua, ba + 32, &ubb, &bb);
+      int pos_a, pos_b;
+      if (ub == 0 && ua == 0 && ba == spec_base) {
+        // the speculative loads were the right ones; drop what lies past the unit's end
+        const int e = __shfl_sync(0xffffffffu, t_end, 0);
+        pos_a = ba + lane < e ? spec_a : -1;
+        pos_b = (ubb == 0 && bb == spec_base + 32) ? (bb + lane < e ? spec_b : -1)
+                                                   : load_sel(ubb, bb);
+      } else {
+        pos_a = load_sel(ua, ba);
+        pos_b = load_sel(ubb, bb);
+      }
+      for (; uq <= ua && uq < ue && !stopped; ++uq) stopped = !publish(uq);
+      int raw_a = load_phys(ua, pos_a);
+      while (ua < ue && !stopped) {
+        seek(ubb, bb + 32, &uc, &bc);
+        const int pos_c = load_sel(uc, bc);
+        const int raw_b = load_phys(ubb, pos_b);
+        for (; uq <= ua && uq < ue && !stopped; ++uq) stopped = !publish(uq);
+        if (stopped) break;
+        // issue chunk A
+        const int row = __shfl_sync(0xffffffffu, t_row, ua - ub);
+        const int e = __shfl_sync(0xffffffffu, t_end, ua - ub);
+        const int h = row % kv.Hkv;
+        const int nb = min(32, e - ba);
+        const bool in_range = pos_a >= 0 && raw_a >= 0;  // position inside the request
+        const bool ok = in_range && raw_a < kv.num_phys;
+        if (in_range && !ok) raise_status(kv.status, DSA_STATUS_BAD_PAGE);
+        for (int q0 = 0; q0 < nb; q0 += NL) {
+          const int src = min(31, q0 + (lane < NL ? lane : 0));
+          const int pk = __shfl_sync(0xffffffffu, pos_a, src);
+          const int phk = __shfl_sync(0xffffffffu, raw_a, src);
+          const int okk = __shfl_sync(0xffffffffu, ok ? 1 : 0, src);
+          const bool active = lane < NL && q0 + lane < nb;
+          const int ii = i + q0 + lane;
+          const int s = ii % S, uu = ii / S;
           int stop = 0;
-          if (lane == 0 && uu > 0 &&
+          if (active && uu > 0 &&
               !mbar_wait(smem_u32(&bars[S + s]), (uu - 1) & 1, abort_flag, kv.status))
             stop = 1;
-          if (__shfl_sync(0xffffffffu, stop, 0)) {  // the whole warp leaves together
+          if (__any_sync(0xffffffffu, stop)) {  // the whole warp leaves together
             stopped = true;
             break;
           }
-          if (lane == 0) {
+          if (active) {
             const uint32_t full = smem_u32(&bars[s]);
             stage_pos[s] = pk;
             stage_ok[s] = okk;  // both published by the arrive below
@@ -137,51 +301,64 @@ __global__ void __launch_bounds__(kSThreads, 1)
               const uint32_t dst = smem_base + s * stage_bytes;
               const int row0 = (phk * kv.Hkv + h) * page;
               mbar_arrive_expect_tx(full, stage_bytes);
-              tma_load_2d(dst, &tmK, 0, row0, full);
-              tma_load_2d(dst + page * 128, &tmK, 64, row0, full);
-              tma_load_2d(dst + 2 * page * 128, &tmV, 0, row0, full);
-              tma_load_2d(dst + 3 * page * 128, &tmV, 64, row0, full);
+              tma_load_page(dst, &tmK, row0, full);
+              tma_load_page(dst + 2 * page * 128, &tmV, row0, full);
             }
           }
+          if (lane == 0) *issued = i + min(nb, q0 + NL);
         }
+        i += nb;
+        ua = ubb;
+        ba = bb;
+        pos_a = pos_b;
+        raw_a = raw_b;
+        ubb = uc;
+        bb = bc;
+        pos_b = pos_c;
       }
+      for (; uq < ue && !stopped; ++uq) stopped = !publish(uq);  // units without pages
     }
+    __syncwarp();
+    if (lane == 0) *producer_done = 1;
     return;  // the producer takes no part in the epilogues (they use named barrier 1)
   }
 
-  // ---- consumers
-  const int tiles = page / 16;
+  // ---- consumers: warp `warp` owns tile t of stage s when (s * tiles + t) % kSW == warp
+  uint32_t own_stages = 0;
+  for (int s = 0; s < S; ++s)
+    if (((warp - s * tiles) % kSW + kSW) % kSW < tiles) own_stages |= 1u << s;
   int i = 0;  // ring position, in lock-step with the producer
-  for (int u = blockIdx.x; u < units_total; u += gridDim.x) {
-    int row, beg, end;
-    unit_range(u, &row, &beg, &end);
+  bool any_cut = false;
+  for (int u = 0; u < n_units; ++u) {
+    const int slot = u & 1;
+    const bool got = mbar_wait(smem_u32(&qbars[slot]), (u >> 1) & 1, abort_flag, kv.status);
+    const int row = desc[slot * 4 + 0];
+    const int beg = desc[slot * 4 + 1];
+    const int end = got ? desc[slot * 4 + 2] : beg;
+    const int L = desc[slot * 4 + 3];
     const int b = row / kv.Hkv, h = row % kv.Hkv;
-    const int L = request_len(kv, b);
-    named_barrier(1, kSConsumers);
-    for (int e = tid; e < 16 * 16; e += kSConsumers) {
-      const int r = e >> 4, c = e & 15;
-      uint4 v = make_uint4(0, 0, 0, 0);
-      if (r < G)
-        v = *reinterpret_cast<const uint4*>(
-            a.q + (static_cast<size_t>(b) * kv.Hq + h * G + r) * kHeadDim + c * 8);
-      *reinterpret_cast<uint4*>(sQ + r * kQStride + c * 8) = v;
-    }
-    named_barrier(1, kSConsumers);
+    const int di = d_first + u;
     uint32_t qa[8][4];
-    load_q_frags(sQ, qa);
+    load_q_frags(sQ + slot * 16 * kHeadDim, qa, kHeadDim);
+    __syncwarp();
+    if (lane == 0) mbar_arrive(smem_u32(&qbars[2 + slot]));
     WarpSoftmaxState st;
     state_init(st);
-    int gkt = 0;
-    for (int j = beg; j < end; ++j, ++i) {
-      const int s = i % S, uu = i / S;
-      if (!mbar_wait(smem_u32(&bars[s]), uu & 1, abort_flag, kv.status)) break;
+    const int npg = end - beg;
+    for (int k = 0; k < npg; ++k) {
+      const int ii = i + k;
+      const int s = ii % S;
+      if (!((own_stages >> s) & 1u)) continue;
+      if (!mbar_wait(smem_u32(&bars[s]), (ii / S) & 1, abort_flag, kv.status)) break;
       const int pos = stage_pos[s];
       const bool loaded = stage_ok[s] != 0;
       const uint32_t kb = smem_base + s * stage_bytes;
       const uint32_t vb = kb + 2 * page * 128;
       bool wrote = false;
-      for (int t = 0; loaded && t < tiles; ++t) {
-        if (((gkt + t) & (kSW - 1)) != warp) continue;
+      int arrivals = 0;
+      for (int t = ((warp - s * tiles) % kSW + kSW) % kSW; t < tiles; t += kSW) {
+        ++arrivals;
+        if (!loaded) continue;
         const bool in = pos * page + t * 16 + (lane & 15) < L;
         const uint32_t vm = __ballot_sync(0xffffffffu, in) & 0xffffu;
         if (vm == 0u) continue;
@@ -191,150 +368,194 @@ __global__ void __launch_bounds__(kSThreads, 1)
         tile_scores(qa, kb, page, t * 16, sc);
         tile_softmax_pv(st, sc, a.scale_log2, vm, vb, page, t * 16);
       }
-      gkt += tiles;
       if (wrote) fence_proxy_async_smem();
       __syncwarp();
-      if (lane == 0) mbar_arrive(smem_u32(&bars[S + s]));
+      if (lane == 0)
+        for (int r = 0; r < arrivals; ++r) mbar_arrive(smem_u32(&bars[S + s]));
     }
+    i += npg;
     state_finish(st);
 
-    // ---- unit epilogue: merge the warps, write the unit's record, take a ticket
-    state_store(st, sO + warp * 2048, sM + warp * 16, sL + warp * 16);
+    // ---- unit epilogue: merge the warps' states of the G query heads
+    {
+      const int r0 = lane >> 2, c0 = (lane & 3) * 2;
+      float* wO = sO + warp * G * kHeadDim;
+#pragma unroll
+      for (int j = 0; j < 16; ++j) {
+        if (r0 < G)
+          *reinterpret_cast<float2*>(wO + r0 * kHeadDim + j * 8 + c0) =
+              make_float2(st.o[j][0], st.o[j][1]);
+        if (r0 + 8 < G)
+          *reinterpret_cast<float2*>(wO + (r0 + 8) * kHeadDim + j * 8 + c0) =
+              make_float2(st.o[j][2], st.o[j][3]);
+      }
+      if ((lane & 3) == 0) {
+        if (r0 < G) {
+          sM[warp * G + r0] = st.m[0];
+          sL[warp * G + r0] = st.l[0];
+        }
+        if (r0 + 8 < G) {
+          sM[warp * G + r0 + 8] = st.m[1];
+          sL[warp * G + r0 + 8] = st.l[1];
+        }
+      }
+    }
     named_barrier(1, kSConsumers);
-    const int c = u % chunks;
-    float* rec0 = a.part + (static_cast<size_t>(row) * a.chunks + c) * G * kRecordFloats;
+    const long long rs = static_cast<long long>(di) * stride;
+    const bool cut = slot_owner(rs, T, n_act) != slot_owner(rs + stride - 1, T, n_act);
+    any_cut |= cut;
+    float* rec0 =
+        a.part + (static_cast<size_t>(blockIdx.x) * 2 + (u == 0 ? 0 : 1)) * G * kRecordFloats;
     for (int e = tid; e < G * kHeadDim; e += kSConsumers) {
       const int g = e >> 7, d = e & 127;
       float M = -INFINITY;
 #pragma unroll
-      for (int w = 0; w < kSW; ++w) M = fmaxf(M, sM[w * 16 + g]);
+      for (int w = 0; w < kSW; ++w) M = fmaxf(M, sM[w * G + g]);
       float Lsum = 0.f, acc = 0.f;
       if (M != -INFINITY) {
 #pragma unroll
         for (int w = 0; w < kSW; ++w) {
-          const float mw = sM[w * 16 + g];
+          const float mw = sM[w * G + g];
           if (mw == -INFINITY) continue;
           const float f = fast_exp2(mw - M);
-          Lsum += sL[w * 16 + g] * f;
-          acc += sO[w * 2048 + g * 128 + d] * f;
+          Lsum += sL[w * G + g] * f;
+          acc += sO[(w * G + g) * kHeadDim + d] * f;
         }
       }
-      float* rec = rec0 + g * kRecordFloats;
-      rec[d] = Lsum > 0.f ? acc / Lsum : 0.f;
-      if (d == 0) {
-        rec[128] = Lsum > 0.f ? M * kLn2 : -INFINITY;
-        rec[129] = Lsum;
-      }
-    }
-    __threadfence();
-    named_barrier(1, kSConsumers);
-    if (tid == 0) *last_flag = atomicAdd(a.counters + row, 1) == chunks - 1;
-    named_barrier(1, kSConsumers);
-    if (*last_flag) {
-      // last unit of this row: merge its chunk records in chunk order.  The merge area is free
-      // again and holds each record's m and weight and each head's (M, L).
-      __threadfence();
-      const int C = chunks;
-      const float* base = a.part + static_cast<size_t>(row) * a.chunks * G * kRecordFloats;
-      float* s_m = sO;            // [G][C]
-      float* s_w = sO + G * C;    // [G][C]
-      float* s_ml = s_w + G * C;  // [G][2]
-      for (int e = tid; e < G * C; e += kSConsumers) {
-        const int g = e / C, cc = e - g * C;
-        const float* r = base + (static_cast<size_t>(cc) * G + g) * kRecordFloats;
-        s_m[e] = __ldcg(r + 128);
-        s_w[e] = __ldcg(r + 129);
-      }
-      named_barrier(1, kSConsumers);
-      for (int g = warp; g < G; g += kSW) {
-        float M = -INFINITY;
-        for (int cc = lane; cc < C; cc += 32)
-          if (s_w[g * C + cc] > 0.f) M = fmaxf(M, s_m[g * C + cc]);
-        M = warp_max(M);
-        float Ls = 0.f;
-        for (int cc = lane; cc < C; cc += 32) {
-          const float lp = s_w[g * C + cc];
-          const float wgt = lp > 0.f ? lp * fast_exp2((s_m[g * C + cc] - M) * kLog2e) : 0.f;
-          s_w[g * C + cc] = wgt;
-          Ls += wgt;
-        }
-        Ls = warp_sum(Ls);
-        if (lane == 0) {
-          s_ml[2 * g] = M;
-          s_ml[2 * g + 1] = Ls;
-        }
-      }
-      named_barrier(1, kSConsumers);
-      // warp w finalises heads w, w + 8, ...; lane owns dims 4*lane .. 4*lane + 3
-      for (int g = warp; g < G; g += kSW) {
-        float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
-        int cc = 0;
-        for (; cc + 8 <= C; cc += 8) {
-          float4 v[8];
-          float wv[8];
-#pragma unroll
-          for (int k = 0; k < 8; ++k) {
-            wv[k] = s_w[g * C + cc + k];
-            v[k] = wv[k] > 0.f
-                       ? __ldcg(reinterpret_cast<const float4*>(
-                                    base + (static_cast<size_t>(cc + k) * G + g) * kRecordFloats) +
-                                lane)
-                       : make_float4(0.f, 0.f, 0.f, 0.f);
-          }
-#pragma unroll
-          for (int k = 0; k < 8; ++k) {
-            acc.x += wv[k] * v[k].x;
-            acc.y += wv[k] * v[k].y;
-            acc.z += wv[k] * v[k].z;
-            acc.w += wv[k] * v[k].w;
-          }
-        }
-        for (; cc < C; ++cc) {
-          const float wk = s_w[g * C + cc];
-          if (!(wk > 0.f)) continue;
-          const float4 v = __ldcg(
-              reinterpret_cast<const float4*>(base + (static_cast<size_t>(cc) * G + g) *
-                                                         kRecordFloats) +
-              lane);
-          acc.x += wk * v.x;
-          acc.y += wk * v.y;
-          acc.z += wk * v.z;
-          acc.w += wk * v.w;
-        }
-        const float Ls = s_ml[2 * g + 1];
-        const float inv = Ls > 0.f ? 1.f / Ls : 0.f;
+      const float o = Lsum > 0.f ? acc / Lsum : 0.f;
+      const float mn = Lsum > 0.f ? M * kLn2 : -INFINITY;
+      if (!cut) {
         const size_t qh = static_cast<size_t>(b) * kv.Hq + static_cast<size_t>(h) * G + g;
-        *reinterpret_cast<float4*>(a.out + qh * kHeadDim + lane * 4) =
-            make_float4(acc.x * inv, acc.y * inv, acc.z * inv, acc.w * inv);
-        if (lane == 0) {
-          a.m[qh] = Ls > 0.f ? s_ml[2 * g] : -INFINITY;
-          a.l[qh] = Ls;
+        a.out[qh * kHeadDim + d] = o;
+        if (d == 0) {
+          a.m[qh] = mn;
+          a.l[qh] = Lsum;
+        }
+      } else {
+        float* rec = rec0 + g * kRecordFloats;
+        rec[d] = o;
+        if (d == 0) {
+          rec[128] = mn;
+          rec[129] = Lsum;
         }
       }
-      if (tid == 0) a.counters[row] = 0;  // ready for the next call
     }
+    named_barrier(1, kSConsumers);  // the merge area is rewritten by the next unit
+  }
+
+  // ---- rows cut across CTAs (only this CTA's first and last units can be).  Both tickets are
+  // taken at once when all of this CTA's records are written; the CTA that takes a row's last
+  // ticket merges the row's records in CTA order, eight records per round trip, one query head
+  // per warp.
+  if (any_cut) {
+    const int n_cut = n_units > 1 ? 2 : 1;
+    if (warp == 0 && lane < n_cut) {
+      const int di = d_first + (lane == 0 ? 0 : n_units - 1);
+      const long long rs = static_cast<long long>(di) * stride;
+      const int c_first = slot_owner(rs, T, n_act);
+      const int c_last = slot_owner(rs + stride - 1, T, n_act);
+      int last = 0;
+      if (c_first != c_last) {
+        const int row = (di / nd_heads) * kv.Hkv + dense_heads[di % nd_heads];
+        last = ticket_add(a.counters + row) == c_last - c_first;
+      }
+      last_flag[lane] = last;
+    }
+    named_barrier(1, kSConsumers);
+    const int n_jobs = n_cut * G;  // (cut row, head) pairs
+    for (int job = warp; job < n_jobs; job += kSW) {
+      const int k = job / G, g = job - k * G;
+      if (!last_flag[k]) continue;
+      const int di = d_first + (k == 0 ? 0 : n_units - 1);
+      const int row = (di / nd_heads) * kv.Hkv + dense_heads[di % nd_heads];
+      const long long rs = static_cast<long long>(di) * stride;
+      const int c_first = slot_owner(rs, T, n_act);
+      const int C = slot_owner(rs + stride - 1, T, n_act) - c_first + 1;
+      float M = -INFINITY, Ls = 0.f;
+      float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
+      for (int c0 = 0; c0 < C; c0 += 8) {
+        float4 v[8];
+        float mv[8], lv[8];
+#pragma unroll
+        for (int j = 0; j < 8; ++j) {
+          mv[j] = -INFINITY;
+          lv[j] = 0.f;
+          v[j] = make_float4(0.f, 0.f, 0.f, 0.f);
+          const int c = c_first + c0 + j;
+          if (c0 + j < C) {
+            const int slot = static_cast<int>(slot_start(c, T, n_act) / stride) == di ? 0 : 1;
+            const float* r = a.part + ((static_cast<size_t>(c) * 2 + slot) * G + g) * kRecordFloats;
+            v[j] = __ldcg(reinterpret_cast<const float4*>(r) + lane);
+            mv[j] = __ldcg(r + 128);
+            lv[j] = __ldcg(r + 129);
+          }
+        }
+        float Mn = M;
+#pragma unroll
+        for (int j = 0; j < 8; ++j)
+          if (lv[j] > 0.f) Mn = fmaxf(Mn, mv[j]);
+        if (Mn == -INFINITY) continue;
+        const float f = M == -INFINITY ? 0.f : fast_exp2((M - Mn) * kLog2e);
+        Ls *= f;
+        acc.x *= f;
+        acc.y *= f;
+        acc.z *= f;
+        acc.w *= f;
+#pragma unroll
+        for (int j = 0; j < 8; ++j) {
+          const float wgt = lv[j] > 0.f ? lv[j] * fast_exp2((mv[j] - Mn) * kLog2e) : 0.f;
+          Ls += wgt;
+          acc.x += wgt * v[j].x;
+          acc.y += wgt * v[j].y;
+          acc.z += wgt * v[j].z;
+          acc.w += wgt * v[j].w;
+        }
+        M = Mn;
+      }
+      const float inv = Ls > 0.f ? 1.f / Ls : 0.f;
+      const int b = row / kv.Hkv, h = row % kv.Hkv;
+      const size_t qh = static_cast<size_t>(b) * kv.Hq + static_cast<size_t>(h) * G + g;
+      *reinterpret_cast<float4*>(a.out + qh * kHeadDim + lane * 4) =
+          make_float4(acc.x * inv, acc.y * inv, acc.z * inv, acc.w * inv);
+      if (lane == 0) {
+        a.m[qh] = Ls > 0.f ? M : -INFINITY;
+        a.l[qh] = Ls;
+        if (g == 0) a.counters[row] = 0;  // ready for the next call
+      }
+    }
+  }
+
+  // after a timeout, wait (bounded) for the page loads still in flight before the CTA exits
+  if (tid == 0 && *abort_flag) {
+    const unsigned long long t0 = global_timer_ns();
+    while (!*producer_done && global_timer_ns() - t0 < 50000000ull) {
+    }
+    const int n = *issued;
+    for (int k = max(0, n - S); k < n; ++k)
+      if (!mbar_wait_drain(smem_u32(&bars[k % S]), (k / S) & 1)) break;
   }
 }
 
 }  // namespace
 
-size_t stream_attn_smem_bytes(int page, int stages) { return slayout(page, stages).total; }
+size_t stream_attn_smem_bytes(int page, int stages, int G) {
+  return slayout(page, stages, G).total;
+}
+
+int stream_attn_grid() {
+  int dev = 0, sms = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess ||
+      cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess || sms < 1)
+    return kStreamMaxGrid;
+  return sms < kStreamMaxGrid ? sms : kStreamMaxGrid;
+}
 
 cudaError_t launch_stream_attn(const CUtensorMap& tmK, const CUtensorMap& tmV,
-                               const StreamAttnArgs& a, cudaStream_t s) {
-  const size_t bytes = slayout(a.kv.p, a.stages).total;
+                               const StreamAttnArgs& a, int grid, cudaStream_t s) {
+  const size_t bytes = slayout(a.kv.p, a.stages, a.kv.G).total;
   cudaError_t e = ensure_dynamic_smem(reinterpret_cast<const void*>(stream_attn_kernel), bytes);
   if (e != cudaSuccess) return e;
-  // a persistent grid: as many CTAs as are resident at once
-  int dev = 0, sms = 0, per_sm = 0;
-  if ((e = cudaGetDevice(&dev)) != cudaSuccess) return e;
-  if ((e = cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev)) != cudaSuccess)
-    return e;
-  if ((e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, stream_attn_kernel, kSThreads,
-                                                         bytes)) != cudaSuccess)
-    return e;
-  if (per_sm < 1) return cudaErrorInvalidConfiguration;
-  stream_attn_kernel<<<per_sm * sms, kSThreads, bytes, s>>>(tmK, tmV, a);
+  stream_attn_kernel<<<grid, kSThreads, bytes, s>>>(tmK, tmV, a);
   return cudaGetLastError();
 }
 

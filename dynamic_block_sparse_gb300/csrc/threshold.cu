@@ -153,10 +153,8 @@ __global__ void __launch_bounds__(kThrThreads)
         if (s_phys[cc] < 0) continue;
         const uint32_t dst = smem_base + cc * stage_bytes;
         const int row0 = (s_phys[cc] * kv.Hkv + h) * page;
-        tma_load_2d(dst, &tmK, 0, row0, full);
-        tma_load_2d(dst + page * 128, &tmK, 64, row0, full);
-        tma_load_2d(dst + 2 * page * 128, &tmV, 0, row0, full);
-        tma_load_2d(dst + 3 * page * 128, &tmV, 64, row0, full);
+        tma_load_page(dst, &tmK, row0, full);
+        tma_load_page(dst + 2 * page * 128, &tmV, row0, full);
       }
     }
     __syncthreads();

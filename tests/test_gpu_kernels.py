@@ -192,6 +192,48 @@ def test_sparse_decode_attn(Hq, Hkv, page, splits):
     assert int(cache.status.item()) == 0
 
 
+# The default (persistent) path cuts the global page-slot space into one equal range per CTA:
+# one long row split across every CTA, many short rows inside single CTAs, fewer slots than CTAs,
+# streaming heads left out of the slot space, and a second call on the same workspace (the row
+# tickets must be back at zero).
+@pytest.mark.parametrize("shape", ["one_long_row", "many_short_rows", "fewer_slots_than_ctas",
+                                   "streaming_heads"])
+def test_persistent_partition(shape):
+    streaming = ()
+    if shape == "one_long_row":
+        w, inp, cache = small(B_=1, Hq=8, Hkv=1, page=16, L=16 * 1100 + 3, seed=11)
+        k = 1024
+    elif shape == "many_short_rows":
+        w, inp, cache = small(B_=40, Hq=32, Hkv=8, page=16, L=16 * 30 + 5, seed=12)
+        k = 3
+    elif shape == "fewer_slots_than_ctas":
+        w, inp, cache = small(B_=1, Hq=8, Hkv=2, page=16, L=16 * 9, seed=13)
+        k = 5
+    else:
+        streaming = (1, 3)
+        w, inp, cache = small(B_=3, Hq=16, Hkv=4, page=64, L=64 * 50 + 3, seed=14,
+                              streaming=streaming)
+        k = 20
+    idx, cnt = _random_selection(w, inp, k, seed=k, allow_bad=False)
+    scale = 1 / math.sqrt(128)
+    q = inp["q"][0]
+    ws = torch.empty(max(16, B.dsa_sparse_decode_attn_workspace_size(cache.kv, k)),
+                     dtype=torch.uint8, device="cuda")
+    ref = _oracle_sparse(w, inp, cache, q, idx, cnt, scale)
+    dense = np.array([h not in streaming for h in range(w.num_kv_heads)]).repeat(w.group)
+    for call in range(2):
+        out, m, l = cache.outputs()
+        B.dsa_sparse_decode_attn(cache.kv, q, torch.from_numpy(idx).cuda(),
+                                 torch.from_numpy(cnt).cuda(), scale, out, m, l, workspace=ws)
+        torch.cuda.synchronize()
+        assert_outputs(out.cpu().numpy()[:, dense], m.cpu().numpy()[:, dense],
+                       l.cpu().numpy()[:, dense], [x[:, dense] for x in ref],
+                       f"{shape} call {call}")
+        if streaming:  # rows of streaming heads are not this call's to write
+            assert not out[:, ~torch.from_numpy(dense).cuda()].any()
+        assert int(cache.status.item()) == 0
+
+
 @pytest.mark.parametrize("Hq,Hkv,page", [(32, 2, 64), (8, 2, 16)])
 def test_page_partials_and_merge(Hq, Hkv, page):
     w, inp, cache = small(Hq=Hq, Hkv=Hkv, page=page, L=page * 30 + 1, seed=3)
