@@ -41,6 +41,19 @@ class PagedKV(ctypes.Structure):
     ]
 
 
+class PrrStepArgs(ctypes.Structure):
+    """Mirror of ``dsa_prr_step_args``."""
+    _fields_ = [
+        ("q", c_void_p), ("meta", c_void_p), ("scores", c_void_p), ("stride", c_int32),
+        ("ell", c_void_p), ("trend", c_void_p), ("alpha", c_float), ("beta", c_float),
+        ("gamma", c_float), ("pred", c_void_p), ("spec_idx", c_void_p), ("spec_count", c_void_p),
+        ("k_pred", c_int32), ("page_partials", c_void_p), ("idx", c_void_p),
+        ("count", c_void_p), ("k", c_int32), ("next_idx", c_void_p), ("next_count", c_void_p),
+        ("superset", c_int32), ("scale", c_float), ("out", c_void_p), ("m", c_void_p),
+        ("l", c_void_p),
+    ]
+
+
 _P = c_void_p
 _I = c_int32
 _SIGNATURES = {
@@ -64,6 +77,8 @@ _SIGNATURES = {
     "dsa_ema_predict_update": ([_P, _I, _I, _I, _P, _P, _I, c_float, c_float, c_float, _P, _I,
                                 _P, _I, _P, _P], _I),
     "dsa_merge_partials": ([_P, _I, _I, _I, _I, _P, _P, _P, _P], _I),
+    "dsa_prr_step": ([_P, _P, _P, c_size_t, _P], _I),
+    "dsa_prr_step_workspace_size": ([_P], c_size_t),
 }
 
 _lib = None
@@ -242,3 +257,30 @@ def dsa_merge_partials(partials, out, m, l, stream=None):
     assert rec == RECORD_FLOATS
     _check("dsa_merge_partials", load().dsa_merge_partials(
         _ptr(partials), rows, parts, G, 128, _ptr(out), _ptr(m), _ptr(l), _stream(stream)))
+
+
+def dsa_prr_step_workspace_size(kv: PagedKV) -> int:
+    return int(load().dsa_prr_step_workspace_size(ctypes.byref(kv)))
+
+
+def dsa_prr_step(kv: PagedKV, q, meta, scores, ell, trend, alpha: float, beta: float,
+                 gamma: float, spec_idx, spec_count, page_partials, idx, count, next_idx,
+                 next_count, scale: float, out, m, l, workspace, pred=None,
+                 superset: bool = False, stream=None):
+    """One PRR decode step (scoring, top-k, speculation over P_t, EMA update with the selection
+    of P_{t+1}, repair and merge) in one launch.  ``workspace`` must be zero-filled before its
+    first use (each completed call leaves it zero-filled)."""
+    a = PrrStepArgs()
+    a.q, a.meta, a.scores, a.stride = _ptr(q), _ptr(meta), _ptr(scores), scores.shape[-1]
+    a.ell, a.trend = _ptr(ell), _ptr(trend)
+    a.alpha, a.beta, a.gamma, a.pred = alpha, beta, gamma, _ptr(pred)
+    a.spec_idx, a.spec_count, a.k_pred = _ptr(spec_idx), _ptr(spec_count), spec_idx.shape[-1]
+    a.page_partials = _ptr(page_partials)
+    a.idx, a.count, a.k = _ptr(idx), _ptr(count), idx.shape[-1]
+    a.next_idx, a.next_count = _ptr(next_idx), _ptr(next_count)
+    assert next_idx.shape[-1] == spec_idx.shape[-1]
+    a.superset, a.scale = 1 if superset else 0, scale
+    a.out, a.m, a.l = _ptr(out), _ptr(m), _ptr(l)
+    ws_bytes = workspace.numel() * workspace.element_size()
+    _check("dsa_prr_step", load().dsa_prr_step(ctypes.byref(kv), ctypes.byref(a), _ptr(workspace),
+                                               ws_bytes, _stream(stream)))

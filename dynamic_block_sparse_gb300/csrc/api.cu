@@ -652,4 +652,88 @@ int dsa_sparse_decode_attn_noalloc(const dsa_paged_kv* kv, const void* q, const 
   return ok();
 }
 
+size_t dsa_prr_step_workspace_size(const dsa_paged_kv* kv) {
+  if (!kv || kv->batch <= 0 || kv->num_kv_heads <= 0) return 0;
+  return prr_step_workspace_bytes(kv->batch * kv->num_kv_heads);
+}
+
+int dsa_prr_step(const dsa_paged_kv* kv, const dsa_prr_step_args* args, void* workspace,
+                 size_t workspace_bytes, dsa_stream_t stream) {
+  KvView v;
+  int rc = check_kv(kv, 2, &v);
+  if (rc) return rc;
+  if (!args) return fail(DSA_ERR_INVALID_ARG, "dsa_prr_step: args is NULL");
+  const dsa_prr_step_args& x = *args;
+  if (!x.q || !x.meta || !x.scores || !x.ell || !x.trend || !x.spec_idx || !x.spec_count ||
+      !x.page_partials || !x.idx || !x.count || !x.next_idx || !x.next_count || !x.out || !x.m ||
+      !x.l)
+    return fail(DSA_ERR_INVALID_ARG, "dsa_prr_step: a required pointer is NULL");
+  if (v.streaming != nullptr)
+    return fail(DSA_ERR_UNSUPPORTED, "dsa_prr_step: streaming heads are not supported");
+  if (x.k < 1 || x.k_pred < 1) return fail(DSA_ERR_INVALID_ARG, "dsa_prr_step: k and k_pred >= 1");
+  if (x.stride < v.max_pages || x.stride > kMaxSelectN)
+    return fail(DSA_ERR_INVALID_ARG, "dsa_prr_step: stride must be in [max_pages_per_seq, %d]",
+                kMaxSelectN);
+  if (x.k > kMaxListPages || x.k_pred > kMaxListPages)
+    return fail(DSA_ERR_UNSUPPORTED, "dsa_prr_step: k and k_pred must be <= %d", kMaxListPages);
+  if (x.next_idx == x.spec_idx || x.next_count == x.spec_count)
+    return fail(DSA_ERR_INVALID_ARG, "dsa_prr_step: next_idx/next_count must not alias P_t");
+  if (!aligned(x.q, 16) || !aligned(x.meta, 16) || !aligned(x.page_partials, 16))
+    return fail(DSA_ERR_ALIGNMENT, "dsa_prr_step: q, meta and page_partials must be 16-byte aligned");
+  const size_t ws_need = prr_step_workspace_bytes(v.B * v.Hkv);
+  if (!workspace || workspace_bytes < ws_need)
+    return fail(DSA_ERR_WORKSPACE, "workspace of %zu bytes needed", ws_need);
+  if (!aligned(workspace, 16)) return fail(DSA_ERR_ALIGNMENT, "workspace must be 16-byte aligned");
+  if (prr_step_smem_bytes(v.p, v.G, x.stride, x.k, x.k_pred) > 200 * 1024)
+    return fail(DSA_ERR_UNSUPPORTED, "dsa_prr_step: shape needs too much shared memory");
+  int dev = 0, coop = 0;
+  cudaError_t e = cudaGetDevice(&dev);
+  if (e == cudaSuccess) e = cudaDeviceGetAttribute(&coop, cudaDevAttrCooperativeLaunch, dev);
+  if (e != cudaSuccess) return cuda_fail(e, "dsa_prr_step device query");
+  if (!coop) return fail(DSA_ERR_UNSUPPORTED, "dsa_prr_step: the device has no cooperative launch");
+  CUtensorMap tk, tv;
+  if ((rc = pool_map(kv->k_pages, kv, &tk)) || (rc = pool_map(kv->v_pages, kv, &tv))) return rc;
+  PrrStepArgs a = {};
+  a.kv = v;
+  a.kpool = static_cast<const __nv_bfloat16*>(kv->k_pages);
+  a.vpool = static_cast<const __nv_bfloat16*>(kv->v_pages);
+  a.q = static_cast<const __nv_bfloat16*>(x.q);
+  a.meta = static_cast<const uint8_t*>(x.meta);
+  a.scores = x.scores;
+  a.stride = x.stride;
+  a.ell = x.ell;
+  a.trend = x.trend;
+  a.alpha = x.alpha;
+  a.beta = x.beta;
+  a.gamma = x.gamma;
+  a.pred = x.pred;
+  a.spec_idx = x.spec_idx;
+  a.spec_count = x.spec_count;
+  a.k_pred = x.k_pred;
+  a.partials = x.page_partials;
+  a.idx = x.idx;
+  a.count = x.count;
+  a.k = x.k;
+  a.next_idx = x.next_idx;
+  a.next_count = x.next_count;
+  a.superset = x.superset != 0;
+  a.scale_log2 = scale_log2(x.scale);
+  a.out = x.out;
+  a.m = x.m;
+  a.l = x.l;
+  a.sync = static_cast<unsigned*>(workspace);
+  {
+    const size_t rows = static_cast<size_t>(v.B) * v.Hkv;
+    const size_t cnt = (4 * rows + 15) & ~static_cast<size_t>(15);
+    const size_t list = rows * 512 * sizeof(uint2);
+    char* w = static_cast<char*>(workspace) + 256;
+    a.cand_cnt = reinterpret_cast<unsigned*>(w);
+    a.cand = reinterpret_cast<uint2*>(w + cnt);
+    a.cand_cnt2 = reinterpret_cast<unsigned*>(w + cnt + list);
+    a.cand2 = reinterpret_cast<uint2*>(w + 2 * cnt + list);
+  }
+  e = launch_prr_step(tk, tv, a, static_cast<cudaStream_t>(stream));
+  return e == cudaSuccess ? ok() : cuda_fail(e, "dsa_prr_step launch");
+}
+
 }  // extern "C"

@@ -119,6 +119,45 @@ int stream_attn_grid();  // CTAs of one launch: one per SM
 cudaError_t launch_stream_attn(const CUtensorMap& tmK, const CUtensorMap& tmV,
                                const StreamAttnArgs& a, int grid, cudaStream_t s);
 
+// One PRR decode step in one cooperative launch (prr_step.cu).
+struct PrrStepArgs {
+  KvView kv;
+  const __nv_bfloat16* kpool;
+  const __nv_bfloat16* vpool;
+  const __nv_bfloat16* q;
+  const uint8_t* meta;  // MINMAX, logical page = page
+  float* scores;
+  int stride;
+  float* ell;
+  float* trend;
+  float alpha, beta, gamma;
+  float* pred;
+  const int32_t* spec_idx;
+  const int32_t* spec_count;
+  int k_pred;
+  float* partials;
+  int32_t* idx;
+  int32_t* count;
+  int k;
+  int32_t* next_idx;
+  int32_t* next_count;
+  int superset;
+  float scale_log2;
+  float* out;
+  float* m;
+  float* l;
+  unsigned* sync;      // 3 words, zero on entry, left zero
+  unsigned* cand_cnt;   // [rows], zero on entry, left zero
+  uint2* cand;          // [rows][512]
+  unsigned* cand_cnt2;  // [rows], zero on entry, left zero
+  uint2* cand2;         // [rows][512]
+};
+size_t prr_step_smem_bytes(int page, int G, int n, int k, int k_pred);
+// sync words, then for A_t and for P_{t+1}: candidate counts, candidate lists
+size_t prr_step_workspace_bytes(int rows);
+cudaError_t launch_prr_step(const CUtensorMap& tmK, const CUtensorMap& tmV, const PrrStepArgs& a,
+                            cudaStream_t s);
+
 // metadata and scoring
 cudaError_t launch_build_meta(const KvView& kv, const __nv_bfloat16* k_pages, int kind, int lp,
                               void* meta, cudaStream_t s);

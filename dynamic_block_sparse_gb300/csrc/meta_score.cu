@@ -2,6 +2,7 @@
 // vector loads, several independent loads in flight per thread, no shared-memory staging needed.
 #include "common.cuh"
 #include "internal.h"
+#include "score_core.cuh"
 
 namespace dsa {
 namespace {
@@ -120,34 +121,9 @@ __global__ void __launch_bounds__(256)
 }
 
 // ------------------------------------------------------------------------------------ scoring
-// Each 512-byte metadata record (MINMAX: 128 x (max, min) bf16; MEAN: 128 fp32) is read by a
-// group of 8 lanes, 4 x 16 bytes each; chunk c covers dims 4c..4c+3 in both formats, so lane
-// (l & 7) always needs the same 16 query dims and keeps them in registers.
+// Record groups of 8 lanes (arithmetic in score_core.cuh).
 constexpr int kScoreThreads = 256;
 constexpr int kScoreGroups = kScoreThreads / 8;
-
-template <int KIND>
-DSA_DEV float record_partial(const uint4 (&raw)[4], const float (&qv)[16]) {
-  float s = 0.f;
-#pragma unroll
-  for (int i = 0; i < 4; ++i) {
-    if (KIND == DSA_META_MINMAX) {
-      const __nv_bfloat16* v = reinterpret_cast<const __nv_bfloat16*>(&raw[i]);
-#pragma unroll
-      for (int e = 0; e < 4; ++e) {
-        const float q = qv[i * 4 + e];
-        const float hi = q * __bfloat162float(v[2 * e]);
-        const float lo = q * __bfloat162float(v[2 * e + 1]);
-        s += fmaxf(hi, lo);
-      }
-    } else {
-      const float* v = reinterpret_cast<const float*>(&raw[i]);
-#pragma unroll
-      for (int e = 0; e < 4; ++e) s = fmaf(qv[i * 4 + e], v[e], s);
-    }
-  }
-  return s;
-}
 
 template <int KIND>
 __global__ void __launch_bounds__(kScoreThreads)
@@ -167,20 +143,13 @@ __global__ void __launch_bounds__(kScoreThreads)
   const int g = kv.p / lp;
   const int L = request_len(kv, b);
   const int nl = (L + lp - 1) / lp;
-  if (threadIdx.x < kHeadDim) {
-    const __nv_bfloat16* qg = q + (static_cast<size_t>(b) * kv.Hq + h * kv.G) * kHeadDim;
-    float s = 0.f;
-    for (int r = 0; r < kv.G; ++r) s += __bfloat162float(qg[r * kHeadDim + threadIdx.x]);
-    sQbar[threadIdx.x] = s / static_cast<float>(kv.G);
-  }
+  group_mean_query(q + (static_cast<size_t>(b) * kv.Hq + h * kv.G) * kHeadDim, kv.G, sQbar,
+                   threadIdx.x, kScoreThreads);
   __syncthreads();
   const int lane = threadIdx.x & 31;
   const int gl = lane & 7;
   float qv[16];
-#pragma unroll
-  for (int i = 0; i < 4; ++i)
-#pragma unroll
-    for (int e = 0; e < 4; ++e) qv[i * 4 + e] = sQbar[(gl + 8 * i) * 4 + e];
+  group_query_dims(sQbar, gl, qv);
 
   const int32_t* table = kv.page_table + static_cast<size_t>(b) * kv.max_pages;
   // warp-uniform loop: warp w, group gi of its 4 groups, handles records jA and jA + 32
@@ -194,25 +163,10 @@ __global__ void __launch_bounds__(kScoreThreads)
     const bool okB = inB && physB >= 0 && physB < kv.num_phys;
     if (gl == 0 && ((inA && !okA) || (inB && !okB))) raise_status(kv.status, DSA_STATUS_BAD_PAGE);
     uint4 ra[4], rb[4];
-    if (okA) {
-      const uint4* rec = reinterpret_cast<const uint4*>(
-          meta + ((static_cast<size_t>(physA) * kv.Hkv + h) * g + jA % g) * 512);
-#pragma unroll
-      for (int i = 0; i < 4; ++i) ra[i] = __ldg(rec + gl + 8 * i);
-    }
-    if (okB) {
-      const uint4* rec = reinterpret_cast<const uint4*>(
-          meta + ((static_cast<size_t>(physB) * kv.Hkv + h) * g + jB % g) * 512);
-#pragma unroll
-      for (int i = 0; i < 4; ++i) rb[i] = __ldg(rec + gl + 8 * i);
-    }
-    float sA = okA ? record_partial<KIND>(ra, qv) : 0.f;
-    float sB = okB ? record_partial<KIND>(rb, qv) : 0.f;
-#pragma unroll
-    for (int o = 1; o < 8; o <<= 1) {
-      sA += __shfl_xor_sync(0xffffffffu, sA, o);
-      sB += __shfl_xor_sync(0xffffffffu, sB, o);
-    }
+    if (okA) load_record(meta, (static_cast<size_t>(physA) * kv.Hkv + h) * g + jA % g, gl, ra);
+    if (okB) load_record(meta, (static_cast<size_t>(physB) * kv.Hkv + h) * g + jB % g, gl, rb);
+    const float sA = group_sum(okA ? record_partial<KIND>(ra, qv) : 0.f);
+    const float sB = group_sum(okB ? record_partial<KIND>(rb, qv) : 0.f);
     if (gl == 0) {
       if (jA < j1) out[jA] = okA ? sA : -INFINITY;
       if (jB < j1) out[jB] = okB ? sB : -INFINITY;

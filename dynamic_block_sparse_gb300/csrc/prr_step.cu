@@ -1,0 +1,1078 @@
+// One whole PRR decode step (t >= 1) in a single cooperative launch ("Predict, Reuse, and Repair"
+// §3: speculation over the predicted set, predictor update, repair and merge).
+//
+// Every CTA (one per SM, all resident) runs three phases separated by two grid barriers:
+//   1. its share of the speculative per-page attention over P_t (one TMA-staged page per item,
+//      the whole query group as the m16 tile) while it scores its equal share of the (row, page)
+//      metadata records with the scoring kernel's exact arithmetic;
+//   2. per row, one CTA selects A_t = top-k of the scores and another updates the EMA predictor
+//      and selects P_{t+1} = top-k_pred of the prediction (the selection kernels' code);
+//   3. per (row, query head), one CTA attends to the missed pages A_t \ P_t on the CUDA cores and
+//      merges that part with the speculative records of A_t ∩ P_t (or all of P_t) by log-sum-exp.
+// Barrier waits are bounded: a CTA that gives up raises DSA_STATUS_TIMEOUT and skips the rest.
+// The barrier counters live in the caller's workspace; the last CTA out resets them to zero.
+#include "attn_core.cuh"
+#include "internal.h"
+#include "score_core.cuh"
+#include "select.cuh"
+
+namespace dsa {
+namespace {
+
+constexpr int kPW = 8;                     // compute warps of phase 1
+constexpr int kPThreads = (kPW + 1) * 32;  // + one TMA issue warp; phases 2 and 3 use all nine
+constexpr int kPWarps = kPThreads / 32;
+constexpr int kPStages = 2;
+constexpr int kPGroups = kPW * 32 / 8;  // scoring record groups of 8 lanes
+constexpr int kCandCap = kTopkMaxCand;  // candidates kept per row for the selection of A_t
+constexpr int kEmaCap = 1024;  // EMA updates a CTA stages on chip during scoring (its slot share)
+
+struct PLayout {
+  // phase 1
+  uint32_t stage_off, merge_off, q_off, qbar_off, wt_off, sps_off, ppk_off, ema_off, bar_off, ctl_off,
+      p1_end;
+  // phase 3
+  uint32_t sp_off, sa_off, list_off, part_off, pm_off, pl_off, qh_off, ws_off, wf_off, acc_off,
+      p3_end;
+  uint32_t total;
+};
+
+__host__ __device__ inline uint32_t up(uint32_t x, uint32_t a) { return (x + a - 1) / a * a; }
+
+__host__ __device__ inline PLayout playout(int page, int G, int n, int k, int k_pred) {
+  PLayout L;
+  L.stage_off = 0;
+  L.merge_off = up(kPStages * 512u * page, 1024);
+  L.q_off = up(L.merge_off + kPW * G * (kHeadDim + 2) * 4u, 16);
+  L.qbar_off = up(L.q_off + 16u * kQStride * 2u, 16);
+  L.wt_off = up(L.qbar_off + kHeadDim * 4u, 16);
+  L.sps_off = up(L.wt_off + (kPW + 1) * 16 * 4u, 16);
+  L.ppk_off = up(L.sps_off + 4u * k_pred, 16);
+  L.ema_off = up(L.ppk_off + 4u * k_pred, 16);
+  L.bar_off = up(L.ema_off + 3u * 4u * kEmaCap, 16);
+  L.ctl_off = L.bar_off + 2 * kPStages * 8u;
+  L.p1_end = L.ctl_off + 2 * kPStages * 4u;
+  // phase 2: keys [n] at offset 0
+  const uint32_t p2_end = 4u * static_cast<uint32_t>(n);
+  // phase 3
+  L.sp_off = 0;
+  L.sa_off = up(4u * k_pred, 16);
+  L.list_off = up(L.sa_off + 4u * k, 16);
+  L.part_off = up(L.list_off + 8u * k, 16);
+  L.pm_off = up(L.part_off + 4u * k_pred, 16);
+  L.pl_off = up(L.pm_off + 4u * k_pred, 16);
+  L.qh_off = up(L.pl_off + 4u * k_pred, 16);
+  L.ws_off = up(L.qh_off + 4u * kHeadDim, 16);
+  L.wf_off = up(L.ws_off + kPWarps * (kHeadDim + 4) * 4u, 16);
+  L.acc_off = up(L.wf_off + kPWarps * 4u, 16);
+  L.p3_end = L.acc_off + kPWarps * kHeadDim * 4u;
+  uint32_t t = L.p1_end;
+  if (p2_end > t) t = p2_end;
+  if (L.p3_end > t) t = L.p3_end;
+  L.total = t + 1024u;  // alignment slack
+  return L;
+}
+
+DSA_DEV unsigned ld_acquire(const unsigned* p) {
+  unsigned v;
+  asm volatile("ld.acquire.gpu.global.u32 %0, [%1];" : "=r"(v) : "l"(p) : "memory");
+  return v;
+}
+
+// Grid-wide barrier over a monotonically counting word: arrive, then wait until every CTA has.
+// Bounded: gives up after kWaitLimitNs, raising DSA_STATUS_TIMEOUT.  Returns false when this CTA
+// (or an earlier barrier of it) gave up.
+DSA_DEV bool grid_barrier(unsigned* ctr, unsigned target, volatile int* abort, int32_t* status) {
+  __syncthreads();
+  if (threadIdx.x == 0 && !*abort) {
+    __threadfence();  // this CTA's writes (ordered before by the CTA barrier) become visible
+    atomicAdd(ctr, 1u);
+    const unsigned long long t0 = global_timer_ns();
+    while (ld_acquire(ctr) < target) {
+      if (global_timer_ns() - t0 > kWaitLimitNs) {
+        *abort = 1;
+        raise_status(status, DSA_STATUS_TIMEOUT);
+        break;
+      }
+      __nanosleep(500);
+    }
+  }
+  __syncthreads();
+  return !*abort;
+}
+
+// Arrival without waiting (for CTAs whose later work does not depend on the barrier).
+DSA_DEV void grid_arrive(unsigned* ctr, volatile int* abort) {
+  __syncthreads();
+  if (threadIdx.x == 0 && !*abort) {
+    __threadfence();
+    atomicAdd(ctr, 1u);
+  }
+}
+
+struct PrrArgs {
+  KvView kv;
+  const __nv_bfloat16* kpool;  // bf16 [P][Hkv][p][128]
+  const __nv_bfloat16* vpool;
+  const __nv_bfloat16* q;
+  const uint8_t* meta;
+  float* scores;
+  int stride;  // score / EMA row stride = candidates per row
+  float* ell;
+  float* trend;
+  float alpha, beta, gamma;
+  float* pred;
+  const int32_t* spec_idx;
+  const int32_t* spec_count;
+  int k_pred;
+  float* partials;  // [rows][k_pred][G][kRecordFloats]
+  int32_t* idx;
+  int32_t* count;
+  int k;
+  int32_t* next_idx;
+  int32_t* next_count;
+  int superset;
+  float scale_log2;
+  float* out;
+  float* m;
+  float* l;
+  unsigned* sync;        // [0] barrier 1, [1] barrier 2, [2] exit count
+  unsigned* cand_cnt;    // [rows] candidates for A_t appended (zero on entry, left zero)
+  uint2* cand;           // [rows][kCandCap] (key, index)
+  unsigned* cand_cnt2;   // [rows] candidates for P_{t+1} (zero on entry, left zero)
+  uint2* cand2;          // [rows][kCandCap]
+};
+
+__global__ void __launch_bounds__(kPThreads, 1)
+    prr_step_kernel(const __grid_constant__ CUtensorMap tmK,
+                    const __grid_constant__ CUtensorMap tmV, const PrrArgs a) {
+  extern __shared__ uint8_t smem_raw[];
+  uint8_t* smem = reinterpret_cast<uint8_t*>(
+      (reinterpret_cast<uintptr_t>(smem_raw) + 1023u) & ~static_cast<uintptr_t>(1023u));
+  __shared__ SelectAnyScratch<kPThreads> sel_scratch;
+  __shared__ int s_abort, s_issued, s_red[33];
+  __shared__ unsigned s_t0key, s_t1key;
+  __shared__ float s_f[kPWarps];
+  const KvView& kv = a.kv;
+  const int page = kv.p, G = kv.G, tiles = page / 16;
+  const int rows = kv.B * kv.Hkv;
+  const int n = a.stride;
+  const PLayout lay = playout(page, G, n, a.k, a.k_pred);
+  const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+  volatile int* abort_flag = &s_abort;
+  const uint32_t smem_base = smem_u32(smem);
+  const uint32_t stage_bytes = 512u * page;
+
+  // ================================================================ phase 1
+  float* sO = reinterpret_cast<float*>(smem + lay.merge_off);  // [kPW][G][128]
+  float* sM = sO + kPW * G * kHeadDim;                          // [kPW][G]
+  float* sL = sM + kPW * G;                                     // [kPW][G]
+  __nv_bfloat16* sQ = reinterpret_cast<__nv_bfloat16*>(smem + lay.q_off);
+  float* qbar = reinterpret_cast<float*>(smem + lay.qbar_off);
+  float* wt = reinterpret_cast<float*>(smem + lay.wt_off);  // [kPW][16] warp weight / l
+  uint32_t* spk = reinterpret_cast<uint32_t*>(smem + lay.sps_off);  // keys of P_t's true scores
+  uint32_t* ppk = reinterpret_cast<uint32_t*>(smem + lay.ppk_off);  // ... of their predictions
+  float* st_ell = reinterpret_cast<float*>(smem + lay.ema_off);     // staged EMA updates [kEmaCap]
+  float* st_v = st_ell + kEmaCap;
+  float* st_pred = st_v + kEmaCap;
+  // this CTA's equal share [s_beg, s_end) of the (row, page) slots, for scoring and the EMA
+  const long long T = static_cast<long long>(rows) * n;
+  const long long s_beg = static_cast<long long>(blockIdx.x) * T / gridDim.x;
+  const long long s_end = static_cast<long long>(blockIdx.x + 1) * T / gridDim.x;
+  // the EMA update rides along with scoring when every share fits on chip and enough CTAs take the
+  // roles of phase 2; its writes wait for the second barrier (until then the old state is read)
+  const bool roles = static_cast<int>(gridDim.x) > 2 * rows;
+  const bool ema1 = roles && (T + gridDim.x - 1) / gridDim.x <= kEmaCap;
+  uint64_t* bars = reinterpret_cast<uint64_t*>(smem + lay.bar_off);  // [S] full, [S] empty
+  volatile int* stage_ok = reinterpret_cast<int*>(smem + lay.ctl_off);  // [S]: -1 none, 0, 1
+  volatile int* stage_pos = stage_ok + kPStages;
+  if (tid == 0) {
+    for (int s = 0; s < kPStages; ++s) {
+      mbar_init(smem_u32(&bars[s]), 1);
+      mbar_init(smem_u32(&bars[kPStages + s]), kPW);
+    }
+    fence_mbar_init();
+    s_abort = 0;
+    s_issued = 0;
+  }
+  __syncthreads();
+  const int n_items_total = rows * a.k_pred;
+  const int my_items = blockIdx.x < static_cast<unsigned>(n_items_total)
+                           ? (n_items_total - 1 - static_cast<int>(blockIdx.x)) / gridDim.x + 1
+                           : 0;
+
+  if (warp == kPW) {
+    // ---- TMA issue warp: the speculative pages of this CTA's items
+    if (lane == 0) {
+      prefetch_tensormap(&tmK);
+      prefetch_tensormap(&tmV);
+      for (int j = 0; j < my_items; ++j) {
+        const int it = blockIdx.x + j * gridDim.x;
+        const int row = it / a.k_pred, slot = it - row * a.k_pred;
+        const int b = row / kv.Hkv, h = row % kv.Hkv;
+        const int s = j % kPStages, u = j / kPStages;
+        if (u > 0 && !mbar_wait(smem_u32(&bars[kPStages + s]), (u - 1) & 1, abort_flag, kv.status))
+          break;
+        const int cnt = min(max(a.spec_count[row], 0), a.k_pred);
+        int okv = -1, pos = -1, phys = 0;
+        if (slot < cnt) {
+          pos = a.spec_idx[static_cast<size_t>(row) * a.k_pred + slot];
+          const int npos = (request_len(kv, b) + page - 1) / page;
+          okv = lookup_page(kv, b, pos, npos, &phys) ? 1 : 0;
+        }
+        const uint32_t full = smem_u32(&bars[s]);
+        stage_ok[s] = okv;
+        stage_pos[s] = pos;
+        if (okv == 1) {
+          const uint32_t dst = smem_base + s * stage_bytes;
+          const int row0 = (phys * kv.Hkv + h) * page;
+          mbar_arrive_expect_tx(full, stage_bytes);
+          tma_load_page(dst, &tmK, row0, full);
+          tma_load_page(dst + 2 * page * 128, &tmV, row0, full);
+        } else {
+          mbar_arrive(full);
+        }
+        *reinterpret_cast<volatile int*>(&s_issued) = j + 1;
+      }
+    }
+    __syncwarp();
+  } else {
+    // the first speculative item's query rows, fetched before scoring so they are on chip when the
+    // page lands (one 16-byte piece per thread: row tid / 16, dims 8 (tid % 16) ...)
+    uint4 q_first = make_uint4(0, 0, 0, 0);
+    if (my_items > 0 && (tid >> 4) < G) {
+      const int row = static_cast<int>(blockIdx.x) / a.k_pred;
+      const int b = row / kv.Hkv, h = row % kv.Hkv;
+      q_first = __ldg(reinterpret_cast<const uint4*>(
+          a.q + (static_cast<size_t>(b) * kv.Hq + h * G + (tid >> 4)) * kHeadDim + (tid & 15) * 8));
+    }
+    // ---- scoring: this CTA's equal share of the (row, page) slots
+    const int gl = lane & 7;
+    for (long long seg = s_beg; seg < s_end;) {
+      const int row = static_cast<int>(seg / n);
+      const int j0 = static_cast<int>(seg - static_cast<long long>(row) * n);
+      const int j1 = static_cast<int>(min(s_end - static_cast<long long>(row) * n,
+                                          static_cast<long long>(n)));
+      seg = static_cast<long long>(row) * n + j1;
+      const int b = row / kv.Hkv, h = row % kv.Hkv;
+      named_barrier(1, kPW * 32);  // qbar of the previous segment is no longer read
+      group_mean_query(a.q + (static_cast<size_t>(b) * kv.Hq + h * G) * kHeadDim, G, qbar, tid,
+                       kPW * 32);
+      named_barrier(1, kPW * 32);
+      float qv[16];
+      group_query_dims(qbar, gl, qv);
+      const int nl = (request_len(kv, b) + page - 1) / page;
+      const int32_t* table = kv.page_table + static_cast<size_t>(b) * kv.max_pages;
+      float* outs = a.scores + static_cast<size_t>(row) * n;
+      // T0: the k-th largest true score over P_t's pages.  At least k pages score >= T0, so the
+      // pages scoring >= T0 contain A_t: they are appended as candidates while scoring, and the
+      // selection after the barrier ranks only them (exactly).  No threshold (P_t has fewer than
+      // k scored pages) marks the row's list overflowed, and the selection scans every score.
+      const int cntP = min(max(a.spec_count[row], 0), a.k_pred);
+      const int32_t* P = a.spec_idx + static_cast<size_t>(row) * a.k_pred;
+      if (tid == 0) s_t0key = 0u;
+      for (int base = warp * 4; base < cntP; base += kPGroups) {
+        const int sl = base + (lane >> 3);
+        const int pos = sl < cntP ? P[sl] : -1;
+        const bool in = pos >= 0 && pos < nl;
+        const int phys = in ? table[pos] : 0;
+        const bool ok = in && phys >= 0 && phys < kv.num_phys;
+        uint4 rp[4];
+        if (ok) load_record(a.meta, static_cast<size_t>(phys) * kv.Hkv + h, gl, rp);
+        const float sp = group_sum(ok ? record_partial<DSA_META_MINMAX>(rp, qv) : 0.f);
+        if (gl == 0 && sl < cntP) spk[sl] = ok ? score_key(sp) : 0u;
+      }
+      named_barrier(1, kPW * 32);
+      // T0': the k_pred-th largest prediction over P_t's pages (from the old EMA state), a lower
+      // bound for the k_pred-th largest prediction of all pages: P_{t+1}'s candidates
+      if (ema1) {
+        if (tid == 0) s_t1key = 0u;
+        const float* ell_r = a.ell + static_cast<size_t>(row) * n;
+        const float* v_r = a.trend + static_cast<size_t>(row) * n;
+        for (int i = tid; i < cntP; i += kPW * 32) {
+          const int pp = P[i];
+          uint32_t key = 0u;
+          if (pp >= 0 && pp < n) {
+            float l_new, v_new;
+            const float is = spk[i] != 0u ? key_score(spk[i]) : -INFINITY;
+            ema_step(is, ell_r[pp], v_r[pp], DSA_EMA_UPDATE, a.alpha, a.beta, l_new, v_new);
+            key = score_key(ema_predict(l_new, v_new, a.gamma));
+          }
+          ppk[i] = key;
+        }
+        named_barrier(1, kPW * 32);
+        for (int i = tid; i < cntP; i += kPW * 32) {
+          const uint32_t ki = ppk[i];
+          if (ki == 0u) continue;
+          int ge = 0;
+          for (int j0 = 0; j0 < cntP; j0 += 8) {
+            uint32_t kj[8];
+#pragma unroll
+            for (int u = 0; u < 8; ++u) kj[u] = j0 + u < cntP ? ppk[j0 + u] : 0u;
+#pragma unroll
+            for (int u = 0; u < 8; ++u) ge += kj[u] >= ki;
+          }
+          if (ge >= a.k_pred) atomicMax(&s_t1key, ki);
+        }
+      }
+      for (int i = tid; i < cntP; i += kPW * 32) {
+        const uint32_t ki = spk[i];
+        if (ki == 0u) continue;
+        int ge = 0;
+        for (int j0 = 0; j0 < cntP; j0 += 8) {
+          uint32_t kj[8];
+#pragma unroll
+          for (int u = 0; u < 8; ++u) kj[u] = j0 + u < cntP ? spk[j0 + u] : 0u;
+#pragma unroll
+          for (int u = 0; u < 8; ++u) ge += kj[u] >= ki;
+        }
+        if (ge >= a.k) atomicMax(&s_t0key, ki);
+      }
+      named_barrier(1, kPW * 32);
+      const uint32_t t0key = s_t0key;
+      const uint32_t t1key = ema1 ? s_t1key : 0u;
+      if (tid == 0 && t0key == 0u) atomicAdd(a.cand_cnt + row, static_cast<unsigned>(kCandCap + 1));
+      if (tid == 0 && ema1 && t1key == 0u)
+        atomicAdd(a.cand_cnt2 + row, static_cast<unsigned>(kCandCap + 1));
+      // appends the lanes' candidates (lanes with gl == 0 hold a record's score) to a row's list:
+      // one counter update per warp
+      auto append = [&](unsigned* cnt, uint2* list, bool c, int j, uint32_t key) {
+        const unsigned bal = __ballot_sync(0xffffffffu, c);
+        if (bal == 0u) return;
+        unsigned base = 0;
+        if (lane == 0) base = atomicAdd(cnt + row, static_cast<unsigned>(__popc(bal)));
+        base = __shfl_sync(0xffffffffu, base, 0);
+        const unsigned at = base + __popc(bal & ((1u << lane) - 1u));
+        if (c && at < static_cast<unsigned>(kCandCap))
+          list[static_cast<size_t>(row) * kCandCap + at] = make_uint2(key, j);
+      };
+      const float* ell_r = a.ell + static_cast<size_t>(row) * n;
+      const float* v_r = a.trend + static_cast<size_t>(row) * n;
+      const long long stage0 = static_cast<long long>(row) * n - s_beg;  // staging index of j = 0
+      // the EMA update of page j with score s (staged until the second barrier); returns the key
+      // of the prediction
+      auto ema_page = [&](int j, float s, float l_old, float v_old) -> uint32_t {
+        float l_new, v_new;
+        ema_step(s, l_old, v_old, DSA_EMA_UPDATE, a.alpha, a.beta, l_new, v_new);
+        const float pr = ema_predict(l_new, v_new, a.gamma);
+        const int at = static_cast<int>(stage0 + j);
+        st_ell[at] = l_new;
+        st_v[at] = v_new;
+        st_pred[at] = pr;
+        return score_key(pr);
+      };
+      // warp-uniform loop: each group handles records jA and jA + kPGroups per round
+      for (int jbase = j0 + warp * 4; jbase < j1; jbase += 2 * kPGroups) {
+        const int jA = jbase + (lane >> 3);
+        const int jB = jA + kPGroups;
+        const bool inA = jA < j1 && jA < nl, inB = jB < j1 && jB < nl;
+        const int physA = inA ? table[jA] : 0;
+        const int physB = inB ? table[jB] : 0;
+        const bool okA = inA && physA >= 0 && physA < kv.num_phys;
+        const bool okB = inB && physB >= 0 && physB < kv.num_phys;
+        if (gl == 0 && ((inA && !okA) || (inB && !okB))) raise_status(kv.status, DSA_STATUS_BAD_PAGE);
+        uint4 ra[4], rb[4];
+        if (okA) load_record(a.meta, static_cast<size_t>(physA) * kv.Hkv + h, gl, ra);
+        if (okB) load_record(a.meta, static_cast<size_t>(physB) * kv.Hkv + h, gl, rb);
+        const bool emaA = ema1 && gl == 0 && jA < j1, emaB = ema1 && gl == 0 && jB < j1;
+        const float lA = emaA ? ell_r[jA] : 0.f, vA = emaA ? v_r[jA] : 0.f;
+        const float lB = emaB ? ell_r[jB] : 0.f, vB = emaB ? v_r[jB] : 0.f;
+        const float sA = group_sum(okA ? record_partial<DSA_META_MINMAX>(ra, qv) : 0.f);
+        const float sB = group_sum(okB ? record_partial<DSA_META_MINMAX>(rb, qv) : 0.f);
+        const float isA = okA ? sA : -INFINITY, isB = okB ? sB : -INFINITY;
+        if (gl == 0) {
+          if (jA < j1) outs[jA] = isA;
+          if (jB < j1) outs[jB] = isB;
+        }
+        const uint32_t kA = okA ? score_key(sA) : 0u, kB = okB ? score_key(sB) : 0u;
+        append(a.cand_cnt, a.cand, t0key != 0u && gl == 0 && jA < j1 && kA != 0u && kA >= t0key,
+               jA, kA);
+        append(a.cand_cnt, a.cand, t0key != 0u && gl == 0 && jB < j1 && kB != 0u && kB >= t0key,
+               jB, kB);
+        if (ema1) {
+          const uint32_t pA = emaA ? ema_page(jA, isA, lA, vA) : 0u;
+          const uint32_t pB = emaB ? ema_page(jB, isB, lB, vB) : 0u;
+          append(a.cand_cnt2, a.cand2, t1key != 0u && pA != 0u && pA >= t1key, jA, pA);
+          append(a.cand_cnt2, a.cand2, t1key != 0u && pB != 0u && pB >= t1key, jB, pB);
+        }
+      }
+    }
+
+    // ---- speculative per-page attention of this CTA's items
+    for (int j = 0; j < my_items; ++j) {
+      const int it = blockIdx.x + j * gridDim.x;
+      const int row = it / a.k_pred, slot = it - row * a.k_pred;
+      const int b = row / kv.Hkv, h = row % kv.Hkv;
+      const int L = request_len(kv, b);
+      const int s = j % kPStages;
+      named_barrier(1, kPW * 32);
+      {
+        const int r = tid >> 4, c = tid & 15;  // 256 consumer threads = 16 rows x 16 pieces
+        uint4 v = q_first;
+        if (j > 0)
+          v = r < G ? __ldg(reinterpret_cast<const uint4*>(
+                          a.q + (static_cast<size_t>(b) * kv.Hq + h * G + r) * kHeadDim + c * 8))
+                    : make_uint4(0, 0, 0, 0);
+        *reinterpret_cast<uint4*>(sQ + r * kQStride + c * 8) = v;
+      }
+      named_barrier(1, kPW * 32);
+      uint32_t qa[8][4];
+      load_q_frags(sQ, qa);
+      WarpSoftmaxState st;
+      state_init(st);
+      const bool got = mbar_wait(smem_u32(&bars[s]), (j / kPStages) & 1, abort_flag, kv.status);
+      const int okv = got ? stage_ok[s] : -1;
+      const int pos = stage_pos[s];
+      if (okv == 1) {
+        const uint32_t kb = smem_base + s * stage_bytes;
+        const uint32_t vb = kb + 2 * page * 128;
+        bool wrote = false;
+        for (int t = warp; t < tiles; t += kPW) {
+          const bool in = pos * page + t * 16 + (lane & 15) < L;
+          const uint32_t vm = __ballot_sync(0xffffffffu, in) & 0xffffu;
+          if (vm == 0u) continue;
+          if (vm != 0xffffu)
+            wrote |= zero_invalid_v_rows(vm, smem + s * stage_bytes + 2 * page * 128, page, t * 16);
+          float sc[2][4];
+          tile_scores(qa, kb, page, t * 16, sc);
+          tile_softmax_pv(st, sc, a.scale_log2, vm, vb, page, t * 16);
+        }
+        if (wrote) fence_proxy_async_smem();
+      }
+      __syncwarp();
+      if (got && lane == 0) mbar_arrive(smem_u32(&bars[kPStages + s]));
+      state_finish(st);
+      {
+        const int r0 = lane >> 2, c0 = (lane & 3) * 2;
+        float* wO = sO + warp * G * kHeadDim;
+#pragma unroll
+        for (int jj = 0; jj < 16; ++jj) {
+          if (r0 < G)
+            *reinterpret_cast<float2*>(wO + r0 * kHeadDim + jj * 8 + c0) =
+                make_float2(st.o[jj][0], st.o[jj][1]);
+          if (r0 + 8 < G)
+            *reinterpret_cast<float2*>(wO + (r0 + 8) * kHeadDim + jj * 8 + c0) =
+                make_float2(st.o[jj][2], st.o[jj][3]);
+        }
+        if ((lane & 3) == 0) {
+          if (r0 < G) {
+            sM[warp * G + r0] = st.m[0];
+            sL[warp * G + r0] = st.l[0];
+          }
+          if (r0 + 8 < G) {
+            sM[warp * G + r0 + 8] = st.m[1];
+            sL[warp * G + r0 + 8] = st.l[1];
+          }
+        }
+      }
+      // a wait that gave up in any consumer warp makes every warp skip the record (the OR over
+      // the barrier is the same in all of them), so the barrier inside stays uniform
+      const bool gave_up = named_barrier_or(1, kPW * 32, !got || *abort_flag);
+      if (okv >= 0 && !gave_up) {
+        float* rec0 = a.partials + (static_cast<size_t>(row) * a.k_pred + slot) * G * kRecordFloats;
+        if (okv == 0) {  // a position outside the request: the empty part
+          for (int g = tid; g < G; g += kPW * 32)
+            *reinterpret_cast<float4*>(rec0 + g * kRecordFloats + 128) =
+                make_float4(-INFINITY, 0.f, 0.f, 0.f);
+        } else {
+          // per head: the warps' weights exp(m_w - M) / l (one division each) and the record's
+          // (m, l); then O = sum_w weight_w O_w as float4 rows
+          const int nwu = min(tiles, kPW);  // warps that attended a tile
+          if (tid < G) {
+            const int g = tid;
+            float M = -INFINITY;
+            for (int w = 0; w < nwu; ++w) M = fmaxf(M, sM[w * G + g]);
+            float Lsum = 0.f;
+            for (int w = 0; w < nwu; ++w) {
+              const float mw = sM[w * G + g];
+              const float f = mw == -INFINITY ? 0.f : fast_exp2(mw - M);
+              wt[w * 16 + g] = f;
+              Lsum += sL[w * G + g] * f;
+            }
+            const float inv = Lsum > 0.f ? 1.f / Lsum : 0.f;
+            for (int w = 0; w < nwu; ++w) wt[w * 16 + g] *= inv;
+            *reinterpret_cast<float4*>(rec0 + g * kRecordFloats + 128) =
+                make_float4(M == -INFINITY ? -INFINITY : M * kLn2, Lsum, 0.f, 0.f);
+          }
+          named_barrier(1, kPW * 32);
+          for (int e = tid; e < G * 32; e += kPW * 32) {
+            const int g = e >> 5, d4 = e & 31;
+            float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
+            for (int w = 0; w < nwu; ++w) {
+              const float f = wt[w * 16 + g];
+              const float4 o = *reinterpret_cast<const float4*>(sO + (w * G + g) * kHeadDim + d4 * 4);
+              acc.x = fmaf(f, o.x, acc.x);
+              acc.y = fmaf(f, o.y, acc.y);
+              acc.z = fmaf(f, o.z, acc.z);
+              acc.w = fmaf(f, o.w, acc.w);
+            }
+            *reinterpret_cast<float4*>(rec0 + g * kRecordFloats + d4 * 4) = acc;
+          }
+        }
+      }
+    }
+  }
+  if (!grid_barrier(a.sync + 0, gridDim.x, abort_flag, kv.status)) {
+    // gave up: wait (bounded) for this CTA's page loads still in flight before exiting
+    if (tid == 0) {
+      const int n_iss = *reinterpret_cast<volatile int*>(&s_issued);
+      for (int j = max(0, n_iss - kPStages); j < n_iss; ++j) {
+        const unsigned long long t0 = global_timer_ns();
+        while (!mbar_try_wait(smem_u32(&bars[j % kPStages]), (j / kPStages) & 1))
+          if (global_timer_ns() - t0 > 50000000ull) break;
+      }
+    }
+    return;
+  }
+
+  // ================================================================ phase 2
+  // CTAs [0, rows) select A_t (phase 3 waits for them); CTAs [rows, 2 rows) update the EMA and
+  // select P_{t+1}, which only the next step reads: they arrive at the second barrier at once and
+  // run beside phase 3.  Rows are read as float4, four per thread in flight.
+  uint32_t* keys = reinterpret_cast<uint32_t*>(smem);
+  const bool vec4 = (n & 3) == 0 &&
+                    ((reinterpret_cast<uintptr_t>(a.scores) | reinterpret_cast<uintptr_t>(a.ell) |
+                      reinterpret_cast<uintptr_t>(a.trend) |
+                      reinterpret_cast<uintptr_t>(a.pred)) & 15) == 0;
+  // with more than 2 rows CTAs: CTA r < rows selects row r, CTA rows + r selects P_{t+1} of row r
+  // (and updates its EMA unless scoring did), the rest wait and repair; with fewer CTAs everyone
+  // selects, waits, then updates and repairs
+  auto select_into = [&](int kk, int32_t* out, int32_t* cnt, KeyStats st) {
+    __syncthreads();
+    const int total = select_topk_block<kPThreads>(keys, n, kk, out, sel_scratch, st);
+    if (tid == 0) *cnt = total;
+  };
+  // P_{t+1} = top-k_pred of the prediction.  Speculated like A_t: the k_pred-th largest predicted
+  // score over P_t's pages bounds it from below, so the pages predicted at or above that bound are
+  // collected while the EMA state is updated, and only they are ranked (the whole row falls back
+  // to the full selection when P_t has fewer than k_pred scored pages or too many pages pass).
+  TopkScratch& ts = sel_scratch.small;
+  unsigned* pkeys = reinterpret_cast<unsigned*>(ts.crank);  // predicted keys of P_t's pages
+  auto ema_row = [&](int row) {
+    const size_t base = static_cast<size_t>(row) * n;
+    KeyStats st;
+    __syncthreads();  // keys / scratch of a previous task are no longer read
+    const int cntP = min(max(a.spec_count[row], 0), a.k_pred);
+    const int32_t* P = a.spec_idx + static_cast<size_t>(row) * a.k_pred;
+    if (tid == 0) {
+      s_t0key = 0u;
+      ts.n_cand = 0;
+    }
+    for (int i = tid; i < cntP; i += kPThreads) {
+      const int p = P[i];
+      uint32_t key = 0u;
+      if (p >= 0 && p < n) {
+        float l_new, v_new;
+        ema_step(__ldcg(a.scores + base + p), a.ell[base + p], a.trend[base + p], DSA_EMA_UPDATE,
+                 a.alpha, a.beta, l_new, v_new);
+        key = score_key(ema_predict(l_new, v_new, a.gamma));
+      }
+      pkeys[i] = key;
+    }
+    __syncthreads();
+    for (int i = tid; i < cntP; i += kPThreads) {
+      const uint32_t ki = pkeys[i];
+      if (ki == 0u) continue;
+      int ge = 0;
+      for (int j0 = 0; j0 < cntP; j0 += 8) {
+        uint32_t kj[8];
+#pragma unroll
+        for (int u = 0; u < 8; ++u) kj[u] = j0 + u < cntP ? pkeys[j0 + u] : 0u;
+#pragma unroll
+        for (int u = 0; u < 8; ++u) ge += kj[u] >= ki;
+      }
+      if (ge >= a.k_pred) atomicMax(&s_t0key, ki);
+    }
+    __syncthreads();
+    const uint32_t t0 = s_t0key;
+    // predicted keys >= t0 become candidates (one shared counter update per warp)
+    auto collect = [&](int j, uint32_t key) {
+      const bool c = t0 != 0u && key != 0u && key >= t0;
+      const unsigned bal = __ballot_sync(0xffffffffu, c);
+      if (bal == 0u) return;
+      int at0 = 0;
+      if (lane == 0) at0 = atomicAdd(&ts.n_cand, __popc(bal));
+      at0 = __shfl_sync(0xffffffffu, at0, 0);
+      const int at = at0 + __popc(bal & ((1u << lane) - 1u));
+      if (c && at < kTopkMaxCand) {
+        ts.ckey[at] = key;
+        ts.cidx[at] = j;
+      }
+    };
+    if (vec4) {
+      const int n4 = n >> 2;
+      for (int i0 = tid; i0 < ((n4 + 31) & ~31); i0 += 2 * kPThreads) {
+        float4 is[2], lo[2], vo[2];
+#pragma unroll
+        for (int u = 0; u < 2; ++u) {
+          const int i = i0 + u * kPThreads;
+          if (i < n4) {
+            is[u] = __ldcg(reinterpret_cast<const float4*>(a.scores + base) + i);
+            lo[u] = *(reinterpret_cast<const float4*>(a.ell + base) + i);
+            vo[u] = *(reinterpret_cast<const float4*>(a.trend + base) + i);
+          }
+        }
+#pragma unroll
+        for (int u = 0; u < 2; ++u) {
+          const int i = i0 + u * kPThreads;
+          uint32_t kq[4] = {0u, 0u, 0u, 0u};
+          if (i < n4) {
+            float4 ln, vn, pr;
+            ema_step(is[u].x, lo[u].x, vo[u].x, DSA_EMA_UPDATE, a.alpha, a.beta, ln.x, vn.x);
+            ema_step(is[u].y, lo[u].y, vo[u].y, DSA_EMA_UPDATE, a.alpha, a.beta, ln.y, vn.y);
+            ema_step(is[u].z, lo[u].z, vo[u].z, DSA_EMA_UPDATE, a.alpha, a.beta, ln.z, vn.z);
+            ema_step(is[u].w, lo[u].w, vo[u].w, DSA_EMA_UPDATE, a.alpha, a.beta, ln.w, vn.w);
+            pr.x = ema_predict(ln.x, vn.x, a.gamma);
+            pr.y = ema_predict(ln.y, vn.y, a.gamma);
+            pr.z = ema_predict(ln.z, vn.z, a.gamma);
+            pr.w = ema_predict(ln.w, vn.w, a.gamma);
+            *(reinterpret_cast<float4*>(a.ell + base) + i) = ln;
+            *(reinterpret_cast<float4*>(a.trend + base) + i) = vn;
+            if (a.pred) *(reinterpret_cast<float4*>(a.pred + base) + i) = pr;
+            kq[0] = score_key(pr.x);
+            kq[1] = score_key(pr.y);
+            kq[2] = score_key(pr.z);
+            kq[3] = score_key(pr.w);
+#pragma unroll
+            for (int e = 0; e < 4; ++e) {
+              keys[4 * i + e] = kq[e];
+              st.add(kq[e]);
+            }
+          }
+#pragma unroll
+          for (int e = 0; e < 4; ++e) collect(4 * i + e, kq[e]);
+        }
+      }
+    } else {
+      for (int j0 = tid; j0 < ((n + 31) & ~31); j0 += kPThreads) {
+        uint32_t key = 0u;
+        if (j0 < n) {
+          float l_new, v_new;
+          ema_step(__ldcg(a.scores + base + j0), a.ell[base + j0], a.trend[base + j0],
+                   DSA_EMA_UPDATE, a.alpha, a.beta, l_new, v_new);
+          a.ell[base + j0] = l_new;
+          a.trend[base + j0] = v_new;
+          const float p = ema_predict(l_new, v_new, a.gamma);
+          if (a.pred) a.pred[base + j0] = p;
+          key = score_key(p);
+          keys[j0] = key;
+          st.add(key);
+        }
+        collect(j0, key);
+      }
+    }
+    __syncthreads();
+    int32_t* out = a.next_idx + static_cast<size_t>(row) * a.k_pred;
+    const int C = ts.n_cand;
+    if (t0 != 0u && C <= kTopkMaxCand) {
+      const int total = topk_candidates<kPThreads>(C, a.k_pred, n, out, ts);
+      for (int i = total + tid; i < a.k_pred; i += kPThreads) out[i] = -1;
+      if (tid == 0) a.next_count[row] = total;
+    } else {
+      select_into(a.k_pred, out, a.next_count + row, st);
+    }
+  };
+  auto select_row = [&](int row) {
+    const size_t base = static_cast<size_t>(row) * n;
+    KeyStats st;
+    __syncthreads();  // keys of a previous task are no longer read
+    const unsigned C = __ldcg(a.cand_cnt + row);
+    if (C <= static_cast<unsigned>(kCandCap)) {
+      const uint2* cr = a.cand + static_cast<size_t>(row) * kCandCap;
+      for (int i = tid; i < static_cast<int>(C); i += kPThreads) {
+        const uint2 e = __ldcg(cr + i);
+        sel_scratch.small.ckey[i] = e.x;
+        sel_scratch.small.cidx[i] = static_cast<int>(e.y);
+      }
+      __syncthreads();
+      int32_t* out = a.idx + static_cast<size_t>(row) * a.k;
+      const int total =
+          topk_candidates<kPThreads>(static_cast<int>(C), a.k, n, out, sel_scratch.small);
+      for (int i = total + tid; i < a.k; i += kPThreads) out[i] = -1;
+      if (tid == 0) a.count[row] = total;
+      return;
+    }
+    if (vec4) {
+      const int n4 = n >> 2;
+      for (int i0 = tid; i0 < n4; i0 += 8 * kPThreads) {
+        float4 v[8];
+#pragma unroll
+        for (int u = 0; u < 8; ++u) {
+          const int i = i0 + u * kPThreads;
+          if (i < n4) v[u] = __ldcg(reinterpret_cast<const float4*>(a.scores + base) + i);
+        }
+#pragma unroll
+        for (int u = 0; u < 8; ++u) {
+          const int i = i0 + u * kPThreads;
+          if (i >= n4) continue;
+          keys[4 * i + 0] = score_key(v[u].x);
+          keys[4 * i + 1] = score_key(v[u].y);
+          keys[4 * i + 2] = score_key(v[u].z);
+          keys[4 * i + 3] = score_key(v[u].w);
+          st.add(keys[4 * i + 0]);
+          st.add(keys[4 * i + 1]);
+          st.add(keys[4 * i + 2]);
+          st.add(keys[4 * i + 3]);
+        }
+      }
+    } else {
+      for (int j = tid; j < n; j += kPThreads) {
+        keys[j] = score_key(__ldcg(a.scores + base + j));
+        st.add(keys[j]);
+      }
+    }
+    select_into(a.k, a.idx + static_cast<size_t>(row) * a.k, a.count + row, st);
+  };
+  // P_{t+1} of a row whose EMA update rode along with scoring: rank the candidates, or (no
+  // bound, or too many candidates) recompute the row's predictions from the old state, which is
+  // only overwritten after the second barrier, and select from all of them
+  auto next_row = [&](int row) {
+    const size_t base = static_cast<size_t>(row) * n;
+    __syncthreads();  // keys / scratch of a previous task are no longer read
+    int32_t* out = a.next_idx + static_cast<size_t>(row) * a.k_pred;
+    const unsigned C = __ldcg(a.cand_cnt2 + row);
+    if (C <= static_cast<unsigned>(kCandCap)) {
+      const uint2* cr = a.cand2 + static_cast<size_t>(row) * kCandCap;
+      for (int i = tid; i < static_cast<int>(C); i += kPThreads) {
+        const uint2 e = __ldcg(cr + i);
+        ts.ckey[i] = e.x;
+        ts.cidx[i] = static_cast<int>(e.y);
+      }
+      __syncthreads();
+      const int total = topk_candidates<kPThreads>(static_cast<int>(C), a.k_pred, n, out, ts);
+      for (int i = total + tid; i < a.k_pred; i += kPThreads) out[i] = -1;
+      if (tid == 0) a.next_count[row] = total;
+      return;
+    }
+    KeyStats st;
+    for (int j = tid; j < n; j += kPThreads) {
+      float l_new, v_new;
+      ema_step(__ldcg(a.scores + base + j), a.ell[base + j], a.trend[base + j], DSA_EMA_UPDATE,
+               a.alpha, a.beta, l_new, v_new);
+      keys[j] = score_key(ema_predict(l_new, v_new, a.gamma));
+      st.add(keys[j]);
+    }
+    select_into(a.k_pred, out, a.next_count + row, st);
+  };
+  if (ema1) {
+    if (static_cast<int>(blockIdx.x) < rows) select_row(blockIdx.x);
+    else if (static_cast<int>(blockIdx.x) < 2 * rows) next_row(blockIdx.x - rows);
+    if (!grid_barrier(a.sync + 1, gridDim.x, abort_flag, kv.status)) return;
+    // the staged EMA updates of this CTA's share (every read of the old state is behind us)
+    const int cnt = static_cast<int>(s_end - s_beg);
+    for (int i = tid; i < cnt; i += kPThreads) {
+      a.ell[s_beg + i] = st_ell[i];
+      a.trend[s_beg + i] = st_v[i];
+      if (a.pred) a.pred[s_beg + i] = st_pred[i];
+    }
+  } else if (roles) {
+    if (static_cast<int>(blockIdx.x) < rows) {
+      select_row(blockIdx.x);
+      grid_arrive(a.sync + 1, abort_flag);
+    } else if (static_cast<int>(blockIdx.x) < 2 * rows) {
+      grid_arrive(a.sync + 1, abort_flag);
+      ema_row(blockIdx.x - rows);
+    } else if (!grid_barrier(a.sync + 1, gridDim.x, abort_flag, kv.status)) {
+      return;
+    }
+  } else {
+    for (int row = blockIdx.x; row < rows; row += gridDim.x) select_row(row);
+    if (!grid_barrier(a.sync + 1, gridDim.x, abort_flag, kv.status)) return;
+    for (int row = blockIdx.x; row < rows; row += gridDim.x) ema_row(row);
+  }
+
+  // ================================================================ phase 3
+  int32_t* sP = reinterpret_cast<int32_t*>(smem + lay.sp_off);
+  int32_t* sA = reinterpret_cast<int32_t*>(smem + lay.sa_off);
+  int2* list = reinterpret_cast<int2*>(smem + lay.list_off);         // missed (phys, pos)
+  int32_t* parts = reinterpret_cast<int32_t*>(smem + lay.part_off);  // merged P slots
+  float* pm = reinterpret_cast<float*>(smem + lay.pm_off);           // their m (log2 units)
+  float* pl = reinterpret_cast<float*>(smem + lay.pl_off);           // their l, then weight
+  float* qh = reinterpret_cast<float*>(smem + lay.qh_off);
+  float* wst = reinterpret_cast<float*>(smem + lay.ws_off);  // [warp][m, l, -, -, O[128]]
+  float* wf = reinterpret_cast<float*>(smem + lay.wf_off);   // [warp] state weights
+  float* s_acc = reinterpret_cast<float*>(smem + lay.acc_off);
+  constexpr int kWs = kHeadDim + 4;
+  const int rep_first = roles ? static_cast<int>(blockIdx.x) - 2 * rows : blockIdx.x;
+  const int rep_step = roles ? static_cast<int>(gridDim.x) - 2 * rows : gridDim.x;
+  for (int task = rep_first; task >= 0 && task < rows * G; task += rep_step) {
+    const int row = task / G, g = task - row * G;
+    const int b = row / kv.Hkv, h = row % kv.Hkv;
+    const int L = request_len(kv, b);
+    const int npos = (L + page - 1) / page;
+    const size_t qhead = static_cast<size_t>(b) * kv.Hq + static_cast<size_t>(h) * G + g;
+    __syncthreads();  // shared lists of a previous task are no longer read
+    const int cntA = min(max(__ldcg(a.count + row), 0), a.k);
+    const int cntP = min(max(a.spec_count[row], 0), a.k_pred);
+    for (int i = tid; i < cntA; i += kPThreads)
+      sA[i] = __ldcg(a.idx + static_cast<size_t>(row) * a.k + i);
+    for (int i = tid; i < cntP; i += kPThreads)
+      sP[i] = a.spec_idx[static_cast<size_t>(row) * a.k_pred + i];
+    for (int d = tid; d < kHeadDim; d += kPThreads)
+      qh[d] = __bfloat162float(a.q[qhead * kHeadDim + d]) * a.scale_log2;
+    __syncthreads();
+    // merged speculative parts: P slots whose page is in A (every slot in superset mode)
+    int n_parts = 0;
+    for (int base = 0; base < cntP; base += kPThreads) {
+      const int i = base + tid;
+      const bool take = i < cntP && (a.superset || contains_sorted(sA, cntA, sP[i]));
+      int tot;
+      const int at = block_exclusive_scan(take ? 1 : 0, s_red, &tot);
+      if (take) parts[n_parts + at] = i;
+      n_parts += tot;
+    }
+    // missed pages A \ P inside the request with a valid page-table entry
+    int n_miss = 0;
+    for (int base = 0; base < cntA; base += kPThreads) {
+      const int i = base + tid;
+      int phys = 0, pos = -1;
+      bool miss = false;
+      if (i < cntA) {
+        pos = sA[i];
+        miss = !contains_sorted(sP, cntP, pos) && lookup_page(kv, b, pos, npos, &phys);
+      }
+      int tot;
+      const int at = block_exclusive_scan(miss ? 1 : 0, s_red, &tot);
+      if (miss) list[n_miss + at] = make_int2(phys, pos);
+      n_miss += tot;
+    }
+    __syncthreads();
+
+    // ---- attention of query head g over the missed tokens: 32 tokens per warp round (lane =
+    // token for q.k, lane = 4 dims for p.v), online softmax in log2 units per warp
+    const int cpp = (page + 31) / 32;  // 32-token chunks per page
+    float wm = -INFINITY, wl = 0.f;
+    float4 wo = make_float4(0.f, 0.f, 0.f, 0.f);
+    for (int c = warp; c < n_miss * cpp; c += kPWarps) {
+      const int pi = c / cpp, sub = c - pi * cpp;
+      const int phys = list[pi].x, pos = list[pi].y;
+      const int t0 = sub * 32;  // first slot of the chunk within the page
+      const int nvalid = max(0, min(min(32, page - t0), L - (pos * page + t0)));
+      const size_t row0 = (static_cast<size_t>(phys) * kv.Hkv + h) * page + t0;
+      float s = -INFINITY;
+      if (lane < nvalid) {
+        const uint4* kr = reinterpret_cast<const uint4*>(a.kpool + (row0 + lane) * kHeadDim);
+        float acc = 0.f;
+#pragma unroll
+        for (int h8 = 0; h8 < 2; ++h8) {
+          uint4 raw[8];
+#pragma unroll
+          for (int c8 = 0; c8 < 8; ++c8) raw[c8] = __ldg(kr + h8 * 8 + c8);
+#pragma unroll
+          for (int c8 = 0; c8 < 8; ++c8) {
+            const __nv_bfloat16* v = reinterpret_cast<const __nv_bfloat16*>(&raw[c8]);
+#pragma unroll
+            for (int e = 0; e < 8; ++e)
+              acc = fmaf(qh[(h8 * 8 + c8) * 8 + e], __bfloat162float(v[e]), acc);
+          }
+        }
+        s = acc;
+      }
+      const float cmax = warp_max(s);
+      if (cmax == -INFINITY) continue;
+      const float mnew = fmaxf(wm, cmax);
+      const float alpha = wm == -INFINITY ? 0.f : fast_exp2(wm - mnew);
+      const float p = lane < nvalid ? fast_exp2(s - mnew) : 0.f;
+      wl = wl * alpha + warp_sum(p);
+      wo.x *= alpha;
+      wo.y *= alpha;
+      wo.z *= alpha;
+      wo.w *= alpha;
+      wm = mnew;
+      const __nv_bfloat16* vrow = a.vpool + row0 * kHeadDim + lane * 4;
+      for (int t0 = 0; t0 < nvalid; t0 += 8) {  // eight V rows in flight
+        uint2 raw[8];
+#pragma unroll
+        for (int u = 0; u < 8; ++u)
+          raw[u] = t0 + u < nvalid ? __ldg(reinterpret_cast<const uint2*>(
+                                         vrow + static_cast<size_t>(t0 + u) * kHeadDim))
+                                   : make_uint2(0u, 0u);
+#pragma unroll
+        for (int u = 0; u < 8; ++u) {
+          const float pt = __shfl_sync(0xffffffffu, p, (t0 + u) & 31);
+          const __nv_bfloat16* v = reinterpret_cast<const __nv_bfloat16*>(&raw[u]);
+          wo.x = fmaf(pt, __bfloat162float(v[0]), wo.x);
+          wo.y = fmaf(pt, __bfloat162float(v[1]), wo.y);
+          wo.z = fmaf(pt, __bfloat162float(v[2]), wo.z);
+          wo.w = fmaf(pt, __bfloat162float(v[3]), wo.w);
+        }
+      }
+    }
+    if (lane == 0) {
+      wst[warp * kWs] = wm;
+      wst[warp * kWs + 1] = wl;
+    }
+    *reinterpret_cast<float4*>(wst + warp * kWs + 4 + lane * 4) = wo;
+    // ---- merge the warps' missed states (log2 units) with the speculative records (natural m)
+    float mloc = -INFINITY;
+    for (int i = tid; i < n_parts; i += kPThreads) {
+      const float* r =
+          a.partials + ((static_cast<size_t>(row) * a.k_pred + parts[i]) * G + g) * kRecordFloats;
+      const float lp = __ldcg(r + 129), mp = __ldcg(r + 128) * kLog2e;
+      pm[i] = mp;
+      pl[i] = lp;
+      if (lp > 0.f) mloc = fmaxf(mloc, mp);
+    }
+    if (lane == 0 && wl > 0.f) mloc = fmaxf(mloc, wm);
+    mloc = warp_max(mloc);
+    if (lane == 0) s_f[warp] = mloc;
+    __syncthreads();
+    float M = -INFINITY;
+#pragma unroll
+    for (int w = 0; w < kPWarps; ++w) M = fmaxf(M, s_f[w]);
+    __syncthreads();  // s_f is reused below
+    float lsum = 0.f;
+    for (int i = tid; i < n_parts; i += kPThreads) {
+      const float wgt = pl[i] > 0.f ? pl[i] * fast_exp2(pm[i] - M) : 0.f;
+      pl[i] = wgt;
+      lsum += wgt;
+    }
+    if (lane == 0) {
+      const float f = wl > 0.f ? fast_exp2(wm - M) : 0.f;
+      wf[warp] = f;
+      lsum += wl * f;
+    }
+    lsum = warp_sum(lsum);
+    if (lane == 0) s_f[warp] = lsum;
+    __syncthreads();
+    float Lsum = 0.f;
+#pragma unroll
+    for (int w = 0; w < kPWarps; ++w) Lsum += s_f[w];
+    // weighted sum: warp w takes its own missed state and parts w, w + 9, ...; lane = 4 dims
+    float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
+    {
+      const float f = wf[warp];
+      if (f > 0.f) {
+        acc.x = f * wo.x;
+        acc.y = f * wo.y;
+        acc.z = f * wo.z;
+        acc.w = f * wo.w;
+      }
+    }
+    for (int i0 = warp; i0 < n_parts; i0 += 4 * kPWarps) {
+      float4 v[4];
+      float wv[4];
+#pragma unroll
+      for (int u = 0; u < 4; ++u) {
+        const int i = i0 + u * kPWarps;
+        wv[u] = i < n_parts ? pl[i] : 0.f;
+        v[u] = wv[u] > 0.f
+                   ? __ldcg(reinterpret_cast<const float4*>(
+                                a.partials + ((static_cast<size_t>(row) * a.k_pred + parts[i]) * G + g) *
+                                                 kRecordFloats) +
+                            lane)
+                   : make_float4(0.f, 0.f, 0.f, 0.f);
+      }
+#pragma unroll
+      for (int u = 0; u < 4; ++u) {
+        acc.x += wv[u] * v[u].x;
+        acc.y += wv[u] * v[u].y;
+        acc.z += wv[u] * v[u].z;
+        acc.w += wv[u] * v[u].w;
+      }
+    }
+    *reinterpret_cast<float4*>(s_acc + warp * kHeadDim + lane * 4) = acc;
+    __syncthreads();
+    if (tid < kHeadDim) {
+      float o = 0.f;
+#pragma unroll
+      for (int w = 0; w < kPWarps; ++w) o += s_acc[w * kHeadDim + tid];
+      a.out[qhead * kHeadDim + tid] = Lsum > 0.f ? o / Lsum : 0.f;
+    }
+    if (tid == 0) {
+      a.m[qhead] = Lsum > 0.f ? M * kLn2 : -INFINITY;
+      a.l[qhead] = Lsum;
+    }
+  }
+
+  // ---- the last CTA out resets the barrier counters for the next call
+  __syncthreads();
+  if (tid == 0) {
+    __threadfence();
+    if (atomicAdd(a.sync + 2, 1u) == gridDim.x - 1) {
+      for (int r = 0; r < rows; ++r) {
+        a.cand_cnt[r] = 0u;
+        a.cand_cnt2[r] = 0u;
+      }
+      a.sync[0] = 0u;
+      a.sync[1] = 0u;
+      a.sync[2] = 0u;
+      __threadfence();
+    }
+  }
+}
+
+}  // namespace
+
+size_t prr_step_workspace_bytes(int rows) {
+  const size_t cnt = (4 * static_cast<size_t>(rows) + 15) & ~static_cast<size_t>(15);
+  const size_t list = static_cast<size_t>(rows) * kCandCap * sizeof(uint2);
+  return 256 + 2 * (cnt + list);
+}
+
+size_t prr_step_smem_bytes(int page, int G, int n, int k, int k_pred) {
+  return playout(page, G, n, k, k_pred).total;
+}
+
+cudaError_t launch_prr_step(const CUtensorMap& tmK, const CUtensorMap& tmV, const PrrStepArgs& s,
+                            cudaStream_t stream) {
+  PrrArgs a;
+  a.kv = s.kv;
+  a.kpool = s.kpool;
+  a.vpool = s.vpool;
+  a.q = s.q;
+  a.meta = s.meta;
+  a.scores = s.scores;
+  a.stride = s.stride;
+  a.ell = s.ell;
+  a.trend = s.trend;
+  a.alpha = s.alpha;
+  a.beta = s.beta;
+  a.gamma = s.gamma;
+  a.pred = s.pred;
+  a.spec_idx = s.spec_idx;
+  a.spec_count = s.spec_count;
+  a.k_pred = s.k_pred;
+  a.partials = s.partials;
+  a.idx = s.idx;
+  a.count = s.count;
+  a.k = s.k;
+  a.next_idx = s.next_idx;
+  a.next_count = s.next_count;
+  a.superset = s.superset;
+  a.scale_log2 = s.scale_log2;
+  a.out = s.out;
+  a.m = s.m;
+  a.l = s.l;
+  a.sync = s.sync;
+  a.cand_cnt = s.cand_cnt;
+  a.cand = s.cand;
+  a.cand_cnt2 = s.cand_cnt2;
+  a.cand2 = s.cand2;
+  const size_t bytes = playout(s.kv.p, s.kv.G, s.stride, s.k, s.k_pred).total;
+  cudaError_t e = ensure_dynamic_smem(reinterpret_cast<const void*>(prr_step_kernel), bytes);
+  if (e != cudaSuccess) return e;
+  int dev = 0, sms = 0, per_sm = 0;
+  if ((e = cudaGetDevice(&dev)) != cudaSuccess) return e;
+  if ((e = cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev)) != cudaSuccess)
+    return e;
+  if ((e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, prr_step_kernel, kPThreads,
+                                                         bytes)) != cudaSuccess)
+    return e;
+  if (per_sm < 1) return cudaErrorInvalidConfiguration;
+  // every CTA must be resident at once (the phases wait on each other): a cooperative launch
+  // of one CTA per SM
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3(sms);
+  cfg.blockDim = dim3(kPThreads);
+  cfg.dynamicSmemBytes = bytes;
+  cfg.stream = stream;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeCooperative;
+  attr[0].val.cooperative = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  return cudaLaunchKernelEx(&cfg, prr_step_kernel, tmK, tmV, a);
+}
+
+}  // namespace dsa

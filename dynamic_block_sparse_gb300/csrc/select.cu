@@ -1,6 +1,7 @@
 // Top-K / hierarchical page selection and the PRR EMA predictor with speculative-set selection.
 // One CTA per (request, KV head) row; the row's keys live in shared memory.
 #include "internal.h"
+#include "score_core.cuh"
 #include "select.cuh"
 
 namespace dsa {
@@ -29,13 +30,18 @@ __global__ void __launch_bounds__(kSelectThreads)
     select_kernel(const float* __restrict__ scores, int n_logical, int stride, int g, int k,
                   int32_t* __restrict__ idx, int idx_stride, int32_t* __restrict__ count) {
   extern __shared__ uint32_t keys[];
-  __shared__ SelectScratch<kSelectThreads> sh;
+  __shared__ SelectAnyScratch<kSelectThreads> sh;
   const int row = blockIdx.x;
   const int n = (n_logical + g - 1) / g;
   const float* s = scores + static_cast<size_t>(row) * stride;
+  KeyStats st;
   if (g == 1) {
     const bool vec4 = (stride & 3) == 0 && (reinterpret_cast<uintptr_t>(scores) & 15) == 0;
-    for_each_row_value(s, n, vec4, [&](int j, float x) { keys[j] = score_key(x); });
+    for_each_row_value(s, n, vec4, [&](int j, float x) {
+      const uint32_t key = score_key(x);
+      keys[j] = key;
+      st.add(key);
+    });
   } else {
     for (int j = threadIdx.x; j < n; j += kSelectThreads) {
       float best = -INFINITY;
@@ -44,13 +50,12 @@ __global__ void __launch_bounds__(kSelectThreads)
         if (jj < n_logical) best = fmaxf(best, s[jj]);  // fmaxf drops NaN
       }
       keys[j] = score_key(best);
+      st.add(keys[j]);
     }
   }
   __syncthreads();
-  const Selection sel = radix_select<kSelectThreads>(keys, n, k, sh);
   int32_t* out = idx + static_cast<size_t>(row) * idx_stride;
-  const int total = compact_ascending<kSelectThreads>(keys, n, sel, out, sh);
-  for (int i = total + threadIdx.x; i < k; i += kSelectThreads) out[i] = -1;
+  const int total = select_topk_block<kSelectThreads>(keys, n, k, out, sh, st);
   if (threadIdx.x == 0) count[row] = total;
 }
 
@@ -60,20 +65,12 @@ __global__ void __launch_bounds__(kSelectThreads)
                float* __restrict__ pred, int k_pred, int32_t* __restrict__ pred_idx,
                int pred_idx_stride, int32_t* __restrict__ pred_count) {
   extern __shared__ uint32_t keys[];
-  __shared__ SelectScratch<kSelectThreads> sh;
+  __shared__ SelectAnyScratch<kSelectThreads> sh;
   const int row = blockIdx.x;
   const size_t base = static_cast<size_t>(row) * stride;
+  KeyStats st;
   auto update = [&](float is, float l_old, float v_old, float& l_new, float& v_new) {
-    l_new = -INFINITY;
-    v_new = 0.f;
-    if (is > -INFINITY) {
-      if (mode == DSA_EMA_INIT || !(l_old > -INFINITY)) {
-        l_new = is;  // no history yet: start from the observed score with zero trend
-      } else {
-        v_new = beta * (is - l_old) + (1.f - beta) * v_old;
-        l_new = alpha * is + (1.f - alpha) * l_old;
-      }
-    }
+    ema_step(is, l_old, v_old, mode, alpha, beta, l_new, v_new);
   };
   const bool vec4 = (stride & 3) == 0 && (n & 3) == 0 &&
                     ((reinterpret_cast<uintptr_t>(IS) | reinterpret_cast<uintptr_t>(ell) |
@@ -92,10 +89,10 @@ __global__ void __launch_bounds__(kSelectThreads)
       update(is.y, lo.y, vo.y, ln.y, vn.y);
       update(is.z, lo.z, vo.z, ln.z, vn.z);
       update(is.w, lo.w, vo.w, ln.w, vn.w);
-      pr.x = ln.x > -INFINITY ? ln.x + gamma * vn.x : -INFINITY;
-      pr.y = ln.y > -INFINITY ? ln.y + gamma * vn.y : -INFINITY;
-      pr.z = ln.z > -INFINITY ? ln.z + gamma * vn.z : -INFINITY;
-      pr.w = ln.w > -INFINITY ? ln.w + gamma * vn.w : -INFINITY;
+      pr.x = ema_predict(ln.x, vn.x, gamma);
+      pr.y = ema_predict(ln.y, vn.y, gamma);
+      pr.z = ema_predict(ln.z, vn.z, gamma);
+      pr.w = ema_predict(ln.w, vn.w, gamma);
       *reinterpret_cast<float4*>(ell + o) = ln;
       *reinterpret_cast<float4*>(v + o) = vn;
       if (pred) *reinterpret_cast<float4*>(pred + o) = pr;
@@ -103,6 +100,10 @@ __global__ void __launch_bounds__(kSelectThreads)
       keys[j4 * 4 + 1] = score_key(pr.y);
       keys[j4 * 4 + 2] = score_key(pr.z);
       keys[j4 * 4 + 3] = score_key(pr.w);
+      st.add(keys[j4 * 4 + 0]);
+      st.add(keys[j4 * 4 + 1]);
+      st.add(keys[j4 * 4 + 2]);
+      st.add(keys[j4 * 4 + 3]);
     }
   } else {
     for (int j = threadIdx.x; j < n; j += kSelectThreads) {
@@ -112,17 +113,16 @@ __global__ void __launch_bounds__(kSelectThreads)
       update(IS[base + j], l_old, v_old, l_new, v_new);
       ell[base + j] = l_new;
       v[base + j] = v_new;
-      const float p = l_new > -INFINITY ? l_new + gamma * v_new : -INFINITY;
+      const float p = ema_predict(l_new, v_new, gamma);
       if (pred) pred[base + j] = p;
       keys[j] = score_key(p);
+      st.add(keys[j]);
     }
   }
   if (k_pred <= 0 || pred_idx == nullptr) return;
   __syncthreads();
-  const Selection sel = radix_select<kSelectThreads>(keys, n, k_pred, sh);
   int32_t* out = pred_idx + static_cast<size_t>(row) * pred_idx_stride;
-  const int total = compact_ascending<kSelectThreads>(keys, n, sel, out, sh);
-  for (int i = total + threadIdx.x; i < k_pred; i += kSelectThreads) out[i] = -1;
+  const int total = select_topk_block<kSelectThreads>(keys, n, k_pred, out, sh, st);
   if (threadIdx.x == 0) pred_count[row] = total;
 }
 

@@ -174,16 +174,18 @@ class ThresholdDecoder:
 class PRRDecoder:
     """Predict, reuse and repair over top-K block selection (PRR §3.1-§3.4, fixed budget).
 
-    Step t (t >= 1) runs on three streams: the speculative pass over P_t on ``side``; scoring,
-    top-K selection of the true set A_t and the repair/merge on the caller's stream; and the EMA
-    update (which needs only this step's scores) on ``ema_stream``, writing P_{t+1} into the other
-    half of a double-buffered list so that it never races the readers of P_t.  The step ends with
-    every stream joined back to the caller's stream.
+    With ``fused`` (the default) step t >= 1 is one ``dsa_prr_step`` launch: speculation over P_t
+    beside scoring, then top-K selection of the true set A_t beside the EMA update that selects
+    P_{t+1}, then repair and merge, all separated by on-device grid barriers.  Otherwise the same
+    library calls run as separate launches on three streams: the speculative pass over P_t on
+    ``side``; scoring, top-K selection and the repair/merge on the caller's stream; the EMA update
+    (which needs only this step's scores) on ``ema_stream``.  Either way P_{t+1} goes into the
+    other half of a double-buffered list so that it never races the readers of P_t.
     """
 
     def __init__(self, cache: Cache, k: int, k_pred: int, alpha: float, beta: float,
                  gamma: float, superset: bool = False, scale: float | None = None,
-                 two_streams: bool = True):
+                 two_streams: bool = True, fused: bool = True):
         c = cache
         self.cache, self.k, self.k_pred = c, k, k_pred
         self.alpha, self.beta, self.gamma = alpha, beta, gamma
@@ -211,6 +213,11 @@ class PRRDecoder:
         self.workspace = torch.empty(max(16, ws), dtype=torch.uint8, device=dev)
         self.side = torch.cuda.Stream(device=dev) if two_streams else None
         self.ema_stream = torch.cuda.Stream(device=dev) if two_streams else None
+        self.fused = fused
+        # the fused step's barrier words and candidate counts: zero before the first call, left
+        # zero by each call
+        self.step_workspace = torch.zeros(B.dsa_prr_step_workspace_size(c.kv), dtype=torch.uint8,
+                                          device=dev)
         self.t = 0
 
     @property
@@ -259,6 +266,13 @@ class PRRDecoder:
             B.dsa_sparse_decode_attn(c.kv, q, self.idx, self.count, self.scale, self.out, self.m,
                                      self.l, workspace=self.workspace, stream=main)
             self.stage_ema(B.DSA_EMA_INIT, nxt, main)
+        elif self.fused:
+            B.dsa_prr_step(c.kv, q, self.meta, self.scores, self.ell, self.trend, self.alpha,
+                           self.beta, self.gamma, self.spec_bufs[cur], self.spec_counts[cur],
+                           self.partials, self.idx, self.count, self.spec_bufs[nxt],
+                           self.spec_counts[nxt], self.scale, self.out, self.m, self.l,
+                           self.step_workspace, pred=self.pred, superset=self.superset,
+                           stream=main)
         elif self.side is None:
             self.stage_score(q, main)
             self.stage_select(main)

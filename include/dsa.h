@@ -179,8 +179,9 @@ int dsa_select_threshold(const dsa_paged_kv* kv, const void* q, const float* sco
  *   page_partials: NULL, or fp32 [B][Hkv][idx_stride][G][D + 4]: for selected slot i the partial
  *                  record (O_0..O_{D-1}, m, l, 0, 0) of attention over that page alone (the
  *                  per-page partials PRR's exact repair merges).  Slots >= count are not written.
- *   num_splits   : 0 (default) = one persistent launch: every row's pages are cut into chunks,
- *                  one per resident CTA, and the CTA finishing a row's last chunk merges the row;
+ *   num_splits   : 0 (default) = one persistent launch of one CTA per SM: the selected pages of
+ *                  all dense rows are split into equal ranges, one per CTA; a row cut across
+ *                  CTAs is merged by the CTA that finishes its last part (no second kernel);
  *                  > 0 = the pages of a row are spread over exactly this many CTAs and merged
  *                  by a second kernel.
  *   workspace    : device scratch of at least dsa_sparse_decode_attn_workspace_size() bytes,
@@ -263,6 +264,69 @@ int dsa_ema_predict_update(const float* IS, int32_t rows, int32_t n, int32_t str
                            float* v, int32_t mode, float alpha, float beta, float gamma,
                            float* pred, int32_t k_pred, int32_t* pred_idx,
                            int32_t pred_idx_stride, int32_t* pred_count, dsa_stream_t stream);
+
+/*
+ * One whole PRR decode step t >= 1 in a single launch ([PRR] §3 end to end: speculation over the
+ * predicted set P_t (§3.4), the true selection A_t, the predictor update (§3.1), repair of the
+ * missed pages and the merge (§3.3)).  It computes exactly what this sequence computes:
+ *   dsa_score_pages(q, meta, DSA_META_MINMAX, logical_page = page_size)     -> scores (= IS_t)
+ *   dsa_select_topk(scores, n = stride, k)                                  -> idx/count (= A_t)
+ *   dsa_sparse_decode_attn(P_t = spec_idx/spec_count, page_partials)        -> page_partials
+ *   dsa_ema_predict_update(scores, DSA_EMA_UPDATE, k_pred)                  -> ell, trend, pred,
+ *                                                                              next_idx/next_count
+ *   dsa_repair_merge(P_t, page_partials, A_t, superset)                     -> out/m/l
+ * with scores, A_t, the EMA state and P_{t+1} bit for bit and out/m/l up to fp32 rounding.  The
+ * speculative attention and the scoring run side by side on every SM; selection, prediction and
+ * repair follow after on-device grid barriers (a cooperative launch of one CTA per SM).
+ *   args->q            : bf16 [B][Hq][D], 16-byte aligned.
+ *   args->meta         : DSA_META_MINMAX metadata built with logical_page == page_size.
+ *   args->scores (out) : fp32 [B][Hkv][stride]; max_pages_per_seq <= stride <= 32768.
+ *   args->ell, trend   : fp32 [B][Hkv][stride], EMA level and trend, updated in place.
+ *   args->pred (out)   : fp32 [B][Hkv][stride] or NULL.
+ *   args->spec_idx/spec_count : P_t, int32 [B][Hkv][k_pred] ASCENDING and unique, int32 [B][Hkv].
+ *   args->page_partials (out) : fp32 [B][Hkv][k_pred][G][D + 4], 16-byte aligned.
+ *   args->idx/count (out)     : A_t, int32 [B][Hkv][k] ascending, int32 [B][Hkv].
+ *   args->next_idx/next_count (out): P_{t+1}, int32 [B][Hkv][k_pred], int32 [B][Hkv]; must not
+ *                        alias spec_idx/spec_count (double-buffer them across steps).
+ *   1 <= k, k_pred <= 256.  kv->head_is_streaming must be NULL.
+ *   workspace          : dsa_prr_step_workspace_size(kv) bytes, 16-byte aligned, ZERO-FILLED
+ *                        before its first use; every call that completes leaves its counters at
+ *                        zero again.  If a call raised DSA_STATUS_TIMEOUT the workspace must be
+ *                        zero-filled again.
+ * A_t is selected exactly, but its search is speculative too: T0, the k-th largest true score over
+ * P_t's pages, bounds the k-th largest of all scores from below, so only the pages scoring >= T0
+ * (appended while scoring) are ranked; when P_t has fewer than k scored pages, or more than 512
+ * pages pass T0, every score of the row is scanned instead.
+ */
+typedef struct dsa_prr_step_args {
+  const void* q;
+  const void* meta;
+  float* scores;
+  int32_t stride;
+  float* ell;
+  float* trend;
+  float alpha;
+  float beta;
+  float gamma;
+  float* pred;
+  const int32_t* spec_idx;
+  const int32_t* spec_count;
+  int32_t k_pred;
+  float* page_partials;
+  int32_t* idx;
+  int32_t* count;
+  int32_t k;
+  int32_t* next_idx;
+  int32_t* next_count;
+  int32_t superset;
+  float scale;
+  float* out;
+  float* m;
+  float* l;
+} dsa_prr_step_args;
+int dsa_prr_step(const dsa_paged_kv* kv, const dsa_prr_step_args* args, void* workspace,
+                 size_t workspace_bytes, dsa_stream_t stream);
+size_t dsa_prr_step_workspace_size(const dsa_paged_kv* kv);
 
 /*
  * Log-sum-exp merge of partial records ([PRR] §3.3 recurrence, applied to all parts at once).

@@ -125,6 +125,28 @@ def test_select_topk_exact(n, k):
         assert np.all(idx[r, cnt[r]:k] == -1)
 
 
+def test_select_topk_crowded_cutoff():
+    """Rows whose cut-off bin holds more keys than the one-pass path gathers (all keys equal; 600
+    keys tied at the k-th score; two values only) take the radix path and give the same exact
+    selection; rows with a few keys per bin take the one-pass path."""
+    n, k = 8192, 64
+    g = torch.Generator().manual_seed(5)
+    rows = [torch.ones(n), torch.randn(n, generator=g), torch.where(torch.rand(n, generator=g) < 0.5,
+                                                                    1.0, 2.0)]
+    r = torch.randn(n, generator=g) - 10.0
+    r[torch.randperm(n, generator=g)[:600]] = 3.0
+    r[torch.randperm(n, generator=g)[:20]] = 7.0
+    rows.append(r)
+    s = torch.stack(rows)
+    idx = torch.full((len(rows), k), -7, dtype=torch.int32, device="cuda")
+    cnt = torch.empty(len(rows), dtype=torch.int32, device="cuda")
+    B.dsa_select_topk(s.cuda(), n, k, idx, cnt)
+    idx, cnt = idx.cpu().numpy(), cnt.cpu().numpy()
+    for i in range(len(rows)):
+        ref = O.select_topk(s[i].double().numpy(), k)
+        assert cnt[i] == k and list(idx[i]) == ref, f"row {i}"
+
+
 @pytest.mark.parametrize("n_logical,g,k", [(8192, 4, 64), (1001, 4, 12), (64, 1, 8), (999, 3, 50)])
 def test_select_hier_exact(n_logical, g, k):
     s = _tied_scores(4, n_logical, seed=g * 100 + k)

@@ -144,10 +144,11 @@ def run_threshold(w, inp, sample):
     return counts
 
 
-def run_prr(w, inp, sample, superset=False):
+def run_prr(w, inp, sample, superset=False, fused=True):
     _META_CACHE.clear()
     cache = Cache.from_inputs(inp)
-    dec = PRRDecoder(cache, w.k, w.k_pred, w.alpha, w.beta, w.gamma, superset=superset)
+    dec = PRRDecoder(cache, w.k, w.k_pred, w.alpha, w.beta, w.gamma, superset=superset,
+                     fused=fused)
     dec.build_meta()
     G = w.group
     rows = _rows(w, sample)
@@ -206,13 +207,100 @@ def test_prr_superset_mode_at_oracle_scale():
     run_prr(w, inp, None, superset=True)
 
 
+@pytest.mark.parametrize("superset", [False, True])
+def test_prr_staged_path_at_oracle_scale(superset):
+    """The separate-launch path (three streams) against the oracle, as the fused path above."""
+    w = oracle_scale(BY_NAME["prr_512k"])
+    inp = to_cuda(make_inputs(w, "cpu"))
+    run_prr(w, inp, None, superset=superset, fused=False)
+
+
+def _prr_fused_vs_staged(w, inp, superset):
+    """Runs the fused one-launch step and the separate-launch step side by side: scores, both
+    selections, the EMA state and the prediction agree bit for bit; the partial records and the
+    outputs agree to fp32 rounding."""
+    decs = []
+    for fused in (True, False):
+        cache = Cache.from_inputs(inp)
+        dec = PRRDecoder(cache, w.k, w.k_pred, w.alpha, w.beta, w.gamma, superset=superset,
+                         fused=fused)
+        dec.build_meta()
+        decs.append(dec)
+    for t in range(w.steps):
+        for dec in decs:
+            dec.step(inp["q"][t])
+        torch.cuda.synchronize()
+        f, s = decs
+        for name in ("scores", "ell", "trend", "pred", "idx", "count"):
+            assert torch.equal(getattr(f, name), getattr(s, name)), f"{name} differs at step {t}"
+        assert torch.equal(f.spec_idx, s.spec_idx) and torch.equal(f.spec_count, s.spec_count)
+        if t > 0:
+            P_cnt = s.spec_counts[(t - 1) % 2]
+            for r in range(P_cnt.numel()):
+                b, h = divmod(r, w.num_kv_heads)
+                n = int(P_cnt[b, h])
+                rec_f = f.partials[b, h, :n].double().cpu().numpy()
+                rec_s = s.partials[b, h, :n].double().cpu().numpy()
+                assert_close(rec_f[..., :130], rec_s[..., :130], f"records t{t} b{b} h{h}")
+        assert_outputs(f.out.cpu().numpy(), f.m.cpu().numpy(), f.l.cpu().numpy(),
+                       [x.double().cpu().numpy() for x in (s.out, s.m, s.l)], f"step {t}")
+        assert int(f.cache.status.item()) == 0
+    ws = decs[0].step_workspace
+    rows = w.batch * w.num_kv_heads
+    cnt = (4 * rows + 15) // 16 * 16
+    lst = rows * 512 * 8
+    assert int(ws[:256 + cnt].sum()) == 0 and int(ws[256 + cnt + lst:256 + 2 * cnt + lst].sum()) == 0, \
+        "barrier words / candidate counts not left at zero"
+
+
+@pytest.mark.parametrize("superset", [False, True])
+def test_prr_fused_step_matches_staged_at_oracle_scale(superset):
+    w = oracle_scale(BY_NAME["prr_512k"])
+    _prr_fused_vs_staged(w, to_cuda(make_inputs(w, "cpu")), superset)
+
+
+# Shapes that take the fused step's other paths: more rows than half the CTAs (every CTA selects,
+# waits, then updates the EMA and repairs), a small group on 16-token pages (one tile per page,
+# G = 4), and ragged requests with pages past the end of the shorter ones.
+@pytest.mark.parametrize("shape", ["many_rows", "g4_page16", "ragged", "wide_table"])
+def test_prr_fused_step_shapes(shape):
+    base = BY_NAME["prr_512k"]
+    if shape == "wide_table":
+        # a page table far wider than the requests: each CTA's share of the score rows is too big
+        # to stage the EMA update on chip, so the update runs after scoring instead
+        w = base.replace(batch=4, seq_len=64 * 100 + 9, k=12, steps=4, ragged=True)
+        inp = to_cuda(make_inputs(w, "cpu"))
+        table = inp["page_table"]
+        inp["page_table"] = torch.cat(
+            [table, torch.zeros((table.shape[0], 20000 - table.shape[1]), dtype=table.dtype,
+                                device=table.device)], dim=1).contiguous()
+        _prr_fused_vs_staged(w, inp, False)
+        return
+    if shape == "many_rows":
+        w = base.replace(batch=48, num_kv_heads=2, num_q_heads=32, seq_len=64 * 40 + 7, k=8,
+                         steps=3, ragged=True, extra_phys_pages=3)
+    elif shape == "g4_page16":
+        w = base.replace(batch=3, num_q_heads=8, num_kv_heads=2, seq_len=16 * 300 + 5,
+                         page_size=16, logical_page=16, k=20, steps=4, ragged=True)
+    else:
+        w = base.replace(batch=5, seq_len=64 * 90, k=12, steps=4, ragged=True,
+                         extra_phys_pages=9)
+    _prr_fused_vs_staged(w, to_cuda(make_inputs(w, "cpu")), shape == "ragged")
+
+
+def test_prr_fused_step_matches_staged_full_size():
+    w = BY_NAME["prr_512k"].replace(steps=6)
+    _prr_fused_vs_staged(w, make_inputs(w, "cuda"), False)
+
+
 def test_prr_without_second_stream_matches():
     w = oracle_scale(BY_NAME["prr_512k"]).replace(steps=3)
     inp = to_cuda(make_inputs(w, "cpu"))
     outs = []
     for two in (True, False):
         cache = Cache.from_inputs(inp)
-        dec = PRRDecoder(cache, w.k, w.k_pred, w.alpha, w.beta, w.gamma, two_streams=two)
+        dec = PRRDecoder(cache, w.k, w.k_pred, w.alpha, w.beta, w.gamma, two_streams=two,
+                         fused=False)
         dec.build_meta()
         for t in range(w.steps):
             dec.step(inp["q"][t])

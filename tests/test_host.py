@@ -37,9 +37,28 @@ def test_library_exports_every_header_function(lib):
     assert set(binding._SIGNATURES) == set(names), "binding signatures out of sync with the header"
 
 
-def test_header_struct_layout_matches_binding():
+def test_header_struct_layout_matches_binding(tmp_path):
+    """Every field of the header's structs sits at the offset the ctypes mirror uses (a C
+    program compiled against include/dsa.h prints the offsets)."""
     from dynamic_block_sparse_gb300 import binding
     assert ctypes.sizeof(binding.PagedKV) == 6 * 8 + 7 * 4 + 4  # 6 pointers, 7 int32, padding
+    lines = ["#include <stdio.h>", "#include <stddef.h>", '#include "dsa.h"', "int main(void) {"]
+    for cname, cls in (("dsa_paged_kv", binding.PagedKV), ("dsa_prr_step_args", binding.PrrStepArgs)):
+        lines.append(f'  printf("{cname} %zu\\n", sizeof({cname}));')
+        for f, _ in cls._fields_:
+            lines.append(f'  printf("{cname}.{f} %zu\\n", offsetof({cname}, {f}));')
+    lines += ["  return 0;", "}"]
+    src = tmp_path / "layout.c"
+    src.write_text("\n".join(lines) + "\n")
+    exe = tmp_path / "layout"
+    subprocess.run(["gcc", "-I", os.path.join(ROOT, "include"), "-o", str(exe), str(src)],
+                   check=True)
+    got = dict(ln.split() for ln in subprocess.run([str(exe)], capture_output=True, text=True,
+                                                    check=True).stdout.splitlines())
+    for cname, cls in (("dsa_paged_kv", binding.PagedKV), ("dsa_prr_step_args", binding.PrrStepArgs)):
+        assert int(got[cname]) == ctypes.sizeof(cls), cname
+        for f, _ in cls._fields_:
+            assert int(got[f"{cname}.{f}"]) == getattr(cls, f).offset, f"{cname}.{f}"
 
 
 def test_version_and_empty_error(lib):
@@ -86,6 +105,42 @@ def test_binding_refuses_cpu_tensors(lib):
     with pytest.raises(ValueError, match="CUDA"):
         B.dsa_select_topk(torch.zeros(2, 8), 8, 2, torch.zeros((2, 2), dtype=torch.int32),
                           torch.zeros(2, dtype=torch.int32))
+
+
+def test_prr_step_host_validation_without_gpu(lib):
+    """dsa_prr_step rejects bad arguments on the host, before any CUDA call."""
+    from dynamic_block_sparse_gb300 import binding as B
+    kv = B.PagedKV()
+    kv.k_pages = kv.v_pages = kv.page_table = kv.seq_lens = 4096
+    kv.batch, kv.num_q_heads, kv.num_kv_heads = 1, 32, 2
+    kv.head_dim, kv.page_size, kv.max_pages_per_seq, kv.num_phys_pages = 128, 64, 64, 64
+    a = B.PrrStepArgs()
+    for i, f in enumerate(("q", "meta", "scores", "ell", "trend", "spec_idx", "spec_count",
+                           "page_partials", "idx", "count", "next_count", "out", "m", "l")):
+        setattr(a, f, 4096 * (1 + i))
+    a.stride, a.k, a.k_pred, a.scale = 64, 8, 10, 0.1
+    ws = 1 << 20
+    call = lambda: lib.dsa_prr_step(ctypes.byref(kv), ctypes.byref(a), ws, 1 << 20, None)
+    assert call() == -1 and b"NULL" in lib.dsa_last_error()          # next_idx missing
+    a.next_idx = a.spec_idx
+    assert call() == -1 and b"alias" in lib.dsa_last_error()
+    a.next_idx = 4096 * 99
+    a.stride = 32
+    assert call() == -1 and b"stride" in lib.dsa_last_error()        # < max_pages_per_seq
+    a.stride = 64
+    a.k = 300
+    assert call() == -3
+    a.k = 8
+    a.q = 4100
+    assert call() == -2                                               # misaligned q
+    a.q = 4096
+    need = lib.dsa_prr_step_workspace_size(ctypes.byref(kv))
+    assert need == 256 + 2 * (16 + 2 * 512 * 8)
+    assert lib.dsa_prr_step(ctypes.byref(kv), ctypes.byref(a), ws, need - 1, None) == -5
+    kv.head_is_streaming = 4096
+    assert call() == -3 and b"streaming" in lib.dsa_last_error()
+    assert lib.dsa_prr_step(ctypes.byref(kv), None, ws, 1 << 20, None) == -1
+    assert lib.dsa_prr_step_workspace_size(None) == 0
 
 
 def test_generator_is_deterministic_and_plants_hot_pages():
