@@ -29,12 +29,11 @@ constexpr int kEmaCap = 1024;  // EMA updates a CTA stages on chip during scorin
 
 struct PLayout {
   // phase 1
-  uint32_t stage_off, merge_off, q_off, qbar_off, wt_off, sps_off, ppk_off, ema_off, bar_off, ctl_off,
-      p1_end;
+  uint32_t stage_off, merge_off, q_off, qbar_off, wt_off, sps_off, ppk_off, bar_off, ctl_off;
   // phase 3
-  uint32_t sp_off, sa_off, list_off, part_off, pm_off, pl_off, qh_off, ws_off, wf_off, acc_off,
-      p3_end;
-  uint32_t total;
+  uint32_t sp_off, sa_off, list_off, part_off, qh_off, ws_off, bmp_off, bma_off, rec_off;
+  // the EMA updates staged from phase 1 to the end of phase 2: past every other region
+  uint32_t ema_off, total;
 };
 
 __host__ __device__ inline uint32_t up(uint32_t x, uint32_t a) { return (x + a - 1) / a * a; }
@@ -48,10 +47,9 @@ __host__ __device__ inline PLayout playout(int page, int G, int n, int k, int k_
   L.wt_off = up(L.qbar_off + kHeadDim * 4u, 16);
   L.sps_off = up(L.wt_off + (kPW + 1) * 16 * 4u, 16);
   L.ppk_off = up(L.sps_off + 4u * k_pred, 16);
-  L.ema_off = up(L.ppk_off + 4u * k_pred, 16);
-  L.bar_off = up(L.ema_off + 3u * 4u * kEmaCap, 16);
+  L.bar_off = up(L.ppk_off + 4u * k_pred, 16);
   L.ctl_off = L.bar_off + 2 * kPStages * 8u;
-  L.p1_end = L.ctl_off + 2 * kPStages * 4u;
+  const uint32_t p1_end = L.ctl_off + 2 * kPStages * 4u;
   // phase 2: keys [n] at offset 0
   const uint32_t p2_end = 4u * static_cast<uint32_t>(n);
   // phase 3
@@ -59,17 +57,17 @@ __host__ __device__ inline PLayout playout(int page, int G, int n, int k, int k_
   L.sa_off = up(4u * k_pred, 16);
   L.list_off = up(L.sa_off + 4u * k, 16);
   L.part_off = up(L.list_off + 8u * k, 16);
-  L.pm_off = up(L.part_off + 4u * k_pred, 16);
-  L.pl_off = up(L.pm_off + 4u * k_pred, 16);
-  L.qh_off = up(L.pl_off + 4u * k_pred, 16);
+  L.qh_off = up(L.part_off + 4u * k_pred, 16);
   L.ws_off = up(L.qh_off + 4u * kHeadDim, 16);
-  L.wf_off = up(L.ws_off + kPWarps * (kHeadDim + 4) * 4u, 16);
-  L.acc_off = up(L.wf_off + kPWarps * 4u, 16);
-  L.p3_end = L.acc_off + kPWarps * kHeadDim * 4u;
-  uint32_t t = L.p1_end;
+  L.bmp_off = up(L.ws_off + kPWarps * (kHeadDim + 4) * 4u, 16);
+  L.bma_off = up(L.bmp_off + 4u * ((n + 31) / 32), 16);
+  L.rec_off = up(L.bma_off + 4u * ((n + 31) / 32), 16);
+  const uint32_t p3_end = L.rec_off + 4u * kRecordFloats * k_pred;
+  uint32_t t = p1_end;
   if (p2_end > t) t = p2_end;
-  if (L.p3_end > t) t = L.p3_end;
-  L.total = t + 1024u;  // alignment slack
+  if (p3_end > t) t = p3_end;
+  L.ema_off = up(t, 16);
+  L.total = L.ema_off + 3u * 4u * kEmaCap + 1024u;  // + alignment slack
   return L;
 }
 
@@ -94,7 +92,7 @@ DSA_DEV bool grid_barrier(unsigned* ctr, unsigned target, volatile int* abort, i
         raise_status(status, DSA_STATUS_TIMEOUT);
         break;
       }
-      __nanosleep(500);
+      __nanosleep(100);
     }
   }
   __syncthreads();
@@ -186,6 +184,25 @@ __global__ void __launch_bounds__(kPThreads, 1)
   uint64_t* bars = reinterpret_cast<uint64_t*>(smem + lay.bar_off);  // [S] full, [S] empty
   volatile int* stage_ok = reinterpret_cast<int*>(smem + lay.ctl_off);  // [S]: -1 none, 0, 1
   volatile int* stage_pos = stage_ok + kPStages;
+  if (warp == 1 && lane < 8) {
+    // phase 1 reads these first: start their address translations at once
+    const long long T0 = static_cast<long long>(rows) * n;
+    const long long sb = static_cast<long long>(blockIdx.x) * T0 / gridDim.x;
+    const int row = static_cast<int>(sb / n);
+    const int b = row / kv.Hkv;
+    const void* p = nullptr;
+    switch (lane) {
+      case 0: p = a.spec_count + row; break;
+      case 1: p = a.spec_idx + static_cast<size_t>(row) * a.k_pred; break;
+      case 2: p = kv.page_table + static_cast<size_t>(b) * kv.max_pages; break;
+      case 3: p = kv.seq_lens + b; break;
+      case 4: p = a.scores + sb; break;
+      case 5: p = a.ell + sb; break;
+      case 6: p = a.trend + sb; break;
+      default: p = a.q + static_cast<size_t>(b) * kv.Hq * kHeadDim; break;
+    }
+    prefetch_l2(p);
+  }
   if (tid == 0) {
     for (int s = 0; s < kPStages; ++s) {
       mbar_init(smem_u32(&bars[s]), 1);
@@ -512,6 +529,17 @@ __global__ void __launch_bounds__(kPThreads, 1)
       }
     }
   }
+  // addresses a phase-2 role reads and writes after the barrier
+  if (tid == 0 && roles && static_cast<int>(blockIdx.x) < 2 * rows) {
+    const int row = static_cast<int>(blockIdx.x) % rows;
+    const bool sel = static_cast<int>(blockIdx.x) < rows;
+    prefetch_l2((sel ? a.cand_cnt : a.cand_cnt2) + row);
+    prefetch_l2((sel ? a.cand : a.cand2) + static_cast<size_t>(row) * kCandCap);
+    prefetch_l2(sel ? a.idx + static_cast<size_t>(row) * a.k
+                    : a.next_idx + static_cast<size_t>(row) * a.k_pred);
+    prefetch_l2(sel ? a.count + row : a.next_count + row);
+    prefetch_l2(a.scores + static_cast<size_t>(row) * n);
+  }
   if (!grid_barrier(a.sync + 0, gridDim.x, abort_flag, kv.status)) {
     // gave up: wait (bounded) for this CTA's page loads still in flight before exiting
     if (tid == 0) {
@@ -676,14 +704,17 @@ __global__ void __launch_bounds__(kPThreads, 1)
     const size_t base = static_cast<size_t>(row) * n;
     KeyStats st;
     __syncthreads();  // keys of a previous task are no longer read
+    // the list up to its capacity is read together with its count (one round trip)
     const unsigned C = __ldcg(a.cand_cnt + row);
-    if (C <= static_cast<unsigned>(kCandCap)) {
+    {
       const uint2* cr = a.cand + static_cast<size_t>(row) * kCandCap;
-      for (int i = tid; i < static_cast<int>(C); i += kPThreads) {
+      for (int i = tid; i < kCandCap; i += kPThreads) {
         const uint2 e = __ldcg(cr + i);
         sel_scratch.small.ckey[i] = e.x;
         sel_scratch.small.cidx[i] = static_cast<int>(e.y);
       }
+    }
+    if (C <= static_cast<unsigned>(kCandCap)) {
       __syncthreads();
       int32_t* out = a.idx + static_cast<size_t>(row) * a.k;
       const int total =
@@ -723,6 +754,62 @@ __global__ void __launch_bounds__(kPThreads, 1)
     }
     select_into(a.k, a.idx + static_cast<size_t>(row) * a.k, a.count + row, st);
   };
+  // Phase 3 tasks of this CTA: (row, query head) pairs; with the phase-2 roles, only the CTAs past
+  // them repair.  A task's P_t and query head do not depend on phase 2: the first task's are
+  // fetched before waiting at the second barrier.
+  const int rep_first = roles ? static_cast<int>(blockIdx.x) - 2 * rows : blockIdx.x;
+  const int rep_step = roles ? static_cast<int>(gridDim.x) - 2 * rows : gridDim.x;
+  // membership bitmaps over page positions [0, n): P_t's and A_t's
+  const int bm_words = (n + 31) >> 5;
+  auto fetch_task = [&](int task) {
+    int32_t* sP = reinterpret_cast<int32_t*>(smem + lay.sp_off);
+    float* qh = reinterpret_cast<float*>(smem + lay.qh_off);
+    uint32_t* bmP = reinterpret_cast<uint32_t*>(smem + lay.bmp_off);
+    uint32_t* bmA = reinterpret_cast<uint32_t*>(smem + lay.bma_off);
+    const int row = task / G, g = task - row * G;
+    const int b = row / kv.Hkv, h = row % kv.Hkv;
+    const int cntP = min(max(a.spec_count[row], 0), a.k_pred);
+    for (int w = tid; w < bm_words; w += kPThreads) {
+      bmP[w] = 0u;
+      bmA[w] = 0u;
+    }
+    const size_t qhead = static_cast<size_t>(b) * kv.Hq + static_cast<size_t>(h) * G + g;
+    for (int d = tid; d < kHeadDim; d += kPThreads)
+      qh[d] = __bfloat162float(a.q[qhead * kHeadDim + d]) * a.scale_log2;
+    __syncthreads();
+    for (int i = tid; i < cntP; i += kPThreads) {
+      const int pos = a.spec_idx[static_cast<size_t>(row) * a.k_pred + i];
+      sP[i] = pos;
+      if (pos >= 0 && pos < n) atomicOr(&bmP[pos >> 5], 1u << (pos & 31));
+    }
+    // the speculative records of this query head (phase 1 wrote them before the first barrier)
+    float* srec = reinterpret_cast<float*>(smem + lay.rec_off);
+    for (int e = tid; e < cntP * (kRecordFloats / 4); e += kPThreads) {
+      const int i = e / (kRecordFloats / 4), c = e - i * (kRecordFloats / 4);
+      const float4 v = __ldcg(reinterpret_cast<const float4*>(
+                                  a.partials + ((static_cast<size_t>(row) * a.k_pred + i) * G + g) *
+                                                   kRecordFloats) +
+                              c);
+      *reinterpret_cast<float4*>(srec + i * kRecordFloats + c * 4) = v;
+    }
+  };
+  const bool prefetch_first = roles && rep_first >= 0 && rep_first < rows * G;
+  if (prefetch_first) {
+    fetch_task(rep_first);
+    // addresses the first task reads and writes after the barrier
+    if (tid == 0) {
+      const int row = rep_first / G, g = rep_first - row * G;
+      const int b = row / kv.Hkv, h = row % kv.Hkv;
+      const size_t qhead = static_cast<size_t>(b) * kv.Hq + static_cast<size_t>(h) * G + g;
+      prefetch_l2(a.count + row);
+      prefetch_l2(a.idx + static_cast<size_t>(row) * a.k);
+      prefetch_l2(a.out + qhead * kHeadDim);
+      prefetch_l2(a.m + qhead);
+      prefetch_l2(a.l + qhead);
+      prefetch_l2(kv.page_table + static_cast<size_t>(b) * kv.max_pages);
+    }
+  }
+
   // P_{t+1} of a row whose EMA update rode along with scoring: rank the candidates, or (no
   // bound, or too many candidates) recompute the row's predictions from the old state, which is
   // only overwritten after the second barrier, and select from all of them
@@ -731,13 +818,15 @@ __global__ void __launch_bounds__(kPThreads, 1)
     __syncthreads();  // keys / scratch of a previous task are no longer read
     int32_t* out = a.next_idx + static_cast<size_t>(row) * a.k_pred;
     const unsigned C = __ldcg(a.cand_cnt2 + row);
-    if (C <= static_cast<unsigned>(kCandCap)) {
+    {
       const uint2* cr = a.cand2 + static_cast<size_t>(row) * kCandCap;
-      for (int i = tid; i < static_cast<int>(C); i += kPThreads) {
+      for (int i = tid; i < kCandCap; i += kPThreads) {
         const uint2 e = __ldcg(cr + i);
         ts.ckey[i] = e.x;
         ts.cidx[i] = static_cast<int>(e.y);
       }
+    }
+    if (C <= static_cast<unsigned>(kCandCap)) {
       __syncthreads();
       const int total = topk_candidates<kPThreads>(static_cast<int>(C), a.k_pred, n, out, ts);
       for (int i = total + tid; i < a.k_pred; i += kPThreads) out[i] = -1;
@@ -782,73 +871,101 @@ __global__ void __launch_bounds__(kPThreads, 1)
   }
 
   // ================================================================ phase 3
+  // per (row, query head): attention over the missed pages A_t \ P_t on the CUDA cores, merged
+  // with the speculative records of A_t ∩ P_t (every record of P_t in superset mode).  Each warp
+  // keeps one online-softmax state (log2 units, unnormalised O) over its missed tokens and its
+  // share of the records; the nine states are combined at the end.
   int32_t* sP = reinterpret_cast<int32_t*>(smem + lay.sp_off);
   int32_t* sA = reinterpret_cast<int32_t*>(smem + lay.sa_off);
   int2* list = reinterpret_cast<int2*>(smem + lay.list_off);         // missed (phys, pos)
   int32_t* parts = reinterpret_cast<int32_t*>(smem + lay.part_off);  // merged P slots
-  float* pm = reinterpret_cast<float*>(smem + lay.pm_off);           // their m (log2 units)
-  float* pl = reinterpret_cast<float*>(smem + lay.pl_off);           // their l, then weight
   float* qh = reinterpret_cast<float*>(smem + lay.qh_off);
   float* wst = reinterpret_cast<float*>(smem + lay.ws_off);  // [warp][m, l, -, -, O[128]]
-  float* wf = reinterpret_cast<float*>(smem + lay.wf_off);   // [warp] state weights
-  float* s_acc = reinterpret_cast<float*>(smem + lay.acc_off);
   constexpr int kWs = kHeadDim + 4;
-  const int rep_first = roles ? static_cast<int>(blockIdx.x) - 2 * rows : blockIdx.x;
-  const int rep_step = roles ? static_cast<int>(gridDim.x) - 2 * rows : gridDim.x;
   for (int task = rep_first; task >= 0 && task < rows * G; task += rep_step) {
     const int row = task / G, g = task - row * G;
     const int b = row / kv.Hkv, h = row % kv.Hkv;
     const int L = request_len(kv, b);
     const int npos = (L + page - 1) / page;
     const size_t qhead = static_cast<size_t>(b) * kv.Hq + static_cast<size_t>(h) * G + g;
-    __syncthreads();  // shared lists of a previous task are no longer read
-    const int cntA = min(max(__ldcg(a.count + row), 0), a.k);
     const int cntP = min(max(a.spec_count[row], 0), a.k_pred);
-    for (int i = tid; i < cntA; i += kPThreads)
-      sA[i] = __ldcg(a.idx + static_cast<size_t>(row) * a.k + i);
-    for (int i = tid; i < cntP; i += kPThreads)
-      sP[i] = a.spec_idx[static_cast<size_t>(row) * a.k_pred + i];
-    for (int d = tid; d < kHeadDim; d += kPThreads)
-      qh[d] = __bfloat162float(a.q[qhead * kHeadDim + d]) * a.scale_log2;
-    __syncthreads();
-    // merged speculative parts: P slots whose page is in A (every slot in superset mode)
-    int n_parts = 0;
-    for (int base = 0; base < cntP; base += kPThreads) {
-      const int i = base + tid;
-      const bool take = i < cntP && (a.superset || contains_sorted(sA, cntA, sP[i]));
-      int tot;
-      const int at = block_exclusive_scan(take ? 1 : 0, s_red, &tot);
-      if (take) parts[n_parts + at] = i;
-      n_parts += tot;
+    if (task != rep_first || !prefetch_first) {  // else fetched before the second barrier
+      __syncthreads();  // shared lists of a previous task are no longer read
+      fetch_task(task);
     }
-    // missed pages A \ P inside the request with a valid page-table entry
-    int n_miss = 0;
-    for (int base = 0; base < cntA; base += kPThreads) {
-      const int i = base + tid;
-      int phys = 0, pos = -1;
-      bool miss = false;
-      if (i < cntA) {
-        pos = sA[i];
-        miss = !contains_sorted(sP, cntP, pos) && lookup_page(kv, b, pos, npos, &phys);
+    uint32_t* bmP = reinterpret_cast<uint32_t*>(smem + lay.bmp_off);
+    uint32_t* bmA = reinterpret_cast<uint32_t*>(smem + lay.bma_off);
+    // the whole index row at once (slots past the count hold -1), together with the count
+    const int cntA = min(max(__ldcg(a.count + row), 0), a.k);
+    for (int i = tid; i < a.k; i += kPThreads) {
+      const int pos = __ldcg(a.idx + static_cast<size_t>(row) * a.k + i);
+      sA[i] = pos;
+      if (i < cntA && pos >= 0 && pos < n) atomicOr(&bmA[pos >> 5], 1u << (pos & 31));
+    }
+    __syncthreads();
+    auto in_bm = [&](const uint32_t* bm, int pos) {
+      return pos >= 0 && pos < n && ((bm[pos >> 5] >> (pos & 31)) & 1u);
+    };
+    // merged speculative parts (warp 0): P slots whose page is in A (every slot in superset
+    // mode); missed pages (warp 1): A \ P inside the request with a valid page-table entry
+    if (warp == 0) {
+      int np = 0;
+      for (int base = 0; base < cntP; base += 32) {
+        const int i = base + lane;
+        const bool take = i < cntP && (a.superset || in_bm(bmA, sP[i]));
+        const unsigned bal = __ballot_sync(0xffffffffu, take);
+        if (take) parts[np + __popc(bal & ((1u << lane) - 1u))] = i;
+        np += __popc(bal);
       }
-      int tot;
-      const int at = block_exclusive_scan(miss ? 1 : 0, s_red, &tot);
-      if (miss) list[n_miss + at] = make_int2(phys, pos);
-      n_miss += tot;
+      if (lane == 0) s_red[0] = np;
+    } else if (warp == 1) {
+      int nm = 0;
+      for (int base = 0; base < cntA; base += 32) {
+        const int i = base + lane;
+        int phys = 0, pos = -1;
+        bool miss = false;
+        if (i < cntA) {
+          pos = sA[i];
+          miss = !in_bm(bmP, pos) && lookup_page(kv, b, pos, npos, &phys);
+        }
+        const unsigned bal = __ballot_sync(0xffffffffu, miss);
+        if (miss) list[nm + __popc(bal & ((1u << lane) - 1u))] = make_int2(phys, pos);
+        nm += __popc(bal);
+      }
+      if (lane == 0) s_red[1] = nm;
     }
     __syncthreads();
+    const int n_parts = s_red[0], n_miss = s_red[1];
 
-    // ---- attention of query head g over the missed tokens: 32 tokens per warp round (lane =
-    // token for q.k, lane = 4 dims for p.v), online softmax in log2 units per warp
-    const int cpp = (page + 31) / 32;  // 32-token chunks per page
-    float wm = -INFINITY, wl = 0.f;
+    float wm = -INFINITY, wl = 0.f;  // this warp's state: max (log2 units), sum, unnormalised O
     float4 wo = make_float4(0.f, 0.f, 0.f, 0.f);
+    auto absorb = [&](float m2, float l, float4 o) {  // adds a part (max m2, sum l, O = o * l)
+      if (!(l > 0.f)) return;
+      const float mn = fmaxf(wm, m2);
+      const float f_old = wm == -INFINITY ? 0.f : fast_exp2(wm - mn);
+      const float f_new = fast_exp2(m2 - mn) * l;
+      wl = wl * f_old + f_new;
+      wo.x = wo.x * f_old + o.x * f_new;
+      wo.y = wo.y * f_old + o.y * f_new;
+      wo.z = wo.z * f_old + o.z * f_new;
+      wo.w = wo.w * f_old + o.w * f_new;
+      wm = mn;
+    };
+    // ---- missed tokens, 32 per warp round (lane = token for q.k, lane = 4 dims for p.v); the
+    // round's V rows are requested together with its K rows
+    const int cpp = (page + 31) / 32;  // 32-token chunks per page
     for (int c = warp; c < n_miss * cpp; c += kPWarps) {
       const int pi = c / cpp, sub = c - pi * cpp;
       const int phys = list[pi].x, pos = list[pi].y;
       const int t0 = sub * 32;  // first slot of the chunk within the page
       const int nvalid = max(0, min(min(32, page - t0), L - (pos * page + t0)));
       const size_t row0 = (static_cast<size_t>(phys) * kv.Hkv + h) * page + t0;
+      const __nv_bfloat16* vrow = a.vpool + row0 * kHeadDim + lane * 4;
+      uint2 vr[32];
+#pragma unroll
+      for (int u = 0; u < 32; ++u)
+        vr[u] = u < nvalid ? __ldg(reinterpret_cast<const uint2*>(vrow + static_cast<size_t>(u) * kHeadDim))
+                           : make_uint2(0u, 0u);
       float s = -INFINITY;
       if (lane < nvalid) {
         const uint4* kr = reinterpret_cast<const uint4*>(a.kpool + (row0 + lane) * kHeadDim);
@@ -870,118 +987,67 @@ __global__ void __launch_bounds__(kPThreads, 1)
       }
       const float cmax = warp_max(s);
       if (cmax == -INFINITY) continue;
-      const float mnew = fmaxf(wm, cmax);
-      const float alpha = wm == -INFINITY ? 0.f : fast_exp2(wm - mnew);
-      const float p = lane < nvalid ? fast_exp2(s - mnew) : 0.f;
-      wl = wl * alpha + warp_sum(p);
-      wo.x *= alpha;
-      wo.y *= alpha;
-      wo.z *= alpha;
-      wo.w *= alpha;
-      wm = mnew;
-      const __nv_bfloat16* vrow = a.vpool + row0 * kHeadDim + lane * 4;
-      for (int t0 = 0; t0 < nvalid; t0 += 8) {  // eight V rows in flight
-        uint2 raw[8];
+      const float p = lane < nvalid ? fast_exp2(s - cmax) : 0.f;
+      const float lsum = warp_sum(p);
+      float4 o = make_float4(0.f, 0.f, 0.f, 0.f);
 #pragma unroll
-        for (int u = 0; u < 8; ++u)
-          raw[u] = t0 + u < nvalid ? __ldg(reinterpret_cast<const uint2*>(
-                                         vrow + static_cast<size_t>(t0 + u) * kHeadDim))
-                                   : make_uint2(0u, 0u);
+      for (int u = 0; u < 32; ++u) {
+        const float pt = __shfl_sync(0xffffffffu, p, u);
+        const __nv_bfloat16* v = reinterpret_cast<const __nv_bfloat16*>(&vr[u]);
+        o.x = fmaf(pt, __bfloat162float(v[0]), o.x);
+        o.y = fmaf(pt, __bfloat162float(v[1]), o.y);
+        o.z = fmaf(pt, __bfloat162float(v[2]), o.z);
+        o.w = fmaf(pt, __bfloat162float(v[3]), o.w);
+      }
+      const float inv = 1.f / lsum;
+      absorb(cmax, lsum, make_float4(o.x * inv, o.y * inv, o.z * inv, o.w * inv));
+    }
+    // ---- speculative records (prefetched to shared memory), eight per warp round
+    for (int i0 = warp; i0 < n_parts; i0 += 8 * kPWarps) {
+      float mv[8], lv[8];
+      float4 ov[8];
 #pragma unroll
-        for (int u = 0; u < 8; ++u) {
-          const float pt = __shfl_sync(0xffffffffu, p, (t0 + u) & 31);
-          const __nv_bfloat16* v = reinterpret_cast<const __nv_bfloat16*>(&raw[u]);
-          wo.x = fmaf(pt, __bfloat162float(v[0]), wo.x);
-          wo.y = fmaf(pt, __bfloat162float(v[1]), wo.y);
-          wo.z = fmaf(pt, __bfloat162float(v[2]), wo.z);
-          wo.w = fmaf(pt, __bfloat162float(v[3]), wo.w);
+      for (int u = 0; u < 8; ++u) {
+        const int i = i0 + u * kPWarps;
+        mv[u] = -INFINITY;
+        lv[u] = 0.f;
+        ov[u] = make_float4(0.f, 0.f, 0.f, 0.f);
+        if (i < n_parts) {
+          const float* r = reinterpret_cast<const float*>(smem + lay.rec_off) + parts[i] * kRecordFloats;
+          mv[u] = r[128];
+          lv[u] = r[129];
+          ov[u] = *(reinterpret_cast<const float4*>(r) + lane);
         }
       }
+#pragma unroll
+      for (int u = 0; u < 8; ++u) absorb(mv[u] * kLog2e, lv[u], ov[u]);
     }
     if (lane == 0) {
       wst[warp * kWs] = wm;
       wst[warp * kWs + 1] = wl;
     }
     *reinterpret_cast<float4*>(wst + warp * kWs + 4 + lane * 4) = wo;
-    // ---- merge the warps' missed states (log2 units) with the speculative records (natural m)
-    float mloc = -INFINITY;
-    for (int i = tid; i < n_parts; i += kPThreads) {
-      const float* r =
-          a.partials + ((static_cast<size_t>(row) * a.k_pred + parts[i]) * G + g) * kRecordFloats;
-      const float lp = __ldcg(r + 129), mp = __ldcg(r + 128) * kLog2e;
-      pm[i] = mp;
-      pl[i] = lp;
-      if (lp > 0.f) mloc = fmaxf(mloc, mp);
-    }
-    if (lane == 0 && wl > 0.f) mloc = fmaxf(mloc, wm);
-    mloc = warp_max(mloc);
-    if (lane == 0) s_f[warp] = mloc;
     __syncthreads();
+    // ---- combine the warps' states
     float M = -INFINITY;
 #pragma unroll
-    for (int w = 0; w < kPWarps; ++w) M = fmaxf(M, s_f[w]);
-    __syncthreads();  // s_f is reused below
-    float lsum = 0.f;
-    for (int i = tid; i < n_parts; i += kPThreads) {
-      const float wgt = pl[i] > 0.f ? pl[i] * fast_exp2(pm[i] - M) : 0.f;
-      pl[i] = wgt;
-      lsum += wgt;
-    }
-    if (lane == 0) {
-      const float f = wl > 0.f ? fast_exp2(wm - M) : 0.f;
-      wf[warp] = f;
-      lsum += wl * f;
-    }
-    lsum = warp_sum(lsum);
-    if (lane == 0) s_f[warp] = lsum;
-    __syncthreads();
-    float Lsum = 0.f;
-#pragma unroll
-    for (int w = 0; w < kPWarps; ++w) Lsum += s_f[w];
-    // weighted sum: warp w takes its own missed state and parts w, w + 9, ...; lane = 4 dims
-    float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
-    {
-      const float f = wf[warp];
-      if (f > 0.f) {
-        acc.x = f * wo.x;
-        acc.y = f * wo.y;
-        acc.z = f * wo.z;
-        acc.w = f * wo.w;
-      }
-    }
-    for (int i0 = warp; i0 < n_parts; i0 += 4 * kPWarps) {
-      float4 v[4];
-      float wv[4];
-#pragma unroll
-      for (int u = 0; u < 4; ++u) {
-        const int i = i0 + u * kPWarps;
-        wv[u] = i < n_parts ? pl[i] : 0.f;
-        v[u] = wv[u] > 0.f
-                   ? __ldcg(reinterpret_cast<const float4*>(
-                                a.partials + ((static_cast<size_t>(row) * a.k_pred + parts[i]) * G + g) *
-                                                 kRecordFloats) +
-                            lane)
-                   : make_float4(0.f, 0.f, 0.f, 0.f);
-      }
-#pragma unroll
-      for (int u = 0; u < 4; ++u) {
-        acc.x += wv[u] * v[u].x;
-        acc.y += wv[u] * v[u].y;
-        acc.z += wv[u] * v[u].z;
-        acc.w += wv[u] * v[u].w;
-      }
-    }
-    *reinterpret_cast<float4*>(s_acc + warp * kHeadDim + lane * 4) = acc;
-    __syncthreads();
+    for (int w = 0; w < kPWarps; ++w)
+      if (wst[w * kWs + 1] > 0.f) M = fmaxf(M, wst[w * kWs]);
     if (tid < kHeadDim) {
-      float o = 0.f;
+      float o = 0.f, lsum = 0.f;
 #pragma unroll
-      for (int w = 0; w < kPWarps; ++w) o += s_acc[w * kHeadDim + tid];
-      a.out[qhead * kHeadDim + tid] = Lsum > 0.f ? o / Lsum : 0.f;
-    }
-    if (tid == 0) {
-      a.m[qhead] = Lsum > 0.f ? M * kLn2 : -INFINITY;
-      a.l[qhead] = Lsum;
+      for (int w = 0; w < kPWarps; ++w) {
+        const float lw = wst[w * kWs + 1];
+        if (!(lw > 0.f)) continue;
+        const float f = fast_exp2(wst[w * kWs] - M);
+        lsum += lw * f;
+        o += wst[w * kWs + 4 + tid] * f;
+      }
+      a.out[qhead * kHeadDim + tid] = lsum > 0.f ? o / lsum : 0.f;
+      if (tid == 0) {
+        a.m[qhead] = lsum > 0.f ? M * kLn2 : -INFINITY;
+        a.l[qhead] = lsum;
+      }
     }
   }
 
