@@ -109,6 +109,14 @@ DSA_DEV void bulk_load(uint32_t dst, const void* src, uint32_t bytes, uint32_t b
       : "memory");
 }
 
+// 16-byte asynchronous global -> shared copy through L2 (no register staging); completed for the
+// issuing thread by cp_async_wait_all.
+DSA_DEV void cp_async16(uint32_t dst, const void* src) {
+  asm volatile("cp.async.cg.shared.global [%0], [%1], 16;" ::"r"(dst), "l"(src) : "memory");
+}
+
+DSA_DEV void cp_async_wait_all() { asm volatile("cp.async.wait_all;" ::: "memory"); }
+
 // Named barrier over `count` threads (a multiple of 32) of the CTA.
 DSA_DEV void named_barrier(int id, int count) {
   asm volatile("bar.sync %0, %1;" ::"r"(id), "r"(count) : "memory");

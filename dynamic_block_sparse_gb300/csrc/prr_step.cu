@@ -25,6 +25,8 @@ constexpr int kPWarps = kPThreads / 32;
 constexpr int kPStages = 2;
 constexpr int kPGroups = kPW * 32 / 8;  // scoring record groups of 8 lanes
 constexpr int kCandCap = kTopkMaxCand;  // candidates kept per row for the selection of A_t
+constexpr int kScoutEvery = 19;  // every 19th CTA (8 of 152) is a scout that does not score
+constexpr int kScoreRecs = 128;  // metadata records a CTA's scoring stages in shared memory at once
 constexpr int kEmaCap = 1024;  // EMA updates a CTA stages on chip during scoring (its slot share)
 
 struct PLayout {
@@ -42,7 +44,9 @@ __host__ __device__ inline PLayout playout(int page, int G, int n, int k, int k_
   PLayout L;
   L.stage_off = 0;
   L.merge_off = up(kPStages * 512u * page, 1024);
-  L.q_off = up(L.merge_off + kPW * G * (kHeadDim + 2) * 4u, 16);
+  uint32_t merge_bytes = kPW * G * (kHeadDim + 2) * 4u;
+  if (merge_bytes < kScoreRecs * 512u) merge_bytes = kScoreRecs * 512u;  // scoring record buffer
+  L.q_off = up(L.merge_off + merge_bytes, 16);
   L.qbar_off = up(L.q_off + 16u * kQStride * 2u, 16);
   L.wt_off = up(L.qbar_off + kHeadDim * 4u, 16);
   L.sps_off = up(L.wt_off + (kPW + 1) * 16 * 4u, 16);
@@ -173,14 +177,21 @@ __global__ void __launch_bounds__(kPThreads, 1)
   float* st_ell = reinterpret_cast<float*>(smem + lay.ema_off);     // staged EMA updates [kEmaCap]
   float* st_v = st_ell + kEmaCap;
   float* st_pred = st_v + kEmaCap;
-  // this CTA's equal share [s_beg, s_end) of the (row, page) slots, for scoring and the EMA
+  // This CTA's equal share [s_beg, s_end) of the (row, page) slots, for scoring and the EMA.  On
+  // a full grid every kScoutEvery-th CTA is a scout that takes no share: it goes straight to its
+  // speculative pages, so the code of that part is in L2 before the scoring CTAs reach it.
   const long long T = static_cast<long long>(rows) * n;
-  const long long s_beg = static_cast<long long>(blockIdx.x) * T / gridDim.x;
-  const long long s_end = static_cast<long long>(blockIdx.x + 1) * T / gridDim.x;
+  const int grid = static_cast<int>(gridDim.x), cta = static_cast<int>(blockIdx.x);
+  const bool scouts = grid >= 2 * kScoutEvery;
+  const bool scout = scouts && cta % kScoutEvery == 0;
+  const int scorers = scouts ? grid - (grid + kScoutEvery - 1) / kScoutEvery : grid;
+  const int rank = scouts ? cta - (cta / kScoutEvery + 1) : cta;  // among the scorers
+  const long long s_beg = scout ? 0 : static_cast<long long>(rank) * T / scorers;
+  const long long s_end = scout ? 0 : static_cast<long long>(rank + 1) * T / scorers;
   // the EMA update rides along with scoring when every share fits on chip and enough CTAs take the
   // roles of phase 2; its writes wait for the second barrier (until then the old state is read)
-  const bool roles = static_cast<int>(gridDim.x) > 2 * rows;
-  const bool ema1 = roles && (T + gridDim.x - 1) / gridDim.x <= kEmaCap;
+  const bool roles = grid > 2 * rows;
+  const bool ema1 = roles && (T + scorers - 1) / scorers <= kEmaCap;
   uint64_t* bars = reinterpret_cast<uint64_t*>(smem + lay.bar_off);  // [S] full, [S] empty
   volatile int* stage_ok = reinterpret_cast<int*>(smem + lay.ctl_off);  // [S]: -1 none, 0, 1
   volatile int* stage_pos = stage_ok + kPStages;
@@ -254,280 +265,375 @@ __global__ void __launch_bounds__(kPThreads, 1)
     }
     __syncwarp();
   } else {
-    // the first speculative item's query rows, fetched before scoring so they are on chip when the
-    // page lands (one 16-byte piece per thread: row tid / 16, dims 8 (tid % 16) ...)
-    uint4 q_first = make_uint4(0, 0, 0, 0);
-    if (my_items > 0 && (tid >> 4) < G) {
-      const int row = static_cast<int>(blockIdx.x) / a.k_pred;
+    // copies the query rows of speculative item j to shared memory, one 16-byte piece per thread
+    // (row tid / 16, dims 8 (tid % 16) ...; rows past the group are zero).  The first item's are
+    // copied before scoring, so they are on chip when its page lands.
+    auto stage_q = [&](int j) {
+      const int row = static_cast<int>(blockIdx.x + j * gridDim.x) / a.k_pred;
       const int b = row / kv.Hkv, h = row % kv.Hkv;
-      q_first = __ldg(reinterpret_cast<const uint4*>(
-          a.q + (static_cast<size_t>(b) * kv.Hq + h * G + (tid >> 4)) * kHeadDim + (tid & 15) * 8));
-    }
-    // ---- scoring: this CTA's equal share of the (row, page) slots
-    const int gl = lane & 7;
-    for (long long seg = s_beg; seg < s_end;) {
-      const int row = static_cast<int>(seg / n);
-      const int j0 = static_cast<int>(seg - static_cast<long long>(row) * n);
-      const int j1 = static_cast<int>(min(s_end - static_cast<long long>(row) * n,
-                                          static_cast<long long>(n)));
-      seg = static_cast<long long>(row) * n + j1;
-      const int b = row / kv.Hkv, h = row % kv.Hkv;
-      named_barrier(1, kPW * 32);  // qbar of the previous segment is no longer read
-      group_mean_query(a.q + (static_cast<size_t>(b) * kv.Hq + h * G) * kHeadDim, G, qbar, tid,
-                       kPW * 32);
-      named_barrier(1, kPW * 32);
-      float qv[16];
-      group_query_dims(qbar, gl, qv);
-      const int nl = (request_len(kv, b) + page - 1) / page;
-      const int32_t* table = kv.page_table + static_cast<size_t>(b) * kv.max_pages;
-      float* outs = a.scores + static_cast<size_t>(row) * n;
-      // T0: the k-th largest true score over P_t's pages.  At least k pages score >= T0, so the
-      // pages scoring >= T0 contain A_t: they are appended as candidates while scoring, and the
-      // selection after the barrier ranks only them (exactly).  No threshold (P_t has fewer than
-      // k scored pages) marks the row's list overflowed, and the selection scans every score.
-      const int cntP = min(max(a.spec_count[row], 0), a.k_pred);
-      const int32_t* P = a.spec_idx + static_cast<size_t>(row) * a.k_pred;
-      if (tid == 0) s_t0key = 0u;
-      for (int base = warp * 4; base < cntP; base += kPGroups) {
-        const int sl = base + (lane >> 3);
-        const int pos = sl < cntP ? P[sl] : -1;
-        const bool in = pos >= 0 && pos < nl;
-        const int phys = in ? table[pos] : 0;
-        const bool ok = in && phys >= 0 && phys < kv.num_phys;
-        uint4 rp[4];
-        if (ok) load_record(a.meta, static_cast<size_t>(phys) * kv.Hkv + h, gl, rp);
-        const float sp = group_sum(ok ? record_partial<DSA_META_MINMAX>(rp, qv) : 0.f);
-        if (gl == 0 && sl < cntP) spk[sl] = ok ? score_key(sp) : 0u;
-      }
-      named_barrier(1, kPW * 32);
-      // T0': the k_pred-th largest prediction over P_t's pages (from the old EMA state), a lower
-      // bound for the k_pred-th largest prediction of all pages: P_{t+1}'s candidates
-      if (ema1) {
-        if (tid == 0) s_t1key = 0u;
+      const int r = tid >> 4, c = tid & 15;
+      __nv_bfloat16* dst = sQ + r * kQStride + c * 8;
+      if (r < G)
+        cp_async16(smem_u32(dst), a.q + (static_cast<size_t>(b) * kv.Hq + h * G + r) * kHeadDim + c * 8);
+      else
+        *reinterpret_cast<uint4*>(dst) = make_uint4(0, 0, 0, 0);
+    };
+    if (my_items > 0) stage_q(0);
+    // ---- scoring: this CTA's equal share of the (row, page) slots.  Per segment (the part of
+    // one row) the loads go out in three waves of independent requests: (1) the group query,
+    // P_t's positions, the chunk's page-table entries and EMA state; (2) the chunk's metadata
+    // records (copied asynchronously into the merge area, idle until the speculative attention)
+    // and P_t's page-table entries; (3) P_t's metadata records and EMA state.  Record groups of
+    // 8 lanes (32 per CTA): group gid takes P_t slots gid + 32 i and chunk slots j0 + gid + 32 i.
+    // Each lane copies and later reads the same 64 bytes of a staged record: no barrier needed.
+    const int gl = lane & 7, gid = tid >> 3;
+    constexpr int kPB = 256 / kPGroups;  // P_t slots per group (k_pred <= 256)
+    constexpr int kCB = kScoreRecs / kPGroups;  // chunk slots per group per wave
+    constexpr int kPR = 4;  // P_t records in flight per group in wave 3 (divides kPB)
+    const uint32_t rbuf = smem_u32(sO);
+    // copies this lane's part of record `rec` into buffer slot `slot` / reads it back
+    auto stage_record = [&](size_t rec, int slot) {
+      const uint8_t* src = a.meta + rec * 512;
+#pragma unroll
+      for (int c = 0; c < 4; ++c)
+        cp_async16(rbuf + slot * 512 + (gl + 8 * c) * 16, src + (gl + 8 * c) * 16);
+    };
+    auto staged_record = [&](int slot, uint4 (&raw)[4]) {
+      const uint4* p =
+          reinterpret_cast<const uint4*>(reinterpret_cast<const uint8_t*>(sO) + slot * 512);
+#pragma unroll
+      for (int c = 0; c < 4; ++c) raw[c] = p[gl + 8 * c];
+    };
+    auto score_share = [&]() {
+      for (long long seg = s_beg; seg < s_end;) {
+        const int row = static_cast<int>(seg / n);
+        const int j0 = static_cast<int>(seg - static_cast<long long>(row) * n);
+        const int j1 = static_cast<int>(min(s_end - static_cast<long long>(row) * n,
+                                            static_cast<long long>(n)));
+        seg = static_cast<long long>(row) * n + j1;
+        const int b = row / kv.Hkv, h = row % kv.Hkv;
+        const int nl = (request_len(kv, b) + page - 1) / page;
+        const int32_t* table = kv.page_table + static_cast<size_t>(b) * kv.max_pages;
+        float* outs = a.scores + static_cast<size_t>(row) * n;
+        const int cntP = min(max(a.spec_count[row], 0), a.k_pred);
+        const int32_t* P = a.spec_idx + static_cast<size_t>(row) * a.k_pred;
         const float* ell_r = a.ell + static_cast<size_t>(row) * n;
         const float* v_r = a.trend + static_cast<size_t>(row) * n;
-        for (int i = tid; i < cntP; i += kPW * 32) {
-          const int pp = P[i];
-          uint32_t key = 0u;
-          if (pp >= 0 && pp < n) {
-            float l_new, v_new;
-            const float is = spk[i] != 0u ? key_score(spk[i]) : -INFINITY;
-            ema_step(is, ell_r[pp], v_r[pp], DSA_EMA_UPDATE, a.alpha, a.beta, l_new, v_new);
-            key = score_key(ema_predict(l_new, v_new, a.gamma));
-          }
-          ppk[i] = key;
+        named_barrier(1, kPW * 32);  // qbar, spk and ppk of the previous segment are no longer read
+
+        // ---- wave 1
+        float qacc = 0.f;
+        if (tid < kHeadDim) {
+          const __nv_bfloat16* qg = a.q + (static_cast<size_t>(b) * kv.Hq + h * G) * kHeadDim;
+          __nv_bfloat16 qr[16];  // G <= 16: all loads in flight, then the sum in row order
+  #pragma unroll
+          for (int r = 0; r < 16; ++r) qr[r] = r < G ? qg[r * kHeadDim + tid] : __float2bfloat16(0.f);
+  #pragma unroll
+          for (int r = 0; r < 16; ++r)
+            if (r < G) qacc += __bfloat162float(qr[r]);
+        }
+        int ppos[kPB];
+  #pragma unroll
+        for (int i = 0; i < kPB; ++i) {
+          const int sl = gid + kPGroups * i;
+          ppos[i] = sl < cntP ? P[sl] : -1;
+        }
+        int cph[kCB];
+        float cl[kCB], cvv[kCB];
+  #pragma unroll
+        for (int i = 0; i < kCB; ++i) {
+          const int jj = j0 + gid + kPGroups * i;
+          cph[i] = jj < j1 && jj < nl ? table[jj] : -1;
+          cl[i] = ema1 && gl == 0 && jj < j1 ? ell_r[jj] : 0.f;
+          cvv[i] = ema1 && gl == 0 && jj < j1 ? v_r[jj] : 0.f;
+        }
+        if (tid < kHeadDim) qbar[tid] = qacc / static_cast<float>(G);
+        if (tid == 0) {
+          s_t0key = 0u;
+          s_t1key = 0u;
         }
         named_barrier(1, kPW * 32);
-        for (int i = tid; i < cntP; i += kPW * 32) {
-          const uint32_t ki = ppk[i];
-          if (ki == 0u) continue;
-          int ge = 0;
-          for (int j0 = 0; j0 < cntP; j0 += 8) {
-            uint32_t kj[8];
-#pragma unroll
-            for (int u = 0; u < 8; ++u) kj[u] = j0 + u < cntP ? ppk[j0 + u] : 0u;
-#pragma unroll
-            for (int u = 0; u < 8; ++u) ge += kj[u] >= ki;
+        float qv[16];
+        group_query_dims(qbar, gl, qv);
+
+        // ---- wave 2
+  #pragma unroll
+        for (int i = 0; i < kCB; ++i)
+          if (cph[i] >= 0 && cph[i] < kv.num_phys)
+            stage_record(static_cast<size_t>(cph[i]) * kv.Hkv + h, gid + kPGroups * i);
+        int pph[kPB];
+  #pragma unroll
+        for (int i = 0; i < kPB; ++i) {
+          const int pos = ppos[i];
+          pph[i] = pos >= 0 && pos < nl ? table[pos] : -1;
+        }
+        float cs[kCB];
+
+        // ---- wave 3 (P_t's records, kPR per group at a time)
+  #pragma unroll
+        for (int i0 = 0; i0 < kPB; i0 += kPR) {
+          if (i0 > 0 && warp * 4 + kPGroups * i0 >= cntP) break;  // warp-uniform: none of its slots left
+          uint4 rp[kPR][4];
+          float pl[kPR], pv[kPR];  // the old EMA state of those pages
+  #pragma unroll
+          for (int u = 0; u < kPR; ++u) {
+            const int pos = ppos[i0 + u];
+            if (pph[i0 + u] >= 0 && pph[i0 + u] < kv.num_phys)
+              load_record(a.meta, static_cast<size_t>(pph[i0 + u]) * kv.Hkv + h, gl, rp[u]);
+            pl[u] = ema1 && gl == 0 && pos >= 0 && pos < n ? ell_r[pos] : 0.f;
+            pv[u] = ema1 && gl == 0 && pos >= 0 && pos < n ? v_r[pos] : 0.f;
           }
-          if (ge >= a.k_pred) atomicMax(&s_t1key, ki);
+          if (i0 == 0) {  // the chunk's scores while P_t's first records are in flight
+            cp_async_wait_all();
+  #pragma unroll
+            for (int i = 0; i < kCB; ++i) {
+              const bool ok = cph[i] >= 0 && cph[i] < kv.num_phys;
+              uint4 rc[4];
+              if (ok) staged_record(gid + kPGroups * i, rc);
+              cs[i] = group_sum(ok ? record_partial<DSA_META_MINMAX>(rc, qv) : 0.f);
+            }
+          }
+  #pragma unroll
+          for (int u = 0; u < kPR; ++u) {
+            const int i = i0 + u, sl = gid + kPGroups * i;
+            const bool ok = pph[i] >= 0 && pph[i] < kv.num_phys;
+            const float sp = group_sum(ok ? record_partial<DSA_META_MINMAX>(rp[u], qv) : 0.f);
+            if (gl == 0 && sl < cntP) {
+              spk[sl] = ok ? score_key(sp) : 0u;
+              if (ema1) {
+                uint32_t key = 0u;
+                if (ppos[i] >= 0 && ppos[i] < n) {
+                  float l_new, v_new;
+                  ema_step(ok ? sp : -INFINITY, pl[u], pv[u], DSA_EMA_UPDATE, a.alpha, a.beta,
+                           l_new, v_new);
+                  key = score_key(ema_predict(l_new, v_new, a.gamma));
+                }
+                ppk[sl] = key;
+              }
+            }
+          }
+        }
+        named_barrier(1, kPW * 32);
+        // T0: the k-th largest true score over P_t's pages.  At least k pages score >= T0, so the
+        // pages scoring >= T0 contain A_t: they are appended as candidates while scoring, and the
+        // selection after the barrier ranks only them (exactly).  T0' likewise for the predictions
+        // and P_{t+1} (from the old EMA state).  A missing bound (fewer than k scored pages in P_t)
+        // marks the row's list overflowed, and the selection scans every score.
+        auto kth_key = [&](const uint32_t* keys, int kk, unsigned* result) {
+          for (int i = tid; i < cntP; i += kPW * 32) {
+            const uint32_t ki = keys[i];
+            if (ki == 0u) continue;
+            int ge = 0;
+            for (int q0 = 0; q0 < cntP; q0 += 8) {
+              uint32_t kj[8];
+  #pragma unroll
+              for (int u = 0; u < 8; ++u) kj[u] = q0 + u < cntP ? keys[q0 + u] : 0u;
+  #pragma unroll
+              for (int u = 0; u < 8; ++u) ge += kj[u] >= ki;
+            }
+            if (ge >= kk) atomicMax(result, ki);
+          }
+        };
+        kth_key(spk, a.k, &s_t0key);
+        if (ema1) kth_key(ppk, a.k_pred, &s_t1key);
+        named_barrier(1, kPW * 32);
+        const uint32_t t0key = s_t0key;
+        const uint32_t t1key = ema1 ? s_t1key : 0u;
+        if (tid == 0 && t0key == 0u) atomicAdd(a.cand_cnt + row, static_cast<unsigned>(kCandCap + 1));
+        if (tid == 0 && ema1 && t1key == 0u)
+          atomicAdd(a.cand_cnt2 + row, static_cast<unsigned>(kCandCap + 1));
+        // appends the lanes' candidates (lanes with gl == 0 hold a record's score) to a row's list:
+        // one counter update per warp
+        auto append = [&](unsigned* cnt, uint2* list, bool c, int j, uint32_t key) {
+          const unsigned bal = __ballot_sync(0xffffffffu, c);
+          if (bal == 0u) return;
+          unsigned base = 0;
+          if (lane == 0) base = atomicAdd(cnt + row, static_cast<unsigned>(__popc(bal)));
+          base = __shfl_sync(0xffffffffu, base, 0);
+          const unsigned at = base + __popc(bal & ((1u << lane) - 1u));
+          if (c && at < static_cast<unsigned>(kCandCap))
+            list[static_cast<size_t>(row) * kCandCap + at] = make_uint2(key, j);
+        };
+        const long long stage0 = static_cast<long long>(row) * n - s_beg;  // staging index of j = 0
+        // the EMA update of page j with score s (staged until the second barrier); returns the key
+        // of the prediction
+        auto ema_page = [&](int j, float sc, float l_old, float v_old) -> uint32_t {
+          float l_new, v_new;
+          ema_step(sc, l_old, v_old, DSA_EMA_UPDATE, a.alpha, a.beta, l_new, v_new);
+          const float pr = ema_predict(l_new, v_new, a.gamma);
+          const int at = static_cast<int>(stage0 + j);
+          st_ell[at] = l_new;
+          st_v[at] = v_new;
+          st_pred[at] = pr;
+          return score_key(pr);
+        };
+        // a scored chunk slot: output, candidate for A_t, EMA update and candidate for P_{t+1}
+        auto finish_slot = [&](int jj, bool ok, float sc, float l_old, float v_old) {
+          const bool mine = gl == 0 && jj < j1;
+          const float is = ok ? sc : -INFINITY;
+          if (mine) outs[jj] = is;
+          const uint32_t kA = ok ? score_key(sc) : 0u;
+          append(a.cand_cnt, a.cand, t0key != 0u && mine && kA != 0u && kA >= t0key, jj, kA);
+          if (ema1) {
+            const uint32_t pk = mine ? ema_page(jj, is, l_old, v_old) : 0u;
+            append(a.cand_cnt2, a.cand2, t1key != 0u && pk != 0u && pk >= t1key, jj, pk);
+          }
+        };
+        {
+          bool bad = false;
+  #pragma unroll
+          for (int i = 0; i < kCB; ++i) {
+            const int jj = j0 + gid + kPGroups * i;
+            const bool in = jj < j1 && jj < nl;
+            const bool ok = in && cph[i] >= 0 && cph[i] < kv.num_phys;
+            bad |= in && !ok;
+            finish_slot(jj, ok, cs[i], cl[i], cvv[i]);
+          }
+          if (gl == 0 && bad) raise_status(kv.status, DSA_STATUS_BAD_PAGE);
+        }
+        // the rest of a long segment, kCB slots per group per round
+        for (int jb = j0 + kScoreRecs; jb < j1; jb += kScoreRecs) {
+          int ph[kCB];
+          float lo[kCB], vo[kCB];
+  #pragma unroll
+          for (int i = 0; i < kCB; ++i) {
+            const int jj = jb + gid + kPGroups * i;
+            ph[i] = jj < j1 && jj < nl ? table[jj] : -1;
+            lo[i] = ema1 && gl == 0 && jj < j1 ? ell_r[jj] : 0.f;
+            vo[i] = ema1 && gl == 0 && jj < j1 ? v_r[jj] : 0.f;
+          }
+  #pragma unroll
+          for (int i = 0; i < kCB; ++i)
+            if (ph[i] >= 0 && ph[i] < kv.num_phys)
+              stage_record(static_cast<size_t>(ph[i]) * kv.Hkv + h, gid + kPGroups * i);
+          cp_async_wait_all();
+          bool bad = false;
+  #pragma unroll
+          for (int i = 0; i < kCB; ++i) {
+            const int jj = jb + gid + kPGroups * i;
+            const bool in = jj < j1 && jj < nl;
+            const bool ok = in && ph[i] >= 0 && ph[i] < kv.num_phys;
+            bad |= in && !ok;
+            uint4 rc[4];
+            if (ok) staged_record(gid + kPGroups * i, rc);
+            const float sc = group_sum(ok ? record_partial<DSA_META_MINMAX>(rc, qv) : 0.f);
+            finish_slot(jj, ok, sc, lo[i], vo[i]);
+          }
+          if (gl == 0 && bad) raise_status(kv.status, DSA_STATUS_BAD_PAGE);
         }
       }
-      for (int i = tid; i < cntP; i += kPW * 32) {
-        const uint32_t ki = spk[i];
-        if (ki == 0u) continue;
-        int ge = 0;
-        for (int j0 = 0; j0 < cntP; j0 += 8) {
-          uint32_t kj[8];
-#pragma unroll
-          for (int u = 0; u < 8; ++u) kj[u] = j0 + u < cntP ? spk[j0 + u] : 0u;
-#pragma unroll
-          for (int u = 0; u < 8; ++u) ge += kj[u] >= ki;
-        }
-        if (ge >= a.k) atomicMax(&s_t0key, ki);
-      }
-      named_barrier(1, kPW * 32);
-      const uint32_t t0key = s_t0key;
-      const uint32_t t1key = ema1 ? s_t1key : 0u;
-      if (tid == 0 && t0key == 0u) atomicAdd(a.cand_cnt + row, static_cast<unsigned>(kCandCap + 1));
-      if (tid == 0 && ema1 && t1key == 0u)
-        atomicAdd(a.cand_cnt2 + row, static_cast<unsigned>(kCandCap + 1));
-      // appends the lanes' candidates (lanes with gl == 0 hold a record's score) to a row's list:
-      // one counter update per warp
-      auto append = [&](unsigned* cnt, uint2* list, bool c, int j, uint32_t key) {
-        const unsigned bal = __ballot_sync(0xffffffffu, c);
-        if (bal == 0u) return;
-        unsigned base = 0;
-        if (lane == 0) base = atomicAdd(cnt + row, static_cast<unsigned>(__popc(bal)));
-        base = __shfl_sync(0xffffffffu, base, 0);
-        const unsigned at = base + __popc(bal & ((1u << lane) - 1u));
-        if (c && at < static_cast<unsigned>(kCandCap))
-          list[static_cast<size_t>(row) * kCandCap + at] = make_uint2(key, j);
-      };
-      const float* ell_r = a.ell + static_cast<size_t>(row) * n;
-      const float* v_r = a.trend + static_cast<size_t>(row) * n;
-      const long long stage0 = static_cast<long long>(row) * n - s_beg;  // staging index of j = 0
-      // the EMA update of page j with score s (staged until the second barrier); returns the key
-      // of the prediction
-      auto ema_page = [&](int j, float s, float l_old, float v_old) -> uint32_t {
-        float l_new, v_new;
-        ema_step(s, l_old, v_old, DSA_EMA_UPDATE, a.alpha, a.beta, l_new, v_new);
-        const float pr = ema_predict(l_new, v_new, a.gamma);
-        const int at = static_cast<int>(stage0 + j);
-        st_ell[at] = l_new;
-        st_v[at] = v_new;
-        st_pred[at] = pr;
-        return score_key(pr);
-      };
-      // warp-uniform loop: each group handles records jA and jA + kPGroups per round
-      for (int jbase = j0 + warp * 4; jbase < j1; jbase += 2 * kPGroups) {
-        const int jA = jbase + (lane >> 3);
-        const int jB = jA + kPGroups;
-        const bool inA = jA < j1 && jA < nl, inB = jB < j1 && jB < nl;
-        const int physA = inA ? table[jA] : 0;
-        const int physB = inB ? table[jB] : 0;
-        const bool okA = inA && physA >= 0 && physA < kv.num_phys;
-        const bool okB = inB && physB >= 0 && physB < kv.num_phys;
-        if (gl == 0 && ((inA && !okA) || (inB && !okB))) raise_status(kv.status, DSA_STATUS_BAD_PAGE);
-        uint4 ra[4], rb[4];
-        if (okA) load_record(a.meta, static_cast<size_t>(physA) * kv.Hkv + h, gl, ra);
-        if (okB) load_record(a.meta, static_cast<size_t>(physB) * kv.Hkv + h, gl, rb);
-        const bool emaA = ema1 && gl == 0 && jA < j1, emaB = ema1 && gl == 0 && jB < j1;
-        const float lA = emaA ? ell_r[jA] : 0.f, vA = emaA ? v_r[jA] : 0.f;
-        const float lB = emaB ? ell_r[jB] : 0.f, vB = emaB ? v_r[jB] : 0.f;
-        const float sA = group_sum(okA ? record_partial<DSA_META_MINMAX>(ra, qv) : 0.f);
-        const float sB = group_sum(okB ? record_partial<DSA_META_MINMAX>(rb, qv) : 0.f);
-        const float isA = okA ? sA : -INFINITY, isB = okB ? sB : -INFINITY;
-        if (gl == 0) {
-          if (jA < j1) outs[jA] = isA;
-          if (jB < j1) outs[jB] = isB;
-        }
-        const uint32_t kA = okA ? score_key(sA) : 0u, kB = okB ? score_key(sB) : 0u;
-        append(a.cand_cnt, a.cand, t0key != 0u && gl == 0 && jA < j1 && kA != 0u && kA >= t0key,
-               jA, kA);
-        append(a.cand_cnt, a.cand, t0key != 0u && gl == 0 && jB < j1 && kB != 0u && kB >= t0key,
-               jB, kB);
-        if (ema1) {
-          const uint32_t pA = emaA ? ema_page(jA, isA, lA, vA) : 0u;
-          const uint32_t pB = emaB ? ema_page(jB, isB, lB, vB) : 0u;
-          append(a.cand_cnt2, a.cand2, t1key != 0u && pA != 0u && pA >= t1key, jA, pA);
-          append(a.cand_cnt2, a.cand2, t1key != 0u && pB != 0u && pB >= t1key, jB, pB);
-        }
-      }
-    }
+    };
 
     // ---- speculative per-page attention of this CTA's items
-    for (int j = 0; j < my_items; ++j) {
-      const int it = blockIdx.x + j * gridDim.x;
-      const int row = it / a.k_pred, slot = it - row * a.k_pred;
-      const int b = row / kv.Hkv, h = row % kv.Hkv;
-      const int L = request_len(kv, b);
-      const int s = j % kPStages;
-      named_barrier(1, kPW * 32);
-      {
-        const int r = tid >> 4, c = tid & 15;  // 256 consumer threads = 16 rows x 16 pieces
-        uint4 v = q_first;
-        if (j > 0)
-          v = r < G ? __ldg(reinterpret_cast<const uint4*>(
-                          a.q + (static_cast<size_t>(b) * kv.Hq + h * G + r) * kHeadDim + c * 8))
-                    : make_uint4(0, 0, 0, 0);
-        *reinterpret_cast<uint4*>(sQ + r * kQStride + c * 8) = v;
-      }
-      named_barrier(1, kPW * 32);
-      uint32_t qa[8][4];
-      load_q_frags(sQ, qa);
-      WarpSoftmaxState st;
-      state_init(st);
-      const bool got = mbar_wait(smem_u32(&bars[s]), (j / kPStages) & 1, abort_flag, kv.status);
-      const int okv = got ? stage_ok[s] : -1;
-      const int pos = stage_pos[s];
-      if (okv == 1) {
-        const uint32_t kb = smem_base + s * stage_bytes;
-        const uint32_t vb = kb + 2 * page * 128;
-        bool wrote = false;
-        for (int t = warp; t < tiles; t += kPW) {
-          const bool in = pos * page + t * 16 + (lane & 15) < L;
-          const uint32_t vm = __ballot_sync(0xffffffffu, in) & 0xffffu;
-          if (vm == 0u) continue;
-          if (vm != 0xffffu)
-            wrote |= zero_invalid_v_rows(vm, smem + s * stage_bytes + 2 * page * 128, page, t * 16);
-          float sc[2][4];
-          tile_scores(qa, kb, page, t * 16, sc);
-          tile_softmax_pv(st, sc, a.scale_log2, vm, vb, page, t * 16);
-        }
-        if (wrote) fence_proxy_async_smem();
-      }
-      __syncwarp();
-      if (got && lane == 0) mbar_arrive(smem_u32(&bars[kPStages + s]));
-      state_finish(st);
-      {
-        const int r0 = lane >> 2, c0 = (lane & 3) * 2;
-        float* wO = sO + warp * G * kHeadDim;
-#pragma unroll
-        for (int jj = 0; jj < 16; ++jj) {
-          if (r0 < G)
-            *reinterpret_cast<float2*>(wO + r0 * kHeadDim + jj * 8 + c0) =
-                make_float2(st.o[jj][0], st.o[jj][1]);
-          if (r0 + 8 < G)
-            *reinterpret_cast<float2*>(wO + (r0 + 8) * kHeadDim + jj * 8 + c0) =
-                make_float2(st.o[jj][2], st.o[jj][3]);
-        }
-        if ((lane & 3) == 0) {
-          if (r0 < G) {
-            sM[warp * G + r0] = st.m[0];
-            sL[warp * G + r0] = st.l[0];
+    auto spec_items = [&]() {
+      for (int j = 0; j < my_items; ++j) {
+        const int it = blockIdx.x + j * gridDim.x;
+        const int row = it / a.k_pred, slot = it - row * a.k_pred;
+        const int b = row / kv.Hkv, h = row % kv.Hkv;
+        const int L = request_len(kv, b);
+        const int s = j % kPStages;
+        named_barrier(1, kPW * 32);  // the previous item's query rows are no longer read
+        if (j > 0) stage_q(j);
+        cp_async_wait_all();
+        named_barrier(1, kPW * 32);
+        uint32_t qa[8][4];
+        load_q_frags(sQ, qa);
+        WarpSoftmaxState st;
+        state_init(st);
+        const bool got = mbar_wait(smem_u32(&bars[s]), (j / kPStages) & 1, abort_flag, kv.status);
+        const int okv = got ? stage_ok[s] : -1;
+        const int pos = stage_pos[s];
+        if (okv == 1) {
+          const uint32_t kb = smem_base + s * stage_bytes;
+          const uint32_t vb = kb + 2 * page * 128;
+          bool wrote = false;
+          for (int t = warp; t < tiles; t += kPW) {
+            const bool in = pos * page + t * 16 + (lane & 15) < L;
+            const uint32_t vm = __ballot_sync(0xffffffffu, in) & 0xffffu;
+            if (vm == 0u) continue;
+            if (vm != 0xffffu)
+              wrote |= zero_invalid_v_rows(vm, smem + s * stage_bytes + 2 * page * 128, page, t * 16);
+            float sc[2][4];
+            tile_scores(qa, kb, page, t * 16, sc);
+            tile_softmax_pv(st, sc, a.scale_log2, vm, vb, page, t * 16);
           }
-          if (r0 + 8 < G) {
-            sM[warp * G + r0 + 8] = st.m[1];
-            sL[warp * G + r0 + 8] = st.l[1];
-          }
+          if (wrote) fence_proxy_async_smem();
         }
-      }
-      // a wait that gave up in any consumer warp makes every warp skip the record (the OR over
-      // the barrier is the same in all of them), so the barrier inside stays uniform
-      const bool gave_up = named_barrier_or(1, kPW * 32, !got || *abort_flag);
-      if (okv >= 0 && !gave_up) {
-        float* rec0 = a.partials + (static_cast<size_t>(row) * a.k_pred + slot) * G * kRecordFloats;
-        if (okv == 0) {  // a position outside the request: the empty part
-          for (int g = tid; g < G; g += kPW * 32)
-            *reinterpret_cast<float4*>(rec0 + g * kRecordFloats + 128) =
-                make_float4(-INFINITY, 0.f, 0.f, 0.f);
-        } else {
-          // per head: the warps' weights exp(m_w - M) / l (one division each) and the record's
-          // (m, l); then O = sum_w weight_w O_w as float4 rows
-          const int nwu = min(tiles, kPW);  // warps that attended a tile
-          if (tid < G) {
-            const int g = tid;
-            float M = -INFINITY;
-            for (int w = 0; w < nwu; ++w) M = fmaxf(M, sM[w * G + g]);
-            float Lsum = 0.f;
-            for (int w = 0; w < nwu; ++w) {
-              const float mw = sM[w * G + g];
-              const float f = mw == -INFINITY ? 0.f : fast_exp2(mw - M);
-              wt[w * 16 + g] = f;
-              Lsum += sL[w * G + g] * f;
+        __syncwarp();
+        if (got && lane == 0) mbar_arrive(smem_u32(&bars[kPStages + s]));
+        state_finish(st);
+        {
+          const int r0 = lane >> 2, c0 = (lane & 3) * 2;
+          float* wO = sO + warp * G * kHeadDim;
+  #pragma unroll
+          for (int jj = 0; jj < 16; ++jj) {
+            if (r0 < G)
+              *reinterpret_cast<float2*>(wO + r0 * kHeadDim + jj * 8 + c0) =
+                  make_float2(st.o[jj][0], st.o[jj][1]);
+            if (r0 + 8 < G)
+              *reinterpret_cast<float2*>(wO + (r0 + 8) * kHeadDim + jj * 8 + c0) =
+                  make_float2(st.o[jj][2], st.o[jj][3]);
+          }
+          if ((lane & 3) == 0) {
+            if (r0 < G) {
+              sM[warp * G + r0] = st.m[0];
+              sL[warp * G + r0] = st.l[0];
             }
-            const float inv = Lsum > 0.f ? 1.f / Lsum : 0.f;
-            for (int w = 0; w < nwu; ++w) wt[w * 16 + g] *= inv;
-            *reinterpret_cast<float4*>(rec0 + g * kRecordFloats + 128) =
-                make_float4(M == -INFINITY ? -INFINITY : M * kLn2, Lsum, 0.f, 0.f);
-          }
-          named_barrier(1, kPW * 32);
-          for (int e = tid; e < G * 32; e += kPW * 32) {
-            const int g = e >> 5, d4 = e & 31;
-            float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
-            for (int w = 0; w < nwu; ++w) {
-              const float f = wt[w * 16 + g];
-              const float4 o = *reinterpret_cast<const float4*>(sO + (w * G + g) * kHeadDim + d4 * 4);
-              acc.x = fmaf(f, o.x, acc.x);
-              acc.y = fmaf(f, o.y, acc.y);
-              acc.z = fmaf(f, o.z, acc.z);
-              acc.w = fmaf(f, o.w, acc.w);
+            if (r0 + 8 < G) {
+              sM[warp * G + r0 + 8] = st.m[1];
+              sL[warp * G + r0 + 8] = st.l[1];
             }
-            *reinterpret_cast<float4*>(rec0 + g * kRecordFloats + d4 * 4) = acc;
+          }
+        }
+        // a wait that gave up in any consumer warp makes every warp skip the record (the OR over
+        // the barrier is the same in all of them), so the barrier inside stays uniform
+        const bool gave_up = named_barrier_or(1, kPW * 32, !got || *abort_flag);
+        if (okv >= 0 && !gave_up) {
+          float* rec0 = a.partials + (static_cast<size_t>(row) * a.k_pred + slot) * G * kRecordFloats;
+          if (okv == 0) {  // a position outside the request: the empty part
+            for (int g = tid; g < G; g += kPW * 32)
+              *reinterpret_cast<float4*>(rec0 + g * kRecordFloats + 128) =
+                  make_float4(-INFINITY, 0.f, 0.f, 0.f);
+          } else {
+            // per head: the warps' weights exp(m_w - M) / l (one division each) and the record's
+            // (m, l); then O = sum_w weight_w O_w as float4 rows
+            const int nwu = min(tiles, kPW);  // warps that attended a tile
+            if (tid < G) {
+              const int g = tid;
+              float M = -INFINITY;
+              for (int w = 0; w < nwu; ++w) M = fmaxf(M, sM[w * G + g]);
+              float Lsum = 0.f;
+              for (int w = 0; w < nwu; ++w) {
+                const float mw = sM[w * G + g];
+                const float f = mw == -INFINITY ? 0.f : fast_exp2(mw - M);
+                wt[w * 16 + g] = f;
+                Lsum += sL[w * G + g] * f;
+              }
+              const float inv = Lsum > 0.f ? 1.f / Lsum : 0.f;
+              for (int w = 0; w < nwu; ++w) wt[w * 16 + g] *= inv;
+              *reinterpret_cast<float4*>(rec0 + g * kRecordFloats + 128) =
+                  make_float4(M == -INFINITY ? -INFINITY : M * kLn2, Lsum, 0.f, 0.f);
+            }
+            named_barrier(1, kPW * 32);
+            for (int e = tid; e < G * 32; e += kPW * 32) {
+              const int g = e >> 5, d4 = e & 31;
+              float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
+              for (int w = 0; w < nwu; ++w) {
+                const float f = wt[w * 16 + g];
+                const float4 o = *reinterpret_cast<const float4*>(sO + (w * G + g) * kHeadDim + d4 * 4);
+                acc.x = fmaf(f, o.x, acc.x);
+                acc.y = fmaf(f, o.y, acc.y);
+                acc.z = fmaf(f, o.z, acc.z);
+                acc.w = fmaf(f, o.w, acc.w);
+              }
+              *reinterpret_cast<float4*>(rec0 + g * kRecordFloats + d4 * 4) = acc;
+            }
           }
         }
       }
-    }
+    };
+    score_share();
+    spec_items();
   }
   // addresses a phase-2 role reads and writes after the barrier
   if (tid == 0 && roles && static_cast<int>(blockIdx.x) < 2 * rows) {
