@@ -33,7 +33,7 @@ struct PLayout {
   // phase 1
   uint32_t stage_off, merge_off, q_off, qbar_off, wt_off, sps_off, ppk_off, bar_off, ctl_off;
   // phase 3
-  uint32_t sp_off, sa_off, list_off, part_off, qh_off, ws_off, bmp_off, bma_off, rec_off;
+  uint32_t sp_off, sa_off, list_off, part_off, qh_off, ws_off, bmp_off, bma_off, rec_off, keys_off;
   // the EMA updates staged from phase 1 to the end of phase 2: past every other region
   uint32_t ema_off, total;
 };
@@ -54,8 +54,6 @@ __host__ __device__ inline PLayout playout(int page, int G, int n, int k, int k_
   L.bar_off = up(L.ppk_off + 4u * k_pred, 16);
   L.ctl_off = L.bar_off + 2 * kPStages * 8u;
   const uint32_t p1_end = L.ctl_off + 2 * kPStages * 4u;
-  // phase 2: keys [n] at offset 0
-  const uint32_t p2_end = 4u * static_cast<uint32_t>(n);
   // phase 3
   L.sp_off = 0;
   L.sa_off = up(4u * k_pred, 16);
@@ -66,9 +64,13 @@ __host__ __device__ inline PLayout playout(int page, int G, int n, int k, int k_
   L.bmp_off = up(L.ws_off + kPWarps * (kHeadDim + 4) * 4u, 16);
   L.bma_off = up(L.bmp_off + 4u * ((n + 31) / 32), 16);
   L.rec_off = up(L.bma_off + 4u * ((n + 31) / 32), 16);
-  const uint32_t p3_end = L.rec_off + 4u * kRecordFloats * k_pred;
+  // keys [n] of a full-row selection share the record area: a task that needs one selects before
+  // it fetches the records
+  L.keys_off = L.rec_off;
+  uint32_t rec_bytes = 4u * kRecordFloats * k_pred;
+  if (rec_bytes < 4u * static_cast<uint32_t>(n)) rec_bytes = 4u * static_cast<uint32_t>(n);
+  const uint32_t p3_end = L.rec_off + rec_bytes;
   uint32_t t = p1_end;
-  if (p2_end > t) t = p2_end;
   if (p3_end > t) t = p3_end;
   L.ema_off = up(t, 16);
   L.total = L.ema_off + 3u * 4u * kEmaCap + 1024u;  // + alignment slack
@@ -81,14 +83,19 @@ DSA_DEV unsigned ld_acquire(const unsigned* p) {
   return v;
 }
 
-// Grid-wide barrier over a monotonically counting word: arrive, then wait until every CTA has.
-// Bounded: gives up after kWaitLimitNs, raising DSA_STATUS_TIMEOUT.  Returns false when this CTA
-// (or an earlier barrier of it) gave up.
-DSA_DEV bool grid_barrier(unsigned* ctr, unsigned target, volatile int* abort, int32_t* status) {
+// Arrival on a monotonically counting word, after every write of this CTA so far.
+DSA_DEV void grid_arrive(unsigned* ctr, volatile int* abort) {
   __syncthreads();
   if (threadIdx.x == 0 && !*abort) {
     __threadfence();  // this CTA's writes (ordered before by the CTA barrier) become visible
     atomicAdd(ctr, 1u);
+  }
+}
+
+// Waits until the word reaches `target`.  Bounded: gives up after kWaitLimitNs, raising
+// DSA_STATUS_TIMEOUT.  Returns false when this CTA (or an earlier wait of it) gave up.
+DSA_DEV bool grid_wait(unsigned* ctr, unsigned target, volatile int* abort, int32_t* status) {
+  if (threadIdx.x == 0 && !*abort) {
     const unsigned long long t0 = global_timer_ns();
     while (ld_acquire(ctr) < target) {
       if (global_timer_ns() - t0 > kWaitLimitNs) {
@@ -103,13 +110,10 @@ DSA_DEV bool grid_barrier(unsigned* ctr, unsigned target, volatile int* abort, i
   return !*abort;
 }
 
-// Arrival without waiting (for CTAs whose later work does not depend on the barrier).
-DSA_DEV void grid_arrive(unsigned* ctr, volatile int* abort) {
-  __syncthreads();
-  if (threadIdx.x == 0 && !*abort) {
-    __threadfence();
-    atomicAdd(ctr, 1u);
-  }
+// Grid-wide barrier: arrive, then wait until every CTA has.
+DSA_DEV bool grid_barrier(unsigned* ctr, unsigned target, volatile int* abort, int32_t* status) {
+  grid_arrive(ctr, abort);
+  return grid_wait(ctr, target, abort, status);
 }
 
 struct PrrArgs {
@@ -635,16 +639,25 @@ __global__ void __launch_bounds__(kPThreads, 1)
     score_share();
     spec_items();
   }
-  // addresses a phase-2 role reads and writes after the barrier
-  if (tid == 0 && roles && static_cast<int>(blockIdx.x) < 2 * rows) {
-    const int row = static_cast<int>(blockIdx.x) % rows;
-    const bool sel = static_cast<int>(blockIdx.x) < rows;
-    prefetch_l2((sel ? a.cand_cnt : a.cand_cnt2) + row);
-    prefetch_l2((sel ? a.cand : a.cand2) + static_cast<size_t>(row) * kCandCap);
-    prefetch_l2(sel ? a.idx + static_cast<size_t>(row) * a.k
-                    : a.next_idx + static_cast<size_t>(row) * a.k_pred);
-    prefetch_l2(sel ? a.count + row : a.next_count + row);
-    prefetch_l2(a.scores + static_cast<size_t>(row) * n);
+  // Roles after the first barrier (with more than 2 rows CTAs): CTA rows + r selects P_{t+1} of
+  // row r; every other CTA repairs (row, query head) tasks, selecting A_t of the task's row itself
+  // from the candidate list, so the repair waits for no further barrier.
+  const bool p_role = roles && cta >= rows && cta < 2 * rows;
+  const int rep_first = !roles ? cta : p_role ? -1 : (cta < rows ? cta : cta - rows);
+  const int rep_step = roles ? grid - rows : grid;
+  // addresses a role reads first after the barrier
+  if (tid == 0 && roles) {
+    if (p_role) {
+      const int row = cta - rows;
+      prefetch_l2(a.cand_cnt2 + row);
+      prefetch_l2(a.cand2 + static_cast<size_t>(row) * kCandCap);
+      prefetch_l2(a.next_idx + static_cast<size_t>(row) * a.k_pred);
+      prefetch_l2(a.next_count + row);
+    } else if (rep_first < rows * G) {
+      const int row = rep_first / G;
+      prefetch_l2(a.cand_cnt + row);
+      prefetch_l2(a.cand + static_cast<size_t>(row) * kCandCap);
+    }
   }
   if (!grid_barrier(a.sync + 0, gridDim.x, abort_flag, kv.status)) {
     // gave up: wait (bounded) for this CTA's page loads still in flight before exiting
@@ -660,17 +673,16 @@ __global__ void __launch_bounds__(kPThreads, 1)
   }
 
   // ================================================================ phase 2
-  // CTAs [0, rows) select A_t (phase 3 waits for them); CTAs [rows, 2 rows) update the EMA and
-  // select P_{t+1}, which only the next step reads: they arrive at the second barrier at once and
-  // run beside phase 3.  Rows are read as float4, four per thread in flight.
-  uint32_t* keys = reinterpret_cast<uint32_t*>(smem);
+  // With the roles, CTAs [rows, 2 rows) select P_{t+1} (and update the EMA unless scoring did),
+  // which only the next step reads, beside the repair.  Rows are read as float4, four per thread
+  // in flight.
+  uint32_t* keys = reinterpret_cast<uint32_t*>(smem + lay.keys_off);
   const bool vec4 = (n & 3) == 0 &&
                     ((reinterpret_cast<uintptr_t>(a.scores) | reinterpret_cast<uintptr_t>(a.ell) |
                       reinterpret_cast<uintptr_t>(a.trend) |
                       reinterpret_cast<uintptr_t>(a.pred)) & 15) == 0;
-  // with more than 2 rows CTAs: CTA r < rows selects row r, CTA rows + r selects P_{t+1} of row r
-  // (and updates its EMA unless scoring did), the rest wait and repair; with fewer CTAs everyone
-  // selects, waits, then updates and repairs
+  // Without the roles (2 rows CTAs or fewer) everyone selects A_t of its rows, waits, then
+  // updates the EMA and repairs.
   auto select_into = [&](int kk, int32_t* out, int32_t* cnt, KeyStats st) {
     __syncthreads();
     const int total = select_topk_block<kPThreads>(keys, n, kk, out, sel_scratch, st);
@@ -806,29 +818,31 @@ __global__ void __launch_bounds__(kPThreads, 1)
       select_into(a.k_pred, out, a.next_count + row, st);
     }
   };
-  auto select_row = [&](int row) {
+  // A_t of a row into out[0, k) (ascending, -1 past the count); returns the count.  The top-k of
+  // the candidates that scored at or above T0 (exact, see scoring), else of the whole row.
+  // `side` is work that overlaps the ranking (after it in the whole-row case, whose keys share the
+  // record area).
+  auto select_a = [&](int row, int32_t* out, auto&& side) -> int {
     const size_t base = static_cast<size_t>(row) * n;
-    KeyStats st;
-    __syncthreads();  // keys of a previous task are no longer read
+    __syncthreads();  // keys / scratch of a previous task are no longer read
     // the list up to its capacity is read together with its count (one round trip)
     const unsigned C = __ldcg(a.cand_cnt + row);
     {
       const uint2* cr = a.cand + static_cast<size_t>(row) * kCandCap;
       for (int i = tid; i < kCandCap; i += kPThreads) {
         const uint2 e = __ldcg(cr + i);
-        sel_scratch.small.ckey[i] = e.x;
-        sel_scratch.small.cidx[i] = static_cast<int>(e.y);
+        ts.ckey[i] = e.x;
+        ts.cidx[i] = static_cast<int>(e.y);
       }
     }
     if (C <= static_cast<unsigned>(kCandCap)) {
+      side();
       __syncthreads();
-      int32_t* out = a.idx + static_cast<size_t>(row) * a.k;
-      const int total =
-          topk_candidates<kPThreads>(static_cast<int>(C), a.k, n, out, sel_scratch.small);
+      const int total = topk_candidates<kPThreads>(static_cast<int>(C), a.k, n, out, ts);
       for (int i = total + tid; i < a.k; i += kPThreads) out[i] = -1;
-      if (tid == 0) a.count[row] = total;
-      return;
+      return total;
     }
+    KeyStats st;
     if (vec4) {
       const int n4 = n >> 2;
       for (int i0 = tid; i0 < n4; i0 += 8 * kPThreads) {
@@ -858,16 +872,16 @@ __global__ void __launch_bounds__(kPThreads, 1)
         st.add(keys[j]);
       }
     }
-    select_into(a.k, a.idx + static_cast<size_t>(row) * a.k, a.count + row, st);
+    __syncthreads();
+    const int total = select_topk_block<kPThreads>(keys, n, a.k, out, sel_scratch, st);
+    __syncthreads();  // the keys are no longer read
+    side();
+    return total;
   };
-  // Phase 3 tasks of this CTA: (row, query head) pairs; with the phase-2 roles, only the CTAs past
-  // them repair.  A task's P_t and query head do not depend on phase 2: the first task's are
-  // fetched before waiting at the second barrier.
-  const int rep_first = roles ? static_cast<int>(blockIdx.x) - 2 * rows : blockIdx.x;
-  const int rep_step = roles ? static_cast<int>(gridDim.x) - 2 * rows : gridDim.x;
   // membership bitmaps over page positions [0, n): P_t's and A_t's
   const int bm_words = (n + 31) >> 5;
-  auto fetch_task = [&](int task) {
+  // a repair task's lists: P_t (positions and bitmap), the query head; A_t's bitmap cleared
+  auto fetch_lists = [&](int task) {
     int32_t* sP = reinterpret_cast<int32_t*>(smem + lay.sp_off);
     float* qh = reinterpret_cast<float*>(smem + lay.qh_off);
     uint32_t* bmP = reinterpret_cast<uint32_t*>(smem + lay.bmp_off);
@@ -888,33 +902,21 @@ __global__ void __launch_bounds__(kPThreads, 1)
       sP[i] = pos;
       if (pos >= 0 && pos < n) atomicOr(&bmP[pos >> 5], 1u << (pos & 31));
     }
-    // the speculative records of this query head (phase 1 wrote them before the first barrier)
-    float* srec = reinterpret_cast<float*>(smem + lay.rec_off);
-    for (int e = tid; e < cntP * (kRecordFloats / 4); e += kPThreads) {
-      const int i = e / (kRecordFloats / 4), c = e - i * (kRecordFloats / 4);
-      const float4 v = __ldcg(reinterpret_cast<const float4*>(
-                                  a.partials + ((static_cast<size_t>(row) * a.k_pred + i) * G + g) *
-                                                   kRecordFloats) +
-                              c);
-      *reinterpret_cast<float4*>(srec + i * kRecordFloats + c * 4) = v;
+  };
+  // the speculative records of a task's query head (phase 1 wrote them before the first
+  // barrier), copied asynchronously into shared memory: complete after cp_async_wait_all
+  auto fetch_records = [&](int task) {
+    const int row = task / G, g = task - row * G;
+    const int cntP = min(max(a.spec_count[row], 0), a.k_pred);
+    const uint32_t srec = smem_u32(smem + lay.rec_off);
+    constexpr int kPieces = kRecordFloats / 4;  // 16-byte pieces of a record
+    for (int e = tid; e < cntP * kPieces; e += kPThreads) {
+      const int i = e / kPieces, c = e - i * kPieces;
+      cp_async16(srec + static_cast<uint32_t>(i * kRecordFloats + c * 4) * 4u,
+                 a.partials + ((static_cast<size_t>(row) * a.k_pred + i) * G + g) * kRecordFloats +
+                     c * 4);
     }
   };
-  const bool prefetch_first = roles && rep_first >= 0 && rep_first < rows * G;
-  if (prefetch_first) {
-    fetch_task(rep_first);
-    // addresses the first task reads and writes after the barrier
-    if (tid == 0) {
-      const int row = rep_first / G, g = rep_first - row * G;
-      const int b = row / kv.Hkv, h = row % kv.Hkv;
-      const size_t qhead = static_cast<size_t>(b) * kv.Hq + static_cast<size_t>(h) * G + g;
-      prefetch_l2(a.count + row);
-      prefetch_l2(a.idx + static_cast<size_t>(row) * a.k);
-      prefetch_l2(a.out + qhead * kHeadDim);
-      prefetch_l2(a.m + qhead);
-      prefetch_l2(a.l + qhead);
-      prefetch_l2(kv.page_table + static_cast<size_t>(b) * kv.max_pages);
-    }
-  }
 
   // P_{t+1} of a row whose EMA update rode along with scoring: rank the candidates, or (no
   // bound, or too many candidates) recompute the row's predictions from the old state, which is
@@ -949,31 +951,19 @@ __global__ void __launch_bounds__(kPThreads, 1)
     }
     select_into(a.k_pred, out, a.next_count + row, st);
   };
-  if (ema1) {
-    if (static_cast<int>(blockIdx.x) < rows) select_row(blockIdx.x);
-    else if (static_cast<int>(blockIdx.x) < 2 * rows) next_row(blockIdx.x - rows);
-    if (!grid_barrier(a.sync + 1, gridDim.x, abort_flag, kv.status)) return;
-    // the staged EMA updates of this CTA's share (every read of the old state is behind us)
-    const int cnt = static_cast<int>(s_end - s_beg);
-    for (int i = tid; i < cnt; i += kPThreads) {
-      a.ell[s_beg + i] = st_ell[i];
-      a.trend[s_beg + i] = st_v[i];
-      if (a.pred) a.pred[s_beg + i] = st_pred[i];
+  if (p_role) {
+    if (ema1) next_row(cta - rows);
+    else ema_row(cta - rows);
+    // counts the P_{t+1} CTAs past their reads of the old EMA state (the staged updates wait
+    // for all of them)
+    grid_arrive(a.sync + 1, abort_flag);
+  } else if (!roles) {
+    for (int row = cta; row < rows; row += grid) {
+      const int total = select_a(row, a.idx + static_cast<size_t>(row) * a.k, [] {});
+      if (tid == 0) a.count[row] = total;
     }
-  } else if (roles) {
-    if (static_cast<int>(blockIdx.x) < rows) {
-      select_row(blockIdx.x);
-      grid_arrive(a.sync + 1, abort_flag);
-    } else if (static_cast<int>(blockIdx.x) < 2 * rows) {
-      grid_arrive(a.sync + 1, abort_flag);
-      ema_row(blockIdx.x - rows);
-    } else if (!grid_barrier(a.sync + 1, gridDim.x, abort_flag, kv.status)) {
-      return;
-    }
-  } else {
-    for (int row = blockIdx.x; row < rows; row += gridDim.x) select_row(row);
     if (!grid_barrier(a.sync + 1, gridDim.x, abort_flag, kv.status)) return;
-    for (int row = blockIdx.x; row < rows; row += gridDim.x) ema_row(row);
+    for (int row = cta; row < rows; row += grid) ema_row(row);
   }
 
   // ================================================================ phase 3
@@ -995,19 +985,32 @@ __global__ void __launch_bounds__(kPThreads, 1)
     const int npos = (L + page - 1) / page;
     const size_t qhead = static_cast<size_t>(b) * kv.Hq + static_cast<size_t>(h) * G + g;
     const int cntP = min(max(a.spec_count[row], 0), a.k_pred);
-    if (task != rep_first || !prefetch_first) {  // else fetched before the second barrier
-      __syncthreads();  // shared lists of a previous task are no longer read
-      fetch_task(task);
-    }
+    __syncthreads();  // shared lists of a previous task are no longer read
+    fetch_lists(task);
     uint32_t* bmP = reinterpret_cast<uint32_t*>(smem + lay.bmp_off);
     uint32_t* bmA = reinterpret_cast<uint32_t*>(smem + lay.bma_off);
-    // the whole index row at once (slots past the count hold -1), together with the count
-    const int cntA = min(max(__ldcg(a.count + row), 0), a.k);
-    for (int i = tid; i < a.k; i += kPThreads) {
-      const int pos = __ldcg(a.idx + static_cast<size_t>(row) * a.k + i);
-      sA[i] = pos;
-      if (i < cntA && pos >= 0 && pos < n) atomicOr(&bmA[pos >> 5], 1u << (pos & 31));
+    int cntA;
+    if (roles) {
+      cntA = select_a(row, sA, [&] { fetch_records(task); });
+      __syncthreads();  // sA is complete
+      if (g == 0) {  // the task of the row's first query head publishes A_t
+        for (int i = tid; i < a.k; i += kPThreads) a.idx[static_cast<size_t>(row) * a.k + i] = sA[i];
+        if (tid == 0) a.count[row] = cntA;
+      }
+    } else {
+      fetch_records(task);
+      // the whole index row at once (slots past the count hold -1), together with the count
+      cntA = __ldcg(a.count + row);
+      for (int i = tid; i < a.k; i += kPThreads)
+        sA[i] = __ldcg(a.idx + static_cast<size_t>(row) * a.k + i);
+      __syncthreads();
     }
+    cntA = min(max(cntA, 0), a.k);
+    for (int i = tid; i < cntA; i += kPThreads) {
+      const int pos = sA[i];
+      if (pos >= 0 && pos < n) atomicOr(&bmA[pos >> 5], 1u << (pos & 31));
+    }
+    cp_async_wait_all();  // this thread's record pieces
     __syncthreads();
     auto in_bm = [&](const uint32_t* bm, int pos) {
       return pos >= 0 && pos < n && ((bm[pos >> 5] >> (pos & 31)) & 1u);
@@ -1154,6 +1157,18 @@ __global__ void __launch_bounds__(kPThreads, 1)
         a.m[qhead] = lsum > 0.f ? M * kLn2 : -INFINITY;
         a.l[qhead] = lsum;
       }
+    }
+  }
+
+  if (ema1) {
+    // the staged EMA updates of this CTA's share, once every P_{t+1} CTA is past its reads of
+    // the old state
+    if (!grid_wait(a.sync + 1, rows, abort_flag, kv.status)) return;
+    const int cnt = static_cast<int>(s_end - s_beg);
+    for (int i = tid; i < cnt; i += kPThreads) {
+      a.ell[s_beg + i] = st_ell[i];
+      a.trend[s_beg + i] = st_v[i];
+      if (a.pred) a.pred[s_beg + i] = st_pred[i];
     }
   }
 
