@@ -659,7 +659,13 @@ __global__ void __launch_bounds__(kPThreads, 1)
       prefetch_l2(a.cand + static_cast<size_t>(row) * kCandCap);
     }
   }
-  if (!grid_barrier(a.sync + 0, gridDim.x, abort_flag, kv.status)) {
+  // A scout without a repair task of its own rehearses one (its writes suppressed) between its
+  // arrival at the first barrier and the end: the repair code is then in L2 when the repair CTAs
+  // reach it after the barrier.  It needs nothing behind the barrier.
+  const bool rehearse =
+      roles && scout && !p_role && !(rep_first >= 0 && rep_first < rows * G) && rows * G > 0;
+  grid_arrive(a.sync + 0, abort_flag);
+  if (!rehearse && !grid_wait(a.sync + 0, gridDim.x, abort_flag, kv.status)) {
     // gave up: wait (bounded) for this CTA's page loads still in flight before exiting
     if (tid == 0) {
       const int n_iss = *reinterpret_cast<volatile int*>(&s_issued);
@@ -825,14 +831,16 @@ __global__ void __launch_bounds__(kPThreads, 1)
   auto select_a = [&](int row, int32_t* out, auto&& side) -> int {
     const size_t base = static_cast<size_t>(row) * n;
     __syncthreads();  // keys / scratch of a previous task are no longer read
-    // the list up to its capacity is read together with its count (one round trip)
+    // the list up to its capacity is read together with its count (one round trip); the entries
+    // below the count index pages < n, and the clamp keeps a rehearsal, which reads the list while
+    // it is still being appended to, inside the bitmap
     const unsigned C = __ldcg(a.cand_cnt + row);
     {
       const uint2* cr = a.cand + static_cast<size_t>(row) * kCandCap;
       for (int i = tid; i < kCandCap; i += kPThreads) {
         const uint2 e = __ldcg(cr + i);
         ts.ckey[i] = e.x;
-        ts.cidx[i] = static_cast<int>(e.y);
+        ts.cidx[i] = static_cast<int>(min(e.y, static_cast<unsigned>(n - 1)));
       }
     }
     if (C <= static_cast<unsigned>(kCandCap)) {
@@ -931,7 +939,7 @@ __global__ void __launch_bounds__(kPThreads, 1)
       for (int i = tid; i < kCandCap; i += kPThreads) {
         const uint2 e = __ldcg(cr + i);
         ts.ckey[i] = e.x;
-        ts.cidx[i] = static_cast<int>(e.y);
+        ts.cidx[i] = static_cast<int>(min(e.y, static_cast<unsigned>(n - 1)));
       }
     }
     if (C <= static_cast<unsigned>(kCandCap)) {
@@ -978,7 +986,10 @@ __global__ void __launch_bounds__(kPThreads, 1)
   float* qh = reinterpret_cast<float*>(smem + lay.qh_off);
   float* wst = reinterpret_cast<float*>(smem + lay.ws_off);  // [warp][m, l, -, -, O[128]]
   constexpr int kWs = kHeadDim + 4;
-  for (int task = rep_first; task >= 0 && task < rows * G; task += rep_step) {
+  const bool dry = rehearse;
+  const int task0 = dry ? (cta / kScoutEvery) % (rows * G) : rep_first;
+  const int task_step = dry ? rows * G : rep_step;
+  for (int task = task0; task >= 0 && task < rows * G; task += task_step) {
     const int row = task / G, g = task - row * G;
     const int b = row / kv.Hkv, h = row % kv.Hkv;
     const int L = request_len(kv, b);
@@ -993,7 +1004,7 @@ __global__ void __launch_bounds__(kPThreads, 1)
     if (roles) {
       cntA = select_a(row, sA, [&] { fetch_records(task); });
       __syncthreads();  // sA is complete
-      if (g == 0) {  // the task of the row's first query head publishes A_t
+      if (g == 0 && !dry) {  // the task of the row's first query head publishes A_t
         for (int i = tid; i < a.k; i += kPThreads) a.idx[static_cast<size_t>(row) * a.k + i] = sA[i];
         if (tid == 0) a.count[row] = cntA;
       }
@@ -1044,7 +1055,8 @@ __global__ void __launch_bounds__(kPThreads, 1)
       if (lane == 0) s_red[1] = nm;
     }
     __syncthreads();
-    const int n_parts = s_red[0], n_miss = s_red[1];
+    const int n_parts = s_red[0];
+    const int n_miss = dry ? min(s_red[1], 1) : s_red[1];  // a rehearsal attends one page at most
 
     float wm = -INFINITY, wl = 0.f;  // this warp's state: max (log2 units), sum, unnormalised O
     float4 wo = make_float4(0.f, 0.f, 0.f, 0.f);
@@ -1152,8 +1164,9 @@ __global__ void __launch_bounds__(kPThreads, 1)
         lsum += lw * f;
         o += wst[w * kWs + 4 + tid] * f;
       }
-      a.out[qhead * kHeadDim + tid] = lsum > 0.f ? o / lsum : 0.f;
-      if (tid == 0) {
+      const float ov = lsum > 0.f ? o / lsum : 0.f;
+      if (!dry) a.out[qhead * kHeadDim + tid] = ov;
+      if (tid == 0 && !dry) {
         a.m[qhead] = lsum > 0.f ? M * kLn2 : -INFINITY;
         a.l[qhead] = lsum;
       }
