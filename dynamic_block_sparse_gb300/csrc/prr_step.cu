@@ -196,13 +196,44 @@ __global__ void __launch_bounds__(kPThreads, 1)
   // roles of phase 2; its writes wait for the second barrier (until then the old state is read)
   const bool roles = grid > 2 * rows;
   const bool ema1 = roles && (T + scorers - 1) / scorers <= kEmaCap;
+  // Roles after the first barrier (with more than 2 rows CTAs): CTA rows + r selects P_{t+1} of
+  // row r; every other CTA repairs (row, query head) tasks, selecting A_t of the task's row itself
+  // from the candidate list, so the repair waits for no further barrier.
+  const bool p_role = roles && cta >= rows && cta < 2 * rows;
+  const int rep_first = !roles ? cta : p_role ? -1 : (cta < rows ? cta : cta - rows);
+  const int rep_step = roles ? grid - rows : grid;
+  // A scout without a repair task of its own rehearses one (its writes suppressed) between its
+  // arrival at the first barrier and the end: the repair code is then in L2 when the repair CTAs
+  // reach it after the barrier.  It needs nothing behind the barrier.  The odd-numbered ones past
+  // every repair task (CTA >= rows (G + 1)) attend no speculative pages either and rehearse from
+  // the start; the speculative items go round-robin over the other CTAs.
+  const bool rehearse =
+      roles && scout && !p_role && !(rep_first >= 0 && rep_first < rows * G) && rows * G > 0;
+  const bool dry = rehearse;
+  auto early_rehearser = [&](int c) {
+    return roles && scouts && c % kScoutEvery == 0 && (c / kScoutEvery) % 2 == 1 &&
+           c >= rows * (G + 1);
+  };
+  int n_early = 0, early_before = 0;
+  for (int c = kScoutEvery; c < grid; c += 2 * kScoutEvery)
+    if (early_rehearser(c)) {
+      ++n_early;
+      if (c < cta) ++early_before;
+    }
+  const bool early = early_rehearser(cta);
+  const int item_ctas = grid - n_early;
+  // rank among the CTAs with speculative items: the scouts first, so that the ones left with an
+  // extra item (the first items % item_ctas) are CTAs that do not score
+  const int n_scouts = scouts ? (grid + kScoutEvery - 1) / kScoutEvery : 0;
+  const int irank = !scouts ? cta
+                    : scout ? cta / kScoutEvery - early_before
+                            : n_scouts - n_early + rank;
   uint64_t* bars = reinterpret_cast<uint64_t*>(smem + lay.bar_off);  // [S] full, [S] empty
   volatile int* stage_ok = reinterpret_cast<int*>(smem + lay.ctl_off);  // [S]: -1 none, 0, 1
   volatile int* stage_pos = stage_ok + kPStages;
   if (warp == 1 && lane < 8) {
     // phase 1 reads these first: start their address translations at once
-    const long long T0 = static_cast<long long>(rows) * n;
-    const long long sb = static_cast<long long>(blockIdx.x) * T0 / gridDim.x;
+    const long long sb = s_beg;
     const int row = static_cast<int>(sb / n);
     const int b = row / kv.Hkv;
     const void* p = nullptr;
@@ -229,9 +260,8 @@ __global__ void __launch_bounds__(kPThreads, 1)
   }
   __syncthreads();
   const int n_items_total = rows * a.k_pred;
-  const int my_items = blockIdx.x < static_cast<unsigned>(n_items_total)
-                           ? (n_items_total - 1 - static_cast<int>(blockIdx.x)) / gridDim.x + 1
-                           : 0;
+  const int my_items =
+      !early && irank < n_items_total ? (n_items_total - 1 - irank) / item_ctas + 1 : 0;
 
   if (warp == kPW) {
     // ---- TMA issue warp: the speculative pages of this CTA's items
@@ -239,7 +269,7 @@ __global__ void __launch_bounds__(kPThreads, 1)
       prefetch_tensormap(&tmK);
       prefetch_tensormap(&tmV);
       for (int j = 0; j < my_items; ++j) {
-        const int it = blockIdx.x + j * gridDim.x;
+        const int it = irank + j * item_ctas;
         const int row = it / a.k_pred, slot = it - row * a.k_pred;
         const int b = row / kv.Hkv, h = row % kv.Hkv;
         const int s = j % kPStages, u = j / kPStages;
@@ -273,7 +303,7 @@ __global__ void __launch_bounds__(kPThreads, 1)
     // (row tid / 16, dims 8 (tid % 16) ...; rows past the group are zero).  The first item's are
     // copied before scoring, so they are on chip when its page lands.
     auto stage_q = [&](int j) {
-      const int row = static_cast<int>(blockIdx.x + j * gridDim.x) / a.k_pred;
+      const int row = (irank + j * item_ctas) / a.k_pred;
       const int b = row / kv.Hkv, h = row % kv.Hkv;
       const int r = tid >> 4, c = tid & 15;
       __nv_bfloat16* dst = sQ + r * kQStride + c * 8;
@@ -531,7 +561,7 @@ __global__ void __launch_bounds__(kPThreads, 1)
     // ---- speculative per-page attention of this CTA's items
     auto spec_items = [&]() {
       for (int j = 0; j < my_items; ++j) {
-        const int it = blockIdx.x + j * gridDim.x;
+        const int it = irank + j * item_ctas;
         const int row = it / a.k_pred, slot = it - row * a.k_pred;
         const int b = row / kv.Hkv, h = row % kv.Hkv;
         const int L = request_len(kv, b);
@@ -639,12 +669,6 @@ __global__ void __launch_bounds__(kPThreads, 1)
     score_share();
     spec_items();
   }
-  // Roles after the first barrier (with more than 2 rows CTAs): CTA rows + r selects P_{t+1} of
-  // row r; every other CTA repairs (row, query head) tasks, selecting A_t of the task's row itself
-  // from the candidate list, so the repair waits for no further barrier.
-  const bool p_role = roles && cta >= rows && cta < 2 * rows;
-  const int rep_first = !roles ? cta : p_role ? -1 : (cta < rows ? cta : cta - rows);
-  const int rep_step = roles ? grid - rows : grid;
   // addresses a role reads first after the barrier
   if (tid == 0 && roles) {
     if (p_role) {
@@ -659,11 +683,6 @@ __global__ void __launch_bounds__(kPThreads, 1)
       prefetch_l2(a.cand + static_cast<size_t>(row) * kCandCap);
     }
   }
-  // A scout without a repair task of its own rehearses one (its writes suppressed) between its
-  // arrival at the first barrier and the end: the repair code is then in L2 when the repair CTAs
-  // reach it after the barrier.  It needs nothing behind the barrier.
-  const bool rehearse =
-      roles && scout && !p_role && !(rep_first >= 0 && rep_first < rows * G) && rows * G > 0;
   grid_arrive(a.sync + 0, abort_flag);
   if (!rehearse && !grid_wait(a.sync + 0, gridDim.x, abort_flag, kv.status)) {
     // gave up: wait (bounded) for this CTA's page loads still in flight before exiting
@@ -834,7 +853,9 @@ __global__ void __launch_bounds__(kPThreads, 1)
     // the list up to its capacity is read together with its count (one round trip); the entries
     // below the count index pages < n, and the clamp keeps a rehearsal, which reads the list while
     // it is still being appended to, inside the bitmap
-    const unsigned C = __ldcg(a.cand_cnt + row);
+    unsigned C = __ldcg(a.cand_cnt + row);
+    // a rehearsal ranks at least 2k entries (whatever the list holds), so that code runs
+    if (dry) C = min(max(C, static_cast<unsigned>(2 * a.k)), static_cast<unsigned>(kCandCap));
     {
       const uint2* cr = a.cand + static_cast<size_t>(row) * kCandCap;
       for (int i = tid; i < kCandCap; i += kPThreads) {
@@ -986,7 +1007,6 @@ __global__ void __launch_bounds__(kPThreads, 1)
   float* qh = reinterpret_cast<float*>(smem + lay.qh_off);
   float* wst = reinterpret_cast<float*>(smem + lay.ws_off);  // [warp][m, l, -, -, O[128]]
   constexpr int kWs = kHeadDim + 4;
-  const bool dry = rehearse;
   const int task0 = dry ? (cta / kScoutEvery) % (rows * G) : rep_first;
   const int task_step = dry ? rows * G : rep_step;
   for (int task = task0; task >= 0 && task < rows * G; task += task_step) {
