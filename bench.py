@@ -360,7 +360,9 @@ def bench_prr(args, w, dev, rank):
         _entry("step-staged", w.name, "PRR decode step, separate launches on three streams",
                staged_ms, bytes_step, peak),
     ]
-    return dict(rows=prr_rows, mean_ms=mean_ms, bytes_step=bytes_step, clocks=clocks,
+    return dict(rows=prr_rows, mean_ms=mean_ms, p50_ms=statistics.median(step_ms),
+                p90_ms=sorted(step_ms)[int(0.9 * (len(step_ms) - 1))], bytes_step=bytes_step,
+                clocks=clocks,
                 dominant=dominant, dominant_ms=mean_ms, dominant_bytes=bytes_step, e2e=e2e,
                 launches_per_step=1, extra=extra)
 
@@ -719,6 +721,7 @@ def main():
     line = {
         "metric": METRIC, "value": value, "unit": "GB/s", "n_gpus": world, "steps": args.steps,
         "warmup": args.warmup, "ms_per_step": mean_ms, "us_per_step": mean_ms * 1e3,
+        "us_per_step_p50": res["p50_ms"] * 1e3, "us_per_step_p90": res["p90_ms"] * 1e3,
         "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "bf16",
         "data": "synthetic", "config": config,
         "roofline": {"bound": "hbm", "kernel": res["dominant"], "achieved": achieved,

@@ -158,6 +158,7 @@ __global__ void __launch_bounds__(kPThreads, 1)
   __shared__ SelectAnyScratch<kPThreads> sel_scratch;
   __shared__ int s_abort, s_issued, s_red[33];
   __shared__ unsigned s_t0key, s_t1key;
+  __shared__ unsigned s_cand[4];  // scoring's candidate counts of a round: CTA-local, CTA base
   __shared__ float s_f[kPWarps];
   const KvView& kv = a.kv;
   const int page = kv.p, G = kv.G, tiles = page / 16;
@@ -256,6 +257,8 @@ __global__ void __launch_bounds__(kPThreads, 1)
     }
     fence_mbar_init();
     s_abort = 0;
+    s_cand[0] = 0u;
+    s_cand[1] = 0u;
     s_issued = 0;
   }
   __syncthreads();
@@ -308,7 +311,8 @@ __global__ void __launch_bounds__(kPThreads, 1)
       const int r = tid >> 4, c = tid & 15;
       __nv_bfloat16* dst = sQ + r * kQStride + c * 8;
       if (r < G)
-        cp_async16(smem_u32(dst), a.q + (static_cast<size_t>(b) * kv.Hq + h * G + r) * kHeadDim + c * 8);
+        cp_async16(smem_u32(dst),
+                   a.q + (static_cast<size_t>(b) * kv.Hq + h * G + r) * kHeadDim + c * 8);
       else
         *reinterpret_cast<uint4*>(dst) = make_uint4(0, 0, 0, 0);
     };
@@ -360,21 +364,22 @@ __global__ void __launch_bounds__(kPThreads, 1)
         if (tid < kHeadDim) {
           const __nv_bfloat16* qg = a.q + (static_cast<size_t>(b) * kv.Hq + h * G) * kHeadDim;
           __nv_bfloat16 qr[16];  // G <= 16: all loads in flight, then the sum in row order
-  #pragma unroll
-          for (int r = 0; r < 16; ++r) qr[r] = r < G ? qg[r * kHeadDim + tid] : __float2bfloat16(0.f);
-  #pragma unroll
+#pragma unroll
+          for (int r = 0; r < 16; ++r)
+            qr[r] = r < G ? qg[r * kHeadDim + tid] : __float2bfloat16(0.f);
+#pragma unroll
           for (int r = 0; r < 16; ++r)
             if (r < G) qacc += __bfloat162float(qr[r]);
         }
         int ppos[kPB];
-  #pragma unroll
+#pragma unroll
         for (int i = 0; i < kPB; ++i) {
           const int sl = gid + kPGroups * i;
           ppos[i] = sl < cntP ? P[sl] : -1;
         }
         int cph[kCB];
         float cl[kCB], cvv[kCB];
-  #pragma unroll
+#pragma unroll
         for (int i = 0; i < kCB; ++i) {
           const int jj = j0 + gid + kPGroups * i;
           cph[i] = jj < j1 && jj < nl ? table[jj] : -1;
@@ -391,12 +396,12 @@ __global__ void __launch_bounds__(kPThreads, 1)
         group_query_dims(qbar, gl, qv);
 
         // ---- wave 2
-  #pragma unroll
+#pragma unroll
         for (int i = 0; i < kCB; ++i)
           if (cph[i] >= 0 && cph[i] < kv.num_phys)
             stage_record(static_cast<size_t>(cph[i]) * kv.Hkv + h, gid + kPGroups * i);
         int pph[kPB];
-  #pragma unroll
+#pragma unroll
         for (int i = 0; i < kPB; ++i) {
           const int pos = ppos[i];
           pph[i] = pos >= 0 && pos < nl ? table[pos] : -1;
@@ -404,12 +409,13 @@ __global__ void __launch_bounds__(kPThreads, 1)
         float cs[kCB];
 
         // ---- wave 3 (P_t's records, kPR per group at a time)
-  #pragma unroll
+#pragma unroll
         for (int i0 = 0; i0 < kPB; i0 += kPR) {
-          if (i0 > 0 && warp * 4 + kPGroups * i0 >= cntP) break;  // warp-uniform: none of its slots left
+          // warp-uniform: none of the warp's slots left
+          if (i0 > 0 && warp * 4 + kPGroups * i0 >= cntP) break;
           uint4 rp[kPR][4];
           float pl[kPR], pv[kPR];  // the old EMA state of those pages
-  #pragma unroll
+#pragma unroll
           for (int u = 0; u < kPR; ++u) {
             const int pos = ppos[i0 + u];
             if (pph[i0 + u] >= 0 && pph[i0 + u] < kv.num_phys)
@@ -419,7 +425,7 @@ __global__ void __launch_bounds__(kPThreads, 1)
           }
           if (i0 == 0) {  // the chunk's scores while P_t's first records are in flight
             cp_async_wait_all();
-  #pragma unroll
+#pragma unroll
             for (int i = 0; i < kCB; ++i) {
               const bool ok = cph[i] >= 0 && cph[i] < kv.num_phys;
               uint4 rc[4];
@@ -427,7 +433,7 @@ __global__ void __launch_bounds__(kPThreads, 1)
               cs[i] = group_sum(ok ? record_partial<DSA_META_MINMAX>(rc, qv) : 0.f);
             }
           }
-  #pragma unroll
+#pragma unroll
           for (int u = 0; u < kPR; ++u) {
             const int i = i0 + u, sl = gid + kPGroups * i;
             const bool ok = pph[i] >= 0 && pph[i] < kv.num_phys;
@@ -453,41 +459,33 @@ __global__ void __launch_bounds__(kPThreads, 1)
         // selection after the barrier ranks only them (exactly).  T0' likewise for the predictions
         // and P_{t+1} (from the old EMA state).  A missing bound (fewer than k scored pages in P_t)
         // marks the row's list overflowed, and the selection scans every score.
-        auto kth_key = [&](const uint32_t* keys, int kk, unsigned* result) {
-          for (int i = tid; i < cntP; i += kPW * 32) {
-            const uint32_t ki = keys[i];
-            if (ki == 0u) continue;
-            int ge = 0;
-            for (int q0 = 0; q0 < cntP; q0 += 8) {
-              uint32_t kj[8];
-  #pragma unroll
-              for (int u = 0; u < 8; ++u) kj[u] = q0 + u < cntP ? keys[q0 + u] : 0u;
-  #pragma unroll
-              for (int u = 0; u < 8; ++u) ge += kj[u] >= ki;
+        // (both ranks in one pass over P_t's keys)
+        for (int i = tid; i < cntP; i += kPW * 32) {
+          const uint32_t ki = spk[i], pi = ema1 ? ppk[i] : 0u;
+          int ge = 0, gp = 0;
+          for (int q0 = 0; q0 < cntP; q0 += 8) {
+            uint32_t kj[8], pj[8];
+#pragma unroll
+            for (int u = 0; u < 8; ++u) {
+              kj[u] = q0 + u < cntP ? spk[q0 + u] : 0u;
+              pj[u] = ema1 && q0 + u < cntP ? ppk[q0 + u] : 0u;
             }
-            if (ge >= kk) atomicMax(result, ki);
+#pragma unroll
+            for (int u = 0; u < 8; ++u) {
+              ge += kj[u] >= ki;
+              gp += pj[u] >= pi;
+            }
           }
-        };
-        kth_key(spk, a.k, &s_t0key);
-        if (ema1) kth_key(ppk, a.k_pred, &s_t1key);
+          if (ki != 0u && ge >= a.k) atomicMax(&s_t0key, ki);
+          if (pi != 0u && gp >= a.k_pred) atomicMax(&s_t1key, pi);
+        }
         named_barrier(1, kPW * 32);
         const uint32_t t0key = s_t0key;
         const uint32_t t1key = ema1 ? s_t1key : 0u;
-        if (tid == 0 && t0key == 0u) atomicAdd(a.cand_cnt + row, static_cast<unsigned>(kCandCap + 1));
+        if (tid == 0 && t0key == 0u)
+          atomicAdd(a.cand_cnt + row, static_cast<unsigned>(kCandCap + 1));
         if (tid == 0 && ema1 && t1key == 0u)
           atomicAdd(a.cand_cnt2 + row, static_cast<unsigned>(kCandCap + 1));
-        // appends the lanes' candidates (lanes with gl == 0 hold a record's score) to a row's list:
-        // one counter update per warp
-        auto append = [&](unsigned* cnt, uint2* list, bool c, int j, uint32_t key) {
-          const unsigned bal = __ballot_sync(0xffffffffu, c);
-          if (bal == 0u) return;
-          unsigned base = 0;
-          if (lane == 0) base = atomicAdd(cnt + row, static_cast<unsigned>(__popc(bal)));
-          base = __shfl_sync(0xffffffffu, base, 0);
-          const unsigned at = base + __popc(bal & ((1u << lane) - 1u));
-          if (c && at < static_cast<unsigned>(kCandCap))
-            list[static_cast<size_t>(row) * kCandCap + at] = make_uint2(key, j);
-        };
         const long long stage0 = static_cast<long long>(row) * n - s_beg;  // staging index of j = 0
         // the EMA update of page j with score s (staged until the second barrier); returns the key
         // of the prediction
@@ -501,59 +499,104 @@ __global__ void __launch_bounds__(kPThreads, 1)
           st_pred[at] = pr;
           return score_key(pr);
         };
-        // a scored chunk slot: output, candidate for A_t, EMA update and candidate for P_{t+1}
-        auto finish_slot = [&](int jj, bool ok, float sc, float l_old, float v_old) {
-          const bool mine = gl == 0 && jj < j1;
-          const float is = ok ? sc : -INFINITY;
-          if (mine) outs[jj] = is;
-          const uint32_t kA = ok ? score_key(sc) : 0u;
-          append(a.cand_cnt, a.cand, t0key != 0u && mine && kA != 0u && kA >= t0key, jj, kA);
-          if (ema1) {
-            const uint32_t pk = mine ? ema_page(jj, is, l_old, v_old) : 0u;
-            append(a.cand_cnt2, a.cand2, t1key != 0u && pk != 0u && pk >= t1key, jj, pk);
+        // A round of kCB scored chunk slots per group (lanes with gl == 0 hold a record's score):
+        // the outputs, the EMA updates, and the candidates for A_t and P_{t+1}, appended to the
+        // row's lists with one counter update per list for the whole CTA.
+        auto finish_round = [&](int jb, const bool (&ok)[kCB], const float (&sc)[kCB],
+                                const float (&lo)[kCB], const float (&vo)[kCB]) {
+          uint32_t kA[kCB], kP[kCB];
+          unsigned bA[kCB], bP[kCB];
+          int nA = 0, nP = 0;
+#pragma unroll
+          for (int i = 0; i < kCB; ++i) {
+            const int jj = jb + gid + kPGroups * i;
+            const bool mine = gl == 0 && jj < j1;
+            const float is = ok[i] ? sc[i] : -INFINITY;
+            if (mine) outs[jj] = is;
+            kA[i] = ok[i] ? score_key(sc[i]) : 0u;
+            kP[i] = ema1 && mine ? ema_page(jj, is, lo[i], vo[i]) : 0u;
+            bA[i] =
+                __ballot_sync(0xffffffffu, t0key != 0u && mine && kA[i] != 0u && kA[i] >= t0key);
+            bP[i] = __ballot_sync(0xffffffffu, t1key != 0u && kP[i] != 0u && kP[i] >= t1key);
+            nA += __popc(bA[i]);
+            nP += __popc(bP[i]);
+          }
+          // this warp's places among the CTA's candidates, then the CTA's places in the lists; a
+          // local counter is cleared by its reader before the second barrier, so the next round
+          // finds it zero
+          int wA = 0, wP = 0;
+          if (lane == 0) {
+            if (nA) wA = static_cast<int>(atomicAdd(&s_cand[0], static_cast<unsigned>(nA)));
+            if (nP) wP = static_cast<int>(atomicAdd(&s_cand[1], static_cast<unsigned>(nP)));
+          }
+          named_barrier(1, kPW * 32);
+          if (tid == 0) {
+            const unsigned c = s_cand[0];
+            if (c) s_cand[2] = atomicAdd(a.cand_cnt + row, c);
+            s_cand[0] = 0u;
+          } else if (tid == 32) {
+            const unsigned c = s_cand[1];
+            if (c) s_cand[3] = atomicAdd(a.cand_cnt2 + row, c);
+            s_cand[1] = 0u;
+          }
+          named_barrier(1, kPW * 32);
+          const unsigned below = (1u << lane) - 1u;
+          unsigned atA = s_cand[2] + static_cast<unsigned>(__shfl_sync(0xffffffffu, wA, 0));
+          unsigned atP = s_cand[3] + static_cast<unsigned>(__shfl_sync(0xffffffffu, wP, 0));
+#pragma unroll
+          for (int i = 0; i < kCB; ++i) {
+            const int jj = jb + gid + kPGroups * i;
+            const unsigned ra = atA + __popc(bA[i] & below), rp = atP + __popc(bP[i] & below);
+            if (((bA[i] >> lane) & 1u) && ra < static_cast<unsigned>(kCandCap))
+              a.cand[static_cast<size_t>(row) * kCandCap + ra] = make_uint2(kA[i], jj);
+            if (((bP[i] >> lane) & 1u) && rp < static_cast<unsigned>(kCandCap))
+              a.cand2[static_cast<size_t>(row) * kCandCap + rp] = make_uint2(kP[i], jj);
+            atA += __popc(bA[i]);
+            atP += __popc(bP[i]);
           }
         };
         {
-          bool bad = false;
-  #pragma unroll
+          bool bad = false, okv[kCB];
+#pragma unroll
           for (int i = 0; i < kCB; ++i) {
             const int jj = j0 + gid + kPGroups * i;
             const bool in = jj < j1 && jj < nl;
-            const bool ok = in && cph[i] >= 0 && cph[i] < kv.num_phys;
-            bad |= in && !ok;
-            finish_slot(jj, ok, cs[i], cl[i], cvv[i]);
+            okv[i] = in && cph[i] >= 0 && cph[i] < kv.num_phys;
+            bad |= in && !okv[i];
           }
           if (gl == 0 && bad) raise_status(kv.status, DSA_STATUS_BAD_PAGE);
+          finish_round(j0, okv, cs, cl, cvv);
         }
         // the rest of a long segment, kCB slots per group per round
         for (int jb = j0 + kScoreRecs; jb < j1; jb += kScoreRecs) {
           int ph[kCB];
           float lo[kCB], vo[kCB];
-  #pragma unroll
+#pragma unroll
           for (int i = 0; i < kCB; ++i) {
             const int jj = jb + gid + kPGroups * i;
             ph[i] = jj < j1 && jj < nl ? table[jj] : -1;
             lo[i] = ema1 && gl == 0 && jj < j1 ? ell_r[jj] : 0.f;
             vo[i] = ema1 && gl == 0 && jj < j1 ? v_r[jj] : 0.f;
           }
-  #pragma unroll
+#pragma unroll
           for (int i = 0; i < kCB; ++i)
             if (ph[i] >= 0 && ph[i] < kv.num_phys)
               stage_record(static_cast<size_t>(ph[i]) * kv.Hkv + h, gid + kPGroups * i);
           cp_async_wait_all();
-          bool bad = false;
-  #pragma unroll
+          bool bad = false, okv[kCB];
+          float sc[kCB];
+#pragma unroll
           for (int i = 0; i < kCB; ++i) {
             const int jj = jb + gid + kPGroups * i;
             const bool in = jj < j1 && jj < nl;
-            const bool ok = in && ph[i] >= 0 && ph[i] < kv.num_phys;
-            bad |= in && !ok;
+            okv[i] = in && ph[i] >= 0 && ph[i] < kv.num_phys;
+            bad |= in && !okv[i];
             uint4 rc[4];
-            if (ok) staged_record(gid + kPGroups * i, rc);
-            const float sc = group_sum(ok ? record_partial<DSA_META_MINMAX>(rc, qv) : 0.f);
-            finish_slot(jj, ok, sc, lo[i], vo[i]);
+            if (okv[i]) staged_record(gid + kPGroups * i, rc);
+            sc[i] = group_sum(okv[i] ? record_partial<DSA_META_MINMAX>(rc, qv) : 0.f);
           }
           if (gl == 0 && bad) raise_status(kv.status, DSA_STATUS_BAD_PAGE);
+          finish_round(jb, okv, sc, lo, vo);
         }
       }
     };
@@ -586,7 +629,8 @@ __global__ void __launch_bounds__(kPThreads, 1)
             const uint32_t vm = __ballot_sync(0xffffffffu, in) & 0xffffu;
             if (vm == 0u) continue;
             if (vm != 0xffffu)
-              wrote |= zero_invalid_v_rows(vm, smem + s * stage_bytes + 2 * page * 128, page, t * 16);
+              wrote |=
+                  zero_invalid_v_rows(vm, smem + s * stage_bytes + 2 * page * 128, page, t * 16);
             float sc[2][4];
             tile_scores(qa, kb, page, t * 16, sc);
             tile_softmax_pv(st, sc, a.scale_log2, vm, vb, page, t * 16);
@@ -599,7 +643,7 @@ __global__ void __launch_bounds__(kPThreads, 1)
         {
           const int r0 = lane >> 2, c0 = (lane & 3) * 2;
           float* wO = sO + warp * G * kHeadDim;
-  #pragma unroll
+#pragma unroll
           for (int jj = 0; jj < 16; ++jj) {
             if (r0 < G)
               *reinterpret_cast<float2*>(wO + r0 * kHeadDim + jj * 8 + c0) =
@@ -623,7 +667,8 @@ __global__ void __launch_bounds__(kPThreads, 1)
         // the barrier is the same in all of them), so the barrier inside stays uniform
         const bool gave_up = named_barrier_or(1, kPW * 32, !got || *abort_flag);
         if (okv >= 0 && !gave_up) {
-          float* rec0 = a.partials + (static_cast<size_t>(row) * a.k_pred + slot) * G * kRecordFloats;
+          float* rec0 =
+              a.partials + (static_cast<size_t>(row) * a.k_pred + slot) * G * kRecordFloats;
           if (okv == 0) {  // a position outside the request: the empty part
             for (int g = tid; g < G; g += kPW * 32)
               *reinterpret_cast<float4*>(rec0 + g * kRecordFloats + 128) =
@@ -654,7 +699,8 @@ __global__ void __launch_bounds__(kPThreads, 1)
               float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
               for (int w = 0; w < nwu; ++w) {
                 const float f = wt[w * 16 + g];
-                const float4 o = *reinterpret_cast<const float4*>(sO + (w * G + g) * kHeadDim + d4 * 4);
+                const float4 o =
+                    *reinterpret_cast<const float4*>(sO + (w * G + g) * kHeadDim + d4 * 4);
                 acc.x = fmaf(f, o.x, acc.x);
                 acc.y = fmaf(f, o.y, acc.y);
                 acc.z = fmaf(f, o.z, acc.z);
@@ -1025,7 +1071,8 @@ __global__ void __launch_bounds__(kPThreads, 1)
       cntA = select_a(row, sA, [&] { fetch_records(task); });
       __syncthreads();  // sA is complete
       if (g == 0 && !dry) {  // the task of the row's first query head publishes A_t
-        for (int i = tid; i < a.k; i += kPThreads) a.idx[static_cast<size_t>(row) * a.k + i] = sA[i];
+        for (int i = tid; i < a.k; i += kPThreads)
+          a.idx[static_cast<size_t>(row) * a.k + i] = sA[i];
         if (tid == 0) a.count[row] = cntA;
       }
     } else {
@@ -1105,7 +1152,8 @@ __global__ void __launch_bounds__(kPThreads, 1)
       uint2 vr[32];
 #pragma unroll
       for (int u = 0; u < 32; ++u)
-        vr[u] = u < nvalid ? __ldg(reinterpret_cast<const uint2*>(vrow + static_cast<size_t>(u) * kHeadDim))
+        vr[u] = u < nvalid ? __ldg(reinterpret_cast<const uint2*>(vrow + static_cast<size_t>(u) *
+                                                                                kHeadDim))
                            : make_uint2(0u, 0u);
       float s = -INFINITY;
       if (lane < nvalid) {
@@ -1154,7 +1202,8 @@ __global__ void __launch_bounds__(kPThreads, 1)
         lv[u] = 0.f;
         ov[u] = make_float4(0.f, 0.f, 0.f, 0.f);
         if (i < n_parts) {
-          const float* r = reinterpret_cast<const float*>(smem + lay.rec_off) + parts[i] * kRecordFloats;
+          const float* r =
+              reinterpret_cast<const float*>(smem + lay.rec_off) + parts[i] * kRecordFloats;
           mv[u] = r[128];
           lv[u] = r[129];
           ov[u] = *(reinterpret_cast<const float4*>(r) + lane);
