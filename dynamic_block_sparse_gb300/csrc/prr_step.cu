@@ -92,12 +92,13 @@ DSA_DEV void grid_arrive(unsigned* ctr, volatile int* abort) {
   }
 }
 
-// Waits until the word reaches `target`.  Bounded: gives up after kWaitLimitNs, raising
-// DSA_STATUS_TIMEOUT.  Returns false when this CTA (or an earlier wait of it) gave up.
+// Waits until the word reaches `target` (compared as a sequence number, so a word that wrapped
+// around still orders).  Bounded: gives up after kWaitLimitNs, raising DSA_STATUS_TIMEOUT.
+// Returns false when this CTA (or an earlier wait of it) gave up.
 DSA_DEV bool grid_wait(unsigned* ctr, unsigned target, volatile int* abort, int32_t* status) {
   if (threadIdx.x == 0 && !*abort) {
     const unsigned long long t0 = global_timer_ns();
-    while (ld_acquire(ctr) < target) {
+    while (static_cast<int>(ld_acquire(ctr) - target) < 0) {
       if (global_timer_ns() - t0 > kWaitLimitNs) {
         *abort = 1;
         raise_status(status, DSA_STATUS_TIMEOUT);

@@ -6,6 +6,7 @@ times) a sample of rows is checked against the oracle computed row by row.
 """
 
 import math
+import time
 
 import numpy as np
 import pytest
@@ -307,6 +308,48 @@ def test_prr_without_second_stream_matches():
         torch.cuda.synchronize()
         outs.append(dec.out.clone())
     assert torch.equal(outs[0], outs[1])
+
+
+def test_prr_step_barrier_timeout_sets_status():
+    """Failure detection without a fault: the fused step's first grid barrier is made unreachable
+    (its counter starts at 0x80000000, so the arrival of every CTA still leaves it short of the
+    target: a flag that nothing sets).  Each bounded wait gives up after its limit, the kernel
+    returns early with DSA_STATUS_TIMEOUT in the status word, and the context stays usable: with
+    the workspace and the status zeroed again, the next step selects A_t exactly as the staged
+    path does and attends over it."""
+    w = BY_NAME["prr_512k"].replace(seq_len=65536, steps=4)
+    inp = make_inputs(w, "cuda")
+    decs = []
+    for fused in (True, False):
+        cache = Cache.from_inputs(inp)
+        dec = PRRDecoder(cache, w.k, w.k_pred, w.alpha, w.beta, w.gamma, fused=fused)
+        dec.build_meta()
+        decs.append(dec)
+    f, s = decs
+    for t in range(2):
+        for dec in decs:
+            dec.step(inp["q"][t])
+    torch.cuda.synchronize()
+    ws = f.step_workspace
+    ws[:4].copy_(torch.tensor([0, 0, 0, 0x80], dtype=torch.uint8, device=ws.device))
+    t0 = time.monotonic()
+    f.step(inp["q"][2])
+    torch.cuda.synchronize()
+    elapsed = time.monotonic() - t0
+    assert int(f.cache.status.item()) & B.DSA_STATUS_TIMEOUT, "the unreachable barrier went unseen"
+    assert elapsed < 60.0, f"the bounded waits took {elapsed:.1f} s"
+    s.step(inp["q"][2])
+    # recovery: the caller zeroes the workspace and the status, then steps on
+    ws.zero_()
+    f.cache.status.zero_()
+    for dec in decs:
+        dec.step(inp["q"][3])
+    torch.cuda.synchronize()
+    assert int(f.cache.status.item()) == 0
+    assert torch.equal(f.scores, s.scores)
+    assert torch.equal(f.idx, s.idx) and torch.equal(f.count, s.count)
+    assert_outputs(f.out.cpu().numpy(), f.m.cpu().numpy(), f.l.cpu().numpy(),
+                   [x.double().cpu().numpy() for x in (s.out, s.m, s.l)], "step after recovery")
 
 
 SAMPLE = {"tiny_topk": None, "llama3_8b_layer": 4, "lserve_hier": 3, "psa_threshold": 4,
