@@ -368,38 +368,53 @@ def bench_prr(args, w, dev, rank):
 
 
 def e2e_prr(args, w, dec, qs, flush, bytes_step):
-    """Same step through the public Python API with host buffers: pinned host query -> device,
-    decode step (eager library calls), output/m/l -> pinned host, every step."""
+    """Same step through the public Python API with host buffers, every step inside the window:
+    the pinned host query reaches the device, the step runs (eager library call), and the step's
+    result (O, m, l: one contiguous buffer) reaches pinned host memory.  Measured two ways:
+    ``copies`` with a host-to-device copy of the query and a device-to-host copy of the result
+    around the step, and ``zero_copy`` (the line's ``e2e``) with the query and the result in
+    page-locked host memory that the fused step reads and writes itself over the host link
+    (NVLink-C2C on a Grace-Blackwell node); the same bytes cross it either way."""
     import torch
 
     nq = qs.shape[0]
     host_q = torch.empty((nq,) + tuple(qs.shape[1:]), dtype=qs.dtype, pin_memory=True)
     host_q.copy_(qs.cpu())
     dev_q = torch.empty_like(qs[0])
-    out_h = torch.empty(dec.out.shape, dtype=torch.float32, pin_memory=True)
-    m_h = torch.empty(dec.m.shape, dtype=torch.float32, pin_memory=True)
-    l_h = torch.empty(dec.l.shape, dtype=torch.float32, pin_memory=True)
+    res_h = torch.empty(dec.result.shape, dtype=torch.float32, pin_memory=True)
     n = max(20, min(300, args.steps))
     stream = torch.cuda.current_stream()
-    times = []
-    for i in range(n + 5):
-        flush(i & 0xFF)
-        s, e = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
-        s.record(stream)
+
+    def run(step):
+        times = []
+        for i in range(n + 5):
+            flush(i & 0xFF)
+            s, e = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+            s.record(stream)
+            step(i)
+            e.record(stream)
+            e.synchronize()
+            if i >= 5:
+                times.append(s.elapsed_time(e))
+        return statistics.mean(times)
+
+    def with_copies(i):
         dev_q.copy_(host_q[i % nq], non_blocking=True)
         dec.step(dev_q)
-        out_h.copy_(dec.out, non_blocking=True)
-        m_h.copy_(dec.m, non_blocking=True)
-        l_h.copy_(dec.l, non_blocking=True)
-        e.record(stream)
-        e.synchronize()
-        if i >= 5:
-            times.append(s.elapsed_time(e))
-    ms = statistics.mean(times)
+        res_h.copy_(dec.result, non_blocking=True)
+
+    ms_copies = run(with_copies)
+    dec.host_result()
+    ms = run(lambda i: dec.step(host_q[i % nq]))
     h2d = dev_q.numel() * dev_q.element_size()
-    d2h = (dec.out.numel() + dec.m.numel() + dec.l.numel()) * 4
+    d2h = dec.result.numel() * 4
     return {"value": bytes_step / (ms * 1e6), "unit": "GB/s", "ms_per_step": ms,
-            "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h}
+            "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h,
+            "transfer": "zero-copy: the fused step reads the pinned host query and writes the "
+                        "pinned host result over the host link",
+            "copies": {"value": bytes_step / (ms_copies * 1e6), "unit": "GB/s",
+                       "ms_per_step": ms_copies,
+                       "transfer": "cudaMemcpyAsync of the query in, one of the result out"}}
 
 
 # ------------------------------------------------------------------------------------ rows

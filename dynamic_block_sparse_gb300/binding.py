@@ -117,6 +117,14 @@ def _ptr(t) -> int | None:
     return t.data_ptr()
 
 
+def _io_ptr(t) -> int:
+    """A CUDA tensor, or a page-locked host tensor the device reads or writes over the host link
+    (the fused PRR step's query and result)."""
+    if t.is_cuda or t.is_pinned():
+        return t.data_ptr()
+    raise ValueError("tensor must live on a CUDA device or in page-locked host memory")
+
+
 def _stream(stream) -> int | None:
     if stream is None:
         stream = torch.cuda.current_stream()
@@ -269,9 +277,10 @@ def dsa_prr_step(kv: PagedKV, q, meta, scores, ell, trend, alpha: float, beta: f
                  superset: bool = False, stream=None):
     """One PRR decode step (scoring, top-k, speculation over P_t, EMA update with the selection
     of P_{t+1}, repair and merge) in one launch.  ``workspace`` must be zero-filled before its
-    first use (each completed call leaves it zero-filled)."""
+    first use (each completed call leaves it zero-filled).  ``q`` and ``out``/``m``/``l`` may be
+    page-locked host tensors: the kernel reads and writes them over the host link."""
     a = PrrStepArgs()
-    a.q, a.meta, a.scores, a.stride = _ptr(q), _ptr(meta), _ptr(scores), scores.shape[-1]
+    a.q, a.meta, a.scores, a.stride = _io_ptr(q), _ptr(meta), _ptr(scores), scores.shape[-1]
     a.ell, a.trend = _ptr(ell), _ptr(trend)
     a.alpha, a.beta, a.gamma, a.pred = alpha, beta, gamma, _ptr(pred)
     a.spec_idx, a.spec_count, a.k_pred = _ptr(spec_idx), _ptr(spec_count), spec_idx.shape[-1]
@@ -280,7 +289,7 @@ def dsa_prr_step(kv: PagedKV, q, meta, scores, ell, trend, alpha: float, beta: f
     a.next_idx, a.next_count = _ptr(next_idx), _ptr(next_count)
     assert next_idx.shape[-1] == spec_idx.shape[-1]
     a.superset, a.scale = 1 if superset else 0, scale
-    a.out, a.m, a.l = _ptr(out), _ptr(m), _ptr(l)
+    a.out, a.m, a.l = _io_ptr(out), _io_ptr(m), _io_ptr(l)
     ws_bytes = workspace.numel() * workspace.element_size()
     _check("dsa_prr_step", load().dsa_prr_step(ctypes.byref(kv), ctypes.byref(a), _ptr(workspace),
                                                ws_bytes, _stream(stream)))

@@ -58,11 +58,21 @@ class Cache:
         return torch.zeros((self.num_phys_pages, self.num_kv_heads, g, self.head_dim),
                            dtype=torch.float32, device=self.device)
 
+    def result_views(self):
+        """(O, m, l, result): the three outputs as views of one contiguous fp32 buffer
+        (``result``), so that a step's whole result reaches the host in one copy; each view starts
+        on a 16-byte boundary."""
+        nh = self.batch * self.num_q_heads
+        nh4 = (nh + 3) // 4 * 4
+        buf = torch.zeros(nh * self.head_dim + 2 * nh4, dtype=torch.float32, device=self.device)
+        o = buf[:nh * self.head_dim].view(self.batch, self.num_q_heads, self.head_dim)
+        m = buf[nh * self.head_dim:nh * self.head_dim + nh].view(self.batch, self.num_q_heads)
+        l = buf[nh * self.head_dim + nh4:nh * self.head_dim + nh4 + nh].view(self.batch,
+                                                                           self.num_q_heads)
+        return o, m, l, buf
+
     def outputs(self):
-        o = torch.zeros((self.batch, self.num_q_heads, self.head_dim), dtype=torch.float32,
-                        device=self.device)
-        m = torch.zeros((self.batch, self.num_q_heads), dtype=torch.float32, device=self.device)
-        l = torch.zeros_like(m)
+        o, m, l, _ = self.result_views()
         return o, m, l
 
 
@@ -81,7 +91,7 @@ class TopKDecoder:
         self.idx = torch.empty((c.batch, c.num_kv_heads, max(1, k)), dtype=torch.int32,
                                device=c.device)
         self.count = torch.empty((c.batch, c.num_kv_heads), dtype=torch.int32, device=c.device)
-        self.out, self.m, self.l = c.outputs()
+        self.out, self.m, self.l, self.result = c.result_views()
         ws = B.dsa_sparse_decode_attn_workspace_size(c.kv, self.idx.shape[-1])
         self.workspace = torch.empty(max(16, ws), dtype=torch.uint8, device=c.device)
 
@@ -118,7 +128,7 @@ class HierDecoder:
         self.idx = torch.empty((c.batch, c.num_kv_heads, max(1, k_phys)), dtype=torch.int32,
                                device=c.device)
         self.count = torch.empty((c.batch, c.num_kv_heads), dtype=torch.int32, device=c.device)
-        self.out, self.m, self.l = c.outputs()
+        self.out, self.m, self.l, self.result = c.result_views()
         ws = B.dsa_sparse_decode_attn_workspace_size(c.kv, self.idx.shape[-1])
         self.workspace = torch.empty(max(16, ws), dtype=torch.uint8, device=c.device)
 
@@ -157,7 +167,7 @@ class ThresholdDecoder:
                                   device=c.device)
         self.idx = torch.empty((c.batch, c.num_kv_heads, cap), dtype=torch.int32, device=c.device)
         self.count = torch.empty((c.batch, c.num_kv_heads), dtype=torch.int32, device=c.device)
-        self.out, self.m, self.l = c.outputs()
+        self.out, self.m, self.l, self.result = c.result_views()
 
     def build_meta(self, stream=None):
         B.dsa_build_page_meta(self.cache.kv, B.DSA_META_MEAN, self.cache.page_size, self.meta,
@@ -207,7 +217,7 @@ class PRRDecoder:
                             for _ in range(2)]
         self.partials = torch.empty((c.batch, c.num_kv_heads, k_pred, c.group, B.RECORD_FLOATS),
                                     dtype=torch.float32, device=dev)
-        self.out, self.m, self.l = c.outputs()
+        self.out, self.m, self.l, self.result = c.result_views()
         ws = max(B.dsa_repair_merge_workspace_size(c.kv, k),
                  B.dsa_sparse_decode_attn_workspace_size(c.kv, k))
         self.workspace = torch.empty(max(16, ws), dtype=torch.uint8, device=dev)
@@ -219,6 +229,20 @@ class PRRDecoder:
         self.step_workspace = torch.zeros(B.dsa_prr_step_workspace_size(c.kv), dtype=torch.uint8,
                                           device=dev)
         self.t = 0
+
+    def host_result(self):
+        """Moves (O, m, l) into one page-locked host buffer that the fused step writes directly
+        (no device-to-host copy); a fused step t >= 1 also accepts a page-locked host query.  The
+        other steps (t = 0, or ``fused=False``) take device tensors only and refuse host ones."""
+        o, m, l, buf = self.cache.result_views()  # the same layout, on the host
+        pinned = torch.zeros(buf.shape, dtype=buf.dtype, pin_memory=True)
+        n_o, n_h = o.numel(), m.numel()
+        n_h4 = (buf.numel() - n_o) // 2
+        self.result = pinned
+        self.out = pinned[:n_o].view(o.shape)
+        self.m = pinned[n_o:n_o + n_h].view(m.shape)
+        self.l = pinned[n_o + n_h4:n_o + n_h4 + n_h].view(l.shape)
+        return self
 
     @property
     def spec_idx(self):

@@ -278,7 +278,9 @@ int dsa_ema_predict_update(const float* IS, int32_t rows, int32_t n, int32_t str
  * with scores, A_t, the EMA state and P_{t+1} bit for bit and out/m/l up to fp32 rounding.  The
  * speculative attention and the scoring run side by side on every SM; selection, prediction and
  * repair follow after on-device grid barriers (a cooperative launch of one CTA per SM).
- *   args->q            : bf16 [B][Hq][D], 16-byte aligned.
+ *   args->q            : bf16 [B][Hq][D], 16-byte aligned.  Device memory, or page-locked host
+ *                        memory mapped for the device (cudaHostAlloc / cudaHostRegister): the
+ *                        kernel then reads the query over the host link itself, no copy needed.
  *   args->meta         : DSA_META_MINMAX metadata built with logical_page == page_size.
  *   args->scores (out) : fp32 [B][Hkv][stride]; max_pages_per_seq <= stride <= 32768.
  *   args->ell, trend   : fp32 [B][Hkv][stride], EMA level and trend, updated in place.
@@ -288,6 +290,8 @@ int dsa_ema_predict_update(const float* IS, int32_t rows, int32_t n, int32_t str
  *   args->idx/count (out)     : A_t, int32 [B][Hkv][k] ascending, int32 [B][Hkv].
  *   args->next_idx/next_count (out): P_{t+1}, int32 [B][Hkv][k_pred], int32 [B][Hkv]; must not
  *                        alias spec_idx/spec_count (double-buffer them across steps).
+ *   args->out/m/l (out): fp32 [B][Hq][D], [B][Hq], [B][Hq].  Like q, they may be mapped
+ *                        page-locked host memory, which the kernel writes directly.
  *   1 <= k, k_pred <= 256.  kv->head_is_streaming must be NULL.
  *   workspace          : dsa_prr_step_workspace_size(kv) bytes, 16-byte aligned, ZERO-FILLED
  *                        before its first use; every call that completes leaves its counters at

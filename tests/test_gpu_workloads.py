@@ -310,6 +310,33 @@ def test_prr_without_second_stream_matches():
     assert torch.equal(outs[0], outs[1])
 
 
+def test_prr_step_with_host_query_and_result():
+    """The fused step with its query and its result (O, m, l) in page-locked host memory, which the
+    kernel reads and writes over the host link itself, gives the same scores, selections, EMA
+    state and outputs as with device buffers."""
+    w = oracle_scale(BY_NAME["prr_512k"]).replace(steps=5)
+    inp = to_cuda(make_inputs(w, "cpu"))
+    decs = []
+    for _ in range(2):
+        dec = PRRDecoder(Cache.from_inputs(inp), w.k, w.k_pred, w.alpha, w.beta, w.gamma)
+        dec.build_meta()
+        dec.step(inp["q"][0])  # step 0 (separate launches) takes device buffers only
+        decs.append(dec)
+    dev, host = decs
+    host.host_result()
+    assert not host.out.is_cuda and host.out.is_pinned()
+    q_host = inp["q"].cpu().pin_memory()
+    for t in range(1, w.steps):
+        dev.step(inp["q"][t])
+        host.step(q_host[t])
+        torch.cuda.synchronize()
+        for name in ("scores", "ell", "trend", "pred", "idx", "count"):
+            assert torch.equal(getattr(dev, name), getattr(host, name)), f"{name} at step {t}"
+        assert_outputs(host.out.numpy(), host.m.numpy(), host.l.numpy(),
+                       [x.double().cpu().numpy() for x in (dev.out, dev.m, dev.l)], f"step {t}")
+        assert int(host.cache.status.item()) == 0
+
+
 def test_prr_step_barrier_timeout_sets_status():
     """Failure detection without a fault: the fused step's first grid barrier is made unreachable
     (its counter starts at 0x80000000, so the arrival of every CTA still leaves it short of the
