@@ -10,6 +10,7 @@ from __future__ import annotations
 import ctypes
 import os
 import re
+import struct
 from ctypes import c_float, c_int32, c_size_t, c_void_p
 
 import torch
@@ -77,6 +78,8 @@ _SIGNATURES = {
     "dsa_ema_predict_update": ([_P, _I, _I, _I, _P, _P, _I, c_float, c_float, c_float, _P, _I,
                                 _P, _I, _P, _P], _I),
     "dsa_merge_partials": ([_P, _I, _I, _I, _I, _P, _P, _P, _P], _I),
+    "dsa_calibrate_ema": ([_P, _I, _I, _I, _I, _I, _I, _P, _P, _P, c_size_t, _P], _I),
+    "dsa_calibrate_ema_workspace_size": ([_I], c_size_t),
     "dsa_prr_step": ([_P, _P, _P, c_size_t, _P], _I),
     "dsa_prr_step_workspace_size": ([_P], c_size_t),
 }
@@ -257,6 +260,36 @@ def dsa_ema_predict_update(IS, n: int, ell, v, mode: int, alpha: float, beta: fl
         _ptr(IS), rows, n, IS.shape[-1], _ptr(ell), _ptr(v), mode, alpha, beta, gamma,
         _ptr(pred), k_pred, _ptr(pred_idx), 0 if pred_idx is None else pred_idx.shape[-1],
         _ptr(pred_count), _stream(stream)))
+
+
+CALIB_POINTS = 80
+
+
+def calibration_point(c: int) -> tuple[float, float, float]:
+    """(alpha, beta, gamma) of grid point c of dsa_calibrate_ema (alpha outermost, gamma
+    innermost), as the fp32 values the kernel uses."""
+    def f32(x: float) -> float:
+        return struct.unpack("f", struct.pack("f", x))[0]
+
+    # an fp32 constant times a small integer, rounded to fp32 (as the kernel computes it)
+    return (f32(f32(0.2) * (1 + c // 20)), f32(f32(0.1) * (1 + (c // 4) % 5)),
+            f32(f32(0.25) * (c % 4)))
+
+
+def dsa_calibrate_ema_workspace_size(rows: int) -> int:
+    return int(load().dsa_calibrate_ema_workspace_size(rows))
+
+
+def dsa_calibrate_ema(traj, n: int, k: int, k_pred: int, H, best, workspace, stream=None):
+    """``traj`` fp32 ``[steps][rows][stride]`` -> ``H`` fp32 ``[rows][80]`` and ``best`` int32
+    ``[rows]`` (the winning grid point).  ``workspace`` must be zero-filled before its first use
+    (each completed call leaves it zero-filled)."""
+    steps, rows, stride = traj.shape
+    assert H.shape[-1] == CALIB_POINTS
+    ws_bytes = workspace.numel() * workspace.element_size()
+    _check("dsa_calibrate_ema", load().dsa_calibrate_ema(
+        _ptr(traj), steps, rows, n, stride, k, k_pred, _ptr(H), _ptr(best), _ptr(workspace),
+        ws_bytes, _stream(stream)))
 
 
 def dsa_merge_partials(partials, out, m, l, stream=None):

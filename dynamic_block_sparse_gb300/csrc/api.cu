@@ -564,6 +564,33 @@ int dsa_ema_predict_update(const float* IS, int32_t rows, int32_t n, int32_t str
   return e == cudaSuccess ? ok() : cuda_fail(e, "dsa_ema_predict_update launch");
 }
 
+size_t dsa_calibrate_ema_workspace_size(int32_t rows) {
+  return rows > 0 ? (static_cast<size_t>(rows) * 4 + 15) & ~static_cast<size_t>(15) : 16;
+}
+
+int dsa_calibrate_ema(const float* traj, int32_t steps, int32_t rows, int32_t n, int32_t stride,
+                      int32_t k, int32_t k_pred, float* H, int32_t* best, void* workspace,
+                      size_t workspace_bytes, dsa_stream_t stream) {
+  if (steps < 0 || rows < 0 || n < 0) return fail(DSA_ERR_INVALID_ARG, "negative size");
+  if (rows == 0) return ok();
+  if (steps < 1) return fail(DSA_ERR_INVALID_ARG, "dsa_calibrate_ema: steps must be >= 1");
+  if (!traj || !H || !best) return fail(DSA_ERR_INVALID_ARG, "traj/H/best is NULL");
+  if (n < 1 || n > stride) return fail(DSA_ERR_INVALID_ARG, "need 1 <= n <= stride");
+  if (n > kCalibMaxN) return fail(DSA_ERR_UNSUPPORTED, "n %d > %d", n, kCalibMaxN);
+  if (k < 1 || k_pred < 1) return fail(DSA_ERR_INVALID_ARG, "k and k_pred must be >= 1");
+  if (k > kMaxListPages || k_pred > kMaxListPages)
+    return fail(DSA_ERR_UNSUPPORTED, "k and k_pred must be <= %d", kMaxListPages);
+  if (static_cast<long long>(rows) * kCalibPoints > 0x7fffffffLL)
+    return fail(DSA_ERR_UNSUPPORTED, "too many rows");
+  if (!workspace || workspace_bytes < dsa_calibrate_ema_workspace_size(rows))
+    return fail(DSA_ERR_WORKSPACE, "workspace of %zu bytes needed",
+                dsa_calibrate_ema_workspace_size(rows));
+  cudaError_t e = launch_calib(traj, steps, rows, n, stride, k, k_pred, H, best,
+                               static_cast<unsigned*>(workspace),
+                               static_cast<cudaStream_t>(stream));
+  return e == cudaSuccess ? ok() : cuda_fail(e, "dsa_calibrate_ema launch");
+}
+
 int dsa_merge_partials(const float* partials, int32_t rows, int32_t num_parts, int32_t group,
                        int32_t head_dim, float* out, float* m, float* l, dsa_stream_t stream) {
   if (rows < 0 || num_parts < 0) return fail(DSA_ERR_INVALID_ARG, "negative size");

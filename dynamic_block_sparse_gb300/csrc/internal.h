@@ -172,6 +172,13 @@ cudaError_t launch_ema(const float* IS, int rows, int n, int stride, float* ell,
                        int32_t* pred_idx, int pred_idx_stride, int32_t* pred_count,
                        cudaStream_t s);
 
+// PRR §3.2 calibration of the EMA predictor over its 80-point grid (csrc/calib.cu)
+constexpr int kCalibPoints = 80;
+constexpr int kCalibMaxN = 16384;  // pages per row whose predictor state fits in shared memory
+size_t calib_smem_bytes(int n);
+cudaError_t launch_calib(const float* traj, int T, int rows, int n, int stride, int k, int k_pred,
+                         float* H, int32_t* best, unsigned* done, cudaStream_t s);
+
 struct ThresholdArgs {
   KvView kv;
   const __nv_bfloat16* q;

@@ -266,6 +266,31 @@ int dsa_ema_predict_update(const float* IS, int32_t rows, int32_t n, int32_t str
                            int32_t pred_idx_stride, int32_t* pred_count, dsa_stream_t stream);
 
 /*
+ * Calibration of the EMA predictor ([PRR] §3.2): every (alpha, beta, gamma) of the 80-point grid
+ * runs the predictor of dsa_ema_predict_update over a trajectory of true score vectors, and is
+ * rated by the mean score-weighted hit rate
+ *     H = mean over t = 1..steps-1 of  sum_{j in A_t ∩ P_t} IS_t[j] / sum_{j in A_t} IS_t[j]
+ * (1 for a step whose A_t scores sum to 0), where A_t = top-k of IS_t and P_t = top-k_pred of the
+ * prediction made from steps 0..t-1 (step 0 initialises the state); both selections rank as
+ * dsa_select_topk does.  The grid point with the largest H wins, ties to the lower point.
+ * Grid point c (0..79): alpha = 0.2 (1 + c / 20), beta = 0.1 (1 + (c / 4) % 5),
+ * gamma = 0.25 (c % 4) -- alpha outermost, gamma innermost.  One launch, one CTA per
+ * (row, grid point); the parameters are fp32.
+ *   traj      : fp32 [steps][rows][stride], IS_t of row r at traj[(t * rows + r) * stride];
+ *               entries 0..n-1 are pages (-inf = no page).  1 <= n <= min(stride, 16384).
+ *   H (out)   : fp32 [rows][80].
+ *   best (out): int32 [rows], the winning grid point.
+ *   1 <= k, k_pred <= 256; steps >= 1 (steps = 1 rates every point 0 and picks point 0).
+ *   workspace : dsa_calibrate_ema_workspace_size(rows) bytes, ZERO-FILLED before its first use;
+ *               each completed call leaves it zero-filled.
+ */
+#define DSA_CALIB_POINTS 80
+int dsa_calibrate_ema(const float* traj, int32_t steps, int32_t rows, int32_t n, int32_t stride,
+                      int32_t k, int32_t k_pred, float* H, int32_t* best, void* workspace,
+                      size_t workspace_bytes, dsa_stream_t stream);
+size_t dsa_calibrate_ema_workspace_size(int32_t rows);
+
+/*
  * One whole PRR decode step t >= 1 in a single launch ([PRR] §3 end to end: speculation over the
  * predicted set P_t (§3.4), the true selection A_t, the predictor update (§3.1), repair of the
  * missed pages and the merge (§3.3)).  It computes exactly what this sequence computes:

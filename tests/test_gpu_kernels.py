@@ -381,6 +381,99 @@ def test_repair_merge(case, superset):
 
 # ---------------------------------------------------------------------------------- EMA
 
+def _calib_oracle(traj, rows, n, k, k_pred, points=None):
+    """H of the oracle's calibration per row (PRR §3.2), for all grid points or a subset."""
+    out = []
+    grid = O.calibration_grid()
+    for r in range(rows):
+        tr = [np.asarray(t[r, :n], dtype=np.float64) for t in traj]
+        if points is None:
+            _, Hs = O.calibrate_ema(tr, k, k_pred)
+            out.append(np.array(Hs))
+            continue
+        Hs = []
+        for c in points:
+            a, b, g = grid[c]
+            ell, v = O.ema_init(tr[0])
+            tot = 0.0
+            for t in range(1, len(tr)):
+                P = O.select_topk(O.ema_predict(ell, v, g), k_pred)
+                A = O.select_topk(tr[t], k)
+                tot += O.score_weighted_hit(P, A, tr[t])
+                ell, v = O.ema_update(tr[t], ell, v, a, b)
+            Hs.append(tot / max(1, len(tr) - 1))
+        out.append(np.array(Hs))
+    return out
+
+
+def _calib_gpu(traj, n, k, k_pred, stride):
+    steps, rows = len(traj), traj[0].shape[0]
+    T = torch.full((steps, rows, stride), -math.inf, device="cuda")
+    for t, x in enumerate(traj):
+        T[t, :, :n] = x.cuda()
+    H = torch.empty((rows, B.CALIB_POINTS), device="cuda")
+    best = torch.full((rows,), -1, dtype=torch.int32, device="cuda")
+    ws = torch.zeros(B.dsa_calibrate_ema_workspace_size(rows), dtype=torch.uint8, device="cuda")
+    B.dsa_calibrate_ema(T, n, k, k_pred, H, best, ws)
+    torch.cuda.synchronize()
+    assert int(ws.sum()) == 0, "the workspace is left zero-filled"
+    return H.double().cpu().numpy(), best.cpu().numpy()
+
+
+def test_calibrate_ema_matches_oracle():
+    """Every grid point's score-weighted hit rate H against the oracle's calibration (PRR §3.2), on
+    drifting trajectories with pages past the request and a page that drops out and comes back;
+    the chosen point is the oracle's best up to fp32 selection ties."""
+    rows, n, k, k_pred, steps = 3, 700, 24, 29, 9
+    gen = torch.Generator().manual_seed(11)
+    base = torch.randn(rows, n, generator=gen) * 3 + 100
+    slope = torch.randn(rows, n, generator=gen) * 0.8
+    traj = [base + slope * t + 0.4 * torch.randn(rows, n, generator=gen) for t in range(steps)]
+    for t in traj:
+        t[:, n - 60:] = -math.inf                       # pages beyond the request
+    traj[4][1, 5:9] = -math.inf                         # a page that drops out, then comes back
+    H, best = _calib_gpu(traj, n, k, k_pred, stride=n + 4)
+    ref = _calib_oracle(traj, rows, n, k, k_pred)
+    for r in range(rows):
+        np.testing.assert_allclose(H[r], ref[r], atol=2e-3, rtol=0, err_msg=f"H row {r}")
+        assert ref[r][best[r]] >= ref[r].max() - 2e-3, f"row {r}: best {best[r]}"
+
+
+def test_calibrate_ema_prefers_trend_when_rankings_cross():
+    """The crossing-rankings trajectory of the oracle's pins: the GPU also picks a point with
+    gamma > 0, and it matches the oracle's choice."""
+    n = 40
+    slope = np.linspace(-1, 1, n)
+    traj = [torch.tensor(np.stack([20 - 6 * slope + slope * t + 0.001 * np.arange(n)] * 2),
+                         dtype=torch.float32) for t in range(12)]
+    H, best = _calib_gpu(traj, n, 5, 6, stride=48)
+    ref = _calib_oracle(traj, 2, n, 5, 6)
+    for r in range(2):
+        assert B.calibration_point(int(best[r]))[2] > 0
+        np.testing.assert_allclose(H[r], ref[r], atol=1e-4, rtol=0)
+        assert int(best[r]) == int(np.argmax(ref[r]))
+
+
+def test_calibrate_ema_full_size_sampled():
+    """The PRR 512K shape (2 rows of 8192 blocks, top-64, |P| = 76) over a 16-step random-walk
+    trajectory; eight grid points checked against the oracle, and the rest against properties
+    (0 <= H <= 1 for positive scores)."""
+    rows, n, k, k_pred, steps = 2, 8192, 64, 76, 16
+    gen = torch.Generator().manual_seed(12)
+    x = torch.randn(rows, n, generator=gen) * 4 + 300
+    traj = []
+    for _ in range(steps):
+        traj.append(x.clone())
+        x = x + 0.6 * torch.randn(rows, n, generator=gen)
+    H, best = _calib_gpu(traj, n, k, k_pred, stride=n)
+    assert np.all((H >= 0) & (H <= 1 + 1e-6))
+    points = [0, 7, 22, 39, 41, 58, 63, 79]
+    ref = _calib_oracle(traj, rows, n, k, k_pred, points)
+    for r in range(rows):
+        np.testing.assert_allclose(H[r][points], ref[r], atol=2e-3, rtol=0, err_msg=f"row {r}")
+        assert 0 <= best[r] < 80 and H[r][best[r]] == H[r].max()
+
+
 def test_ema_predict_update_sequence():
     rows, n, k_pred = 3, 5000, 76
     gen = torch.Generator().manual_seed(5)

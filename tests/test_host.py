@@ -107,6 +107,22 @@ def test_binding_refuses_cpu_tensors(lib):
                           torch.zeros(2, dtype=torch.int32))
 
 
+def test_calibrate_ema_host_validation_without_gpu(lib):
+    """dsa_calibrate_ema rejects bad arguments on the host, before any CUDA call."""
+    p = 4096
+    need = lib.dsa_calibrate_ema_workspace_size(3)
+    assert need == 16
+    call = lambda steps=8, rows=3, n=500, stride=512, k=16, kp=20, ws=need: \
+        lib.dsa_calibrate_ema(p, steps, rows, n, stride, k, kp, p * 2, p * 3, p * 4, ws, None)
+    assert lib.dsa_calibrate_ema(p, 8, 0, 500, 512, 16, 20, p, p, p, 0, None) == 0  # no rows
+    assert call(steps=0) == -1 and b"steps" in lib.dsa_last_error()
+    assert call(n=600) == -1                                           # n > stride
+    assert call(n=20000, stride=20000) == -3                           # predictor state too big
+    assert call(k=300) == -3 and call(kp=0) == -1
+    assert call(ws=need - 1) == -5
+    assert lib.dsa_calibrate_ema(0, 8, 3, 500, 512, 16, 20, p, p, p, need, None) == -1  # NULL traj
+
+
 def test_prr_step_host_validation_without_gpu(lib):
     """dsa_prr_step rejects bad arguments on the host, before any CUDA call."""
     from dynamic_block_sparse_gb300 import binding as B
