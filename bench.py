@@ -204,6 +204,7 @@ def prr_bytes(w, n_valid_pages, P_pages, missed_pages):
 def bench_prr(args, w, dev, rank):
     import torch
 
+    from dynamic_block_sparse_gb300 import binding as B
     from dynamic_block_sparse_gb300.pipeline import Cache, PRRDecoder
     from dynamic_block_sparse_gb300.workloads import make_inputs
 
@@ -299,6 +300,20 @@ def bench_prr(args, w, dev, rank):
     # the separate-launch step (state keeps evolving; the parity alternation is the same)
     state["i"] = 0
     staged_ms = statistics.mean(timed_replay(staged_graphs, max(50, min(400, args.steps))))
+    # EMA calibration (PRR §3.2) over a 16-step trajectory of this workload's true scores
+    calib_steps = 16
+    traj = torch.empty((calib_steps,) + tuple(dec.scores.shape), dtype=torch.float32, device=dev)
+    for t in range(calib_steps):
+        dec.stage_score(qs[t % nq])
+        traj[t].copy_(dec.scores)
+    t3 = traj.view(calib_steps, -1, traj.shape[-1])
+    cH = torch.empty((t3.shape[1], B.CALIB_POINTS), dtype=torch.float32, device=dev)
+    cbest = torch.empty(t3.shape[1], dtype=torch.int32, device=dev)
+    cws = torch.zeros(B.dsa_calibrate_ema_workspace_size(calib_steps, t3.shape[1], dec.stride,
+                                                         w.k), dtype=torch.uint8, device=dev)
+    calib_ms = _time_graph(_graph(lambda: B.dsa_calibrate_ema(t3, dec.stride, w.k, w.k_pred, cH,
+                                                               cbest, cws)), flush)
+    calib_bytes = t3.numel() * 4 + cH.numel() * 4 + cbest.numel() * 4
     clocks = sampler.stop()
 
     # pages attended per timed step
@@ -355,6 +370,8 @@ def bench_prr(args, w, dev, rank):
                stage_bytes["ema_predict"], peak),
         _entry("A10", w.name, "dsa_repair_merge (attention over A minus P, merge with the hits)",
                stage_ms["repair_merge"], rep_bytes, peak),
+        _entry("N1", w.name, "dsa_calibrate_ema: 80-point (alpha, beta, gamma) grid, 16 steps",
+               calib_ms, calib_bytes, peak),
         _entry("step", w.name, "PRR decode step, one cooperative launch (dsa_prr_step)", mean_ms,
                bytes_step, peak),
         _entry("step-staged", w.name, "PRR decode step, separate launches on three streams",

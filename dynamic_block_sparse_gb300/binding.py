@@ -79,7 +79,7 @@ _SIGNATURES = {
                                 _P, _I, _P, _P], _I),
     "dsa_merge_partials": ([_P, _I, _I, _I, _I, _P, _P, _P, _P], _I),
     "dsa_calibrate_ema": ([_P, _I, _I, _I, _I, _I, _I, _P, _P, _P, c_size_t, _P], _I),
-    "dsa_calibrate_ema_workspace_size": ([_I], c_size_t),
+    "dsa_calibrate_ema_workspace_size": ([_I, _I, _I, _I], c_size_t),
     "dsa_prr_step": ([_P, _P, _P, c_size_t, _P], _I),
     "dsa_prr_step_workspace_size": ([_P], c_size_t),
 }
@@ -276,14 +276,15 @@ def calibration_point(c: int) -> tuple[float, float, float]:
             f32(f32(0.25) * (c % 4)))
 
 
-def dsa_calibrate_ema_workspace_size(rows: int) -> int:
-    return int(load().dsa_calibrate_ema_workspace_size(rows))
+def dsa_calibrate_ema_workspace_size(steps: int, rows: int, n: int, k: int) -> int:
+    return int(load().dsa_calibrate_ema_workspace_size(steps, rows, n, k))
 
 
 def dsa_calibrate_ema(traj, n: int, k: int, k_pred: int, H, best, workspace, stream=None):
     """``traj`` fp32 ``[steps][rows][stride]`` -> ``H`` fp32 ``[rows][80]`` and ``best`` int32
-    ``[rows]`` (the winning grid point).  ``workspace`` must be zero-filled before its first use
-    (each completed call leaves it zero-filled)."""
+    ``[rows]`` (the winning grid point).  ``workspace``: dsa_calibrate_ema_workspace_size(steps,
+    rows, n, k) bytes, zero-filled before its first use (each completed call leaves the part that
+    must be zero zero-filled)."""
     steps, rows, stride = traj.shape
     assert H.shape[-1] == CALIB_POINTS
     ws_bytes = workspace.numel() * workspace.element_size()

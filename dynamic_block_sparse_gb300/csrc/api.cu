@@ -564,8 +564,9 @@ int dsa_ema_predict_update(const float* IS, int32_t rows, int32_t n, int32_t str
   return e == cudaSuccess ? ok() : cuda_fail(e, "dsa_ema_predict_update launch");
 }
 
-size_t dsa_calibrate_ema_workspace_size(int32_t rows) {
-  return rows > 0 ? (static_cast<size_t>(rows) * 4 + 15) & ~static_cast<size_t>(15) : 16;
+size_t dsa_calibrate_ema_workspace_size(int32_t steps, int32_t rows, int32_t n, int32_t k) {
+  if (steps < 1 || rows < 1 || n < 1 || k < 1) return 16;
+  return calib_workspace(steps, rows, n, k).total;
 }
 
 int dsa_calibrate_ema(const float* traj, int32_t steps, int32_t rows, int32_t n, int32_t stride,
@@ -582,11 +583,13 @@ int dsa_calibrate_ema(const float* traj, int32_t steps, int32_t rows, int32_t n,
     return fail(DSA_ERR_UNSUPPORTED, "k and k_pred must be <= %d", kMaxListPages);
   if (static_cast<long long>(rows) * kCalibPoints > 0x7fffffffLL)
     return fail(DSA_ERR_UNSUPPORTED, "too many rows");
-  if (!workspace || workspace_bytes < dsa_calibrate_ema_workspace_size(rows))
-    return fail(DSA_ERR_WORKSPACE, "workspace of %zu bytes needed",
-                dsa_calibrate_ema_workspace_size(rows));
-  cudaError_t e = launch_calib(traj, steps, rows, n, stride, k, k_pred, H, best,
-                               static_cast<unsigned*>(workspace),
+  const size_t need = dsa_calibrate_ema_workspace_size(steps, rows, n, k);
+  if (!workspace || workspace_bytes < need)
+    return fail(DSA_ERR_WORKSPACE, "workspace of %zu bytes needed", need);
+  if (!aligned(workspace, 16)) return fail(DSA_ERR_ALIGNMENT, "workspace must be 16-byte aligned");
+  if (static_cast<long long>(steps) * rows > 0x7fffffffLL)
+    return fail(DSA_ERR_UNSUPPORTED, "steps * rows too large");
+  cudaError_t e = launch_calib(traj, steps, rows, n, stride, k, k_pred, H, best, workspace,
                                static_cast<cudaStream_t>(stream));
   return e == cudaSuccess ? ok() : cuda_fail(e, "dsa_calibrate_ema launch");
 }

@@ -176,8 +176,14 @@ cudaError_t launch_ema(const float* IS, int rows, int n, int stride, float* ell,
 constexpr int kCalibPoints = 80;
 constexpr int kCalibMaxN = 16384;  // pages per row whose predictor state fits in shared memory
 size_t calib_smem_bytes(int n);
+// workspace: per-row counters, A_t of every (step, row) (counts, indices), the predictor state of
+// every (row, grid point)
+struct CalibWorkspace {
+  size_t done_off, cnt_off, idx_off, state_off, total;
+};
+CalibWorkspace calib_workspace(int T, int rows, int n, int k);
 cudaError_t launch_calib(const float* traj, int T, int rows, int n, int stride, int k, int k_pred,
-                         float* H, int32_t* best, unsigned* done, cudaStream_t s);
+                         float* H, int32_t* best, void* workspace, cudaStream_t s);
 
 struct ThresholdArgs {
   KvView kv;

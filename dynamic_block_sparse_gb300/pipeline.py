@@ -230,6 +230,27 @@ class PRRDecoder:
                                           device=dev)
         self.t = 0
 
+    def calibrate(self, traj, stream=None):
+        """PRR §3.2: rates the 80-point (alpha, beta, gamma) grid on a trajectory of true score
+        vectors ``traj`` fp32 ``[steps][B][Hkv][stride]`` (e.g. scored during prefill) with
+        ``dsa_calibrate_ema`` and adopts, for every row, the point that wins for most rows (ties to
+        the lower point).  Returns (H ``[rows][80]``, best ``[rows]``)."""
+        c = self.cache
+        steps = traj.shape[0]
+        t3 = traj.reshape(steps, c.batch * c.num_kv_heads, traj.shape[-1])
+        rows = t3.shape[1]
+        H = torch.empty((rows, B.CALIB_POINTS), dtype=torch.float32, device=c.device)
+        best = torch.empty(rows, dtype=torch.int32, device=c.device)
+        need = B.dsa_calibrate_ema_workspace_size(steps, rows, c.max_pages, self.k)
+        ws = getattr(self, "calib_workspace", None)
+        if ws is None or ws.numel() < need:
+            self.calib_workspace = torch.zeros(need, dtype=torch.uint8, device=c.device)
+        B.dsa_calibrate_ema(t3, c.max_pages, self.k, self.k_pred, H, best, self.calib_workspace,
+                            stream)
+        votes = torch.bincount(best.long(), minlength=B.CALIB_POINTS)
+        self.alpha, self.beta, self.gamma = B.calibration_point(int(torch.argmax(votes)))
+        return H, best
+
     def host_result(self):
         """Moves (O, m, l) into one page-locked host buffer that the fused step writes directly
         (no device-to-host copy); a fused step t >= 1 also accepts a page-locked host query.  The

@@ -274,21 +274,25 @@ int dsa_ema_predict_update(const float* IS, int32_t rows, int32_t n, int32_t str
  * prediction made from steps 0..t-1 (step 0 initialises the state); both selections rank as
  * dsa_select_topk does.  The grid point with the largest H wins, ties to the lower point.
  * Grid point c (0..79): alpha = 0.2 (1 + c / 20), beta = 0.1 (1 + (c / 4) % 5),
- * gamma = 0.25 (c % 4) -- alpha outermost, gamma innermost.  One launch, one CTA per
- * (row, grid point); the parameters are fp32.
+ * gamma = 0.25 (c % 4) -- alpha outermost, gamma innermost.  One CTA per (row, grid point);
+ * the parameters are fp32.
  *   traj      : fp32 [steps][rows][stride], IS_t of row r at traj[(t * rows + r) * stride];
  *               entries 0..n-1 are pages (-inf = no page).  1 <= n <= min(stride, 16384).
  *   H (out)   : fp32 [rows][80].
  *   best (out): int32 [rows], the winning grid point.
  *   1 <= k, k_pred <= 256; steps >= 1 (steps = 1 rates every point 0 and picks point 0).
- *   workspace : dsa_calibrate_ema_workspace_size(rows) bytes, ZERO-FILLED before its first use;
- *               each completed call leaves it zero-filled.
+ *   workspace : dsa_calibrate_ema_workspace_size(steps, rows, n, k) bytes, 16-byte aligned, its
+ *               first 4 * rows bytes ZERO-FILLED before the first use (each completed call
+ *               leaves them zero-filled); the rest is scratch: A_t of every (step, row), selected
+ *               once because it does not depend on the grid point, and the predictor state of
+ *               every (row, grid point), 640 * n bytes per row.
+ * Two launches: the top-k selection of A_t over the whole trajectory, then the grid.
  */
 #define DSA_CALIB_POINTS 80
 int dsa_calibrate_ema(const float* traj, int32_t steps, int32_t rows, int32_t n, int32_t stride,
                       int32_t k, int32_t k_pred, float* H, int32_t* best, void* workspace,
                       size_t workspace_bytes, dsa_stream_t stream);
-size_t dsa_calibrate_ema_workspace_size(int32_t rows);
+size_t dsa_calibrate_ema_workspace_size(int32_t steps, int32_t rows, int32_t n, int32_t k);
 
 /*
  * One whole PRR decode step t >= 1 in a single launch ([PRR] §3 end to end: speculation over the

@@ -413,10 +413,11 @@ def _calib_gpu(traj, n, k, k_pred, stride):
         T[t, :, :n] = x.cuda()
     H = torch.empty((rows, B.CALIB_POINTS), device="cuda")
     best = torch.full((rows,), -1, dtype=torch.int32, device="cuda")
-    ws = torch.zeros(B.dsa_calibrate_ema_workspace_size(rows), dtype=torch.uint8, device="cuda")
+    ws = torch.zeros(B.dsa_calibrate_ema_workspace_size(steps, rows, n, k), dtype=torch.uint8,
+                     device="cuda")
     B.dsa_calibrate_ema(T, n, k, k_pred, H, best, ws)
     torch.cuda.synchronize()
-    assert int(ws.sum()) == 0, "the workspace is left zero-filled"
+    assert int(ws[:4 * rows].sum()) == 0, "the row counters are left zero-filled"
     return H.double().cpu().numpy(), best.cpu().numpy()
 
 

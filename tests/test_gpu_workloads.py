@@ -310,6 +310,40 @@ def test_prr_without_second_stream_matches():
     assert torch.equal(outs[0], outs[1])
 
 
+def test_prr_decoder_calibrates_on_its_score_trajectory():
+    """PRRDecoder.calibrate rates the grid on a trajectory of the workload's own true scores (the
+    scoring call over a random-walking query) and adopts the majority point; the rates match the
+    oracle's calibration on sampled grid points."""
+    w = oracle_scale(BY_NAME["prr_512k"]).replace(steps=8)
+    inp = to_cuda(make_inputs(w, "cpu"))
+    dec = PRRDecoder(Cache.from_inputs(inp), w.k, w.k_pred, w.alpha, w.beta, w.gamma)
+    dec.build_meta()
+    traj = torch.empty((w.steps,) + tuple(dec.scores.shape), device="cuda")
+    for t in range(w.steps):
+        dec.stage_score(inp["q"][t])
+        traj[t].copy_(dec.scores)
+    H, best = dec.calibrate(traj)
+    torch.cuda.synchronize()
+    rows = traj.shape[1] * traj.shape[2]
+    t3 = traj.view(w.steps, rows, -1).cpu().double().numpy()
+    grid = O.calibration_grid()
+    for r in range(rows):
+        n = int(np.isfinite(t3[0, r]).sum())
+        tr = [t3[t, r, :n] for t in range(w.steps)]
+        for c in (0, 13, 42, int(best[r])):
+            a, b, g = grid[c]
+            ell, v = O.ema_init(tr[0])
+            tot = 0.0
+            for t in range(1, w.steps):
+                P = O.select_topk(O.ema_predict(ell, v, g), w.k_pred)
+                A = O.select_topk(tr[t], w.k)
+                tot += O.score_weighted_hit(P, A, tr[t])
+                ell, v = O.ema_update(tr[t], ell, v, a, b)
+            assert abs(float(H[r, c]) - tot / (w.steps - 1)) < 2e-3, f"row {r} point {c}"
+    assert (dec.alpha, dec.beta, dec.gamma) == B.calibration_point(
+        int(torch.bincount(best.long(), minlength=80).argmax()))
+
+
 def test_prr_step_with_host_query_and_result():
     """The fused step with its query and its result (O, m, l) in page-locked host memory, which the
     kernel reads and writes over the host link itself, gives the same scores, selections, EMA

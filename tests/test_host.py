@@ -110,8 +110,9 @@ def test_binding_refuses_cpu_tensors(lib):
 def test_calibrate_ema_host_validation_without_gpu(lib):
     """dsa_calibrate_ema rejects bad arguments on the host, before any CUDA call."""
     p = 4096
-    need = lib.dsa_calibrate_ema_workspace_size(3)
-    assert need == 16
+    need = lib.dsa_calibrate_ema_workspace_size(8, 3, 500, 16)
+    # counters, A_t counts and indices of every (step, row), predictor state of every (row, point)
+    assert need == 16 + 96 + 8 * 3 * 16 * 4 + 3 * 80 * 2 * 500 * 4
     call = lambda steps=8, rows=3, n=500, stride=512, k=16, kp=20, ws=need: \
         lib.dsa_calibrate_ema(p, steps, rows, n, stride, k, kp, p * 2, p * 3, p * 4, ws, None)
     assert lib.dsa_calibrate_ema(p, 8, 0, 500, 512, 16, 20, p, p, p, 0, None) == 0  # no rows
