@@ -514,6 +514,15 @@ def bench_rows(dev, flush, peak):
     ms = _time_graph(_graph(lambda: dec.step(q)), flush)
     out.append(_entry("step", w.name, "score + top-K + attention", ms,
                       rows * npg * 512 + sel * w.page_size * KVP + rows * dec.stride * 8, peak))
+    # decode-time append of one token per request (replayed: it rewrites the newest token and
+    # recomputes its page's metadata, the work of every append)
+    k_new = torch.randn((w.batch, w.num_kv_heads, w.head_dim), device=dev).bfloat16()
+    v_new = torch.randn_like(k_new)
+    ms = _time_graph(_graph(lambda: B.dsa_append_kv(cache.kv, k_new, v_new, B.DSA_META_MINMAX,
+                                                    w.logical_page, dec.meta)), flush)
+    tail = [(int(L) - 1) % w.page_size + 1 for L in cache.seq_lens.tolist()]
+    out.append(_entry("N2", w.name, "dsa_append_kv: K/V of one token + its page's kmax/kmin", ms,
+                      sum(w.num_kv_heads * (KVP + t * 256 + 512) for t in tail), peak))
     del dec, cache, inp
     torch.cuda.empty_cache()
 

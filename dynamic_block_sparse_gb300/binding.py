@@ -61,6 +61,7 @@ _SIGNATURES = {
     "dsa_last_error": ([], ctypes.c_char_p),
     "dsa_version": ([], ctypes.c_char_p),
     "dsa_build_page_meta": ([_P, _I, _I, _P, _P], _I),
+    "dsa_append_kv": ([_P, _P, _P, _I, _I, _P, _P], _I),
     "dsa_score_pages": ([_P, _P, _P, _I, _I, _P, _I, _P], _I),
     "dsa_select_topk": ([_P, _I, _I, _I, _I, _P, _I, _P, _P], _I),
     "dsa_select_hier": ([_P, _I, _I, _I, _I, _I, _P, _I, _P, _P], _I),
@@ -173,6 +174,15 @@ def paged_kv(k_pages, v_pages, page_table, seq_lens, num_q_heads: int,
 def dsa_build_page_meta(kv: PagedKV, meta_kind: int, logical_page: int, meta, stream=None):
     _check("dsa_build_page_meta", load().dsa_build_page_meta(
         ctypes.byref(kv), meta_kind, logical_page, _ptr(meta), _stream(stream)))
+
+
+def dsa_append_kv(kv: PagedKV, k_new, v_new, meta_kind: int = 0, logical_page: int = 0,
+                  meta=None, stream=None):
+    """Writes the token at position seq_lens[b] - 1 (already counted) of every request into the
+    pools and recomputes its page's metadata in ``meta`` (if given)."""
+    _check("dsa_append_kv", load().dsa_append_kv(
+        ctypes.byref(kv), _ptr(k_new), _ptr(v_new), meta_kind, logical_page, _ptr(meta),
+        _stream(stream)))
 
 
 def dsa_score_pages(kv: PagedKV, q, meta, meta_kind: int, logical_page: int, scores,

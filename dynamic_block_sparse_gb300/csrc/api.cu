@@ -220,6 +220,31 @@ int dsa_build_page_meta(const dsa_paged_kv* kv, int32_t meta_kind, int32_t logic
   return e == cudaSuccess ? ok() : cuda_fail(e, "dsa_build_page_meta launch");
 }
 
+int dsa_append_kv(const dsa_paged_kv* kv, const void* k_new, const void* v_new,
+                  int32_t meta_kind, int32_t logical_page, void* meta, dsa_stream_t stream) {
+  KvView v;
+  int rc = check_kv(kv, 1, &v);
+  if (rc) return rc;
+  if (!k_new || !v_new) return fail(DSA_ERR_INVALID_ARG, "k_new/v_new is NULL");
+  if (!aligned(k_new, 16) || !aligned(v_new, 16))
+    return fail(DSA_ERR_ALIGNMENT, "k_new/v_new must be 16-byte aligned");
+  if (meta) {
+    if (meta_kind != DSA_META_MINMAX && meta_kind != DSA_META_MEAN)
+      return fail(DSA_ERR_INVALID_ARG, "unknown meta_kind %d", meta_kind);
+    if (logical_page <= 0 || v.p % logical_page != 0)
+      return fail(DSA_ERR_INVALID_ARG, "logical_page %d must divide page_size %d", logical_page,
+                  v.p);
+    if (!aligned(meta, 16)) return fail(DSA_ERR_ALIGNMENT, "meta must be 16-byte aligned");
+  }
+  // the pools are the caller's, written here (the struct's pointers are const for the readers)
+  cudaError_t e = launch_append_kv(
+      v, static_cast<__nv_bfloat16*>(const_cast<void*>(kv->k_pages)),
+      static_cast<__nv_bfloat16*>(const_cast<void*>(kv->v_pages)),
+      static_cast<const __nv_bfloat16*>(k_new), static_cast<const __nv_bfloat16*>(v_new),
+      meta_kind, logical_page, meta, static_cast<cudaStream_t>(stream));
+  return e == cudaSuccess ? ok() : cuda_fail(e, "dsa_append_kv launch");
+}
+
 int dsa_score_pages(const dsa_paged_kv* kv, const void* q, const void* meta, int32_t meta_kind,
                     int32_t logical_page, float* scores, int32_t score_stride,
                     dsa_stream_t stream) {

@@ -161,6 +161,9 @@ cudaError_t launch_prr_step(const CUtensorMap& tmK, const CUtensorMap& tmV, cons
 // metadata and scoring
 cudaError_t launch_build_meta(const KvView& kv, const __nv_bfloat16* k_pages, int kind, int lp,
                               void* meta, cudaStream_t s);
+cudaError_t launch_append_kv(const KvView& kv, __nv_bfloat16* k_pages, __nv_bfloat16* v_pages,
+                             const __nv_bfloat16* k_new, const __nv_bfloat16* v_new, int kind,
+                             int lp, void* meta, cudaStream_t s);
 cudaError_t launch_score(const KvView& kv, const __nv_bfloat16* q, const void* meta, int kind,
                          int lp, float* scores, int stride, cudaStream_t s);
 

@@ -8,27 +8,22 @@ namespace dsa {
 namespace {
 
 // ------------------------------------------------------------------------------------ metadata
-// One warp per (request, page position, KV head).  Lane l reads 16-byte chunk (l & 15) of token
-// rows of parity (l >> 4); the two half-warps are combined at the end of every logical page.
-template <int KIND>
-__global__ void __launch_bounds__(256)
-    build_meta_kernel(const KvView kv, const __nv_bfloat16* __restrict__ k_pages, int lp,
-                      void* __restrict__ meta) {
-  const int lane = threadIdx.x & 31;
-  const long long item = static_cast<long long>(blockIdx.x) * 8 + (threadIdx.x >> 5);
-  const int h = static_cast<int>(item % kv.Hkv);
-  const long long bj = item / kv.Hkv;
-  const int b = static_cast<int>(bj / kv.max_pages), j = static_cast<int>(bj % kv.max_pages);
-  if (b >= kv.B) return;
+// 16 bytes of a K row: through the read-only path, or through L2 when the row was written by the
+// same kernel (the read-only path is not coherent with such writes).
+template <bool COHERENT>
+DSA_DEV uint4 ld16(const __nv_bfloat16* p) {
+  return COHERENT ? __ldcg(reinterpret_cast<const uint4*>(p))
+                  : __ldg(reinterpret_cast<const uint4*>(p));
+}
+
+// Metadata of every logical sub-page of page position j of request b (length L), KV head h, on
+// physical page phys, computed by one warp.  Lane l reads 16-byte chunk (l & 15) of token rows of
+// parity (l >> 4); the two half-warps are combined at the end of every logical page.  The build
+// and the append share it, so both write the same bits.
+template <int KIND, bool COHERENT>
+DSA_DEV void page_meta(const KvView& kv, const __nv_bfloat16* __restrict__ k_pages, int lp,
+                       void* __restrict__ meta, int j, int h, int phys, int L, int lane) {
   const int page = kv.p;
-  const int L = request_len(kv, b);
-  const int npos = (L + page - 1) / page;
-  if (j >= npos) return;
-  const int phys = kv.page_table[static_cast<size_t>(b) * kv.max_pages + j];
-  if (phys < 0 || phys >= kv.num_phys) {
-    if (lane == 0) raise_status(kv.status, DSA_STATUS_BAD_PAGE);
-    return;
-  }
   const int valid = min(page, L - j * page);
   const int g = page / lp;
   const int half = lane >> 4, c = lane & 15;
@@ -49,7 +44,7 @@ __global__ void __launch_bounds__(256)
       uint4 raw[4];
 #pragma unroll
       for (int u = 0; u < 4; ++u)
-        raw[u] = __ldg(reinterpret_cast<const uint4*>(base + static_cast<size_t>(t + 2 * u) * kHeadDim));
+        raw[u] = ld16<COHERENT>(base + static_cast<size_t>(t + 2 * u) * kHeadDim);
 #pragma unroll
       for (int u = 0; u < 4; ++u) {
         const __nv_bfloat16* v = reinterpret_cast<const __nv_bfloat16*>(&raw[u]);
@@ -66,7 +61,7 @@ __global__ void __launch_bounds__(256)
       }
     }
     for (; t < t_hi; t += 2) {
-      const uint4 raw = __ldg(reinterpret_cast<const uint4*>(base + static_cast<size_t>(t) * kHeadDim));
+      const uint4 raw = ld16<COHERENT>(base + static_cast<size_t>(t) * kHeadDim);
       const __nv_bfloat16* v = reinterpret_cast<const __nv_bfloat16*>(&raw);
 #pragma unroll
       for (int e = 0; e < 8; ++e) {
@@ -118,6 +113,60 @@ __global__ void __launch_bounds__(256)
       *reinterpret_cast<float4*>(dst) = o;
     }
   }
+}
+
+// One warp per (request, page position, KV head).
+template <int KIND>
+__global__ void __launch_bounds__(256)
+    build_meta_kernel(const KvView kv, const __nv_bfloat16* __restrict__ k_pages, int lp,
+                      void* __restrict__ meta) {
+  const int lane = threadIdx.x & 31;
+  const long long item = static_cast<long long>(blockIdx.x) * 8 + (threadIdx.x >> 5);
+  const int h = static_cast<int>(item % kv.Hkv);
+  const long long bj = item / kv.Hkv;
+  const int b = static_cast<int>(bj / kv.max_pages), j = static_cast<int>(bj % kv.max_pages);
+  if (b >= kv.B) return;
+  const int L = request_len(kv, b);
+  const int npos = (L + kv.p - 1) / kv.p;
+  if (j >= npos) return;
+  const int phys = kv.page_table[static_cast<size_t>(b) * kv.max_pages + j];
+  if (phys < 0 || phys >= kv.num_phys) {
+    if (lane == 0) raise_status(kv.status, DSA_STATUS_BAD_PAGE);
+    return;
+  }
+  page_meta<KIND, false>(kv, k_pages, lp, meta, j, h, phys, L, lane);
+}
+
+// One warp per (request, KV head): writes the request's newest token (position L - 1) into its
+// page of the pools, then recomputes that page's metadata (when meta is given).
+template <int KIND>
+__global__ void __launch_bounds__(256)
+    append_kv_kernel(const KvView kv, __nv_bfloat16* __restrict__ k_pages,
+                     __nv_bfloat16* __restrict__ v_pages, const __nv_bfloat16* __restrict__ k_new,
+                     const __nv_bfloat16* __restrict__ v_new, int lp, void* __restrict__ meta) {
+  const int lane = threadIdx.x & 31;
+  const long long item = static_cast<long long>(blockIdx.x) * 8 + (threadIdx.x >> 5);
+  const int h = static_cast<int>(item % kv.Hkv);
+  const int b = static_cast<int>(item / kv.Hkv);
+  if (b >= kv.B) return;
+  const int L = request_len(kv, b);
+  if (L <= 0) return;
+  const int t = L - 1, j = t / kv.p;
+  const int phys = kv.page_table[static_cast<size_t>(b) * kv.max_pages + j];
+  if (phys < 0 || phys >= kv.num_phys) {
+    if (lane == 0) raise_status(kv.status, DSA_STATUS_BAD_PAGE);
+    return;
+  }
+  const size_t row = (static_cast<size_t>(phys) * kv.Hkv + h) * kv.p + (t - j * kv.p);
+  const size_t src = (static_cast<size_t>(b) * kv.Hkv + h) * kHeadDim;
+  const int c = lane & 15;  // lanes 0..15 copy the K row, 16..31 the V row, 16 bytes each
+  const __nv_bfloat16* from = (lane < 16 ? k_new : v_new) + src + c * 8;
+  __nv_bfloat16* to = (lane < 16 ? k_pages : v_pages) + row * kHeadDim + c * 8;
+  *reinterpret_cast<uint4*>(to) = __ldg(reinterpret_cast<const uint4*>(from));
+  if (meta == nullptr) return;
+  __threadfence_block();
+  __syncwarp();  // the new K row is visible to the whole warp
+  page_meta<KIND, true>(kv, k_pages, lp, meta, j, h, phys, L, lane);
 }
 
 // ------------------------------------------------------------------------------------ scoring
@@ -185,6 +234,21 @@ cudaError_t launch_build_meta(const KvView& kv, const __nv_bfloat16* k_pages, in
     build_meta_kernel<DSA_META_MINMAX><<<static_cast<unsigned>(blocks), 256, 0, s>>>(kv, k_pages, lp, meta);
   else
     build_meta_kernel<DSA_META_MEAN><<<static_cast<unsigned>(blocks), 256, 0, s>>>(kv, k_pages, lp, meta);
+  return cudaGetLastError();
+}
+
+cudaError_t launch_append_kv(const KvView& kv, __nv_bfloat16* k_pages, __nv_bfloat16* v_pages,
+                             const __nv_bfloat16* k_new, const __nv_bfloat16* v_new, int kind,
+                             int lp, void* meta, cudaStream_t s) {
+  const long long items = static_cast<long long>(kv.B) * kv.Hkv;
+  const long long blocks = (items + 7) / 8;
+  if (blocks > 0x7fffffffLL) return cudaErrorInvalidValue;
+  if (kind == DSA_META_MINMAX)
+    append_kv_kernel<DSA_META_MINMAX><<<static_cast<unsigned>(blocks), 256, 0, s>>>(
+        kv, k_pages, v_pages, k_new, v_new, lp, meta);
+  else
+    append_kv_kernel<DSA_META_MEAN><<<static_cast<unsigned>(blocks), 256, 0, s>>>(
+        kv, k_pages, v_pages, k_new, v_new, lp, meta);
   return cudaGetLastError();
 }
 

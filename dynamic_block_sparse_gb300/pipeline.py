@@ -50,6 +50,17 @@ class Cache:
         hs = t["head_is_streaming"] if w.streaming_kv_heads else None
         return cls(t["k_pages"], t["v_pages"], t["page_table"], t["seq_lens"], w.num_q_heads, hs)
 
+    def append(self, k_new, v_new, metas=(), stream=None):
+        """Decode-time append of one token per request (K and V bf16 ``[B][Hkv][D]``): advances
+        ``seq_lens``, writes the token into its page and recomputes that page of every
+        ``(kind, logical_page, meta)`` buffer in ``metas``.  The page table must already map the
+        new position (a token that starts a page needs its page assigned first)."""
+        self.seq_lens.add_(1)
+        if not metas:
+            B.dsa_append_kv(self.kv, k_new, v_new, stream=stream)
+        for kind, lp, meta in metas:
+            B.dsa_append_kv(self.kv, k_new, v_new, kind, lp, meta, stream)
+
     def meta_buffer(self, kind: int, logical_page: int) -> torch.Tensor:
         g = self.page_size // logical_page
         if kind == B.DSA_META_MINMAX:
@@ -98,6 +109,10 @@ class TopKDecoder:
     def build_meta(self, stream=None):
         B.dsa_build_page_meta(self.cache.kv, self.kind, self.lp, self.meta, stream)
 
+    def append(self, k_new, v_new, stream=None):
+        """Appends one decoded token per request, keeping this decoder's metadata current."""
+        self.cache.append(k_new, v_new, [(self.kind, self.lp, self.meta)], stream)
+
     def select(self, q, stream=None):
         c = self.cache
         B.dsa_score_pages(c.kv, q, self.meta, self.kind, self.lp, self.scores, stream)
@@ -134,6 +149,10 @@ class HierDecoder:
 
     def build_meta(self, stream=None):
         B.dsa_build_page_meta(self.cache.kv, B.DSA_META_MINMAX, self.lp, self.meta, stream)
+
+    def append(self, k_new, v_new, stream=None):
+        """Appends one decoded token per request, keeping this decoder's metadata current."""
+        self.cache.append(k_new, v_new, [(B.DSA_META_MINMAX, self.lp, self.meta)], stream)
 
     def select(self, q, stream=None):
         c = self.cache
@@ -172,6 +191,11 @@ class ThresholdDecoder:
     def build_meta(self, stream=None):
         B.dsa_build_page_meta(self.cache.kv, B.DSA_META_MEAN, self.cache.page_size, self.meta,
                               stream)
+
+    def append(self, k_new, v_new, stream=None):
+        """Appends one decoded token per request, keeping this decoder's metadata current."""
+        self.cache.append(k_new, v_new, [(B.DSA_META_MEAN, self.cache.page_size, self.meta)],
+                          stream)
 
     def step(self, q, stream=None):
         c = self.cache
@@ -277,6 +301,14 @@ class PRRDecoder:
     def build_meta(self, stream=None):
         B.dsa_build_page_meta(self.cache.kv, B.DSA_META_MINMAX, self.cache.page_size, self.meta,
                               stream)
+
+    def append(self, k_new, v_new, stream=None):
+        """Appends one decoded token per request, keeping the metadata current.  The score rows
+        and the predictor state already span the page table (stride = max pages), so a page that
+        opens later needs nothing else: it gets a score once it holds a token, and the predictor
+        treats it as fresh (level = its score, trend 0)."""
+        c = self.cache
+        c.append(k_new, v_new, [(B.DSA_META_MINMAX, c.page_size, self.meta)], stream)
 
     # ---- stages (one or two library calls each), exposed so a caller can time them one by one
     def stage_score(self, q, stream=None):

@@ -110,6 +110,22 @@ int dsa_build_page_meta(const dsa_paged_kv* kv, int32_t meta_kind, int32_t logic
                         void* meta, dsa_stream_t stream);
 
 /*
+ * Decode-time KV append ([LServe] §4.2: the page metadata is kept current as decoding adds
+ * tokens): for every request b with L_b > 0, writes the token at position L_b - 1 -- kv->seq_lens
+ * ALREADY counts it -- into its page of the pools (WRITTEN through kv->k_pages / kv->v_pages),
+ * then recomputes the metadata of that page (every logical sub-page of it) exactly as
+ * dsa_build_page_meta computes it, bit for bit.
+ *   k_new, v_new : bf16 [B][Hkv][D], 16-byte aligned: the new token's key and value per KV head.
+ *   meta         : as for dsa_build_page_meta, or NULL to write the KV only.  A caller keeping
+ *                  several metadata buffers calls once per buffer (the KV write repeats
+ *                  harmlessly).
+ * The caller assigns page_table[b][(L_b - 1) / p] before a token that starts a new page.  A bad
+ * page id skips the request and raises DSA_STATUS_BAD_PAGE.  One warp per (request, KV head).
+ */
+int dsa_append_kv(const dsa_paged_kv* kv, const void* k_new, const void* v_new,
+                  int32_t meta_kind, int32_t logical_page, void* meta, dsa_stream_t stream);
+
+/*
  * Page criticality ([LServe] §4.2: S^j = sum_i max(q_i kmax^j_i, q_i kmin^j_i); [PSA] §3.2:
  * CS = q . meta; [PRR] §5: one representative query per KV head for GQA).
  *   q            : bf16 [B][Hq][D].  The representative query of KV head h is the fp32 mean of

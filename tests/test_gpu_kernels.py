@@ -10,8 +10,8 @@ import oracle as O
 from dynamic_block_sparse_gb300 import binding as B
 from dynamic_block_sparse_gb300.pipeline import Cache
 from dynamic_block_sparse_gb300.workloads import Workload, make_inputs
-from support import (assert_outputs, check_topk, f64, oracle_mean_scores, oracle_minmax_scores,
-                     row_tokens, to_cuda)
+from support import (assert_outputs, attend_pages, check_topk, f64, oracle_mean_scores,
+                     oracle_minmax_scores, row_tokens, to_cuda)
 
 pytestmark = pytest.mark.gpu
 
@@ -60,6 +60,113 @@ def test_build_page_meta(page, lp, kind):
                 for j in range(len(mean)):
                     rec = mcpu[table[b, j // g], h, j % g]
                     np.testing.assert_allclose(rec, mean[j], rtol=1e-6, atol=1e-6)
+    assert int(cache.status.item()) == 0
+
+
+@pytest.mark.parametrize("page,lp,kind", [(16, 16, "minmax"), (64, 16, "minmax"),
+                                          (32, 8, "mean"), (64, 64, "mean")])
+def test_append_kv_keeps_metadata_exact(page, lp, kind):
+    """Decode-time KV append (LServe §4.2): each request loses 2 pages + 3 tokens of its context,
+    then grows back one token at a time (crossing page boundaries) with fresh random K/V.  After
+    every append the pools hold the token and the incrementally kept metadata equals a full
+    rebuild bit for bit; at the end it also equals the oracle's metadata of the grown context."""
+    w, inp, cache = small(page=page, lp=lp, kind=kind, L=page * 9 + 5)
+    code = B.DSA_META_MINMAX if kind == "minmax" else B.DSA_META_MEAN
+    grow = 2 * page + 3
+    L_end = cache.seq_lens.clone()
+    cache.seq_lens.sub_(torch.clamp(L_end - 1, max=grow))      # every request keeps >= 1 token
+    meta = cache.meta_buffer(code, lp)
+    B.dsa_build_page_meta(cache.kv, code, lp, meta)
+    gen = torch.Generator(device="cuda").manual_seed(21)
+    kp, vp = cache.k_pages.clone(), cache.v_pages.clone()     # the expected pools
+    table = cache.page_table.long()
+    for step in range(grow):
+        live = cache.seq_lens < L_end
+        if not bool(live.any()):
+            break
+        k_new = torch.randn((w.batch, w.num_kv_heads, 128), generator=gen, device="cuda")
+        v_new = torch.randn((w.batch, w.num_kv_heads, 128), generator=gen, device="cuda")
+        k_new, v_new = k_new.bfloat16(), v_new.bfloat16()
+        # requests that reached their length append nothing: their length stays 0-advanced
+        lens = cache.seq_lens + live.int()
+        cache.seq_lens.copy_(lens)
+        for b in range(w.batch):
+            if not bool(live[b]):
+                continue
+            t = int(lens[b]) - 1
+            phys = int(table[b, t // page])
+            kp[phys, :, t % page] = k_new[b]
+            vp[phys, :, t % page] = v_new[b]
+        # a request that did not grow is given its current last token again (a no-op rewrite)
+        for b in range(w.batch):
+            if not bool(live[b]):
+                t = int(lens[b]) - 1
+                phys = int(table[b, t // page])
+                k_new[b] = kp[phys, :, t % page]
+                v_new[b] = vp[phys, :, t % page]
+        B.dsa_append_kv(cache.kv, k_new, v_new, code, lp, meta)
+        full = cache.meta_buffer(code, lp)
+        B.dsa_build_page_meta(cache.kv, code, lp, full)
+        torch.cuda.synchronize()
+        assert torch.equal(cache.k_pages, kp) and torch.equal(cache.v_pages, vp), f"pools {step}"
+        assert torch.equal(meta, full), f"metadata after append {step}"
+    assert torch.equal(cache.seq_lens, L_end)
+    g = page // lp
+    mcpu = meta.float().cpu().numpy()
+    for b in range(w.batch):
+        for h in range(w.num_kv_heads):
+            L = int(L_end[b])
+            K = row_tokens(cache.k_pages, cache.page_table, L, b, h)
+            if kind == "minmax":
+                kmax, kmin = O.page_meta_minmax(K, lp)
+                for jj in range(len(kmax)):
+                    rec = mcpu[int(table[b, jj // g]), h, jj % g]
+                    np.testing.assert_array_equal(rec[:, 0], kmax[jj])
+                    np.testing.assert_array_equal(rec[:, 1], kmin[jj])
+            else:
+                mean = O.page_meta_mean(K, lp)
+                for jj in range(len(mean)):
+                    rec = mcpu[int(table[b, jj // g]), h, jj % g]
+                    np.testing.assert_allclose(rec, mean[jj], rtol=1e-6, atol=1e-6)
+    assert int(cache.status.item()) == 0
+
+
+def test_decode_loop_with_kv_append():
+    """A top-K decode loop that appends each step's token before attending (the metadata kept by
+    the appends, never rebuilt): every step selects the oracle's top-K over the grown context and
+    attends exactly over it."""
+    w, inp, cache = small(page=16, L=16 * 40 + 9, seed=8)
+    grow = 20
+    L_end = cache.seq_lens.clone()
+    cache.seq_lens.sub_(grow)
+    from dynamic_block_sparse_gb300.pipeline import TopKDecoder
+    dec = TopKDecoder(cache, 12)
+    dec.build_meta()
+    gen = torch.Generator(device="cuda").manual_seed(22)
+    G = w.num_q_heads // w.num_kv_heads
+    for step in range(grow):
+        k_new = torch.randn((w.batch, w.num_kv_heads, 128), generator=gen, device="cuda").bfloat16()
+        v_new = torch.randn((w.batch, w.num_kv_heads, 128), generator=gen, device="cuda").bfloat16()
+        q = torch.randn((w.batch, w.num_q_heads, 128), generator=gen, device="cuda").bfloat16()
+        dec.append(k_new, v_new)
+        out, m, l = dec.step(q)
+        torch.cuda.synchronize()
+        if step % 5 != 4:
+            continue
+        for b in range(w.batch):
+            L = int(cache.seq_lens[b])
+            for h in range(w.num_kv_heads):
+                K = row_tokens(cache.k_pages, cache.page_table, L, b, h)
+                qg = q[b, h * G:(h + 1) * G]
+                IS = oracle_minmax_scores(K, qg, 16, dec.stride)
+                A = dec.idx[b, h, :int(dec.count[b, h])].cpu().numpy()
+                check_topk(A, IS, 12, f"step {step} b{b} h{h}")
+                ref = attend_pages(qg, cache.k_pages, cache.v_pages, cache.page_table, L, b, h,
+                                   sorted(A.tolist()), dec.scale)
+                sl = slice(h * G, (h + 1) * G)
+                assert_outputs(out[b, sl].cpu().numpy(), m[b, sl].cpu().numpy(),
+                               l[b, sl].cpu().numpy(), ref, f"step {step} b{b} h{h}")
+    assert torch.equal(cache.seq_lens, L_end)
     assert int(cache.status.item()) == 0
 
 

@@ -344,6 +344,45 @@ def test_prr_decoder_calibrates_on_its_score_trajectory():
         int(torch.bincount(best.long(), minlength=80).argmax()))
 
 
+def test_prr_decode_loop_with_kv_append():
+    """PRR decoding while the context grows: before every step each request appends a token
+    (metadata kept by the append, never rebuilt), opening new pages along the way.  The fused step
+    and the separate-launch path agree bit for bit on scores, selections and the EMA state (new
+    pages start fresh), and to fp32 rounding on the outputs."""
+    w = oracle_scale(BY_NAME["prr_512k"]).replace(steps=10, ragged=True, batch=2)
+    inp = to_cuda(make_inputs(w, "cpu"))
+    grow = 2 * w.page_size + 5
+    decs = []
+    for fused in (True, False):
+        # each decoder grows its own copy of the cache (inputs already on the device are not
+        # copied by Cache.from_inputs)
+        own = {k: (v.clone() if torch.is_tensor(v) else v) for k, v in inp.items()}
+        cache = Cache.from_inputs(own)
+        cache.seq_lens.sub_(grow)
+        dec = PRRDecoder(cache, w.k, w.k_pred, w.alpha, w.beta, w.gamma, fused=fused)
+        dec.build_meta()
+        decs.append(dec)
+    f, s_ = decs
+    gen = torch.Generator(device="cuda").manual_seed(31)
+    shape = (w.batch, w.num_kv_heads, 128)
+    for t in range(w.steps):
+        for _ in range(grow // w.steps):
+            k_new = torch.randn(shape, generator=gen, device="cuda").bfloat16()
+            v_new = torch.randn(shape, generator=gen, device="cuda").bfloat16()
+            for dec in decs:
+                dec.append(k_new, v_new)
+        for dec in decs:
+            dec.step(inp["q"][t % inp["q"].shape[0]])
+        torch.cuda.synchronize()
+        assert torch.equal(f.cache.k_pages, s_.cache.k_pages)
+        assert torch.equal(f.meta, s_.meta)
+        for name in ("scores", "ell", "trend", "idx", "count"):
+            assert torch.equal(getattr(f, name), getattr(s_, name)), f"{name} at step {t}"
+        assert_outputs(f.out.cpu().numpy(), f.m.cpu().numpy(), f.l.cpu().numpy(),
+                       [x.double().cpu().numpy() for x in (s_.out, s_.m, s_.l)], f"step {t}")
+        assert int(f.cache.status.item()) == 0 and int(s_.cache.status.item()) == 0
+
+
 def test_prr_step_with_host_query_and_result():
     """The fused step with its query and its result (O, m, l) in page-locked host memory, which the
     kernel reads and writes over the host link itself, gives the same scores, selections, EMA

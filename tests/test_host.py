@@ -107,6 +107,22 @@ def test_binding_refuses_cpu_tensors(lib):
                           torch.zeros(2, dtype=torch.int32))
 
 
+def test_append_kv_host_validation_without_gpu(lib):
+    """dsa_append_kv rejects bad arguments on the host, before any CUDA call."""
+    from dynamic_block_sparse_gb300 import binding as B
+    kv = B.PagedKV()
+    kv.k_pages = kv.v_pages = kv.page_table = kv.seq_lens = 4096
+    kv.batch, kv.num_q_heads, kv.num_kv_heads = 2, 8, 2
+    kv.head_dim, kv.page_size, kv.max_pages_per_seq, kv.num_phys_pages = 128, 64, 8, 16
+    call = lambda k=8192, v=8192, kind=0, lp=16, meta=16384: lib.dsa_append_kv(
+        ctypes.byref(kv), k, v, kind, lp, meta, None)
+    assert call(k=0) == -1
+    assert call(v=8200) == -2                                          # misaligned v_new
+    assert call(kind=7) == -1
+    assert call(lp=24) == -1 and b"divide" in lib.dsa_last_error()     # 24 does not divide 64
+    assert call(meta=16392) == -2                                      # misaligned meta
+
+
 def test_calibrate_ema_host_validation_without_gpu(lib):
     """dsa_calibrate_ema rejects bad arguments on the host, before any CUDA call."""
     p = 4096
