@@ -76,6 +76,8 @@ _SIGNATURES = {
                           c_size_t, _P], _I),
     "dsa_repair_merge_workspace_size": ([_P, _I], c_size_t),
     "dsa_streaming_head_attn": ([_P, _P, _I, _I, c_float, _P, _P, _P, _P], _I),
+    "dsa_hybrid_decode_attn": ([_P, _P, _P, _I, _P, _I, _I, c_float, _P, _P, _P, _P, c_size_t,
+                                _P], _I),
     "dsa_ema_predict_update": ([_P, _I, _I, _I, _P, _P, _I, c_float, c_float, c_float, _P, _I,
                                 _P, _I, _P, _P], _I),
     "dsa_merge_partials": ([_P, _I, _I, _I, _I, _P, _P, _P, _P], _I),
@@ -253,6 +255,16 @@ def dsa_repair_merge(kv: PagedKV, q, spec_idx, spec_count, page_partials, true_i
         _ptr(page_partials), _ptr(true_idx), true_idx.shape[-1], _ptr(true_count),
         1 if superset else 0, scale, _ptr(out), _ptr(m), _ptr(l), _ptr(workspace), ws_bytes,
         _stream(stream)))
+
+
+def dsa_hybrid_decode_attn(kv: PagedKV, q, idx, count, sink: int, local: int, scale: float,
+                           out, m, l, workspace, stream=None):
+    """Dense heads over their selected pages and streaming heads over sink + local tokens, one
+    launch."""
+    ws_bytes = workspace.numel() * workspace.element_size()
+    _check("dsa_hybrid_decode_attn", load().dsa_hybrid_decode_attn(
+        ctypes.byref(kv), _ptr(q), _ptr(idx), idx.shape[-1], _ptr(count), sink, local, scale,
+        _ptr(out), _ptr(m), _ptr(l), _ptr(workspace), ws_bytes, _stream(stream)))
 
 
 def dsa_streaming_head_attn(kv: PagedKV, q, sink: int, local: int, scale: float, out, m, l,

@@ -347,6 +347,60 @@ size_t dsa_sparse_decode_attn_workspace_size(const dsa_paged_kv* kv, int32_t idx
   return classic > streamed ? classic : streamed;
 }
 
+int dsa_hybrid_decode_attn(const dsa_paged_kv* kv, const void* q, const int32_t* idx,
+                           int32_t idx_stride, const int32_t* count, int32_t sink_tokens,
+                           int32_t local_tokens, float scale, float* out, float* m, float* l,
+                           void* workspace, size_t workspace_bytes, dsa_stream_t stream) {
+  KvView v;
+  int rc = check_kv(kv, 2, &v);
+  if (rc) return rc;
+  if (!q || !idx || !count || !out || !m || !l)
+    return fail(DSA_ERR_INVALID_ARG, "q/idx/count/out/m/l is NULL");
+  if (idx_stride < 1) return fail(DSA_ERR_INVALID_ARG, "idx_stride < 1");
+  if (sink_tokens < 0 || local_tokens < 0)
+    return fail(DSA_ERR_INVALID_ARG, "negative sink/local tokens");
+  if (!aligned(q, 16) || !aligned(out, 16))
+    return fail(DSA_ERR_ALIGNMENT, "q and out must be 16-byte aligned");
+  if (v.Hkv > 1024) return fail(DSA_ERR_UNSUPPORTED, "more than 1024 KV heads");
+  // pages a streaming row may touch: those of its sink tokens and of its local window
+  const long long sslots = (static_cast<long long>(sink_tokens) + v.p - 1) / v.p +
+                           (static_cast<long long>(local_tokens) + v.p - 1) / v.p + 1;
+  if (sslots > 65536) return fail(DSA_ERR_UNSUPPORTED, "sink/local window too long");
+  const int grid = stream_attn_grid();
+  const int rows = v.B * v.Hkv;
+  const size_t rec = stream_records_bytes(grid, v.G);
+  const size_t need = stream_workspace_bytes(rows, grid, v.G);
+  if (!workspace || workspace_bytes < need)
+    return fail(DSA_ERR_WORKSPACE, "workspace of %zu bytes needed", need);
+  if (!aligned(workspace, 16)) return fail(DSA_ERR_ALIGNMENT, "workspace must be 16-byte aligned");
+  CUtensorMap tk, tv;
+  if ((rc = pool_map(kv->k_pages, kv, &tk)) || (rc = pool_map(kv->v_pages, kv, &tv))) return rc;
+  cudaStream_t s = static_cast<cudaStream_t>(stream);
+  int stages = 131072 / (512 * v.p);
+  if (stages < 1) stages = 1;
+  if (stages > kStreamMaxStages) stages = kStreamMaxStages;
+  StreamAttnArgs sa = {};
+  sa.kv = v;
+  sa.q = static_cast<const __nv_bfloat16*>(q);
+  sa.scale_log2 = scale_log2(scale);
+  sa.idx = idx;
+  sa.idx_stride = idx_stride;
+  sa.count = count;
+  sa.stages = stages;
+  sa.part = static_cast<float*>(workspace);
+  sa.counters = reinterpret_cast<int32_t*>(static_cast<char*>(workspace) + rec);
+  sa.out = out;
+  sa.m = m;
+  sa.l = l;
+  sa.sink = sink_tokens;
+  sa.local = local_tokens;
+  sa.stream_stride = v.streaming != nullptr ? static_cast<int>(sslots) : 0;
+  cudaError_t e = cudaMemsetAsync(sa.counters, 0, static_cast<size_t>(rows) * sizeof(int32_t), s);
+  if (e != cudaSuccess) return cuda_fail(e, "dsa_hybrid_decode_attn counter reset");
+  e = launch_stream_attn(tk, tv, sa, grid, s);
+  return e == cudaSuccess ? ok() : cuda_fail(e, "dsa_hybrid_decode_attn launch");
+}
+
 int dsa_sparse_decode_attn(const dsa_paged_kv* kv, const void* q, const int32_t* idx,
                            int32_t idx_stride, const int32_t* count, float scale, float* out,
                            float* m, float* l, float* page_partials, int32_t num_splits,

@@ -111,6 +111,9 @@ struct StreamAttnArgs {
   float* out;
   float* m;
   float* l;
+  // streaming heads in the same launch: their sink + local tokens as extra units of
+  // stream_stride slots each (0: streaming heads are skipped)
+  int sink, local, stream_stride;
 };
 constexpr int kStreamMaxStages = 16;
 constexpr int kStreamMaxGrid = 512;  // bounds the row merge's [G][parts] weights in shared memory

@@ -41,7 +41,7 @@ __host__ __device__ inline SLayout slayout(int page, int stages, int G) {
   L.q_off = L.merge_off + static_cast<uint32_t>(kSW * G * (kHeadDim + 2) * 4 + 127) / 128 * 128;
   L.bar_off = L.q_off + 2u * 16u * kHeadDim * 2u;
   L.misc_off = L.bar_off + 16u * static_cast<uint32_t>(stages) + 32u;
-  L.total = L.misc_off + 256u + 4u * kSMaxHeads + 1024u;
+  L.total = L.misc_off + 256u + 8u * kSMaxHeads + 1024u;
   return L;
 }
 
@@ -70,6 +70,9 @@ DSA_DEV int ticket_add(int32_t* p) {
   return old;
 }
 
+// STREAMING: the launch also serves the streaming heads (a second region of the slot space);
+// without it every streaming-specific path compiles away.
+template <bool STREAMING>
 __global__ void __launch_bounds__(kSThreads, 1)
     stream_attn_kernel(const __grid_constant__ CUtensorMap tmK,
                        const __grid_constant__ CUtensorMap tmV, const StreamAttnArgs a) {
@@ -94,10 +97,13 @@ __global__ void __launch_bounds__(kSThreads, 1)
   volatile int* issued = misc + 3;          // [3] ring positions the producer has issued
   volatile int* producer_done = misc + 4;   // [4]
   int* n_dense_heads = misc + 5;            // [5]
+  int* n_stream_heads = misc + 6;           // [6]
   int* desc = misc + 8;                     // [8, 16): mailbox [2][row, beg, end, len]
   volatile int* stage_ok = misc + 16;       // [16, 32): did the producer load this stage
   volatile int* stage_pos = misc + 32;      // [32, 48): page position held by this stage
+  int* desc_kind = misc + 48;               // [48, 50): mailbox [2]: 1 for a streaming unit
   int* dense_heads = misc + 64;             // [64, 64 + Hkv)
+  int* stream_heads = misc + 64 + kSMaxHeads;  // [.., + Hkv) when streaming units are on
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
   const uint32_t stage_bytes = 512u * page;
   const uint32_t smem_base = smem_u32(smem);
@@ -117,16 +123,24 @@ __global__ void __launch_bounds__(kSThreads, 1)
       misc[3] = 0;
       misc[4] = 0;
     }
-    // dense (non-streaming) KV heads in ascending order, 32 heads per ballot
-    int nd = 0;
+    // dense (non-streaming) KV heads in ascending order, 32 heads per ballot; the streaming
+    // ones too when this launch serves them
+    int nd = 0, ns = 0;
     for (int h0 = 0; h0 < kv.Hkv; h0 += 32) {
       const int hh = h0 + lane;
       const bool dense = hh < kv.Hkv && (kv.streaming == nullptr || kv.streaming[hh] == 0);
+      const bool strm = STREAMING && hh < kv.Hkv && !dense;
       const unsigned bal = __ballot_sync(0xffffffffu, dense);
+      const unsigned bas = __ballot_sync(0xffffffffu, strm);
       if (dense) dense_heads[nd + __popc(bal & ((1u << lane) - 1u))] = hh;
+      if (strm) stream_heads[ns + __popc(bas & ((1u << lane) - 1u))] = hh;
       nd += __popc(bal);
+      ns += __popc(bas);
     }
-    if (lane == 0) *n_dense_heads = nd;
+    if (lane == 0) {
+      *n_dense_heads = nd;
+      *n_stream_heads = ns;
+    }
   } else if (warp < kSW) {
     // query rows G..15 of both mailbox tiles stay zero (the bulk copies write rows < G only)
     for (int e = tid - 32; e < 2 * 16 * 16; e += kSConsumers - 32) {
@@ -136,15 +150,46 @@ __global__ void __launch_bounds__(kSThreads, 1)
   }
   __syncthreads();
   const int nd_heads = *n_dense_heads;
-  const int stride = a.idx_stride;
-  const long long T = static_cast<long long>(kv.B) * nd_heads * stride;
+  const int ns_heads = STREAMING ? *n_stream_heads : 0;
+  // The slot space: every dense row's idx_stride selection slots, then (when streaming heads are
+  // served) every streaming row's stream_stride slots, one per page of its sink and local tokens.
+  // A unit is one row's slots; units are numbered dense rows first.
+  const int stride = a.idx_stride, sstride = a.stream_stride;
+  const int Nd = kv.B * nd_heads;
+  const long long Td = static_cast<long long>(Nd) * stride;
+  const long long T = Td + static_cast<long long>(kv.B) * ns_heads * sstride;
+  auto unit_of = [&](long long x) -> int {  // the unit holding slot x
+    if (!STREAMING || x < Td) return static_cast<int>(x / stride);
+    return Nd + static_cast<int>((x - Td) / sstride);
+  };
+  auto unit_start = [&](int di) -> long long {  // its first slot
+    if (!STREAMING || di < Nd) return static_cast<long long>(di) * stride;
+    return Td + static_cast<long long>(di - Nd) * sstride;
+  };
+  auto unit_stride = [&](int di) { return !STREAMING || di < Nd ? stride : sstride; };
+  auto unit_row = [&](int di) -> int {  // its (request, KV head) row
+    if (!STREAMING || di < Nd) return (di / nd_heads) * kv.Hkv + dense_heads[di % nd_heads];
+    const int e = di - Nd;
+    return (e / ns_heads) * kv.Hkv + stream_heads[e % ns_heads];
+  };
+  // a streaming row of length L attends the pages of its sink tokens [0, min(sink, L)), then
+  // those of its local tokens [max(0, L - local), L): sink_n pages from position 0, the rest
+  // from position first2 (the two runs merge when they touch)
+  auto stream_geom = [&](int L, int* sink_n, int* first2) -> int {
+    const int npos = (L + page - 1) / page;
+    const int sn = (min(a.sink, L) + page - 1) / page;
+    const int f2 = max(max(0, L - a.local) / page, sn);
+    *sink_n = sn;
+    *first2 = f2;
+    return sn + max(0, npos - f2);
+  };
   // active CTAs: at most one per slot, so that every active CTA holds at least one slot
   const long long n_act = T < static_cast<long long>(gridDim.x) ? T : gridDim.x;
   if (static_cast<long long>(blockIdx.x) >= n_act) return;
   const long long my_beg = slot_start(blockIdx.x, T, n_act);
   const long long my_end = slot_start(blockIdx.x + 1, T, n_act);
-  const int d_first = static_cast<int>(my_beg / stride);
-  const int n_units = static_cast<int>((my_end - 1) / stride) - d_first + 1;
+  const int d_first = unit_of(my_beg);
+  const int n_units = unit_of(my_end - 1) - d_first + 1;
 
   if (warp == kSW) {
     // ---- producer.  Unit u of this CTA is dense row d_first + u; lane l holds the descriptor of
@@ -160,32 +205,43 @@ __global__ void __launch_bounds__(kSThreads, 1)
     bool stopped = false;
     // Selections of the first unit's first two chunks, loaded before its count is known (any slot
     // below idx_stride is a valid address): they are used if the count leaves them selected.
-    const int spec_base = static_cast<int>(my_beg - static_cast<long long>(d_first) * stride);
+    const long long us0 = unit_start(d_first);
+    const int spec_base = static_cast<int>(my_beg - us0);
     int spec_a = -1, spec_b = -1;
     {
-      const int row0 = (d_first / nd_heads) * kv.Hkv + dense_heads[d_first % nd_heads];
-      const int cap_end = static_cast<int>(
-          (my_end < static_cast<long long>(d_first + 1) * stride ? my_end
-                                                                 : static_cast<long long>(d_first + 1) * stride) -
-          static_cast<long long>(d_first) * stride);
-      const int32_t* sel0 = a.idx + static_cast<size_t>(row0) * stride;
-      if (spec_base + lane < cap_end) spec_a = sel0[spec_base + lane];
-      if (spec_base + 32 + lane < cap_end) spec_b = sel0[spec_base + 32 + lane];
+      const int row0 = unit_row(d_first);
+      const long long ue0 = us0 + unit_stride(d_first);
+      const int cap_end = static_cast<int>((my_end < ue0 ? my_end : ue0) - us0);
+      if (!STREAMING || d_first < Nd) {
+        const int32_t* sel0 = a.idx + static_cast<size_t>(row0) * stride;
+        if (spec_base + lane < cap_end) spec_a = sel0[spec_base + lane];
+        if (spec_base + 32 + lane < cap_end) spec_b = sel0[spec_base + 32 + lane];
+      } else {  // a streaming unit's positions follow from its length
+        int sn, f2;
+        stream_geom(request_len(kv, row0 / kv.Hkv), &sn, &f2);
+        const int j0 = spec_base + lane, j1 = spec_base + 32 + lane;
+        if (j0 < cap_end) spec_a = j0 < sn ? j0 : f2 + (j0 - sn);
+        if (j1 < cap_end) spec_b = j1 < sn ? j1 : f2 + (j1 - sn);
+      }
     }
     for (int ub = 0; ub < n_units && !stopped; ub += 32) {
-      int t_row = 0, t_beg = 0, t_end = 0, t_len = 0;
+      int t_row = 0, t_beg = 0, t_end = 0, t_len = 0, t_kind = 0;
       {
         const int u = ub + lane;
         if (u < n_units) {
           const int di = d_first + u;
-          t_row = (di / nd_heads) * kv.Hkv + dense_heads[di % nd_heads];
-          const long long r0 = static_cast<long long>(di) * stride;
+          t_row = unit_row(di);
+          const long long r0 = unit_start(di);
+          const int us = unit_stride(di);
           const int pb = static_cast<int>((my_beg > r0 ? my_beg : r0) - r0);
-          const int pe = static_cast<int>((my_end < r0 + stride ? my_end : r0 + stride) - r0);
-          const int cnt = min(max(a.count[t_row], 0), stride);
+          const int pe = static_cast<int>((my_end < r0 + us ? my_end : r0 + us) - r0);
+          t_len = request_len(kv, t_row / kv.Hkv);
+          t_kind = STREAMING && di >= Nd;
+          int sn, f2;
+          const int cnt = t_kind ? min(stream_geom(t_len, &sn, &f2), us)
+                                 : min(max(a.count[t_row], 0), stride);
           t_beg = min(pb, cnt);
           t_end = min(pe, cnt);
-          t_len = request_len(kv, t_row / kv.Hkv);
         }
       }
       const int ue = min(n_units, ub + 32);
@@ -202,11 +258,13 @@ __global__ void __launch_bounds__(kSThreads, 1)
         const int end = __shfl_sync(0xffffffffu, t_end, u - ub);
         const int len = __shfl_sync(0xffffffffu, t_len, u - ub);
         if (__shfl_sync(0xffffffffu, stop, 0)) return false;
+        const int kind = STREAMING ? __shfl_sync(0xffffffffu, t_kind, u - ub) : 0;
         if (lane == 0) {
           desc[slot * 4 + 0] = row;
           desc[slot * 4 + 1] = beg;
           desc[slot * 4 + 2] = end;
           desc[slot * 4 + 3] = len;
+          desc_kind[slot] = kind;
           const uint32_t full = smem_u32(&qbars[slot]);
           const int b = row / kv.Hkv, h = row % kv.Hkv;
           mbar_arrive_expect_tx(full, static_cast<uint32_t>(G) * kHeadDim * 2);
@@ -233,7 +291,18 @@ __global__ void __launch_bounds__(kSThreads, 1)
         const int row = __shfl_sync(0xffffffffu, t_row, u - ub);
         const int e = __shfl_sync(0xffffffffu, t_end, u - ub);
         const int j = base + lane;
-        return j < e ? a.idx[static_cast<size_t>(row) * stride + j] : -1;
+        if (STREAMING) {  // every lane takes the shuffles, before any lane returns
+          const int kind = __shfl_sync(0xffffffffu, t_kind, u - ub);
+          const int len = __shfl_sync(0xffffffffu, t_len, u - ub);
+          if (kind) {
+            if (j >= e) return -1;
+            int sn, f2;
+            stream_geom(len, &sn, &f2);
+            return j < sn ? j : f2 + (j - sn);
+          }
+        }
+        if (j >= e) return -1;
+        return a.idx[static_cast<size_t>(row) * stride + j];
       };
       // raw page-table entry of a position inside the request, -1 outside
       auto load_phys = [&](int u, int pos) -> int {
@@ -336,6 +405,9 @@ __global__ void __launch_bounds__(kSThreads, 1)
     const int beg = desc[slot * 4 + 1];
     const int end = got ? desc[slot * 4 + 2] : beg;
     const int L = desc[slot * 4 + 3];
+    const bool strm = STREAMING && desc_kind[slot] != 0;
+    // a streaming unit attends only tokens [0, sink) and [L - local, L) of its pages
+    const int lo_end = strm ? min(a.sink, L) : L, hi_beg = strm ? max(0, L - a.local) : 0;
     const int b = row / kv.Hkv, h = row % kv.Hkv;
     const int di = d_first + u;
     uint32_t qa[8][4];
@@ -359,7 +431,8 @@ __global__ void __launch_bounds__(kSThreads, 1)
       for (int t = ((warp - s * tiles) % kSW + kSW) % kSW; t < tiles; t += kSW) {
         ++arrivals;
         if (!loaded) continue;
-        const bool in = pos * page + t * 16 + (lane & 15) < L;
+        const int tok = pos * page + t * 16 + (lane & 15);
+        const bool in = tok < L && (tok < lo_end || tok >= hi_beg);
         const uint32_t vm = __ballot_sync(0xffffffffu, in) & 0xffffu;
         if (vm == 0u) continue;
         if (vm != 0xffffu)
@@ -401,8 +474,8 @@ __global__ void __launch_bounds__(kSThreads, 1)
       }
     }
     named_barrier(1, kSConsumers);
-    const long long rs = static_cast<long long>(di) * stride;
-    const bool cut = slot_owner(rs, T, n_act) != slot_owner(rs + stride - 1, T, n_act);
+    const long long rs = unit_start(di);
+    const bool cut = slot_owner(rs, T, n_act) != slot_owner(rs + unit_stride(di) - 1, T, n_act);
     any_cut |= cut;
     float* rec0 =
         a.part + (static_cast<size_t>(blockIdx.x) * 2 + (u == 0 ? 0 : 1)) * G * kRecordFloats;
@@ -451,12 +524,12 @@ __global__ void __launch_bounds__(kSThreads, 1)
     const int n_cut = n_units > 1 ? 2 : 1;
     if (warp == 0 && lane < n_cut) {
       const int di = d_first + (lane == 0 ? 0 : n_units - 1);
-      const long long rs = static_cast<long long>(di) * stride;
+      const long long rs = unit_start(di);
       const int c_first = slot_owner(rs, T, n_act);
-      const int c_last = slot_owner(rs + stride - 1, T, n_act);
+      const int c_last = slot_owner(rs + unit_stride(di) - 1, T, n_act);
       int last = 0;
       if (c_first != c_last) {
-        const int row = (di / nd_heads) * kv.Hkv + dense_heads[di % nd_heads];
+        const int row = unit_row(di);
         last = ticket_add(a.counters + row) == c_last - c_first;
       }
       last_flag[lane] = last;
@@ -467,10 +540,10 @@ __global__ void __launch_bounds__(kSThreads, 1)
       const int k = job / G, g = job - k * G;
       if (!last_flag[k]) continue;
       const int di = d_first + (k == 0 ? 0 : n_units - 1);
-      const int row = (di / nd_heads) * kv.Hkv + dense_heads[di % nd_heads];
-      const long long rs = static_cast<long long>(di) * stride;
+      const int row = unit_row(di);
+      const long long rs = unit_start(di);
       const int c_first = slot_owner(rs, T, n_act);
-      const int C = slot_owner(rs + stride - 1, T, n_act) - c_first + 1;
+      const int C = slot_owner(rs + unit_stride(di) - 1, T, n_act) - c_first + 1;
       float M = -INFINITY, Ls = 0.f;
       float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
       for (int c0 = 0; c0 < C; c0 += 8) {
@@ -483,7 +556,7 @@ __global__ void __launch_bounds__(kSThreads, 1)
           v[j] = make_float4(0.f, 0.f, 0.f, 0.f);
           const int c = c_first + c0 + j;
           if (c0 + j < C) {
-            const int slot = static_cast<int>(slot_start(c, T, n_act) / stride) == di ? 0 : 1;
+            const int slot = unit_of(slot_start(c, T, n_act)) == di ? 0 : 1;
             const float* r = a.part + ((static_cast<size_t>(c) * 2 + slot) * G + g) * kRecordFloats;
             v[j] = __ldcg(reinterpret_cast<const float4*>(r) + lane);
             mv[j] = __ldcg(r + 128);
@@ -553,9 +626,17 @@ int stream_attn_grid() {
 cudaError_t launch_stream_attn(const CUtensorMap& tmK, const CUtensorMap& tmV,
                                const StreamAttnArgs& a, int grid, cudaStream_t s) {
   const size_t bytes = slayout(a.kv.p, a.stages, a.kv.G).total;
-  cudaError_t e = ensure_dynamic_smem(reinterpret_cast<const void*>(stream_attn_kernel), bytes);
-  if (e != cudaSuccess) return e;
-  stream_attn_kernel<<<grid, kSThreads, bytes, s>>>(tmK, tmV, a);
+  if (a.stream_stride > 0) {
+    cudaError_t e =
+        ensure_dynamic_smem(reinterpret_cast<const void*>(stream_attn_kernel<true>), bytes);
+    if (e != cudaSuccess) return e;
+    stream_attn_kernel<true><<<grid, kSThreads, bytes, s>>>(tmK, tmV, a);
+  } else {
+    cudaError_t e =
+        ensure_dynamic_smem(reinterpret_cast<const void*>(stream_attn_kernel<false>), bytes);
+    if (e != cudaSuccess) return e;
+    stream_attn_kernel<false><<<grid, kSThreads, bytes, s>>>(tmK, tmV, a);
+  }
   return cudaGetLastError();
 }
 

@@ -130,9 +130,13 @@ class TopKDecoder:
 
 class HierDecoder:
     def __init__(self, cache: Cache, k_phys: int, logical_page: int, sink: int, local: int,
-                 reuse: int = 4, scale: float | None = None):
+                 reuse: int = 4, scale: float | None = None, one_launch: bool = True):
+        """``one_launch``: dense and streaming heads attend in one launch
+        (``dsa_hybrid_decode_attn``); otherwise as two (``dsa_sparse_decode_attn`` then
+        ``dsa_streaming_head_attn``)."""
         c = cache
         self.cache, self.k, self.lp = c, k_phys, logical_page
+        self.one_launch = one_launch
         self.g = c.page_size // logical_page
         self.sink, self.local, self.reuse = sink, local, reuse
         self.scale = scale if scale is not None else 1.0 / math.sqrt(c.head_dim)
@@ -165,12 +169,20 @@ class HierDecoder:
         c = self.cache
         if t % self.reuse == 0:
             self.select(q, stream)
+        self.attend(q, stream)
+        return self.out, self.m, self.l
+
+    def attend(self, q, stream=None):
+        c = self.cache
+        if c.head_is_streaming is not None and self.one_launch:
+            B.dsa_hybrid_decode_attn(c.kv, q, self.idx, self.count, self.sink, self.local,
+                                     self.scale, self.out, self.m, self.l, self.workspace, stream)
+            return
         B.dsa_sparse_decode_attn(c.kv, q, self.idx, self.count, self.scale, self.out, self.m,
                                  self.l, workspace=self.workspace, stream=stream)
         if c.head_is_streaming is not None:
             B.dsa_streaming_head_attn(c.kv, q, self.sink, self.local, self.scale, self.out,
                                       self.m, self.l, stream)
-        return self.out, self.m, self.l
 
 
 class ThresholdDecoder:

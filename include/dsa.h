@@ -262,6 +262,22 @@ int dsa_streaming_head_attn(const dsa_paged_kv* kv, const void* q, int32_t sink_
                             dsa_stream_t stream);
 
 /*
+ * Dense and streaming heads in one launch ([LServe] §3.2-§4.1: one sparse-attention pass serves
+ * both head kinds): the dense KV heads attend their selected pages exactly as the persistent path
+ * of dsa_sparse_decode_attn does, and the KV heads marked in kv->head_is_streaming attend tokens
+ * [0, min(sink_tokens, L_b)) ∪ [max(0, L_b - local_tokens), L_b) as dsa_streaming_head_attn does
+ * -- the streaming rows' pages join the same stream-K cut of work over one CTA per SM.
+ * With kv->head_is_streaming NULL it equals dsa_sparse_decode_attn (persistent path).
+ *   idx/count/idx_stride : the dense rows' selections (streaming rows' entries are not read).
+ *   out/m/l (out)        : every query head, 16-byte aligned out.
+ *   workspace            : dsa_sparse_decode_attn_workspace_size(kv, idx_stride, 0) bytes.
+ */
+int dsa_hybrid_decode_attn(const dsa_paged_kv* kv, const void* q, const int32_t* idx,
+                           int32_t idx_stride, const int32_t* count, int32_t sink_tokens,
+                           int32_t local_tokens, float scale, float* out, float* m, float* l,
+                           void* workspace, size_t workspace_bytes, dsa_stream_t stream);
+
+/*
  * PRR EMA predictor ([PRR] §3.1) fused with the speculative-set selection ([PRR] §3.4 with a fixed
  * budget |P| = k_pred).
  *   IS           : fp32 [rows][stride], the true scores of this step (entries 0..n-1; -inf =

@@ -434,6 +434,73 @@ def test_streaming_head_attn(L, sink, local, page):
             assert_outputs(oc[b, sl], mc[b, sl], lc[b, sl], ref, f"stream b{b} h{h}")
 
 
+@pytest.mark.parametrize("L,sink,local,page", [(16 * 50 + 7, 64, 256, 16), (64 * 30 + 9, 64, 256, 64),
+                                               (300, 64, 256, 64), (100, 64, 256, 16),
+                                               (64 * 20, 0, 200, 64), (64 * 20 + 3, 40, 0, 64)])
+def test_hybrid_decode_attn(L, sink, local, page):
+    """Dense and streaming heads in one launch: the dense heads attend exactly their selected pages
+    and the streaming heads exactly tokens [0, sink) ∪ [L - local, L) (oracle), including windows
+    that overlap on short requests, an empty sink and an empty local window."""
+    w, inp, cache = small(Hq=16, Hkv=4, page=page, L=L, streaming=(1, 3), seed=L + sink)
+    scale = 1 / math.sqrt(128)
+    q = inp["q"][0]
+    G = w.group
+    k = 7
+    rows = w.batch * 4
+    gsel = np.random.default_rng(L)
+    idx = np.full((rows, 9), -1, np.int32)
+    cnt = np.zeros(rows, np.int32)
+    for r in range(rows):
+        b, h = divmod(r, 4)
+        npos = -(-int(inp["seq_lens"][b]) // page)
+        sel = np.sort(gsel.choice(npos, min(k, npos), replace=False))
+        idx[r, :len(sel)] = sel
+        cnt[r] = len(sel)
+    idx_t = torch.tensor(idx, device="cuda").view(w.batch, 4, 9)
+    cnt_t = torch.tensor(cnt, device="cuda").view(w.batch, 4)
+    out, m, l = cache.outputs()
+    ws = torch.empty(max(16, B.dsa_sparse_decode_attn_workspace_size(cache.kv, 9)),
+                     dtype=torch.uint8, device="cuda")
+    B.dsa_hybrid_decode_attn(cache.kv, q, idx_t, cnt_t, sink, local, scale, out, m, l, ws)
+    torch.cuda.synchronize()
+    oc, mc, lc = out.cpu().numpy(), m.cpu().numpy(), l.cpu().numpy()
+    for b in range(w.batch):
+        for h in range(4):
+            sl = slice(h * G, (h + 1) * G)
+            K, V, Lb = keys_values(inp, cache, b, h)
+            if h in (1, 3):
+                tok = O.streaming_token_ids(Lb, sink, local)
+            else:
+                r = b * 4 + h
+                tok = O.page_token_ids(idx[r, :cnt[r]], page, Lb)
+            ref = O.attend(q[b, sl], K, V, tok, scale)
+            assert_outputs(oc[b, sl], mc[b, sl], lc[b, sl], ref, f"hybrid b{b} h{h}")
+    assert int(cache.status.item()) == 0
+
+
+def test_hybrid_matches_two_launches_on_lserve_shape():
+    """The LServe workload at oracle scale: one launch equals the dense launch plus the streaming
+    launch to fp32 rounding, step after step of the reuse schedule."""
+    from dynamic_block_sparse_gb300.pipeline import HierDecoder
+    from dynamic_block_sparse_gb300.workloads import BY_NAME, oracle_scale
+    w = oracle_scale(BY_NAME["lserve_hier"])
+    inp = to_cuda(make_inputs(w, "cpu"))
+    outs = []
+    for one in (True, False):
+        cache = Cache(inp["k_pages"], inp["v_pages"], inp["page_table"], inp["seq_lens"],
+                      w.num_q_heads, inp["head_is_streaming"])
+        dec = HierDecoder(cache, w.k, w.logical_page, w.sink, w.local, w.reuse, one_launch=one)
+        dec.build_meta()
+        res = []
+        for t in range(w.steps):
+            o, m, l = dec.step(inp["q"][t], t)
+            res.append([x.double().cpu().numpy() for x in (o, m, l)])
+        torch.cuda.synchronize()
+        outs.append(res)
+    for t in range(w.steps):
+        assert_outputs(*outs[0][t], outs[1][t], f"step {t}")
+
+
 @pytest.mark.parametrize("case", ["random", "disjoint", "p_superset", "equal", "empty_p"])
 @pytest.mark.parametrize("superset", [False, True])
 def test_repair_merge(case, superset):
