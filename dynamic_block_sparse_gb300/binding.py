@@ -78,6 +78,10 @@ _SIGNATURES = {
     "dsa_streaming_head_attn": ([_P, _P, _I, _I, c_float, _P, _P, _P, _P], _I),
     "dsa_hybrid_decode_attn": ([_P, _P, _P, _I, _P, _I, _I, c_float, _P, _P, _P, _P, c_size_t,
                                 _P], _I),
+    "dsa_quantize_kv8": ([_P, _P, _P, _P, _P, _P], _I),
+    "dsa_sparse_decode_attn_kv8": ([_P, _P, _P, _P, _P, _P, _P, _I, _P, c_float, _P, _P, _P, _P,
+                                    c_size_t, _P], _I),
+    "dsa_sparse_decode_attn_kv8_workspace_size": ([_P, _I], c_size_t),
     "dsa_ema_predict_update": ([_P, _I, _I, _I, _P, _P, _I, c_float, c_float, c_float, _P, _I,
                                 _P, _I, _P, _P], _I),
     "dsa_merge_partials": ([_P, _I, _I, _I, _I, _P, _P, _P, _P], _I),
@@ -265,6 +269,26 @@ def dsa_hybrid_decode_attn(kv: PagedKV, q, idx, count, sink: int, local: int, sc
     _check("dsa_hybrid_decode_attn", load().dsa_hybrid_decode_attn(
         ctypes.byref(kv), _ptr(q), _ptr(idx), idx.shape[-1], _ptr(count), sink, local, scale,
         _ptr(out), _ptr(m), _ptr(l), _ptr(workspace), ws_bytes, _stream(stream)))
+
+
+def dsa_quantize_kv8(kv: PagedKV, k8, k_scale, v8, v_scale, stream=None):
+    """bf16 pools -> KV8 pages: e4m3 ``[P][Hkv][p][D]`` (uint8 tensors) and fp32 row scales
+    ``[P][Hkv][p]``."""
+    _check("dsa_quantize_kv8", load().dsa_quantize_kv8(
+        ctypes.byref(kv), _ptr(k8), _ptr(k_scale), _ptr(v8), _ptr(v_scale), _stream(stream)))
+
+
+def dsa_sparse_decode_attn_kv8_workspace_size(kv: PagedKV, idx_stride: int) -> int:
+    return int(load().dsa_sparse_decode_attn_kv8_workspace_size(ctypes.byref(kv), idx_stride))
+
+
+def dsa_sparse_decode_attn_kv8(kv: PagedKV, k8, k_scale, v8, v_scale, q, idx, count,
+                               scale: float, out, m, l, workspace, stream=None):
+    ws_bytes = workspace.numel() * workspace.element_size()
+    _check("dsa_sparse_decode_attn_kv8", load().dsa_sparse_decode_attn_kv8(
+        ctypes.byref(kv), _ptr(k8), _ptr(k_scale), _ptr(v8), _ptr(v_scale), _ptr(q), _ptr(idx),
+        idx.shape[-1], _ptr(count), scale, _ptr(out), _ptr(m), _ptr(l), _ptr(workspace), ws_bytes,
+        _stream(stream)))
 
 
 def dsa_streaming_head_attn(kv: PagedKV, q, sink: int, local: int, scale: float, out, m, l,

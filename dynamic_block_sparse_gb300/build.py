@@ -20,8 +20,8 @@ INCLUDE = os.path.join(ROOT, "include")
 BUILD_DIR = os.path.join(HERE, "_build")
 LIB_PATH = os.path.join(HERE, "libdsa.so")
 
-SOURCES = ["api.cu", "attn.cu", "calib.cu", "meta_score.cu", "prr_step.cu", "select.cu",
-           "stream_attn.cu", "threshold.cu"]
+SOURCES = ["api.cu", "attn.cu", "calib.cu", "kv8.cu", "meta_score.cu", "prr_step.cu",
+           "select.cu", "stream_attn.cu", "threshold.cu"]
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
 FLAGS = ["-O3", "-lineinfo", "-std=c++17", "-Xcompiler", "-fPIC", "-Xcompiler", "-O3",
          "--expt-relaxed-constexpr", "-I" + INCLUDE, "-I" + CSRC]

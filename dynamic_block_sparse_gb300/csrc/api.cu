@@ -643,6 +643,95 @@ int dsa_ema_predict_update(const float* IS, int32_t rows, int32_t n, int32_t str
   return e == cudaSuccess ? ok() : cuda_fail(e, "dsa_ema_predict_update launch");
 }
 
+int dsa_quantize_kv8(const dsa_paged_kv* kv, void* k8, float* k_scale, void* v8, float* v_scale,
+                     dsa_stream_t stream) {
+  KvView v;
+  int rc = check_kv(kv, 2, &v);
+  if (rc) return rc;
+  if (!k8 || !k_scale || !v8 || !v_scale)
+    return fail(DSA_ERR_INVALID_ARG, "k8/k_scale/v8/v_scale is NULL");
+  if (!aligned(k8, 16) || !aligned(v8, 16))
+    return fail(DSA_ERR_ALIGNMENT, "k8 and v8 must be 16-byte aligned");
+  const long long n_rows = static_cast<long long>(v.num_phys) * v.Hkv * v.p;
+  cudaStream_t s = static_cast<cudaStream_t>(stream);
+  cudaError_t e = launch_quantize_kv8(static_cast<const __nv_bfloat16*>(kv->k_pages), n_rows,
+                                      static_cast<uint8_t*>(k8), k_scale, s);
+  if (e == cudaSuccess)
+    e = launch_quantize_kv8(static_cast<const __nv_bfloat16*>(kv->v_pages), n_rows,
+                            static_cast<uint8_t*>(v8), v_scale, s);
+  return e == cudaSuccess ? ok() : cuda_fail(e, "dsa_quantize_kv8 launch");
+}
+
+static int kv8_splits(int rows, int idx_stride) {
+  int sm = 152, dev = 0;
+  if (cudaGetDevice(&dev) == cudaSuccess)
+    cudaDeviceGetAttribute(&sm, cudaDevAttrMultiProcessorCount, dev);
+  int splits = (4 * sm + rows - 1) / (rows > 0 ? rows : 1);
+  if (splits > idx_stride) splits = idx_stride;
+  if (splits > 64) splits = 64;
+  return splits < 1 ? 1 : splits;
+}
+
+size_t dsa_sparse_decode_attn_kv8_workspace_size(const dsa_paged_kv* kv, int32_t idx_stride) {
+  if (!kv || kv->num_kv_heads <= 0 || kv->batch <= 0 || idx_stride <= 0) return 0;
+  const int rows = kv->batch * kv->num_kv_heads;
+  const int G = kv->num_q_heads / kv->num_kv_heads;
+  return static_cast<size_t>(rows) * kv8_splits(rows, idx_stride) * G * kRecordFloats * 4;
+}
+
+int dsa_sparse_decode_attn_kv8(const dsa_paged_kv* kv, const void* k8, const float* k_scale,
+                               const void* v8, const float* v_scale, const void* q,
+                               const int32_t* idx, int32_t idx_stride, const int32_t* count,
+                               float scale, float* out, float* m, float* l, void* workspace,
+                               size_t workspace_bytes, dsa_stream_t stream) {
+  KvView v;
+  int rc = check_kv(kv, 0, &v);
+  if (rc) return rc;
+  if (!k8 || !k_scale || !v8 || !v_scale || !q || !idx || !count || !out || !m || !l)
+    return fail(DSA_ERR_INVALID_ARG, "a required pointer is NULL");
+  if (idx_stride < 1) return fail(DSA_ERR_INVALID_ARG, "idx_stride < 1");
+  if (!aligned(k8, 16) || !aligned(v8, 16) || !aligned(q, 16))
+    return fail(DSA_ERR_ALIGNMENT, "k8, v8 and q must be 16-byte aligned");
+  const int rows = v.B * v.Hkv;
+  const int splits = kv8_splits(rows, idx_stride);
+  const size_t need = static_cast<size_t>(rows) * splits * v.G * kRecordFloats * 4;
+  if (!workspace || workspace_bytes < need)
+    return fail(DSA_ERR_WORKSPACE, "workspace of %zu bytes needed", need);
+  if (!aligned(workspace, 16)) return fail(DSA_ERR_ALIGNMENT, "workspace must be 16-byte aligned");
+  if (rows > 65535) return fail(DSA_ERR_UNSUPPORTED, "more than 65535 rows");
+  cudaStream_t s = static_cast<cudaStream_t>(stream);
+  Kv8AttnArgs a = {};
+  a.kv = v;
+  a.k8 = static_cast<const uint8_t*>(k8);
+  a.ks = k_scale;
+  a.v8 = static_cast<const uint8_t*>(v8);
+  a.vs = v_scale;
+  a.q = static_cast<const __nv_bfloat16*>(q);
+  a.scale_log2 = scale_log2(scale);
+  a.idx = idx;
+  a.idx_stride = idx_stride;
+  a.count = count;
+  a.splits = splits;
+  a.part = static_cast<float*>(workspace);
+  cudaError_t e = launch_kv8_attn(a, s);
+  if (e != cudaSuccess) return cuda_fail(e, "dsa_sparse_decode_attn_kv8 launch");
+  MergeArgs mg = {};
+  mg.part = a.part;
+  mg.slots = splits;
+  mg.count = nullptr;
+  mg.rows = rows;
+  mg.G = v.G;
+  mg.Hkv = v.Hkv;
+  mg.Hq = v.Hq;
+  mg.streaming = v.streaming;
+  mg.out = out;
+  mg.m = m;
+  mg.l = l;
+  mg.out_rows_are_heads = 1;
+  e = launch_merge(mg, s);
+  return e == cudaSuccess ? ok() : cuda_fail(e, "dsa_sparse_decode_attn_kv8 merge");
+}
+
 size_t dsa_calibrate_ema_workspace_size(int32_t steps, int32_t rows, int32_t n, int32_t k) {
   if (steps < 1 || rows < 1 || n < 1 || k < 1) return 16;
   return calib_workspace(steps, rows, n, k).total;

@@ -178,6 +178,25 @@ cudaError_t launch_ema(const float* IS, int rows, int n, int stride, float* ell,
                        int32_t* pred_idx, int pred_idx_stride, int32_t* pred_count,
                        cudaStream_t s);
 
+// KV8 pages (csrc/kv8.cu): e4m3 K and V with an fp32 scale per (page, KV head, token) row
+struct Kv8AttnArgs {
+  KvView kv;
+  const uint8_t* k8;   // e4m3 [P][Hkv][p][128]
+  const float* ks;     // [P][Hkv][p]
+  const uint8_t* v8;
+  const float* vs;
+  const __nv_bfloat16* q;
+  float scale_log2;
+  const int32_t* idx;
+  int idx_stride;
+  const int32_t* count;
+  int splits;
+  float* part;  // [rows][splits][G][kRecordFloats]
+};
+cudaError_t launch_kv8_attn(const Kv8AttnArgs& a, cudaStream_t s);
+cudaError_t launch_quantize_kv8(const __nv_bfloat16* src, long long n_rows, uint8_t* dst,
+                                float* scales, cudaStream_t s);
+
 // PRR §3.2 calibration of the EMA predictor over its 80-point grid (csrc/calib.cu)
 constexpr int kCalibPoints = 80;
 constexpr int kCalibMaxN = 16384;  // pages per row whose predictor state fits in shared memory

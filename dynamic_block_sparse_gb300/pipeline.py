@@ -61,6 +61,17 @@ class Cache:
         for kind, lp, meta in metas:
             B.dsa_append_kv(self.kv, k_new, v_new, kind, lp, meta, stream)
 
+    def kv8(self, stream=None):
+        """The pools as KV8 pages (e4m3 rows with one fp32 scale each): (k8, k_scale, v8,
+        v_scale)."""
+        P, H, p, D = self.k_pages.shape
+        k8 = torch.empty((P, H, p, D), dtype=torch.uint8, device=self.device)
+        v8 = torch.empty_like(k8)
+        ks = torch.empty((P, H, p), dtype=torch.float32, device=self.device)
+        vs = torch.empty_like(ks)
+        B.dsa_quantize_kv8(self.kv, k8, ks, v8, vs, stream)
+        return k8, ks, v8, vs
+
     def meta_buffer(self, kind: int, logical_page: int) -> torch.Tensor:
         g = self.page_size // logical_page
         if kind == B.DSA_META_MINMAX:
@@ -113,12 +124,27 @@ class TopKDecoder:
         """Appends one decoded token per request, keeping this decoder's metadata current."""
         self.cache.append(k_new, v_new, [(self.kind, self.lp, self.meta)], stream)
 
+    def use_kv8(self, stream=None):
+        """Attends over KV8 pages from now on (the pools are quantised once, here); selection is
+        unchanged (it reads the metadata)."""
+        c = self.cache
+        self.kv8 = c.kv8(stream)
+        ws = B.dsa_sparse_decode_attn_kv8_workspace_size(c.kv, self.idx.shape[-1])
+        self.kv8_workspace = torch.empty(max(16, ws), dtype=torch.uint8, device=c.device)
+        return self
+
     def select(self, q, stream=None):
         c = self.cache
         B.dsa_score_pages(c.kv, q, self.meta, self.kind, self.lp, self.scores, stream)
         B.dsa_select_topk(self.scores, self.stride, self.k, self.idx, self.count, stream)
 
     def attend(self, q, stream=None):
+        if getattr(self, "kv8", None) is not None:
+            k8, ks, v8, vs = self.kv8
+            B.dsa_sparse_decode_attn_kv8(self.cache.kv, k8, ks, v8, vs, q, self.idx, self.count,
+                                         self.scale, self.out, self.m, self.l,
+                                         self.kv8_workspace, stream)
+            return
         B.dsa_sparse_decode_attn(self.cache.kv, q, self.idx, self.count, self.scale, self.out,
                                  self.m, self.l, workspace=self.workspace, stream=stream)
 

@@ -27,7 +27,10 @@ Readings taken where the pages are silent or garbled (each also listed in the de
 * the EMA update uses the previous level in both equations, exactly as printed; a page without
   a level yet starts at its score with zero trend;
 * PRR's exact mode drops speculative pages outside the true set (output equals attention over the
-  true set); its superset mode keeps them (output equals attention over the union).
+  true set); its superset mode keeps them (output equals attention over the union);
+* the 8-bit page format (KV8) is the library's own (LServe §3.2.1 keeps quantised KV pages; its
+  format is not given): one fp32 scale per token row, ``max |x| / 448`` computed in fp32, and
+  e4m3 codes of ``x / scale`` (fp32 division) rounded to nearest even; a zero row keeps scale 0.
 """
 
 from __future__ import annotations
@@ -48,6 +51,7 @@ __all__ = [
     "psa_progressive",
     "ema_init", "ema_update", "ema_predict",
     "spec_repair", "hit_rate", "score_weighted_hit", "calibration_grid", "calibrate_ema",
+    "kv8_encode_rows", "kv8_decode_rows",
 ]
 
 
@@ -414,3 +418,38 @@ def calibrate_ema(IS_traj, k: int, k_pred: int):
         Hs.append(total / max(1, len(traj) - 1))
     best = int(np.argmax(Hs))
     return calibration_grid()[best], Hs
+
+
+# --------------------------------------------------------------------------------------------
+# KV8 pages: 8-bit e4m3 rows with one fp32 scale each (the library's own format)
+# --------------------------------------------------------------------------------------------
+
+E4M3_MAX = 448.0  # largest finite e4m3 value: 1.75 * 2^8
+
+
+def kv8_encode_rows(x):
+    """Rows ``x`` ``[..., D]`` (bf16 values) -> (codes uint8 ``[..., D]``, scales float32 ``[...]``).
+
+    scale = max |x| / 448 in fp32; code = e4m3(x / scale) with the fp32 division, rounded to the
+    nearest e4m3 value (ties to even), |x / scale| <= 448 by construction; a zero row keeps scale 0
+    and zero codes.  The rounding step is torch's float8_e4m3fn conversion (a library primitive;
+    the pins check it against values of the format itself)."""
+    import torch
+
+    x32 = np.asarray(x, dtype=np.float32)
+    amax = np.max(np.abs(x32), axis=-1)
+    scale = (amax / np.float32(E4M3_MAX)).astype(np.float32)
+    safe = np.where(scale > 0, scale, np.float32(1.0)).astype(np.float32)
+    y = (x32 / safe[..., None]).astype(np.float32)
+    codes = torch.from_numpy(np.ascontiguousarray(y)).to(torch.float8_e4m3fn).view(torch.uint8)
+    codes = np.where(scale[..., None] > 0, codes.numpy(), 0).astype(np.uint8)
+    return codes, scale
+
+
+def kv8_decode_rows(codes, scales) -> np.ndarray:
+    """float64 values ``e4m3_value(code) * scale`` of KV8 rows."""
+    import torch
+
+    c = torch.from_numpy(np.ascontiguousarray(np.asarray(codes, dtype=np.uint8)))
+    vals = c.view(torch.float8_e4m3fn).to(torch.float64).numpy()
+    return vals * np.asarray(scales, dtype=np.float64)[..., None]

@@ -501,6 +501,57 @@ def test_hybrid_matches_two_launches_on_lserve_shape():
         assert_outputs(*outs[0][t], outs[1][t], f"step {t}")
 
 
+def test_quantize_kv8_matches_oracle_bitwise():
+    """KV8 conversion of the whole pool: every code and every row scale equals the oracle's
+    encoding (fp32 scale and division, e4m3 rounding to nearest even)."""
+    w, inp, cache = small(page=16, L=16 * 30 + 5, seed=41)
+    cache.k_pages[3, 1, 5] = 0          # a zero row keeps scale 0
+    cache.v_pages[2, 0, :4] *= 1e3      # rows of large magnitude
+    k8, ks, v8, vs = cache.kv8()
+    torch.cuda.synchronize()
+    for pool, codes, scales in ((cache.k_pages, k8, ks), (cache.v_pages, v8, vs)):
+        ref_c, ref_s = O.kv8_encode_rows(pool.float().cpu().numpy())
+        np.testing.assert_array_equal(scales.cpu().numpy(), ref_s)
+        np.testing.assert_array_equal(codes.cpu().numpy(), ref_c)
+    assert float(ks[3, 1, 5]) == 0.0
+
+
+@pytest.mark.parametrize("page,G", [(16, 4), (64, 16), (32, 1)])
+def test_sparse_decode_attn_kv8(page, G):
+    """Attention over KV8 pages against the oracle's attention over the decoded rows of the
+    selected pages (ragged requests, a short last page); and its distance to the bf16 attention
+    stays within the 8-bit format's error."""
+    Hkv = 2
+    w, inp, cache = small(Hq=G * Hkv, Hkv=Hkv, page=page, L=page * 40 + 7, seed=42 + page)
+    from dynamic_block_sparse_gb300.pipeline import TopKDecoder
+    dec = TopKDecoder(cache, 9)
+    dec.build_meta()
+    q = inp["q"][0]
+    out16, m16, l16 = [x.clone() for x in dec.step(q)]
+    dec.use_kv8()
+    out, m, l = dec.step(q)
+    torch.cuda.synchronize()
+    k8, ks, v8, vs = [x.cpu().numpy() for x in dec.kv8]
+    Kd = O.kv8_decode_rows(k8, ks)
+    Vd = O.kv8_decode_rows(v8, vs)
+    table = cache.page_table.cpu().numpy()
+    for b in range(w.batch):
+        L = int(cache.seq_lens[b])
+        for h in range(Hkv):
+            A = dec.idx[b, h, :int(dec.count[b, h])].cpu().numpy()
+            toks = O.page_token_ids(A, page, L)
+            K = np.stack([Kd[table[b, t // page], h, t % page] for t in range(L)])
+            V = np.stack([Vd[table[b, t // page], h, t % page] for t in range(L)])
+            sl = slice(h * G, (h + 1) * G)
+            ref = O.attend(q[b, sl], K, V, toks, dec.scale)
+            assert_outputs(out[b, sl].cpu().numpy(), m[b, sl].cpu().numpy(),
+                           l[b, sl].cpu().numpy(), ref, f"kv8 b{b} h{h}")
+    # the 8-bit pages move the output by at most a few percent of its scale
+    d = (out - out16).abs().max().item()
+    assert d < 0.1 * out16.abs().max().item() + 1e-3
+    assert int(cache.status.item()) == 0
+
+
 @pytest.mark.parametrize("case", ["random", "disjoint", "p_superset", "equal", "empty_p"])
 @pytest.mark.parametrize("superset", [False, True])
 def test_repair_merge(case, superset):

@@ -455,3 +455,35 @@ def test_pins_catch_planted_mistakes(monkeypatch):
 
     s = np.array([1.0, 2.0, 2.0, 0.5])
     assert sorted(sorted(range(4), key=lambda j: (-s[j], -j))[:1]) != _brute_topk(s, 1)
+
+
+# ------------------------------------------------------------------------------------ KV8
+
+def test_kv8_codes_match_the_e4m3_format():
+    """The e4m3 rounding step against the format's own values: exponent bias 7, 3 mantissa bits,
+    448 = 0x7E the largest finite, 2^-9 the smallest subnormal, ties to even."""
+    rows = np.array([[448.0, 1.0, -2.0, 0.0, 2.0 ** -9, 1.0625, 1.1875, -0.0]], dtype=np.float32)
+    codes, scale = O.kv8_encode_rows(rows)
+    assert scale[0] == np.float32(1.0)           # max |x| = 448 maps to scale 1
+    assert codes[0].tolist() == [0x7E, 0x38, 0xC0, 0x00, 0x01, 0x38, 0x3A, 0x80]
+    dec = O.kv8_decode_rows(codes, scale)
+    assert dec[0].tolist() == [448.0, 1.0, -2.0, 0.0, 2.0 ** -9, 1.0, 1.25, -0.0]
+
+
+def test_kv8_round_trip_error_is_bounded():
+    """Decoded rows stay within half an e4m3 step of the input: relative 2^-4 for values in the
+    normal range of the row's scale, absolute 2^-10 * scale below it; a zero row decodes to zero."""
+    r = rng(3)
+    x = r.normal(size=(50, 128)).astype(np.float32) * r.uniform(0.01, 30, size=(50, 1)).astype(np.float32)
+    x[7] = 0.0
+    codes, scale = O.kv8_encode_rows(x)
+    dec = O.kv8_decode_rows(codes, scale)
+    assert scale[7] == 0 and np.all(dec[7] == 0)
+    err = np.abs(dec - x)
+    bound = np.maximum(np.abs(x) * 2.0 ** -4, scale[:, None] * 2.0 ** -10) * (1 + 1e-6)
+    assert np.all(err <= bound)
+    # the largest magnitude of every row is represented exactly (it maps to 448)
+    for i in range(50):
+        if scale[i] > 0:
+            j = int(np.argmax(np.abs(x[i])))
+            assert abs(dec[i, j] - x[i, j]) <= abs(x[i, j]) * 1e-6
