@@ -78,9 +78,10 @@ _SIGNATURES = {
     "dsa_streaming_head_attn": ([_P, _P, _I, _I, c_float, _P, _P, _P, _P], _I),
     "dsa_hybrid_decode_attn": ([_P, _P, _P, _I, _P, _I, _I, c_float, _P, _P, _P, _P, c_size_t,
                                 _P], _I),
-    "dsa_quantize_kv8": ([_P, _P, _P, _P, _P, _P], _I),
-    "dsa_sparse_decode_attn_kv8": ([_P, _P, _P, _P, _P, _P, _P, _I, _P, c_float, _P, _P, _P, _P,
-                                    c_size_t, _P], _I),
+    "dsa_quantize_kv8": ([_P, _P, _P], _I),
+    "dsa_kv8_bytes": ([_P], c_size_t),
+    "dsa_sparse_decode_attn_kv8": ([_P, _P, _P, _P, _I, _P, c_float, _P, _P, _P, _P, c_size_t,
+                                    _P], _I),
     "dsa_sparse_decode_attn_kv8_workspace_size": ([_P, _I], c_size_t),
     "dsa_ema_predict_update": ([_P, _I, _I, _I, _P, _P, _I, c_float, c_float, c_float, _P, _I,
                                 _P, _I, _P, _P], _I),
@@ -271,24 +272,38 @@ def dsa_hybrid_decode_attn(kv: PagedKV, q, idx, count, sink: int, local: int, sc
         _ptr(out), _ptr(m), _ptr(l), _ptr(workspace), ws_bytes, _stream(stream)))
 
 
-def dsa_quantize_kv8(kv: PagedKV, k8, k_scale, v8, v_scale, stream=None):
-    """bf16 pools -> KV8 pages: e4m3 ``[P][Hkv][p][D]`` (uint8 tensors) and fp32 row scales
-    ``[P][Hkv][p]``."""
-    _check("dsa_quantize_kv8", load().dsa_quantize_kv8(
-        ctypes.byref(kv), _ptr(k8), _ptr(k_scale), _ptr(v8), _ptr(v_scale), _stream(stream)))
+def dsa_kv8_bytes(kv: PagedKV) -> int:
+    return int(load().dsa_kv8_bytes(ctypes.byref(kv)))
+
+
+def dsa_quantize_kv8(kv: PagedKV, kv8, stream=None):
+    """bf16 pools -> KV8 blocks (uint8 tensor of dsa_kv8_bytes(kv) bytes): per (physical page, KV
+    head) the e4m3 K codes [p][128], V codes [p][128], K scales fp32 [p], V scales fp32 [p]."""
+    _check("dsa_quantize_kv8", load().dsa_quantize_kv8(ctypes.byref(kv), _ptr(kv8),
+                                                       _stream(stream)))
+
+
+def kv8_unpack(kv8, num_phys_pages: int, num_kv_heads: int, page: int):
+    """Views of a KV8 buffer: (K codes, V codes) uint8 ``[P][Hkv][p][128]`` and (K scales, V
+    scales) fp32 ``[P][Hkv][p]``."""
+    blk = kv8.view(num_phys_pages, num_kv_heads, 264 * page)
+    kc = blk[..., :128 * page].view(num_phys_pages, num_kv_heads, page, 128)
+    vc = blk[..., 128 * page:256 * page].view(num_phys_pages, num_kv_heads, page, 128)
+    ks = blk[..., 256 * page:260 * page].contiguous().view(torch.float32)
+    vs = blk[..., 260 * page:].contiguous().view(torch.float32)
+    return kc, vc, ks, vs
 
 
 def dsa_sparse_decode_attn_kv8_workspace_size(kv: PagedKV, idx_stride: int) -> int:
     return int(load().dsa_sparse_decode_attn_kv8_workspace_size(ctypes.byref(kv), idx_stride))
 
 
-def dsa_sparse_decode_attn_kv8(kv: PagedKV, k8, k_scale, v8, v_scale, q, idx, count,
-                               scale: float, out, m, l, workspace, stream=None):
+def dsa_sparse_decode_attn_kv8(kv: PagedKV, kv8, q, idx, count, scale: float, out, m, l,
+                               workspace, stream=None):
     ws_bytes = workspace.numel() * workspace.element_size()
     _check("dsa_sparse_decode_attn_kv8", load().dsa_sparse_decode_attn_kv8(
-        ctypes.byref(kv), _ptr(k8), _ptr(k_scale), _ptr(v8), _ptr(v_scale), _ptr(q), _ptr(idx),
-        idx.shape[-1], _ptr(count), scale, _ptr(out), _ptr(m), _ptr(l), _ptr(workspace), ws_bytes,
-        _stream(stream)))
+        ctypes.byref(kv), _ptr(kv8), _ptr(q), _ptr(idx), idx.shape[-1], _ptr(count), scale,
+        _ptr(out), _ptr(m), _ptr(l), _ptr(workspace), ws_bytes, _stream(stream)))
 
 
 def dsa_streaming_head_attn(kv: PagedKV, q, sink: int, local: int, scale: float, out, m, l,

@@ -643,93 +643,82 @@ int dsa_ema_predict_update(const float* IS, int32_t rows, int32_t n, int32_t str
   return e == cudaSuccess ? ok() : cuda_fail(e, "dsa_ema_predict_update launch");
 }
 
-int dsa_quantize_kv8(const dsa_paged_kv* kv, void* k8, float* k_scale, void* v8, float* v_scale,
-                     dsa_stream_t stream) {
+int dsa_quantize_kv8(const dsa_paged_kv* kv, void* kv8, dsa_stream_t stream) {
   KvView v;
   int rc = check_kv(kv, 2, &v);
   if (rc) return rc;
-  if (!k8 || !k_scale || !v8 || !v_scale)
-    return fail(DSA_ERR_INVALID_ARG, "k8/k_scale/v8/v_scale is NULL");
-  if (!aligned(k8, 16) || !aligned(v8, 16))
-    return fail(DSA_ERR_ALIGNMENT, "k8 and v8 must be 16-byte aligned");
+  if (!kv8) return fail(DSA_ERR_INVALID_ARG, "kv8 is NULL");
+  if (!aligned(kv8, 16)) return fail(DSA_ERR_ALIGNMENT, "kv8 must be 16-byte aligned");
   const long long n_rows = static_cast<long long>(v.num_phys) * v.Hkv * v.p;
   cudaStream_t s = static_cast<cudaStream_t>(stream);
-  cudaError_t e = launch_quantize_kv8(static_cast<const __nv_bfloat16*>(kv->k_pages), n_rows,
-                                      static_cast<uint8_t*>(k8), k_scale, s);
+  cudaError_t e = launch_quantize_kv8(static_cast<const __nv_bfloat16*>(kv->k_pages), n_rows, v.p,
+                                      0, static_cast<uint8_t*>(kv8), s);
   if (e == cudaSuccess)
-    e = launch_quantize_kv8(static_cast<const __nv_bfloat16*>(kv->v_pages), n_rows,
-                            static_cast<uint8_t*>(v8), v_scale, s);
+    e = launch_quantize_kv8(static_cast<const __nv_bfloat16*>(kv->v_pages), n_rows, v.p, 1,
+                            static_cast<uint8_t*>(kv8), s);
   return e == cudaSuccess ? ok() : cuda_fail(e, "dsa_quantize_kv8 launch");
 }
 
-static int kv8_splits(int rows, int idx_stride) {
-  int sm = 152, dev = 0;
-  if (cudaGetDevice(&dev) == cudaSuccess)
-    cudaDeviceGetAttribute(&sm, cudaDevAttrMultiProcessorCount, dev);
-  int splits = (4 * sm + rows - 1) / (rows > 0 ? rows : 1);
-  if (splits > idx_stride) splits = idx_stride;
-  if (splits > 64) splits = 64;
-  return splits < 1 ? 1 : splits;
+size_t dsa_kv8_bytes(const dsa_paged_kv* kv) {
+  if (!kv || kv->num_phys_pages <= 0 || kv->num_kv_heads <= 0 || kv->page_size <= 0) return 0;
+  return static_cast<size_t>(kv->num_phys_pages) * kv->num_kv_heads * kv->page_size * 264;
 }
 
 size_t dsa_sparse_decode_attn_kv8_workspace_size(const dsa_paged_kv* kv, int32_t idx_stride) {
   if (!kv || kv->num_kv_heads <= 0 || kv->batch <= 0 || idx_stride <= 0) return 0;
   const int rows = kv->batch * kv->num_kv_heads;
   const int G = kv->num_q_heads / kv->num_kv_heads;
-  return static_cast<size_t>(rows) * kv8_splits(rows, idx_stride) * G * kRecordFloats * 4;
+  return stream_workspace_bytes(rows, stream_attn_grid(), G);
 }
 
-int dsa_sparse_decode_attn_kv8(const dsa_paged_kv* kv, const void* k8, const float* k_scale,
-                               const void* v8, const float* v_scale, const void* q,
+int dsa_sparse_decode_attn_kv8(const dsa_paged_kv* kv, const void* kv8, const void* q,
                                const int32_t* idx, int32_t idx_stride, const int32_t* count,
                                float scale, float* out, float* m, float* l, void* workspace,
                                size_t workspace_bytes, dsa_stream_t stream) {
   KvView v;
   int rc = check_kv(kv, 0, &v);
   if (rc) return rc;
-  if (!k8 || !k_scale || !v8 || !v_scale || !q || !idx || !count || !out || !m || !l)
+  if (!kv8 || !q || !idx || !count || !out || !m || !l)
     return fail(DSA_ERR_INVALID_ARG, "a required pointer is NULL");
   if (idx_stride < 1) return fail(DSA_ERR_INVALID_ARG, "idx_stride < 1");
-  if (!aligned(k8, 16) || !aligned(v8, 16) || !aligned(q, 16))
-    return fail(DSA_ERR_ALIGNMENT, "k8, v8 and q must be 16-byte aligned");
+  if (!aligned(kv8, 16) || !aligned(q, 16) || !aligned(out, 16))
+    return fail(DSA_ERR_ALIGNMENT, "kv8, q and out must be 16-byte aligned");
+  if (v.Hkv > 1024) return fail(DSA_ERR_UNSUPPORTED, "more than 1024 KV heads");
   const int rows = v.B * v.Hkv;
-  const int splits = kv8_splits(rows, idx_stride);
-  const size_t need = static_cast<size_t>(rows) * splits * v.G * kRecordFloats * 4;
+  const int grid = stream_attn_grid();
+  const size_t rec = stream_records_bytes(grid, v.G);
+  const size_t need = stream_workspace_bytes(rows, grid, v.G);
   if (!workspace || workspace_bytes < need)
     return fail(DSA_ERR_WORKSPACE, "workspace of %zu bytes needed", need);
   if (!aligned(workspace, 16)) return fail(DSA_ERR_ALIGNMENT, "workspace must be 16-byte aligned");
-  if (rows > 65535) return fail(DSA_ERR_UNSUPPORTED, "more than 65535 rows");
+  // as many stages (of 264 B per token) as fit beside the decode tiles, up to 96 KB of them
+  const size_t smem_cap = 227 * 1024;
+  const int stride = (264 * v.p + 1023) & ~1023;
+  int stages = 98304 / stride;
+  if (stages > kStreamMaxStages) stages = kStreamMaxStages;
+  while (stages > 1 && stream_attn_smem_bytes(v.p, stages, v.G, true) > smem_cap) --stages;
+  if (stages < 1 || stream_attn_smem_bytes(v.p, stages, v.G, true) > smem_cap)
+    return fail(DSA_ERR_UNSUPPORTED, "dsa_sparse_decode_attn_kv8: shape needs too much shared memory");
   cudaStream_t s = static_cast<cudaStream_t>(stream);
-  Kv8AttnArgs a = {};
-  a.kv = v;
-  a.k8 = static_cast<const uint8_t*>(k8);
-  a.ks = k_scale;
-  a.v8 = static_cast<const uint8_t*>(v8);
-  a.vs = v_scale;
-  a.q = static_cast<const __nv_bfloat16*>(q);
-  a.scale_log2 = scale_log2(scale);
-  a.idx = idx;
-  a.idx_stride = idx_stride;
-  a.count = count;
-  a.splits = splits;
-  a.part = static_cast<float*>(workspace);
-  cudaError_t e = launch_kv8_attn(a, s);
-  if (e != cudaSuccess) return cuda_fail(e, "dsa_sparse_decode_attn_kv8 launch");
-  MergeArgs mg = {};
-  mg.part = a.part;
-  mg.slots = splits;
-  mg.count = nullptr;
-  mg.rows = rows;
-  mg.G = v.G;
-  mg.Hkv = v.Hkv;
-  mg.Hq = v.Hq;
-  mg.streaming = v.streaming;
-  mg.out = out;
-  mg.m = m;
-  mg.l = l;
-  mg.out_rows_are_heads = 1;
-  e = launch_merge(mg, s);
-  return e == cudaSuccess ? ok() : cuda_fail(e, "dsa_sparse_decode_attn_kv8 merge");
+  StreamAttnArgs sa = {};
+  sa.kv = v;
+  sa.q = static_cast<const __nv_bfloat16*>(q);
+  sa.scale_log2 = scale_log2(scale);
+  sa.idx = idx;
+  sa.idx_stride = idx_stride;
+  sa.count = count;
+  sa.stages = stages;
+  sa.part = static_cast<float*>(workspace);
+  sa.counters = reinterpret_cast<int32_t*>(static_cast<char*>(workspace) + rec);
+  sa.out = out;
+  sa.m = m;
+  sa.l = l;
+  sa.kv8 = static_cast<const uint8_t*>(kv8);
+  cudaError_t e = cudaMemsetAsync(sa.counters, 0, static_cast<size_t>(rows) * sizeof(int32_t), s);
+  if (e != cudaSuccess) return cuda_fail(e, "dsa_sparse_decode_attn_kv8 counter reset");
+  CUtensorMap none = {};  // KV8 pages move by plain bulk copies: no tensor maps
+  e = launch_stream_attn(none, none, sa, grid, s);
+  return e == cudaSuccess ? ok() : cuda_fail(e, "dsa_sparse_decode_attn_kv8 launch");
 }
 
 size_t dsa_calibrate_ema_workspace_size(int32_t steps, int32_t rows, int32_t n, int32_t k) {

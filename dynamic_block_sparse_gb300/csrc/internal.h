@@ -114,10 +114,12 @@ struct StreamAttnArgs {
   // streaming heads in the same launch: their sink + local tokens as extra units of
   // stream_stride slots each (0: streaming heads are skipped)
   int sink, local, stream_stride;
+  // KV8 pages instead of the bf16 pools (non-null): one 264 p-byte block per (page, KV head)
+  const uint8_t* kv8;
 };
 constexpr int kStreamMaxStages = 16;
 constexpr int kStreamMaxGrid = 512;  // bounds the row merge's [G][parts] weights in shared memory
-size_t stream_attn_smem_bytes(int page, int stages, int G);
+size_t stream_attn_smem_bytes(int page, int stages, int G, bool kv8 = false);
 int stream_attn_grid();  // CTAs of one launch: one per SM
 cudaError_t launch_stream_attn(const CUtensorMap& tmK, const CUtensorMap& tmV,
                                const StreamAttnArgs& a, int grid, cudaStream_t s);
@@ -179,23 +181,8 @@ cudaError_t launch_ema(const float* IS, int rows, int n, int stride, float* ell,
                        cudaStream_t s);
 
 // KV8 pages (csrc/kv8.cu): e4m3 K and V with an fp32 scale per (page, KV head, token) row
-struct Kv8AttnArgs {
-  KvView kv;
-  const uint8_t* k8;   // e4m3 [P][Hkv][p][128]
-  const float* ks;     // [P][Hkv][p]
-  const uint8_t* v8;
-  const float* vs;
-  const __nv_bfloat16* q;
-  float scale_log2;
-  const int32_t* idx;
-  int idx_stride;
-  const int32_t* count;
-  int splits;
-  float* part;  // [rows][splits][G][kRecordFloats]
-};
-cudaError_t launch_kv8_attn(const Kv8AttnArgs& a, cudaStream_t s);
-cudaError_t launch_quantize_kv8(const __nv_bfloat16* src, long long n_rows, uint8_t* dst,
-                                float* scales, cudaStream_t s);
+cudaError_t launch_quantize_kv8(const __nv_bfloat16* src, long long n_rows, int page, int v,
+                                uint8_t* kv8, cudaStream_t s);
 
 // PRR §3.2 calibration of the EMA predictor over its 80-point grid (csrc/calib.cu)
 constexpr int kCalibPoints = 80;

@@ -17,6 +17,8 @@
 // by a 1-D bulk copy) through a two-slot mailbox, so the consumers never touch global memory
 // before their epilogues.
 #include "attn_core.cuh"
+#include <cuda_fp8.h>
+
 #include "internal.h"
 
 namespace dsa {
@@ -29,20 +31,41 @@ constexpr int kSMaxHeads = 1024;           // KV heads the dense-head table can 
 constexpr int kIssueLanes = 4;             // producer lanes issuing page loads at once
 
 struct SLayout {
-  uint32_t merge_off, q_off, bar_off, misc_off, total;
+  uint32_t stage_stride, merge_off, q_off, bar_off, misc_off, conv_off, total;
 };
 
 // merge area: per warp G rows of O (fp32) and G (m, l) pairs; later the row merge's weights.
 // q: two unpadded [16][128] bf16 query tiles (mailbox slots).  bars: [S] full, [S] empty, then the
 // mailbox's [2] full and [2] empty.
-__host__ __device__ inline SLayout slayout(int page, int stages, int G) {
+// kv8: a stage holds a KV8 page (e4m3 K rows, V rows, then the two fp32 scale rows), and every
+// consumer warp has an 8 KB bf16 tile (16 tokens of K and V, swizzled as a loaded page) it decodes
+// its tiles into.
+__host__ __device__ inline SLayout slayout(int page, int stages, int G, bool kv8 = false) {
   SLayout L;
-  L.merge_off = ((512u * page * stages) + 1023u) & ~1023u;
+  L.stage_stride = kv8 ? (264u * page + 1023u) & ~1023u : 512u * page;
+  L.merge_off = ((L.stage_stride * stages) + 1023u) & ~1023u;
   L.q_off = L.merge_off + static_cast<uint32_t>(kSW * G * (kHeadDim + 2) * 4 + 127) / 128 * 128;
   L.bar_off = L.q_off + 2u * 16u * kHeadDim * 2u;
   L.misc_off = L.bar_off + 16u * static_cast<uint32_t>(stages) + 32u;
-  L.total = L.misc_off + 256u + 8u * kSMaxHeads + 1024u;
+  L.conv_off = (L.misc_off + 256u + 8u * kSMaxHeads + 1023u) & ~1023u;
+  L.total = L.conv_off + (kv8 ? static_cast<uint32_t>(kSW) * 8192u : 0u) + 1024u;
   return L;
+}
+
+// Eight e4m3 values times a scale, as eight bf16 (one 16-byte piece of a staged bf16 row).
+DSA_DEV uint4 decode8(uint2 w, float scale) {
+  uint4 o;
+  uint32_t* po = reinterpret_cast<uint32_t*>(&o);
+  const uint16_t* pw = reinterpret_cast<const uint16_t*>(&w);
+#pragma unroll
+  for (int e = 0; e < 4; ++e) {
+    const __half2_raw hr =
+        __nv_cvt_fp8x2_to_halfraw2(static_cast<__nv_fp8x2_storage_t>(pw[e]), __NV_E4M3);
+    const float2 f = __half22float2(*reinterpret_cast<const __half2*>(&hr));
+    const __nv_bfloat162 b = __floats2bfloat162_rn(f.x * scale, f.y * scale);
+    po[e] = *reinterpret_cast<const uint32_t*>(&b);
+  }
+  return o;
 }
 
 // Slot range [beg, end) of the active CTA c among n over T slots.
@@ -72,7 +95,7 @@ DSA_DEV int ticket_add(int32_t* p) {
 
 // STREAMING: the launch also serves the streaming heads (a second region of the slot space);
 // without it every streaming-specific path compiles away.
-template <bool STREAMING>
+template <bool STREAMING, bool KV8>
 __global__ void __launch_bounds__(kSThreads, 1)
     stream_attn_kernel(const __grid_constant__ CUtensorMap tmK,
                        const __grid_constant__ CUtensorMap tmV, const StreamAttnArgs a) {
@@ -84,7 +107,7 @@ __global__ void __launch_bounds__(kSThreads, 1)
   const int S = a.stages;
   const int G = kv.G;
   const int tiles = page / 16;
-  const SLayout lay = slayout(page, S, G);
+  const SLayout lay = slayout(page, S, G, KV8);
   float* sO = reinterpret_cast<float*>(smem + lay.merge_off);  // [kSW][G][128]
   float* sM = sO + kSW * G * kHeadDim;                          // [kSW][G]
   float* sL = sM + kSW * G;                                     // [kSW][G]
@@ -105,7 +128,8 @@ __global__ void __launch_bounds__(kSThreads, 1)
   int* dense_heads = misc + 64;             // [64, 64 + Hkv)
   int* stream_heads = misc + 64 + kSMaxHeads;  // [.., + Hkv) when streaming units are on
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
-  const uint32_t stage_bytes = 512u * page;
+  const uint32_t stage_bytes = lay.stage_stride;           // stage s at smem + s * stage_bytes
+  const uint32_t stage_tx = KV8 ? 264u * page : 512u * page;  // bytes a stage's loads bring
   const uint32_t smem_base = smem_u32(smem);
 
   if (warp == 0) {
@@ -196,7 +220,7 @@ __global__ void __launch_bounds__(kSThreads, 1)
     // unit ub + l of the current batch of 32.  Chunks of up to 32 selected slots of one unit are
     // software-pipelined: while chunk A's pages are issued, the page-table entries of chunk B and
     // the selections of chunk C are already in flight.
-    if (lane == 0) {
+    if (lane == 0 && !KV8) {
       prefetch_tensormap(&tmK);
       prefetch_tensormap(&tmV);
     }
@@ -369,9 +393,13 @@ __global__ void __launch_bounds__(kSThreads, 1)
             } else {
               const uint32_t dst = smem_base + s * stage_bytes;
               const int row0 = (phk * kv.Hkv + h) * page;
-              mbar_arrive_expect_tx(full, stage_bytes);
-              tma_load_page(dst, &tmK, row0, full);
-              tma_load_page(dst + 2 * page * 128, &tmV, row0, full);
+              mbar_arrive_expect_tx(full, stage_tx);
+              if (KV8) {  // the page's block (K and V codes, their scales): one bulk copy
+                bulk_load(dst, a.kv8 + static_cast<size_t>(row0) * 264, 264u * page, full);
+              } else {
+                tma_load_page(dst, &tmK, row0, full);
+                tma_load_page(dst + 2 * page * 128, &tmV, row0, full);
+              }
             }
           }
           if (lane == 0) *issued = i + min(nb, q0 + NL);
@@ -435,11 +463,38 @@ __global__ void __launch_bounds__(kSThreads, 1)
         const bool in = tok < L && (tok < lo_end || tok >= hi_beg);
         const uint32_t vm = __ballot_sync(0xffffffffu, in) & 0xffffu;
         if (vm == 0u) continue;
-        if (vm != 0xffffu)
-          wrote |= zero_invalid_v_rows(vm, smem + s * stage_bytes + 2 * page * 128, page, t * 16);
         float sc[2][4];
-        tile_scores(qa, kb, page, t * 16, sc);
-        tile_softmax_pv(st, sc, a.scale_log2, vm, vb, page, t * 16);
+        if (KV8) {
+          // decode the tile into this warp's bf16 tile (K and V rows times their scales; V rows
+          // of tokens that take no part as zeros), laid out and swizzled as a loaded page of 16
+          const uint8_t* st8 = smem + s * stage_bytes;
+          const float* ksc = reinterpret_cast<const float*>(st8 + 256 * page) + t * 16;
+          const float* vsc = ksc + page;
+          uint8_t* cb = smem + lay.conv_off + warp * 8192;
+#pragma unroll
+          for (int k = 0; k < 8; ++k) {  // 16 rows x 16 pieces of 8 dims, 8 per lane
+            const int unit = lane + 32 * k;
+            const int r = unit >> 4, c16 = unit & 15;
+            const size_t src = static_cast<size_t>(t * 16 + r) * 128 + c16 * 8;
+            const uint2 kw = *reinterpret_cast<const uint2*>(st8 + src);
+            const uint2 vw = *reinterpret_cast<const uint2*>(st8 + 128 * page + src);
+            const uint32_t off = (c16 >> 3) * 2048u + sw128(static_cast<uint32_t>(r), c16 & 7u);
+            *reinterpret_cast<uint4*>(cb + off) = decode8(kw, ksc[r]);
+            *reinterpret_cast<uint4*>(cb + 4096 + off) =
+                ((vm >> r) & 1u) ? decode8(vw, vsc[r]) : make_uint4(0u, 0u, 0u, 0u);
+          }
+          __syncwarp();
+          const uint32_t kt = smem_u32(cb);
+          tile_scores(qa, kt, 16, 0, sc);
+          tile_softmax_pv(st, sc, a.scale_log2, vm, kt + 4096, 16, 0);
+          __syncwarp();  // the tile is rewritten by the warp's next one
+        } else {
+          if (vm != 0xffffu)
+            wrote |=
+                zero_invalid_v_rows(vm, smem + s * stage_bytes + 2 * page * 128, page, t * 16);
+          tile_scores(qa, kb, page, t * 16, sc);
+          tile_softmax_pv(st, sc, a.scale_log2, vm, vb, page, t * 16);
+        }
       }
       if (wrote) fence_proxy_async_smem();
       __syncwarp();
@@ -611,8 +666,8 @@ __global__ void __launch_bounds__(kSThreads, 1)
 
 }  // namespace
 
-size_t stream_attn_smem_bytes(int page, int stages, int G) {
-  return slayout(page, stages, G).total;
+size_t stream_attn_smem_bytes(int page, int stages, int G, bool kv8) {
+  return slayout(page, stages, G, kv8).total;
 }
 
 int stream_attn_grid() {
@@ -625,19 +680,16 @@ int stream_attn_grid() {
 
 cudaError_t launch_stream_attn(const CUtensorMap& tmK, const CUtensorMap& tmV,
                                const StreamAttnArgs& a, int grid, cudaStream_t s) {
-  const size_t bytes = slayout(a.kv.p, a.stages, a.kv.G).total;
-  if (a.stream_stride > 0) {
-    cudaError_t e =
-        ensure_dynamic_smem(reinterpret_cast<const void*>(stream_attn_kernel<true>), bytes);
+  const size_t bytes = slayout(a.kv.p, a.stages, a.kv.G, a.kv8 != nullptr).total;
+  auto go = [&](auto kernel) -> cudaError_t {
+    cudaError_t e = ensure_dynamic_smem(reinterpret_cast<const void*>(kernel), bytes);
     if (e != cudaSuccess) return e;
-    stream_attn_kernel<true><<<grid, kSThreads, bytes, s>>>(tmK, tmV, a);
-  } else {
-    cudaError_t e =
-        ensure_dynamic_smem(reinterpret_cast<const void*>(stream_attn_kernel<false>), bytes);
-    if (e != cudaSuccess) return e;
-    stream_attn_kernel<false><<<grid, kSThreads, bytes, s>>>(tmK, tmV, a);
-  }
-  return cudaGetLastError();
+    kernel<<<grid, kSThreads, bytes, s>>>(tmK, tmV, a);
+    return cudaGetLastError();
+  };
+  if (a.kv8 != nullptr) return go(stream_attn_kernel<false, true>);
+  return a.stream_stride > 0 ? go(stream_attn_kernel<true, false>)
+                             : go(stream_attn_kernel<false, false>);
 }
 
 }  // namespace dsa

@@ -62,15 +62,11 @@ class Cache:
             B.dsa_append_kv(self.kv, k_new, v_new, kind, lp, meta, stream)
 
     def kv8(self, stream=None):
-        """The pools as KV8 pages (e4m3 rows with one fp32 scale each): (k8, k_scale, v8,
-        v_scale)."""
-        P, H, p, D = self.k_pages.shape
-        k8 = torch.empty((P, H, p, D), dtype=torch.uint8, device=self.device)
-        v8 = torch.empty_like(k8)
-        ks = torch.empty((P, H, p), dtype=torch.float32, device=self.device)
-        vs = torch.empty_like(ks)
-        B.dsa_quantize_kv8(self.kv, k8, ks, v8, vs, stream)
-        return k8, ks, v8, vs
+        """The pools as KV8 blocks (e4m3 rows with one fp32 scale each, one contiguous block per
+        (physical page, KV head)): a uint8 tensor; ``binding.kv8_unpack`` gives its parts."""
+        buf = torch.empty(B.dsa_kv8_bytes(self.kv), dtype=torch.uint8, device=self.device)
+        B.dsa_quantize_kv8(self.kv, buf, stream)
+        return buf
 
     def meta_buffer(self, kind: int, logical_page: int) -> torch.Tensor:
         g = self.page_size // logical_page
@@ -140,8 +136,7 @@ class TopKDecoder:
 
     def attend(self, q, stream=None):
         if getattr(self, "kv8", None) is not None:
-            k8, ks, v8, vs = self.kv8
-            B.dsa_sparse_decode_attn_kv8(self.cache.kv, k8, ks, v8, vs, q, self.idx, self.count,
+            B.dsa_sparse_decode_attn_kv8(self.cache.kv, self.kv8, q, self.idx, self.count,
                                          self.scale, self.out, self.m, self.l,
                                          self.kv8_workspace, stream)
             return

@@ -283,22 +283,24 @@ int dsa_hybrid_decode_attn(const dsa_paged_kv* kv, const void* q, const int32_t*
  * stored as 128 e4m3 values with one fp32 scale: scale = max_i |x_i| / 448 (448 = the largest
  * finite e4m3 value) and byte_i = e4m3(x_i / scale), rounded to nearest even, saturating; a row of
  * zeros gets scale 0 and zero bytes.  A value decodes as e4m3_value(byte) * scale.
- *   k8, v8 (out)          : e4m3 [num_phys_pages][Hkv][p][D], 16-byte aligned.
- *   k_scale, v_scale (out): fp32 [num_phys_pages][Hkv][p].
+ * Layout: one contiguous block of 264 p bytes per (physical page P, KV head h), at offset
+ * (P * Hkv + h) * 264 p: the K codes [p][128], the V codes [p][128], the K scales fp32 [p], the V
+ * scales fp32 [p] -- so the attention brings a selected page with one bulk copy.
+ *   kv8 (out) : dsa_kv8_bytes(kv) bytes, 16-byte aligned.
  * Every physical page is converted (the bf16 pools are read, not changed).
  */
-int dsa_quantize_kv8(const dsa_paged_kv* kv, void* k8, float* k_scale, void* v8, float* v_scale,
-                     dsa_stream_t stream);
+int dsa_quantize_kv8(const dsa_paged_kv* kv, void* kv8, dsa_stream_t stream);
+size_t dsa_kv8_bytes(const dsa_paged_kv* kv);
 
 /*
- * Sparse decode attention over KV8 pages: as dsa_sparse_decode_attn (exact attention of every
- * dense head's query group over the tokens of its selected pages, split-K and merged by
- * log-sum-exp) with K and V decoded from the KV8 pool.  kv->k_pages / v_pages are not read
+ * Sparse decode attention over KV8 pages: as the persistent path of dsa_sparse_decode_attn (exact
+ * attention of every dense head's query group over the tokens of its selected pages, one stream-K
+ * launch) with K and V decoded from the KV8 blocks: each consumer warp decodes its 16-token tiles
+ * to bf16 (value times scale) before the tensor-core products.  kv->k_pages / v_pages are not read
  * (may be NULL); the page table, lengths and shapes are.  Streaming heads are skipped.
  *   workspace : dsa_sparse_decode_attn_kv8_workspace_size(kv, idx_stride) bytes.
  */
-int dsa_sparse_decode_attn_kv8(const dsa_paged_kv* kv, const void* k8, const float* k_scale,
-                               const void* v8, const float* v_scale, const void* q,
+int dsa_sparse_decode_attn_kv8(const dsa_paged_kv* kv, const void* kv8, const void* q,
                                const int32_t* idx, int32_t idx_stride, const int32_t* count,
                                float scale, float* out, float* m, float* l, void* workspace,
                                size_t workspace_bytes, dsa_stream_t stream);

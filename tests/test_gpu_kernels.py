@@ -507,8 +507,11 @@ def test_quantize_kv8_matches_oracle_bitwise():
     w, inp, cache = small(page=16, L=16 * 30 + 5, seed=41)
     cache.k_pages[3, 1, 5] = 0          # a zero row keeps scale 0
     cache.v_pages[2, 0, :4] *= 1e3      # rows of large magnitude
-    k8, ks, v8, vs = cache.kv8()
+    buf = cache.kv8()
     torch.cuda.synchronize()
+    assert buf.numel() == cache.num_phys_pages * cache.num_kv_heads * 264 * cache.page_size
+    k8, v8, ks, vs = B.kv8_unpack(buf, cache.num_phys_pages, cache.num_kv_heads,
+                                  cache.page_size)
     for pool, codes, scales in ((cache.k_pages, k8, ks), (cache.v_pages, v8, vs)):
         ref_c, ref_s = O.kv8_encode_rows(pool.float().cpu().numpy())
         np.testing.assert_array_equal(scales.cpu().numpy(), ref_s)
@@ -531,7 +534,8 @@ def test_sparse_decode_attn_kv8(page, G):
     dec.use_kv8()
     out, m, l = dec.step(q)
     torch.cuda.synchronize()
-    k8, ks, v8, vs = [x.cpu().numpy() for x in dec.kv8]
+    k8, v8, ks, vs = [x.cpu().numpy() for x in B.kv8_unpack(dec.kv8, cache.num_phys_pages,
+                                                                cache.num_kv_heads, page)]
     Kd = O.kv8_decode_rows(k8, ks)
     Vd = O.kv8_decode_rows(v8, vs)
     table = cache.page_table.cpu().numpy()
