@@ -526,7 +526,7 @@ def bench_rows(dev, flush, peak):
     # attention over KV8 pages (e4m3 rows + fp32 row scales: 264 B per token per KV head)
     dec.use_kv8()
     ms = _time_graph(_graph(lambda: dec.attend(q)), flush)
-    out.append(_entry("N4", w.name, "dsa_sparse_decode_attn_kv8 (8-bit pages, split-K)", ms,
+    out.append(_entry("N4", w.name, "dsa_sparse_decode_attn_kv8 (8-bit pages, persistent split-K)", ms,
                       sel * w.page_size * 264 + q.numel() * 2 + q.numel() * 4, peak, pages=sel))
     del dec, cache, inp
     torch.cuda.empty_cache()

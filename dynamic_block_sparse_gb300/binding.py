@@ -278,17 +278,28 @@ def dsa_kv8_bytes(kv: PagedKV) -> int:
 
 def dsa_quantize_kv8(kv: PagedKV, kv8, stream=None):
     """bf16 pools -> KV8 blocks (uint8 tensor of dsa_kv8_bytes(kv) bytes): per (physical page, KV
-    head) the e4m3 K codes [p][128], V codes [p][128], K scales fp32 [p], V scales fp32 [p]."""
+    head) the e4m3 K codes [p][128], V codes [p][128] (16-byte pieces XOR-permuted by the token
+    slot mod 8), K scales fp32 [p], V scales fp32 [p]; ``kv8_unpack`` takes them apart."""
     _check("dsa_quantize_kv8", load().dsa_quantize_kv8(ctypes.byref(kv), _ptr(kv8),
                                                        _stream(stream)))
 
 
 def kv8_unpack(kv8, num_phys_pages: int, num_kv_heads: int, page: int):
-    """Views of a KV8 buffer: (K codes, V codes) uint8 ``[P][Hkv][p][128]`` and (K scales, V
+    """The parts of a KV8 buffer: (K codes, V codes) uint8 ``[P][Hkv][p][128]`` in dim order (the
+    stored rows keep their 16-byte pieces XOR-permuted by the token slot mod 8) and (K scales, V
     scales) fp32 ``[P][Hkv][p]``."""
     blk = kv8.view(num_phys_pages, num_kv_heads, 264 * page)
-    kc = blk[..., :128 * page].view(num_phys_pages, num_kv_heads, page, 128)
-    vc = blk[..., 128 * page:256 * page].view(num_phys_pages, num_kv_heads, page, 128)
+    # piece c of slot r is stored at piece c ^ (r % 8); the permutation is its own inverse
+    r = torch.arange(page, device=kv8.device).view(page, 1)
+    c = torch.arange(8, device=kv8.device).view(1, 8)
+    perm = (c ^ (r % 8)).view(1, 1, page, 8, 1).expand(num_phys_pages, num_kv_heads, page, 8, 16)
+
+    def codes(part):
+        rows = part.reshape(num_phys_pages, num_kv_heads, page, 8, 16)
+        return torch.gather(rows, 3, perm).reshape(num_phys_pages, num_kv_heads, page, 128)
+
+    kc = codes(blk[..., :128 * page])
+    vc = codes(blk[..., 128 * page:256 * page])
     ks = blk[..., 256 * page:260 * page].contiguous().view(torch.float32)
     vs = blk[..., 260 * page:].contiguous().view(torch.float32)
     return kc, vc, ks, vs

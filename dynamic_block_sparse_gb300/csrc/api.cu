@@ -691,10 +691,10 @@ int dsa_sparse_decode_attn_kv8(const dsa_paged_kv* kv, const void* kv8, const vo
   if (!workspace || workspace_bytes < need)
     return fail(DSA_ERR_WORKSPACE, "workspace of %zu bytes needed", need);
   if (!aligned(workspace, 16)) return fail(DSA_ERR_ALIGNMENT, "workspace must be 16-byte aligned");
-  // as many stages (of 264 B per token) as fit beside the decode tiles, up to 96 KB of them
+  // as many stages (of 264 B per token) as fit, up to 128 KB of them (the bf16 path's budget)
   const size_t smem_cap = 227 * 1024;
   const int stride = (264 * v.p + 1023) & ~1023;
-  int stages = 98304 / stride;
+  int stages = 131072 / stride;
   if (stages > kStreamMaxStages) stages = kStreamMaxStages;
   while (stages > 1 && stream_attn_smem_bytes(v.p, stages, v.G, true) > smem_cap) --stages;
   if (stages < 1 || stream_attn_smem_bytes(v.p, stages, v.G, true) > smem_cap)

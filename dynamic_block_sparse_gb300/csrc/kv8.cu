@@ -1,8 +1,10 @@
 // KV8 pages: the KV pool quantised to 8-bit floats (e4m3) with one fp32 scale per (page, KV head,
 // token) for K and one for V -- half the bytes of every selected page the attention reads.  A
 // (physical page, KV head) block is contiguous, 264 p bytes: the K codes [p][128], the V codes
-// [p][128], the K scales [p], the V scales [p], so that one bulk copy brings a page.  The
-// quantiser; the persistent attention (stream_attn.cu) reads the blocks and decodes them per tile.
+// [p][128], the K scales [p], the V scales [p], so that one bulk copy brings a page.  Within the
+// 128-byte code row of token slot r, the 16-byte piece of dims 16 c .. 16 c + 15 sits at piece
+// c ^ (r mod 8), so that the attention's operand loads (eight rows at once) hit distinct banks.
+// The quantiser; the persistent attention (stream_attn.cu) reads the codes per tile.
 #include <cuda_fp8.h>
 
 #include "internal.h"
@@ -24,10 +26,11 @@ __global__ void __launch_bounds__(kQ8Threads)
   const long long blk = r / page;
   const int slot = static_cast<int>(r - blk * page);
   uint8_t* base = kv8 + blk * 264 * page;
-  uint8_t* dst =
-      base + static_cast<long long>(which) * 128 * page + static_cast<long long>(slot) * 128;
-  float* scale_out = reinterpret_cast<float*>(base + (256 + 4 * which) * page) + slot;
   const int lane = threadIdx.x & 31;
+  const int piece = (lane >> 2) ^ (slot & 7);  // the lane's 4 dims lie in piece lane / 4
+  uint8_t* dst = base + static_cast<long long>(which) * 128 * page +
+                 static_cast<long long>(slot) * 128 + piece * 16 + (lane & 3) * 4;
+  float* scale_out = reinterpret_cast<float*>(base + (256 + 4 * which) * page) + slot;
   const uint2 raw = __ldg(reinterpret_cast<const uint2*>(src + r * kHeadDim) + lane);
   const __nv_bfloat16* x = reinterpret_cast<const __nv_bfloat16*>(&raw);
   float v[4];
@@ -49,7 +52,7 @@ __global__ void __launch_bounds__(kQ8Threads)
         make_float2(v[2] / scale, v[3] / scale), __NV_SATFINITE, __NV_E4M3);
     packed = static_cast<uint32_t>(lo) | (static_cast<uint32_t>(hi) << 16);
   }
-  reinterpret_cast<uint32_t*>(dst)[lane] = packed;
+  *reinterpret_cast<uint32_t*>(dst) = packed;
   if (lane == 0) *scale_out = scale;
 }
 

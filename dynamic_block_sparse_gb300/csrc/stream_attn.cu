@@ -31,15 +31,14 @@ constexpr int kSMaxHeads = 1024;           // KV heads the dense-head table can 
 constexpr int kIssueLanes = 4;             // producer lanes issuing page loads at once
 
 struct SLayout {
-  uint32_t stage_stride, merge_off, q_off, bar_off, misc_off, conv_off, total;
+  uint32_t stage_stride, merge_off, q_off, bar_off, misc_off, total;
 };
 
 // merge area: per warp G rows of O (fp32) and G (m, l) pairs; later the row merge's weights.
 // q: two unpadded [16][128] bf16 query tiles (mailbox slots).  bars: [S] full, [S] empty, then the
 // mailbox's [2] full and [2] empty.
-// kv8: a stage holds a KV8 page (e4m3 K rows, V rows, then the two fp32 scale rows), and every
-// consumer warp has an 8 KB bf16 tile (16 tokens of K and V, swizzled as a loaded page) it decodes
-// its tiles into.
+// kv8: a stage holds a KV8 page block (e4m3 K rows, V rows, then the two fp32 scale rows); the
+// consumers read the codes straight into tensor-core operands (no decoded copy in shared memory).
 __host__ __device__ inline SLayout slayout(int page, int stages, int G, bool kv8 = false) {
   SLayout L;
   L.stage_stride = kv8 ? (264u * page + 1023u) & ~1023u : 512u * page;
@@ -47,25 +46,188 @@ __host__ __device__ inline SLayout slayout(int page, int stages, int G, bool kv8
   L.q_off = L.merge_off + static_cast<uint32_t>(kSW * G * (kHeadDim + 2) * 4 + 127) / 128 * 128;
   L.bar_off = L.q_off + 2u * 16u * kHeadDim * 2u;
   L.misc_off = L.bar_off + 16u * static_cast<uint32_t>(stages) + 32u;
-  L.conv_off = (L.misc_off + 256u + 8u * kSMaxHeads + 1023u) & ~1023u;
-  L.total = L.conv_off + (kv8 ? static_cast<uint32_t>(kSW) * 8192u : 0u) + 1024u;
+  L.total = ((L.misc_off + 256u + 8u * kSMaxHeads + 1023u) & ~1023u) + 1024u;
   return L;
 }
 
-// Eight e4m3 values times a scale, as eight bf16 (one 16-byte piece of a staged bf16 row).
-DSA_DEV uint4 decode8(uint2 w, float scale) {
-  uint4 o;
-  uint32_t* po = reinterpret_cast<uint32_t*>(&o);
-  const uint16_t* pw = reinterpret_cast<const uint16_t*>(&w);
+// ---- KV8 tiles, read from the codes in registers.  Products run in f16 (an e4m3 value is exact
+// in f16): S = Q . codes_K^T, then each token's logit times its K scale; P times each token's V
+// scale, then O += (P * s_V) . codes_V.  A code row keeps its 16-byte pieces XOR-permuted by the
+// row's index mod 8 (the KV8 layout), so the loads below hit distinct banks.
+
+// Two e4m3 values (the low 16 bits of w) as an f16 pair.
+DSA_DEV uint32_t e4m3x2_f16x2(uint32_t w) {
+  const __half2_raw h =
+      __nv_cvt_fp8x2_to_halfraw2(static_cast<__nv_fp8x2_storage_t>(w & 0xffffu), __NV_E4M3);
+  return static_cast<uint32_t>(h.x) | (static_cast<uint32_t>(h.y) << 16);
+}
+
+DSA_DEV uint32_t pack_f16(float lo, float hi) {
+  const __half2 v = __floats2half2_rn(lo, hi);
+  return *reinterpret_cast<const uint32_t*>(&v);
+}
+
+DSA_DEV void mma_f16(float (&d)[4], const uint32_t (&a)[4], uint32_t b0, uint32_t b1) {
+  asm volatile(
+      "mma.sync.aligned.m16n8k16.row.col.f32.f16.f16.f32 {%0, %1, %2, %3}, {%4, %5, %6, %7}, "
+      "{%8, %9}, {%0, %1, %2, %3};"
+      : "+f"(d[0]), "+f"(d[1]), "+f"(d[2]), "+f"(d[3])
+      : "r"(a[0]), "r"(a[1]), "r"(a[2]), "r"(a[3]), "r"(b0), "r"(b1));
+}
+
+// Query fragments (f16) for the KV8 scores.  The head dims are permuted inside the k-steps so that
+// a lane's K operand is one 32-byte run of a code row: lane column tig owns dims 32 tig .. +31,
+// k-step ks takes dims 32 tig + 4 ks .. +3 of them (+0, +1 as k = 2 tig, 2 tig + 1; +2, +3 as
+// k = 2 tig + 8, + 9).  sQ: 16 rows of 128 bf16.
+DSA_DEV void load_q_frags_kv8(const __nv_bfloat16* sQ, uint32_t (&qa)[8][4]) {
+  const int lane = threadIdx.x & 31;
+  const int r0 = lane >> 2, tig = lane & 3;
+  auto f16_pair = [](uint32_t bf2) {
+    const __nv_bfloat162 b = *reinterpret_cast<const __nv_bfloat162*>(&bf2);
+    const float2 f = __bfloat1622float2(b);
+    return pack_f16(f.x, f.y);
+  };
 #pragma unroll
-  for (int e = 0; e < 4; ++e) {
-    const __half2_raw hr =
-        __nv_cvt_fp8x2_to_halfraw2(static_cast<__nv_fp8x2_storage_t>(pw[e]), __NV_E4M3);
-    const float2 f = __half22float2(*reinterpret_cast<const __half2*>(&hr));
-    const __nv_bfloat162 b = __floats2bfloat162_rn(f.x * scale, f.y * scale);
-    po[e] = *reinterpret_cast<const uint32_t*>(&b);
+  for (int ks = 0; ks < 8; ++ks) {
+    const int c = 32 * tig + 4 * ks;
+    const uint2 lo = *reinterpret_cast<const uint2*>(sQ + r0 * kHeadDim + c);
+    const uint2 hi = *reinterpret_cast<const uint2*>(sQ + (r0 + 8) * kHeadDim + c);
+    qa[ks][0] = f16_pair(lo.x);
+    qa[ks][1] = f16_pair(hi.x);
+    qa[ks][2] = f16_pair(lo.y);
+    qa[ks][3] = f16_pair(hi.y);
   }
-  return o;
+}
+
+// S = Q . codes^T for the 16 code rows at kc (rows 16t .. 16t + 15 of a page block).
+DSA_DEV void tile_scores_kv8(const uint32_t (&qa)[8][4], const uint8_t* kc, float (&sc)[2][4]) {
+  const int lane = threadIdx.x & 31;
+  const int g = lane >> 2, tig = lane & 3;
+  float acc[2][2][4];
+#pragma unroll
+  for (int c = 0; c < 2; ++c)
+#pragma unroll
+    for (int nt = 0; nt < 2; ++nt)
+#pragma unroll
+      for (int e = 0; e < 4; ++e) acc[c][nt][e] = 0.f;
+#pragma unroll
+  for (int nt = 0; nt < 2; ++nt) {
+    const uint8_t* row = kc + (nt * 8 + g) * 128;  // token nt * 8 + g; its index mod 8 is g
+    const uint4 w0 = *reinterpret_cast<const uint4*>(row + (((2 * tig) ^ g) << 4));
+    const uint4 w1 = *reinterpret_cast<const uint4*>(row + (((2 * tig + 1) ^ g) << 4));
+    const uint32_t w[8] = {w0.x, w0.y, w0.z, w0.w, w1.x, w1.y, w1.z, w1.w};
+#pragma unroll
+    for (int ks = 0; ks < 8; ++ks)
+      mma_f16(acc[ks & 1][nt], qa[ks], e4m3x2_f16x2(w[ks]), e4m3x2_f16x2(w[ks] >> 16));
+  }
+#pragma unroll
+  for (int nt = 0; nt < 2; ++nt)
+#pragma unroll
+    for (int e = 0; e < 4; ++e) sc[nt][e] = acc[0][nt][e] + acc[1][nt][e];
+}
+
+// Online-softmax update with the tile's logits (q . codes in sc; ks / vs: the 16 tokens' K and V
+// scales), then O += (P * s_V) . codes_V.  The output dims are permuted: n-tile j, column c holds
+// dim 16 c + j, so that a lane's V operand is one 16-byte piece of each of its four code rows.
+DSA_DEV void tile_softmax_pv_kv8(WarpSoftmaxState& st, float (&sc)[2][4], float scale_log2,
+                                 uint32_t valid, const uint8_t* vc, const float* ks,
+                                 const float* vs) {
+  const int lane = threadIdx.x & 31;
+  const int g = lane >> 2, tig = lane & 3;
+  const float2 k0 = *reinterpret_cast<const float2*>(ks + 2 * tig);
+  const float2 k1 = *reinterpret_cast<const float2*>(ks + 8 + 2 * tig);
+  const float kscale[2][2] = {{k0.x, k0.y}, {k1.x, k1.y}};
+  float x[2][4];
+#pragma unroll
+  for (int nt = 0; nt < 2; ++nt)
+#pragma unroll
+    for (int e = 0; e < 4; ++e) {
+      const int col = nt * 8 + tig * 2 + (e & 1);
+      x[nt][e] = ((valid >> col) & 1u) ? sc[nt][e] * kscale[nt][e & 1] * scale_log2 : -INFINITY;
+    }
+  float mx[2];
+  mx[0] = fmaxf(fmaxf(x[0][0], x[0][1]), fmaxf(x[1][0], x[1][1]));
+  mx[1] = fmaxf(fmaxf(x[0][2], x[0][3]), fmaxf(x[1][2], x[1][3]));
+#pragma unroll
+  for (int r = 0; r < 2; ++r) {
+    mx[r] = fmaxf(mx[r], __shfl_xor_sync(0xffffffffu, mx[r], 1));
+    mx[r] = fmaxf(mx[r], __shfl_xor_sync(0xffffffffu, mx[r], 2));
+  }
+  float alpha[2], mnew[2];
+#pragma unroll
+  for (int r = 0; r < 2; ++r) {
+    mnew[r] = fmaxf(st.m[r], mx[r]);
+    alpha[r] = (mnew[r] == -INFINITY) ? 1.f : fast_exp2(st.m[r] - mnew[r]);
+  }
+  float p[2][4];
+#pragma unroll
+  for (int nt = 0; nt < 2; ++nt)
+#pragma unroll
+    for (int e = 0; e < 4; ++e) {
+      const int r = e >> 1;
+      p[nt][e] = (mnew[r] == -INFINITY) ? 0.f : fast_exp2(x[nt][e] - mnew[r]);
+    }
+  st.l[0] = st.l[0] * alpha[0] + (p[0][0] + p[0][1] + p[1][0] + p[1][1]);
+  st.l[1] = st.l[1] * alpha[1] + (p[0][2] + p[0][3] + p[1][2] + p[1][3]);
+  st.m[0] = mnew[0];
+  st.m[1] = mnew[1];
+  if (!__all_sync(0xffffffffu, alpha[0] == 1.f && alpha[1] == 1.f)) {
+#pragma unroll
+    for (int j = 0; j < 16; ++j) {
+      st.o[j][0] *= alpha[0];
+      st.o[j][1] *= alpha[0];
+      st.o[j][2] *= alpha[1];
+      st.o[j][3] *= alpha[1];
+    }
+  }
+  // P * s_V (0 for tokens that take no part, whatever their scale holds)
+  const float2 v0 = *reinterpret_cast<const float2*>(vs + 2 * tig);
+  const float2 v1 = *reinterpret_cast<const float2*>(vs + 8 + 2 * tig);
+  const float vscale[2][2] = {{v0.x, v0.y}, {v1.x, v1.y}};
+  float pv[2][4];
+#pragma unroll
+  for (int nt = 0; nt < 2; ++nt)
+#pragma unroll
+    for (int e = 0; e < 4; ++e) {
+      const int col = nt * 8 + tig * 2 + (e & 1);
+      pv[nt][e] = ((valid >> col) & 1u) ? p[nt][e] * vscale[nt][e & 1] : 0.f;
+    }
+  uint32_t pa[4];
+  pa[0] = pack_f16(pv[0][0], pv[0][1]);
+  pa[1] = pack_f16(pv[0][2], pv[0][3]);
+  pa[2] = pack_f16(pv[1][0], pv[1][1]);
+  pa[3] = pack_f16(pv[1][2], pv[1][3]);
+  // V operand of n-tile j: tokens 2 tig, 2 tig + 1 (b0) and 2 tig + 8, + 9 (b1) at dim 16 g + j:
+  // byte j of the 16-byte piece g of those four code rows (zeros for tokens that take no part,
+  // so that stale codes never meet a zero probability)
+  uint4 rv[4];
+#pragma unroll
+  for (int i = 0; i < 4; ++i) {
+    const int r = 2 * tig + (i & 1) + (i >> 1) * 8;
+    rv[i] = *reinterpret_cast<const uint4*>(vc + r * 128 + ((g ^ (r & 7)) << 4));
+    if (!((valid >> r) & 1u)) rv[i] = make_uint4(0u, 0u, 0u, 0u);
+  }
+  const uint32_t* w0 = reinterpret_cast<const uint32_t*>(&rv[0]);
+  const uint32_t* w1 = reinterpret_cast<const uint32_t*>(&rv[1]);
+  const uint32_t* w2 = reinterpret_cast<const uint32_t*>(&rv[2]);
+  const uint32_t* w3 = reinterpret_cast<const uint32_t*>(&rv[3]);
+#pragma unroll
+  for (int q = 0; q < 4; ++q) {  // dims 16 g + 4 q .. + 3
+    const uint32_t a01 = __byte_perm(w0[q], w1[q], 0x5140), b01 = __byte_perm(w0[q], w1[q], 0x7362);
+    const uint32_t a23 = __byte_perm(w2[q], w3[q], 0x5140), b23 = __byte_perm(w2[q], w3[q], 0x7362);
+    mma_f16(st.o[4 * q], pa, e4m3x2_f16x2(a01), e4m3x2_f16x2(a23));
+    mma_f16(st.o[4 * q + 1], pa, e4m3x2_f16x2(a01 >> 16), e4m3x2_f16x2(a23 >> 16));
+    mma_f16(st.o[4 * q + 2], pa, e4m3x2_f16x2(b01), e4m3x2_f16x2(b23));
+    mma_f16(st.o[4 * q + 3], pa, e4m3x2_f16x2(b01 >> 16), e4m3x2_f16x2(b23 >> 16));
+  }
+}
+
+// Shared position of output dim d of query head r in the KV8 path's merge area: the pieces of 16
+// dims are XOR-permuted by the writer's column pair and row, so that the fragment stores of a warp
+// spread over the banks.
+DSA_DEV int kv8_o_pos(int r, int d) {
+  const int c = d >> 4;
+  return (d & ~15) | ((d & 15) ^ (((c >> 1) & 3) | ((r & 3) << 2)));
 }
 
 // Slot range [beg, end) of the active CTA c among n over T slots.
@@ -439,7 +601,10 @@ __global__ void __launch_bounds__(kSThreads, 1)
     const int b = row / kv.Hkv, h = row % kv.Hkv;
     const int di = d_first + u;
     uint32_t qa[8][4];
-    load_q_frags(sQ + slot * 16 * kHeadDim, qa, kHeadDim);
+    if (KV8)
+      load_q_frags_kv8(sQ + slot * 16 * kHeadDim, qa);
+    else
+      load_q_frags(sQ + slot * 16 * kHeadDim, qa, kHeadDim);
     __syncwarp();
     if (lane == 0) mbar_arrive(smem_u32(&qbars[2 + slot]));
     WarpSoftmaxState st;
@@ -465,29 +630,11 @@ __global__ void __launch_bounds__(kSThreads, 1)
         if (vm == 0u) continue;
         float sc[2][4];
         if (KV8) {
-          // decode the tile into this warp's bf16 tile (K and V rows times their scales; V rows
-          // of tokens that take no part as zeros), laid out and swizzled as a loaded page of 16
-          const uint8_t* st8 = smem + s * stage_bytes;
-          const float* ksc = reinterpret_cast<const float*>(st8 + 256 * page) + t * 16;
-          const float* vsc = ksc + page;
-          uint8_t* cb = smem + lay.conv_off + warp * 8192;
-#pragma unroll
-          for (int k = 0; k < 8; ++k) {  // 16 rows x 16 pieces of 8 dims, 8 per lane
-            const int unit = lane + 32 * k;
-            const int r = unit >> 4, c16 = unit & 15;
-            const size_t src = static_cast<size_t>(t * 16 + r) * 128 + c16 * 8;
-            const uint2 kw = *reinterpret_cast<const uint2*>(st8 + src);
-            const uint2 vw = *reinterpret_cast<const uint2*>(st8 + 128 * page + src);
-            const uint32_t off = (c16 >> 3) * 2048u + sw128(static_cast<uint32_t>(r), c16 & 7u);
-            *reinterpret_cast<uint4*>(cb + off) = decode8(kw, ksc[r]);
-            *reinterpret_cast<uint4*>(cb + 4096 + off) =
-                ((vm >> r) & 1u) ? decode8(vw, vsc[r]) : make_uint4(0u, 0u, 0u, 0u);
-          }
-          __syncwarp();
-          const uint32_t kt = smem_u32(cb);
-          tile_scores(qa, kt, 16, 0, sc);
-          tile_softmax_pv(st, sc, a.scale_log2, vm, kt + 4096, 16, 0);
-          __syncwarp();  // the tile is rewritten by the warp's next one
+          const uint8_t* blk = smem + s * stage_bytes;  // the page's KV8 block
+          const float* ksc = reinterpret_cast<const float*>(blk + 256 * page) + t * 16;
+          tile_scores_kv8(qa, blk + t * 16 * 128, sc);
+          tile_softmax_pv_kv8(st, sc, a.scale_log2, vm, blk + (page + t * 16) * 128, ksc,
+                              ksc + page);
         } else {
           if (vm != 0xffffu)
             wrote |=
@@ -510,6 +657,17 @@ __global__ void __launch_bounds__(kSThreads, 1)
       float* wO = sO + warp * G * kHeadDim;
 #pragma unroll
       for (int j = 0; j < 16; ++j) {
+        if (KV8) {  // column c of n-tile j is dim 16 c + j
+          if (r0 < G) {
+            wO[r0 * kHeadDim + kv8_o_pos(r0, 16 * c0 + j)] = st.o[j][0];
+            wO[r0 * kHeadDim + kv8_o_pos(r0, 16 * c0 + 16 + j)] = st.o[j][1];
+          }
+          if (r0 + 8 < G) {
+            wO[(r0 + 8) * kHeadDim + kv8_o_pos(r0 + 8, 16 * c0 + j)] = st.o[j][2];
+            wO[(r0 + 8) * kHeadDim + kv8_o_pos(r0 + 8, 16 * c0 + 16 + j)] = st.o[j][3];
+          }
+          continue;
+        }
         if (r0 < G)
           *reinterpret_cast<float2*>(wO + r0 * kHeadDim + j * 8 + c0) =
               make_float2(st.o[j][0], st.o[j][1]);
@@ -540,6 +698,7 @@ __global__ void __launch_bounds__(kSThreads, 1)
 #pragma unroll
       for (int w = 0; w < kSW; ++w) M = fmaxf(M, sM[w * G + g]);
       float Lsum = 0.f, acc = 0.f;
+      const int pos = KV8 ? kv8_o_pos(g, d) : d;
       if (M != -INFINITY) {
 #pragma unroll
         for (int w = 0; w < kSW; ++w) {
@@ -547,7 +706,7 @@ __global__ void __launch_bounds__(kSThreads, 1)
           if (mw == -INFINITY) continue;
           const float f = fast_exp2(mw - M);
           Lsum += sL[w * G + g] * f;
-          acc += sO[(w * G + g) * kHeadDim + d] * f;
+          acc += sO[(w * G + g) * kHeadDim + pos] * f;
         }
       }
       const float o = Lsum > 0.f ? acc / Lsum : 0.f;

@@ -285,7 +285,9 @@ int dsa_hybrid_decode_attn(const dsa_paged_kv* kv, const void* q, const int32_t*
  * zeros gets scale 0 and zero bytes.  A value decodes as e4m3_value(byte) * scale.
  * Layout: one contiguous block of 264 p bytes per (physical page P, KV head h), at offset
  * (P * Hkv + h) * 264 p: the K codes [p][128], the V codes [p][128], the K scales fp32 [p], the V
- * scales fp32 [p] -- so the attention brings a selected page with one bulk copy.
+ * scales fp32 [p] -- so the attention brings a selected page with one bulk copy.  In the code row
+ * of token slot r the 16 codes of dims 16 c .. 16 c + 15 are stored at bytes 16 (c ^ (r mod 8))
+ * .. +15 (a bank-spreading permutation for the attention's operand loads).
  *   kv8 (out) : dsa_kv8_bytes(kv) bytes, 16-byte aligned.
  * Every physical page is converted (the bf16 pools are read, not changed).
  */
@@ -295,9 +297,10 @@ size_t dsa_kv8_bytes(const dsa_paged_kv* kv);
 /*
  * Sparse decode attention over KV8 pages: as the persistent path of dsa_sparse_decode_attn (exact
  * attention of every dense head's query group over the tokens of its selected pages, one stream-K
- * launch) with K and V decoded from the KV8 blocks: each consumer warp decodes its 16-token tiles
- * to bf16 (value times scale) before the tensor-core products.  kv->k_pages / v_pages are not read
- * (may be NULL); the page table, lengths and shapes are.  Streaming heads are skipped.
+ * launch) over the KV8 blocks: the tensor-core products take the e4m3 codes as f16 (exact) with
+ * the query in f16 (|q| below 65504), each logit times its token's K scale and each probability
+ * times its token's V scale (rounded to f16 for the P.V product).  kv->k_pages / v_pages are not
+ * read (may be NULL); the page table, lengths and shapes are.  Streaming heads are skipped.
  *   workspace : dsa_sparse_decode_attn_kv8_workspace_size(kv, idx_stride) bytes.
  */
 int dsa_sparse_decode_attn_kv8(const dsa_paged_kv* kv, const void* kv8, const void* q,

@@ -244,3 +244,36 @@ def test_replica_timing_takes_max_over_ranks_gloo(tmp_path):
     mp.spawn(_replica_worker, args=(2, port, out), nprocs=2, join=True)
     vals = [json.load(open(out + f".{r}")) for r in range(2)]
     assert vals == [3.5, 3.5]
+
+
+def test_kv8_unpack_reads_the_documented_layout():
+    """A KV8 buffer written byte by byte from the layout the header documents (per (page, KV
+    head): K codes, V codes with the 16-byte pieces of slot r's row at piece c ^ (r mod 8), then
+    the K and V scales) comes apart into codes in dim order and the scales."""
+    from dynamic_block_sparse_gb300 import binding as B
+    P, H, p = 3, 2, 16
+    rng = np.random.default_rng(5)
+    kc = rng.integers(0, 256, size=(P, H, p, 128), dtype=np.uint8)
+    vc = rng.integers(0, 256, size=(P, H, p, 128), dtype=np.uint8)
+    ks = rng.random((P, H, p), dtype=np.float32)
+    vs = rng.random((P, H, p), dtype=np.float32)
+    buf = bytearray(P * H * 264 * p)
+    for b in range(P):
+        for h in range(H):
+            base = (b * H + h) * 264 * p
+            for r in range(p):
+                for c in range(8):
+                    at = 16 * (c ^ (r % 8))
+                    buf[base + r * 128 + at: base + r * 128 + at + 16] = \
+                        kc[b, h, r, 16 * c:16 * c + 16].tobytes()
+                    vbase = base + 128 * p
+                    buf[vbase + r * 128 + at: vbase + r * 128 + at + 16] = \
+                        vc[b, h, r, 16 * c:16 * c + 16].tobytes()
+            buf[base + 256 * p: base + 260 * p] = ks[b, h].tobytes()
+            buf[base + 260 * p: base + 264 * p] = vs[b, h].tobytes()
+    t = torch.frombuffer(buf, dtype=torch.uint8)
+    k8, v8, ks8, vs8 = B.kv8_unpack(t, P, H, p)
+    np.testing.assert_array_equal(k8.numpy(), kc)
+    np.testing.assert_array_equal(v8.numpy(), vc)
+    np.testing.assert_array_equal(ks8.numpy(), ks)
+    np.testing.assert_array_equal(vs8.numpy(), vs)
