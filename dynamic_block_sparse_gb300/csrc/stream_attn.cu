@@ -12,7 +12,9 @@
 // whole K/V pages (one 3-D tensor load per pool) through a ring of about 128 KB, several lanes
 // issuing at once.  Warps 0..7 attend with the mma core.  Every (stage, 16-token tile) slot of the
 // ring belongs to one consumer warp for the whole launch, so a warp waits only for the pages it
-// computes on and each stage is released by exactly the warps that read it.  The producer also
+// computes on, it waits on every phase of its stages in order (a phase-parity wait is only
+// unambiguous for a waiter that never skips a phase), and each stage is released by exactly the
+// warps that read it.  The producer also
 // publishes each unit (its row, selected slots and request length, and the row's G query vectors
 // by a 1-D bulk copy) through a two-slot mailbox, so the consumers never touch global memory
 // before their epilogues.
@@ -610,11 +612,17 @@ __global__ void __launch_bounds__(kSThreads, 1)
     WarpSoftmaxState st;
     state_init(st);
     const int npg = end - beg;
+    // stage and phase parity of ring position i + k, stepped along without divisions (a warp
+    // passes over the positions of stages it does not own many times per page)
+    int s_next = i % S, ph_next = (i / S) & 1;
     for (int k = 0; k < npg; ++k) {
-      const int ii = i + k;
-      const int s = ii % S;
+      const int s = s_next, ph = ph_next;
+      if (++s_next == S) {
+        s_next = 0;
+        ph_next ^= 1;
+      }
       if (!((own_stages >> s) & 1u)) continue;
-      if (!mbar_wait(smem_u32(&bars[s]), (ii / S) & 1, abort_flag, kv.status)) break;
+      if (!mbar_wait(smem_u32(&bars[s]), ph, abort_flag, kv.status)) break;
       const int pos = stage_pos[s];
       const bool loaded = stage_ok[s] != 0;
       const uint32_t kb = smem_base + s * stage_bytes;
@@ -687,8 +695,9 @@ __global__ void __launch_bounds__(kSThreads, 1)
       }
     }
     named_barrier(1, kSConsumers);
+    // cut: the unit reaches outside this CTA's slot range (other CTAs hold part of the row)
     const long long rs = unit_start(di);
-    const bool cut = slot_owner(rs, T, n_act) != slot_owner(rs + unit_stride(di) - 1, T, n_act);
+    const bool cut = rs < my_beg || rs + unit_stride(di) > my_end;
     any_cut |= cut;
     float* rec0 =
         a.part + (static_cast<size_t>(blockIdx.x) * 2 + (u == 0 ? 0 : 1)) * G * kRecordFloats;
@@ -733,9 +742,11 @@ __global__ void __launch_bounds__(kSThreads, 1)
   // ---- rows cut across CTAs (only this CTA's first and last units can be).  Both tickets are
   // taken at once when all of this CTA's records are written; the CTA that takes a row's last
   // ticket merges the row's records in CTA order, eight records per round trip, one query head
-  // per warp.
+  // per warp.  The row's record geometry (first CTA, CTA count, the first CTA's record slot) is
+  // worked out once per cut row, beside its ticket: the merge itself divides nothing.
   if (any_cut) {
     const int n_cut = n_units > 1 ? 2 : 1;
+    int* cut_info = misc + 50;  // [2][first CTA, CTA count, row, record slot of the first CTA]
     if (warp == 0 && lane < n_cut) {
       const int di = d_first + (lane == 0 ? 0 : n_units - 1);
       const long long rs = unit_start(di);
@@ -744,6 +755,11 @@ __global__ void __launch_bounds__(kSThreads, 1)
       int last = 0;
       if (c_first != c_last) {
         const int row = unit_row(di);
+        cut_info[lane * 4 + 0] = c_first;
+        cut_info[lane * 4 + 1] = c_last - c_first + 1;
+        cut_info[lane * 4 + 2] = row;
+        // the row is the first CTA's last unit: slot 1 unless it is also that CTA's first
+        cut_info[lane * 4 + 3] = slot_start(c_first, T, n_act) < rs ? 1 : 0;
         last = ticket_add(a.counters + row) == c_last - c_first;
       }
       last_flag[lane] = last;
@@ -753,11 +769,10 @@ __global__ void __launch_bounds__(kSThreads, 1)
     for (int job = warp; job < n_jobs; job += kSW) {
       const int k = job / G, g = job - k * G;
       if (!last_flag[k]) continue;
-      const int di = d_first + (k == 0 ? 0 : n_units - 1);
-      const int row = unit_row(di);
-      const long long rs = unit_start(di);
-      const int c_first = slot_owner(rs, T, n_act);
-      const int C = slot_owner(rs + unit_stride(di) - 1, T, n_act) - c_first + 1;
+      const int c_first = cut_info[k * 4 + 0];
+      const int C = cut_info[k * 4 + 1];
+      const int row = cut_info[k * 4 + 2];
+      const int slot_first = cut_info[k * 4 + 3];
       float M = -INFINITY, Ls = 0.f;
       float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
       for (int c0 = 0; c0 < C; c0 += 8) {
@@ -770,7 +785,7 @@ __global__ void __launch_bounds__(kSThreads, 1)
           v[j] = make_float4(0.f, 0.f, 0.f, 0.f);
           const int c = c_first + c0 + j;
           if (c0 + j < C) {
-            const int slot = unit_of(slot_start(c, T, n_act)) == di ? 0 : 1;
+            const int slot = c0 + j == 0 ? slot_first : 0;  // later CTAs start inside the row
             const float* r = a.part + ((static_cast<size_t>(c) * 2 + slot) * G + g) * kRecordFloats;
             v[j] = __ldcg(reinterpret_cast<const float4*>(r) + lane);
             mv[j] = __ldcg(r + 128);
