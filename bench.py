@@ -790,13 +790,18 @@ def main():
 
 
 def source_hash() -> str:
+    """Hash of what the fused step's kernel is compiled from: prr_step.cu, every header of the
+    library and the C header (the other translation units do not reach prr_step_kernel)."""
     import hashlib
 
     h = hashlib.sha256()
     csrc = os.path.join(ROOT, "dynamic_block_sparse_gb300", "csrc")
-    for f in sorted(os.listdir(csrc)):
-        with open(os.path.join(csrc, f), "rb") as fh:
-            h.update(f.encode() + fh.read())
+    files = [os.path.join(csrc, f) for f in sorted(os.listdir(csrc))
+             if f == "prr_step.cu" or f.endswith((".cuh", ".h"))]
+    files.append(os.path.join(ROOT, "include", "dsa.h"))
+    for path in files:
+        with open(path, "rb") as fh:
+            h.update(os.path.basename(path).encode() + fh.read())
     return h.hexdigest()[:16]
 
 
