@@ -182,7 +182,7 @@ def dist_env():
 def prr_bytes(w, n_valid_pages, P_pages, missed_pages):
     """Algorithmic bytes of one PRR decode step (see module docstring) for a step that attends
     ``P_pages`` speculative and ``missed_pages`` repaired (page, KV head) units summed over rows
-    (averages are fine); also the spec form (metadata + K/V of the true set A only)."""
+    (averages are fine); also the true-set form (metadata + K/V of the true set A only)."""
     rows = w.batch * w.num_kv_heads
     G, D = w.group, w.head_dim
     page_kv = w.page_size * D * 2 * 2
@@ -195,8 +195,8 @@ def prr_bytes(w, n_valid_pages, P_pages, missed_pages):
     idx = rows * (w.k + w.k_pred) * 4 * 3
     out = w.batch * w.num_q_heads * (D + 2) * 4
     total = meta + q + kv + records + scores + ema + idx + out
-    north = meta + rows * w.k * page_kv
-    return total, north, dict(meta=meta, kv=kv, records=records, aux=q + scores + ema + idx + out)
+    true_set = meta + rows * w.k * page_kv
+    return total, true_set, dict(meta=meta, kv=kv, records=records, aux=q + scores + ema + idx + out)
 
 
 # ------------------------------------------------------------------------------------ ours
@@ -330,7 +330,7 @@ def bench_prr(args, w, dev, rank):
         P_counts.append(pcount)
         missed.append(mcount)
     n = len(step_ms)
-    bytes_step, north_step, parts = prr_bytes(w, n_valid, sum(P_counts) / n, sum(missed) / n)
+    bytes_step, true_set_step, parts = prr_bytes(w, n_valid, sum(P_counts) / n, sum(missed) / n)
     mean_ms = statistics.mean(step_ms)
 
     rows = w.batch * w.num_kv_heads
@@ -352,8 +352,8 @@ def bench_prr(args, w, dev, rank):
                                  + rows * n_valid * 512) / (meta_build_ms * 1e6),
                  stage_ms=stage_ms, stage_bytes=stage_bytes,
                  mean_P=sum(P_counts) / n / rows, mean_missed=sum(missed) / n / rows,
-                 bytes_per_step=bytes_step, north_star_bytes_per_step=north_step,
-                 north_star_gbs=north_step / (mean_ms * 1e6),
+                 bytes_per_step=bytes_step, true_set_bytes_per_step=true_set_step,
+                 true_set_gbs=true_set_step / (mean_ms * 1e6),
                  byte_parts=parts,
                  step_ms_p50=statistics.median(step_ms), step_ms_min=min(step_ms))
     peak, _ = load_peaks()

@@ -217,10 +217,10 @@ def test_bench_byte_accounting():
     import bench
     from dynamic_block_sparse_gb300.workloads import BY_NAME
     w = BY_NAME["prr_512k"]
-    total, north, parts = bench.prr_bytes(w, 8192, 152, 4)
+    total, true_set, parts = bench.prr_bytes(w, 8192, 152, 4)
     assert parts["meta"] == 2 * 8192 * 512
     assert parts["kv"] == 156 * 64 * 512
-    assert north == 2 * 8192 * 512 + 2 * 64 * 64 * 512
+    assert true_set == 2 * 8192 * 512 + 2 * 64 * 64 * 512
     assert total > parts["meta"] + parts["kv"]
 
 
