@@ -79,6 +79,9 @@ def parse_args(argv=None):
     p.add_argument("--cpu-seconds", type=float, default=12.0)
     p.add_argument("--no-cpu-baseline", action="store_true")
     p.add_argument("--no-rows", action="store_true", help="skip the per-row table")
+    p.add_argument("--rows-only", default=None, metavar="WORKLOAD",
+                   help="time only the rows of one row workload (llama3_8b_layer, lserve_hier, "
+                        "psa_threshold, tiny_topk) and print them; no decode-step line")
     p.add_argument("--oracle-child", action="store_true", help=argparse.SUPPRESS)
     return p.parse_args(argv)
 
@@ -196,7 +199,8 @@ def prr_bytes(w, n_valid_pages, P_pages, missed_pages):
     out = w.batch * w.num_q_heads * (D + 2) * 4
     total = meta + q + kv + records + scores + ema + idx + out
     true_set = meta + rows * w.k * page_kv
-    return total, true_set, dict(meta=meta, kv=kv, records=records, aux=q + scores + ema + idx + out)
+    aux = q + scores + ema + idx + out
+    return total, true_set, dict(meta=meta, kv=kv, records=records, aux=aux)
 
 
 # ------------------------------------------------------------------------------------ ours
@@ -473,7 +477,7 @@ def _entry(row, workload, op, ms, nbytes, peak, **kw):
     return d
 
 
-def bench_rows(dev, flush, peak):
+def bench_rows(dev, flush, peak, only=None):
     """Every hot-path row on the workload it belongs to: one library call captured as a graph and
     replayed with L2 flushed before each replay.  Bytes are algorithmic (what the call must read
     and write), from the counts the call actually produced."""
@@ -487,133 +491,138 @@ def bench_rows(dev, flush, peak):
     out = []
     KVP = 512  # K + V bytes per token per KV head
 
-    # ---- Llama-3-8B layer: kmax/kmin metadata, scores, top-256, sparse attention
-    w = BY_NAME["llama3_8b_layer"]
-    inp = make_inputs(w, dev, shuffle_pages=False)
-    cache = Cache.from_inputs(inp, dev)
-    dec = TopKDecoder(cache, w.k, w.logical_page)
-    q = inp["q"][0].clone()
-    rows, npg = w.batch * w.num_kv_heads, w.pages_per_seq
-    ms = _time_graph(_graph(dec.build_meta), flush)
-    out.append(_entry("A1", w.name, "dsa_build_page_meta MINMAX", ms,
-                      rows * npg * w.page_size * 256 + rows * npg * 512, peak))
-    dec.step(q)
-    torch.cuda.synchronize()
-    sel = int(dec.count.sum())
-    ms = _time_graph(_graph(lambda: B.dsa_score_pages(cache.kv, q, dec.meta, B.DSA_META_MINMAX,
-                                                      w.logical_page, dec.scores)), flush)
-    out.append(_entry("A2", w.name, "dsa_score_pages MINMAX", ms,
-                      rows * npg * 512 + q.numel() * 2 + rows * dec.stride * 4, peak))
-    ms = _time_graph(_graph(lambda: B.dsa_select_topk(dec.scores, dec.stride, w.k, dec.idx,
-                                                      dec.count)), flush)
-    out.append(_entry("A3", w.name, "dsa_select_topk k=256 of 2048", ms,
-                      rows * dec.stride * 4 + rows * w.k * 4, peak))
-    ms = _time_graph(_graph(lambda: dec.attend(q)), flush)
-    out.append(_entry("A6", w.name, "dsa_sparse_decode_attn (persistent split-K)", ms,
-                      sel * w.page_size * KVP + q.numel() * 2 + q.numel() * 4, peak, pages=sel))
-    ms = _time_graph(_graph(lambda: dec.step(q)), flush)
-    out.append(_entry("step", w.name, "score + top-K + attention", ms,
-                      rows * npg * 512 + sel * w.page_size * KVP + rows * dec.stride * 8, peak))
-    # decode-time append of one token per request (replayed: it rewrites the newest token and
-    # recomputes its page's metadata, the work of every append)
-    k_new = torch.randn((w.batch, w.num_kv_heads, w.head_dim), device=dev).bfloat16()
-    v_new = torch.randn_like(k_new)
-    ms = _time_graph(_graph(lambda: B.dsa_append_kv(cache.kv, k_new, v_new, B.DSA_META_MINMAX,
-                                                    w.logical_page, dec.meta)), flush)
-    tail = [(int(L) - 1) % w.page_size + 1 for L in cache.seq_lens.tolist()]
-    out.append(_entry("N2", w.name, "dsa_append_kv: K/V of one token + its page's kmax/kmin", ms,
-                      sum(w.num_kv_heads * (KVP + t * 256 + 512) for t in tail), peak))
-    # attention over KV8 pages (e4m3 rows + fp32 row scales: 264 B per token per KV head)
-    dec.use_kv8()
-    ms = _time_graph(_graph(lambda: dec.attend(q)), flush)
-    out.append(_entry("N4", w.name, "dsa_sparse_decode_attn_kv8 (8-bit pages, persistent split-K)", ms,
-                      sel * w.page_size * 264 + q.numel() * 2 + q.numel() * 4, peak, pages=sel))
-    del dec, cache, inp
-    torch.cuda.empty_cache()
+    if only in (None, "llama3_8b_layer"):
+        # ---- Llama-3-8B layer: kmax/kmin metadata, scores, top-256, sparse attention
+        w = BY_NAME["llama3_8b_layer"]
+        inp = make_inputs(w, dev, shuffle_pages=False)
+        cache = Cache.from_inputs(inp, dev)
+        dec = TopKDecoder(cache, w.k, w.logical_page)
+        q = inp["q"][0].clone()
+        rows, npg = w.batch * w.num_kv_heads, w.pages_per_seq
+        ms = _time_graph(_graph(dec.build_meta), flush)
+        out.append(_entry("A1", w.name, "dsa_build_page_meta MINMAX", ms,
+                          rows * npg * w.page_size * 256 + rows * npg * 512, peak))
+        dec.step(q)
+        torch.cuda.synchronize()
+        sel = int(dec.count.sum())
+        ms = _time_graph(_graph(lambda: B.dsa_score_pages(cache.kv, q, dec.meta, B.DSA_META_MINMAX,
+                                                          w.logical_page, dec.scores)), flush)
+        out.append(_entry("A2", w.name, "dsa_score_pages MINMAX", ms,
+                          rows * npg * 512 + q.numel() * 2 + rows * dec.stride * 4, peak))
+        ms = _time_graph(_graph(lambda: B.dsa_select_topk(dec.scores, dec.stride, w.k, dec.idx,
+                                                          dec.count)), flush)
+        out.append(_entry("A3", w.name, "dsa_select_topk k=256 of 2048", ms,
+                          rows * dec.stride * 4 + rows * w.k * 4, peak))
+        ms = _time_graph(_graph(lambda: dec.attend(q)), flush)
+        out.append(_entry("A6", w.name, "dsa_sparse_decode_attn (persistent split-K)", ms,
+                          sel * w.page_size * KVP + q.numel() * 2 + q.numel() * 4, peak, pages=sel))
+        ms = _time_graph(_graph(lambda: dec.step(q)), flush)
+        out.append(_entry("step", w.name, "score + top-K + attention", ms,
+                          rows * npg * 512 + sel * w.page_size * KVP + rows * dec.stride * 8, peak))
+        # decode-time append of one token per request (replayed: it rewrites the newest token and
+        # recomputes its page's metadata, the work of every append)
+        k_new = torch.randn((w.batch, w.num_kv_heads, w.head_dim), device=dev).bfloat16()
+        v_new = torch.randn_like(k_new)
+        ms = _time_graph(_graph(lambda: B.dsa_append_kv(cache.kv, k_new, v_new, B.DSA_META_MINMAX,
+                                                        w.logical_page, dec.meta)), flush)
+        tail = [(int(L) - 1) % w.page_size + 1 for L in cache.seq_lens.tolist()]
+        out.append(_entry("N2", w.name, "dsa_append_kv: K/V of one token + its page's kmax/kmin",
+                          ms, sum(w.num_kv_heads * (KVP + t * 256 + 512) for t in tail), peak))
+        # attention over KV8 pages (e4m3 rows + fp32 row scales: 264 B per token per KV head)
+        dec.use_kv8()
+        ms = _time_graph(_graph(lambda: dec.attend(q)), flush)
+        out.append(_entry("N4", w.name,
+                          "dsa_sparse_decode_attn_kv8 (8-bit pages, persistent split-K)", ms,
+                          sel * w.page_size * 264 + q.numel() * 2 + q.numel() * 4, peak, pages=sel))
+        del dec, cache, inp
+        torch.cuda.empty_cache()
 
-    # ---- LServe hierarchical paging + streaming heads
-    w = BY_NAME["lserve_hier"]
-    inp = make_inputs(w, dev, shuffle_pages=False)
-    cache = Cache.from_inputs(inp, dev)
-    dec = HierDecoder(cache, w.k, w.logical_page, w.sink, w.local, w.reuse)
-    q = inp["q"][0].clone()
-    rows, npg = w.batch * w.num_kv_heads, w.pages_per_seq
-    dense = w.batch * (w.num_kv_heads - len(w.streaming_kv_heads))
-    stream_rows = rows - dense
-    ms = _time_graph(_graph(dec.build_meta), flush)
-    out.append(_entry("A1", w.name, "dsa_build_page_meta MINMAX (logical 16 in physical 64)", ms,
-                      rows * npg * w.page_size * 256 + rows * npg * w.g * 512, peak))
-    dec.step(q, 0)
-    torch.cuda.synchronize()
-    sel = int(dec.count.sum())
-    ms = _time_graph(_graph(lambda: B.dsa_score_pages(cache.kv, q, dec.meta, B.DSA_META_MINMAX,
-                                                      w.logical_page, dec.scores)), flush)
-    out.append(_entry("A2", w.name, "dsa_score_pages MINMAX logical pages (dense heads)", ms,
-                      dense * npg * w.g * 512 + q.numel() * 2 + rows * dec.stride * 4, peak))
-    ms = _time_graph(_graph(lambda: B.dsa_select_hier(dec.scores, dec.stride, w.g, w.k, dec.idx,
-                                                      dec.count)), flush)
-    out.append(_entry("A4", w.name, "dsa_select_hier g=4 k=64 of 2048", ms,
-                      rows * dec.stride * 4 + rows * w.k * 4, peak))
-    ms = _time_graph(_graph(lambda: B.dsa_sparse_decode_attn(
-        cache.kv, q, dec.idx, dec.count, dec.scale, dec.out, dec.m, dec.l,
-        workspace=dec.workspace)), flush)
-    out.append(_entry("A6", w.name, "dsa_sparse_decode_attn dense heads (persistent split-K)",
-                      ms, sel * w.page_size * KVP + q.numel() * 2, peak, pages=sel))
-    ms = _time_graph(_graph(lambda: B.dsa_streaming_head_attn(
-        cache.kv, q, w.sink, w.local, dec.scale, dec.out, dec.m, dec.l)), flush)
-    out.append(_entry("A7", w.name, "dsa_streaming_head_attn 64 sink + 256 local", ms,
-                      stream_rows * (w.sink + w.local) * KVP + q.numel(), peak))
-    ms0 = _time_graph(_graph(lambda: dec.step(q, 0)), flush)
-    out.append(_entry("step", w.name, "selection step (score + hier select + attention)", ms0,
-                      dense * npg * w.g * 512 + sel * w.page_size * KVP
-                      + stream_rows * (w.sink + w.local) * KVP, peak))
-    ms1 = _time_graph(_graph(lambda: dec.step(q, 1)), flush)
-    out.append(_entry("A8", w.name, "reuse step (attention with the reused selection)", ms1,
-                      sel * w.page_size * KVP + stream_rows * (w.sink + w.local) * KVP, peak))
-    del dec, cache, inp
-    torch.cuda.empty_cache()
+    if only in (None, "lserve_hier"):
+        # ---- LServe hierarchical paging + streaming heads
+        w = BY_NAME["lserve_hier"]
+        inp = make_inputs(w, dev, shuffle_pages=False)
+        cache = Cache.from_inputs(inp, dev)
+        dec = HierDecoder(cache, w.k, w.logical_page, w.sink, w.local, w.reuse)
+        q = inp["q"][0].clone()
+        rows, npg = w.batch * w.num_kv_heads, w.pages_per_seq
+        dense = w.batch * (w.num_kv_heads - len(w.streaming_kv_heads))
+        stream_rows = rows - dense
+        ms = _time_graph(_graph(dec.build_meta), flush)
+        out.append(_entry("A1", w.name, "dsa_build_page_meta MINMAX (logical 16 in physical 64)",
+                          ms, rows * npg * w.page_size * 256 + rows * npg * w.g * 512, peak))
+        dec.step(q, 0)
+        torch.cuda.synchronize()
+        sel = int(dec.count.sum())
+        ms = _time_graph(_graph(lambda: B.dsa_score_pages(cache.kv, q, dec.meta, B.DSA_META_MINMAX,
+                                                          w.logical_page, dec.scores)), flush)
+        out.append(_entry("A2", w.name, "dsa_score_pages MINMAX logical pages (dense heads)", ms,
+                          dense * npg * w.g * 512 + q.numel() * 2 + rows * dec.stride * 4, peak))
+        ms = _time_graph(_graph(lambda: B.dsa_select_hier(dec.scores, dec.stride, w.g, w.k, dec.idx,
+                                                          dec.count)), flush)
+        out.append(_entry("A4", w.name, "dsa_select_hier g=4 k=64 of 2048", ms,
+                          rows * dec.stride * 4 + rows * w.k * 4, peak))
+        ms = _time_graph(_graph(lambda: B.dsa_sparse_decode_attn(
+            cache.kv, q, dec.idx, dec.count, dec.scale, dec.out, dec.m, dec.l,
+            workspace=dec.workspace)), flush)
+        out.append(_entry("A6", w.name, "dsa_sparse_decode_attn dense heads (persistent split-K)",
+                          ms, sel * w.page_size * KVP + q.numel() * 2, peak, pages=sel))
+        ms = _time_graph(_graph(lambda: B.dsa_streaming_head_attn(
+            cache.kv, q, w.sink, w.local, dec.scale, dec.out, dec.m, dec.l)), flush)
+        out.append(_entry("A7", w.name, "dsa_streaming_head_attn 64 sink + 256 local", ms,
+                          stream_rows * (w.sink + w.local) * KVP + q.numel(), peak))
+        ms0 = _time_graph(_graph(lambda: dec.step(q, 0)), flush)
+        out.append(_entry("step", w.name, "selection step (score + hier select + attention)", ms0,
+                          dense * npg * w.g * 512 + sel * w.page_size * KVP
+                          + stream_rows * (w.sink + w.local) * KVP, peak))
+        ms1 = _time_graph(_graph(lambda: dec.step(q, 1)), flush)
+        out.append(_entry("A8", w.name, "reuse step (attention with the reused selection)", ms1,
+                          sel * w.page_size * KVP + stream_rows * (w.sink + w.local) * KVP, peak))
+        del dec, cache, inp
+        torch.cuda.empty_cache()
 
-    # ---- PSA progressive threshold
-    w = BY_NAME["psa_threshold"]
-    inp = make_inputs(w, dev, shuffle_pages=False)
-    cache = Cache.from_inputs(inp, dev)
-    dec = ThresholdDecoder(cache, w.tau, w.cap)
-    q = inp["q"][0].clone()
-    rows, npg = w.batch * w.num_kv_heads, w.pages_per_seq
-    ms = _time_graph(_graph(dec.build_meta), flush)
-    out.append(_entry("A1", w.name, "dsa_build_page_meta MEAN", ms,
-                      rows * npg * w.page_size * 256 + rows * npg * 512, peak))
-    dec.step(q)
-    torch.cuda.synchronize()
-    visited = int(dec.count.sum())
-    ms = _time_graph(_graph(lambda: B.dsa_score_pages(cache.kv, q, dec.meta, B.DSA_META_MEAN,
-                                                      w.page_size, dec.scores)), flush)
-    out.append(_entry("A2", w.name, "dsa_score_pages MEAN", ms,
-                      rows * npg * 512 + q.numel() * 2 + rows * dec.stride * 4, peak))
-    ms = _time_graph(_graph(lambda: B.dsa_select_threshold(
-        cache.kv, q, dec.scores, w.tau, w.cap, dec.scale, dec.idx, dec.count, dec.out, dec.m,
-        dec.l)), flush)
-    out.append(_entry("A5", w.name, "dsa_select_threshold tau=0.95 (rank, attend, stop)", ms,
-                      rows * npg * 4 + visited * w.page_size * KVP + q.numel() * 6, peak,
-                      mean_blocks=round(visited / rows, 2)))
-    ms = _time_graph(_graph(lambda: dec.step(q)), flush)
-    out.append(_entry("step", w.name, "score + threshold selection", ms,
-                      rows * npg * 516 + visited * w.page_size * KVP, peak))
-    del dec, cache, inp
-    torch.cuda.empty_cache()
+    if only in (None, "psa_threshold"):
+        # ---- PSA progressive threshold
+        w = BY_NAME["psa_threshold"]
+        inp = make_inputs(w, dev, shuffle_pages=False)
+        cache = Cache.from_inputs(inp, dev)
+        dec = ThresholdDecoder(cache, w.tau, w.cap)
+        q = inp["q"][0].clone()
+        rows, npg = w.batch * w.num_kv_heads, w.pages_per_seq
+        ms = _time_graph(_graph(dec.build_meta), flush)
+        out.append(_entry("A1", w.name, "dsa_build_page_meta MEAN", ms,
+                          rows * npg * w.page_size * 256 + rows * npg * 512, peak))
+        dec.step(q)
+        torch.cuda.synchronize()
+        visited = int(dec.count.sum())
+        ms = _time_graph(_graph(lambda: B.dsa_score_pages(cache.kv, q, dec.meta, B.DSA_META_MEAN,
+                                                          w.page_size, dec.scores)), flush)
+        out.append(_entry("A2", w.name, "dsa_score_pages MEAN", ms,
+                          rows * npg * 512 + q.numel() * 2 + rows * dec.stride * 4, peak))
+        ms = _time_graph(_graph(lambda: B.dsa_select_threshold(
+            cache.kv, q, dec.scores, w.tau, w.cap, dec.scale, dec.idx, dec.count, dec.out, dec.m,
+            dec.l)), flush)
+        out.append(_entry("A5", w.name, "dsa_select_threshold tau=0.95 (rank, attend, stop)", ms,
+                          rows * npg * 4 + visited * w.page_size * KVP + q.numel() * 6, peak,
+                          mean_blocks=round(visited / rows, 2)))
+        ms = _time_graph(_graph(lambda: dec.step(q)), flush)
+        out.append(_entry("step", w.name, "score + threshold selection", ms,
+                          rows * npg * 516 + visited * w.page_size * KVP, peak))
+        del dec, cache, inp
+        torch.cuda.empty_cache()
 
-    # ---- tiny top-K (the oracle-scale case)
-    w = BY_NAME["tiny_topk"]
-    inp = make_inputs(w, dev, shuffle_pages=False)
-    cache = Cache.from_inputs(inp, dev)
-    dec = TopKDecoder(cache, w.k, w.logical_page)
-    dec.build_meta()
-    q = inp["q"][0].clone()
-    ms = _time_graph(_graph(lambda: dec.step(q)), flush)
-    out.append(_entry("step", w.name, "score + top-32 + attention", ms,
-                      w.pages_per_seq * 512 + w.k * w.page_size * KVP, peak))
-    del dec, cache, inp
-    torch.cuda.empty_cache()
+    if only in (None, "tiny_topk"):
+        # ---- tiny top-K (the oracle-scale case)
+        w = BY_NAME["tiny_topk"]
+        inp = make_inputs(w, dev, shuffle_pages=False)
+        cache = Cache.from_inputs(inp, dev)
+        dec = TopKDecoder(cache, w.k, w.logical_page)
+        dec.build_meta()
+        q = inp["q"][0].clone()
+        ms = _time_graph(_graph(lambda: dec.step(q)), flush)
+        out.append(_entry("step", w.name, "score + top-32 + attention", ms,
+                          w.pages_per_seq * 512 + w.k * w.page_size * KVP, peak))
+        del dec, cache, inp
+        torch.cuda.empty_cache()
     return out
 
 
@@ -725,6 +734,17 @@ def main():
               "256 MiB read of a second buffer) before every timed step, outside the timed window",
               "timing": "CUDA graph of one decode step, CUDA events on the launching stream; a "
               "~50 us GPU spin is queued before each flush so the window never waits on the host"}
+
+    if args.rows_only is not None:
+        import torch
+
+        if args.rows_only not in ("llama3_8b_layer", "lserve_hier", "psa_threshold", "tiny_topk"):
+            raise SystemExit(f"--rows-only: no rows for {args.rows_only}")
+        dev = torch.device("cuda", torch.cuda.current_device())
+        peak, _ = load_peaks()
+        rows = bench_rows(dev, L2Flush(dev), peak, only=args.rows_only)
+        print(json.dumps({"rows": rows}))
+        return
 
     if args.impl == "reference":
         if rank != 0:

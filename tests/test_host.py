@@ -277,3 +277,14 @@ def test_kv8_unpack_reads_the_documented_layout():
     np.testing.assert_array_equal(v8.numpy(), vc)
     np.testing.assert_array_equal(ks8.numpy(), ks)
     np.testing.assert_array_equal(vs8.numpy(), vs)
+
+
+def test_bench_rows_only_rejects_unknown_workload():
+    """``bench.py --rows-only`` accepts the four row workloads and refuses anything else before it
+    touches a GPU."""
+    sys.path.insert(0, ROOT)
+    import bench
+    assert bench.parse_args(["--rows-only", "llama3_8b_layer"]).rows_only == "llama3_8b_layer"
+    r = subprocess.run([sys.executable, os.path.join(ROOT, "bench.py"), "--rows-only", "prr_512k"],
+                       capture_output=True, text=True, timeout=300)
+    assert r.returncode != 0 and "no rows for prr_512k" in r.stderr
