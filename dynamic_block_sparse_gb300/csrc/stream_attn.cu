@@ -733,15 +733,14 @@ __global__ void __launch_bounds__(kSThreads, 1)
       }
       const float o = Lsum > 0.f ? acc / Lsum : 0.f;
       const float mn = Lsum > 0.f ? M * kLn2 : -INFINITY;
-      if (dry) {
-      } else if (!cut) {
+      if (!dry && !cut) {  // the rehearsal writes nothing
         const size_t qh = static_cast<size_t>(b) * kv.Hq + static_cast<size_t>(h) * G + g;
         a.out[qh * kHeadDim + d] = o;
         if (d == 0) {
           a.m[qh] = mn;
           a.l[qh] = Lsum;
         }
-      } else {
+      } else if (!dry) {
         float* rec = rec0 + g * kRecordFloats;
         rec[d] = o;
         if (d == 0) {
