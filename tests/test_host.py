@@ -288,3 +288,34 @@ def test_bench_rows_only_rejects_unknown_workload():
     r = subprocess.run([sys.executable, os.path.join(ROOT, "bench.py"), "--rows-only", "prr_512k"],
                        capture_output=True, text=True, timeout=300)
     assert r.returncode != 0 and "no rows for prr_512k" in r.stderr
+
+
+def test_stream_k_cut_geometry():
+    """The persistent attention's stream-K bookkeeping, restated: CTA c of n holds the slots
+    [c T / n, (c + 1) T / n) of T, and slot x belongs to CTA ((x + 1) n - 1) / T.  A row (unit) is
+    cut exactly when it reaches outside the CTA's own range, and the record a cut row leaves in CTA
+    c sits in slot 0 unless c is the row's first CTA and starts before the row: there the row is
+    c's last unit of several, slot 1.  Checked against the division-based definitions."""
+    r = np.random.default_rng(17)
+    for _ in range(300):
+        rows = int(r.integers(1, 40))
+        stride = int(r.integers(1, 300))
+        T = rows * stride
+        n = int(min(r.integers(1, 153), T))
+        start = lambda c: c * T // n
+        owner = lambda x: ((x + 1) * n - 1) // T
+        for c in range(n):
+            beg, end = start(c), start(c + 1)
+            assert owner(beg) == c and owner(end - 1) == c
+            units = list(range(beg // stride, (end - 1) // stride + 1))
+            for u, row in enumerate(units):
+                rs = row * stride
+                cut_by_owner = owner(rs) != owner(rs + stride - 1)
+                cut_by_range = rs < beg or rs + stride > end
+                assert cut_by_owner == cut_by_range
+                if not cut_by_range:
+                    continue
+                writer_slot = 0 if u == 0 else 1       # what CTA c writes
+                c_first = owner(rs)
+                reader_slot = 1 if (c == c_first and start(c_first) < rs) else 0
+                assert reader_slot == writer_slot
