@@ -30,6 +30,7 @@ constexpr int kSW = 8;                     // consumer warps
 constexpr int kSThreads = (kSW + 1) * 32;  // + one TMA producer warp
 constexpr int kSConsumers = kSW * 32;
 constexpr int kSMaxHeads = 1024;           // KV heads the dense-head table can hold
+constexpr int kUnitPadTokens = 128;        // empty slots per dense row, in tokens of pages
 constexpr int kIssueLanes = 4;             // producer lanes issuing page loads at once
 
 struct SLayout {
@@ -339,10 +340,15 @@ __global__ void __launch_bounds__(kSThreads, 1)
   __syncthreads();
   const int nd_heads = *n_dense_heads;
   const int ns_heads = STREAMING ? *n_stream_heads : 0;
-  // The slot space: every dense row's idx_stride selection slots, then (when streaming heads are
-  // served) every streaming row's stream_stride slots, one per page of its sink and local tokens.
-  // A unit is one row's slots; units are numbered dense rows first.
-  const int stride = a.idx_stride, sstride = a.stream_stride;
+  // The slot space: every dense row's idx_stride selection slots followed by `pad` empty slots,
+  // then (when streaming heads are served) every streaming row's stream_stride slots, one per page
+  // of its sink and local tokens.  A unit is one row's slots; units are numbered dense rows first.
+  // The empty slots (about 128 tokens' worth of pages) charge each row boundary for the unit
+  // epilogue it costs: a CTA holding two units gets that many fewer pages, instead of finishing
+  // one epilogue later than the CTAs holding one.
+  const int istride = a.idx_stride;  // selection slots per dense row (the idx row stride)
+  const int pad = max(1, kUnitPadTokens / page);
+  const int stride = istride + pad, sstride = a.stream_stride;
   const int Nd = kv.B * nd_heads;
   const long long Td = static_cast<long long>(Nd) * stride;
   const long long T = Td + static_cast<long long>(kv.B) * ns_heads * sstride;
@@ -401,9 +407,10 @@ __global__ void __launch_bounds__(kSThreads, 1)
       const long long ue0 = us0 + unit_stride(d_first);
       const int cap_end = static_cast<int>((my_end < ue0 ? my_end : ue0) - us0);
       if (!STREAMING || d_first < Nd) {
-        const int32_t* sel0 = a.idx + static_cast<size_t>(row0) * stride;
-        if (spec_base + lane < cap_end) spec_a = sel0[spec_base + lane];
-        if (spec_base + 32 + lane < cap_end) spec_b = sel0[spec_base + 32 + lane];
+        const int sel_end = min(cap_end, istride);  // the empty slots have no selection entry
+        const int32_t* sel0 = a.idx + static_cast<size_t>(row0) * istride;
+        if (spec_base + lane < sel_end) spec_a = sel0[spec_base + lane];
+        if (spec_base + 32 + lane < sel_end) spec_b = sel0[spec_base + 32 + lane];
       } else {  // a streaming unit's positions follow from its length
         int sn, f2;
         stream_geom(request_len(kv, row0 / kv.Hkv), &sn, &f2);
@@ -427,7 +434,7 @@ __global__ void __launch_bounds__(kSThreads, 1)
           t_kind = STREAMING && di >= Nd;
           int sn, f2;
           const int cnt = t_kind ? min(stream_geom(t_len, &sn, &f2), us)
-                                 : min(max(a.count[t_row], 0), stride);
+                                 : min(max(a.count[t_row], 0), istride);
           t_beg = min(pb, cnt);
           t_end = min(pe, cnt);
         }
@@ -490,7 +497,7 @@ __global__ void __launch_bounds__(kSThreads, 1)
           }
         }
         if (j >= e) return -1;
-        return a.idx[static_cast<size_t>(row) * stride + j];
+        return a.idx[static_cast<size_t>(row) * istride + j];
       };
       // raw page-table entry of a position inside the request, -1 outside
       auto load_phys = [&](int u, int pos) -> int {
