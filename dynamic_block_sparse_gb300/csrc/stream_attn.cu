@@ -500,6 +500,13 @@ __global__ void __launch_bounds__(kSThreads, 1)
         return a.idx[static_cast<size_t>(row) * istride + j];
       };
       // raw page-table entry of a position inside the request, -1 outside
+      // whether position pos lies inside unit u's request (its page-table entry is then read and
+      // must name a physical page: a bad entry, negative or too large, raises the status)
+      auto pos_in = [&](int u, int pos) -> bool {
+        if (u >= ue) return false;
+        const int len = __shfl_sync(0xffffffffu, t_len, u - ub);
+        return pos >= 0 && pos < (len + page - 1) / page;
+      };
       auto load_phys = [&](int u, int pos) -> int {
         if (u >= ue) return -1;
         const int row = __shfl_sync(0xffffffffu, t_row, u - ub);
@@ -525,10 +532,12 @@ __global__ void __launch_bounds__(kSThreads, 1)
       }
       for (; uq <= ua && uq < ue && !stopped; ++uq) stopped = !publish(uq);
       int raw_a = load_phys(ua, pos_a);
+      bool in_a = pos_in(ua, pos_a);
       while (ua < ue && !stopped) {
         seek(ubb, bb + 32, &uc, &bc);
         const int pos_c = load_sel(uc, bc);
         const int raw_b = load_phys(ubb, pos_b);
+        const bool in_b = pos_in(ubb, pos_b);
         for (; uq <= ua && uq < ue && !stopped; ++uq) stopped = !publish(uq);
         if (stopped) break;
         // issue chunk A
@@ -536,8 +545,8 @@ __global__ void __launch_bounds__(kSThreads, 1)
         const int e = __shfl_sync(0xffffffffu, t_end, ua - ub);
         const int h = row % kv.Hkv;
         const int nb = min(32, e - ba);
-        const bool in_range = pos_a >= 0 && raw_a >= 0;  // position inside the request
-        const bool ok = in_range && raw_a < kv.num_phys;
+        const bool in_range = in_a;  // position inside the request
+        const bool ok = in_range && raw_a >= 0 && raw_a < kv.num_phys;
         if (in_range && !ok) raise_status(kv.status, DSA_STATUS_BAD_PAGE);
         for (int q0 = 0; q0 < nb; q0 += NL) {
           const int src = min(31, q0 + (lane < NL ? lane : 0));
@@ -580,6 +589,7 @@ __global__ void __launch_bounds__(kSThreads, 1)
         ba = bb;
         pos_a = pos_b;
         raw_a = raw_b;
+        in_a = in_b;
         ubb = uc;
         bb = bc;
         pos_b = pos_c;

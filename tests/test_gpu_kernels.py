@@ -785,24 +785,48 @@ def test_select_threshold(tau, cap, nleft, G):
 
 # ---------------------------------------------------------------------------------- robustness
 
-def test_bad_page_ids_raise_status_without_fault():
-    w, inp, cache = small(Hq=8, Hkv=2, page=16, L=16 * 20)
+@pytest.mark.parametrize("bad", ["negative", "too_large"])
+@pytest.mark.parametrize("path", ["meta", "score", "persistent", "splits", "page_partials",
+                                  "streaming"])
+def test_bad_page_id_raises_status_without_fault(bad, path):
+    """One bad page-table entry inside a request (negative, or past the pool) per call: the call
+    raises DSA_STATUS_BAD_PAGE, skips the page and leaves finite outputs."""
+    w, inp, cache = small(Hq=8, Hkv=2, page=16, L=16 * 20, streaming=(1,))
     table = inp["page_table"].clone()
-    table[0, 3] = cache.num_phys_pages + 11
-    table[1, 0] = -4
-    kv = B.paged_kv(inp["k_pages"], inp["v_pages"], table, inp["seq_lens"], 8, None, cache.status)
+    table[1, 0] = -4 if bad == "negative" else cache.num_phys_pages + 11
+    status = torch.zeros(1, dtype=torch.int32, device="cuda")
+    strm = inp["head_is_streaming"] if path == "streaming" else None
+    kv = B.paged_kv(inp["k_pages"], inp["v_pages"], table, inp["seq_lens"], 8, strm, status)
     meta = cache.meta_buffer(B.DSA_META_MINMAX, 16)
-    B.dsa_build_page_meta(kv, B.DSA_META_MINMAX, 16, meta)
-    idx = torch.tensor([[[3, 4]] * 2] * 2, dtype=torch.int32, device="cuda")
-    idx[1, :, 0] = 0
-    cnt = torch.full((2, 2), 2, dtype=torch.int32, device="cuda")
     out, m, l = cache.outputs()
-    ws = torch.empty(max(16, B.dsa_sparse_decode_attn_workspace_size(kv, 2)), dtype=torch.uint8,
-                     device="cuda")
-    B.dsa_sparse_decode_attn(kv, inp["q"][0], idx, cnt, 0.1, out, m, l, workspace=ws)
+    idx = torch.tensor([[[3, 4]] * 2, [[0, 1]] * 2], dtype=torch.int32, device="cuda")
+    cnt = torch.full((2, 2), 2, dtype=torch.int32, device="cuda")
+    if path == "meta":
+        B.dsa_build_page_meta(kv, B.DSA_META_MINMAX, 16, meta)
+    else:  # metadata from the intact table (its own status word)
+        B.dsa_build_page_meta(cache.kv, B.DSA_META_MINMAX, 16, meta)
+    elif path == "score":
+        scores = torch.empty((2, 2, table.shape[1]), dtype=torch.float32, device="cuda")
+        B.dsa_score_pages(kv, inp["q"][0], meta, B.DSA_META_MINMAX, 16, scores)
+        torch.cuda.synchronize()
+        assert torch.isinf(scores[1, :, 0]).all() and (scores[1, :, 0] < 0).all()
+    elif path == "streaming":
+        B.dsa_streaming_head_attn(kv, inp["q"][0], 16, 32, 0.1, out, m, l)
+    else:
+        splits = {"persistent": 0, "splits": 2, "page_partials": 1}[path]
+        parts = None
+        if path == "page_partials":
+            parts = torch.zeros((2, 2, 2, 4, 132), dtype=torch.float32, device="cuda")
+        ws = torch.empty(max(16, B.dsa_sparse_decode_attn_workspace_size(kv, 2, splits)),
+                         dtype=torch.uint8, device="cuda")
+        B.dsa_sparse_decode_attn(kv, inp["q"][0], idx, cnt, 0.1, out, m, l,
+                                 page_partials=parts, num_splits=splits, workspace=ws)
+        if parts is not None:
+            torch.cuda.synchronize()
+            assert torch.isfinite(parts[..., :128]).all() and torch.isfinite(parts[..., 129]).all()
     torch.cuda.synchronize()
-    assert int(cache.status.item()) & B.DSA_STATUS_BAD_PAGE
-    assert torch.isfinite(out).all()
+    assert int(status.item()) == B.DSA_STATUS_BAD_PAGE
+    assert torch.isfinite(out).all() and torch.isfinite(l).all()
 
 
 def test_host_errors_are_reported():

@@ -15,6 +15,7 @@ import pytest
 import torch
 
 import oracle as O
+import oracle.dsa_oracle as OD
 
 GOLDEN = os.path.join(os.path.dirname(__file__), "golden")
 rng = np.random.default_rng
@@ -295,6 +296,30 @@ def test_psa_tau_one_visits_everything_and_equals_dense():
     np.testing.assert_allclose(res["O_fused"], _sdpa(q, K, V, 0.125), rtol=1e-12, atol=1e-12)
 
 
+def _gqa_psa_row():
+    gold = json.load(open(os.path.join(GOLDEN, "psa_gqa_stop.json")))
+    a = np.asarray(gold["masses_head0"], dtype=np.float64)
+    n = len(a)
+    q = np.array([[1.0, 0.0], [0.0, 1.0]])
+    K = np.stack([np.log(a), np.zeros(n)], axis=1)
+    V = rng(5).normal(size=(n, 2))
+    scores = np.arange(n, 0, -1, dtype=np.float64)      # visit in index order
+    return gold, q, K, V, scores
+
+
+def test_psa_group_stops_when_every_head_satisfies_the_rule():
+    """A group of two query heads on one KV head: one head satisfies the stop rule after 4 blocks,
+    the other after 9; the walk stops after 9 (tests/golden/psa_gqa_stop.json)."""
+    gold, q, K, V, scores = _gqa_psa_row()
+    n = len(scores)
+    res = O.psa_progressive(q, K, V, scores, 1, n, gold["tau"], 100, 1.0)
+    assert res["ranked"] == list(range(gold["stop_blocks_every_head"]))
+    np.testing.assert_allclose(res["ratios"][-1], [gold["ratio_head0_at_stop"],
+                                                   gold["ratio_head1_at_stop"]], rtol=1e-12)
+    np.testing.assert_allclose(res["ratios"][3][0], 15 / 16, rtol=1e-12)
+    np.testing.assert_allclose(res["ratios"][7][1], 8 / 9, rtol=1e-12)
+
+
 @pytest.mark.parametrize("tau,cap", [(0.95, 100), (0.99, 5), (0.8, 100)])
 def test_psa_fused_output_is_attention_over_visited_blocks(tau, cap):
     """PSA §3.2 weighted fusion is exact: it equals softmax attention over the union of visited
@@ -389,6 +414,19 @@ def test_calibration_prefers_trend_when_rankings_cross():
     assert max(Hs) > level_only + 0.05
 
 
+def test_calibration_hand_derived_hit_rates():
+    """H of two grid points on a 3-step, 5-page trajectory, worked by hand
+    (tests/golden/ema_calibration_hand.json): the mean over steps 1..T-1 of the covered share of
+    the true set's score mass."""
+    gold = json.load(open(os.path.join(GOLDEN, "ema_calibration_hand.json")))
+    traj = [np.asarray(x, dtype=np.float64) for x in gold["trajectory"]]
+    _, Hs = O.calibrate_ema(traj, gold["k"], gold["k_pred"])
+    grid = O.calibration_grid()
+    for c, h in gold["H"].items():
+        np.testing.assert_allclose(grid[int(c)], gold["points"][c], rtol=1e-12)
+        assert abs(Hs[int(c)] - h) < 1e-12, (c, Hs[int(c)], h)
+
+
 # ------------------------------------------------------------------------------------ PRR
 
 @pytest.mark.parametrize("case", ["random", "disjoint", "superset_of_A", "equal", "empty_P"])
@@ -455,6 +493,23 @@ def test_pins_catch_planted_mistakes(monkeypatch):
 
     s = np.array([1.0, 2.0, 2.0, 0.5])
     assert sorted(sorted(range(4), key=lambda j: (-s[j], -j))[:1]) != _brute_topk(s, 1)
+
+    # PSA with a query group: stopping when ANY head satisfies the rule (instead of every head)
+    gold, q, K, V, scores = _gqa_psa_row()
+    with monkeypatch.context() as mp:
+        mp.setattr(OD.np, "all", np.any)
+        res = O.psa_progressive(q, K, V, scores, 1, len(scores), gold["tau"], 100, 1.0)
+    assert len(res["ranked"]) == gold["stop_blocks_any_head"] != gold["stop_blocks_every_head"]
+
+    # calibration: averaging over all T steps, or counting hits instead of score mass
+    cal = json.load(open(os.path.join(GOLDEN, "ema_calibration_hand.json")))
+    traj = [np.asarray(x, dtype=np.float64) for x in cal["trajectory"]]
+    _, Hs = O.calibrate_ema(traj, cal["k"], cal["k_pred"])
+    assert abs(Hs[79] * 2 / 3 - cal["H"]["79"]) > 0.05
+    with monkeypatch.context() as mp:
+        mp.setattr(OD, "score_weighted_hit", lambda P, A, IS: OD.hit_rate(P, A))
+        _, Hs_count = O.calibrate_ema(traj, cal["k"], cal["k_pred"])
+    assert abs(Hs_count[79] - cal["H"]["79"]) > 0.01
 
 
 # ------------------------------------------------------------------------------------ KV8
