@@ -801,10 +801,10 @@ def test_bad_page_id_raises_status_without_fault(bad, path):
     out, m, l = cache.outputs()
     idx = torch.tensor([[[3, 4]] * 2, [[0, 1]] * 2], dtype=torch.int32, device="cuda")
     cnt = torch.full((2, 2), 2, dtype=torch.int32, device="cuda")
+    if path != "meta":  # metadata from the intact table (its own status word)
+        B.dsa_build_page_meta(cache.kv, B.DSA_META_MINMAX, 16, meta)
     if path == "meta":
         B.dsa_build_page_meta(kv, B.DSA_META_MINMAX, 16, meta)
-    else:  # metadata from the intact table (its own status word)
-        B.dsa_build_page_meta(cache.kv, B.DSA_META_MINMAX, 16, meta)
     elif path == "score":
         scores = torch.empty((2, 2, table.shape[1]), dtype=torch.float32, device="cuda")
         B.dsa_score_pages(kv, inp["q"][0], meta, B.DSA_META_MINMAX, 16, scores)
