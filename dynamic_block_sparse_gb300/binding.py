@@ -90,6 +90,7 @@ _SIGNATURES = {
     "dsa_calibrate_ema_workspace_size": ([_I, _I, _I, _I], c_size_t),
     "dsa_prr_step": ([_P, _P, _P, c_size_t, _P], _I),
     "dsa_prr_step_workspace_size": ([_P], c_size_t),
+    "dsa_prr_step_counter_bytes": ([_P], c_size_t),
 }
 
 _lib = None
@@ -375,6 +376,10 @@ def dsa_merge_partials(partials, out, m, l, stream=None):
 
 def dsa_prr_step_workspace_size(kv: PagedKV) -> int:
     return int(load().dsa_prr_step_workspace_size(ctypes.byref(kv)))
+
+
+def dsa_prr_step_counter_bytes(kv: PagedKV) -> int:
+    return int(load().dsa_prr_step_counter_bytes(ctypes.byref(kv)))
 
 
 def dsa_prr_step(kv: PagedKV, q, meta, scores, ell, trend, alpha: float, beta: float,

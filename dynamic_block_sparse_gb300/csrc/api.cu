@@ -840,8 +840,13 @@ int dsa_sparse_decode_attn_noalloc(const dsa_paged_kv* kv, const void* q, const 
 }
 
 size_t dsa_prr_step_workspace_size(const dsa_paged_kv* kv) {
+  if (!kv || kv->batch <= 0 || kv->num_kv_heads <= 0 || kv->max_pages_per_seq <= 0) return 0;
+  return prr_step_workspace_bytes(kv->batch * kv->num_kv_heads, kv->max_pages_per_seq);
+}
+
+size_t dsa_prr_step_counter_bytes(const dsa_paged_kv* kv) {
   if (!kv || kv->batch <= 0 || kv->num_kv_heads <= 0) return 0;
-  return prr_step_workspace_bytes(kv->batch * kv->num_kv_heads);
+  return prr_step_counter_bytes(kv->batch * kv->num_kv_heads);
 }
 
 int dsa_prr_step(const dsa_paged_kv* kv, const dsa_prr_step_args* args, void* workspace,
@@ -867,17 +872,17 @@ int dsa_prr_step(const dsa_paged_kv* kv, const dsa_prr_step_args* args, void* wo
     return fail(DSA_ERR_INVALID_ARG, "dsa_prr_step: next_idx/next_count must not alias P_t");
   if (!aligned(x.q, 16) || !aligned(x.meta, 16) || !aligned(x.page_partials, 16))
     return fail(DSA_ERR_ALIGNMENT, "dsa_prr_step: q, meta and page_partials must be 16-byte aligned");
-  const size_t ws_need = prr_step_workspace_bytes(v.B * v.Hkv);
+  const size_t ws_need = prr_step_workspace_bytes(v.B * v.Hkv, v.max_pages);
   if (!workspace || workspace_bytes < ws_need)
     return fail(DSA_ERR_WORKSPACE, "workspace of %zu bytes needed", ws_need);
   if (!aligned(workspace, 16)) return fail(DSA_ERR_ALIGNMENT, "workspace must be 16-byte aligned");
-  if (prr_step_smem_bytes(v.p, v.G, x.stride, x.k, x.k_pred) > 200 * 1024)
-    return fail(DSA_ERR_UNSUPPORTED, "dsa_prr_step: shape needs too much shared memory");
   int dev = 0, coop = 0;
   cudaError_t e = cudaGetDevice(&dev);
   if (e == cudaSuccess) e = cudaDeviceGetAttribute(&coop, cudaDevAttrCooperativeLaunch, dev);
   if (e != cudaSuccess) return cuda_fail(e, "dsa_prr_step device query");
   if (!coop) return fail(DSA_ERR_UNSUPPORTED, "dsa_prr_step: the device has no cooperative launch");
+  if (prr_step_smem_bytes(v.p, x.stride, x.k_pred) > kPrrSmemLimit)
+    return fail(DSA_ERR_UNSUPPORTED, "dsa_prr_step: shape needs too much shared memory");
   CUtensorMap tk, tv;
   if ((rc = pool_map(kv->k_pages, kv, &tk)) || (rc = pool_map(kv->v_pages, kv, &tv))) return rc;
   PrrStepArgs a = {};
@@ -908,18 +913,7 @@ int dsa_prr_step(const dsa_paged_kv* kv, const dsa_prr_step_args* args, void* wo
   a.out = x.out;
   a.m = x.m;
   a.l = x.l;
-  a.sync = static_cast<unsigned*>(workspace);
-  {
-    const size_t rows = static_cast<size_t>(v.B) * v.Hkv;
-    const size_t cnt = (4 * rows + 15) & ~static_cast<size_t>(15);
-    const size_t list = rows * 512 * sizeof(uint2);
-    char* w = static_cast<char*>(workspace) + 256;
-    a.cand_cnt = reinterpret_cast<unsigned*>(w);
-    a.cand = reinterpret_cast<uint2*>(w + cnt);
-    a.cand_cnt2 = reinterpret_cast<unsigned*>(w + cnt + list);
-    a.cand2 = reinterpret_cast<uint2*>(w + 2 * cnt + list);
-  }
-  e = launch_prr_step(tk, tv, a, static_cast<cudaStream_t>(stream));
+  e = launch_prr_step(tk, tv, a, workspace, static_cast<cudaStream_t>(stream));
   return e == cudaSuccess ? ok() : cuda_fail(e, "dsa_prr_step launch");
 }
 

@@ -125,6 +125,8 @@ cudaError_t launch_stream_attn(const CUtensorMap& tmK, const CUtensorMap& tmV,
                                const StreamAttnArgs& a, int grid, cudaStream_t s);
 
 // One PRR decode step in one cooperative launch (prr_step.cu).
+constexpr int kPrrPredMax = 256;   // bound of k and k_pred
+constexpr size_t kPrrSmemLimit = 227 * 1024;
 struct PrrStepArgs {
   KvView kv;
   const __nv_bfloat16* kpool;
@@ -151,17 +153,15 @@ struct PrrStepArgs {
   float* out;
   float* m;
   float* l;
-  unsigned* sync;      // 3 words, zero on entry, left zero
-  unsigned* cand_cnt;   // [rows], zero on entry, left zero
-  uint2* cand;          // [rows][512]
-  unsigned* cand_cnt2;  // [rows], zero on entry, left zero
-  uint2* cand2;         // [rows][512]
 };
-size_t prr_step_smem_bytes(int page, int G, int n, int k, int k_pred);
-// sync words, then for A_t and for P_{t+1}: candidate counts, candidate lists
-size_t prr_step_workspace_bytes(int rows);
+// shared memory of one launch (SIZE_MAX when no ring depth fits)
+size_t prr_step_smem_bytes(int page, int n, int k_pred);
+// workspace: per-row counters first (prr_step_counter_bytes of them, zero on entry, left zero),
+// then the new predictions [rows][max_pages]
+size_t prr_step_workspace_bytes(int rows, int max_pages);
+size_t prr_step_counter_bytes(int rows);
 cudaError_t launch_prr_step(const CUtensorMap& tmK, const CUtensorMap& tmV, const PrrStepArgs& a,
-                            cudaStream_t s);
+                            void* workspace, cudaStream_t s);
 
 // metadata and scoring
 cudaError_t launch_build_meta(const KvView& kv, const __nv_bfloat16* k_pages, int kind, int lp,

@@ -368,9 +368,10 @@ size_t dsa_calibrate_ema_workspace_size(int32_t steps, int32_t rows, int32_t n, 
  *   dsa_ema_predict_update(scores, DSA_EMA_UPDATE, k_pred)                  -> ell, trend, pred,
  *                                                                              next_idx/next_count
  *   dsa_repair_merge(P_t, page_partials, A_t, superset)                     -> out/m/l
- * with scores, A_t, the EMA state and P_{t+1} bit for bit and out/m/l up to fp32 rounding.  The
- * speculative attention and the scoring run side by side on every SM; selection, prediction and
- * repair follow after on-device grid barriers (a cooperative launch of one CTA per SM).
+ * with scores, A_t, the EMA state and P_{t+1} bit for bit and out/m/l up to fp32 rounding.  One
+ * cooperative launch of one CTA per SM; no CTA waits for the whole grid: every CTA scores an equal
+ * share of the (request, KV head, page) slots beside its pages of P_t, and the selections, the
+ * repair and the merges wait only for their own row's counters.
  *   args->q            : bf16 [B][Hq][D], 16-byte aligned.  Device memory, or page-locked host
  *                        memory mapped for the device (cudaHostAlloc / cudaHostRegister): the
  *                        kernel then reads the query over the host link itself, no copy needed.
@@ -379,21 +380,24 @@ size_t dsa_calibrate_ema_workspace_size(int32_t steps, int32_t rows, int32_t n, 
  *   args->ell, trend   : fp32 [B][Hkv][stride], EMA level and trend, updated in place.
  *   args->pred (out)   : fp32 [B][Hkv][stride] or NULL.
  *   args->spec_idx/spec_count : P_t, int32 [B][Hkv][k_pred] ASCENDING and unique, int32 [B][Hkv].
- *   args->page_partials (out) : fp32 [B][Hkv][k_pred][G][D + 4], 16-byte aligned.
+ *   args->page_partials (out) : fp32 [B][Hkv][k_pred][G][D + 4], 16-byte aligned: the per-page
+ *                        records of P_t (a slot whose page lies outside the request holds the
+ *                        empty part).
  *   args->idx/count (out)     : A_t, int32 [B][Hkv][k] ascending, int32 [B][Hkv].
  *   args->next_idx/next_count (out): P_{t+1}, int32 [B][Hkv][k_pred], int32 [B][Hkv]; must not
  *                        alias spec_idx/spec_count (double-buffer them across steps).
  *   args->out/m/l (out): fp32 [B][Hq][D], [B][Hq], [B][Hq].  Like q, they may be mapped
  *                        page-locked host memory, which the kernel writes directly.
  *   1 <= k, k_pred <= 256.  kv->head_is_streaming must be NULL.
- *   workspace          : dsa_prr_step_workspace_size(kv) bytes, 16-byte aligned, ZERO-FILLED
- *                        before its first use; every call that completes leaves its counters at
- *                        zero again.  If a call raised DSA_STATUS_TIMEOUT the workspace must be
- *                        zero-filled again.
+ *   workspace          : dsa_prr_step_workspace_size(kv) bytes, 16-byte aligned.  Its first
+ *                        dsa_prr_step_counter_bytes(kv) bytes hold per-row counters and must be
+ *                        ZERO-FILLED before the first use; every call that completes leaves them
+ *                        at zero again.  If a call raised DSA_STATUS_TIMEOUT they must be
+ *                        zero-filled again.  The rest is scratch the call writes before it reads.
  * A_t is selected exactly, but its search is speculative too: T0, the k-th largest true score over
  * P_t's pages, bounds the k-th largest of all scores from below, so only the pages scoring >= T0
- * (appended while scoring) are ranked; when P_t has fewer than k scored pages, or more than 512
- * pages pass T0, every score of the row is scanned instead.
+ * are ranked (likewise P_{t+1} with the k_pred-th largest prediction over P_t); when P_t has fewer
+ * than k scored pages, or more than 512 pages pass the bound, every entry of the row is ranked.
  */
 typedef struct dsa_prr_step_args {
   const void* q;
@@ -424,6 +428,7 @@ typedef struct dsa_prr_step_args {
 int dsa_prr_step(const dsa_paged_kv* kv, const dsa_prr_step_args* args, void* workspace,
                  size_t workspace_bytes, dsa_stream_t stream);
 size_t dsa_prr_step_workspace_size(const dsa_paged_kv* kv);
+size_t dsa_prr_step_counter_bytes(const dsa_paged_kv* kv);
 
 /*
  * Log-sum-exp merge of partial records ([PRR] §3.3 recurrence, applied to all parts at once).

@@ -247,11 +247,8 @@ def _prr_fused_vs_staged(w, inp, superset):
                        [x.double().cpu().numpy() for x in (s.out, s.m, s.l)], f"step {t}")
         assert int(f.cache.status.item()) == 0
     ws = decs[0].step_workspace
-    rows = w.batch * w.num_kv_heads
-    cnt = (4 * rows + 15) // 16 * 16
-    lst = rows * 512 * 8
-    assert int(ws[:256 + cnt].sum()) == 0 and int(ws[256 + cnt + lst:256 + 2 * cnt + lst].sum()) == 0, \
-        "barrier words / candidate counts not left at zero"
+    nctr = B.dsa_prr_step_counter_bytes(decs[0].cache.kv)
+    assert nctr > 0 and int(ws[:nctr].sum()) == 0, "the step's counters were not left at zero"
 
 
 @pytest.mark.parametrize("superset", [False, True])
@@ -410,13 +407,13 @@ def test_prr_step_with_host_query_and_result():
         assert int(host.cache.status.item()) == 0
 
 
-def test_prr_step_barrier_timeout_sets_status():
-    """Failure detection without a fault: the fused step's first grid barrier is made unreachable
-    (its counter starts at 0x80000000, so the arrival of every CTA still leaves it short of the
-    target: a flag that nothing sets).  Each bounded wait gives up after its limit, the kernel
-    returns early with DSA_STATUS_TIMEOUT in the status word, and the context stays usable: with
-    the workspace and the status zeroed again, the next step selects A_t exactly as the staged
-    path does and attends over it."""
+def test_prr_step_wait_timeout_sets_status():
+    """Failure detection without a fault: every per-row counter of the fused step starts at
+    -2^30, so the increments of all CTAs still leave each one short of its target (a flag that
+    nothing sets; the waits compare counters as sequence numbers).  Each bounded wait gives up after its limit, the kernel returns early with
+    DSA_STATUS_TIMEOUT in the status word, and the context stays usable: with the counters and
+    the status zeroed again, the next step selects A_t exactly as the staged path does and attends
+    over it."""
     w = BY_NAME["prr_512k"].replace(seq_len=65536, steps=4)
     inp = make_inputs(w, "cuda")
     decs = []
@@ -431,7 +428,8 @@ def test_prr_step_barrier_timeout_sets_status():
             dec.step(inp["q"][t])
     torch.cuda.synchronize()
     ws = f.step_workspace
-    ws[:4].copy_(torch.tensor([0, 0, 0, 0x80], dtype=torch.uint8, device=ws.device))
+    nctr = B.dsa_prr_step_counter_bytes(f.cache.kv)
+    ws[:nctr].view(torch.int32).fill_(-(1 << 30))
     t0 = time.monotonic()
     f.step(inp["q"][2])
     torch.cuda.synchronize()
