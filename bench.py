@@ -6,15 +6,19 @@ KV heads, head_dim 128, block 64, top-64 true blocks, |P| = 76 predicted blocks,
 alpha 0.6 / beta 0.3 / gamma 0.5, query random walk N(0, 0.05)).  One bench step is one decode
 step of the whole path: page scoring over the kmax/kmin metadata, top-K selection, speculative
 attention over P (beside scoring), repair of A \\ P with the log-sum-exp merge, and the EMA
-update that predicts the next P -- one cooperative launch (dsa_prr_step).  The step is captured
-once as a CUDA graph and replayed; L2 is flushed before every timed step (a 256 MiB write, then a
-256 MiB read of another buffer so that no dirty flush lines are written back inside the timed
-window), outside the timed window, and a short GPU spin queued before the flush keeps the host
-ahead of the GPU, so the window never waits for the host to submit the step.
+update that predicts the next P -- one cooperative launch (dsa_prr_step).
+
+Timing.  The steps rotate over the caches of 32 layers (each layer its own K/V pools, metadata
+and predictor state; one CUDA graph holds one step of every layer), as consecutive decode steps
+of a model's layers do: each step reads what the 31 steps before it did not touch, about 430 MB
+later, far past the 129 MB L2, so its inputs come from HBM while the kernel's code stays warm.
+Exactly --steps steps are timed with CUDA events.  The single-step figure with L2 flushed before
+each step (a 256 MiB write, then a 256 MiB read of another buffer, outside the timed window;
+this also evicts the kernel's code) is reported beside it as cold_step.
 
 value = algorithmic bytes of the step / device time of the step (GB/s): metadata read by scoring
 + K/V of every page attended (P and A \\ P) + auxiliary state (query, scores, EMA level/trend,
-predictions, index lists, partial records).  ms_per_step is the same step's device time.
+predictions, index lists); the speculative partial records stay in L2 and are not counted.
 
 --impl reference times the float64 oracle (the CPU definition the CUDA path is checked against)
 on the same workload, metric and unit, on this host's cores.
@@ -185,7 +189,8 @@ def dist_env():
 def prr_bytes(w, n_valid_pages, P_pages, missed_pages):
     """Algorithmic bytes of one PRR decode step (see module docstring) for a step that attends
     ``P_pages`` speculative and ``missed_pages`` repaired (page, KV head) units summed over rows
-    (averages are fine); also the true-set form (metadata + K/V of the true set A only)."""
+    (averages are fine); also the true-set form (metadata + K/V of the true set A only) and the
+    parts (the L2-resident partial records are reported apart, not counted)."""
     rows = w.batch * w.num_kv_heads
     G, D = w.group, w.head_dim
     page_kv = w.page_size * D * 2 * 2
@@ -197,31 +202,81 @@ def prr_bytes(w, n_valid_pages, P_pages, missed_pages):
     ema = rows * n_valid_pages * 4 * 5               # level, trend read+write, prediction write
     idx = rows * (w.k + w.k_pred) * 4 * 3
     out = w.batch * w.num_q_heads * (D + 2) * 4
-    total = meta + q + kv + records + scores + ema + idx + out
+    total = meta + q + kv + scores + ema + idx + out
     true_set = meta + rows * w.k * page_kv
     aux = q + scores + ema + idx + out
-    return total, true_set, dict(meta=meta, kv=kv, records=records, aux=aux)
+    # the per-page partial records of the speculative pass stay in L2 (not counted in total)
+    return total, true_set, dict(meta=meta, kv=kv, aux=aux, records_l2=records)
 
 
 # ------------------------------------------------------------------------------------ ours
+
+N_LAYERS = 32  # layers of the timed rotation (one cache each)
+
+
+def build_layers(w, dev, n_layers):
+    """Decoders of the workload for n_layers layers, each over its own copy of the K/V pools (and
+    its own metadata, scores and predictor state), all stepped once (step 0 initialises the
+    predictor) and then three times more."""
+    import torch
+
+    from dynamic_block_sparse_gb300.pipeline import Cache, PRRDecoder
+    from dynamic_block_sparse_gb300.workloads import make_inputs
+
+    inputs = make_inputs(w, device=dev, shuffle_pages=False)
+    decs = []
+    for layer in range(n_layers):
+        inp = dict(inputs)
+        if layer > 0:
+            inp["k_pages"] = inputs["k_pages"].clone()
+            inp["v_pages"] = inputs["v_pages"].clone()
+        cache = Cache.from_inputs(inp, dev)
+        dec = PRRDecoder(cache, w.k, w.k_pred, w.alpha, w.beta, w.gamma)
+        dec.build_meta()
+        decs.append(dec)
+    qs = inputs["q"]
+    static_q = qs[0].clone()
+    for i in range(4):
+        static_q.copy_(qs[i % qs.shape[0]])
+        for dec in decs:
+            dec.step(static_q)
+    torch.cuda.synchronize()
+    return inputs, decs, static_q
+
+
+def capture(decs, static_q, parity_steps=2):
+    """CUDA graphs of one step of every decoder in `decs`, one graph per parity of the step index
+    (the speculative-set buffers alternate); the decoders' step counters are left unchanged."""
+    import torch
+
+    t0 = [d.t for d in decs]
+    graphs = []
+    for _ in range(parity_steps):
+        g = torch.cuda.CUDAGraph()
+        with torch.cuda.graph(g):
+            for dec in decs:
+                dec.step(static_q)
+        graphs.append(g)
+    for d, t in zip(decs, t0):
+        d.t = t
+    return graphs
+
 
 def bench_prr(args, w, dev, rank):
     import torch
 
     from dynamic_block_sparse_gb300 import binding as B
-    from dynamic_block_sparse_gb300.pipeline import Cache, PRRDecoder
-    from dynamic_block_sparse_gb300.workloads import make_inputs
 
-    inputs = make_inputs(w, device=dev, shuffle_pages=False)
-    cache = Cache.from_inputs(inputs, dev)
-    dec = PRRDecoder(cache, w.k, w.k_pred, w.alpha, w.beta, w.gamma)
+    n_layers = N_LAYERS
+    inputs, decs, static_q = build_layers(w, dev, n_layers)
     qs = inputs["q"]
     nq = qs.shape[0]
     n_valid = -(-w.seq_len // w.page_size)
     flush = L2Flush(dev)
     stream = torch.cuda.current_stream()
+    dec = decs[0]
 
-    # metadata build (context stage): timed on its own
+    # metadata build (context stage): timed on its own, L2 flushed
     ev = [torch.cuda.Event(enable_timing=True) for _ in range(2)]
     meta_ms = []
     for i in range(4):
@@ -234,76 +289,109 @@ def bench_prr(args, w, dev, rank):
         meta_ms.append(ev[0].elapsed_time(ev[1]))
     meta_build_ms = statistics.median(meta_ms[1:])
 
-    static_q = qs[0].clone()
-    dec.step(static_q)                                   # step 0: EMA init
-    for i in range(1, 4):                                # eager steady-state steps
-        static_q.copy_(qs[i % nq])
-        dec.step(static_q)
-    torch.cuda.synchronize()
+    # ---- the timed rotation: exactly args.steps steps, each on the next layer
+    full = capture(decs, static_q)
+    R, r = divmod(args.steps, n_layers)
+    part = capture(decs[:r], static_q) if r else None
+    warm_rep = max(1, -(-args.warmup // n_layers))
+    done = 0  # full-rotation replays so far (every layer advanced by that many steps)
 
-    # one graph per parity of the step index (the speculative-set buffers alternate): the fused
-    # one-launch step, and for comparison the same step as separate launches on three streams
-    parity0 = dec.t % 2
-    graphs, staged_graphs = [], []
-    for fused, lst in ((False, staged_graphs), (True, graphs)):
-        dec.fused = fused
-        for _ in range(2):
-            g = torch.cuda.CUDAGraph()
-            with torch.cuda.graph(g):
-                dec.step(static_q)
-            lst.append(g)
-    dec.fused = True
-    stage_graphs = {}
-    for name, fn in (("score_pages", lambda: dec.stage_score(static_q)),
-                     ("select_topk", lambda: dec.stage_select()),
-                     ("spec_attn", lambda: dec.stage_spec(static_q, 0)),
-                     ("repair_merge", lambda: dec.stage_repair(static_q, 0)),
-                     ("ema_predict", lambda: dec.stage_ema(buf=1))):
-        g = torch.cuda.CUDAGraph()
-        with torch.cuda.graph(g):
-            fn()
-        stage_graphs[name] = [g]
+    def replay_full(k):
+        full[k % 2].replay()
+
+    for _ in range(warm_rep):
+        static_q.copy_(qs[(4 + done) % nq])
+        replay_full(done)
+        done += 1
     torch.cuda.synchronize()
+    sampler = ClockSampler(gpu_selector(dev))
+    sampler.start()
+    time.sleep(0.3)
+    if hasattr(torch.distributed, "is_initialized") and torch.distributed.is_initialized():
+        torch.distributed.barrier()
+    torch.cuda.synchronize()
+    marks = [torch.cuda.Event(enable_timing=True) for _ in range(R + 2)]
+    t_host0 = time.perf_counter()
+    marks[0].record(stream)
+    for i in range(R):
+        replay_full(done)
+        done += 1
+        marks[i + 1].record(stream)
+    if r:
+        part[done % 2].replay()
+    marks[R + 1].record(stream)
+    torch.cuda.synchronize()
+    host_s = time.perf_counter() - t_host0
+    clocks = sampler.stop()
+    total_ms = marks[0].elapsed_time(marks[R + 1])
+    mean_ms = total_ms / args.steps
+    per_rot = [marks[i].elapsed_time(marks[i + 1]) / n_layers for i in range(R)] or [mean_ms]
+    for i, d in enumerate(decs):
+        d.t += done + (1 if i < r else 0)
+
+    # pages attended per step (layer 0's next steps, eager), for the byte count
+    P_counts, missed = [], []
+    for i in range(8):
+        P, Pc = dec.spec_idx.clone(), dec.spec_count.clone()
+        static_q.copy_(qs[(8 + i) % nq])
+        dec.step(static_q)
+        torch.cuda.synchronize()
+        pc = mc = 0
+        for b in range(w.batch):
+            for h in range(w.num_kv_heads):
+                Ps = set(P[b, h, :int(Pc[b, h])].tolist())
+                A = dec.idx[b, h, :int(dec.count[b, h])].tolist()
+                pc += len(Ps)
+                mc += sum(1 for a in A if a not in Ps)
+        P_counts.append(pc)
+        missed.append(mc)
+    bytes_step, true_set_step, parts = prr_bytes(w, n_valid, statistics.mean(P_counts),
+                                                 statistics.mean(missed))
+
+    # ---- one step alone with L2 flushed before it (code and data cold): layer 0's graphs
+    single = capture([dec], static_q)
     state = {"i": 0}
 
-    def timed_replay(glist, n, qi0=0, collect=None):
+    def timed_replay(glist, n, qi0=0, parity_of=None):
         """Replays the graphs in turn (L2 flushed before each, outside the timed window)."""
         starts = [torch.cuda.Event(enable_timing=True) for _ in range(n)]
         ends = [torch.cuda.Event(enable_timing=True) for _ in range(n)]
         for i in range(n):
             gi = state["i"] % len(glist)
             static_q.copy_(qs[(qi0 + i) % nq])
-            if collect is not None:
-                buf = (parity0 + gi) % 2
-                collect[0].append((dec.spec_bufs[buf].clone(), dec.spec_counts[buf].clone()))
             flush.lead()
             flush(i & 0xFF)
             starts[i].record(stream)
             glist[gi].replay()
             ends[i].record(stream)
             state["i"] += 1
-            if collect is not None:
-                collect[1].append((dec.idx.clone(), dec.count.clone()))
         torch.cuda.synchronize()
-        return [s.elapsed_time(e) for s, e in zip(starts, ends)]
+        return [st.elapsed_time(en) for st, en in zip(starts, ends)]
 
-    timed_replay(graphs, args.warmup, qi0=4)
-    sampler = ClockSampler(gpu_selector(dev))
-    sampler.start()
-    time.sleep(0.3)
-    collect = ([], [])
-    if hasattr(torch.distributed, "is_initialized") and torch.distributed.is_initialized():
-        torch.distributed.barrier()
-    torch.cuda.synchronize()
-    step_ms = timed_replay(graphs, args.steps, qi0=4 + args.warmup, collect=collect)
+    n_cold = 2 * max(25, min(200, args.steps // 2))
+    cold_ms = timed_replay(single, n_cold, qi0=4)
+    dec.t += n_cold
+
+    # ---- stages of the step as separate launches (layer 0, L2 flushed before each)
+    stage_graphs = {}
+    for name, fn in (("score_pages", lambda: dec.stage_score(static_q)),
+                     ("select_topk", lambda: dec.stage_select()),
+                     ("spec_attn", lambda: dec.stage_spec(static_q, 0)),
+                     ("repair_merge", lambda: dec.stage_repair(static_q, 0)),
+                     ("ema_predict", lambda: dec.stage_ema(buf=1))):
+        stage_graphs[name] = [_graph(fn)]
     torch.cuda.synchronize()
     stage_ms = {}
     for name, g in stage_graphs.items():
         state["i"] = 0
         stage_ms[name] = statistics.mean(timed_replay(g, max(50, min(400, args.steps))))
-    # the separate-launch step (state keeps evolving; the parity alternation is the same)
+    dec.fused = False
+    staged = capture([dec], static_q)
     state["i"] = 0
-    staged_ms = statistics.mean(timed_replay(staged_graphs, max(50, min(400, args.steps))))
+    n_staged = 2 * max(25, min(200, args.steps // 2))
+    staged_ms = statistics.mean(timed_replay(staged, n_staged))
+    dec.t += n_staged
+    dec.fused = True
     # EMA calibration (PRR §3.2) over a 16-step trajectory of this workload's true scores
     calib_steps = 16
     traj = torch.empty((calib_steps,) + tuple(dec.scores.shape), dtype=torch.float32, device=dev)
@@ -318,51 +406,38 @@ def bench_prr(args, w, dev, rank):
     calib_ms = _time_graph(_graph(lambda: B.dsa_calibrate_ema(t3, dec.stride, w.k, w.k_pred, cH,
                                                                cbest, cws)), flush)
     calib_bytes = t3.numel() * 4 + cH.numel() * 4 + cbest.numel() * 4
-    clocks = sampler.stop()
-
-    # pages attended per timed step
-    P_counts, missed = [], []
-    for (pi, pc), (ai, ac) in zip(*collect):
-        pi, pc, ai, ac = pi.cpu(), pc.cpu(), ai.cpu(), ac.cpu()
-        pcount, mcount = 0, 0
-        for b in range(w.batch):
-            for h in range(w.num_kv_heads):
-                P = set(pi[b, h, :int(pc[b, h])].tolist())
-                A = ai[b, h, :int(ac[b, h])].tolist()
-                pcount += len(P)
-                mcount += sum(1 for a in A if a not in P)
-        P_counts.append(pcount)
-        missed.append(mcount)
-    n = len(step_ms)
-    bytes_step, true_set_step, parts = prr_bytes(w, n_valid, sum(P_counts) / n, sum(missed) / n)
-    mean_ms = statistics.mean(step_ms)
 
     rows = w.batch * w.num_kv_heads
     page_kv = w.page_size * w.head_dim * 4
     q_bytes = w.batch * w.num_q_heads * w.head_dim * 2
+    mean_P, mean_missed = statistics.mean(P_counts), statistics.mean(missed)
     stage_bytes = {
         "score_pages": rows * n_valid * 512 + q_bytes + rows * n_valid * 4,
         "select_topk": rows * n_valid * 4 + rows * w.k * 4,
-        "spec_attn": (sum(P_counts) / n) * (page_kv + w.group * 528) + q_bytes,
+        "spec_attn": mean_P * page_kv + q_bytes,
         "ema_predict": rows * n_valid * 4 * 6 + rows * w.k_pred * 4,
     }
-    # the step is one kernel launch (the fused PRR step): its roofline is the step's own
-    dominant = "prr_step_kernel"
     e2e = None
     if not args.no_e2e:
-        e2e = e2e_prr(args, w, dec, qs, flush, bytes_step)
-    extra = dict(meta_build_ms=meta_build_ms,
+        e2e = e2e_prr(args, w, decs, qs, bytes_step)
+    cold_mean = statistics.mean(cold_ms)
+    extra = dict(n_layers=n_layers,
+                 rotation_us_per_step_p50=statistics.median(per_rot) * 1e3,
+                 rotation_us_per_step_p90=sorted(per_rot)[int(0.9 * (len(per_rot) - 1))] * 1e3,
+                 host_us_per_step=host_s / args.steps * 1e6,
+                 cold_step={"us": cold_mean * 1e3, "us_p50": statistics.median(cold_ms) * 1e3,
+                            "gbs": bytes_step / (cold_mean * 1e6),
+                            "note": "one step alone, L2 flushed before it (code and data cold)"},
+                 meta_build_ms=meta_build_ms,
                  meta_build_gbs=(rows * n_valid * w.page_size * w.head_dim * 2
                                  + rows * n_valid * 512) / (meta_build_ms * 1e6),
                  stage_ms=stage_ms, stage_bytes=stage_bytes,
-                 mean_P=sum(P_counts) / n / rows, mean_missed=sum(missed) / n / rows,
+                 mean_P=mean_P / rows, mean_missed=mean_missed / rows,
                  bytes_per_step=bytes_step, true_set_bytes_per_step=true_set_step,
-                 true_set_gbs=true_set_step / (mean_ms * 1e6),
-                 byte_parts=parts,
-                 step_ms_p50=statistics.median(step_ms), step_ms_min=min(step_ms))
+                 true_set_gbs=true_set_step / (mean_ms * 1e6), byte_parts=parts)
     peak, _ = load_peaks()
-    hits = rows * w.k - sum(missed) / n
-    rep_bytes = (sum(missed) / n) * page_kv + hits * w.group * 528 + q_bytes
+    hits = rows * w.k - mean_missed
+    rep_bytes = mean_missed * page_kv + hits * w.group * 528 + q_bytes
     prr_rows = [
         _entry("A2", w.name, "dsa_score_pages MINMAX", stage_ms["score_pages"],
                stage_bytes["score_pages"], peak),
@@ -376,65 +451,73 @@ def bench_prr(args, w, dev, rank):
                stage_ms["repair_merge"], rep_bytes, peak),
         _entry("N1", w.name, "dsa_calibrate_ema: 80-point (alpha, beta, gamma) grid, 16 steps",
                calib_ms, calib_bytes, peak),
-        _entry("step", w.name, "PRR decode step, one cooperative launch (dsa_prr_step)", mean_ms,
+        _entry("step", w.name, f"PRR decode step, one cooperative launch (dsa_prr_step), "
+               f"{n_layers}-layer rotation", mean_ms, bytes_step, peak),
+        _entry("step-cold", w.name, "the same step alone, L2 flushed before it", cold_mean,
                bytes_step, peak),
-        _entry("step-staged", w.name, "PRR decode step, separate launches on three streams",
-               staged_ms, bytes_step, peak),
+        _entry("step-staged", w.name, "PRR decode step, separate launches on three streams "
+               "(L2 flushed before it)", staged_ms, bytes_step, peak),
     ]
-    return dict(rows=prr_rows, mean_ms=mean_ms, p50_ms=statistics.median(step_ms),
-                p90_ms=sorted(step_ms)[int(0.9 * (len(step_ms) - 1))], bytes_step=bytes_step,
-                clocks=clocks,
-                dominant=dominant, dominant_ms=mean_ms, dominant_bytes=bytes_step, e2e=e2e,
-                launches_per_step=1, extra=extra)
+    return dict(rows=prr_rows, mean_ms=mean_ms, p50_ms=statistics.median(per_rot),
+                p90_ms=sorted(per_rot)[int(0.9 * (len(per_rot) - 1))], bytes_step=bytes_step,
+                clocks=clocks, dominant="prr_step_kernel", dominant_ms=mean_ms,
+                dominant_bytes=bytes_step, e2e=e2e, launches_per_step=1, extra=extra)
 
 
-def e2e_prr(args, w, dec, qs, flush, bytes_step):
-    """Same step through the public Python API with host buffers, every step inside the window:
-    the pinned host query reaches the device, the step runs (eager library call), and the step's
-    result (O, m, l: one contiguous buffer) reaches pinned host memory.  Measured two ways:
+def e2e_prr(args, w, decs, qs, bytes_step):
+    """The rotation through the public Python API with host buffers, eagerly (each call submitted
+    by the host): every step's query comes from page-locked host memory and its result (O, m, l:
+    one contiguous buffer per layer) goes to page-locked host memory.  Two ways: ``zero_copy``
+    (the line's ``e2e``) with the query and the result in page-locked host memory that the fused
+    step reads and writes itself over the host link (NVLink-C2C on a Grace-Blackwell node), and
     ``copies`` with a host-to-device copy of the query and a device-to-host copy of the result
-    around the step, and ``zero_copy`` (the line's ``e2e``) with the query and the result in
-    page-locked host memory that the fused step reads and writes itself over the host link
-    (NVLink-C2C on a Grace-Blackwell node); the same bytes cross it either way."""
+    around every step.  Device time comes from CUDA events around a rotation of all layers, host
+    time from the wall clock around the same."""
     import torch
 
     nq = qs.shape[0]
     host_q = torch.empty((nq,) + tuple(qs.shape[1:]), dtype=qs.dtype, pin_memory=True)
     host_q.copy_(qs.cpu())
     dev_q = torch.empty_like(qs[0])
-    res_h = torch.empty(dec.result.shape, dtype=torch.float32, pin_memory=True)
-    n = max(20, min(300, args.steps))
     stream = torch.cuda.current_stream()
+    n_rot = max(4, min(40, args.steps // len(decs)))
+    res_h = [torch.empty(d.result.shape, dtype=torch.float32, pin_memory=True) for d in decs]
 
     def run(step):
-        times = []
-        for i in range(n + 5):
-            flush(i & 0xFF)
+        dev_t, host_t = [], []
+        for i in range(n_rot + 2):
+            torch.cuda.synchronize()
             s, e = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+            h0 = time.perf_counter()
             s.record(stream)
-            step(i)
+            for li in range(len(decs)):
+                step(li, i)
             e.record(stream)
             e.synchronize()
-            if i >= 5:
-                times.append(s.elapsed_time(e))
-        return statistics.mean(times)
+            h1 = time.perf_counter()
+            if i >= 2:
+                dev_t.append(s.elapsed_time(e) / len(decs))
+                host_t.append((h1 - h0) * 1e3 / len(decs))
+        return statistics.mean(dev_t), statistics.mean(host_t)
 
-    def with_copies(i):
+    def with_copies(li, i):
         dev_q.copy_(host_q[i % nq], non_blocking=True)
-        dec.step(dev_q)
-        res_h.copy_(dec.result, non_blocking=True)
+        decs[li].step(dev_q)
+        res_h[li].copy_(decs[li].result, non_blocking=True)
 
-    ms_copies = run(with_copies)
-    dec.host_result()
-    ms = run(lambda i: dec.step(host_q[i % nq]))
+    ms_copies, host_copies = run(with_copies)
+    for d in decs:
+        d.host_result()
+    ms, host_ms = run(lambda li, i: decs[li].step(host_q[i % nq]))
     h2d = dev_q.numel() * dev_q.element_size()
-    d2h = dec.result.numel() * 4
+    d2h = decs[0].result.numel() * 4
     return {"value": bytes_step / (ms * 1e6), "unit": "GB/s", "ms_per_step": ms,
+            "host_ms_per_step": host_ms, "host_value": bytes_step / (host_ms * 1e6),
             "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h,
             "transfer": "zero-copy: the fused step reads the pinned host query and writes the "
                         "pinned host result over the host link",
             "copies": {"value": bytes_step / (ms_copies * 1e6), "unit": "GB/s",
-                       "ms_per_step": ms_copies,
+                       "ms_per_step": ms_copies, "host_ms_per_step": host_copies,
                        "transfer": "cudaMemcpyAsync of the query in, one of the result out"}}
 
 
@@ -730,10 +813,13 @@ def main():
     config = {"workload": f"{w.name}: B{w.batch}, {w.num_q_heads}q/{w.num_kv_heads}kv heads, "
                           f"D{w.head_dim}, {w.seq_len} tokens, block {w.page_size}, top-{w.k}, "
                           f"|P|={w.k_pred}, EMA a{w.alpha} b{w.beta} g{w.gamma}",
-              "seq_len": w.seq_len, "batch_per_gpu": w.batch, "l2": "flushed (256 MiB write, then "
-              "256 MiB read of a second buffer) before every timed step, outside the timed window",
-              "timing": "CUDA graph of one decode step, CUDA events on the launching stream; a "
-              "~50 us GPU spin is queued before each flush so the window never waits on the host"}
+              "seq_len": w.seq_len, "batch_per_gpu": w.batch,
+              "l2": f"inputs larger than L2: the steps rotate over {N_LAYERS} layers' caches "
+                    f"(each step's ~14 MB was last touched {N_LAYERS - 1} steps, ~430 MB, "
+                    "earlier; L2 is 129 MB)",
+              "timing": f"CUDA graphs of one step of each of the {N_LAYERS} layers, replayed back "
+                        "to back; CUDA events around exactly --steps steps on the launching "
+                        "stream"}
 
     if args.rows_only is not None:
         import torch

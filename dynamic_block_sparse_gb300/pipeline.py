@@ -241,9 +241,9 @@ class ThresholdDecoder:
 class PRRDecoder:
     """Predict, reuse and repair over top-K block selection (PRR §3.1-§3.4, fixed budget).
 
-    With ``fused`` (the default) step t >= 1 is one ``dsa_prr_step`` launch: speculation over P_t
-    beside scoring, then top-K selection of the true set A_t beside the EMA update that selects
-    P_{t+1}, then repair and merge, all separated by on-device grid barriers.  Otherwise the same
+    With ``fused`` (the default) step t >= 1 is one ``dsa_prr_step`` launch: scoring with the EMA
+    update and the speculative pass over P_t on most SMs, the selections of A_t and P_{t+1}, the
+    repair and the merge on others, each waiting only for its own row's counters.  Otherwise the same
     library calls run as separate launches on three streams: the speculative pass over P_t on
     ``side``; scoring, top-K selection and the repair/merge on the caller's stream; the EMA update
     (which needs only this step's scores) on ``ema_stream``.  Either way P_{t+1} goes into the
@@ -281,8 +281,8 @@ class PRRDecoder:
         self.side = torch.cuda.Stream(device=dev) if two_streams else None
         self.ema_stream = torch.cuda.Stream(device=dev) if two_streams else None
         self.fused = fused
-        # the fused step's barrier words and candidate counts: zero before the first call, left
-        # zero by each call
+        # the fused step's workspace: its counters are zero before the first call and left zero
+        # by each call
         self.step_workspace = torch.zeros(B.dsa_prr_step_workspace_size(c.kv), dtype=torch.uint8,
                                           device=dev)
         self.t = 0

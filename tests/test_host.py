@@ -225,7 +225,9 @@ def test_bench_byte_accounting():
     assert parts["meta"] == 2 * 8192 * 512
     assert parts["kv"] == 156 * 64 * 512
     assert true_set == 2 * 8192 * 512 + 2 * 64 * 64 * 512
-    assert total > parts["meta"] + parts["kv"]
+    # the partial records stay in L2: reported apart, not counted
+    assert total == parts["meta"] + parts["kv"] + parts["aux"]
+    assert parts["records_l2"] == 156 * 16 * 132 * 4
 
 
 def _replica_worker(rank, world, port, out):
