@@ -215,9 +215,12 @@ size_t dsa_sparse_decode_attn_workspace_size(const dsa_paged_kv* kv, int32_t idx
  * a counterpart: this is a deployment convenience).  Some callers cannot call cudaMalloc: code
  * running inside a host framework that owns all device memory through its own allocator, and
  * latency-critical loops that cannot accept the device synchronisation cudaMalloc/cudaFree may
- * imply.  This variant computes exactly what dsa_sparse_decode_attn computes (same kernels, same
- * split choice for the same num_splits) but keeps the split-K partial records in a fixed 4 MiB
- * device array inside the library, which every GPU that loads the library holds until exit.
+ * imply.  This variant always runs the explicit split-K path (per-split CTAs, then a merge
+ * kernel): with the same num_splits > 0 it computes exactly what dsa_sparse_decode_attn computes;
+ * with num_splits <= 0 it picks its own split count on that path (dsa_sparse_decode_attn's
+ * default is its persistent kernel instead), so the two agree up to fp32 rounding.  It keeps the
+ * split-K partial records in a fixed 4 MiB device array inside the library, which every GPU that
+ * loads the library holds until exit.
  *   - Allocates nothing; calls no cudaMalloc/cudaFree or allocating library routine.
  *   - The first call on each device looks up the array's device address (cudaGetSymbolAddress,
  *     with that device current) and caches it; make that first call before any stream capture.
