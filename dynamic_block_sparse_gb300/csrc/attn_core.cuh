@@ -174,15 +174,22 @@ DSA_DEV void state_finish(WarpSoftmaxState& st) {
   }
 }
 
-// Writes a warp's (unnormalised O, m, l) to shared scratch: sO [16][128] fp32, sM/sL [16].
-DSA_DEV void state_store(const WarpSoftmaxState& st, float* sO, float* sM, float* sL) {
+// Writes a warp's (unnormalised O, m, l) to shared scratch: sO [16][128] fp32, sM/sL [16].  Only
+// the first `rows` query rows of O are written (the rest are padding).
+DSA_DEV void state_store(const WarpSoftmaxState& st, float* sO, float* sM, float* sL,
+                         int rows = 16) {
   const int lane = threadIdx.x & 31;
   const int r0 = lane >> 2, c0 = (lane & 3) * 2;
+  if (r0 < rows) {
 #pragma unroll
-  for (int j = 0; j < 16; ++j) {
-    *reinterpret_cast<float2*>(sO + r0 * 128 + j * 8 + c0) = make_float2(st.o[j][0], st.o[j][1]);
-    *reinterpret_cast<float2*>(sO + (r0 + 8) * 128 + j * 8 + c0) =
-        make_float2(st.o[j][2], st.o[j][3]);
+    for (int j = 0; j < 16; ++j)
+      *reinterpret_cast<float2*>(sO + r0 * 128 + j * 8 + c0) = make_float2(st.o[j][0], st.o[j][1]);
+  }
+  if (r0 + 8 < rows) {
+#pragma unroll
+    for (int j = 0; j < 16; ++j)
+      *reinterpret_cast<float2*>(sO + (r0 + 8) * 128 + j * 8 + c0) =
+          make_float2(st.o[j][2], st.o[j][3]);
   }
   if ((lane & 3) == 0) {
     sM[r0] = st.m[0];

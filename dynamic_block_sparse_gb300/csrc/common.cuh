@@ -21,6 +21,14 @@ DSA_DEV uint32_t smem_u32(const void* p) {
   return static_cast<uint32_t>(__cvta_generic_to_shared(p));
 }
 
+// The dynamic shared memory window advanced to a 1024-byte boundary (the 128-byte TMA swizzle
+// pattern repeats every 1024 bytes), as an offset from the __shared__ array itself so that every
+// pointer derived from it stays in the shared address space (a detour through an integer would
+// turn its accesses into generic ones).
+DSA_DEV uint8_t* smem_align1024(uint8_t* raw) {
+  return raw + ((1024u - (smem_u32(raw) & 1023u)) & 1023u);
+}
+
 DSA_DEV unsigned long long global_timer_ns() {
   unsigned long long t;
   asm volatile("mov.u64 %0, %%globaltimer;" : "=l"(t));
@@ -49,6 +57,13 @@ DSA_DEV void fence_mbar_init() {
 DSA_DEV void mbar_arrive_expect_tx(uint32_t bar, uint32_t bytes) {
   asm volatile("mbarrier.arrive.expect_tx.release.cta.shared::cta.b64 _, [%0], %1;" ::"r"(bar),
                "r"(bytes)
+               : "memory");
+}
+
+// Adds `bytes` to the transaction count of the barrier's current phase without arriving (several
+// threads may each post the bytes of the copies they issue; one arrival then closes the phase).
+DSA_DEV void mbar_expect_tx(uint32_t bar, uint32_t bytes) {
+  asm volatile("mbarrier.expect_tx.relaxed.cta.shared::cta.b64 [%0], %1;" ::"r"(bar), "r"(bytes)
                : "memory");
 }
 
@@ -190,6 +205,14 @@ DSA_DEV uint32_t pack_bf16(float lo, float hi) {
 DSA_DEV float fast_exp2(float x) {
   float y;
   asm("ex2.approx.ftz.f32 %0, %1;" : "=f"(y) : "f"(x));
+  return y;
+}
+
+// log2(x) via the SFU instruction (approximate: absolute error about 2^-22 on [0.5, 2], relative
+// elsewhere; lg2(0) = -inf).
+DSA_DEV float fast_log2(float x) {
+  float y;
+  asm("lg2.approx.ftz.f32 %0, %1;" : "=f"(y) : "f"(x));
   return y;
 }
 
