@@ -47,8 +47,7 @@ __global__ void __launch_bounds__(kAttnThreads)
     attn_pages_kernel(const __grid_constant__ CUtensorMap tmK,
                       const __grid_constant__ CUtensorMap tmV, const AttnArgs a) {
   extern __shared__ uint8_t smem_raw[];
-  uint8_t* smem = reinterpret_cast<uint8_t*>(
-      (reinterpret_cast<uintptr_t>(smem_raw) + 1023u) & ~static_cast<uintptr_t>(1023u));
+  uint8_t* smem = smem_align1024(smem_raw);
   const KvView& kv = a.kv;
   const int page = kv.p;
   const int S = a.stages;

@@ -168,8 +168,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     prr_step_kernel(const __grid_constant__ CUtensorMap tmK,
                     const __grid_constant__ CUtensorMap tmV, const PrrArgs a) {
   extern __shared__ uint8_t smem_raw[];
-  uint8_t* smem = reinterpret_cast<uint8_t*>(
-      (reinterpret_cast<uintptr_t>(smem_raw) + 1023u) & ~static_cast<uintptr_t>(1023u));
+  uint8_t* smem = smem_align1024(smem_raw);
   __shared__ __align__(16) SelectAnyScratch<kThreads> sel;  // candidate keys are read as uint4
   // the ring's mbarriers ([S] full, [S] empty) and stage descriptors
   __shared__ __align__(8) uint64_t bars[2 * kMaxStages];

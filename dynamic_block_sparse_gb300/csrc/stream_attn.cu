@@ -265,8 +265,7 @@ __global__ void __launch_bounds__(kSThreads, 1)
     stream_attn_kernel(const __grid_constant__ CUtensorMap tmK,
                        const __grid_constant__ CUtensorMap tmV, const StreamAttnArgs a) {
   extern __shared__ uint8_t smem_raw[];
-  uint8_t* smem = reinterpret_cast<uint8_t*>(
-      (reinterpret_cast<uintptr_t>(smem_raw) + 1023u) & ~static_cast<uintptr_t>(1023u));
+  uint8_t* smem = smem_align1024(smem_raw);
   const KvView& kv = a.kv;
   const int page = kv.p;
   const int S = a.stages;
@@ -362,9 +361,13 @@ __global__ void __launch_bounds__(kSThreads, 1)
   };
   auto unit_stride = [&](int di) { return !STREAMING || di < Nd ? stride : sstride; };
   auto unit_row = [&](int di) -> int {  // its (request, KV head) row
-    if (!STREAMING || di < Nd) return (di / nd_heads) * kv.Hkv + dense_heads[di % nd_heads];
-    const int e = di - Nd;
-    return (e / ns_heads) * kv.Hkv + stream_heads[e % ns_heads];
+    if constexpr (STREAMING) {
+      if (di >= Nd) {
+        const int e = di - Nd;
+        return (e / ns_heads) * kv.Hkv + stream_heads[e % ns_heads];
+      }
+    }
+    return (di / nd_heads) * kv.Hkv + dense_heads[di % nd_heads];
   };
   // a streaming row of length L attends the pages of its sink tokens [0, min(sink, L)), then
   // those of its local tokens [max(0, L - local), L): sink_n pages from position 0, the rest
