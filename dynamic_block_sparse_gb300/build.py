@@ -2,7 +2,9 @@
 
 Translation units compile in parallel into ``_build/`` next to this file; the shared library is
 linked to ``dynamic_block_sparse_gb300/libdsa.so``.  A rebuild happens only when a source or
-header is newer than the library (or ``force=True``).
+header is newer than the library (or ``force=True``).  ``build_traced()`` makes the phase-tracing
+variant ``libdsa_trace.so`` (compiled with ``-DDSA_TIMELINE``) in ``_build_trace/``; nothing loads
+it but the tracing script.
 """
 
 from __future__ import annotations
@@ -19,6 +21,8 @@ CSRC = os.path.join(HERE, "csrc")
 INCLUDE = os.path.join(ROOT, "include")
 BUILD_DIR = os.path.join(HERE, "_build")
 LIB_PATH = os.path.join(HERE, "libdsa.so")
+TRACE_BUILD_DIR = os.path.join(HERE, "_build_trace")
+TRACE_LIB_PATH = os.path.join(HERE, "libdsa_trace.so")
 
 SOURCES = ["api.cu", "attn.cu", "calib.cu", "kv8.cu", "meta_score.cu", "prr_step.cu",
            "select.cu", "stream_attn.cu", "threshold.cu"]
@@ -46,19 +50,24 @@ def _inputs() -> list[str]:
     return files
 
 
-def up_to_date() -> bool:
-    return os.path.exists(LIB_PATH) and os.path.getmtime(LIB_PATH) >= _newest(_inputs())
+def up_to_date(lib_path: str = LIB_PATH) -> bool:
+    return os.path.exists(lib_path) and os.path.getmtime(lib_path) >= _newest(_inputs())
 
 
-def build(force: bool = False, verbose: bool = False, ptxas_info: bool = False) -> str:
-    if not force and up_to_date():
-        return LIB_PATH
-    os.makedirs(BUILD_DIR, exist_ok=True)
+def build(force: bool = False, verbose: bool = False, ptxas_info: bool = False,
+          traced: bool = False) -> str:
+    lib_path = TRACE_LIB_PATH if traced else LIB_PATH
+    build_dir = TRACE_BUILD_DIR if traced else BUILD_DIR
+    if not force and up_to_date(lib_path):
+        return lib_path
+    os.makedirs(build_dir, exist_ok=True)
     cc = nvcc()
     extra = ["-Xptxas", "-v"] if ptxas_info else []
+    if traced:
+        extra.append("-DDSA_TIMELINE")
 
     def compile_one(src: str) -> tuple[str, str]:
-        obj = os.path.join(BUILD_DIR, src.replace(".cu", ".o"))
+        obj = os.path.join(build_dir, src.replace(".cu", ".o"))
         cmd = [cc, *ARCH, *FLAGS, *extra, "-c", os.path.join(CSRC, src), "-o", obj]
         r = subprocess.run(cmd, capture_output=True, text=True)
         if r.returncode != 0:
@@ -68,15 +77,19 @@ def build(force: bool = False, verbose: bool = False, ptxas_info: bool = False) 
     with cf.ThreadPoolExecutor(max_workers=min(len(SOURCES), os.cpu_count() or 4)) as ex:
         results = list(ex.map(compile_one, SOURCES))
     logs = "".join(log for _, log in results)
-    tmp = LIB_PATH + ".tmp"
+    tmp = lib_path + ".tmp"
     cmd = [cc, *ARCH, "-shared", "-o", tmp, *[o for o, _ in results]]
     r = subprocess.run(cmd, capture_output=True, text=True)
     if r.returncode != 0:
         raise RuntimeError(f"link failed:\n{r.stdout}\n{r.stderr}")
-    os.replace(tmp, LIB_PATH)
+    os.replace(tmp, lib_path)
     if verbose or ptxas_info:
         sys.stdout.write(logs)
-    return LIB_PATH
+    return lib_path
+
+
+def build_traced(force: bool = False) -> str:
+    return build(force=force, traced=True)
 
 
 if __name__ == "__main__":

@@ -277,4 +277,45 @@ DSA_DEV int block_exclusive_scan(int v, int* scratch, int* total) {
   return res;
 }
 
+// ------------------------------------------------------------------------------- phase tracing
+
+// A library built with -DDSA_TIMELINE (libdsa_trace.so, never libdsa.so) records, for thread 0 of
+// each of the first kTraceCtas CTAs of an instrumented kernel, clock64() and %globaltimer the
+// first time it passes each numbered stamp: DSA_TRACE_BEGIN() at the kernel's start (a barrier
+// and stamp 0), DSA_STAMP(k) at a phase boundary, DSA_TRACE_END(store) where every thread of the
+// CTA meets at the end.  The stamps are ordered against the surrounding code only as volatile
+// operations are, so they bound phases approximately.  Built without the define, all three expand
+// to nothing.
+constexpr int kTraceCtas = 1024, kTraceSlots = 32;
+#ifdef DSA_TIMELINE
+#define DSA_TRACE_BEGIN()                                              \
+  __shared__ unsigned long long s_trace_[2 * ::dsa::kTraceSlots];      \
+  if (threadIdx.x < 2 * ::dsa::kTraceSlots) s_trace_[threadIdx.x] = 0; \
+  __syncthreads();                                                     \
+  DSA_STAMP(0)
+#define DSA_STAMP(k)                                                     \
+  do {                                                                   \
+    if (threadIdx.x == 0 && s_trace_[k] == 0ull) {                       \
+      s_trace_[k] = clock64();                                           \
+      s_trace_[::dsa::kTraceSlots + (k)] = ::dsa::global_timer_ns();     \
+    }                                                                    \
+  } while (0)
+#define DSA_TRACE_END(store)                                                         \
+  do {                                                                               \
+    __syncthreads();                                                                 \
+    if (threadIdx.x < 2 * ::dsa::kTraceSlots && blockIdx.x < ::dsa::kTraceCtas)      \
+      (store)[blockIdx.x * 2 * ::dsa::kTraceSlots + threadIdx.x] = s_trace_[threadIdx.x]; \
+  } while (0)
+#else
+#define DSA_TRACE_BEGIN() \
+  do {                    \
+  } while (0)
+#define DSA_STAMP(k) \
+  do {               \
+  } while (0)
+#define DSA_TRACE_END(store) \
+  do {                       \
+  } while (0)
+#endif
+
 }  // namespace dsa

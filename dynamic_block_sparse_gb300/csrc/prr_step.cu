@@ -3,26 +3,32 @@
 // of the missed pages and the merge), organised so that no CTA ever waits for the whole grid.
 //
 // Roles.  With few (row, query head) tasks (at most a quarter of the grid), the first CTAs only run
-// tasks and the others (the workers) do the rest; otherwise every CTA is a worker first and then
-// takes tasks round robin.
+// tasks and the others (the workers) score; otherwise every CTA is a worker first and then takes
+// tasks round robin.
 //   scoring  each worker scores an equal share of the (row, page) slots with the scoring kernel's
 //            arithmetic (every page-table entry, length, EMA state and query load of a round in
 //            flight at once, then the metadata records), updates the EMA state of those pages at
 //            once (no other CTA reads their old state), and counts the row's scored pages up by
-//            its share (one counter per row);
-//   items    its pages of P_t arrive through a TMA ring issued by its eighth warp; one warp attends
-//            one page (all of its 16-token tiles, the whole query group as the m16 tile of the
-//            tensor-core products) and writes the page's record straight from its registers,
-//            counted per row;
-//   tasks    per (row, query head), once the row is scored: its scores (L2, one batch of loads)
-//            are ranked into A_t.  T0, the k-th largest score over P_t's pages, bounds A_t's
-//            cut-off from below, so only the pages at or above T0 are ranked exactly (collected in
-//            index order; every rank computed by a whole warp), or every page when P_t has fewer
-//            than k scored pages or too many pass T0.  The first head's task publishes A_t.  The
-//            missed pages A_t \ P_t go through the ring (one warp per page), and the task merges
-//            them with the records of A_t ∩ P_t (all of P_t in superset mode).  Per row, one more
-//            task ranks P_{t+1} from the new predictions the same way (bound T1 = the k_pred-th
-//            largest prediction over P_t).
+//            its share (one counter per row).  Pages scoring at or above the row's hint (a key
+//            the previous call left, see below) go to the worker's candidate line for the row as
+//            they are found, so that they are out before the count;
+//   items    the pages of P_t are spread over every CTA's eighth warp, which issues their TMA
+//            loads through the CTA's ring, attends each page (all of its 16-token tiles, the whole
+//            query group as the m16 tile of the tensor-core products) while the other warps score,
+//            and writes the page's record straight from its registers, counted per row;
+//   tasks    per (row, query head), once the row is scored: A_t.  When the covering workers listed
+//            at least k candidates (and none overflowed its line), the row's k best are among
+//            them and only the list is ranked; the k best are marked in a bitmap and read out in
+//            ascending order.  Otherwise the row's scores (L2, one batch of loads) are ranked with
+//            T0, the k-th largest score over P_t's pages, as the lower bound of A_t's cut-off, or
+//            every page when that does not hold.  The first head's task publishes A_t and the next
+//            hint: the key of rank 1.5k when the list reached it, else the score where rank 1.75k
+//            would stand if the top scores' log-rank is linear in the score.  Any hint value is
+//            safe; it only decides how often the list is usable.  The missed pages A_t \ P_t go
+//            through the ring (one warp per page, looked up in a bitmap of P_t), and the task
+//            merges them with the records of A_t ∩ P_t (all of P_t in superset mode).  Per row,
+//            one more task ranks P_{t+1} from the new predictions with T0's counterpart (the
+//            k_pred-th largest prediction over P_t).
 // Each wait is on a per-row counter that only work done before any wait advances, so every wait
 // ends; all are bounded (DSA_STATUS_TIMEOUT after 2 s).  The last CTA out sets the counters back
 // to zero.
@@ -32,6 +38,9 @@
 #include "select.cuh"
 
 namespace dsa {
+#ifdef DSA_TIMELINE
+__device__ unsigned long long g_trace_prr[kTraceCtas * 2 * kTraceSlots];
+#endif
 namespace {
 
 // 8 warps (two per SM sub-partition) leave every thread up to 255 registers
@@ -43,9 +52,11 @@ constexpr int kGroups = kCT / 8;           // scoring record groups of 8 lanes
 constexpr int kRecGroup = 5;               // records per group per scoring round
 constexpr int kRound = kGroups * kRecGroup;
 constexpr int kPredMax = kPrrPredMax;      // bound of k and k_pred
-constexpr int kMaxStages = 2;              // TMA ring depth
+constexpr int kMaxStages = 3;              // TMA ring depth
 constexpr int kWs = kHeadDim + 4;          // a warp's merge state: m, l, -, -, O[128]
 constexpr int kQTile = 16 * kQStride;      // bf16 elements of one warp's query tile
+constexpr int kBitsMax = kTopkMaxN / 2;    // longest row the A_t pass keeps two bitmaps for
+
 
 // ------------------------------------------------------------------------------ shared memory
 
@@ -63,7 +74,7 @@ __host__ __device__ inline SLayout slayout(int page, int n, int k_pred, int S, b
   SLayout L;
   L.stage_off = 0;
   L.q_off = S * 512u * page;
-  const uint32_t ring_end = L.q_off + kW * kQTile * 2u;
+  const uint32_t ring_end = L.q_off + kWarps * kQTile * 2u;  // a query tile per warp
   L.keys_off = 0;
   const uint32_t keys_end = 16u * ((n + 3) / 4);  // zero-padded to whole 4-key groups
   L.rec_off = up(ring_end > keys_end ? ring_end : keys_end, 16);
@@ -80,8 +91,12 @@ __host__ __device__ inline SLayout slayout(int page, int n, int k_pred, int S, b
 
 // ------------------------------------------------------------------------------ workspace
 
+constexpr int kMaxWorkers = 160;  // worker CTAs the candidate lists have room for
+constexpr int kWorkerSlots = 16;  // one 128-byte line per (row, worker): up to 15 candidates, then
+constexpr int kWorkerCand = kWorkerSlots - 1;  // a slot that is nonzero when more were found
+
 struct WsLayout {
-  size_t exit_off, done_off, sdone_off, counters, pred_off, total;
+  size_t exit_off, done_off, sdone_off, counters, hint_off, cand_off, pred_off, total;
 };
 
 inline WsLayout ws_layout(int rows, int max_pages) {
@@ -92,17 +107,31 @@ inline WsLayout ws_layout(int rows, int max_pages) {
   w.done_off = 16;
   w.sdone_off = w.done_off + cnt;
   w.counters = w.sdone_off + cnt;
-  w.pred_off = a16(w.counters);
+  w.hint_off = a16(w.counters);
+  w.cand_off = w.hint_off + cnt;
+  w.pred_off = w.cand_off + 8 * static_cast<size_t>(rows) * kMaxWorkers * kWorkerSlots;
   w.total = w.pred_off + 4 * static_cast<size_t>(rows) * max_pages;
   return w;
 }
 
 struct Ws {
-  unsigned* exit;   // CTAs finished
-  unsigned* done;   // [rows] pages scored (and their EMA state updated)
-  unsigned* sdone;  // [rows] records of P_t written
-  float* pred;      // [rows][max_pages] the new predictions
+  unsigned* exit;    // CTAs finished
+  unsigned* done;    // [rows] pages scored (and their EMA state updated)
+  unsigned* sdone;   // [rows] records of P_t written
+  uint32_t* hint;    // [rows] key the workers list candidates from (0: none); kept across steps
+  unsigned long long* cand;  // [rows][kMaxWorkers][kWorkerSlots] a worker's candidates as (key,
+                             // position) rank values, 0 past them, the last slot nonzero when it
+                             // found more (a worker clears its line each call)
+  float* pred;       // [rows][max_pages] the new predictions
 };
+
+// (key, position) as one 64-bit value ordered by key, then by the lower position.
+DSA_DEV unsigned long long rank_value_of(uint32_t key, int pos) {
+  return (static_cast<unsigned long long>(key) << 32) | (0xffffffffu - static_cast<uint32_t>(pos));
+}
+DSA_DEV int rank_pos_of(unsigned long long v) {
+  return static_cast<int>(0xffffffffu - static_cast<uint32_t>(v));
+}
 
 // ------------------------------------------------------------------------------ waits
 
@@ -174,7 +203,9 @@ __global__ void __launch_bounds__(kThreads, 1)
   __shared__ __align__(8) uint64_t bars[2 * kMaxStages];
   __shared__ int s_ctl[2 * kMaxStages];
   __shared__ int s_abort, s_issued, s_red[4];
-  __shared__ unsigned s_t0;
+  __shared__ unsigned s_t0, s_hint, s_kmid, s_klow;
+  __shared__ int s_wlo, s_whi;  // the workers whose shares meet a task's row
+  __shared__ int s_ccnt;  // a worker's candidates of the current segment
   const KvView& kv = a.kv;
   const Ws& W = a.ws;
   const int page = kv.p, G = kv.G, tiles = page / 16, S = a.stages;
@@ -191,13 +222,14 @@ __global__ void __launch_bounds__(kThreads, 1)
   const bool split = 4 * n_tasks <= grid;
   const int work_base = split ? n_tasks : 0, workers = grid - work_base;
   const int wk = cta - work_base;  // rank among the workers (negative: a task CTA)
-  // a worker's equal share [s_beg, s_end) of the (row, page) slots, and its items of P_t
-  // (item wk + j * workers for j < my_items)
+  // a worker's equal share [s_beg, s_end) of the (row, page) slots.  The items of P_t (the
+  // speculative pages) are spread over every CTA's TMA issue warp, which attends them while the
+  // compute warps score: this CTA's items are cta + j * grid for j < my_items.
   const long long T = static_cast<long long>(rows) * n;
   const long long s_beg = wk < 0 ? 0 : static_cast<long long>(wk) * T / workers;
   const long long s_end = wk < 0 ? 0 : static_cast<long long>(wk + 1) * T / workers;
   const int n_items = rows * kp;
-  const int my_items = wk >= 0 && wk < n_items ? (n_items - 1 - wk) / workers + 1 : 0;
+  const int my_items = cta < n_items ? (n_items - 1 - cta) / grid + 1 : 0;
 
   volatile int* stage_ok = s_ctl;  // -1 nothing, 0 empty part, 1 page loaded
   volatile int* stage_pos = s_ctl + S;
@@ -212,6 +244,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     s_issued = 0;
   }
   __syncthreads();
+  DSA_TRACE_BEGIN();
 
   // ---- the TMA ring, shared by the speculative pages (workers) and the missed pages (tasks):
   // ring position j uses stage j % S with phase parity (j / S) & 1 and is consumed by warp j % S,
@@ -298,106 +331,26 @@ __global__ void __launch_bounds__(kThreads, 1)
 
   if (warp == kW) {
     // ================================================================ TMA issue warp
+    // this CTA's items of P_t: lane 0 issues up to S of them at once, the warp attends each into
+    // its page records (published per item), and each stage it frees takes the item S later
+    auto issue_item = [&](int j) -> bool {
+      const int it = cta + j * grid;
+      const int row = it / kp, slot = it - row * kp;
+      // the three loads go out together
+      const int cnt = a.spec_count[row];
+      const int pos = a.spec_idx[static_cast<size_t>(row) * kp + slot];
+      const int npos = (request_len(kv, row / kv.Hkv) + page - 1) / page;
+      return issue(j, row, pos, slot < min(max(cnt, 0), kp), npos);
+    };
+    bool ok = true;
     if (lane == 0) {
       prefetch_tensormap(&tmK);
       prefetch_tensormap(&tmV);
-      bool ok = true;
-      for (int j = 0; j < my_items && ok; ++j) {
-        const int it = wk + j * workers;
-        const int row = it / kp, slot = it - row * kp;
-        // the three loads go out together
-        const int cnt = a.spec_count[row];
-        const int pos = a.spec_idx[static_cast<size_t>(row) * kp + slot];
-        const int npos = (request_len(kv, row / kv.Hkv) + page - 1) / page;
-        ok = issue(j, row, pos, slot < min(max(cnt, 0), kp), npos);
-      }
+      for (int j = 0; j < my_items && j < S && ok; ++j) ok = issue_item(j);
     }
-    __syncwarp();
-  } else {
-    // ================================================================ compute warps
-    float* qbar = reinterpret_cast<float*>(smem + lay.qbar_off);
-    const int gl = lane & 7, gid = tid >> 3;
-    // ---- scoring of the share, one segment (the part inside one row) at a time
-    for (long long seg = s_beg; seg < s_end;) {
-      const int row = static_cast<int>(seg / n);
-      const int j0 = static_cast<int>(seg - static_cast<long long>(row) * n);
-      const int j1 = static_cast<int>(min(s_end - static_cast<long long>(row) * n,
-                                          static_cast<long long>(n)));
-      seg = static_cast<long long>(row) * n + j1;
-      const int b = row / kv.Hkv, h = row % kv.Hkv;
-      const int32_t* table = kv.page_table + static_cast<size_t>(b) * kv.max_pages;
-      float* outs = a.scores + static_cast<size_t>(row) * n;
-      float* ell_r = a.ell + static_cast<size_t>(row) * n;
-      float* v_r = a.trend + static_cast<size_t>(row) * n;
-      float* pred_r = a.pred ? a.pred + static_cast<size_t>(row) * n : nullptr;
-      float* wpred_r = W.pred + static_cast<size_t>(row) * kv.max_pages;
-      named_barrier(1, kCT);  // the previous segment's query is no longer read
-      int nl = 0;
-      for (int jb = j0; jb < j1; jb += kRound) {
-        int ph[kRecGroup];
-        float lo[kRecGroup], vo[kRecGroup];
-#pragma unroll
-        for (int i = 0; i < kRecGroup; ++i) {
-          const int jj = jb + gid + kGroups * i;
-          ph[i] = jj < j1 && jj < kv.max_pages ? table[jj] : -1;
-          lo[i] = jj < j1 && gl == 0 ? ell_r[jj] : 0.f;
-          vo[i] = jj < j1 && gl == 0 ? v_r[jj] : 0.f;
-        }
-        if (jb == j0) {
-          nl = (request_len(kv, b) + page - 1) / page;
-          // the representative query: the mean of the group's rows (G <= 16: every load in
-          // flight, then the sum in row order, as the scoring kernel rounds it)
-          if (tid < kHeadDim) {
-            const __nv_bfloat16* qg = a.q + (static_cast<size_t>(b) * kv.Hq + h * G) * kHeadDim;
-            __nv_bfloat16 qr[kMaxGroup];
-#pragma unroll
-            for (int r = 0; r < kMaxGroup; ++r)
-              qr[r] = r < G ? qg[r * kHeadDim + tid] : __float2bfloat16(0.f);
-            float qs = 0.f;
-#pragma unroll
-            for (int r = 0; r < kMaxGroup; ++r)
-              if (r < G) qs += __bfloat162float(qr[r]);
-            qbar[tid] = qs / static_cast<float>(G);
-          }
-          named_barrier(1, kCT);
-        }
-        float qv[16];
-        group_query_dims(qbar, gl, qv);
-        uint4 rc[kRecGroup][4];
-        bool okr[kRecGroup], bad = false;
-#pragma unroll
-        for (int i = 0; i < kRecGroup; ++i) {
-          const int jj = jb + gid + kGroups * i;
-          const bool in = jj < j1 && jj < nl;
-          okr[i] = in && ph[i] >= 0 && ph[i] < kv.num_phys;
-          bad |= in && !okr[i];
-          if (okr[i]) load_record(a.meta, static_cast<size_t>(ph[i]) * kv.Hkv + h, gl, rc[i]);
-        }
-        if (gl == 0 && bad) raise_status(kv.status, DSA_STATUS_BAD_PAGE);
-#pragma unroll
-        for (int i = 0; i < kRecGroup; ++i) {
-          const int jj = jb + gid + kGroups * i;
-          const float sc = group_sum(okr[i] ? record_partial<DSA_META_MINMAX>(rc[i], qv) : 0.f);
-          if (gl == 0 && jj < j1) {
-            const float is = okr[i] ? sc : -INFINITY;
-            outs[jj] = is;
-            float l_new, v_new;
-            ema_step(is, lo[i], vo[i], DSA_EMA_UPDATE, a.alpha, a.beta, l_new, v_new);
-            const float pr = ema_predict(l_new, v_new, a.gamma);
-            ell_r[jj] = l_new;
-            v_r[jj] = v_new;
-            if (pred_r) pred_r[jj] = pr;
-            if (jj < kv.max_pages) wpred_r[jj] = pr;
-          }
-        }
-      }
-      named_barrier(1, kCT);
-      if (tid == 0) publish_add(W.done + row, static_cast<unsigned>(j1 - j0));
-    }
-
-    // ---- items: warp w < S attends this CTA's pages of P_t j = w, w + S, ... into their records
-    for (int j = warp; j < my_items && warp < S; j += S) {
-      const int it = wk + j * workers;
+    ok = __shfl_sync(0xffffffffu, ok, 0) != 0;
+    for (int j = 0; j < my_items && ok; ++j) {
+      const int it = cta + j * grid;
       const int row = it / kp, pslot = it - row * kp;
       uint32_t qa[8][4];
       warp_q(row, qa);
@@ -405,6 +358,8 @@ __global__ void __launch_bounds__(kThreads, 1)
       state_init(st);
       const int okv = attend_item(j, request_len(kv, row / kv.Hkv), qa, st);
       if (okv == -2) break;
+      if (lane == 0 && j + S < my_items) ok = issue_item(j + S);  // the stage just freed
+      ok = __shfl_sync(0xffffffffu, ok, 0) != 0;
       if (okv < 0) continue;
       state_finish(st);
       float* rec0 = a.partials + (static_cast<size_t>(row) * kp + pslot) * G * kRecordFloats;
@@ -428,8 +383,117 @@ __global__ void __launch_bounds__(kThreads, 1)
       __syncwarp();
       if (lane == 0) publish_add(W.sdone + row, 1u);
     }
+    __syncwarp();
+  } else {
+    // ================================================================ compute warps
+    float* qbar = reinterpret_cast<float*>(smem + lay.qbar_off);
+    const int gl = lane & 7, gid = tid >> 3;
+    // ---- scoring of the share, one segment (the part inside one row) at a time
+    for (long long seg = s_beg; seg < s_end;) {
+      const int row = static_cast<int>(seg / n);
+      const int j0 = static_cast<int>(seg - static_cast<long long>(row) * n);
+      const int j1 = static_cast<int>(min(s_end - static_cast<long long>(row) * n,
+                                          static_cast<long long>(n)));
+      seg = static_cast<long long>(row) * n + j1;
+      const int b = row / kv.Hkv, h = row % kv.Hkv;
+      const int32_t* table = kv.page_table + static_cast<size_t>(b) * kv.max_pages;
+      float* outs = a.scores + static_cast<size_t>(row) * n;
+      float* ell_r = a.ell + static_cast<size_t>(row) * n;
+      float* v_r = a.trend + static_cast<size_t>(row) * n;
+      float* pred_r = a.pred ? a.pred + static_cast<size_t>(row) * n : nullptr;
+      float* wpred_r = W.pred + static_cast<size_t>(row) * kv.max_pages;
+      // pages scoring at or above the row's hint (0: none) are A_t candidates, stored as they are
+      // found into this worker's slots of the row, cleared first (the merge tasks know which
+      // workers cover a row); all of it goes out well before the scores are published
+      const bool lists = wk < kMaxWorkers;
+      const uint32_t hint = lists ? W.hint[row] : 0u;
+      unsigned long long* cand_w =
+          W.cand + (static_cast<size_t>(row) * kMaxWorkers + max(wk, 0)) * kWorkerSlots;
+      if (lists && tid < kWorkerSlots) cand_w[tid] = 0ull;
+      if (tid == 0) s_ccnt = 0;
+      named_barrier(1, kCT);  // the previous segment's query is no longer read
+      int nl = 0;
+      for (int jb = j0; jb < j1; jb += kRound) {
+        // indices are clamped rather than guarded, so that every load of the round issues at once
+        int ph[kRecGroup];
+        float lo[kRecGroup], vo[kRecGroup];
+#pragma unroll
+        for (int i = 0; i < kRecGroup; ++i) {
+          const int jj = jb + gid + kGroups * i;
+          const int jc = min(jj, j1 - 1);
+          const int phv = table[min(jc, kv.max_pages - 1)];
+          const float lv = ell_r[jc], vv = v_r[jc];
+          ph[i] = jj < j1 && jj < kv.max_pages ? phv : -1;
+          lo[i] = jj < j1 ? lv : 0.f;
+          vo[i] = jj < j1 ? vv : 0.f;
+        }
+        if (jb == j0) {
+          nl = (request_len(kv, b) + page - 1) / page;
+          // the representative query: the mean of the group's rows (G <= 16: every load in
+          // flight, then the sum in row order, as the scoring kernel rounds it)
+          if (tid < kHeadDim) {
+            const __nv_bfloat16* qg = a.q + (static_cast<size_t>(b) * kv.Hq + h * G) * kHeadDim;
+            __nv_bfloat16 qr[kMaxGroup];
+#pragma unroll
+            for (int r = 0; r < kMaxGroup; ++r)
+              qr[r] = r < G ? qg[r * kHeadDim + tid] : __float2bfloat16(0.f);
+            float qs = 0.f;
+#pragma unroll
+            for (int r = 0; r < kMaxGroup; ++r)
+              if (r < G) qs += __bfloat162float(qr[r]);
+            qbar[tid] = qs / static_cast<float>(G);
+          }
+          named_barrier(1, kCT);
+          DSA_STAMP(1);  // worker: the first segment's table, state and query loaded
+        }
+        float qv[16];
+        group_query_dims(qbar, gl, qv);
+        uint4 rc[kRecGroup][4];
+        bool okr[kRecGroup], bad = false;
+#pragma unroll
+        for (int i = 0; i < kRecGroup; ++i) {
+          const int jj = jb + gid + kGroups * i;
+          const bool in = jj < j1 && jj < nl;
+          okr[i] = in && ph[i] >= 0 && ph[i] < kv.num_phys;
+          bad |= in && !okr[i];
+          // a slot without a page loads page 0's record and discards it
+          load_record(a.meta, static_cast<size_t>(okr[i] ? ph[i] : 0) * kv.Hkv + h, gl, rc[i]);
+        }
+        if (gl == 0 && bad) raise_status(kv.status, DSA_STATUS_BAD_PAGE);
+        DSA_STAMP(16);  // worker: the round's record loads issued
+#pragma unroll
+        for (int i = 0; i < kRecGroup; ++i) {
+          const int jj = jb + gid + kGroups * i;
+          const float sc = group_sum(okr[i] ? record_partial<DSA_META_MINMAX>(rc[i], qv) : 0.f);
+          if (gl == 0 && jj < j1) {
+            const float is = okr[i] ? sc : -INFINITY;
+            outs[jj] = is;
+            const uint32_t key = score_key(is);
+            if (hint != 0u && key >= hint) {
+              const int at = atomicAdd(&s_ccnt, 1);
+              cand_w[min(at, kWorkerCand)] = at < kWorkerCand ? rank_value_of(key, jj) : 1ull;
+            }
+            float l_new, v_new;
+            ema_step(is, lo[i], vo[i], DSA_EMA_UPDATE, a.alpha, a.beta, l_new, v_new);
+            const float pr = ema_predict(l_new, v_new, a.gamma);
+            ell_r[jj] = l_new;
+            v_r[jj] = v_new;
+            if (pred_r) pred_r[jj] = pr;
+            if (jj < kv.max_pages) wpred_r[jj] = pr;
+          }
+        }
+        DSA_STAMP(17);  // worker: thread 0's scores and EMA state of the round written
+      }
+      named_barrier(1, kCT);
+      DSA_STAMP(18);  // worker: the segment's rounds done (barrier)
+      if (tid == 0) publish_add(W.done + row, static_cast<unsigned>(j1 - j0));
+    }
+    DSA_STAMP(2);  // worker: its share scored and published
+
+    DSA_STAMP(3);  // the compute warps' part is over (thread 0)
   }
   __syncthreads();
+  DSA_STAMP(4);  // the CTA's worker part is over
   if (*abort_flag) {
     drain();
     return;
@@ -594,18 +658,165 @@ __global__ void __launch_bounds__(kThreads, 1)
       side();
     } else {
       if (tid == 0) wait_count(W.done + row, static_cast<unsigned>(n), abort_flag, kv.status);
+      DSA_STAMP(6);  // task: the row's scores are complete
       int total = -1;
       if (!named_barrier_or(1, kCT, *abort_flag)) {
         load_keys(src, n_src);
         named_barrier(1, kCT);
+        DSA_STAMP(7);  // task: keys loaded
         total = select_fast(kk, cntP, out);
       }
       if (tid == 0) s_red[3] = total;
     }
     __syncthreads();
+    DSA_STAMP(8);  // task: ranked
     if (*abort_flag) return -2;
     const int total = s_red[3];
     return total >= 0 ? total : select_all(kk, out);
+  };
+  // A_t for a merge task (compute warps).  The workers appended every page of the row scoring at or
+  // above its hint to the row's candidate list; when at least kk pages did, the row's kk best are
+  // among them, so only the list is ranked: the kk best are marked in a bitmap and read out in
+  // ascending order.  For the next step's hint the keys of rank C / 2 and C - 1 go to s_kmid and
+  // s_klow, and the key of rank 1.5 kk - 1 to s_hint (0 when the list is shorter).  Otherwise (no hint yet, the scores moved below it, or more than
+  // kCandCap candidates) returns -1 with the row's keys in place for the caller's full selection.
+  // -2 after a timeout.  Bitmaps (rows of at most kBitsMax pages): ts.bits[0, w) A_t,
+  // ts.bits[kBitsMax / 32, +w) P_t, the latter marked while the workers still score the row.
+  auto select_merge = [&](int row, int kk, int cntP, int32_t* out) -> int {
+    const int nwords = (n + 31) >> 5;
+    uint32_t* abits = ts.bits;
+    uint32_t* pbits = ts.bits + kBitsMax / 32;
+    unsigned long long* cv = reinterpret_cast<unsigned long long*>(ts.hist);
+    if (n <= kBitsMax)
+      for (int w = tid; w < nwords; w += kCT) abits[w] = pbits[w] = 0u;
+    if (tid == 0) {
+      s_hint = 0u;
+      ts.n_cand = 0;
+      // the workers whose shares [w T / workers, (w + 1) T / workers) meet [r0, r1): from the
+      // one holding slot r0 to the one holding slot r1 - 1
+      const long long r0 = static_cast<long long>(row) * n, r1 = r0 + n;
+      auto holder = [&](long long x) {
+        int w = static_cast<int>(min(static_cast<long long>(workers - 1), x * workers / T));
+        while (w > 0 && static_cast<long long>(w) * T / workers > x) --w;
+        while (w + 1 < workers && static_cast<long long>(w + 1) * T / workers <= x) ++w;
+        return w;
+      };
+      s_wlo = holder(r0);
+      s_whi = holder(r1 - 1);
+    }
+    named_barrier(1, kCT);
+    if (n <= kBitsMax)
+      for (int i = tid; i < cntP; i += kCT)
+        if (pl[i] >= 0 && pl[i] < n) atomicOr(&pbits[pl[i] >> 5], 1u << (pl[i] & 31));
+    if (tid == 0) wait_count(W.done + row, static_cast<unsigned>(n), abort_flag, kv.status);
+    DSA_STAMP(6);  // task: the row's scores are complete
+    if (named_barrier_or(1, kCT, *abort_flag)) return -2;
+    // the workers whose shares meet the row: half a warp per worker's line (lane s reads slot s),
+    // every round's load in flight; a warp claims the slots of all its workers' candidates at once
+    constexpr int kRounds = (kMaxWorkers + 2 * kW - 1) / (2 * kW);
+    int C = 0;
+    // (fewer slots than workers leave some shares empty, their lines unwritten: no list then)
+    bool over = workers > kMaxWorkers || T < workers;
+    if (!over) {
+      const int half = lane >> 4, sl = lane & 15;
+      const int wlo = s_wlo, whi = s_whi;
+      unsigned long long v[kRounds];
+#pragma unroll
+      for (int rr = 0; rr < kRounds; ++rr) {
+        const int w = (rr * kW + warp) * 2 + half;
+        const bool mine = w >= wlo && w <= whi;
+        const size_t line = static_cast<size_t>(row) * kMaxWorkers + min(w, kMaxWorkers - 1);
+        const unsigned long long x = __ldcg(W.cand + line * kWorkerSlots + sl);
+        v[rr] = mine ? x : 0ull;
+      }
+      int wsum = 0;  // this warp's candidates before each round, then in all
+      bool ovf = false;
+      int off[kRounds];
+#pragma unroll
+      for (int rr = 0; rr < kRounds; ++rr) {
+        const unsigned bal = __ballot_sync(0xffffffffu, v[rr] != 0ull && sl < kWorkerCand);
+        ovf |= sl == kWorkerCand && v[rr] != 0ull;
+        const int c_lo = __popc(bal & 0x7fffu), c_hi = __popc((bal >> 16) & 0x7fffu);
+        off[rr] = wsum + (half ? c_lo : 0);
+        wsum += c_lo + c_hi;
+      }
+      if (__any_sync(0xffffffffu, ovf) && lane == 0) s_hint = 1u;  // (an overflow, until below)
+      int base = 0;
+      if (lane == 0 && wsum > 0) base = atomicAdd(&ts.n_cand, wsum);
+      base = __shfl_sync(0xffffffffu, base, 0);
+#pragma unroll
+      for (int rr = 0; rr < kRounds; ++rr) {
+        const int at = base + off[rr] + sl;
+        if (sl < kWorkerCand && v[rr] != 0ull && at < kTopkMaxCand) cv[at] = v[rr];
+      }
+      named_barrier(1, kCT);
+      C = ts.n_cand;
+      over = s_hint != 0u || C > kTopkMaxCand;
+    }
+    if (over || C < kk || n > kBitsMax || kk < 1) {
+      named_barrier(1, kCT);
+      if (tid == 0) s_hint = 0u;
+      load_keys(a.scores + static_cast<size_t>(row) * n, n);
+      named_barrier(1, kCT);
+      return -1;
+    }
+    if (tid == 0) {
+      s_red[2] = C;
+      s_kmid = s_klow = 0u;
+      cv[C] = 0ull;  // the pair loads read one past an odd count
+    }
+    DSA_STAMP(7);  // task: candidates loaded
+    named_barrier(1, kCT);
+    // candidate i is among the kk best when fewer than kk rank values exceed its own; two threads
+    // per candidate split the comparisons when the candidates are few
+    const int tpc = C <= kCT / 2 ? 2 : 1;
+    const int hint_rank = kk + kk / 2 - 1;
+    for (int i0 = 0; i0 < C; i0 += kCT / tpc) {
+      const int i = i0 + tid / tpc, part = tid % tpc;
+      int r = 0;
+      unsigned long long vi = 0ull;
+      if (i < C) {
+        vi = cv[i];
+        const ulonglong2* c2 = reinterpret_cast<const ulonglong2*>(cv);
+#pragma unroll 4
+        for (int q2 = part; q2 < ((C + 1) >> 1); q2 += tpc) {
+          const ulonglong2 x = c2[q2];
+          r += (x.x > vi) + (x.y > vi);
+        }
+      }
+      if (tpc == 2) r += __shfl_xor_sync(0xffffffffu, r, 1);
+      if (i < C && part == 0) {
+        if (r < kk) {
+          const int pos = rank_pos_of(vi);
+          atomicOr(&abits[pos >> 5], 1u << (pos & 31));
+        }
+        if (r == hint_rank) s_hint = static_cast<uint32_t>(vi >> 32);
+        if (r == C / 2) s_kmid = static_cast<uint32_t>(vi >> 32);
+        if (r == C - 1) s_klow = static_cast<uint32_t>(vi >> 32);
+      }
+    }
+    named_barrier(1, kCT);
+    // the marked positions in ascending order: thread t reads A's bitmap words [t*wpt, (t+1)*wpt)
+    {
+      const int wpt = (nwords + kCT - 1) / kCT;
+      const int w0 = min(nwords, tid * wpt), w1 = min(nwords, w0 + wpt);
+      int cnt = 0;
+      for (int w = w0; w < w1; ++w) cnt += __popc(abits[w]);
+      int incl = cnt;
+#pragma unroll
+      for (int o = 1; o < 32; o <<= 1) {
+        const int y = __shfl_up_sync(0xffffffffu, incl, o);
+        if (lane >= o) incl += y;
+      }
+      if (lane == 31) ts.wcnt[warp] = incl;
+      named_barrier(1, kCT);
+      int at = incl - cnt;
+      for (int w = 0; w < warp; ++w) at += ts.wcnt[w];
+      for (int w = w0; w < w1; ++w)
+        for (uint32_t m = abits[w]; m != 0u; m &= m - 1u) out[at++] = (w << 5) + __ffs(m) - 1;
+    }
+    DSA_STAMP(14);  // task: A_t ranked (compute warps)
+    return kk;      // exactly kk candidates rank below kk (C >= kk, rank values distinct)
   };
   auto load_plist = [&](int row) -> int {
     const int cntP = min(max(a.spec_count[row], 0), kp);
@@ -636,6 +847,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     const size_t qhead = static_cast<size_t>(b) * kv.Hq + static_cast<size_t>(row % kv.Hkv) * G + g;
     const int cntP = load_plist(row);
     __syncthreads();
+    DSA_STAMP(5);  // task (merge): start
     const float* recs = a.partials + static_cast<size_t>(row) * kp * G * kRecordFloats;
     // the issue warp: once the row's records are written, query head g's of them on chip
     auto fetch_records = [&]() {
@@ -651,12 +863,69 @@ __global__ void __launch_bounds__(kThreads, 1)
       }
       cp_async_wait_all();
     };
-    int cntA = select_task(row, a.scores + static_cast<size_t>(row) * n, n, a.k, cntP, sA,
-                           fetch_records);
-    if (cntA == -2) break;
+    int cntA;
+    if (warp == kW) {
+      fetch_records();
+    } else {
+      const int got = select_merge(row, a.k, cntP, sA);
+      if (tid == 0) s_red[3] = got;
+    }
+    __syncthreads();
+    if (*abort_flag) break;
+    DSA_STAMP(8);  // task: ranked
+    cntA = s_red[3];
+    const bool bits_ok = cntA >= 0;  // the A_t and P_t bitmaps hold
+    if (cntA == -1) {  // the keys are in place: P_t's bound over them, else every key
+      DSA_STAMP(15);   // task: A_t from the keys
+      if (warp < kW) {
+        const int t = select_fast(a.k, cntP, sA);
+        if (tid == 0) s_red[3] = t;
+      }
+      __syncthreads();
+      cntA = s_red[3];
+      if (cntA < 0) cntA = select_all(a.k, sA);
+    }
     if (g == 0) {  // the first query head's task publishes A_t
       for (int i = tid; i < a.k; i += kThreads) a.idx[static_cast<size_t>(row) * a.k + i] = sA[i];
       if (tid == 0) a.count[row] = cntA;
+    }
+    if (g == 0) {  // the next step's hint (any value is safe; it only decides the speed)
+      if (!bits_ok) {  // from the row's k best (the keys are still in place): ranks k / 2, k - 1
+        uint32_t* kA = reinterpret_cast<uint32_t*>(mlist);  // their keys, staged once
+        if (tid == 0) s_kmid = s_klow = 0u;
+        for (int i = tid; i < cntA; i += kThreads) kA[i] = keys[sA[i]];
+        __syncthreads();
+        for (int i0 = 0; i0 < cntA; i0 += kThreads / 4) {  // four threads per key
+          const int i = i0 + (tid >> 2), part = tid & 3;
+          int r = 0;
+          if (i < cntA) {
+            const uint32_t ki = kA[i];
+            for (int j = part; j < cntA; j += 4) r += kA[j] > ki || (kA[j] == ki && j < i);
+          }
+          r += __shfl_xor_sync(0xffffffffu, r, 1);
+          r += __shfl_xor_sync(0xffffffffu, r, 2);
+          if (i < cntA && part == 0) {
+            if (r == cntA / 2) s_kmid = kA[i];
+            if (r == cntA - 1) s_klow = kA[i];
+          }
+        }
+        __syncthreads();
+      }
+      if (tid == 0) {
+        // the exact key of rank 1.5k - 1 when the list reached it.  Else, taking the top scores'
+        // log-rank as linear in the score (a drop of d per doubling of the rank, d measured from
+        // rank seen / 2 to seen - 1), the score where rank 1.75k would stand
+        const int seen = bits_ok ? s_red[2] : cntA;
+        uint32_t h = s_hint;
+        if (h == 0u && seen >= 4 && s_kmid != 0u && s_klow != 0u) {
+          const float mid = key_score(s_kmid), low = key_score(s_klow);
+          const float doublings = log2f(static_cast<float>(seen) / (seen / 2 + 1));
+          const float d = (mid - low) / doublings;
+          const float want = low - d * log2f(1.75f * a.k / static_cast<float>(seen));
+          h = (isfinite(want) && want < low) ? score_key(want) : s_klow;
+        }
+        W.hint[row] = h;
+      }
     }
     cntA = min(max(cntA, 0), a.k);
     // merged speculative parts (warp 0): P slots whose page is in A (every slot in superset
@@ -665,7 +934,11 @@ __global__ void __launch_bounds__(kThreads, 1)
       int np = 0;
       for (int base = 0; base < cntP; base += 32) {
         const int i = base + lane;
-        const bool take = i < cntP && (a.superset || contains_sorted(sA, cntA, pl[i]));
+        const bool take =
+            i < cntP && (a.superset ||
+                         (bits_ok ? pl[i] >= 0 && pl[i] < n &&
+                                        ((ts.bits[pl[i] >> 5] >> (pl[i] & 31)) & 1u) != 0u
+                                  : contains_sorted(sA, cntA, pl[i])));
         const unsigned bal = __ballot_sync(0xffffffffu, take);
         if (take) parts[np + __popc(bal & below)] = i;
         np += __popc(bal);
@@ -675,7 +948,9 @@ __global__ void __launch_bounds__(kThreads, 1)
       int nm = 0;
       for (int base = 0; base < cntA; base += 32) {
         const int i = base + lane;
-        const bool miss = i < cntA && !contains_sorted(pl, cntP, sA[i]);
+        const bool miss =
+            i < cntA && !(bits_ok ? ((ts.bits[kBitsMax / 32 + (sA[i] >> 5)] >> (sA[i] & 31)) & 1u) != 0u
+                                  : contains_sorted(pl, cntP, sA[i]));
         const unsigned bal = __ballot_sync(0xffffffffu, miss);
         if (miss) mlist[nm + __popc(bal & below)] = sA[i];
         nm += __popc(bal);
@@ -683,6 +958,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       if (lane == 0) s_red[1] = nm;
     }
     __syncthreads();
+    DSA_STAMP(9);  // task: merged and missed lists
     const int n_parts = s_red[0], n_miss = s_red[1];
     // ---- the missed pages through the ring: warp w < S attends pages w, w + S, ... into one
     // state and leaves query head g's part of it (unnormalised O, max in log2 units, sum) in
@@ -721,6 +997,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     }
     ring += n_miss;
     __syncthreads();
+    DSA_STAMP(10);  // task: missed pages attended
     if (*abort_flag) break;
     // without the on-chip copy, the records are read from L2 once the row's are complete
     if (!a.rec_smem) {
@@ -729,6 +1006,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       if (*abort_flag) break;
     }
 
+    DSA_STAMP(11);  // task: records ready
     float wm = -INFINITY, wl = 0.f;  // this warp's state: max (log2 units), sum, unnormalised O
     float4 wo = make_float4(0.f, 0.f, 0.f, 0.f);
     auto absorb = [&](float m2, float l, float4 o) {  // adds a part (max m2, sum l, O = o * l)
@@ -801,6 +1079,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         a.l[qhead] = lsum;
       }
     }
+    DSA_STAMP(12);  // task: output written
   }
   __syncthreads();
   if (*abort_flag) {
@@ -820,6 +1099,8 @@ __global__ void __launch_bounds__(kThreads, 1)
       __threadfence();
     }
   }
+  DSA_STAMP(13);  // end
+  DSA_TRACE_END(g_trace_prr);
 }
 
 // The deepest ring, with a task's records on chip if possible, that fits the shared-memory limit.
@@ -889,6 +1170,8 @@ cudaError_t launch_prr_step(const CUtensorMap& tmK, const CUtensorMap& tmV, cons
   a.ws.exit = reinterpret_cast<unsigned*>(w + wl.exit_off);
   a.ws.done = reinterpret_cast<unsigned*>(w + wl.done_off);
   a.ws.sdone = reinterpret_cast<unsigned*>(w + wl.sdone_off);
+  a.ws.hint = reinterpret_cast<uint32_t*>(w + wl.hint_off);
+  a.ws.cand = reinterpret_cast<unsigned long long*>(w + wl.cand_off);
   a.ws.pred = reinterpret_cast<float*>(w + wl.pred_off);
   const Shape sh = choose_shape(s.kv.p, s.stride, s.k_pred, static_smem());
   if (sh.stages < 1) return cudaErrorInvalidConfiguration;
@@ -921,3 +1204,16 @@ cudaError_t launch_prr_step(const CUtensorMap& tmK, const CUtensorMap& tmV, cons
 }
 
 }  // namespace dsa
+
+#ifdef DSA_TIMELINE
+// Phase-trace accessors of the traced library (see DSA_TRACE_BEGIN).
+extern "C" int dsa_trace_read_prr(void* host, size_t bytes) {
+  return static_cast<int>(cudaMemcpyFromSymbol(
+      host, dsa::g_trace_prr, bytes < sizeof(dsa::g_trace_prr) ? bytes : sizeof(dsa::g_trace_prr)));
+}
+extern "C" int dsa_trace_clear_prr() {
+  void* p = nullptr;
+  cudaError_t e = cudaGetSymbolAddress(&p, dsa::g_trace_prr);
+  return static_cast<int>(e == cudaSuccess ? cudaMemset(p, 0, sizeof(dsa::g_trace_prr)) : e);
+}
+#endif

@@ -21,6 +21,9 @@
 #include "select.cuh"
 
 namespace dsa {
+#ifdef DSA_TIMELINE
+__device__ unsigned long long g_trace_threshold[kTraceCtas * 2 * kTraceSlots];
+#endif
 namespace {
 
 constexpr int kThrWarps = 8;
@@ -174,6 +177,7 @@ __global__ void __launch_bounds__(kThrThreads)
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
   const uint32_t stage_bytes = 512u * page;
   const uint32_t smem_base = smem_u32(smem);
+  DSA_TRACE_BEGIN();
 
   // ---- the row's scores: one bulk copy of the whole row, issued before anything else and not
   // waiting for the request length (the unaligned head and tail, at most 3 floats each, by plain
@@ -227,6 +231,7 @@ __global__ void __launch_bounds__(kThrThreads)
     }
     return;
   }
+  DSA_STAMP(1);           // the score row has landed
   if (streaming) return;  // the streaming path serves this head
   const int npos = (L + page - 1) / page;
   const int n = min(npos, nload);
@@ -236,6 +241,7 @@ __global__ void __launch_bounds__(kThrThreads)
   thread_top2<true>(keys, n, tid, mine, second, jmine, c);
   // the page-table entry of this thread's largest key, loaded now and used once the chunk is
   // ranked (most of a chunk's blocks are some thread's largest key)
+  DSA_STAMP(2);  // keys converted
   const int32_t* pt_row = kv.page_table + static_cast<size_t>(b) * kv.max_pages;
   int my_phys = mine != 0u ? pt_row[jmine] : kPhysUnknown;
   {
@@ -288,6 +294,7 @@ __global__ void __launch_bounds__(kThrThreads)
       for (int w = 0; w < kThrWarps; ++w) n_valid += s_red[w];
       total = min(a.cap, n_valid);
     }
+    DSA_STAMP(3);  // warp keys shared
     if (visited >= total) break;
     const int ch = min(chunk, total - visited);
     unsigned long long bound = 0ull;  // candidates: rank values at or above it
@@ -336,6 +343,7 @@ __global__ void __launch_bounds__(kThrThreads)
       __syncthreads();
       bound = *s_bound;
     }
+    DSA_STAMP(4);  // bound
     // every thread checks its own keys against the bound (sixteen loads in flight, compared as
     // 32-bit words) and each warp claims the slots of its hits with one atomic; only the key
     // positions where some lane of the warp hit are then visited.  A hit that is the thread's
@@ -373,6 +381,7 @@ __global__ void __launch_bounds__(kThrThreads)
       }
     }
     __syncthreads();
+    DSA_STAMP(5);  // candidates collected
     const int C = min(misc[3], cand_cap);
     // ranks: eight threads per candidate, each counting a strided eighth of the candidates above it
     for (int i0 = 0; i0 < C; i0 += kThrThreads / 8) {
@@ -394,6 +403,7 @@ __global__ void __launch_bounds__(kThrThreads)
     }
     fence_proxy_async_smem();  // the candidates' space is the stage area TMA writes next
     __syncthreads();
+    DSA_STAMP(6);  // ranked
     // ---- 2. blocks w and w + 8 of the chunk are warp w's: lane 0 completes their page-table entries
     // and issues their TMA loads (the warps issue in parallel), posting the bytes before its one
     // arrival per chunk
@@ -419,9 +429,11 @@ __global__ void __launch_bounds__(kThrThreads)
       }
       mbar_arrive(full);
     }
+    DSA_STAMP(7);  // TMA issued
     const bool ok_wait = mbar_wait(smem_u32(&bar), phase & 1u, abort_flag, kv.status);
     ++phase;
     if (named_barrier_or(1, kThrThreads, !ok_wait || *abort_flag)) break;
+    DSA_STAMP(8);  // pages landed
 
     // ---- 3. per-block softmax mass (log2 units) of every query row, one warp per block
     for (int cc = warp; cc < ch; cc += kThrWarps) {
@@ -476,6 +488,7 @@ __global__ void __launch_bounds__(kThrThreads)
     }
     __syncthreads();
 
+    DSA_STAMP(9);  // masses
     // ---- 4. stop rule.  AS_acc and AS_min after each block of the chunk (in rank order) are prefix
     // sums / minima over the chunk on top of the state before it, scanned with lane
     // (head slot gl, block cc) = (lane / 16, lane % 16), two query heads per round; the chunk's
@@ -535,6 +548,7 @@ __global__ void __launch_bounds__(kThrThreads)
       }
     }
 
+    DSA_STAMP(10);  // stop decided
     // ---- 5. P.V for the accepted blocks, one warp per block
     bool wrote = false;
     for (int cc = warp; cc < accepted; cc += kThrWarps) {
@@ -559,8 +573,10 @@ __global__ void __launch_bounds__(kThrThreads)
     }
     if (tid < accepted) idx_out[visited + tid] = s_ranked[tid];
     visited += accepted;
+    DSA_STAMP(11);  // P.V (thread 0's warp)
     if (wrote) fence_proxy_async_smem();
     __syncthreads();
+    DSA_STAMP(12);  // chunk done
     if (stop || visited >= total) break;
   }
   if (tid == 0) a.count[row] = visited;
@@ -604,6 +620,8 @@ __global__ void __launch_bounds__(kThrThreads)
       a.l[qh] = Lsum;
     }
   }
+  DSA_STAMP(13);  // merged and written
+  DSA_TRACE_END(g_trace_threshold);
 }
 
 }  // namespace
@@ -621,3 +639,16 @@ cudaError_t launch_threshold(const CUtensorMap& tmK, const CUtensorMap& tmV,
 size_t threshold_smem_bytes(int page, int max_pages) { return thr_layout(page, max_pages).total; }
 
 }  // namespace dsa
+
+#ifdef DSA_TIMELINE
+// Phase-trace accessors of the traced library (see DSA_TRACE_BEGIN).
+extern "C" int dsa_trace_read_threshold(void* host, size_t bytes) {
+  return static_cast<int>(cudaMemcpyFromSymbol(
+      host, dsa::g_trace_threshold, bytes < sizeof(dsa::g_trace_threshold) ? bytes : sizeof(dsa::g_trace_threshold)));
+}
+extern "C" int dsa_trace_clear_threshold() {
+  void* p = nullptr;
+  cudaError_t e = cudaGetSymbolAddress(&p, dsa::g_trace_threshold);
+  return static_cast<int>(e == cudaSuccess ? cudaMemset(p, 0, sizeof(dsa::g_trace_threshold)) : e);
+}
+#endif

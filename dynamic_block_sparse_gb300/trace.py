@@ -1,0 +1,202 @@
+"""Phase timelines of the fused kernels, read from the tracing build of the library.
+
+    python -m dynamic_block_sparse_gb300.trace threshold   # PSA threshold kernel on psa_threshold
+    python -m dynamic_block_sparse_gb300.trace prr         # fused PRR step on prr_512k
+
+Builds ``libdsa_trace.so`` (every kernel compiled with ``-DDSA_TIMELINE``), runs the workload's
+step several times cold (L2 flushed before each launch) and warm (launches back to back), and
+prints for every stamp the median and the maximum over the CTAs of all runs: clock64 cycles since
+the CTA's own start, and %globaltimer nanoseconds since the earliest CTA start of the launch.  The
+tracing build adds a barrier at each instrumented kernel's start and a few tens of cycles per
+stamp; the stamps bound phases approximately (the compiler orders them against the surrounding
+code only as it orders volatile operations).  The fused PRR step's CTAs are reported by role:
+workers (scoring, speculative pages), merge task CTAs (A_t, repair, merge) and the P_{t+1}
+selection CTAs.
+"""
+
+from __future__ import annotations
+
+import argparse
+import ctypes
+import statistics
+import sys
+
+import numpy as np
+
+LABELS = {
+    "threshold": {
+        1: "score row landed",
+        2: "keys converted, two largest per thread",
+        3: "warp keys shared (barrier)",
+        4: "chunk bound",
+        5: "candidates collected (barrier)",
+        6: "ranked (barrier)",
+        7: "page-table entries done, TMA issued",
+        8: "pages landed",
+        9: "block masses (barrier)",
+        10: "stop rule decided",
+        11: "P.V done (thread 0's warp)",
+        12: "chunk done (barrier)",
+        13: "warp states merged, output written",
+    },
+    "prr": {
+        1: "worker: first segment's table, state and query loaded",
+        2: "worker: share scored, EMA updated, published",
+        3: "worker: compute warps' part over (thread 0)",
+        4: "worker part and this CTA's P_t pages over (barrier)",
+        5: "task: start",
+        6: "task: the row's scores complete",
+        7: "task: keys loaded",
+        8: "task: ranked, records fetched (barrier)",
+        9: "task: merged and missed lists",
+        10: "task: missed pages attended",
+        11: "task: records ready",
+        12: "task: output written",
+        13: "end",
+        14: "task: A_t ranked from the candidate list (compute warps)",
+        15: "task: A_t from the row's keys (no usable list)",
+        16: "worker: first round's record loads issued",
+        17: "worker: thread 0's first-round scores and EMA written",
+        18: "worker: first segment's rounds done (barrier)",
+    },
+}
+SLOTS = 32
+CTAS = 1024
+
+
+def _flusher(torch, dev):
+    wbuf = torch.empty(256 << 20, dtype=torch.uint8, device=dev)
+    rbuf = torch.ones(64 << 20, dtype=torch.int32, device=dev)
+    sink = torch.empty((), dtype=torch.int32, device=dev)
+
+    def flush(i):
+        wbuf.fill_(i & 255)
+        torch.amax(rbuf, dim=0, out=sink)
+    return flush
+
+
+def _setup(kernel, B, torch):
+    from dynamic_block_sparse_gb300.pipeline import Cache, PRRDecoder, ThresholdDecoder
+    from dynamic_block_sparse_gb300.workloads import BY_NAME, make_inputs
+
+    if kernel == "threshold":
+        w = BY_NAME["psa_threshold"]
+        inp = make_inputs(w, "cuda", shuffle_pages=False)
+        cache = Cache.from_inputs(inp, "cuda")
+        dec = ThresholdDecoder(cache, w.tau, w.cap)
+        dec.build_meta()
+        q = inp["q"][0].clone()
+        dec.step(q)
+
+        def step(i):
+            B.dsa_select_threshold(cache.kv, q, dec.scores, w.tau, w.cap, dec.scale, dec.idx,
+                                   dec.count, dec.out, dec.m, dec.l)
+        return step, cache
+    w = BY_NAME["prr_512k"]
+    inp = make_inputs(w, "cuda", shuffle_pages=False)
+    cache = Cache.from_inputs(inp, "cuda")
+    dec = PRRDecoder(cache, w.k, w.k_pred, w.alpha, w.beta, w.gamma)
+    dec.build_meta()
+    qs = inp["q"]
+    q = qs[0].clone()
+    dec.step(q)
+    for i in range(1, 4):
+        q.copy_(qs[i])
+        dec.step(q)
+
+    def step(i):
+        q.copy_(qs[4 + i % (qs.shape[0] - 4)])
+        dec.step(q)
+    return step, cache
+
+
+def _collect(kernel, lib, step, flush, torch, cold: bool, runs: int):
+    read = getattr(lib, f"dsa_trace_read_{kernel}")
+    clear = getattr(lib, f"dsa_trace_clear_{kernel}")
+    read.argtypes, read.restype = [ctypes.c_void_p, ctypes.c_size_t], ctypes.c_int
+    clear.argtypes, clear.restype = [], ctypes.c_int
+    out = []
+    for i in range(runs):
+        if clear() != 0:
+            raise RuntimeError("trace clear failed")
+        torch.cuda.synchronize()
+        if cold:
+            flush(i)
+        else:
+            step(i)  # the launch before the traced one: code and data warm
+        if not cold:
+            if clear() != 0:
+                raise RuntimeError("trace clear failed")
+        step(i)
+        torch.cuda.synchronize()
+        buf = np.zeros(CTAS * 2 * SLOTS, dtype=np.uint64)
+        if read(buf.ctypes.data_as(ctypes.c_void_p), buf.nbytes) != 0:
+            raise RuntimeError("trace read failed")
+        out.append(buf.reshape(CTAS, 2, SLOTS).astype(np.int64))
+    return out
+
+
+def _report(kernel, runs, title):
+    labels = LABELS[kernel]
+    groups = {"all CTAs": None}
+    if kernel == "prr":  # by the first stamp only that role passes (next-P: 6 without 5)
+        groups = {"worker CTAs": 1, "merge task CTAs": 5, "next-P selection CTAs": -6}
+    print(f"-- {title}")
+    for gname, marker in groups.items():
+        cyc = {k: [] for k in labels}
+        ns = {k: [] for k in labels}
+        n_ctas = 0
+        for tr in runs:
+            started = tr[:, 0, 0] > 0
+            if not started.any():
+                continue
+            g0 = tr[started, 1, 0].min()
+            if marker is None:
+                sel = started
+            elif marker > 0:
+                sel = started & (tr[:, 0, marker] > 0)
+            else:
+                sel = started & (tr[:, 0, -marker] > 0) & (tr[:, 0, 5] == 0)
+            n_ctas += int(sel.sum())
+            for k in labels:
+                hit = sel & (tr[:, 0, k] > 0)
+                cyc[k] += (tr[hit, 0, k] - tr[hit, 0, 0]).tolist()
+                ns[k] += (tr[hit, 1, k] - g0).tolist()
+        print(f"   {gname} ({n_ctas // max(1, len(runs))} per launch)"
+              f"{'':14s} cycles since CTA start        ns since launch start")
+        for k, name in labels.items():
+            if not cyc[k]:
+                continue
+            print(f"   {k:2d} {name:46s} median {int(statistics.median(cyc[k])):7d} max "
+                  f"{max(cyc[k]):7d}   median {int(statistics.median(ns[k])):7d} max {max(ns[k]):7d}"
+                  f"   ({len(cyc[k])} CTA stamps)")
+
+
+def main(argv=None):
+    p = argparse.ArgumentParser(description=__doc__.split("\n\n")[0])
+    p.add_argument("kernel", choices=sorted(LABELS))
+    p.add_argument("--runs", type=int, default=5)
+    args = p.parse_args(argv)
+    import torch
+
+    from dynamic_block_sparse_gb300 import binding as B
+    from dynamic_block_sparse_gb300 import build as Bd
+
+    if not torch.cuda.is_available():
+        raise SystemExit("the tracing build runs on a CUDA device")
+    lib = B.load(Bd.build_traced())
+    step, cache = _setup(args.kernel, B, torch)
+    flush = _flusher(torch, "cuda")
+    for i in range(3):
+        step(i)
+    torch.cuda.synchronize()
+    _report(args.kernel, _collect(args.kernel, lib, step, flush, torch, True, args.runs),
+            f"{args.kernel}: cold launches (L2 flushed before each), {args.runs} runs")
+    _report(args.kernel, _collect(args.kernel, lib, step, flush, torch, False, args.runs),
+            f"{args.kernel}: warm launches (right after the same step), {args.runs} runs")
+    if int(cache.status.item()) != 0:
+        raise SystemExit(f"device status raised: {int(cache.status.item())}")
+
+
+if __name__ == "__main__":
+    sys.exit(main())

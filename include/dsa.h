@@ -396,11 +396,16 @@ size_t dsa_calibrate_ema_workspace_size(int32_t steps, int32_t rows, int32_t n, 
  *                        dsa_prr_step_counter_bytes(kv) bytes hold per-row counters and must be
  *                        ZERO-FILLED before the first use; every call that completes leaves them
  *                        at zero again.  If a call raised DSA_STATUS_TIMEOUT they must be
- *                        zero-filled again.  The rest is scratch the call writes before it reads.
- * A_t is selected exactly, but its search is speculative too: T0, the k-th largest true score over
- * P_t's pages, bounds the k-th largest of all scores from below, so only the pages scoring >= T0
- * are ranked (likewise P_{t+1} with the k_pred-th largest prediction over P_t); when P_t has fewer
- * than k scored pages, or more than 512 pages pass the bound, every entry of the row is ranked.
+ *                        zero-filled again.  Next come per-row candidate hints that each call
+ *                        reads and rewrites for the next one (any contents are safe: they only
+ *                        decide how fast A_t is found; zero them with the counters to start
+ *                        clean), then scratch the call writes before it reads.
+ * A_t is selected exactly, but its search is speculative: while scoring, the kernel lists the pages
+ * of each row that score at or above the row's hint (the key ranked k + k/2 at the previous call);
+ * when at least k pages are listed, the row's k best are among them and only the list is ranked.
+ * Otherwise (the first call, scores that fell below the hint, a worker CTA listing more than 15 pages
+ * of a row, or more than 512 listed pages) every entry of the row is ranked.  P_{t+1} is searched the same way from a bound, the k_pred-th
+ * largest prediction over P_t's pages, falling back to ranking every entry when it does not hold.
  */
 typedef struct dsa_prr_step_args {
   const void* q;

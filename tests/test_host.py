@@ -168,11 +168,12 @@ def test_prr_step_host_validation_without_gpu(lib):
     assert call() == -2                                               # misaligned q
     a.q = 4096
     need = lib.dsa_prr_step_workspace_size(ctypes.byref(kv))
-    # 2 rows: the exit word and two per-row counter arrays (16 bytes each), then the new
-    # predictions (max_pages_per_seq = 64 floats per row)
+    # 2 rows: the exit word and two per-row counter arrays (16 bytes each); then the per-row
+    # candidate hints (16 bytes), one 128-byte candidate line per row for each of up to 160 worker
+    # CTAs, and the new predictions (max_pages_per_seq = 64 floats per row)
     counters = 16 + 2 * 16
     assert lib.dsa_prr_step_counter_bytes(ctypes.byref(kv)) == counters
-    assert need == counters + 2 * 64 * 4
+    assert need == counters + 16 + 2 * 160 * 128 + 2 * 64 * 4
     assert lib.dsa_prr_step(ctypes.byref(kv), ctypes.byref(a), ws, need - 1, None) == -5
     kv.head_is_streaming = 4096
     assert call() == -3 and b"streaming" in lib.dsa_last_error()
