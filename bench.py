@@ -79,6 +79,9 @@ def parse_args(argv=None):
     p.add_argument("--warmup", type=int, default=20)
     p.add_argument("--impl", choices=["ours", "reference"], default="ours")
     p.add_argument("--workload", default="prr_512k")
+    p.add_argument("--layers", type=int, default=N_LAYERS,
+                   help="layers (caches) the timed steps rotate over; fewer keep the step's data "
+                        "in L2 (for profiling runs that must stay small)")
     p.add_argument("--no-e2e", action="store_true")
     p.add_argument("--cpu-seconds", type=float, default=12.0)
     p.add_argument("--no-cpu-baseline", action="store_true")
@@ -267,7 +270,7 @@ def bench_prr(args, w, dev, rank):
 
     from dynamic_block_sparse_gb300 import binding as B
 
-    n_layers = N_LAYERS
+    n_layers = max(1, args.layers)
     inputs, decs, static_q = build_layers(w, dev, n_layers)
     qs = inputs["q"]
     nq = qs.shape[0]
@@ -814,10 +817,10 @@ def main():
                           f"D{w.head_dim}, {w.seq_len} tokens, block {w.page_size}, top-{w.k}, "
                           f"|P|={w.k_pred}, EMA a{w.alpha} b{w.beta} g{w.gamma}",
               "seq_len": w.seq_len, "batch_per_gpu": w.batch,
-              "l2": f"inputs larger than L2: the steps rotate over {N_LAYERS} layers' caches "
-                    f"(each step's ~14 MB was last touched {N_LAYERS - 1} steps, ~430 MB, "
-                    "earlier; L2 is 129 MB)",
-              "timing": f"CUDA graphs of one step of each of the {N_LAYERS} layers, replayed back "
+              "l2": f"steps rotate over {args.layers} layers' caches (each step's ~14 MB was "
+                    f"last touched {args.layers - 1} steps, ~{14 * (args.layers - 1)} MB, "
+                    "earlier; L2 is 129 MB: inputs larger than L2 from 10 layers up)",
+              "timing": f"CUDA graphs of one step of each of the {args.layers} layers, replayed back "
                         "to back; CUDA events around exactly --steps steps on the launching "
                         "stream"}
 

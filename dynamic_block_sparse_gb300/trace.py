@@ -46,7 +46,7 @@ LABELS = {
         4: "worker part and this CTA's P_t pages over (barrier)",
         5: "task: start",
         6: "task: the row's scores complete",
-        7: "task: keys loaded",
+        7: "task: A_t candidates (next-P: the keys) loaded",
         8: "task: ranked, records fetched (barrier)",
         9: "task: merged and missed lists",
         10: "task: missed pages attended",
