@@ -137,6 +137,12 @@ DSA_DEV void named_barrier(int id, int count) {
   asm volatile("bar.sync %0, %1;" ::"r"(id), "r"(count) : "memory");
 }
 
+// Arrival at a named barrier without waiting (the arriving threads' earlier shared-memory writes
+// are visible to the threads that wait at it).
+DSA_DEV void named_barrier_arrive(int id, int count) {
+  asm volatile("bar.arrive %0, %1;" ::"r"(id), "r"(count) : "memory");
+}
+
 // Named barrier that also returns the OR of a predicate over the participating threads (the same
 // value in every thread).
 DSA_DEV bool named_barrier_or(int id, int count, bool pred) {
@@ -306,7 +312,21 @@ constexpr int kTraceCtas = 1024, kTraceSlots = 32;
     if (threadIdx.x < 2 * ::dsa::kTraceSlots && blockIdx.x < ::dsa::kTraceCtas)      \
       (store)[blockIdx.x * 2 * ::dsa::kTraceSlots + threadIdx.x] = s_trace_[threadIdx.x]; \
   } while (0)
+// For kernels whose threads do not all meet at the end: thread `thr` writes its stamp k straight
+// to the store (the same layout), the first time it passes it.
+#define DSA_STAMP_DIRECT(store, k, thr)                                                     \
+  do {                                                                                      \
+    if (threadIdx.x == (thr) && s_trace_[k] == 0ull && blockIdx.x < ::dsa::kTraceCtas) {    \
+      s_trace_[k] = 1ull;                                                                   \
+      (store)[blockIdx.x * 2 * ::dsa::kTraceSlots + (k)] = clock64();                       \
+      (store)[blockIdx.x * 2 * ::dsa::kTraceSlots + ::dsa::kTraceSlots + (k)] =             \
+          ::dsa::global_timer_ns();                                                         \
+    }                                                                                       \
+  } while (0)
 #else
+#define DSA_STAMP_DIRECT(store, k, thr) \
+  do {                                  \
+  } while (0)
 #define DSA_TRACE_BEGIN() \
   do {                    \
   } while (0)

@@ -24,6 +24,9 @@
 #include "internal.h"
 
 namespace dsa {
+#ifdef DSA_TIMELINE
+__device__ unsigned long long g_trace_stream[kTraceCtas * 2 * kTraceSlots];
+#endif
 namespace {
 
 constexpr int kSW = 8;                     // consumer warps
@@ -234,13 +237,26 @@ DSA_DEV int kv8_o_pos(int r, int d) {
 }
 
 // Slot range [beg, end) of the active CTA c among n over T slots.
+// (32-bit divisions when the operands fit: a 64-bit division is a long subroutine, and these sit
+// on every CTA's start-up path)
 __device__ __forceinline__ long long slot_start(long long c, long long T, long long n) {
+  const unsigned long long p = static_cast<unsigned long long>(c * T);
+  if (p <= 0xffffffffull && static_cast<unsigned long long>(n) <= 0xffffffffull)
+    return static_cast<unsigned>(p) / static_cast<unsigned>(n);
   return c * T / n;
+}
+
+// x / d for x >= 0, d > 0.
+__device__ __forceinline__ long long div_slots(long long x, long long d) {
+  if (static_cast<unsigned long long>(x) <= 0xffffffffull &&
+      static_cast<unsigned long long>(d) <= 0xffffffffull)
+    return static_cast<unsigned>(x) / static_cast<unsigned>(d);
+  return x / d;
 }
 
 // Index of the active CTA whose slot range holds slot x.
 __device__ __forceinline__ int slot_owner(long long x, long long T, long long n) {
-  return static_cast<int>(((x + 1) * n - 1) / T);
+  return static_cast<int>(div_slots((x + 1) * n - 1, T));
 }
 
 DSA_DEV bool mbar_wait_drain(uint32_t bar, uint32_t parity) {
@@ -295,8 +311,16 @@ __global__ void __launch_bounds__(kSThreads, 1)
   const uint32_t stage_bytes = lay.stage_stride;           // stage s at smem + s * stage_bytes
   const uint32_t stage_tx = KV8 ? 264u * page : 512u * page;  // bytes a stage's loads bring
   const uint32_t smem_base = smem_u32(smem);
+#ifdef DSA_TIMELINE
+  __shared__ unsigned long long s_trace_[2 * kTraceSlots];
+  if (tid < 2 * kTraceSlots) s_trace_[tid] = 0ull;
+#endif
+  DSA_STAMP_DIRECT(g_trace_stream, 0, 0);
 
-  if (warp == 0) {
+  // Set-up.  The producer warp initialises the barriers and the shared words and builds the head
+  // lists, then arrives at named barrier 2 without waiting: everything its own start-up path needs
+  // it wrote itself, so its first loads go out at once.  The consumers wait at that barrier.
+  if (warp == kSW) {
     if (lane == 0) {
       for (int s = 0; s < S; ++s) {
         mbar_init(smem_u32(&bars[s]), 1);
@@ -310,33 +334,45 @@ __global__ void __launch_bounds__(kSThreads, 1)
       misc[0] = 0;
       misc[3] = 0;
       misc[4] = 0;
+      if (!KV8) {
+        prefetch_tensormap(&tmK);
+        prefetch_tensormap(&tmV);
+      }
     }
     // dense (non-streaming) KV heads in ascending order, 32 heads per ballot; the streaming
     // ones too when this launch serves them
     int nd = 0, ns = 0;
-    for (int h0 = 0; h0 < kv.Hkv; h0 += 32) {
-      const int hh = h0 + lane;
-      const bool dense = hh < kv.Hkv && (kv.streaming == nullptr || kv.streaming[hh] == 0);
-      const bool strm = STREAMING && hh < kv.Hkv && !dense;
-      const unsigned bal = __ballot_sync(0xffffffffu, dense);
-      const unsigned bas = __ballot_sync(0xffffffffu, strm);
-      if (dense) dense_heads[nd + __popc(bal & ((1u << lane) - 1u))] = hh;
-      if (strm) stream_heads[ns + __popc(bas & ((1u << lane) - 1u))] = hh;
-      nd += __popc(bal);
-      ns += __popc(bas);
+    if (kv.streaming == nullptr) {
+      nd = kv.Hkv;
+      for (int hh = lane; hh < kv.Hkv; hh += 32) dense_heads[hh] = hh;
+    } else {
+      for (int h0 = 0; h0 < kv.Hkv; h0 += 32) {
+        const int hh = h0 + lane;
+        const bool dense = hh < kv.Hkv && kv.streaming[hh] == 0;
+        const bool strm = STREAMING && hh < kv.Hkv && !dense;
+        const unsigned bal = __ballot_sync(0xffffffffu, dense);
+        const unsigned bas = __ballot_sync(0xffffffffu, strm);
+        if (dense) dense_heads[nd + __popc(bal & ((1u << lane) - 1u))] = hh;
+        if (strm) stream_heads[ns + __popc(bas & ((1u << lane) - 1u))] = hh;
+        nd += __popc(bal);
+        ns += __popc(bas);
+      }
     }
     if (lane == 0) {
       *n_dense_heads = nd;
       *n_stream_heads = ns;
     }
-  } else if (warp < kSW) {
+    __syncwarp();
+    named_barrier_arrive(2, kSThreads);
+  } else {
     // query rows G..15 of both mailbox tiles stay zero (the bulk copies write rows < G only)
-    for (int e = tid - 32; e < 2 * 16 * 16; e += kSConsumers - 32) {
+    for (int e = tid; e < 2 * 16 * 16; e += kSConsumers) {
       const int r = (e >> 4) & 15;
       if (r >= G) reinterpret_cast<uint4*>(sQ)[e] = make_uint4(0, 0, 0, 0);
     }
+    named_barrier(2, kSThreads);
   }
-  __syncthreads();
+  DSA_STAMP_DIRECT(g_trace_stream, 1, 0);  // set-up done (barrier)
   const int nd_heads = *n_dense_heads;
   const int ns_heads = STREAMING ? *n_stream_heads : 0;
   // The slot space: every dense row's idx_stride selection slots followed by `pad` empty slots,
@@ -352,8 +388,8 @@ __global__ void __launch_bounds__(kSThreads, 1)
   const long long Td = static_cast<long long>(Nd) * stride;
   const long long T = Td + static_cast<long long>(kv.B) * ns_heads * sstride;
   auto unit_of = [&](long long x) -> int {  // the unit holding slot x
-    if (!STREAMING || x < Td) return static_cast<int>(x / stride);
-    return Nd + static_cast<int>((x - Td) / sstride);
+    if (!STREAMING || x < Td) return static_cast<int>(div_slots(x, stride));
+    return Nd + static_cast<int>(div_slots(x - Td, sstride));
   };
   auto unit_start = [&](int di) -> long long {  // its first slot
     if (!STREAMING || di < Nd) return static_cast<long long>(di) * stride;
@@ -367,6 +403,7 @@ __global__ void __launch_bounds__(kSThreads, 1)
         return (e / ns_heads) * kv.Hkv + stream_heads[e % ns_heads];
       }
     }
+    if (nd_heads == kv.Hkv) return di;  // every head is a dense one
     return (di / nd_heads) * kv.Hkv + dense_heads[di % nd_heads];
   };
   // a streaming row of length L attends the pages of its sink tokens [0, min(sink, L)), then
@@ -393,34 +430,67 @@ __global__ void __launch_bounds__(kSThreads, 1)
     // unit ub + l of the current batch of 32.  Chunks of up to 32 selected slots of one unit are
     // software-pipelined: while chunk A's pages are issued, the page-table entries of chunk B and
     // the selections of chunk C are already in flight.
-    if (lane == 0 && !KV8) {
-      prefetch_tensormap(&tmK);
-      prefetch_tensormap(&tmV);
-    }
+    DSA_STAMP_DIRECT(g_trace_stream, 13, kSW * 32 + (n_units == -12345));
     const int NL = min(kIssueLanes, S);  // a group of NL pages uses NL distinct stages
     int i = 0;                           // ring position
     bool stopped = false;
-    // Selections of the first unit's first two chunks, loaded before its count is known (any slot
-    // below idx_stride is a valid address): they are used if the count leaves them selected.
-    const long long us0 = unit_start(d_first);
-    const int spec_base = static_cast<int>(my_beg - us0);
-    int spec_a = -1, spec_b = -1;
-    {
+    // First pages, straight-line.  The general loop below is long code that every CTA runs cold at
+    // this point; before entering it, the first unit (when it is a dense one) is published and the
+    // first min(S, 32) pages of its slots are issued, from a short path whose loads (count, length,
+    // selections; then page-table entries) go out together.  The loop then resumes after them.
+    int f_beg = -1;  // the first unit's first slot not yet issued (-1: the short path did not run)
+    if (!STREAMING || d_first < Nd) {
       const int row0 = unit_row(d_first);
-      const long long ue0 = us0 + unit_stride(d_first);
-      const int cap_end = static_cast<int>((my_end < ue0 ? my_end : ue0) - us0);
-      if (!STREAMING || d_first < Nd) {
-        const int sel_end = min(cap_end, istride);  // the empty slots have no selection entry
-        const int32_t* sel0 = a.idx + static_cast<size_t>(row0) * istride;
-        if (spec_base + lane < sel_end) spec_a = sel0[spec_base + lane];
-        if (spec_base + 32 + lane < sel_end) spec_b = sel0[spec_base + 32 + lane];
-      } else {  // a streaming unit's positions follow from its length
-        int sn, f2;
-        stream_geom(request_len(kv, row0 / kv.Hkv), &sn, &f2);
-        const int j0 = spec_base + lane, j1 = spec_base + 32 + lane;
-        if (j0 < cap_end) spec_a = j0 < sn ? j0 : f2 + (j0 - sn);
-        if (j1 < cap_end) spec_b = j1 < sn ? j1 : f2 + (j1 - sn);
+      const long long r0 = unit_start(d_first);
+      const int pb = static_cast<int>(my_beg - r0);
+      const int pe = static_cast<int>((my_end < r0 + stride ? my_end : r0 + stride) - r0);
+      const int b0 = row0 / kv.Hkv, h0 = row0 - b0 * kv.Hkv;
+      const int j = pb + lane;
+      const int selv = j < istride ? a.idx[static_cast<size_t>(row0) * istride + j] : -1;
+      const int cnt = min(max(a.count[row0], 0), istride);
+      const int len = request_len(kv, b0);
+      const int beg = min(pb, cnt), end = min(pe, cnt);  // beg == pb whenever beg < end
+      if (lane == 0) {  // mailbox slot 0 is free at the start
+        desc[0] = row0;
+        desc[1] = beg;
+        desc[2] = end;
+        desc[3] = len;
+        desc_kind[0] = 0;
+        const uint32_t full = smem_u32(&qbars[0]);
+        mbar_arrive_expect_tx(full, static_cast<uint32_t>(G) * kHeadDim * 2);
+        bulk_load(smem_u32(sQ),
+                  a.q + (static_cast<size_t>(b0) * kv.Hq + static_cast<size_t>(h0) * G) * kHeadDim,
+                  static_cast<uint32_t>(G) * kHeadDim * 2, full);
       }
+      const int F = max(0, min(min(end - beg, S), 32));  // ring positions 0..F-1: no waits
+      const int pos = lane < F ? selv : -1;
+      const bool in = lane < F && pos >= 0 && pos < (len + page - 1) / page;
+      const int raw = in ? kv.page_table[static_cast<size_t>(b0) * kv.max_pages + pos] : -1;
+      const bool ok = in && raw >= 0 && raw < kv.num_phys;
+      if (in && !ok) raise_status(kv.status, DSA_STATUS_BAD_PAGE);
+      DSA_STAMP_DIRECT(g_trace_stream, 12, kSW * 32 + (raw == -12345));
+      if (lane < F) {
+        const uint32_t full = smem_u32(&bars[lane]);
+        stage_pos[lane] = pos;
+        stage_ok[lane] = ok ? 1 : 0;  // both published by the arrive below
+        if (!ok) {
+          mbar_arrive(full);
+        } else {
+          const uint32_t dst = smem_base + lane * stage_bytes;
+          const int rowk = (raw * kv.Hkv + h0) * page;
+          mbar_arrive_expect_tx(full, stage_tx);
+          if (KV8) {
+            bulk_load(dst, a.kv8 + static_cast<size_t>(rowk) * 264, 264u * page, full);
+          } else {
+            tma_load_page(dst, &tmK, rowk, full);
+            tma_load_page(dst + 2 * page * 128, &tmV, rowk, full);
+          }
+        }
+      }
+      if (lane == 0) *issued = F;
+      DSA_STAMP_DIRECT(g_trace_stream, 8, kSW * 32);  // producer: its first loads issued
+      i = F;
+      f_beg = beg + F;
     }
     for (int ub = 0; ub < n_units && !stopped; ub += 32) {
       int t_row = 0, t_beg = 0, t_end = 0, t_len = 0, t_kind = 0;
@@ -443,7 +513,8 @@ __global__ void __launch_bounds__(kSThreads, 1)
         }
       }
       const int ue = min(n_units, ub + 32);
-      int uq = ub;  // next unit to publish
+      DSA_STAMP_DIRECT(g_trace_stream, 10, kSW * 32 + (t_len == -12345) + (t_beg == -12345));
+      int uq = ub == 0 && f_beg >= 0 ? 1 : ub;  // next unit to publish (the short path did unit 0)
       // publishes unit u: waits for its mailbox slot, writes the descriptor, copies the queries
       auto publish = [&](int u) -> bool {
         const int slot = u & 1;
@@ -520,20 +591,11 @@ __global__ void __launch_bounds__(kSThreads, 1)
                                       : -1;
       };
       int ua, ba, ubb, bb, uc, bc;
-      seek(ub, __shfl_sync(0xffffffffu, t_beg, 0), &ua, &ba);
+      seek(ub, ub == 0 && f_beg >= 0 ? f_beg : __shfl_sync(0xffffffffu, t_beg, 0), &ua, &ba);
       seek(ua, ba + 32, &ubb, &bb);
-      int pos_a, pos_b;
-      if (ub == 0 && ua == 0 && ba == spec_base) {
-        // the speculative loads were the right ones; drop what lies past the unit's end
-        const int e = __shfl_sync(0xffffffffu, t_end, 0);
-        pos_a = ba + lane < e ? spec_a : -1;
-        pos_b = (ubb == 0 && bb == spec_base + 32) ? (bb + lane < e ? spec_b : -1)
-                                                   : load_sel(ubb, bb);
-      } else {
-        pos_a = load_sel(ua, ba);
-        pos_b = load_sel(ubb, bb);
-      }
+      int pos_a = load_sel(ua, ba), pos_b = load_sel(ubb, bb);
       for (; uq <= ua && uq < ue && !stopped; ++uq) stopped = !publish(uq);
+      DSA_STAMP_DIRECT(g_trace_stream, 11, kSW * 32 + (pos_a == -12345));
       int raw_a = load_phys(ua, pos_a);
       bool in_a = pos_in(ua, pos_a);
       while (ua < ue && !stopped) {
@@ -586,6 +648,7 @@ __global__ void __launch_bounds__(kSThreads, 1)
             }
           }
           if (lane == 0) *issued = i + min(nb, q0 + NL);
+          DSA_STAMP_DIRECT(g_trace_stream, 18, kSW * 32);  // the loop's first loads issued
         }
         i += nb;
         ua = ubb;
@@ -601,6 +664,7 @@ __global__ void __launch_bounds__(kSThreads, 1)
     }
     __syncwarp();
     if (lane == 0) *producer_done = 1;
+    DSA_STAMP_DIRECT(g_trace_stream, 9, kSW * 32);  // producer: every load issued
     return;  // the producer takes no part in the epilogues (they use named barrier 1)
   }
 
@@ -642,6 +706,7 @@ __global__ void __launch_bounds__(kSThreads, 1)
       __syncwarp();
       if (lane == 0) mbar_arrive(smem_u32(&qbars[2 + slot]));
     }
+    DSA_STAMP_DIRECT(g_trace_stream, 2, 0);  // first unit's descriptor and query on chip
     WarpSoftmaxState st;
     state_init(st);
     const int npg = end - beg;
@@ -656,6 +721,7 @@ __global__ void __launch_bounds__(kSThreads, 1)
       }
       if (!((own_stages >> s) & 1u)) continue;
       if (!mbar_wait(smem_u32(&bars[s]), ph, abort_flag, kv.status)) break;
+      DSA_STAMP_DIRECT(g_trace_stream, 3, 0);  // warp 0's first page landed
       const int pos = stage_pos[s];
       const bool loaded = stage_ok[s] != 0;
       const uint32_t kb = smem_base + s * stage_bytes;
@@ -690,6 +756,7 @@ __global__ void __launch_bounds__(kSThreads, 1)
         for (int r = 0; r < arrivals; ++r) mbar_arrive(smem_u32(&bars[S + s]));
     }
     i += npg;
+    DSA_STAMP_DIRECT(g_trace_stream, 4, 0);  // warp 0 through the first unit's pages
     state_finish(st);
 
     // ---- unit epilogue: merge the warps' states of the G query heads
@@ -728,6 +795,7 @@ __global__ void __launch_bounds__(kSThreads, 1)
       }
     }
     named_barrier(1, kSConsumers);
+    DSA_STAMP_DIRECT(g_trace_stream, 14, u == n_units - 1 ? 0 : 1 << 20);  // last unit's pages
     // cut: the unit reaches outside this CTA's slot range (other CTAs hold part of the row)
     const long long rs = dry ? my_beg : unit_start(di);
     const bool cut = !dry && (rs < my_beg || rs + unit_stride(di) > my_end);
@@ -770,6 +838,8 @@ __global__ void __launch_bounds__(kSThreads, 1)
       }
     }
     named_barrier(1, kSConsumers);  // the merge area is rewritten by the next unit
+    DSA_STAMP_DIRECT(g_trace_stream, 5, 0);  // the first unit's epilogue done
+    DSA_STAMP_DIRECT(g_trace_stream, 15, u == n_units - 1 ? 0 : 1 << 20);  // the last one's
 
     // ---- rows cut across CTAs (only this CTA's first and last units can be).  Both tickets are
     // taken at once when all of this CTA's records are written; the CTA that takes a row's last
@@ -806,6 +876,7 @@ __global__ void __launch_bounds__(kSThreads, 1)
       }
       named_barrier(1, kSConsumers);
       if (!dry) merged = last_flag[0] != 0 || (n_cut > 1 && last_flag[1] != 0);
+      DSA_STAMP_DIRECT(g_trace_stream, 16, dry ? 1 << 20 : 0);  // tickets taken
       const int n_jobs = n_cut * G;  // (cut row, head) pairs
       for (int job = warp; job < n_jobs; job += kSW) {
         const int k = job / G, g = job - k * G;
@@ -868,9 +939,11 @@ __global__ void __launch_bounds__(kSThreads, 1)
           if (g == 0) a.counters[row] = 0;  // ready for the next call
         }
       }
+      DSA_STAMP_DIRECT(g_trace_stream, 17, !dry && merged ? 0 : 1 << 20);  // merge done
     }
   }
 
+  DSA_STAMP_DIRECT(g_trace_stream, 6, 0);  // the consumers' work done (end)
   // after a timeout, wait (bounded) for the page loads still in flight before the CTA exits
   if (tid == 0 && *abort_flag) {
     const unsigned long long t0 = global_timer_ns();
@@ -911,3 +984,17 @@ cudaError_t launch_stream_attn(const CUtensorMap& tmK, const CUtensorMap& tmV,
 }
 
 }  // namespace dsa
+
+#ifdef DSA_TIMELINE
+// Phase-trace accessors of the traced library (see DSA_TRACE_BEGIN).
+extern "C" int dsa_trace_read_stream(void* host, size_t bytes) {
+  return static_cast<int>(cudaMemcpyFromSymbol(
+      host, dsa::g_trace_stream,
+      bytes < sizeof(dsa::g_trace_stream) ? bytes : sizeof(dsa::g_trace_stream)));
+}
+extern "C" int dsa_trace_clear_stream() {
+  void* p = nullptr;
+  cudaError_t e = cudaGetSymbolAddress(&p, dsa::g_trace_stream);
+  return static_cast<int>(e == cudaSuccess ? cudaMemset(p, 0, sizeof(dsa::g_trace_stream)) : e);
+}
+#endif

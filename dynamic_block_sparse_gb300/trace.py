@@ -2,6 +2,7 @@
 
     python -m dynamic_block_sparse_gb300.trace threshold   # PSA threshold kernel on psa_threshold
     python -m dynamic_block_sparse_gb300.trace prr         # fused PRR step on prr_512k
+    python -m dynamic_block_sparse_gb300.trace stream      # persistent attention on llama3_8b_layer
 
 Builds ``libdsa_trace.so`` (every kernel compiled with ``-DDSA_TIMELINE``), runs the workload's
 step several times cold (L2 flushed before each launch) and warm (launches back to back), and
@@ -38,6 +39,24 @@ LABELS = {
         11: "P.V done (thread 0's warp)",
         12: "chunk done (barrier)",
         13: "warp states merged, output written",
+    },
+    "stream": {
+        1: "set-up done (barrier)",
+        2: "first unit's descriptor and query on chip (consumer warp 0)",
+        3: "warp 0's first page landed",
+        4: "warp 0 through the first unit's pages",
+        5: "the first unit's epilogue done",
+        6: "the consumers' work done (end)",
+        8: "producer: its first page loads issued",
+        9: "producer: every load issued",
+        10: "producer: first batch's unit descriptors known",
+        11: "producer: the first unit published (mailbox, query copy)",
+        12: "producer: first chunk about to issue (page-table entries in hand)",
+        13: "producer: partition known",
+        14: "last unit: every warp's state stored (its pages done)",
+        15: "last unit: epilogue done",
+        16: "cut rows: tickets taken",
+        17: "cut rows: merge done (merging CTAs)",
     },
     "prr": {
         1: "worker: first segment's table, state and query loaded",
@@ -79,6 +98,19 @@ def _setup(kernel, B, torch):
     from dynamic_block_sparse_gb300.pipeline import Cache, PRRDecoder, ThresholdDecoder
     from dynamic_block_sparse_gb300.workloads import BY_NAME, make_inputs
 
+    if kernel == "stream":
+        from dynamic_block_sparse_gb300.pipeline import TopKDecoder
+        w = BY_NAME["llama3_8b_layer"]
+        inp = make_inputs(w, "cuda", shuffle_pages=False)
+        cache = Cache.from_inputs(inp, "cuda")
+        dec = TopKDecoder(cache, w.k, w.logical_page)
+        dec.build_meta()
+        q = inp["q"][0].clone()
+        dec.step(q)
+
+        def step(i):
+            dec.attend(q)
+        return step, cache
     if kernel == "threshold":
         w = BY_NAME["psa_threshold"]
         inp = make_inputs(w, "cuda", shuffle_pages=False)
@@ -136,6 +168,30 @@ def _collect(kernel, lib, step, flush, torch, cold: bool, runs: int):
     return out
 
 
+# phase lengths worth reading per CTA (stamp pairs, both passed by the same CTA)
+SPANS = {
+    "stream": [(0, 13), (13, 12), (12, 8), (8, 3), (1, 2), (3, 4), (4, 5), (14, 15), (15, 16),
+               (16, 17), (16, 6), (9, 6)],
+}
+
+
+def _spans(kernel, runs):
+    pairs = SPANS.get(kernel)
+    if not pairs:
+        return
+    print("   per-CTA phase lengths (cycles; median / max over the CTAs that passed both stamps)")
+    for a, b in pairs:
+        d = []
+        for tr in runs:
+            hit = (tr[:, 0, a] > 0) & (tr[:, 0, b] > 0)
+            if a == 0:
+                hit &= tr[:, 0, 0] > 0
+            d += (tr[hit, 0, b] - tr[hit, 0, a]).tolist()
+        if d:
+            print(f"   {a:2d} -> {b:2d}  median {int(statistics.median(d)):7d}  max {max(d):7d}"
+                  f"   ({len(d)} CTA spans)")
+
+
 def _report(kernel, runs, title):
     labels = LABELS[kernel]
     groups = {"all CTAs": None}
@@ -170,6 +226,7 @@ def _report(kernel, runs, title):
             print(f"   {k:2d} {name:46s} median {int(statistics.median(cyc[k])):7d} max "
                   f"{max(cyc[k]):7d}   median {int(statistics.median(ns[k])):7d} max {max(ns[k]):7d}"
                   f"   ({len(cyc[k])} CTA stamps)")
+    _spans(kernel, runs)
 
 
 def main(argv=None):
