@@ -35,6 +35,7 @@ import subprocess
 import sys
 import threading
 import time
+from types import SimpleNamespace
 
 ROOT = os.path.dirname(os.path.abspath(__file__))
 sys.path.insert(0, ROOT)
@@ -382,7 +383,7 @@ def bench_prr(args, w, dev, rank):
                      ("spec_attn", lambda: dec.stage_spec(static_q, 0)),
                      ("repair_merge", lambda: dec.stage_repair(static_q, 0)),
                      ("ema_predict", lambda: dec.stage_ema(buf=1))):
-        stage_graphs[name] = [_graph(fn)]
+        stage_graphs[name] = [SimpleNamespace(replay=fn)]  # direct calls, like the rows
     torch.cuda.synchronize()
     stage_ms = {}
     for name, g in stage_graphs.items():
@@ -406,7 +407,7 @@ def bench_prr(args, w, dev, rank):
     cbest = torch.empty(t3.shape[1], dtype=torch.int32, device=dev)
     cws = torch.zeros(B.dsa_calibrate_ema_workspace_size(calib_steps, t3.shape[1], dec.stride,
                                                          w.k), dtype=torch.uint8, device=dev)
-    calib_ms = _time_graph(_graph(lambda: B.dsa_calibrate_ema(t3, dec.stride, w.k, w.k_pred, cH,
+    calib_ms = _time_call((lambda: B.dsa_calibrate_ema(t3, dec.stride, w.k, w.k_pred, cH,
                                                                cbest, cws)), flush)
     calib_bytes = t3.numel() * 4 + cH.numel() * 4 + cbest.numel() * 4
 
@@ -526,22 +527,17 @@ def e2e_prr(args, w, decs, qs, bytes_step):
 
 # ------------------------------------------------------------------------------------ rows
 
-def _graph(fn):
-    import torch
-
-    g = torch.cuda.CUDAGraph()
-    with torch.cuda.graph(g):
-        fn()
-    return g
-
-
-def _time_graph(g, flush, n=30, warm=3):
-    """Mean device time (ms) of one replay, L2 flushed before each (outside the window)."""
+def _time_call(fn, flush, n=30, warm=3):
+    """Mean device time (ms) of one library call made directly on the current stream (as a user
+    makes it: one launch per kernel), L2 flushed before each call (outside the window).  The
+    host enqueues the call while the GPU still runs the ~50 us lead spin and the flush, so the
+    window holds only device work.  (The same window around an empty kernel measures ~5 us on a
+    GB300: launch, block dispatch and the two event records.)"""
     import torch
 
     stream = torch.cuda.current_stream()
     for _ in range(warm):
-        g.replay()
+        fn()
     torch.cuda.synchronize()
     ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
           for _ in range(n)]
@@ -549,7 +545,7 @@ def _time_graph(g, flush, n=30, warm=3):
         flush.lead()
         flush(i & 0xFF)
         s.record(stream)
-        g.replay()
+        fn()
         e.record(stream)
     torch.cuda.synchronize()
     return statistics.mean(s.elapsed_time(e) for s, e in ev)
@@ -585,38 +581,38 @@ def bench_rows(dev, flush, peak, only=None):
         dec = TopKDecoder(cache, w.k, w.logical_page)
         q = inp["q"][0].clone()
         rows, npg = w.batch * w.num_kv_heads, w.pages_per_seq
-        ms = _time_graph(_graph(dec.build_meta), flush)
+        ms = _time_call((dec.build_meta), flush)
         out.append(_entry("A1", w.name, "dsa_build_page_meta MINMAX", ms,
                           rows * npg * w.page_size * 256 + rows * npg * 512, peak))
         dec.step(q)
         torch.cuda.synchronize()
         sel = int(dec.count.sum())
-        ms = _time_graph(_graph(lambda: B.dsa_score_pages(cache.kv, q, dec.meta, B.DSA_META_MINMAX,
+        ms = _time_call((lambda: B.dsa_score_pages(cache.kv, q, dec.meta, B.DSA_META_MINMAX,
                                                           w.logical_page, dec.scores)), flush)
         out.append(_entry("A2", w.name, "dsa_score_pages MINMAX", ms,
                           rows * npg * 512 + q.numel() * 2 + rows * dec.stride * 4, peak))
-        ms = _time_graph(_graph(lambda: B.dsa_select_topk(dec.scores, dec.stride, w.k, dec.idx,
+        ms = _time_call((lambda: B.dsa_select_topk(dec.scores, dec.stride, w.k, dec.idx,
                                                           dec.count)), flush)
         out.append(_entry("A3", w.name, "dsa_select_topk k=256 of 2048", ms,
                           rows * dec.stride * 4 + rows * w.k * 4, peak))
-        ms = _time_graph(_graph(lambda: dec.attend(q)), flush)
+        ms = _time_call((lambda: dec.attend(q)), flush)
         out.append(_entry("A6", w.name, "dsa_sparse_decode_attn (persistent split-K)", ms,
                           sel * w.page_size * KVP + q.numel() * 2 + q.numel() * 4, peak, pages=sel))
-        ms = _time_graph(_graph(lambda: dec.step(q)), flush)
+        ms = _time_call((lambda: dec.step(q)), flush)
         out.append(_entry("step", w.name, "score + top-K + attention", ms,
                           rows * npg * 512 + sel * w.page_size * KVP + rows * dec.stride * 8, peak))
         # decode-time append of one token per request (replayed: it rewrites the newest token and
         # recomputes its page's metadata, the work of every append)
         k_new = torch.randn((w.batch, w.num_kv_heads, w.head_dim), device=dev).bfloat16()
         v_new = torch.randn_like(k_new)
-        ms = _time_graph(_graph(lambda: B.dsa_append_kv(cache.kv, k_new, v_new, B.DSA_META_MINMAX,
+        ms = _time_call((lambda: B.dsa_append_kv(cache.kv, k_new, v_new, B.DSA_META_MINMAX,
                                                         w.logical_page, dec.meta)), flush)
         tail = [(int(L) - 1) % w.page_size + 1 for L in cache.seq_lens.tolist()]
         out.append(_entry("N2", w.name, "dsa_append_kv: K/V of one token + its page's kmax/kmin",
                           ms, sum(w.num_kv_heads * (KVP + t * 256 + 512) for t in tail), peak))
         # attention over KV8 pages (e4m3 rows + fp32 row scales: 264 B per token per KV head)
         dec.use_kv8()
-        ms = _time_graph(_graph(lambda: dec.attend(q)), flush)
+        ms = _time_call((lambda: dec.attend(q)), flush)
         out.append(_entry("N4", w.name,
                           "dsa_sparse_decode_attn_kv8 (8-bit pages, persistent split-K)", ms,
                           sel * w.page_size * 264 + q.numel() * 2 + q.numel() * 4, peak, pages=sel))
@@ -633,34 +629,34 @@ def bench_rows(dev, flush, peak, only=None):
         rows, npg = w.batch * w.num_kv_heads, w.pages_per_seq
         dense = w.batch * (w.num_kv_heads - len(w.streaming_kv_heads))
         stream_rows = rows - dense
-        ms = _time_graph(_graph(dec.build_meta), flush)
+        ms = _time_call((dec.build_meta), flush)
         out.append(_entry("A1", w.name, "dsa_build_page_meta MINMAX (logical 16 in physical 64)",
                           ms, rows * npg * w.page_size * 256 + rows * npg * w.g * 512, peak))
         dec.step(q, 0)
         torch.cuda.synchronize()
         sel = int(dec.count.sum())
-        ms = _time_graph(_graph(lambda: B.dsa_score_pages(cache.kv, q, dec.meta, B.DSA_META_MINMAX,
+        ms = _time_call((lambda: B.dsa_score_pages(cache.kv, q, dec.meta, B.DSA_META_MINMAX,
                                                           w.logical_page, dec.scores)), flush)
         out.append(_entry("A2", w.name, "dsa_score_pages MINMAX logical pages (dense heads)", ms,
                           dense * npg * w.g * 512 + q.numel() * 2 + rows * dec.stride * 4, peak))
-        ms = _time_graph(_graph(lambda: B.dsa_select_hier(dec.scores, dec.stride, w.g, w.k, dec.idx,
+        ms = _time_call((lambda: B.dsa_select_hier(dec.scores, dec.stride, w.g, w.k, dec.idx,
                                                           dec.count)), flush)
         out.append(_entry("A4", w.name, "dsa_select_hier g=4 k=64 of 2048", ms,
                           rows * dec.stride * 4 + rows * w.k * 4, peak))
-        ms = _time_graph(_graph(lambda: B.dsa_sparse_decode_attn(
+        ms = _time_call((lambda: B.dsa_sparse_decode_attn(
             cache.kv, q, dec.idx, dec.count, dec.scale, dec.out, dec.m, dec.l,
             workspace=dec.workspace)), flush)
         out.append(_entry("A6", w.name, "dsa_sparse_decode_attn dense heads (persistent split-K)",
                           ms, sel * w.page_size * KVP + q.numel() * 2, peak, pages=sel))
-        ms = _time_graph(_graph(lambda: B.dsa_streaming_head_attn(
+        ms = _time_call((lambda: B.dsa_streaming_head_attn(
             cache.kv, q, w.sink, w.local, dec.scale, dec.out, dec.m, dec.l)), flush)
         out.append(_entry("A7", w.name, "dsa_streaming_head_attn 64 sink + 256 local", ms,
                           stream_rows * (w.sink + w.local) * KVP + q.numel(), peak))
-        ms0 = _time_graph(_graph(lambda: dec.step(q, 0)), flush)
+        ms0 = _time_call((lambda: dec.step(q, 0)), flush)
         out.append(_entry("step", w.name, "selection step (score + hier select + attention)", ms0,
                           dense * npg * w.g * 512 + sel * w.page_size * KVP
                           + stream_rows * (w.sink + w.local) * KVP, peak))
-        ms1 = _time_graph(_graph(lambda: dec.step(q, 1)), flush)
+        ms1 = _time_call((lambda: dec.step(q, 1)), flush)
         out.append(_entry("A8", w.name, "reuse step (attention with the reused selection)", ms1,
                           sel * w.page_size * KVP + stream_rows * (w.sink + w.local) * KVP, peak))
         del dec, cache, inp
@@ -674,23 +670,23 @@ def bench_rows(dev, flush, peak, only=None):
         dec = ThresholdDecoder(cache, w.tau, w.cap)
         q = inp["q"][0].clone()
         rows, npg = w.batch * w.num_kv_heads, w.pages_per_seq
-        ms = _time_graph(_graph(dec.build_meta), flush)
+        ms = _time_call((dec.build_meta), flush)
         out.append(_entry("A1", w.name, "dsa_build_page_meta MEAN", ms,
                           rows * npg * w.page_size * 256 + rows * npg * 512, peak))
         dec.step(q)
         torch.cuda.synchronize()
         visited = int(dec.count.sum())
-        ms = _time_graph(_graph(lambda: B.dsa_score_pages(cache.kv, q, dec.meta, B.DSA_META_MEAN,
+        ms = _time_call((lambda: B.dsa_score_pages(cache.kv, q, dec.meta, B.DSA_META_MEAN,
                                                           w.page_size, dec.scores)), flush)
         out.append(_entry("A2", w.name, "dsa_score_pages MEAN", ms,
                           rows * npg * 512 + q.numel() * 2 + rows * dec.stride * 4, peak))
-        ms = _time_graph(_graph(lambda: B.dsa_select_threshold(
+        ms = _time_call((lambda: B.dsa_select_threshold(
             cache.kv, q, dec.scores, w.tau, w.cap, dec.scale, dec.idx, dec.count, dec.out, dec.m,
             dec.l)), flush)
         out.append(_entry("A5", w.name, "dsa_select_threshold tau=0.95 (rank, attend, stop)", ms,
                           rows * npg * 4 + visited * w.page_size * KVP + q.numel() * 6, peak,
                           mean_blocks=round(visited / rows, 2)))
-        ms = _time_graph(_graph(lambda: dec.step(q)), flush)
+        ms = _time_call((lambda: dec.step(q)), flush)
         out.append(_entry("step", w.name, "score + threshold selection", ms,
                           rows * npg * 516 + visited * w.page_size * KVP, peak))
         del dec, cache, inp
@@ -704,7 +700,7 @@ def bench_rows(dev, flush, peak, only=None):
         dec = TopKDecoder(cache, w.k, w.logical_page)
         dec.build_meta()
         q = inp["q"][0].clone()
-        ms = _time_graph(_graph(lambda: dec.step(q)), flush)
+        ms = _time_call((lambda: dec.step(q)), flush)
         out.append(_entry("step", w.name, "score + top-32 + attention", ms,
                           w.pages_per_seq * 512 + w.k * w.page_size * KVP, peak))
         del dec, cache, inp

@@ -321,16 +321,12 @@ __global__ void __launch_bounds__(kSThreads, 1)
   // lists, then arrives at named barrier 2 without waiting: everything its own start-up path needs
   // it wrote itself, so its first loads go out at once.  The consumers wait at that barrier.
   if (warp == kSW) {
+    // one barrier per lane: [S] full, [S] empty (one arrival per 16-token tile of the page), then
+    // the mailbox's [2] full and [2] empty
+    for (int k = lane; k < 2 * S + 4; k += 32)
+      mbar_init(smem_u32(&bars[k]), k < S ? 1 : k < 2 * S ? tiles : k < 2 * S + 2 ? 1 : kSW);
+    fence_mbar_init();
     if (lane == 0) {
-      for (int s = 0; s < S; ++s) {
-        mbar_init(smem_u32(&bars[s]), 1);
-        mbar_init(smem_u32(&bars[S + s]), tiles);  // one arrival per 16-token tile of the page
-      }
-      for (int k = 0; k < 2; ++k) {
-        mbar_init(smem_u32(&qbars[k]), 1);
-        mbar_init(smem_u32(&qbars[2 + k]), kSW);
-      }
-      fence_mbar_init();
       misc[0] = 0;
       misc[3] = 0;
       misc[4] = 0;
@@ -364,6 +360,7 @@ __global__ void __launch_bounds__(kSThreads, 1)
     }
     __syncwarp();
     named_barrier_arrive(2, kSThreads);
+    DSA_STAMP_DIRECT(g_trace_stream, 19, kSW * 32);  // producer: set-up done
   } else {
     // query rows G..15 of both mailbox tiles stay zero (the bulk copies write rows < G only)
     for (int e = tid; e < 2 * 16 * 16; e += kSConsumers) {
@@ -436,7 +433,7 @@ __global__ void __launch_bounds__(kSThreads, 1)
     bool stopped = false;
     // First pages, straight-line.  The general loop below is long code that every CTA runs cold at
     // this point; before entering it, the first unit (when it is a dense one) is published and the
-    // first min(S, 32) pages of its slots are issued, from a short path whose loads (count, length,
+    // first min(S, 16) pages of its slots are issued, from a short path whose loads (count, length,
     // selections; then page-table entries) go out together.  The loop then resumes after them.
     int f_beg = -1;  // the first unit's first slot not yet issued (-1: the short path did not run)
     if (!STREAMING || d_first < Nd) {
@@ -462,29 +459,39 @@ __global__ void __launch_bounds__(kSThreads, 1)
                   a.q + (static_cast<size_t>(b0) * kv.Hq + static_cast<size_t>(h0) * G) * kHeadDim,
                   static_cast<uint32_t>(G) * kHeadDim * 2, full);
       }
-      const int F = max(0, min(min(end - beg, S), 32));  // ring positions 0..F-1: no waits
+      const int F = max(0, min(min(end - beg, S), 16));  // ring positions 0..F-1: no waits
       const int pos = lane < F ? selv : -1;
       const bool in = lane < F && pos >= 0 && pos < (len + page - 1) / page;
       const int raw = in ? kv.page_table[static_cast<size_t>(b0) * kv.max_pages + pos] : -1;
       const bool ok = in && raw >= 0 && raw < kv.num_phys;
       if (in && !ok) raise_status(kv.status, DSA_STATUS_BAD_PAGE);
       DSA_STAMP_DIRECT(g_trace_stream, 12, kSW * 32 + (raw == -12345));
-      if (lane < F) {
-        const uint32_t full = smem_u32(&bars[lane]);
-        stage_pos[lane] = pos;
-        stage_ok[lane] = ok ? 1 : 0;  // both published by the arrive below
-        if (!ok) {
-          mbar_arrive(full);
-        } else {
-          const uint32_t dst = smem_base + lane * stage_bytes;
-          const int rowk = (raw * kv.Hkv + h0) * page;
-          mbar_arrive_expect_tx(full, stage_tx);
-          if (KV8) {
-            bulk_load(dst, a.kv8 + static_cast<size_t>(rowk) * 264, 264u * page, full);
+      // issue: lane 2q (K) and lane 2q + 1 (V) take page q, so that the copies go out page by
+      // page (F <= kStreamMaxStages = 16 pages; a KV8 page is one copy, from lane 2q)
+      const int q = lane >> 1;
+      const int pos_q = __shfl_sync(0xffffffffu, pos, q);
+      const int raw_q = __shfl_sync(0xffffffffu, raw, q);
+      const bool ok_q = __shfl_sync(0xffffffffu, ok ? 1 : 0, q) != 0;
+      if (q < F) {
+        const uint32_t full = smem_u32(&bars[q]);
+        const uint32_t dst = smem_base + q * stage_bytes;
+        const int rowk = (raw_q * kv.Hkv + h0) * page;
+        if ((lane & 1) == 0) {
+          stage_pos[q] = pos_q;
+          stage_ok[q] = ok_q ? 1 : 0;  // both published by the arrive below
+          if (!ok_q) {
+            mbar_arrive(full);  // nothing to load: complete the phase with a plain arrival
           } else {
-            tma_load_page(dst, &tmK, rowk, full);
-            tma_load_page(dst + 2 * page * 128, &tmV, rowk, full);
+            mbar_arrive_expect_tx(full, stage_tx);
+            if (KV8) bulk_load(dst, a.kv8 + static_cast<size_t>(rowk) * 264, 264u * page, full);
           }
+        }
+        __syncwarp(0xffffffffu >> (32 - 2 * F));  // the byte count is posted before any copy lands
+        if (!KV8 && ok_q) {
+          if ((lane & 1) == 0)
+            tma_load_page(dst, &tmK, rowk, full);
+          else
+            tma_load_page(dst + 2 * page * 128, &tmV, rowk, full);
         }
       }
       if (lane == 0) *issued = F;
@@ -682,6 +689,20 @@ __global__ void __launch_bounds__(kSThreads, 1)
   // take the last tickets, so the rehearsal's own cold fetches cost the launch nothing.
   bool merged = false;  // this CTA merged a cut row (uniform across the consumer warps)
   const int n_iter = n_units + (n_units == 1 ? 1 : 0);
+  // The geometry of the rows this CTA may share with others (its first and its last unit), worked
+  // out now, while the first pages are on their way: at the end only the tickets remain.
+  int* cut_info = misc + 50;  // [2][first CTA, CTA count, row, record slot of the first CTA]
+  if (warp == 0 && lane < 2) {
+    const int di = d_first + (lane == 0 ? 0 : n_units - 1);
+    const long long rs = unit_start(di);
+    const int c_first = slot_owner(rs, T, n_act);
+    const int c_last = slot_owner(rs + unit_stride(di) - 1, T, n_act);
+    cut_info[lane * 4 + 0] = c_first;
+    cut_info[lane * 4 + 1] = c_last - c_first + 1;
+    cut_info[lane * 4 + 2] = unit_row(di);
+    // the row is the first CTA's last unit: slot 1 unless it is also that CTA's first
+    cut_info[lane * 4 + 3] = slot_start(c_first, T, n_act) < rs ? 1 : 0;
+  }
   for (int u = 0; u < n_iter; ++u) {
     const bool dry = u == n_units;
     if (dry && merged) break;
@@ -802,41 +823,46 @@ __global__ void __launch_bounds__(kSThreads, 1)
     any_cut |= cut;
     float* rec0 =
         a.part + (static_cast<size_t>(blockIdx.x) * 2 + (u == 0 ? 0 : 1)) * G * kRecordFloats;
-    for (int e = tid; e < G * kHeadDim; e += kSConsumers) {
-      const int g = e >> 7, d = e & 127;
-      float M = -INFINITY;
+    // Merge weights first: thread g * kSW + w takes warp w's (m, l) of head g; the kSW threads of a
+    // head (consecutive lanes) reduce the maximum and the denominator with shuffles and leave
+    // exp2(m_w - M) / L_total in place of m_w.  The head's own (m, l) are written here too.
+    if (warp < (kSW * G + 31) / 32) {
+      const int g = tid / kSW, w = tid % kSW;
+      const bool mine = g < G;
+      const float mw = mine ? sM[w * G + g] : -INFINITY;
+      float M = mw;
 #pragma unroll
-      for (int w = 0; w < kSW; ++w) M = fmaxf(M, sM[w * G + g]);
-      float Lsum = 0.f, acc = 0.f;
-      const int pos = KV8 ? kv8_o_pos(g, d) : d;
-      if (M != -INFINITY) {
+      for (int o = 1; o < kSW; o <<= 1) M = fmaxf(M, __shfl_xor_sync(0xffffffffu, M, o));
+      const float f = mw == -INFINITY ? 0.f : fast_exp2(mw - M);
+      float Lsum = mine ? sL[w * G + g] * f : 0.f;
 #pragma unroll
-        for (int w = 0; w < kSW; ++w) {
-          const float mw = sM[w * G + g];
-          if (mw == -INFINITY) continue;
-          const float f = fast_exp2(mw - M);
-          Lsum += sL[w * G + g] * f;
-          acc += sO[(w * G + g) * kHeadDim + pos] * f;
-        }
-      }
-      const float o = Lsum > 0.f ? acc / Lsum : 0.f;
+      for (int o = 1; o < kSW; o <<= 1) Lsum += __shfl_xor_sync(0xffffffffu, Lsum, o);
+      if (mine) sM[w * G + g] = Lsum > 0.f ? __fdividef(f, Lsum) : 0.f;
       const float mn = Lsum > 0.f ? M * kLn2 : -INFINITY;
-      if (!dry && !cut) {  // the rehearsal writes nothing
-        const size_t qh = static_cast<size_t>(b) * kv.Hq + static_cast<size_t>(h) * G + g;
-        a.out[qh * kHeadDim + d] = o;
-        if (d == 0) {
+      if (mine && w == 0 && !dry) {
+        if (!cut) {
+          const size_t qh = static_cast<size_t>(b) * kv.Hq + static_cast<size_t>(h) * G + g;
           a.m[qh] = mn;
           a.l[qh] = Lsum;
-        }
-      } else if (!dry) {
-        float* rec = rec0 + g * kRecordFloats;
-        rec[d] = o;
-        if (d == 0) {
-          rec[128] = mn;
-          rec[129] = Lsum;
+        } else {
+          rec0[g * kRecordFloats + 128] = mn;
+          rec0[g * kRecordFloats + 129] = Lsum;
         }
       }
     }
+    named_barrier(1, kSConsumers);
+    for (int e = tid; e < G * kHeadDim; e += kSConsumers) {
+      const int g = e >> 7, d = e & 127;
+      const int pos = KV8 ? kv8_o_pos(g, d) : d;
+      float o = 0.f;
+#pragma unroll
+      for (int w = 0; w < kSW; ++w) o += sO[(w * G + g) * kHeadDim + pos] * sM[w * G + g];
+      if (!dry && !cut)  // the rehearsal writes nothing
+        a.out[(static_cast<size_t>(b) * kv.Hq + static_cast<size_t>(h) * G + g) * kHeadDim + d] = o;
+      else if (!dry)
+        rec0[g * kRecordFloats + d] = o;
+    }
+    DSA_STAMP_DIRECT(g_trace_stream, 20, u == n_units - 1 ? 0 : 1 << 20);  // thread 0's part
     named_barrier(1, kSConsumers);  // the merge area is rewritten by the next unit
     DSA_STAMP_DIRECT(g_trace_stream, 5, 0);  // the first unit's epilogue done
     DSA_STAMP_DIRECT(g_trace_stream, 15, u == n_units - 1 ? 0 : 1 << 20);  // the last one's
@@ -850,7 +876,6 @@ __global__ void __launch_bounds__(kSThreads, 1)
     // is written to global memory or counted; its unit epilogue writes nothing either.)
     if (dry || (u == n_units - 1 && any_cut)) {
       const int n_cut = dry || n_units > 1 ? 2 : 1;
-      int* cut_info = misc + 50;  // [2][first CTA, CTA count, row, record slot of the first CTA]
       if (dry && warp == 0 && lane < 2) {
         cut_info[lane * 4 + 0] = blockIdx.x;
         cut_info[lane * 4 + 1] = 1;
@@ -858,21 +883,10 @@ __global__ void __launch_bounds__(kSThreads, 1)
         cut_info[lane * 4 + 3] = 0;
         last_flag[lane] = 1;
       } else if (!dry && warp == 0 && lane < n_cut) {
-        const int di = d_first + (lane == 0 ? 0 : n_units - 1);
-        const long long rs = unit_start(di);
-        const int c_first = slot_owner(rs, T, n_act);
-        const int c_last = slot_owner(rs + unit_stride(di) - 1, T, n_act);
-        int last = 0;
-        if (c_first != c_last) {
-          const int row = unit_row(di);
-          cut_info[lane * 4 + 0] = c_first;
-          cut_info[lane * 4 + 1] = c_last - c_first + 1;
-          cut_info[lane * 4 + 2] = row;
-          // the row is the first CTA's last unit: slot 1 unless it is also that CTA's first
-          cut_info[lane * 4 + 3] = slot_start(c_first, T, n_act) < rs ? 1 : 0;
-          last = ticket_add(a.counters + row) == c_last - c_first;
-        }
+        const int C = cut_info[lane * 4 + 1];
+        const int last = C > 1 && ticket_add(a.counters + cut_info[lane * 4 + 2]) == C - 1;
         last_flag[lane] = last;
+        DSA_STAMP_DIRECT(g_trace_stream, 21, last == -12345 ? 1 << 20 : 0);  // ticket returned
       }
       named_barrier(1, kSConsumers);
       if (!dry) merged = last_flag[0] != 0 || (n_cut > 1 && last_flag[1] != 0);

@@ -57,6 +57,10 @@ LABELS = {
         15: "last unit: epilogue done",
         16: "cut rows: tickets taken",
         17: "cut rows: merge done (merging CTAs)",
+        18: "producer: the general loop's first loads issued",
+        19: "producer: set-up done (arrived)",
+        20: "last unit: thread 0's share of the epilogue done",
+        21: "cut rows: thread 0's ticket returned",
     },
     "prr": {
         1: "worker: first segment's table, state and query loaded",
@@ -170,8 +174,8 @@ def _collect(kernel, lib, step, flush, torch, cold: bool, runs: int):
 
 # phase lengths worth reading per CTA (stamp pairs, both passed by the same CTA)
 SPANS = {
-    "stream": [(0, 13), (13, 12), (12, 8), (8, 3), (1, 2), (3, 4), (4, 5), (14, 15), (15, 16),
-               (16, 17), (16, 6), (9, 6)],
+    "stream": [(0, 19), (19, 13), (13, 12), (12, 8), (8, 3), (8, 18), (1, 2), (3, 4), (4, 5),
+               (14, 20), (20, 15), (15, 21), (21, 16), (16, 17), (16, 6), (9, 6)],
 }
 
 
