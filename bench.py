@@ -6,7 +6,7 @@ KV heads, head_dim 128, block 64, top-64 true blocks, |P| = 76 predicted blocks,
 alpha 0.6 / beta 0.3 / gamma 0.5, query random walk N(0, 0.05)).  One bench step is one decode
 step of the whole path: page scoring over the kmax/kmin metadata, top-K selection, speculative
 attention over P (beside scoring), repair of A \\ P with the log-sum-exp merge, and the EMA
-update that predicts the next P -- one cooperative launch (dsa_prr_step).
+update that predicts the next P -- one launch (dsa_prr_step).
 
 Timing.  The steps rotate over the caches of 32 layers (each layer its own K/V pools, metadata
 and predictor state; one CUDA graph holds one step of every layer), as consecutive decode steps
@@ -455,7 +455,7 @@ def bench_prr(args, w, dev, rank):
                stage_ms["repair_merge"], rep_bytes, peak),
         _entry("N1", w.name, "dsa_calibrate_ema: 80-point (alpha, beta, gamma) grid, 16 steps",
                calib_ms, calib_bytes, peak),
-        _entry("step", w.name, f"PRR decode step, one cooperative launch (dsa_prr_step), "
+        _entry("step", w.name, f"PRR decode step, one launch (dsa_prr_step), "
                f"{n_layers}-layer rotation", mean_ms, bytes_step, peak),
         _entry("step-cold", w.name, "the same step alone, L2 flushed before it", cold_mean,
                bytes_step, peak),

@@ -876,11 +876,6 @@ int dsa_prr_step(const dsa_paged_kv* kv, const dsa_prr_step_args* args, void* wo
   if (!workspace || workspace_bytes < ws_need)
     return fail(DSA_ERR_WORKSPACE, "workspace of %zu bytes needed", ws_need);
   if (!aligned(workspace, 16)) return fail(DSA_ERR_ALIGNMENT, "workspace must be 16-byte aligned");
-  int dev = 0, coop = 0;
-  cudaError_t e = cudaGetDevice(&dev);
-  if (e == cudaSuccess) e = cudaDeviceGetAttribute(&coop, cudaDevAttrCooperativeLaunch, dev);
-  if (e != cudaSuccess) return cuda_fail(e, "dsa_prr_step device query");
-  if (!coop) return fail(DSA_ERR_UNSUPPORTED, "dsa_prr_step: the device has no cooperative launch");
   if (prr_step_smem_bytes(v.p, x.stride, x.k_pred) > kPrrSmemLimit)
     return fail(DSA_ERR_UNSUPPORTED, "dsa_prr_step: shape needs too much shared memory");
   CUtensorMap tk, tv;
@@ -913,7 +908,7 @@ int dsa_prr_step(const dsa_paged_kv* kv, const dsa_prr_step_args* args, void* wo
   a.out = x.out;
   a.m = x.m;
   a.l = x.l;
-  e = launch_prr_step(tk, tv, a, workspace, static_cast<cudaStream_t>(stream));
+  const cudaError_t e = launch_prr_step(tk, tv, a, workspace, static_cast<cudaStream_t>(stream));
   return e == cudaSuccess ? ok() : cuda_fail(e, "dsa_prr_step launch");
 }
 

@@ -137,6 +137,16 @@ DSA_DEV void named_barrier(int id, int count) {
   asm volatile("bar.sync %0, %1;" ::"r"(id), "r"(count) : "memory");
 }
 
+// Programmatic dependent launch.  A kernel launched with programmatic stream serialization may
+// start while the kernel before it in the stream is still running: it runs only set-up that
+// touches no global memory written by earlier work, then waits here until every prerequisite
+// grid has completed and its memory operations are visible.  Without such a dependency the wait
+// returns at once.
+DSA_DEV void grid_dependency_wait() { asm volatile("griddepcontrol.wait;" ::: "memory"); }
+// Lets the kernel that follows in the stream be scheduled before this one completes (its blocks
+// take SMs as this kernel's blocks leave them, and wait at grid_dependency_wait).
+DSA_DEV void launch_dependents() { asm volatile("griddepcontrol.launch_dependents;" ::: "memory"); }
+
 // Arrival at a named barrier without waiting (the arriving threads' earlier shared-memory writes
 // are visible to the threads that wait at it).
 DSA_DEV void named_barrier_arrive(int id, int count) {

@@ -124,7 +124,7 @@ int stream_attn_grid();  // CTAs of one launch: one per SM
 cudaError_t launch_stream_attn(const CUtensorMap& tmK, const CUtensorMap& tmV,
                                const StreamAttnArgs& a, int grid, cudaStream_t s);
 
-// One PRR decode step in one cooperative launch (prr_step.cu).
+// One PRR decode step in one launch of one CTA per SM (prr_step.cu).
 constexpr int kPrrPredMax = 256;   // bound of k and k_pred
 constexpr size_t kPrrSmemLimit = 227 * 1024;
 struct PrrStepArgs {

@@ -1,4 +1,4 @@
-// One whole PRR decode step (t >= 1) in a single cooperative launch ("Predict, Reuse, and Repair"
+// One whole PRR decode step (t >= 1) in a single launch of one CTA per SM ("Predict, Reuse, and Repair"
 // §3: speculation over the predicted set P_t, the true selection A_t, the predictor update, repair
 // of the missed pages and the merge), organised so that no CTA ever waits for the whole grid.
 //
@@ -243,6 +243,10 @@ __global__ void __launch_bounds__(kThreads, 1)
     s_abort = 0;
     s_issued = 0;
   }
+  // everything above touches shared memory and the arguments only; from here on global memory
+  // written by earlier kernels is read
+  launch_dependents();
+  grid_dependency_wait();
   __syncthreads();
   DSA_TRACE_BEGIN();
 
@@ -1188,16 +1192,23 @@ cudaError_t launch_prr_step(const CUtensorMap& tmK, const CUtensorMap& tmV, cons
                                                          bytes)) != cudaSuccess)
     return e;
   if (per_sm < 1) return cudaErrorInvalidConfiguration;
-  // CTAs wait on per-row counters that other CTAs advance: every CTA must be resident at once,
-  // hence a cooperative launch of one CTA per SM
+  // CTAs wait on per-row counters that other CTAs advance, so every CTA must be resident at once:
+  // the grid is one CTA per SM and at least one fits on each.  The launch is a programmatic one
+  // without the cooperative attribute (with it, the launch overlapped nothing): its CTAs take SMs
+  // as the previous kernel of the stream leaves them, only after every CTA of that kernel has
+  // started, and wait for it to finish at grid_dependency_wait; once it has, every SM is free for
+  // the rest of this grid.  The counter
+  // waits are bounded (DSA_STATUS_TIMEOUT) should another stream hold SMs for longer.
   cudaLaunchConfig_t cfg = {};
   cfg.gridDim = dim3(sms);
   cfg.blockDim = dim3(kThreads);
   cfg.dynamicSmemBytes = bytes;
   cfg.stream = stream;
+  // programmatic stream serialization: the launch may begin while the previous kernel of the
+  // stream runs; the kernel waits for it (grid_dependency_wait) before its first global read
   cudaLaunchAttribute attr[1];
-  attr[0].id = cudaLaunchAttributeCooperative;
-  attr[0].val.cooperative = 1;
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[0].val.programmaticStreamSerializationAllowed = 1;
   cfg.attrs = attr;
   cfg.numAttrs = 1;
   return cudaLaunchKernelEx(&cfg, prr_step_kernel, tmK, tmV, a);

@@ -372,7 +372,11 @@ size_t dsa_calibrate_ema_workspace_size(int32_t steps, int32_t rows, int32_t n, 
  *                                                                              next_idx/next_count
  *   dsa_repair_merge(P_t, page_partials, A_t, superset)                     -> out/m/l
  * with scores, A_t, the EMA state and P_{t+1} bit for bit and out/m/l up to fp32 rounding.  One
- * cooperative launch of one CTA per SM; no CTA waits for the whole grid: every CTA scores an equal
+ * launch of one CTA per SM, all resident at once (the step assumes no other stream holds SMs for
+ * long while it runs; its waits are bounded and raise DSA_STATUS_TIMEOUT), launched as a
+ * programmatic dependent of the previous kernel in the stream: its CTAs are scheduled while that
+ * kernel finishes and wait for it before reading global memory.  No CTA waits for the whole grid:
+ * every CTA scores an equal
  * share of the (request, KV head, page) slots beside its pages of P_t, and the selections, the
  * repair and the merges wait only for their own row's counters.
  *   args->q            : bf16 [B][Hq][D], 16-byte aligned.  Device memory, or page-locked host
