@@ -46,6 +46,8 @@ template <int LIST>
 __global__ void __launch_bounds__(kAttnThreads)
     attn_pages_kernel(const __grid_constant__ CUtensorMap tmK,
                       const __grid_constant__ CUtensorMap tmV, const AttnArgs a) {
+  launch_dependents();  // the next kernel may be scheduled; it waits for this one
+  grid_dependency_wait();  // the kernels before this one have completed
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = smem_align1024(smem_raw);
   const KvView& kv = a.kv;
@@ -324,6 +326,8 @@ __host__ __device__ inline MergeLayout merge_layout(int max_parts, int a_ints) {
 }
 
 __global__ void __launch_bounds__(kMergeThreads) merge_records_kernel(const MergeArgs a) {
+  launch_dependents();  // the next kernel may be scheduled; it waits for this one
+  grid_dependency_wait();  // the kernels before this one have completed
   extern __shared__ __align__(16) uint8_t msm[];
   const int row = blockIdx.x, g = blockIdx.y;
   const int b = row / a.Hkv, h = row % a.Hkv;
@@ -446,8 +450,7 @@ cudaError_t launch_list(const CUtensorMap& tmK, const CUtensorMap& tmV, const At
       ensure_dynamic_smem(reinterpret_cast<const void*>(attn_pages_kernel<LIST>), bytes);
   if (e != cudaSuccess) return e;
   dim3 grid(grid_x, a.kv.B * a.kv.Hkv);
-  attn_pages_kernel<LIST><<<grid, kAttnThreads, bytes, s>>>(tmK, tmV, a);
-  return cudaGetLastError();
+  return launch_pdl(attn_pages_kernel<LIST>, grid, kAttnThreads, bytes, s, tmK, tmV, a);
 }
 
 }  // namespace
@@ -475,8 +478,7 @@ cudaError_t launch_merge(const MergeArgs& a, cudaStream_t s) {
   cudaError_t e = ensure_dynamic_smem(reinterpret_cast<const void*>(merge_records_kernel), bytes);
   if (e != cudaSuccess) return e;
   dim3 grid(a.rows, a.G);
-  merge_records_kernel<<<grid, kMergeThreads, bytes, s>>>(a);
-  return cudaGetLastError();
+  return launch_pdl(merge_records_kernel, grid, kMergeThreads, bytes, s, a);
 }
 
 }  // namespace dsa

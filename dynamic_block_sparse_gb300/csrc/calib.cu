@@ -32,6 +32,8 @@ __global__ void __launch_bounds__(kCalibThreads, 2)
                  int k_pred, const int32_t* __restrict__ a_idx, const int32_t* __restrict__ a_cnt,
                  float* __restrict__ state, float* __restrict__ H, int32_t* __restrict__ best,
                  unsigned* __restrict__ done) {
+  launch_dependents();  // the next kernel may be scheduled; it waits for this one
+  grid_dependency_wait();  // the kernels before this one have completed
   extern __shared__ uint32_t keys[];  // [n] ranking keys of the prediction
   __shared__ SelectAnyScratch<kCalibThreads> sh;
   __shared__ int32_t listP[kMaxListPages];  // k_pred <= 256
@@ -224,11 +226,9 @@ cudaError_t launch_calib(const float* traj, int T, int rows, int n, int stride, 
   const size_t bytes = calib_smem_bytes(n);
   e = ensure_dynamic_smem(reinterpret_cast<const void*>(calib_kernel), bytes);
   if (e != cudaSuccess) return e;
-  calib_kernel<<<rows * kCalibPoints, kCalibThreads, bytes, s>>>(
-      traj, T, rows, n, stride, k, k_pred, a_idx, a_cnt,
-      reinterpret_cast<float*>(ws + w.state_off), H, best,
-      reinterpret_cast<unsigned*>(ws + w.done_off));
-  return cudaGetLastError();
+  return launch_pdl(calib_kernel, rows * kCalibPoints, kCalibThreads, bytes, s, traj, T, rows, n,
+                    stride, k, k_pred, a_idx, a_cnt, reinterpret_cast<float*>(ws + w.state_off), H,
+                    best, reinterpret_cast<unsigned*>(ws + w.done_off));
 }
 
 }  // namespace dsa

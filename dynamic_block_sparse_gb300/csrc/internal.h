@@ -22,6 +22,26 @@ constexpr int kRecordFloats = 132;     // partial record: O[128], m, l, pad, pad
 constexpr int kMaxSelectN = 32768;     // candidates per row held in shared memory by selection
 constexpr int kMaxThresholdN = 16384;  // candidates per row for the PSA kernel
 
+// Launches `kernel` as a programmatic dependent of the previous kernel in the stream: its blocks
+// may be scheduled while that kernel finishes.  Every kernel of the library starts with
+// launch_dependents() and grid_dependency_wait() (common.cuh), so it touches no global memory
+// before the kernels ahead of it in the stream have completed.
+template <typename... P, typename... A>
+inline cudaError_t launch_pdl(void (*kernel)(P...), dim3 grid, dim3 block, size_t smem,
+                              cudaStream_t s, A&&... args) {
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = grid;
+  cfg.blockDim = block;
+  cfg.dynamicSmemBytes = smem;
+  cfg.stream = s;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[0].val.programmaticStreamSerializationAllowed = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  return cudaLaunchKernelEx(&cfg, kernel, static_cast<A&&>(args)...);
+}
+
 struct KvView {
   const int32_t* page_table;
   const int32_t* seq_lens;

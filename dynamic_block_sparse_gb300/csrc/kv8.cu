@@ -7,6 +7,7 @@
 // The quantiser; the persistent attention (stream_attn.cu) reads the codes per tile.
 #include <cuda_fp8.h>
 
+#include "common.cuh"
 #include "internal.h"
 
 namespace dsa {
@@ -21,6 +22,8 @@ constexpr int kQ8Warps = kQ8Threads / 32;
 __global__ void __launch_bounds__(kQ8Threads)
     quantize_kv8_kernel(const __nv_bfloat16* __restrict__ src, long long n_rows, int page,
                         int which, uint8_t* __restrict__ kv8) {
+  launch_dependents();  // the next kernel may be scheduled; it waits for this one
+  grid_dependency_wait();  // the kernels before this one have completed
   const long long r = static_cast<long long>(blockIdx.x) * kQ8Warps + (threadIdx.x >> 5);
   if (r >= n_rows) return;
   const long long blk = r / page;
@@ -63,9 +66,8 @@ cudaError_t launch_quantize_kv8(const __nv_bfloat16* src, long long n_rows, int 
   const long long blocks = (n_rows + kQ8Warps - 1) / kQ8Warps;
   if (blocks > 0x7fffffffLL) return cudaErrorInvalidValue;
   if (blocks == 0) return cudaSuccess;
-  quantize_kv8_kernel<<<static_cast<unsigned>(blocks), kQ8Threads, 0, s>>>(src, n_rows, page,
-                                                                           which, kv8);
-  return cudaGetLastError();
+  return launch_pdl(quantize_kv8_kernel, static_cast<unsigned>(blocks), kQ8Threads, 0, s, src,
+                    n_rows, page, which, kv8);
 }
 
 }  // namespace dsa

@@ -120,6 +120,8 @@ template <int KIND>
 __global__ void __launch_bounds__(256)
     build_meta_kernel(const KvView kv, const __nv_bfloat16* __restrict__ k_pages, int lp,
                       void* __restrict__ meta) {
+  launch_dependents();  // the next kernel may be scheduled; it waits for this one
+  grid_dependency_wait();  // the kernels before this one have completed
   const int lane = threadIdx.x & 31;
   const long long item = static_cast<long long>(blockIdx.x) * 8 + (threadIdx.x >> 5);
   const int h = static_cast<int>(item % kv.Hkv);
@@ -144,6 +146,8 @@ __global__ void __launch_bounds__(256)
     append_kv_kernel(const KvView kv, __nv_bfloat16* __restrict__ k_pages,
                      __nv_bfloat16* __restrict__ v_pages, const __nv_bfloat16* __restrict__ k_new,
                      const __nv_bfloat16* __restrict__ v_new, int lp, void* __restrict__ meta) {
+  launch_dependents();  // the next kernel may be scheduled; it waits for this one
+  grid_dependency_wait();  // the kernels before this one have completed
   const int lane = threadIdx.x & 31;
   const long long item = static_cast<long long>(blockIdx.x) * 8 + (threadIdx.x >> 5);
   const int h = static_cast<int>(item % kv.Hkv);
@@ -179,6 +183,8 @@ __global__ void __launch_bounds__(kScoreThreads)
     score_kernel(const KvView kv, const __nv_bfloat16* __restrict__ q,
                  const uint8_t* __restrict__ meta, int lp, int pages_per_cta,
                  float* __restrict__ scores, int stride) {
+  launch_dependents();  // the next kernel may be scheduled; it waits for this one
+  grid_dependency_wait();  // the kernels before this one have completed
   __shared__ float sQbar[kHeadDim];
   const int row = blockIdx.y;
   const int b = row / kv.Hkv, h = row % kv.Hkv;
@@ -230,11 +236,10 @@ cudaError_t launch_build_meta(const KvView& kv, const __nv_bfloat16* k_pages, in
   const long long items = static_cast<long long>(kv.B) * kv.max_pages * kv.Hkv;
   const long long blocks = (items + 7) / 8;
   if (blocks > 0x7fffffffLL) return cudaErrorInvalidValue;
-  if (kind == DSA_META_MINMAX)
-    build_meta_kernel<DSA_META_MINMAX><<<static_cast<unsigned>(blocks), 256, 0, s>>>(kv, k_pages, lp, meta);
-  else
-    build_meta_kernel<DSA_META_MEAN><<<static_cast<unsigned>(blocks), 256, 0, s>>>(kv, k_pages, lp, meta);
-  return cudaGetLastError();
+  const unsigned nb = static_cast<unsigned>(blocks);
+  return kind == DSA_META_MINMAX
+             ? launch_pdl(build_meta_kernel<DSA_META_MINMAX>, nb, 256, 0, s, kv, k_pages, lp, meta)
+             : launch_pdl(build_meta_kernel<DSA_META_MEAN>, nb, 256, 0, s, kv, k_pages, lp, meta);
 }
 
 cudaError_t launch_append_kv(const KvView& kv, __nv_bfloat16* k_pages, __nv_bfloat16* v_pages,
@@ -243,13 +248,12 @@ cudaError_t launch_append_kv(const KvView& kv, __nv_bfloat16* k_pages, __nv_bflo
   const long long items = static_cast<long long>(kv.B) * kv.Hkv;
   const long long blocks = (items + 7) / 8;
   if (blocks > 0x7fffffffLL) return cudaErrorInvalidValue;
-  if (kind == DSA_META_MINMAX)
-    append_kv_kernel<DSA_META_MINMAX><<<static_cast<unsigned>(blocks), 256, 0, s>>>(
-        kv, k_pages, v_pages, k_new, v_new, lp, meta);
-  else
-    append_kv_kernel<DSA_META_MEAN><<<static_cast<unsigned>(blocks), 256, 0, s>>>(
-        kv, k_pages, v_pages, k_new, v_new, lp, meta);
-  return cudaGetLastError();
+  const unsigned nb = static_cast<unsigned>(blocks);
+  return kind == DSA_META_MINMAX
+             ? launch_pdl(append_kv_kernel<DSA_META_MINMAX>, nb, 256, 0, s, kv, k_pages, v_pages,
+                          k_new, v_new, lp, meta)
+             : launch_pdl(append_kv_kernel<DSA_META_MEAN>, nb, 256, 0, s, kv, k_pages, v_pages,
+                          k_new, v_new, lp, meta);
 }
 
 cudaError_t launch_score(const KvView& kv, const __nv_bfloat16* q, const void* meta, int kind,
@@ -261,11 +265,11 @@ cudaError_t launch_score(const KvView& kv, const __nv_bfloat16* q, const void* m
     ppc /= 2;
   dim3 grid((stride + ppc - 1) / ppc, rows);
   const uint8_t* m = static_cast<const uint8_t*>(meta);
-  if (kind == DSA_META_MINMAX)
-    score_kernel<DSA_META_MINMAX><<<grid, kScoreThreads, 0, s>>>(kv, q, m, lp, ppc, scores, stride);
-  else
-    score_kernel<DSA_META_MEAN><<<grid, kScoreThreads, 0, s>>>(kv, q, m, lp, ppc, scores, stride);
-  return cudaGetLastError();
+  return kind == DSA_META_MINMAX
+             ? launch_pdl(score_kernel<DSA_META_MINMAX>, grid, kScoreThreads, 0, s, kv, q, m, lp,
+                          ppc, scores, stride)
+             : launch_pdl(score_kernel<DSA_META_MEAN>, grid, kScoreThreads, 0, s, kv, q, m, lp,
+                          ppc, scores, stride);
 }
 
 }  // namespace dsa

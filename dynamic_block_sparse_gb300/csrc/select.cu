@@ -29,6 +29,8 @@ DSA_DEV void for_each_row_value(const float* __restrict__ src, int n, bool vec4,
 __global__ void __launch_bounds__(kSelectThreads)
     select_kernel(const float* __restrict__ scores, int n_logical, int stride, int g, int k,
                   int32_t* __restrict__ idx, int idx_stride, int32_t* __restrict__ count) {
+  launch_dependents();  // the next kernel may be scheduled; it waits for this one
+  grid_dependency_wait();  // the kernels before this one have completed
   extern __shared__ uint32_t keys[];
   __shared__ SelectAnyScratch<kSelectThreads> sh;
   const int row = blockIdx.x;
@@ -64,6 +66,8 @@ __global__ void __launch_bounds__(kSelectThreads)
                float* __restrict__ v, int mode, float alpha, float beta, float gamma,
                float* __restrict__ pred, int k_pred, int32_t* __restrict__ pred_idx,
                int pred_idx_stride, int32_t* __restrict__ pred_count) {
+  launch_dependents();  // the next kernel may be scheduled; it waits for this one
+  grid_dependency_wait();  // the kernels before this one have completed
   extern __shared__ uint32_t keys[];
   __shared__ SelectAnyScratch<kSelectThreads> sh;
   const int row = blockIdx.x;
@@ -136,9 +140,8 @@ cudaError_t launch_select(const float* scores, int rows, int n_logical, int stri
   const size_t bytes = static_cast<size_t>(n > 0 ? n : 1) * 4;
   cudaError_t e = set_smem(reinterpret_cast<const void*>(select_kernel), bytes);
   if (e != cudaSuccess) return e;
-  select_kernel<<<rows, kSelectThreads, bytes, s>>>(scores, n_logical, stride, g, k, idx,
-                                                    idx_stride, count);
-  return cudaGetLastError();
+  return launch_pdl(select_kernel, rows, kSelectThreads, bytes, s, scores, n_logical, stride, g, k,
+                    idx, idx_stride, count);
 }
 
 cudaError_t launch_ema(const float* IS, int rows, int n, int stride, float* ell, float* v,
@@ -148,10 +151,8 @@ cudaError_t launch_ema(const float* IS, int rows, int n, int stride, float* ell,
   const size_t bytes = static_cast<size_t>(n > 0 ? n : 1) * 4;
   cudaError_t e = set_smem(reinterpret_cast<const void*>(ema_kernel), bytes);
   if (e != cudaSuccess) return e;
-  ema_kernel<<<rows, kSelectThreads, bytes, s>>>(IS, n, stride, ell, v, mode, alpha, beta, gamma,
-                                                 pred, k_pred, pred_idx, pred_idx_stride,
-                                                 pred_count);
-  return cudaGetLastError();
+  return launch_pdl(ema_kernel, rows, kSelectThreads, bytes, s, IS, n, stride, ell, v, mode, alpha,
+                    beta, gamma, pred, k_pred, pred_idx, pred_idx_stride, pred_count);
 }
 
 }  // namespace dsa

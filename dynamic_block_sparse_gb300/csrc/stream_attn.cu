@@ -280,6 +280,8 @@ template <bool STREAMING, bool KV8>
 __global__ void __launch_bounds__(kSThreads, 1)
     stream_attn_kernel(const __grid_constant__ CUtensorMap tmK,
                        const __grid_constant__ CUtensorMap tmV, const StreamAttnArgs a) {
+  launch_dependents();  // the next kernel may be scheduled; it waits for this one
+  grid_dependency_wait();  // the kernels before this one have completed
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = smem_align1024(smem_raw);
   const KvView& kv = a.kv;
@@ -989,8 +991,7 @@ cudaError_t launch_stream_attn(const CUtensorMap& tmK, const CUtensorMap& tmV,
   auto go = [&](auto kernel) -> cudaError_t {
     cudaError_t e = ensure_dynamic_smem(reinterpret_cast<const void*>(kernel), bytes);
     if (e != cudaSuccess) return e;
-    kernel<<<grid, kSThreads, bytes, s>>>(tmK, tmV, a);
-    return cudaGetLastError();
+    return launch_pdl(kernel, grid, kSThreads, bytes, s, tmK, tmV, a);
   };
   if (a.kv8 != nullptr) return go(stream_attn_kernel<false, true>);
   return a.stream_stride > 0 ? go(stream_attn_kernel<true, false>)

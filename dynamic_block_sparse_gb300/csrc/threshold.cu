@@ -149,6 +149,8 @@ DSA_DEV unsigned long long warp_max_u64(unsigned long long v) {
 __global__ void __launch_bounds__(kThrThreads)
     psa_threshold_kernel(const __grid_constant__ CUtensorMap tmK,
                          const __grid_constant__ CUtensorMap tmV, const ThresholdArgs a) {
+  launch_dependents();  // the next kernel may be scheduled; it waits for this one
+  grid_dependency_wait();  // the kernels before this one have completed
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = smem_align1024(smem_raw);
   __shared__ int s_red[kThrWarps];              // valid keys per warp
@@ -632,8 +634,8 @@ cudaError_t launch_threshold(const CUtensorMap& tmK, const CUtensorMap& tmV,
   cudaError_t e =
       ensure_dynamic_smem(reinterpret_cast<const void*>(psa_threshold_kernel), lay.total);
   if (e != cudaSuccess) return e;
-  psa_threshold_kernel<<<a.kv.B * a.kv.Hkv, kThrThreads, lay.total, s>>>(tmK, tmV, a);
-  return cudaGetLastError();
+  return launch_pdl(psa_threshold_kernel, a.kv.B * a.kv.Hkv, kThrThreads, lay.total, s, tmK, tmV,
+                    a);
 }
 
 size_t threshold_smem_bytes(int page, int max_pages) { return thr_layout(page, max_pages).total; }
