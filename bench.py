@@ -686,6 +686,22 @@ def bench_rows(dev, flush, peak, only=None):
         out.append(_entry("A5", w.name, "dsa_select_threshold tau=0.95 (rank, attend, stop)", ms,
                           rows * npg * 4 + visited * w.page_size * KVP + q.numel() * 6, peak,
                           mean_blocks=round(visited / rows, 2)))
+        # the same selection under the N_left reading of the stop rule (PSA §3.2's listing keeps
+        # N_left but its test uses AS_min alone): mean n* and time beside the literal rule's
+        B.dsa_select_threshold(cache.kv, q, dec.scores, w.tau, w.cap, dec.scale, dec.idx,
+                               dec.count, dec.out, dec.m, dec.l, flags=B.DSA_PSA_NLEFT)
+        torch.cuda.synchronize()
+        visited_nl = int(dec.count.sum())
+        ms_nl = _time_call((lambda: B.dsa_select_threshold(
+            cache.kv, q, dec.scores, w.tau, w.cap, dec.scale, dec.idx, dec.count, dec.out, dec.m,
+            dec.l, flags=B.DSA_PSA_NLEFT)), flush)
+        out.append(_entry("A5-nleft", w.name,
+                          "dsa_select_threshold tau=0.95, N_left rule AS_acc/(AS_acc+N_left*AS_min)",
+                          ms_nl, rows * npg * 4 + visited_nl * w.page_size * KVP + q.numel() * 6,
+                          peak, mean_blocks=round(visited_nl / rows, 2),
+                          capped_rows=int((dec.count >= w.cap).sum())))
+        dec.step(q)  # the literal rule's selection again, for the step row
+        torch.cuda.synchronize()
         ms = _time_call((lambda: dec.step(q)), flush)
         out.append(_entry("step", w.name, "score + threshold selection", ms,
                           rows * npg * 516 + visited * w.page_size * KVP, peak))
@@ -710,9 +726,10 @@ def bench_rows(dev, flush, peak, only=None):
 
 # ------------------------------------------------------------------------------------ oracle
 
-def oracle_prr(w, seconds: float | None, steps: int | None, warmup: int = 0):
+def oracle_prr(w, seconds: float | None, steps: int | None, warmup: int = 0, ready=None):
     """Times the float64 oracle's PRR decode step (both KV heads, metadata precomputed) on the
-    host.  Returns (seconds per step, steps timed, bytes per step)."""
+    host.  `ready`, if given, is called once the set-up and warm-up are done, just before the
+    timed loop.  Returns (seconds per step, steps timed, bytes per step)."""
     import numpy as np
 
     import oracle as O
@@ -754,6 +771,8 @@ def oracle_prr(w, seconds: float | None, steps: int | None, warmup: int = 0):
     for _ in range(warmup):
         one_step(t)
         t += 1
+    if ready is not None:
+        ready()
     t0 = time.perf_counter()
     done = 0
     while True:
@@ -771,25 +790,78 @@ def oracle_prr(w, seconds: float | None, steps: int | None, warmup: int = 0):
     return el / done, done, total
 
 
-def cpu_baseline(args, w):
-    """Runs the oracle in a child process pinned to one BLAS thread for ~cpu_seconds."""
+def _oracle_procs(args, w, n):
+    """n oracle children at once, one BLAS thread each; they start timing together (each waits
+    for a line on its standard input once its set-up is done).  Returns their JSON results."""
     env = dict(os.environ)
     for k in ("OMP_NUM_THREADS", "OPENBLAS_NUM_THREADS", "MKL_NUM_THREADS"):
         env[k] = "1"
     env["CUDA_VISIBLE_DEVICES"] = ""
     cmd = [sys.executable, os.path.abspath(__file__), "--oracle-child", "--workload", w.name,
            "--cpu-seconds", str(args.cpu_seconds)]
-    r = subprocess.run(cmd, capture_output=True, text=True, env=env, timeout=900)
-    if r.returncode != 0:
-        return {"value": None, "error": r.stderr[-400:]}
-    return json.loads(r.stdout.strip().splitlines()[-1])
+    procs = [subprocess.Popen(cmd, stdin=subprocess.PIPE, stdout=subprocess.PIPE,
+                              stderr=subprocess.PIPE, text=True, env=env) for _ in range(n)]
+    try:
+        for p in procs:  # every child reports its set-up done
+            line = p.stdout.readline()
+            if line.strip() != "ready":
+                raise RuntimeError(f"oracle child: {line.strip()!r} {p.stderr.read()[-300:]}")
+        for p in procs:
+            p.stdin.write("go\n")
+            p.stdin.flush()
+        out = []
+        for p in procs:
+            o, e = p.communicate(timeout=900)
+            if p.returncode != 0:
+                raise RuntimeError(e[-300:])
+            out.append(json.loads(o.strip().splitlines()[-1]))
+        return out
+    finally:
+        for p in procs:
+            if p.poll() is None:
+                p.kill()
+
+
+def cpu_baseline(args, w):
+    """The oracle on the host cores: one child process with one BLAS thread, then one such child
+    per core (each decoding its own copy of the workload, as independent layers or requests
+    would be), timed over the same window; `value` is the all-core aggregate."""
+    nproc = os.cpu_count() or 1
+    try:
+        one = _oracle_procs(args, w, 1)[0]
+    except Exception as e:  # noqa: BLE001 - reported in the line
+        return {"value": None, "error": str(e)[-400:]}
+    # each child holds the workload's K/V in float64 (~2.2 GB for prr_512k): stay inside memory
+    try:
+        ram = os.sysconf("SC_PHYS_PAGES") * os.sysconf("SC_PAGE_SIZE")
+    except (ValueError, OSError):
+        ram = 0
+    n = max(1, min(nproc, int(ram // (4 << 30)) if ram else 1))
+    try:
+        many = _oracle_procs(args, w, n) if n > 1 else [one]
+    except Exception as e:  # noqa: BLE001
+        many, n = [one], 1
+        one["all_core_error"] = str(e)[-300:]
+    agg = sum(r["value"] for r in many)
+    return {"value": agg, "unit": "GB/s", "cores": n, "nproc": nproc, "kind": "oracle",
+            "ms_per_step": statistics.mean(r["ms_per_step"] for r in many),
+            "sample": f"{n} processes at once, each ~{args.cpu_seconds:g} s of consecutive decode "
+                      f"steps of {w.name} (both KV heads, metadata precomputed), float64 numpy, "
+                      f"1 BLAS thread each; value = the sum of their throughputs",
+            "single_core": {"value": one["value"], "unit": "GB/s", "cores": 1,
+                            "ms_per_step": one["ms_per_step"], "sample": one["sample"]}}
 
 
 def oracle_child(args):
     from dynamic_block_sparse_gb300.workloads import BY_NAME
 
     w = BY_NAME[args.workload]
-    sec, n, bytes_step = oracle_prr(w, args.cpu_seconds, None)
+
+    def ready():  # set-up done: tell the parent, wait for the common start
+        print("ready", flush=True)
+        sys.stdin.readline()
+
+    sec, n, bytes_step = oracle_prr(w, args.cpu_seconds, None, ready=ready)
     print(json.dumps({"value": bytes_step / sec / 1e9, "unit": "GB/s", "cores": 1,
                       "kind": "oracle", "ms_per_step": sec * 1e3,
                       "sample": f"{n} consecutive decode steps of {w.name} (both KV heads, "
