@@ -30,7 +30,12 @@ Readings taken where the pages are silent or garbled (each also listed in the de
   true set); its superset mode keeps them (output equals attention over the union);
 * the 8-bit page format (KV8) is the library's own (LServe §3.2.1 keeps quantised KV pages; its
   format is not given): one fp32 scale per token row, ``max |x| / 448`` computed in fp32, and
-  e4m3 codes of ``x / scale`` (fp32 division) rounded to nearest even; a zero row keeps scale 0.
+  e4m3 codes of ``x / scale`` (fp32 division) rounded to nearest even; a zero row keeps scale 0;
+* the 4-bit page format (KV4) is the library's own too (LServe's decode keeps KV in 4 bits, the
+  W4A8KV4 setting it builds on; no format is given): one fp32 scale per token row,
+  ``max |x| / 7`` in fp32, integer codes ``round(x / scale)`` (fp32 division, ties to even) in
+  [-7, 7], stored as the nibble ``code + 8``, two dims per byte (the even dim in the low nibble);
+  a zero row keeps scale 0 and codes 0.
 """
 
 from __future__ import annotations
@@ -51,7 +56,7 @@ __all__ = [
     "psa_progressive",
     "ema_init", "ema_update", "ema_predict",
     "spec_repair", "hit_rate", "score_weighted_hit", "calibration_grid", "calibrate_ema",
-    "kv8_encode_rows", "kv8_decode_rows",
+    "kv8_encode_rows", "kv8_decode_rows", "kv4_encode_rows", "kv4_decode_rows",
 ]
 
 
@@ -453,3 +458,38 @@ def kv8_decode_rows(codes, scales) -> np.ndarray:
     c = torch.from_numpy(np.ascontiguousarray(np.asarray(codes, dtype=np.uint8)))
     vals = c.view(torch.float8_e4m3fn).to(torch.float64).numpy()
     return vals * np.asarray(scales, dtype=np.float64)[..., None]
+
+
+# --------------------------------------------------------------------------------------------
+# KV4 pages: 4-bit integer rows with one fp32 scale each (the library's own format)
+# --------------------------------------------------------------------------------------------
+
+KV4_MAX = 7  # codes -7 .. 7
+
+
+def kv4_encode_rows(x):
+    """Rows ``x`` ``[..., D]`` (bf16 values, D even) -> (packed codes uint8 ``[..., D / 2]``,
+    scales float32 ``[...]``).
+
+    scale = max |x| / 7 in fp32; code = x / scale (fp32 division) rounded to the nearest integer,
+    ties to even, kept in [-7, 7]; the nibble code + 8 of dim 2i goes to the low half of byte i,
+    that of dim 2i + 1 to its high half.  A zero row keeps scale 0 and codes 0 (nibbles 8)."""
+    x32 = np.asarray(x, dtype=np.float32)
+    amax = np.max(np.abs(x32), axis=-1)
+    scale = (amax / np.float32(KV4_MAX)).astype(np.float32)
+    safe = np.where(scale > 0, scale, np.float32(1.0)).astype(np.float32)
+    y = (x32 / safe[..., None]).astype(np.float32)
+    code = np.clip(np.rint(y), -KV4_MAX, KV4_MAX).astype(np.int64)
+    code = np.where(scale[..., None] > 0, code, 0)
+    nib = (code + 8).astype(np.uint8)
+    packed = (nib[..., 0::2] | (nib[..., 1::2] << 4)).astype(np.uint8)
+    return packed, scale
+
+
+def kv4_decode_rows(packed, scales) -> np.ndarray:
+    """float64 values ``(nibble - 8) * scale`` of KV4 rows ``[..., D / 2]`` -> ``[..., D]``."""
+    p = np.asarray(packed, dtype=np.uint8)
+    lo = (p & 0xF).astype(np.int64) - 8
+    hi = (p >> 4).astype(np.int64) - 8
+    code = np.stack([lo, hi], axis=-1).reshape(*p.shape[:-1], 2 * p.shape[-1])
+    return code.astype(np.float64) * np.asarray(scales, dtype=np.float64)[..., None]

@@ -511,6 +511,16 @@ def test_pins_catch_planted_mistakes(monkeypatch):
         _, Hs_count = O.calibrate_ema(traj, cal["k"], cal["k_pred"])
     assert abs(Hs_count[79] - cal["H"]["79"]) > 0.01
 
+    # KV4: rounding half away from zero, or the odd dim in the low nibble
+    kv4 = json.load(open(os.path.join(GOLDEN, "kv4_hand_row.json")))
+    row = np.array([kv4["row"]], dtype=np.float32)
+    with monkeypatch.context() as mp:
+        mp.setattr(OD.np, "rint", lambda y: np.sign(y) * np.floor(np.abs(y) + 0.5))
+        assert O.kv4_encode_rows(row)[0][0].tolist() != kv4["bytes"]
+    packed, _ = O.kv4_encode_rows(row)
+    swapped = ((packed >> 4) | ((packed & 15) << 4)).astype(np.uint8)
+    assert swapped[0].tolist() != kv4["bytes"]
+
 
 # ------------------------------------------------------------------------------------ KV8
 
@@ -542,3 +552,41 @@ def test_kv8_round_trip_error_is_bounded():
         if scale[i] > 0:
             j = int(np.argmax(np.abs(x[i])))
             assert abs(dec[i, j] - x[i, j]) <= abs(x[i, j]) * 1e-6
+
+
+# ------------------------------------------------------------------------------------ KV4
+
+def test_kv4_codes_match_the_hand_row():
+    """Scale, rounding (ties to even), offset-8 nibbles and their order in a byte against a row
+    worked by hand (tests/golden/kv4_hand_row.json)."""
+    g = json.load(open(os.path.join(GOLDEN, "kv4_hand_row.json")))
+    row = np.array([g["row"]], dtype=np.float32)
+    packed, scale = O.kv4_encode_rows(row)
+    assert scale[0] == np.float32(g["scale"])
+    assert packed[0].tolist() == g["bytes"]
+    assert O.kv4_decode_rows(packed, scale)[0].tolist() == g["decoded"]
+    # a power-of-two factor moves the scale only
+    p2, s2 = O.kv4_encode_rows(row * np.float32(0.125))
+    assert p2[0].tolist() == g["bytes"] and s2[0] == np.float32(0.125)
+    pz, sz = O.kv4_encode_rows(np.zeros((1, 8), dtype=np.float32))
+    assert sz[0] == 0 and pz[0].tolist() == [g["zero_row_byte"]] * 4
+
+
+def test_kv4_round_trip_error_is_half_a_step():
+    """Decoded values stay within half a code step (scale / 2) of the input; the largest magnitude
+    of a row decodes to 7 * scale (within fp32 rounding of max|x| / 7); codes stay in [-7, 7]."""
+    r = rng(5)
+    x = r.normal(size=(60, 128)).astype(np.float32) * r.uniform(0.01, 30, size=(60, 1)).astype(np.float32)
+    x[11] = 0.0
+    packed, scale = O.kv4_encode_rows(x)
+    dec = O.kv4_decode_rows(packed, scale)
+    assert scale[11] == 0 and np.all(dec[11] == 0)
+    err = np.abs(dec - x)
+    assert np.all(err <= scale[:, None] * (0.5 + 1e-6))
+    nib = np.stack([packed & 15, packed >> 4], axis=-1)
+    assert nib.min() >= 1 and nib.max() <= 15
+    for i in range(60):
+        if scale[i] > 0:
+            j = int(np.argmax(np.abs(x[i])))
+            assert abs(abs(dec[i, j]) - abs(x[i, j])) <= abs(x[i, j]) * 1e-6
+
