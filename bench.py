@@ -616,6 +616,12 @@ def bench_rows(dev, flush, peak, only=None):
         out.append(_entry("N4", w.name,
                           "dsa_sparse_decode_attn_kv8 (8-bit pages, persistent split-K)", ms,
                           sel * w.page_size * 264 + q.numel() * 2 + q.numel() * 4, peak, pages=sel))
+        # attention over KV4 pages (4-bit codes + fp32 row scales: 136 B per token per KV head)
+        dec.use_kv4()
+        ms = _time_call((lambda: dec.attend(q)), flush)
+        out.append(_entry("N5", w.name,
+                          "dsa_sparse_decode_attn_kv4 (4-bit pages, persistent split-K)", ms,
+                          sel * w.page_size * 136 + q.numel() * 2 + q.numel() * 4, peak, pages=sel))
         del dec, cache, inp
         torch.cuda.empty_cache()
 

@@ -83,6 +83,11 @@ _SIGNATURES = {
     "dsa_sparse_decode_attn_kv8": ([_P, _P, _P, _P, _I, _P, c_float, _P, _P, _P, _P, c_size_t,
                                     _P], _I),
     "dsa_sparse_decode_attn_kv8_workspace_size": ([_P, _I], c_size_t),
+    "dsa_quantize_kv4": ([_P, _P, _P], _I),
+    "dsa_kv4_bytes": ([_P], c_size_t),
+    "dsa_sparse_decode_attn_kv4": ([_P, _P, _P, _P, _I, _P, c_float, _P, _P, _P, _P, c_size_t,
+                                    _P], _I),
+    "dsa_sparse_decode_attn_kv4_workspace_size": ([_P, _I], c_size_t),
     "dsa_ema_predict_update": ([_P, _I, _I, _I, _P, _P, _I, c_float, c_float, c_float, _P, _I,
                                 _P, _I, _P, _P], _I),
     "dsa_merge_partials": ([_P, _I, _I, _I, _I, _P, _P, _P, _P], _I),
@@ -315,6 +320,48 @@ def dsa_sparse_decode_attn_kv8(kv: PagedKV, kv8, q, idx, count, scale: float, ou
     ws_bytes = workspace.numel() * workspace.element_size()
     _check("dsa_sparse_decode_attn_kv8", load().dsa_sparse_decode_attn_kv8(
         ctypes.byref(kv), _ptr(kv8), _ptr(q), _ptr(idx), idx.shape[-1], _ptr(count), scale,
+        _ptr(out), _ptr(m), _ptr(l), _ptr(workspace), ws_bytes, _stream(stream)))
+
+
+def dsa_kv4_bytes(kv: PagedKV) -> int:
+    return int(load().dsa_kv4_bytes(ctypes.byref(kv)))
+
+
+def dsa_quantize_kv4(kv: PagedKV, kv4, stream=None):
+    """bf16 pools -> KV4 blocks (uint8 tensor of dsa_kv4_bytes(kv) bytes): per (physical page, KV
+    head) the K code rows [p][64], V code rows [p][64] (offset-8 nibbles, two dims per byte; row
+    of slot r stored at r ^ ((r >> 1) & 1)), K scales fp32 [p], V scales fp32 [p];
+    ``kv4_unpack`` takes them apart."""
+    _check("dsa_quantize_kv4", load().dsa_quantize_kv4(ctypes.byref(kv), _ptr(kv4),
+                                                       _stream(stream)))
+
+
+def kv4_unpack(kv4, num_phys_pages: int, num_kv_heads: int, page: int):
+    """The parts of a KV4 buffer: (K rows, V rows) uint8 ``[P][Hkv][p][64]`` in token order (packed
+    nibbles as stored) and (K scales, V scales) fp32 ``[P][Hkv][p]``."""
+    blk = kv4.view(num_phys_pages, num_kv_heads, 136 * page)
+    r = torch.arange(page, device=kv4.device)
+    perm = r ^ ((r >> 1) & 1)  # its own inverse
+
+    def rows(part):
+        return part.reshape(num_phys_pages, num_kv_heads, page, 64)[:, :, perm, :]
+
+    kc = rows(blk[..., :64 * page])
+    vc = rows(blk[..., 64 * page:128 * page])
+    ks = blk[..., 128 * page:132 * page].contiguous().view(torch.float32)
+    vs = blk[..., 132 * page:].contiguous().view(torch.float32)
+    return kc, vc, ks, vs
+
+
+def dsa_sparse_decode_attn_kv4_workspace_size(kv: PagedKV, idx_stride: int) -> int:
+    return int(load().dsa_sparse_decode_attn_kv4_workspace_size(ctypes.byref(kv), idx_stride))
+
+
+def dsa_sparse_decode_attn_kv4(kv: PagedKV, kv4, q, idx, count, scale: float, out, m, l,
+                               workspace, stream=None):
+    ws_bytes = workspace.numel() * workspace.element_size()
+    _check("dsa_sparse_decode_attn_kv4", load().dsa_sparse_decode_attn_kv4(
+        ctypes.byref(kv), _ptr(kv4), _ptr(q), _ptr(idx), idx.shape[-1], _ptr(count), scale,
         _ptr(out), _ptr(m), _ptr(l), _ptr(workspace), ws_bytes, _stream(stream)))
 
 

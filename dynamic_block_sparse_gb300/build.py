@@ -24,7 +24,7 @@ LIB_PATH = os.path.join(HERE, "libdsa.so")
 TRACE_BUILD_DIR = os.path.join(HERE, "_build_trace")
 TRACE_LIB_PATH = os.path.join(HERE, "libdsa_trace.so")
 
-SOURCES = ["api.cu", "attn.cu", "calib.cu", "kv8.cu", "meta_score.cu", "prr_step.cu",
+SOURCES = ["api.cu", "attn.cu", "calib.cu", "kvquant.cu", "meta_score.cu", "prr_step.cu",
            "select.cu", "stream_attn.cu", "threshold.cu"]
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
 FLAGS = ["-O3", "-lineinfo", "-std=c++17", "-Xcompiler", "-fPIC", "-Xcompiler", "-O3",

@@ -395,9 +395,8 @@ int dsa_hybrid_decode_attn(const dsa_paged_kv* kv, const void* q, const int32_t*
   sa.sink = sink_tokens;
   sa.local = local_tokens;
   sa.stream_stride = v.streaming != nullptr ? static_cast<int>(sslots) : 0;
-  cudaError_t e = cudaMemsetAsync(sa.counters, 0, static_cast<size_t>(rows) * sizeof(int32_t), s);
-  if (e != cudaSuccess) return cuda_fail(e, "dsa_hybrid_decode_attn counter reset");
-  e = launch_stream_attn(tk, tv, sa, grid, s);
+  // the row tickets are zero on entry (zero-filled workspace, left zero by every completed call)
+  const cudaError_t e = launch_stream_attn(tk, tv, sa, grid, s);
   return e == cudaSuccess ? ok() : cuda_fail(e, "dsa_hybrid_decode_attn launch");
 }
 
@@ -480,8 +479,7 @@ int dsa_sparse_decode_attn(const dsa_paged_kv* kv, const void* q, const int32_t*
     sa.out = out;
     sa.m = m;
     sa.l = l;
-    e = cudaMemsetAsync(sa.counters, 0, static_cast<size_t>(rows) * sizeof(int32_t), s);
-    if (e != cudaSuccess) return cuda_fail(e, "dsa_sparse_decode_attn counter reset");
+    // the row tickets are zero on entry (zero-filled workspace, left zero by every completed call)
     e = launch_stream_attn(tk, tv, sa, grid, s);
     return e == cudaSuccess ? ok() : cuda_fail(e, "dsa_sparse_decode_attn launch");
   }
@@ -643,46 +641,47 @@ int dsa_ema_predict_update(const float* IS, int32_t rows, int32_t n, int32_t str
   return e == cudaSuccess ? ok() : cuda_fail(e, "dsa_ema_predict_update launch");
 }
 
-int dsa_quantize_kv8(const dsa_paged_kv* kv, void* kv8, dsa_stream_t stream) {
+}  // extern "C"
+
+namespace {
+
+// Both quantisers: every K row, then every V row of the pool into its block.
+int quantize_pool(const dsa_paged_kv* kv, void* dst, int qbits, dsa_stream_t stream,
+                  const char* name) {
   KvView v;
   int rc = check_kv(kv, 2, &v);
   if (rc) return rc;
-  if (!kv8) return fail(DSA_ERR_INVALID_ARG, "kv8 is NULL");
-  if (!aligned(kv8, 16)) return fail(DSA_ERR_ALIGNMENT, "kv8 must be 16-byte aligned");
+  if (!dst) return fail(DSA_ERR_INVALID_ARG, "%s: the block buffer is NULL", name);
+  if (!aligned(dst, 16)) return fail(DSA_ERR_ALIGNMENT, "%s: blocks must be 16-byte aligned", name);
   const long long n_rows = static_cast<long long>(v.num_phys) * v.Hkv * v.p;
   cudaStream_t s = static_cast<cudaStream_t>(stream);
-  cudaError_t e = launch_quantize_kv8(static_cast<const __nv_bfloat16*>(kv->k_pages), n_rows, v.p,
-                                      0, static_cast<uint8_t*>(kv8), s);
+  auto launch = qbits == 8 ? launch_quantize_kv8 : launch_quantize_kv4;
+  cudaError_t e = launch(static_cast<const __nv_bfloat16*>(kv->k_pages), n_rows, v.p, 0,
+                         static_cast<uint8_t*>(dst), s);
   if (e == cudaSuccess)
-    e = launch_quantize_kv8(static_cast<const __nv_bfloat16*>(kv->v_pages), n_rows, v.p, 1,
-                            static_cast<uint8_t*>(kv8), s);
-  return e == cudaSuccess ? ok() : cuda_fail(e, "dsa_quantize_kv8 launch");
+    e = launch(static_cast<const __nv_bfloat16*>(kv->v_pages), n_rows, v.p, 1,
+               static_cast<uint8_t*>(dst), s);
+  return e == cudaSuccess ? ok() : cuda_fail(e, name);
 }
 
-size_t dsa_kv8_bytes(const dsa_paged_kv* kv) {
+size_t pool_block_bytes(const dsa_paged_kv* kv, int per_token) {
   if (!kv || kv->num_phys_pages <= 0 || kv->num_kv_heads <= 0 || kv->page_size <= 0) return 0;
-  return static_cast<size_t>(kv->num_phys_pages) * kv->num_kv_heads * kv->page_size * 264;
+  return static_cast<size_t>(kv->num_phys_pages) * kv->num_kv_heads * kv->page_size * per_token;
 }
 
-size_t dsa_sparse_decode_attn_kv8_workspace_size(const dsa_paged_kv* kv, int32_t idx_stride) {
-  if (!kv || kv->num_kv_heads <= 0 || kv->batch <= 0 || idx_stride <= 0) return 0;
-  const int rows = kv->batch * kv->num_kv_heads;
-  const int G = kv->num_q_heads / kv->num_kv_heads;
-  return stream_workspace_bytes(rows, stream_attn_grid(), G);
-}
-
-int dsa_sparse_decode_attn_kv8(const dsa_paged_kv* kv, const void* kv8, const void* q,
-                               const int32_t* idx, int32_t idx_stride, const int32_t* count,
-                               float scale, float* out, float* m, float* l, void* workspace,
-                               size_t workspace_bytes, dsa_stream_t stream) {
+// The persistent attention over quantised blocks (KV8 or KV4).
+int quantized_attn(const dsa_paged_kv* kv, const void* blocks, int qbits, const void* q,
+                   const int32_t* idx, int32_t idx_stride, const int32_t* count, float scale,
+                   float* out, float* m, float* l, void* workspace, size_t workspace_bytes,
+                   dsa_stream_t stream, const char* name) {
   KvView v;
   int rc = check_kv(kv, 0, &v);
   if (rc) return rc;
-  if (!kv8 || !q || !idx || !count || !out || !m || !l)
-    return fail(DSA_ERR_INVALID_ARG, "a required pointer is NULL");
+  if (!blocks || !q || !idx || !count || !out || !m || !l)
+    return fail(DSA_ERR_INVALID_ARG, "%s: a required pointer is NULL", name);
   if (idx_stride < 1) return fail(DSA_ERR_INVALID_ARG, "idx_stride < 1");
-  if (!aligned(kv8, 16) || !aligned(q, 16) || !aligned(out, 16))
-    return fail(DSA_ERR_ALIGNMENT, "kv8, q and out must be 16-byte aligned");
+  if (!aligned(blocks, 16) || !aligned(q, 16) || !aligned(out, 16))
+    return fail(DSA_ERR_ALIGNMENT, "%s: blocks, q and out must be 16-byte aligned", name);
   if (v.Hkv > 1024) return fail(DSA_ERR_UNSUPPORTED, "more than 1024 KV heads");
   const int rows = v.B * v.Hkv;
   const int grid = stream_attn_grid();
@@ -691,15 +690,15 @@ int dsa_sparse_decode_attn_kv8(const dsa_paged_kv* kv, const void* kv8, const vo
   if (!workspace || workspace_bytes < need)
     return fail(DSA_ERR_WORKSPACE, "workspace of %zu bytes needed", need);
   if (!aligned(workspace, 16)) return fail(DSA_ERR_ALIGNMENT, "workspace must be 16-byte aligned");
-  // as many stages (of 264 B per token) as fit, up to 128 KB of them (the bf16 path's budget)
+  // as many stages (one page block each) as fit, up to 128 KB of them (the bf16 path's budget)
   const size_t smem_cap = 227 * 1024;
-  const int stride = (264 * v.p + 1023) & ~1023;
+  const int per_token = qbits == 8 ? 264 : 136;
+  const int stride = (per_token * v.p + 1023) & ~1023;
   int stages = 131072 / stride;
   if (stages > kStreamMaxStages) stages = kStreamMaxStages;
-  while (stages > 1 && stream_attn_smem_bytes(v.p, stages, v.G, true) > smem_cap) --stages;
-  if (stages < 1 || stream_attn_smem_bytes(v.p, stages, v.G, true) > smem_cap)
-    return fail(DSA_ERR_UNSUPPORTED, "dsa_sparse_decode_attn_kv8: shape needs too much shared memory");
-  cudaStream_t s = static_cast<cudaStream_t>(stream);
+  while (stages > 1 && stream_attn_smem_bytes(v.p, stages, v.G, qbits) > smem_cap) --stages;
+  if (stages < 1 || stream_attn_smem_bytes(v.p, stages, v.G, qbits) > smem_cap)
+    return fail(DSA_ERR_UNSUPPORTED, "%s: shape needs too much shared memory", name);
   StreamAttnArgs sa = {};
   sa.kv = v;
   sa.q = static_cast<const __nv_bfloat16*>(q);
@@ -713,12 +712,59 @@ int dsa_sparse_decode_attn_kv8(const dsa_paged_kv* kv, const void* kv8, const vo
   sa.out = out;
   sa.m = m;
   sa.l = l;
-  sa.kv8 = static_cast<const uint8_t*>(kv8);
-  cudaError_t e = cudaMemsetAsync(sa.counters, 0, static_cast<size_t>(rows) * sizeof(int32_t), s);
-  if (e != cudaSuccess) return cuda_fail(e, "dsa_sparse_decode_attn_kv8 counter reset");
-  CUtensorMap none = {};  // KV8 pages move by plain bulk copies: no tensor maps
-  e = launch_stream_attn(none, none, sa, grid, s);
-  return e == cudaSuccess ? ok() : cuda_fail(e, "dsa_sparse_decode_attn_kv8 launch");
+  sa.qkv = static_cast<const uint8_t*>(blocks);
+  sa.qbits = qbits;
+  // the row tickets are zero on entry (zero-filled workspace, left zero by every completed call)
+  CUtensorMap none = {};  // quantised pages move by plain bulk copies: no tensor maps
+  const cudaError_t e = launch_stream_attn(none, none, sa, grid, static_cast<cudaStream_t>(stream));
+  return e == cudaSuccess ? ok() : cuda_fail(e, name);
+}
+
+size_t quantized_attn_workspace(const dsa_paged_kv* kv, int32_t idx_stride) {
+  if (!kv || kv->num_kv_heads <= 0 || kv->batch <= 0 || idx_stride <= 0) return 0;
+  const int rows = kv->batch * kv->num_kv_heads;
+  const int G = kv->num_q_heads / kv->num_kv_heads;
+  return stream_workspace_bytes(rows, stream_attn_grid(), G);
+}
+
+}  // namespace
+
+extern "C" {
+
+int dsa_quantize_kv8(const dsa_paged_kv* kv, void* kv8, dsa_stream_t stream) {
+  return quantize_pool(kv, kv8, 8, stream, "dsa_quantize_kv8");
+}
+
+size_t dsa_kv8_bytes(const dsa_paged_kv* kv) { return pool_block_bytes(kv, 264); }
+
+size_t dsa_sparse_decode_attn_kv8_workspace_size(const dsa_paged_kv* kv, int32_t idx_stride) {
+  return quantized_attn_workspace(kv, idx_stride);
+}
+
+int dsa_sparse_decode_attn_kv8(const dsa_paged_kv* kv, const void* kv8, const void* q,
+                               const int32_t* idx, int32_t idx_stride, const int32_t* count,
+                               float scale, float* out, float* m, float* l, void* workspace,
+                               size_t workspace_bytes, dsa_stream_t stream) {
+  return quantized_attn(kv, kv8, 8, q, idx, idx_stride, count, scale, out, m, l, workspace,
+                        workspace_bytes, stream, "dsa_sparse_decode_attn_kv8");
+}
+
+int dsa_quantize_kv4(const dsa_paged_kv* kv, void* kv4, dsa_stream_t stream) {
+  return quantize_pool(kv, kv4, 4, stream, "dsa_quantize_kv4");
+}
+
+size_t dsa_kv4_bytes(const dsa_paged_kv* kv) { return pool_block_bytes(kv, 136); }
+
+size_t dsa_sparse_decode_attn_kv4_workspace_size(const dsa_paged_kv* kv, int32_t idx_stride) {
+  return quantized_attn_workspace(kv, idx_stride);
+}
+
+int dsa_sparse_decode_attn_kv4(const dsa_paged_kv* kv, const void* kv4, const void* q,
+                               const int32_t* idx, int32_t idx_stride, const int32_t* count,
+                               float scale, float* out, float* m, float* l, void* workspace,
+                               size_t workspace_bytes, dsa_stream_t stream) {
+  return quantized_attn(kv, kv4, 4, q, idx, idx_stride, count, scale, out, m, l, workspace,
+                        workspace_bytes, stream, "dsa_sparse_decode_attn_kv4");
 }
 
 size_t dsa_calibrate_ema_workspace_size(int32_t steps, int32_t rows, int32_t n, int32_t k) {

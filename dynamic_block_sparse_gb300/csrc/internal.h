@@ -134,12 +134,14 @@ struct StreamAttnArgs {
   // streaming heads in the same launch: their sink + local tokens as extra units of
   // stream_stride slots each (0: streaming heads are skipped)
   int sink, local, stream_stride;
-  // KV8 pages instead of the bf16 pools (non-null): one 264 p-byte block per (page, KV head)
-  const uint8_t* kv8;
+  // quantised pages instead of the bf16 pools (non-null): one block per (page, KV head) of
+  // 264 p bytes (qbits 8, KV8) or 136 p bytes (qbits 4, KV4)
+  const uint8_t* qkv;
+  int qbits;
 };
 constexpr int kStreamMaxStages = 16;
 constexpr int kStreamMaxGrid = 512;  // bounds the row merge's [G][parts] weights in shared memory
-size_t stream_attn_smem_bytes(int page, int stages, int G, bool kv8 = false);
+size_t stream_attn_smem_bytes(int page, int stages, int G, int qbits = 0);  // qbits 0: bf16
 int stream_attn_grid();  // CTAs of one launch: one per SM
 cudaError_t launch_stream_attn(const CUtensorMap& tmK, const CUtensorMap& tmV,
                                const StreamAttnArgs& a, int grid, cudaStream_t s);
@@ -200,9 +202,12 @@ cudaError_t launch_ema(const float* IS, int rows, int n, int stride, float* ell,
                        int32_t* pred_idx, int pred_idx_stride, int32_t* pred_count,
                        cudaStream_t s);
 
-// KV8 pages (csrc/kv8.cu): e4m3 K and V with an fp32 scale per (page, KV head, token) row
+// Quantised KV pages (kvquant.cu): KV8 (e4m3) or KV4 (4-bit integer) codes of K and V with an
+// fp32 scale per (page, KV head, token) row
 cudaError_t launch_quantize_kv8(const __nv_bfloat16* src, long long n_rows, int page, int v,
                                 uint8_t* kv8, cudaStream_t s);
+cudaError_t launch_quantize_kv4(const __nv_bfloat16* src, long long n_rows, int page, int v,
+                                uint8_t* kv4, cudaStream_t s);
 
 // PRR §3.2 calibration of the EMA predictor over its 80-point grid (csrc/calib.cu)
 constexpr int kCalibPoints = 80;

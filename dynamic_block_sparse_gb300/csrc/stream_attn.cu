@@ -45,9 +45,17 @@ struct SLayout {
 // mailbox's [2] full and [2] empty.
 // kv8: a stage holds a KV8 page block (e4m3 K rows, V rows, then the two fp32 scale rows); the
 // consumers read the codes straight into tensor-core operands (no decoded copy in shared memory).
-__host__ __device__ inline SLayout slayout(int page, int stages, int G, bool kv8 = false) {
+// Page formats of the stream: bf16 pools (tensor-map loads) or quantised blocks (one bulk copy per
+// page block): KV8 (264 bytes per token) and KV4 (136 bytes per token).
+enum : int { kFmtBf16 = 0, kFmtKv8 = 8, kFmtKv4 = 4 };
+__host__ __device__ constexpr uint32_t block_bytes_per_token(int fmt) {
+  return fmt == kFmtKv8 ? 264u : fmt == kFmtKv4 ? 136u : 512u;
+}
+
+__host__ __device__ inline SLayout slayout(int page, int stages, int G, int fmt = kFmtBf16) {
   SLayout L;
-  L.stage_stride = kv8 ? (264u * page + 1023u) & ~1023u : 512u * page;
+  L.stage_stride = fmt == kFmtBf16 ? 512u * page
+                                   : (block_bytes_per_token(fmt) * page + 1023u) & ~1023u;
   L.merge_off = ((L.stage_stride * stages) + 1023u) & ~1023u;
   L.q_off = L.merge_off + static_cast<uint32_t>(kSW * G * (kHeadDim + 2) * 4 + 127) / 128 * 128;
   L.bar_off = L.q_off + 2u * 16u * kHeadDim * 2u;
@@ -132,12 +140,90 @@ DSA_DEV void tile_scores_kv8(const uint32_t (&qa)[8][4], const uint8_t* kc, floa
     for (int e = 0; e < 4; ++e) sc[nt][e] = acc[0][nt][e] + acc[1][nt][e];
 }
 
+// ---- KV4 tiles.  A code is a nibble u (value u - 8); f16(1024 + u) - 1032 is that value exactly,
+// so two nibbles placed in the mantissas of a 0x6400 pair and shifted down by one packed f16
+// subtraction give an f16 operand pair.  The same dim permutations as the KV8 tiles; the 64-byte
+// code row of token r sits at row r ^ ((r >> 1) & 1) of its tile (r mod 4 is the same in both).
+
+DSA_DEV int kv4_row(int r) { return r ^ ((r >> 1) & 1); }
+
+// f16 pair (lo, hi) = (nibble of `w` at bit `a` - 8, nibble at bit `b` - 8)
+DSA_DEV uint32_t kv4_pair(uint32_t w, int a, int b) {
+  const uint32_t bits = ((w >> a) & 0xfu) | (((w >> b) & 0xfu) << 16) | 0x64006400u;
+  const uint32_t off = 0x64086408u;  // (1032, 1032)
+  const __half2 h = __hsub2(*reinterpret_cast<const __half2*>(&bits),
+                            *reinterpret_cast<const __half2*>(&off));
+  return *reinterpret_cast<const uint32_t*>(&h);
+}
+
+// S = Q . codes^T for the 16 code rows at kc (the tile's rows of a KV4 page block).  Lane column
+// tig reads dims 32 tig .. +31 of its token: 16 bytes, k-step ks taking the nibbles of dims
+// 32 tig + 4 ks .. +3 (one 16-bit half of word ks / 2).
+DSA_DEV void tile_scores_kv4(const uint32_t (&qa)[8][4], const uint8_t* kc, float (&sc)[2][4]) {
+  const int lane = threadIdx.x & 31;
+  const int g = lane >> 2, tig = lane & 3;
+  float acc[2][2][4];
+#pragma unroll
+  for (int c = 0; c < 2; ++c)
+#pragma unroll
+    for (int nt = 0; nt < 2; ++nt)
+#pragma unroll
+      for (int e = 0; e < 4; ++e) acc[c][nt][e] = 0.f;
+#pragma unroll
+  for (int nt = 0; nt < 2; ++nt) {
+    const uint4 w4 = *reinterpret_cast<const uint4*>(kc + kv4_row(nt * 8 + g) * 64 + 16 * tig);
+    const uint32_t w[4] = {w4.x, w4.y, w4.z, w4.w};
+#pragma unroll
+    for (int ks = 0; ks < 8; ++ks) {
+      const int h = 16 * (ks & 1);
+      mma_f16(acc[ks & 1][nt], qa[ks], kv4_pair(w[ks >> 1], h, h + 4),
+              kv4_pair(w[ks >> 1], h + 8, h + 12));
+    }
+  }
+#pragma unroll
+  for (int nt = 0; nt < 2; ++nt)
+#pragma unroll
+    for (int e = 0; e < 4; ++e) sc[nt][e] = acc[0][nt][e] + acc[1][nt][e];
+}
+
+// O += (P * s_V) . codes_V for the tile's V code rows at vc (pa: the P fragment, already scaled).
+// n-tile j, column c holds dim 16 c + j (the KV8 output permutation): lane g reads dims 16 g ..
+// + 15 (8 bytes) of tokens 2 tig, 2 tig + 1, 2 tig + 8, 2 tig + 9.
+DSA_DEV void tile_pv_kv4(WarpSoftmaxState& st, const uint32_t (&pa)[4], const uint8_t* vc) {
+  const int lane = threadIdx.x & 31;
+  const int g = lane >> 2, tig = lane & 3;
+  uint2 rv[4];
+#pragma unroll
+  for (int i = 0; i < 4; ++i) {
+    const int r = 2 * tig + (i & 1) + (i >> 1) * 8;
+    rv[i] = *reinterpret_cast<const uint2*>(vc + kv4_row(r) * 64 + 8 * g);
+  }
+#pragma unroll
+  for (int half = 0; half < 2; ++half) {  // dims 16 g + 8 half .. + 7
+    const uint32_t w0 = half ? rv[0].y : rv[0].x, w1 = half ? rv[1].y : rv[1].x;
+    const uint32_t w2 = half ? rv[2].y : rv[2].x, w3 = half ? rv[3].y : rv[3].x;
+#pragma unroll
+    for (int quad = 0; quad < 2; ++quad) {  // dims + 4 quad .. + 3: bytes 2 quad, 2 quad + 1
+      // rows (2 tig, 2 tig + 1) and (2 tig + 8, 2 tig + 9) side by side, 16 bits each
+      const uint32_t sel = quad ? 0x7632u : 0x5410u;
+      const uint32_t x01 = __byte_perm(w0, w1, sel), x23 = __byte_perm(w2, w3, sel);
+#pragma unroll
+      for (int n = 0; n < 4; ++n) {
+        const int j = 8 * half + 4 * quad + n;
+        mma_f16(st.o[j], pa, kv4_pair(x01, 4 * n, 16 + 4 * n), kv4_pair(x23, 4 * n, 16 + 4 * n));
+      }
+    }
+  }
+}
+
 // Online-softmax update with the tile's logits (q . codes in sc; ks / vs: the 16 tokens' K and V
-// scales), then O += (P * s_V) . codes_V.  The output dims are permuted: n-tile j, column c holds
-// dim 16 c + j, so that a lane's V operand is one 16-byte piece of each of its four code rows.
-DSA_DEV void tile_softmax_pv_kv8(WarpSoftmaxState& st, float (&sc)[2][4], float scale_log2,
-                                 uint32_t valid, const uint8_t* vc, const float* ks,
-                                 const float* vs) {
+// scales), then O += (P * s_V) . codes_V over KV8 (FMT 8) or KV4 (FMT 4) code rows at vc.  The
+// output dims are permuted: n-tile j, column c holds dim 16 c + j, so that a lane's V operand is
+// one piece of each of its four code rows (16 bytes of KV8, 8 bytes of KV4).
+template <int FMT>
+DSA_DEV void tile_softmax_pv_q(WarpSoftmaxState& st, float (&sc)[2][4], float scale_log2,
+                               uint32_t valid, const uint8_t* vc, const float* ks,
+                               const float* vs) {
   const int lane = threadIdx.x & 31;
   const int g = lane >> 2, tig = lane & 3;
   const float2 k0 = *reinterpret_cast<const float2*>(ks + 2 * tig);
@@ -203,28 +289,32 @@ DSA_DEV void tile_softmax_pv_kv8(WarpSoftmaxState& st, float (&sc)[2][4], float 
   pa[1] = pack_f16(pv[0][2], pv[0][3]);
   pa[2] = pack_f16(pv[1][0], pv[1][1]);
   pa[3] = pack_f16(pv[1][2], pv[1][3]);
-  // V operand of n-tile j: tokens 2 tig, 2 tig + 1 (b0) and 2 tig + 8, + 9 (b1) at dim 16 g + j:
-  // byte j of the 16-byte piece g of those four code rows (zeros for tokens that take no part,
-  // so that stale codes never meet a zero probability)
-  uint4 rv[4];
+  if constexpr (FMT == 4) {  // (a nibble always decodes to a finite value: nothing to clear)
+    tile_pv_kv4(st, pa, vc);
+  } else {
+    // V operand of n-tile j: tokens 2 tig, 2 tig + 1 (b0) and 2 tig + 8, + 9 (b1) at dim 16 g + j:
+    // byte j of the 16-byte piece g of those four code rows (zeros for tokens that take no part,
+    // so that stale codes never meet a zero probability)
+    uint4 rv[4];
 #pragma unroll
-  for (int i = 0; i < 4; ++i) {
-    const int r = 2 * tig + (i & 1) + (i >> 1) * 8;
-    rv[i] = *reinterpret_cast<const uint4*>(vc + r * 128 + ((g ^ (r & 7)) << 4));
-    if (!((valid >> r) & 1u)) rv[i] = make_uint4(0u, 0u, 0u, 0u);
-  }
-  const uint32_t* w0 = reinterpret_cast<const uint32_t*>(&rv[0]);
-  const uint32_t* w1 = reinterpret_cast<const uint32_t*>(&rv[1]);
-  const uint32_t* w2 = reinterpret_cast<const uint32_t*>(&rv[2]);
-  const uint32_t* w3 = reinterpret_cast<const uint32_t*>(&rv[3]);
+    for (int i = 0; i < 4; ++i) {
+      const int r = 2 * tig + (i & 1) + (i >> 1) * 8;
+      rv[i] = *reinterpret_cast<const uint4*>(vc + r * 128 + ((g ^ (r & 7)) << 4));
+      if (!((valid >> r) & 1u)) rv[i] = make_uint4(0u, 0u, 0u, 0u);
+    }
+    const uint32_t* w0 = reinterpret_cast<const uint32_t*>(&rv[0]);
+    const uint32_t* w1 = reinterpret_cast<const uint32_t*>(&rv[1]);
+    const uint32_t* w2 = reinterpret_cast<const uint32_t*>(&rv[2]);
+    const uint32_t* w3 = reinterpret_cast<const uint32_t*>(&rv[3]);
 #pragma unroll
-  for (int q = 0; q < 4; ++q) {  // dims 16 g + 4 q .. + 3
-    const uint32_t a01 = __byte_perm(w0[q], w1[q], 0x5140), b01 = __byte_perm(w0[q], w1[q], 0x7362);
-    const uint32_t a23 = __byte_perm(w2[q], w3[q], 0x5140), b23 = __byte_perm(w2[q], w3[q], 0x7362);
-    mma_f16(st.o[4 * q], pa, e4m3x2_f16x2(a01), e4m3x2_f16x2(a23));
-    mma_f16(st.o[4 * q + 1], pa, e4m3x2_f16x2(a01 >> 16), e4m3x2_f16x2(a23 >> 16));
-    mma_f16(st.o[4 * q + 2], pa, e4m3x2_f16x2(b01), e4m3x2_f16x2(b23));
-    mma_f16(st.o[4 * q + 3], pa, e4m3x2_f16x2(b01 >> 16), e4m3x2_f16x2(b23 >> 16));
+    for (int q = 0; q < 4; ++q) {  // dims 16 g + 4 q .. + 3
+      const uint32_t a01 = __byte_perm(w0[q], w1[q], 0x5140), b01 = __byte_perm(w0[q], w1[q], 0x7362);
+      const uint32_t a23 = __byte_perm(w2[q], w3[q], 0x5140), b23 = __byte_perm(w2[q], w3[q], 0x7362);
+      mma_f16(st.o[4 * q], pa, e4m3x2_f16x2(a01), e4m3x2_f16x2(a23));
+      mma_f16(st.o[4 * q + 1], pa, e4m3x2_f16x2(a01 >> 16), e4m3x2_f16x2(a23 >> 16));
+      mma_f16(st.o[4 * q + 2], pa, e4m3x2_f16x2(b01), e4m3x2_f16x2(b23));
+      mma_f16(st.o[4 * q + 3], pa, e4m3x2_f16x2(b01 >> 16), e4m3x2_f16x2(b23 >> 16));
+    }
   }
 }
 
@@ -276,7 +366,7 @@ DSA_DEV int ticket_add(int32_t* p) {
 
 // STREAMING: the launch also serves the streaming heads (a second region of the slot space);
 // without it every streaming-specific path compiles away.
-template <bool STREAMING, bool KV8>
+template <bool STREAMING, int FMT>
 __global__ void __launch_bounds__(kSThreads, 1)
     stream_attn_kernel(const __grid_constant__ CUtensorMap tmK,
                        const __grid_constant__ CUtensorMap tmV, const StreamAttnArgs a) {
@@ -289,7 +379,9 @@ __global__ void __launch_bounds__(kSThreads, 1)
   const int S = a.stages;
   const int G = kv.G;
   const int tiles = page / 16;
-  const SLayout lay = slayout(page, S, G, KV8);
+  constexpr bool KV8 = FMT == kFmtKv8, KV4 = FMT == kFmtKv4, QNT = KV8 || KV4;
+  constexpr uint32_t kBpt = block_bytes_per_token(FMT);  // bytes a page brings per token
+  const SLayout lay = slayout(page, S, G, FMT);
   float* sO = reinterpret_cast<float*>(smem + lay.merge_off);  // [kSW][G][128]
   float* sM = sO + kSW * G * kHeadDim;                          // [kSW][G]
   float* sL = sM + kSW * G;                                     // [kSW][G]
@@ -311,7 +403,7 @@ __global__ void __launch_bounds__(kSThreads, 1)
   int* stream_heads = misc + 64 + kSMaxHeads;  // [.., + Hkv) when streaming units are on
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
   const uint32_t stage_bytes = lay.stage_stride;           // stage s at smem + s * stage_bytes
-  const uint32_t stage_tx = KV8 ? 264u * page : 512u * page;  // bytes a stage's loads bring
+  const uint32_t stage_tx = kBpt * page;  // bytes a stage's loads bring
   const uint32_t smem_base = smem_u32(smem);
 #ifdef DSA_TIMELINE
   __shared__ unsigned long long s_trace_[2 * kTraceSlots];
@@ -332,7 +424,7 @@ __global__ void __launch_bounds__(kSThreads, 1)
       misc[0] = 0;
       misc[3] = 0;
       misc[4] = 0;
-      if (!KV8) {
+      if (!QNT) {
         prefetch_tensormap(&tmK);
         prefetch_tensormap(&tmV);
       }
@@ -469,7 +561,7 @@ __global__ void __launch_bounds__(kSThreads, 1)
       if (in && !ok) raise_status(kv.status, DSA_STATUS_BAD_PAGE);
       DSA_STAMP_DIRECT(g_trace_stream, 12, kSW * 32 + (raw == -12345));
       // issue: lane 2q (K) and lane 2q + 1 (V) take page q, so that the copies go out page by
-      // page (F <= kStreamMaxStages = 16 pages; a KV8 page is one copy, from lane 2q)
+      // page (F <= kStreamMaxStages = 16 pages; a quantised page block is one copy, from lane 2q)
       const int q = lane >> 1;
       const int pos_q = __shfl_sync(0xffffffffu, pos, q);
       const int raw_q = __shfl_sync(0xffffffffu, raw, q);
@@ -485,11 +577,11 @@ __global__ void __launch_bounds__(kSThreads, 1)
             mbar_arrive(full);  // nothing to load: complete the phase with a plain arrival
           } else {
             mbar_arrive_expect_tx(full, stage_tx);
-            if (KV8) bulk_load(dst, a.kv8 + static_cast<size_t>(rowk) * 264, 264u * page, full);
+            if (QNT) bulk_load(dst, a.qkv + static_cast<size_t>(rowk) * kBpt, kBpt * page, full);
           }
         }
         __syncwarp(0xffffffffu >> (32 - 2 * F));  // the byte count is posted before any copy lands
-        if (!KV8 && ok_q) {
+        if (!QNT && ok_q) {
           if ((lane & 1) == 0)
             tma_load_page(dst, &tmK, rowk, full);
           else
@@ -648,8 +740,8 @@ __global__ void __launch_bounds__(kSThreads, 1)
               const uint32_t dst = smem_base + s * stage_bytes;
               const int row0 = (phk * kv.Hkv + h) * page;
               mbar_arrive_expect_tx(full, stage_tx);
-              if (KV8) {  // the page's block (K and V codes, their scales): one bulk copy
-                bulk_load(dst, a.kv8 + static_cast<size_t>(row0) * 264, 264u * page, full);
+              if (QNT) {  // the page's block (K and V codes, their scales): one bulk copy
+                bulk_load(dst, a.qkv + static_cast<size_t>(row0) * kBpt, kBpt * page, full);
               } else {
                 tma_load_page(dst, &tmK, row0, full);
                 tma_load_page(dst + 2 * page * 128, &tmV, row0, full);
@@ -722,7 +814,7 @@ __global__ void __launch_bounds__(kSThreads, 1)
     const int di = d_first + u;
     uint32_t qa[8][4] = {};
     if (!dry) {
-      if (KV8)
+      if (QNT)
         load_q_frags_kv8(sQ + slot * 16 * kHeadDim, qa);
       else
         load_q_frags(sQ + slot * 16 * kHeadDim, qa, kHeadDim);
@@ -763,8 +855,14 @@ __global__ void __launch_bounds__(kSThreads, 1)
           const uint8_t* blk = smem + s * stage_bytes;  // the page's KV8 block
           const float* ksc = reinterpret_cast<const float*>(blk + 256 * page) + t * 16;
           tile_scores_kv8(qa, blk + t * 16 * 128, sc);
-          tile_softmax_pv_kv8(st, sc, a.scale_log2, vm, blk + (page + t * 16) * 128, ksc,
-                              ksc + page);
+          tile_softmax_pv_q<kFmtKv8>(st, sc, a.scale_log2, vm, blk + (page + t * 16) * 128, ksc,
+                                     ksc + page);
+        } else if (KV4) {
+          const uint8_t* blk = smem + s * stage_bytes;  // the page's KV4 block
+          const float* ksc = reinterpret_cast<const float*>(blk + 128 * page) + t * 16;
+          tile_scores_kv4(qa, blk + t * 16 * 64, sc);
+          tile_softmax_pv_q<kFmtKv4>(st, sc, a.scale_log2, vm, blk + (page + t * 16) * 64, ksc,
+                                     ksc + page);
         } else {
           if (vm != 0xffffu)
             wrote |=
@@ -788,7 +886,7 @@ __global__ void __launch_bounds__(kSThreads, 1)
       float* wO = sO + warp * G * kHeadDim;
 #pragma unroll
       for (int j = 0; j < 16; ++j) {
-        if (KV8) {  // column c of n-tile j is dim 16 c + j
+        if (QNT) {  // column c of n-tile j is dim 16 c + j
           if (r0 < G) {
             wO[r0 * kHeadDim + kv8_o_pos(r0, 16 * c0 + j)] = st.o[j][0];
             wO[r0 * kHeadDim + kv8_o_pos(r0, 16 * c0 + 16 + j)] = st.o[j][1];
@@ -855,7 +953,7 @@ __global__ void __launch_bounds__(kSThreads, 1)
     named_barrier(1, kSConsumers);
     for (int e = tid; e < G * kHeadDim; e += kSConsumers) {
       const int g = e >> 7, d = e & 127;
-      const int pos = KV8 ? kv8_o_pos(g, d) : d;
+      const int pos = QNT ? kv8_o_pos(g, d) : d;
       float o = 0.f;
 #pragma unroll
       for (int w = 0; w < kSW; ++w) o += sO[(w * G + g) * kHeadDim + pos] * sM[w * G + g];
@@ -973,8 +1071,8 @@ __global__ void __launch_bounds__(kSThreads, 1)
 
 }  // namespace
 
-size_t stream_attn_smem_bytes(int page, int stages, int G, bool kv8) {
-  return slayout(page, stages, G, kv8).total;
+size_t stream_attn_smem_bytes(int page, int stages, int G, int qbits) {
+  return slayout(page, stages, G, qbits).total;
 }
 
 int stream_attn_grid() {
@@ -987,15 +1085,17 @@ int stream_attn_grid() {
 
 cudaError_t launch_stream_attn(const CUtensorMap& tmK, const CUtensorMap& tmV,
                                const StreamAttnArgs& a, int grid, cudaStream_t s) {
-  const size_t bytes = slayout(a.kv.p, a.stages, a.kv.G, a.kv8 != nullptr).total;
+  const int fmt = a.qkv != nullptr ? a.qbits : kFmtBf16;
+  const size_t bytes = slayout(a.kv.p, a.stages, a.kv.G, fmt).total;
   auto go = [&](auto kernel) -> cudaError_t {
     cudaError_t e = ensure_dynamic_smem(reinterpret_cast<const void*>(kernel), bytes);
     if (e != cudaSuccess) return e;
     return launch_pdl(kernel, grid, kSThreads, bytes, s, tmK, tmV, a);
   };
-  if (a.kv8 != nullptr) return go(stream_attn_kernel<false, true>);
-  return a.stream_stride > 0 ? go(stream_attn_kernel<true, false>)
-                             : go(stream_attn_kernel<false, false>);
+  if (fmt == kFmtKv8) return go(stream_attn_kernel<false, kFmtKv8>);
+  if (fmt == kFmtKv4) return go(stream_attn_kernel<false, kFmtKv4>);
+  return a.stream_stride > 0 ? go(stream_attn_kernel<true, kFmtBf16>)
+                             : go(stream_attn_kernel<false, kFmtBf16>);
 }
 
 }  // namespace dsa

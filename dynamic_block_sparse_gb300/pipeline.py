@@ -68,6 +68,14 @@ class Cache:
         B.dsa_quantize_kv8(self.kv, buf, stream)
         return buf
 
+    def kv4(self, stream=None):
+        """The pools as KV4 blocks (4-bit integer rows with one fp32 scale each, one contiguous
+        block per (physical page, KV head)): a uint8 tensor; ``binding.kv4_unpack`` gives its
+        parts."""
+        buf = torch.empty(B.dsa_kv4_bytes(self.kv), dtype=torch.uint8, device=self.device)
+        B.dsa_quantize_kv4(self.kv, buf, stream)
+        return buf
+
     def meta_buffer(self, kind: int, logical_page: int) -> torch.Tensor:
         g = self.page_size // logical_page
         if kind == B.DSA_META_MINMAX:
@@ -111,7 +119,7 @@ class TopKDecoder:
         self.count = torch.empty((c.batch, c.num_kv_heads), dtype=torch.int32, device=c.device)
         self.out, self.m, self.l, self.result = c.result_views()
         ws = B.dsa_sparse_decode_attn_workspace_size(c.kv, self.idx.shape[-1])
-        self.workspace = torch.empty(max(16, ws), dtype=torch.uint8, device=c.device)
+        self.workspace = torch.zeros(max(16, ws), dtype=torch.uint8, device=c.device)
 
     def build_meta(self, stream=None):
         B.dsa_build_page_meta(self.cache.kv, self.kind, self.lp, self.meta, stream)
@@ -126,7 +134,17 @@ class TopKDecoder:
         c = self.cache
         self.kv8 = c.kv8(stream)
         ws = B.dsa_sparse_decode_attn_kv8_workspace_size(c.kv, self.idx.shape[-1])
-        self.kv8_workspace = torch.empty(max(16, ws), dtype=torch.uint8, device=c.device)
+        self.kv8_workspace = torch.zeros(max(16, ws), dtype=torch.uint8, device=c.device)
+        self.kv4 = None
+        return self
+
+    def use_kv4(self, stream=None):
+        """Attends over KV4 pages from now on (the pools are quantised once, here)."""
+        c = self.cache
+        self.kv4 = c.kv4(stream)
+        ws = B.dsa_sparse_decode_attn_kv4_workspace_size(c.kv, self.idx.shape[-1])
+        self.kv4_workspace = torch.zeros(max(16, ws), dtype=torch.uint8, device=c.device)
+        self.kv8 = None
         return self
 
     def select(self, q, stream=None):
@@ -135,6 +153,11 @@ class TopKDecoder:
         B.dsa_select_topk(self.scores, self.stride, self.k, self.idx, self.count, stream)
 
     def attend(self, q, stream=None):
+        if getattr(self, "kv4", None) is not None:
+            B.dsa_sparse_decode_attn_kv4(self.cache.kv, self.kv4, q, self.idx, self.count,
+                                         self.scale, self.out, self.m, self.l,
+                                         self.kv4_workspace, stream)
+            return
         if getattr(self, "kv8", None) is not None:
             B.dsa_sparse_decode_attn_kv8(self.cache.kv, self.kv8, q, self.idx, self.count,
                                          self.scale, self.out, self.m, self.l,
@@ -170,7 +193,7 @@ class HierDecoder:
         self.count = torch.empty((c.batch, c.num_kv_heads), dtype=torch.int32, device=c.device)
         self.out, self.m, self.l, self.result = c.result_views()
         ws = B.dsa_sparse_decode_attn_workspace_size(c.kv, self.idx.shape[-1])
-        self.workspace = torch.empty(max(16, ws), dtype=torch.uint8, device=c.device)
+        self.workspace = torch.zeros(max(16, ws), dtype=torch.uint8, device=c.device)
 
     def build_meta(self, stream=None):
         B.dsa_build_page_meta(self.cache.kv, B.DSA_META_MINMAX, self.lp, self.meta, stream)
@@ -277,7 +300,7 @@ class PRRDecoder:
         self.out, self.m, self.l, self.result = c.result_views()
         ws = max(B.dsa_repair_merge_workspace_size(c.kv, k),
                  B.dsa_sparse_decode_attn_workspace_size(c.kv, k))
-        self.workspace = torch.empty(max(16, ws), dtype=torch.uint8, device=dev)
+        self.workspace = torch.zeros(max(16, ws), dtype=torch.uint8, device=dev)
         self.side = torch.cuda.Stream(device=dev) if two_streams else None
         self.ema_stream = torch.cuda.Stream(device=dev) if two_streams else None
         self.fused = fused

@@ -201,7 +201,10 @@ int dsa_select_threshold(const dsa_paged_kv* kv, const void* q, const float* sco
  *                  > 0 = the pages of a row are spread over exactly this many CTAs and merged
  *                  by a second kernel.
  *   workspace    : device scratch of at least dsa_sparse_decode_attn_workspace_size() bytes,
- *                  16-byte aligned (may be NULL when that size is 0).
+ *                  16-byte aligned (may be NULL when that size is 0), ZERO-FILLED before its
+ *                  first use: the persistent path keeps one ticket word per row in it, which
+ *                  every completed call leaves at zero again (zero-fill it again after a call
+ *                  that raised DSA_STATUS_TIMEOUT); the rest is scratch.
  */
 int dsa_sparse_decode_attn(const dsa_paged_kv* kv, const void* q, const int32_t* idx,
                            int32_t idx_stride, const int32_t* count, float scale, float* out,
@@ -273,7 +276,8 @@ int dsa_streaming_head_attn(const dsa_paged_kv* kv, const void* q, int32_t sink_
  * With kv->head_is_streaming NULL it equals dsa_sparse_decode_attn (persistent path).
  *   idx/count/idx_stride : the dense rows' selections (streaming rows' entries are not read).
  *   out/m/l (out)        : every query head, 16-byte aligned out.
- *   workspace            : dsa_sparse_decode_attn_workspace_size(kv, idx_stride, 0) bytes.
+ *   workspace            : dsa_sparse_decode_attn_workspace_size(kv, idx_stride, 0) bytes,
+ *                          zero-filled before its first use (as for dsa_sparse_decode_attn).
  */
 int dsa_hybrid_decode_attn(const dsa_paged_kv* kv, const void* q, const int32_t* idx,
                            int32_t idx_stride, const int32_t* count, int32_t sink_tokens,
@@ -304,13 +308,45 @@ size_t dsa_kv8_bytes(const dsa_paged_kv* kv);
  * the query in f16 (|q| below 65504), each logit times its token's K scale and each probability
  * times its token's V scale (rounded to f16 for the P.V product).  kv->k_pages / v_pages are not
  * read (may be NULL); the page table, lengths and shapes are.  Streaming heads are skipped.
- *   workspace : dsa_sparse_decode_attn_kv8_workspace_size(kv, idx_stride) bytes.
+ *   workspace : dsa_sparse_decode_attn_kv8_workspace_size(kv, idx_stride) bytes, zero-filled
+ *               before its first use (as for dsa_sparse_decode_attn).
  */
 int dsa_sparse_decode_attn_kv8(const dsa_paged_kv* kv, const void* kv8, const void* q,
                                const int32_t* idx, int32_t idx_stride, const int32_t* count,
                                float scale, float* out, float* m, float* l, void* workspace,
                                size_t workspace_bytes, dsa_stream_t stream);
 size_t dsa_sparse_decode_attn_kv8_workspace_size(const dsa_paged_kv* kv, int32_t idx_stride);
+
+/*
+ * KV4 pages (an own 4-bit page format; [LServe] §2.2 decodes over 4-bit KV, the W4A8KV4 setting
+ * it builds on, without giving a format).  Every K and V row of the pool is stored as 128 integer
+ * codes with one fp32 scale: scale = max_i |x_i| / 7 and code_i = round(x_i / scale) (fp32
+ * division, ties to even) in [-7, 7], kept as the nibble code_i + 8, dims 2i and 2i + 1 in the low
+ * and high half of byte i; a row of zeros gets scale 0 and codes 0.  A value decodes as
+ * (nibble - 8) * scale.
+ * Layout: one contiguous block of 136 p bytes per (physical page P, KV head h), at offset
+ * (P * Hkv + h) * 136 p: the K codes [p][64], the V codes [p][64], the K scales fp32 [p], the V
+ * scales fp32 [p].  The 64-byte code row of token slot r is stored at row r ^ ((r >> 1) & 1) (in
+ * every other pair of rows the two swap places: a bank-spreading permutation for the attention's
+ * operand loads).
+ *   kv4 (out) : dsa_kv4_bytes(kv) bytes, 16-byte aligned.
+ * Every physical page is converted (the bf16 pools are read, not changed).
+ */
+int dsa_quantize_kv4(const dsa_paged_kv* kv, void* kv4, dsa_stream_t stream);
+size_t dsa_kv4_bytes(const dsa_paged_kv* kv);
+
+/*
+ * Sparse decode attention over KV4 pages: as dsa_sparse_decode_attn_kv8 over KV4 blocks (the codes
+ * enter the tensor-core products as f16, exact; logits times the token's K scale, probabilities
+ * times its V scale, rounded to f16 for the P.V product).
+ *   workspace : dsa_sparse_decode_attn_kv4_workspace_size(kv, idx_stride) bytes, zero-filled
+ *               before its first use (as for dsa_sparse_decode_attn).
+ */
+int dsa_sparse_decode_attn_kv4(const dsa_paged_kv* kv, const void* kv4, const void* q,
+                               const int32_t* idx, int32_t idx_stride, const int32_t* count,
+                               float scale, float* out, float* m, float* l, void* workspace,
+                               size_t workspace_bytes, dsa_stream_t stream);
+size_t dsa_sparse_decode_attn_kv4_workspace_size(const dsa_paged_kv* kv, int32_t idx_stride);
 
 /*
  * PRR EMA predictor ([PRR] §3.1) fused with the speculative-set selection ([PRR] §3.4 with a fixed

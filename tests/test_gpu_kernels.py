@@ -311,7 +311,7 @@ def test_sparse_decode_attn(Hq, Hkv, page, splits):
     scale = 1 / math.sqrt(128)
     q = inp["q"][0]
     ws = B.dsa_sparse_decode_attn_workspace_size(cache.kv, k, splits)
-    wsb = torch.empty(max(ws, 16), dtype=torch.uint8, device="cuda")
+    wsb = torch.zeros(max(ws, 16), dtype=torch.uint8, device="cuda")
     out, m, l = cache.outputs()
     B.dsa_sparse_decode_attn(cache.kv, q, torch.from_numpy(idx).cuda(), torch.from_numpy(cnt).cuda(),
                              scale, out, m, l, num_splits=splits, workspace=wsb)
@@ -346,7 +346,7 @@ def test_persistent_partition(shape):
     idx, cnt = _random_selection(w, inp, k, seed=k, allow_bad=False)
     scale = 1 / math.sqrt(128)
     q = inp["q"][0]
-    ws = torch.empty(max(16, B.dsa_sparse_decode_attn_workspace_size(cache.kv, k)),
+    ws = torch.zeros(max(16, B.dsa_sparse_decode_attn_workspace_size(cache.kv, k)),
                      dtype=torch.uint8, device="cuda")
     ref = _oracle_sparse(w, inp, cache, q, idx, cnt, scale)
     dense = np.array([h not in streaming for h in range(w.num_kv_heads)]).repeat(w.group)
@@ -459,7 +459,7 @@ def test_hybrid_decode_attn(L, sink, local, page):
     idx_t = torch.tensor(idx, device="cuda").view(w.batch, 4, 9)
     cnt_t = torch.tensor(cnt, device="cuda").view(w.batch, 4)
     out, m, l = cache.outputs()
-    ws = torch.empty(max(16, B.dsa_sparse_decode_attn_workspace_size(cache.kv, 9)),
+    ws = torch.zeros(max(16, B.dsa_sparse_decode_attn_workspace_size(cache.kv, 9)),
                      dtype=torch.uint8, device="cuda")
     B.dsa_hybrid_decode_attn(cache.kv, q, idx_t, cnt_t, sink, local, scale, out, m, l, ws)
     torch.cuda.synchronize()
@@ -553,6 +553,63 @@ def test_sparse_decode_attn_kv8(page, G):
     # the 8-bit pages move the output by at most a few percent of its scale
     d = (out - out16).abs().max().item()
     assert d < 0.1 * out16.abs().max().item() + 1e-3
+    assert int(cache.status.item()) == 0
+
+
+def test_quantize_kv4_matches_oracle_bitwise():
+    """KV4 conversion of the whole pool: every packed code byte and every row scale equals the
+    oracle's encoding (fp32 scale and division, rounding ties to even, offset-8 nibbles)."""
+    w, inp, cache = small(page=16, L=16 * 30 + 5, seed=43)
+    cache.k_pages[3, 1, 5] = 0          # a zero row keeps scale 0
+    cache.v_pages[2, 0, :4] *= 1e3      # rows of large magnitude
+    cache.k_pages[1, 0, 2, :8] = torch.tensor([7, -7, 3.5, 0.5, 1.5, 2.5, -2.5, 0],
+                                              dtype=torch.bfloat16)  # ties (scale is not 1 here)
+    buf = cache.kv4()
+    torch.cuda.synchronize()
+    assert buf.numel() == cache.num_phys_pages * cache.num_kv_heads * 136 * cache.page_size
+    k4, v4, ks, vs = B.kv4_unpack(buf, cache.num_phys_pages, cache.num_kv_heads,
+                                  cache.page_size)
+    for pool, codes, scales in ((cache.k_pages, k4, ks), (cache.v_pages, v4, vs)):
+        ref_c, ref_s = O.kv4_encode_rows(pool.float().cpu().numpy())
+        np.testing.assert_array_equal(scales.cpu().numpy(), ref_s)
+        np.testing.assert_array_equal(codes.cpu().numpy(), ref_c)
+    assert float(ks[3, 1, 5]) == 0.0
+
+
+@pytest.mark.parametrize("page,G", [(16, 4), (64, 16), (32, 1)])
+def test_sparse_decode_attn_kv4(page, G):
+    """Attention over KV4 pages against the oracle's attention over the decoded rows of the
+    selected pages (ragged requests, a short last page)."""
+    Hkv = 2
+    w, inp, cache = small(Hq=G * Hkv, Hkv=Hkv, page=page, L=page * 40 + 7, seed=44 + page)
+    from dynamic_block_sparse_gb300.pipeline import TopKDecoder
+    dec = TopKDecoder(cache, 9)
+    dec.build_meta()
+    q = inp["q"][0]
+    out16 = dec.step(q)[0].clone()
+    dec.use_kv4()
+    out, m, l = dec.step(q)
+    torch.cuda.synchronize()
+    k4, v4, ks, vs = [x.cpu().numpy() for x in B.kv4_unpack(dec.kv4, cache.num_phys_pages,
+                                                                cache.num_kv_heads, page)]
+    Kd = O.kv4_decode_rows(k4, ks)
+    Vd = O.kv4_decode_rows(v4, vs)
+    table = cache.page_table.cpu().numpy()
+    for b in range(w.batch):
+        L = int(cache.seq_lens[b])
+        for h in range(Hkv):
+            A = dec.idx[b, h, :int(dec.count[b, h])].cpu().numpy()
+            toks = O.page_token_ids(A, page, L)
+            K = np.stack([Kd[table[b, t // page], h, t % page] for t in range(L)])
+            V = np.stack([Vd[table[b, t // page], h, t % page] for t in range(L)])
+            sl = slice(h * G, (h + 1) * G)
+            ref = O.attend(q[b, sl], K, V, toks, dec.scale)
+            assert_outputs(out[b, sl].cpu().numpy(), m[b, sl].cpu().numpy(),
+                           l[b, sl].cpu().numpy(), ref, f"kv4 b{b} h{h}")
+    # 4-bit pages stay within the format's error of the bf16 attention (half a code step,
+    # max|x| / 14 per value, averaged by the softmax)
+    d = (out - out16).abs().max().item()
+    assert d < 0.5 * out16.abs().max().item() + 1e-2
     assert int(cache.status.item()) == 0
 
 
@@ -817,7 +874,7 @@ def test_bad_page_id_raises_status_without_fault(bad, path):
         parts = None
         if path == "page_partials":
             parts = torch.zeros((2, 2, 2, 4, 132), dtype=torch.float32, device="cuda")
-        ws = torch.empty(max(16, B.dsa_sparse_decode_attn_workspace_size(kv, 2, splits)),
+        ws = torch.zeros(max(16, B.dsa_sparse_decode_attn_workspace_size(kv, 2, splits)),
                          dtype=torch.uint8, device="cuda")
         B.dsa_sparse_decode_attn(kv, inp["q"][0], idx, cnt, 0.1, out, m, l,
                                  page_partials=parts, num_splits=splits, workspace=ws)
@@ -845,7 +902,7 @@ def test_kernels_are_deterministic():
     w, inp, cache = small(Hq=32, Hkv=2, page=64, L=64 * 60, seed=1)
     idx, cnt = _random_selection(w, inp, 40, seed=2, allow_bad=False)
     dI, dC = torch.from_numpy(idx).cuda(), torch.from_numpy(cnt).cuda()
-    ws = torch.empty(B.dsa_sparse_decode_attn_workspace_size(cache.kv, 40) + 16,
+    ws = torch.zeros(B.dsa_sparse_decode_attn_workspace_size(cache.kv, 40) + 16,
                      dtype=torch.uint8, device="cuda")
     outs = []
     for _ in range(2):

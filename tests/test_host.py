@@ -286,6 +286,35 @@ def test_kv8_unpack_reads_the_documented_layout():
     np.testing.assert_array_equal(vs8.numpy(), vs)
 
 
+def test_kv4_unpack_reads_the_documented_layout():
+    """A KV4 buffer written byte by byte from the layout the header documents (per (page, KV
+    head): K code rows, V code rows with slot r's 64-byte row at row r ^ ((r >> 1) & 1), then the
+    K and V scales) comes apart into rows in token order and the scales."""
+    from dynamic_block_sparse_gb300 import binding as B
+    P, H, p = 3, 2, 16
+    rng = np.random.default_rng(6)
+    kc = rng.integers(0, 256, size=(P, H, p, 64), dtype=np.uint8)
+    vc = rng.integers(0, 256, size=(P, H, p, 64), dtype=np.uint8)
+    ks = rng.random((P, H, p), dtype=np.float32)
+    vs = rng.random((P, H, p), dtype=np.float32)
+    buf = bytearray(P * H * 136 * p)
+    for b in range(P):
+        for h in range(H):
+            base = (b * H + h) * 136 * p
+            for r in range(p):
+                at = 64 * (r ^ ((r >> 1) & 1))
+                buf[base + at: base + at + 64] = kc[b, h, r].tobytes()
+                buf[base + 64 * p + at: base + 64 * p + at + 64] = vc[b, h, r].tobytes()
+            buf[base + 128 * p: base + 132 * p] = ks[b, h].tobytes()
+            buf[base + 132 * p: base + 136 * p] = vs[b, h].tobytes()
+    t = torch.frombuffer(buf, dtype=torch.uint8)
+    k4, v4, ks4, vs4 = B.kv4_unpack(t, P, H, p)
+    np.testing.assert_array_equal(k4.numpy(), kc)
+    np.testing.assert_array_equal(v4.numpy(), vc)
+    np.testing.assert_array_equal(ks4.numpy(), ks)
+    np.testing.assert_array_equal(vs4.numpy(), vs)
+
+
 def test_bench_rows_only_rejects_unknown_workload():
     """``bench.py --rows-only`` accepts the four row workloads and refuses anything else before it
     touches a GPU."""
