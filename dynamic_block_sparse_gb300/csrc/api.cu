@@ -690,15 +690,19 @@ int quantized_attn(const dsa_paged_kv* kv, const void* blocks, int qbits, const 
   if (!workspace || workspace_bytes < need)
     return fail(DSA_ERR_WORKSPACE, "workspace of %zu bytes needed", need);
   if (!aligned(workspace, 16)) return fail(DSA_ERR_ALIGNMENT, "workspace must be 16-byte aligned");
-  // as many stages (one page block each) as fit, up to 128 KB of them (the bf16 path's budget)
+  // as many stages (one page block each) as fit in 160 KB: the small blocks need many in flight
+  // to keep the page rate of the bytes' roofline (stages / load latency)
   const size_t smem_cap = 227 * 1024;
   const int per_token = qbits == 8 ? 264 : 136;
-  const int stride = (per_token * v.p + 1023) & ~1023;
-  int stages = 131072 / stride;
+  const int stride = (per_token * v.p + 15) & ~15;
+  int stages = 163840 / stride;
   if (stages > kStreamMaxStages) stages = kStreamMaxStages;
   while (stages > 1 && stream_attn_smem_bytes(v.p, stages, v.G, qbits) > smem_cap) --stages;
   if (stages < 1 || stream_attn_smem_bytes(v.p, stages, v.G, qbits) > smem_cap)
     return fail(DSA_ERR_UNSUPPORTED, "%s: shape needs too much shared memory", name);
+  // every consumer warp owns the same number of (stage, 16-token tile) slots of the ring
+  const int tiles = v.p / 16;
+  while (stages * tiles > 8 && (stages * tiles) % 8 != 0) --stages;
   StreamAttnArgs sa = {};
   sa.kv = v;
   sa.q = static_cast<const __nv_bfloat16*>(q);

@@ -71,14 +71,18 @@ DSA_DEV void mbar_arrive(uint32_t bar) {
   asm volatile("mbarrier.arrive.release.cta.shared::cta.b64 _, [%0];" ::"r"(bar) : "memory");
 }
 
+// The waiting thread is suspended until the phase completes or kWaitSuspendNs pass, so that a
+// waiting warp does not spin on issue slots its SM sub-partition's working warps need.
+constexpr uint32_t kWaitSuspendNs = 100000;
+
 DSA_DEV bool mbar_try_wait(uint32_t bar, uint32_t parity) {
   uint32_t ok;
   asm volatile(
       "{\n\t.reg .pred p;\n\t"
-      "mbarrier.try_wait.parity.acquire.cta.shared::cta.b64 p, [%1], %2;\n\t"
+      "mbarrier.try_wait.parity.acquire.cta.shared::cta.b64 p, [%1], %2, %3;\n\t"
       "selp.u32 %0, 1, 0, p;\n\t}"
       : "=r"(ok)
-      : "r"(bar), "r"(parity)
+      : "r"(bar), "r"(parity), "r"(kWaitSuspendNs)
       : "memory");
   return ok != 0;
 }

@@ -139,7 +139,7 @@ struct StreamAttnArgs {
   const uint8_t* qkv;
   int qbits;
 };
-constexpr int kStreamMaxStages = 16;
+constexpr int kStreamMaxStages = 64;  // ring stages of the persistent attention (a 64-bit mask)
 constexpr int kStreamMaxGrid = 512;  // bounds the row merge's [G][parts] weights in shared memory
 size_t stream_attn_smem_bytes(int page, int stages, int G, int qbits = 0);  // qbits 0: bf16
 int stream_attn_grid();  // CTAs of one launch: one per SM

@@ -35,6 +35,7 @@ constexpr int kSConsumers = kSW * 32;
 constexpr int kSMaxHeads = 1024;           // KV heads the dense-head table can hold
 constexpr int kUnitPadTokens = 128;        // empty slots per dense row, in tokens of pages
 constexpr int kIssueLanes = 4;             // producer lanes issuing page loads at once
+constexpr int kMiscWords = 32 + 2 * kStreamMaxStages;  // shared words before the head tables
 
 struct SLayout {
   uint32_t stage_stride, merge_off, q_off, bar_off, misc_off, total;
@@ -54,13 +55,15 @@ __host__ __device__ constexpr uint32_t block_bytes_per_token(int fmt) {
 
 __host__ __device__ inline SLayout slayout(int page, int stages, int G, int fmt = kFmtBf16) {
   SLayout L;
+  // (a quantised block arrives by a 1-D bulk copy: 16-byte alignment is all it needs; the bf16
+  // pages' 128-byte-swizzled tensor loads want 1024)
   L.stage_stride = fmt == kFmtBf16 ? 512u * page
-                                   : (block_bytes_per_token(fmt) * page + 1023u) & ~1023u;
+                                   : (block_bytes_per_token(fmt) * page + 15u) & ~15u;
   L.merge_off = ((L.stage_stride * stages) + 1023u) & ~1023u;
   L.q_off = L.merge_off + static_cast<uint32_t>(kSW * G * (kHeadDim + 2) * 4 + 127) / 128 * 128;
   L.bar_off = L.q_off + 2u * 16u * kHeadDim * 2u;
   L.misc_off = L.bar_off + 16u * static_cast<uint32_t>(stages) + 32u;
-  L.total = ((L.misc_off + 256u + 8u * kSMaxHeads + 1023u) & ~1023u) + 1024u;
+  L.total = ((L.misc_off + 4u * kMiscWords + 8u * kSMaxHeads + 1023u) & ~1023u) + 1024u;
   return L;
 }
 
@@ -396,11 +399,12 @@ __global__ void __launch_bounds__(kSThreads, 1)
   int* n_dense_heads = misc + 5;            // [5]
   int* n_stream_heads = misc + 6;           // [6]
   int* desc = misc + 8;                     // [8, 16): mailbox [2][row, beg, end, len]
-  volatile int* stage_ok = misc + 16;       // [16, 32): did the producer load this stage
-  volatile int* stage_pos = misc + 32;      // [32, 48): page position held by this stage
-  int* desc_kind = misc + 48;               // [48, 50): mailbox [2]: 1 for a streaming unit
-  int* dense_heads = misc + 64;             // [64, 64 + Hkv)
-  int* stream_heads = misc + 64 + kSMaxHeads;  // [.., + Hkv) when streaming units are on
+  int* desc_kind = misc + 16;               // [16, 18): mailbox [2]: 1 for a streaming unit
+  // [20, 28): the cut rows' geometry (see cut_info below)
+  volatile int* stage_ok = misc + 32;       // [32, 32 + S): did the producer load this stage
+  volatile int* stage_pos = misc + 32 + kStreamMaxStages;  // [.., + S): its page position
+  int* dense_heads = misc + kMiscWords;     // [kMiscWords, + Hkv)
+  int* stream_heads = misc + kMiscWords + kSMaxHeads;  // [.., + Hkv) when streaming units are on
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
   const uint32_t stage_bytes = lay.stage_stride;           // stage s at smem + s * stage_bytes
   const uint32_t stage_tx = kBpt * page;  // bytes a stage's loads bring
@@ -770,9 +774,9 @@ __global__ void __launch_bounds__(kSThreads, 1)
   }
 
   // ---- consumers: warp `warp` owns tile t of stage s when (s * tiles + t) % kSW == warp
-  uint32_t own_stages = 0;
+  uint64_t own_stages = 0;
   for (int s = 0; s < S; ++s)
-    if (((warp - s * tiles) % kSW + kSW) % kSW < tiles) own_stages |= 1u << s;
+    if (((warp - s * tiles) % kSW + kSW) % kSW < tiles) own_stages |= 1ull << s;
   int i = 0;  // ring position, in lock-step with the producer
   bool any_cut = false;
   // Unit u = n_units is a rehearsal: it runs the unit epilogue and the cut-row merge (the same
@@ -782,10 +786,13 @@ __global__ void __launch_bounds__(kSThreads, 1)
   // rehearse: they finish well before the CTAs holding two units, which run one more epilogue and
   // take the last tickets, so the rehearsal's own cold fetches cost the launch nothing.
   bool merged = false;  // this CTA merged a cut row (uniform across the consumer warps)
+#ifdef DSA_TIMELINE
+  int n_owned = 0;  // pages this warp has taken (for the per-page stamps)
+#endif
   const int n_iter = n_units + (n_units == 1 ? 1 : 0);
   // The geometry of the rows this CTA may share with others (its first and its last unit), worked
   // out now, while the first pages are on their way: at the end only the tickets remain.
-  int* cut_info = misc + 50;  // [2][first CTA, CTA count, row, record slot of the first CTA]
+  int* cut_info = misc + 20;  // [2][first CTA, CTA count, row, record slot of the first CTA]
   if (warp == 0 && lane < 2) {
     const int di = d_first + (lane == 0 ? 0 : n_units - 1);
     const long long rs = unit_start(di);
@@ -834,9 +841,14 @@ __global__ void __launch_bounds__(kSThreads, 1)
         s_next = 0;
         ph_next ^= 1;
       }
-      if (!((own_stages >> s) & 1u)) continue;
+      if (!((own_stages >> s) & 1ull)) continue;
+#ifdef DSA_TIMELINE
+      const int owned_k = n_owned++;  // warp 0's fourth page of its first unit, timed alone
+      DSA_STAMP_DIRECT(g_trace_stream, 24, owned_k == 3 ? 0 : 1 << 20);
+#endif
       if (!mbar_wait(smem_u32(&bars[s]), ph, abort_flag, kv.status)) break;
       DSA_STAMP_DIRECT(g_trace_stream, 3, 0);  // warp 0's first page landed
+      DSA_STAMP_DIRECT(g_trace_stream, 22, owned_k == 3 ? 0 : 1 << 20);
       const int pos = stage_pos[s];
       const bool loaded = stage_ok[s] != 0;
       const uint32_t kb = smem_base + s * stage_bytes;
@@ -875,6 +887,7 @@ __global__ void __launch_bounds__(kSThreads, 1)
       __syncwarp();
       if (lane == 0)
         for (int r = 0; r < arrivals; ++r) mbar_arrive(smem_u32(&bars[S + s]));
+      DSA_STAMP_DIRECT(g_trace_stream, 23, owned_k == 3 ? 0 : 1 << 20);
     }
     i += npg;
     DSA_STAMP_DIRECT(g_trace_stream, 4, 0);  // warp 0 through the first unit's pages

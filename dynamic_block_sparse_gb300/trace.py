@@ -3,6 +3,7 @@
     python -m dynamic_block_sparse_gb300.trace threshold   # PSA threshold kernel on psa_threshold
     python -m dynamic_block_sparse_gb300.trace prr         # fused PRR step on prr_512k
     python -m dynamic_block_sparse_gb300.trace stream      # persistent attention on llama3_8b_layer
+    python -m dynamic_block_sparse_gb300.trace stream --pages kv8   # the same over KV8 (or kv4) pages
 
 Builds ``libdsa_trace.so`` (every kernel compiled with ``-DDSA_TIMELINE``), runs the workload's
 step several times cold (L2 flushed before each launch) and warm (launches back to back), and
@@ -61,6 +62,9 @@ LABELS = {
         19: "producer: set-up done (arrived)",
         20: "last unit: thread 0's share of the epilogue done",
         21: "cut rows: thread 0's ticket returned",
+        22: "warp 0: its fourth page landed",
+        23: "warp 0: its fourth page attended and released",
+        24: "warp 0: waiting for its fourth page",
     },
     "prr": {
         1: "worker: first segment's table, state and query loaded",
@@ -98,7 +102,7 @@ def _flusher(torch, dev):
     return flush
 
 
-def _setup(kernel, B, torch):
+def _setup(kernel, B, torch, pages="bf16"):
     from dynamic_block_sparse_gb300.pipeline import Cache, PRRDecoder, ThresholdDecoder
     from dynamic_block_sparse_gb300.workloads import BY_NAME, make_inputs
 
@@ -111,6 +115,10 @@ def _setup(kernel, B, torch):
         dec.build_meta()
         q = inp["q"][0].clone()
         dec.step(q)
+        if pages == "kv8":
+            dec.use_kv8()
+        elif pages == "kv4":
+            dec.use_kv4()
 
         def step(i):
             dec.attend(q)
@@ -175,7 +183,8 @@ def _collect(kernel, lib, step, flush, torch, cold: bool, runs: int):
 # phase lengths worth reading per CTA (stamp pairs, both passed by the same CTA)
 SPANS = {
     "stream": [(0, 19), (19, 13), (13, 12), (12, 8), (8, 3), (8, 18), (1, 2), (3, 4), (4, 5),
-               (14, 20), (20, 15), (15, 21), (21, 16), (16, 17), (16, 6), (9, 6)],
+               (14, 20), (20, 15), (15, 21), (21, 16), (16, 17), (16, 6), (9, 6), (24, 22),
+               (22, 23)],
 }
 
 
@@ -237,6 +246,8 @@ def main(argv=None):
     p = argparse.ArgumentParser(description=__doc__.split("\n\n")[0])
     p.add_argument("kernel", choices=sorted(LABELS))
     p.add_argument("--runs", type=int, default=5)
+    p.add_argument("--pages", choices=["bf16", "kv8", "kv4"], default="bf16",
+                   help="page format of the stream trace")
     args = p.parse_args(argv)
     import torch
 
@@ -246,7 +257,7 @@ def main(argv=None):
     if not torch.cuda.is_available():
         raise SystemExit("the tracing build runs on a CUDA device")
     lib = B.load(Bd.build_traced())
-    step, cache = _setup(args.kernel, B, torch)
+    step, cache = _setup(args.kernel, B, torch, args.pages)
     flush = _flusher(torch, "cuda")
     for i in range(3):
         step(i)
