@@ -54,6 +54,7 @@ constexpr int kRound = kGroups * kRecGroup;
 constexpr int kPredMax = kPrrPredMax;      // bound of k and k_pred
 constexpr int kMaxStages = 3;              // TMA ring depth
 constexpr int kWs = kHeadDim + 4;          // a warp's merge state: m, l, -, -, O[128]
+constexpr int kRoundRecs = 10;             // records a warp loads at once in the merge
 constexpr int kQTile = 16 * kQStride;      // bf16 elements of one warp's query tile
 constexpr int kBitsMax = kTopkMaxN / 2;    // longest row the A_t pass keeps two bitmaps for
 
@@ -1025,18 +1026,31 @@ __global__ void __launch_bounds__(kThreads, 1)
       wo.w = wo.w * f_old + o.w * f_new;
       wm = mn;
     };
+    // adds a sum of parts: max m2, sum l, unnormalised O o (both relative to m2)
+    auto absorb_sum = [&](float m2, float l, float4 o) {
+      const float mn = fmaxf(wm, m2);
+      const float f_old = wm == -INFINITY ? 0.f : fast_exp2(wm - mn);
+      const float f = fast_exp2(m2 - mn);
+      wl = wl * f_old + l * f;
+      wo.x = wo.x * f_old + o.x * f;
+      wo.y = wo.y * f_old + o.y * f;
+      wo.z = wo.z * f_old + o.z * f;
+      wo.w = wo.w * f_old + o.w * f;
+      wm = mn;
+    };
     float* ws = wst + warp * kWs;
     if (warp < kW && ws[1] > 0.f) {  // this warp's missed pages
       const float inv = 1.f / ws[1];
       const float4 o = *(reinterpret_cast<const float4*>(ws + 4) + lane);
       absorb(ws[0], ws[1], make_float4(o.x * inv, o.y * inv, o.z * inv, o.w * inv));
     }
-    // ---- speculative records, eight per warp round
-    for (int i0 = warp; i0 < n_parts; i0 += 8 * kWarps) {
-      float2 ml[8];
-      float4 ov[8];
+    // ---- speculative records, kRoundRecs per warp round: each record's weight against the
+    // round's largest max (independent exponentials), then one merge into the warp's state
+    for (int i0 = warp; i0 < n_parts; i0 += kRoundRecs * kWarps) {
+      float2 ml[kRoundRecs];
+      float4 ov[kRoundRecs];
 #pragma unroll
-      for (int u = 0; u < 8; ++u) {
+      for (int u = 0; u < kRoundRecs; ++u) {
         const int i = i0 + u * kWarps;
         ml[u] = make_float2(-INFINITY, 0.f);
         ov[u] = make_float4(0.f, 0.f, 0.f, 0.f);
@@ -1052,9 +1066,25 @@ __global__ void __launch_bounds__(kThreads, 1)
           }
         }
       }
+      float mr = -INFINITY;  // (every lane holds the same m and l: the branches are uniform)
 #pragma unroll
-      for (int u = 0; u < 8; ++u) absorb(ml[u].x * kLog2e, ml[u].y, ov[u]);
+      for (int u = 0; u < kRoundRecs; ++u)
+        if (ml[u].y > 0.f) mr = fmaxf(mr, ml[u].x * kLog2e);
+      if (mr == -INFINITY) continue;
+      float rl = 0.f;
+      float4 ro = make_float4(0.f, 0.f, 0.f, 0.f);
+#pragma unroll
+      for (int u = 0; u < kRoundRecs; ++u) {
+        const float f = ml[u].y > 0.f ? fast_exp2(ml[u].x * kLog2e - mr) * ml[u].y : 0.f;
+        rl += f;
+        ro.x += f * ov[u].x;
+        ro.y += f * ov[u].y;
+        ro.z += f * ov[u].z;
+        ro.w += f * ov[u].w;
+      }
+      absorb_sum(mr, rl, ro);
     }
+    DSA_STAMP(19);  // task: thread 0's warp has merged its records
     __syncwarp();
     if (lane == 0) {
       ws[0] = wm;
@@ -1062,6 +1092,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     }
     *reinterpret_cast<float4*>(ws + 4 + lane * 4) = wo;
     __syncthreads();
+    DSA_STAMP(20);  // task: every warp's state stored (barrier)
     // ---- combine the warps' states
     float M = -INFINITY;
 #pragma unroll
