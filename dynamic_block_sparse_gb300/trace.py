@@ -85,6 +85,8 @@ LABELS = {
         16: "worker: first round's record loads issued",
         17: "worker: thread 0's first-round scores and EMA written",
         18: "worker: first segment's rounds done (barrier)",
+        19: "task: thread 0's warp has merged its records",
+        20: "task: every warp's merge state stored (barrier)",
     },
 }
 SLOTS = 32
@@ -182,6 +184,8 @@ def _collect(kernel, lib, step, flush, torch, cold: bool, runs: int):
 
 # phase lengths worth reading per CTA (stamp pairs, both passed by the same CTA)
 SPANS = {
+    "prr": [(5, 6), (6, 7), (7, 14), (14, 8), (8, 9), (9, 10), (10, 11), (11, 19), (19, 20),
+            (20, 12), (12, 13)],
     "stream": [(0, 19), (19, 13), (13, 12), (12, 8), (8, 3), (8, 18), (1, 2), (3, 4), (4, 5),
                (14, 20), (20, 15), (15, 21), (21, 16), (16, 17), (16, 6), (9, 6), (24, 22),
                (22, 23)],
