@@ -10,9 +10,10 @@
 //      thread's largest key) and issues the TMA loads of its blocks;
 //   3. one warp per block computes the block's softmax mass of every query head from Q.K alone,
 //      keeping the Q.K tiles for step 5;
-//   4. warp 0 evaluates the stop rule AS_acc / (AS_acc + AS_min) >= tau after every block of the
-//      chunk at once (prefix sums and minima in rank order; with DSA_PSA_NLEFT the rule weighs
-//      AS_min by the blocks left) and accepts up to the first block that meets it;
+//   4. every warp evaluates the stop rule AS_acc / (AS_acc + AS_min) >= tau after every block of
+//      the chunk at once (prefix sums and minima in rank order, the same result in each warp, so
+//      that no warp waits for another's; with DSA_PSA_NLEFT the rule weighs AS_min by the blocks
+//      left) and accepts up to the first block that meets it;
 //   5. the accepted blocks get the P.V pass, one warp per block.
 // No host round trip.  A row whose accepted set fits in one chunk costs a single pass; the chunk is
 // sized so that typical rows do (blocks past the stop point are fetched and then dropped).
