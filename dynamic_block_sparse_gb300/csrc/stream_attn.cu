@@ -21,6 +21,8 @@
 #include "attn_core.cuh"
 #include <cuda_fp8.h>
 
+#include <type_traits>
+
 #include "internal.h"
 
 namespace dsa {
@@ -321,6 +323,212 @@ DSA_DEV void tile_softmax_pv_q(WarpSoftmaxState& st, float (&sc)[2][4], float sc
   }
 }
 
+// ---- Transposed tiles (quantised pages, query groups of at most 8).  S^T = codes_K . Q^T puts
+// the tile's 16 tokens on the m16 rows of the tensor-core product and the group on n8, so each
+// product is one mma per k-step (the untransposed tiles spend two, three quarters of their rows
+// empty at G = 4).  The probabilities leave the scores' accumulator layout as the next product's
+// B operand through two in-register 8x8 transposes (movmatrix).  O^T = codes_V^T . (P * s_V)^T
+// takes 8 m16 tiles of head dims: m-tile mt, row r < 8 is dim 16 r + 2 mt and row r + 8 is dim
+// 16 r + 2 mt + 1, so that a lane's V operands are the same pieces of four code rows as in the
+// untransposed tiles, and each lane ends holding adjacent dims of its two query heads.
+
+struct WarpStateT {
+  float o[8][4];  // O^T m-tile mt: rows g, g + 8 (dims 16 g + 2 mt, + 1), columns 2 tig, 2 tig + 1
+  float m[2];     // running max (log2 units) of query heads 2 tig, 2 tig + 1
+  float l[2];     // this lane's partial denominators of the same heads
+};
+
+DSA_DEV void state_init(WarpStateT& st) {
+#pragma unroll
+  for (int j = 0; j < 8; ++j)
+#pragma unroll
+    for (int e = 0; e < 4; ++e) st.o[j][e] = 0.f;
+  st.m[0] = st.m[1] = -INFINITY;
+  st.l[0] = st.l[1] = 0.f;
+}
+
+// The denominators summed over the eight lanes (g) that hold a head's tokens.
+DSA_DEV void state_finish(WarpStateT& st) {
+#pragma unroll
+  for (int r = 0; r < 2; ++r)
+#pragma unroll
+    for (int o = 4; o < 32; o <<= 1) st.l[r] += __shfl_xor_sync(0xffffffffu, st.l[r], o);
+}
+
+DSA_DEV uint32_t movmatrix_trans(uint32_t a) {
+  uint32_t d;
+  asm volatile("movmatrix.sync.aligned.m8n8.trans.b16 %0, %1;" : "=r"(d) : "r"(a));
+  return d;
+}
+
+// B fragments of Q^T (f16): qb[ks][0] = head g's dims d, d + 1 and qb[ks][1] its dims d + 2, d + 3,
+// d = 32 tig + 4 ks (the K operand's dim permutation); heads g >= G read the zero rows of sQ.
+DSA_DEV void load_qT_frags(const __nv_bfloat16* sQ, uint32_t (&qb)[8][4]) {
+  const int lane = threadIdx.x & 31;
+  const int g = lane >> 2, tig = lane & 3;
+  auto f16_pair = [](uint32_t bf2) {
+    const __nv_bfloat162 b = *reinterpret_cast<const __nv_bfloat162*>(&bf2);
+    const float2 f = __bfloat1622float2(b);
+    return pack_f16(f.x, f.y);
+  };
+#pragma unroll
+  for (int ks = 0; ks < 8; ++ks) {
+    const uint2 v = *reinterpret_cast<const uint2*>(sQ + g * kHeadDim + 32 * tig + 4 * ks);
+    qb[ks][0] = f16_pair(v.x);
+    qb[ks][1] = f16_pair(v.y);
+  }
+}
+
+// S^T for the tile's 16 code rows at kc: sc[0], sc[1] = token g, heads 2 tig, 2 tig + 1;
+// sc[2], sc[3] = token g + 8, the same heads.
+template <int FMT>
+DSA_DEV void tileT_scores(const uint32_t (&qb)[8][4], const uint8_t* kc, float (&sc)[4]) {
+  const int lane = threadIdx.x & 31;
+  const int g = lane >> 2, tig = lane & 3;
+  float acc[2][4];
+#pragma unroll
+  for (int c = 0; c < 2; ++c)
+#pragma unroll
+    for (int e = 0; e < 4; ++e) acc[c][e] = 0.f;
+  if constexpr (FMT == 8) {
+    // rows g and g + 8 (both at index g mod 8): the 16-byte pieces of dims 32 tig .. + 31
+    const uint8_t* ra = kc + g * 128;
+    const uint8_t* rb = kc + (g + 8) * 128;
+    const uint4 a0 = *reinterpret_cast<const uint4*>(ra + (((2 * tig) ^ g) << 4));
+    const uint4 a1 = *reinterpret_cast<const uint4*>(ra + (((2 * tig + 1) ^ g) << 4));
+    const uint4 b0 = *reinterpret_cast<const uint4*>(rb + (((2 * tig) ^ g) << 4));
+    const uint4 b1 = *reinterpret_cast<const uint4*>(rb + (((2 * tig + 1) ^ g) << 4));
+    const uint32_t wa[8] = {a0.x, a0.y, a0.z, a0.w, a1.x, a1.y, a1.z, a1.w};
+    const uint32_t wb[8] = {b0.x, b0.y, b0.z, b0.w, b1.x, b1.y, b1.z, b1.w};
+#pragma unroll
+    for (int ks = 0; ks < 8; ++ks) {
+      const uint32_t af[4] = {e4m3x2_f16x2(wa[ks]), e4m3x2_f16x2(wb[ks]),
+                              e4m3x2_f16x2(wa[ks] >> 16), e4m3x2_f16x2(wb[ks] >> 16)};
+      mma_f16(acc[ks & 1], af, qb[ks][0], qb[ks][1]);
+    }
+  } else {
+    const uint4 a4 = *reinterpret_cast<const uint4*>(kc + kv4_row(g) * 64 + 16 * tig);
+    const uint4 b4 = *reinterpret_cast<const uint4*>(kc + kv4_row(g + 8) * 64 + 16 * tig);
+    const uint32_t wa[4] = {a4.x, a4.y, a4.z, a4.w};
+    const uint32_t wb[4] = {b4.x, b4.y, b4.z, b4.w};
+#pragma unroll
+    for (int ks = 0; ks < 8; ++ks) {
+      const int h = 16 * (ks & 1);
+      const uint32_t af[4] = {kv4_pair(wa[ks >> 1], h, h + 4), kv4_pair(wb[ks >> 1], h, h + 4),
+                              kv4_pair(wa[ks >> 1], h + 8, h + 12),
+                              kv4_pair(wb[ks >> 1], h + 8, h + 12)};
+      mma_f16(acc[ks & 1], af, qb[ks][0], qb[ks][1]);
+    }
+  }
+#pragma unroll
+  for (int e = 0; e < 4; ++e) sc[e] = acc[0][e] + acc[1][e];
+}
+
+// Online-softmax update of the transposed tile (logits q . codes in sc, ks / vs: the 16 tokens'
+// K and V scales), then O^T += codes_V^T . (P * s_V)^T over the tile's V code rows at vc.
+template <int FMT>
+DSA_DEV void tileT_softmax_pv(WarpStateT& st, const float (&sc)[4], float scale_log2,
+                              uint32_t valid, const uint8_t* vc, const float* ks,
+                              const float* vs) {
+  const int lane = threadIdx.x & 31;
+  const int g = lane >> 2, tig = lane & 3;
+  const bool va = (valid >> g) & 1u, vb = (valid >> (g + 8)) & 1u;
+  const float ka = ks[g] * scale_log2, kb = ks[g + 8] * scale_log2;
+  float x[4];
+  x[0] = va ? sc[0] * ka : -INFINITY;
+  x[1] = va ? sc[1] * ka : -INFINITY;
+  x[2] = vb ? sc[2] * kb : -INFINITY;
+  x[3] = vb ? sc[3] * kb : -INFINITY;
+  float mx[2] = {fmaxf(x[0], x[2]), fmaxf(x[1], x[3])};
+#pragma unroll
+  for (int r = 0; r < 2; ++r)
+#pragma unroll
+    for (int o = 4; o < 32; o <<= 1) mx[r] = fmaxf(mx[r], __shfl_xor_sync(0xffffffffu, mx[r], o));
+  float alpha[2], mnew[2];
+#pragma unroll
+  for (int r = 0; r < 2; ++r) {
+    mnew[r] = fmaxf(st.m[r], mx[r]);
+    alpha[r] = (mnew[r] == -INFINITY) ? 1.f : fast_exp2(st.m[r] - mnew[r]);
+  }
+  float p[4];
+#pragma unroll
+  for (int e = 0; e < 4; ++e) {
+    const int r = e & 1;
+    p[e] = (mnew[r] == -INFINITY) ? 0.f : fast_exp2(x[e] - mnew[r]);
+  }
+  st.l[0] = st.l[0] * alpha[0] + (p[0] + p[2]);
+  st.l[1] = st.l[1] * alpha[1] + (p[1] + p[3]);
+  st.m[0] = mnew[0];
+  st.m[1] = mnew[1];
+  if (!__all_sync(0xffffffffu, alpha[0] == 1.f && alpha[1] == 1.f)) {
+#pragma unroll
+    for (int j = 0; j < 8; ++j) {
+      st.o[j][0] *= alpha[0];
+      st.o[j][1] *= alpha[1];
+      st.o[j][2] *= alpha[0];
+      st.o[j][3] *= alpha[1];
+    }
+  }
+  // P * s_V (0 for tokens that take no part, whatever their scale holds), then the B operand:
+  // tokens 2 tig, 2 tig + 1 (b0) and 2 tig + 8, + 9 (b1) of head g
+  const float sa = va ? vs[g] : 0.f, sb = vb ? vs[g + 8] : 0.f;
+  const uint32_t b0 = movmatrix_trans(pack_f16(p[0] * sa, p[1] * sa));
+  const uint32_t b1 = movmatrix_trans(pack_f16(p[2] * sb, p[3] * sb));
+  if constexpr (FMT == 8) {
+    // the 16-byte pieces g (dims 16 g .. + 15) of code rows 2 tig, 2 tig + 1, 2 tig + 8, 2 tig + 9
+    // (zeros for tokens that take no part, so that stale codes never meet a zero probability)
+    uint4 rv[4];
+#pragma unroll
+    for (int i = 0; i < 4; ++i) {
+      const int r = 2 * tig + (i & 1) + (i >> 1) * 8;
+      rv[i] = *reinterpret_cast<const uint4*>(vc + r * 128 + ((g ^ (r & 7)) << 4));
+      if (!((valid >> r) & 1u)) rv[i] = make_uint4(0u, 0u, 0u, 0u);
+    }
+    const uint32_t* w0 = reinterpret_cast<const uint32_t*>(&rv[0]);
+    const uint32_t* w1 = reinterpret_cast<const uint32_t*>(&rv[1]);
+    const uint32_t* w2 = reinterpret_cast<const uint32_t*>(&rv[2]);
+    const uint32_t* w3 = reinterpret_cast<const uint32_t*>(&rv[3]);
+#pragma unroll
+    for (int q = 0; q < 4; ++q) {  // dims 16 g + 4 q .. + 3: m-tiles 2 q and 2 q + 1
+      const uint32_t a01 = __byte_perm(w0[q], w1[q], 0x5140), c01 = __byte_perm(w0[q], w1[q], 0x7362);
+      const uint32_t a23 = __byte_perm(w2[q], w3[q], 0x5140), c23 = __byte_perm(w2[q], w3[q], 0x7362);
+      const uint32_t fa[4] = {e4m3x2_f16x2(a01), e4m3x2_f16x2(a01 >> 16), e4m3x2_f16x2(a23),
+                              e4m3x2_f16x2(a23 >> 16)};
+      const uint32_t fc[4] = {e4m3x2_f16x2(c01), e4m3x2_f16x2(c01 >> 16), e4m3x2_f16x2(c23),
+                              e4m3x2_f16x2(c23 >> 16)};
+      mma_f16(st.o[2 * q], fa, b0, b1);
+      mma_f16(st.o[2 * q + 1], fc, b0, b1);
+    }
+  } else {
+    // 8 bytes (dims 16 g .. + 15) of each of the four code rows; a nibble always decodes to a
+    // finite value, so nothing needs clearing
+    uint2 rv[4];
+#pragma unroll
+    for (int i = 0; i < 4; ++i) {
+      const int r = 2 * tig + (i & 1) + (i >> 1) * 8;
+      rv[i] = *reinterpret_cast<const uint2*>(vc + kv4_row(r) * 64 + 8 * g);
+    }
+#pragma unroll
+    for (int half = 0; half < 2; ++half) {  // dims 16 g + 8 half .. + 7: m-tiles 4 half .. + 3
+      const uint32_t w0 = half ? rv[0].y : rv[0].x, w1 = half ? rv[1].y : rv[1].x;
+      const uint32_t w2 = half ? rv[2].y : rv[2].x, w3 = half ? rv[3].y : rv[3].x;
+#pragma unroll
+      for (int quad = 0; quad < 2; ++quad) {  // dims + 4 quad .. + 3: m-tiles 4 half + 2 quad, + 1
+        const uint32_t sel = quad ? 0x7632u : 0x5410u;
+        const uint32_t x01 = __byte_perm(w0, w1, sel), x23 = __byte_perm(w2, w3, sel);
+#pragma unroll
+        for (int n = 0; n < 2; ++n) {  // dims + 2 n (rows g) and + 2 n + 1 (rows g + 8)
+          const uint32_t fa[4] = {kv4_pair(x01, 8 * n, 16 + 8 * n),
+                                  kv4_pair(x01, 8 * n + 4, 16 + 8 * n + 4),
+                                  kv4_pair(x23, 8 * n, 16 + 8 * n),
+                                  kv4_pair(x23, 8 * n + 4, 16 + 8 * n + 4)};
+          mma_f16(st.o[4 * half + 2 * quad + n], fa, b0, b1);
+        }
+      }
+    }
+  }
+}
+
 // Shared position of output dim d of query head r in the KV8 path's merge area: the pieces of 16
 // dims are XOR-permuted by the writer's column pair and row, so that the fragment stores of a warp
 // spread over the banks.
@@ -369,7 +577,8 @@ DSA_DEV int ticket_add(int32_t* p) {
 
 // STREAMING: the launch also serves the streaming heads (a second region of the slot space);
 // without it every streaming-specific path compiles away.
-template <bool STREAMING, int FMT>
+// TR: the transposed tiles (quantised pages, G <= 8).
+template <bool STREAMING, int FMT, bool TR = false>
 __global__ void __launch_bounds__(kSThreads, 1)
     stream_attn_kernel(const __grid_constant__ CUtensorMap tmK,
                        const __grid_constant__ CUtensorMap tmV, const StreamAttnArgs a) {
@@ -821,7 +1030,9 @@ __global__ void __launch_bounds__(kSThreads, 1)
     const int di = d_first + u;
     uint32_t qa[8][4] = {};
     if (!dry) {
-      if (QNT)
+      if (TR)
+        load_qT_frags(sQ + slot * 16 * kHeadDim, qa);
+      else if (QNT)
         load_q_frags_kv8(sQ + slot * 16 * kHeadDim, qa);
       else
         load_q_frags(sQ + slot * 16 * kHeadDim, qa, kHeadDim);
@@ -829,7 +1040,7 @@ __global__ void __launch_bounds__(kSThreads, 1)
       if (lane == 0) mbar_arrive(smem_u32(&qbars[2 + slot]));
     }
     DSA_STAMP_DIRECT(g_trace_stream, 2, 0);  // first unit's descriptor and query on chip
-    WarpSoftmaxState st;
+    std::conditional_t<TR, WarpStateT, WarpSoftmaxState> st;
     state_init(st);
     const int npg = end - beg;
     // stage and phase parity of ring position i + k, stepped along without divisions (a warp
@@ -862,6 +1073,16 @@ __global__ void __launch_bounds__(kSThreads, 1)
         const bool in = tok < L && (tok < lo_end || tok >= hi_beg);
         const uint32_t vm = __ballot_sync(0xffffffffu, in) & 0xffffu;
         if (vm == 0u) continue;
+        if constexpr (TR) {
+          const uint8_t* blk = smem + s * stage_bytes;  // the page's quantised block
+          const int rowb = KV8 ? 128 : 64;  // bytes per code row
+          const float* ksc = reinterpret_cast<const float*>(blk + 2 * rowb * page) + t * 16;
+          float sc4[4];
+          tileT_scores<FMT>(qa, blk + t * 16 * rowb, sc4);
+          tileT_softmax_pv<FMT>(st, sc4, a.scale_log2, vm, blk + (page + t * 16) * rowb, ksc,
+                                ksc + page);
+          continue;
+        } else {
         float sc[2][4];
         if (KV8) {
           const uint8_t* blk = smem + s * stage_bytes;  // the page's KV8 block
@@ -882,6 +1103,7 @@ __global__ void __launch_bounds__(kSThreads, 1)
           tile_scores(qa, kb, page, t * 16, sc);
           tile_softmax_pv(st, sc, a.scale_log2, vm, vb, page, t * 16);
         }
+        }
       }
       if (wrote) fence_proxy_async_smem();
       __syncwarp();
@@ -894,7 +1116,29 @@ __global__ void __launch_bounds__(kSThreads, 1)
     state_finish(st);
 
     // ---- unit epilogue: merge the warps' states of the G query heads
-    {
+    if constexpr (TR) {  // lane (g, tig): dims 16 g + 2 mt, + 1 of heads 2 tig, 2 tig + 1
+      const int g8 = lane >> 2, q0 = (lane & 3) * 2;
+      float* wO = sO + warp * G * kHeadDim;
+#pragma unroll
+      for (int mt = 0; mt < 8; ++mt) {
+        const int d = 16 * g8 + 2 * mt;
+        if (q0 < G)
+          *reinterpret_cast<float2*>(wO + q0 * kHeadDim + d) = make_float2(st.o[mt][0], st.o[mt][2]);
+        if (q0 + 1 < G)
+          *reinterpret_cast<float2*>(wO + (q0 + 1) * kHeadDim + d) =
+              make_float2(st.o[mt][1], st.o[mt][3]);
+      }
+      if (g8 == 0) {
+        if (q0 < G) {
+          sM[warp * G + q0] = st.m[0];
+          sL[warp * G + q0] = st.l[0];
+        }
+        if (q0 + 1 < G) {
+          sM[warp * G + q0 + 1] = st.m[1];
+          sL[warp * G + q0 + 1] = st.l[1];
+        }
+      }
+    } else {
       const int r0 = lane >> 2, c0 = (lane & 3) * 2;
       float* wO = sO + warp * G * kHeadDim;
 #pragma unroll
@@ -966,7 +1210,7 @@ __global__ void __launch_bounds__(kSThreads, 1)
     named_barrier(1, kSConsumers);
     for (int e = tid; e < G * kHeadDim; e += kSConsumers) {
       const int g = e >> 7, d = e & 127;
-      const int pos = QNT ? kv8_o_pos(g, d) : d;
+      const int pos = QNT && !TR ? kv8_o_pos(g, d) : d;
       float o = 0.f;
 #pragma unroll
       for (int w = 0; w < kSW; ++w) o += sO[(w * G + g) * kHeadDim + pos] * sM[w * G + g];
@@ -1105,8 +1349,12 @@ cudaError_t launch_stream_attn(const CUtensorMap& tmK, const CUtensorMap& tmV,
     if (e != cudaSuccess) return e;
     return launch_pdl(kernel, grid, kSThreads, bytes, s, tmK, tmV, a);
   };
-  if (fmt == kFmtKv8) return go(stream_attn_kernel<false, kFmtKv8>);
-  if (fmt == kFmtKv4) return go(stream_attn_kernel<false, kFmtKv4>);
+  // quantised pages: the transposed tiles when the query group fits their n8 columns
+  const bool tr = a.kv.G <= 8;
+  if (fmt == kFmtKv8)
+    return tr ? go(stream_attn_kernel<false, kFmtKv8, true>) : go(stream_attn_kernel<false, kFmtKv8>);
+  if (fmt == kFmtKv4)
+    return tr ? go(stream_attn_kernel<false, kFmtKv4, true>) : go(stream_attn_kernel<false, kFmtKv4>);
   return a.stream_stride > 0 ? go(stream_attn_kernel<true, kFmtBf16>)
                              : go(stream_attn_kernel<false, kFmtBf16>);
 }
