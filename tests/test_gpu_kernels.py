@@ -519,11 +519,12 @@ def test_quantize_kv8_matches_oracle_bitwise():
     assert float(ks[3, 1, 5]) == 0.0
 
 
-@pytest.mark.parametrize("page,G", [(16, 4), (64, 16), (32, 1)])
+@pytest.mark.parametrize("page,G", [(16, 4), (64, 16), (32, 1), (16, 8), (32, 2)])
 def test_sparse_decode_attn_kv8(page, G):
     """Attention over KV8 pages against the oracle's attention over the decoded rows of the
     selected pages (ragged requests, a short last page); and its distance to the bf16 attention
-    stays within the 8-bit format's error."""
+    stays within the 8-bit format's error.  Groups of at most 8 run the transposed tiles (G = 8 is
+    their widest), larger ones the untransposed."""
     Hkv = 2
     w, inp, cache = small(Hq=G * Hkv, Hkv=Hkv, page=page, L=page * 40 + 7, seed=42 + page)
     from dynamic_block_sparse_gb300.pipeline import TopKDecoder
@@ -576,7 +577,7 @@ def test_quantize_kv4_matches_oracle_bitwise():
     assert float(ks[3, 1, 5]) == 0.0
 
 
-@pytest.mark.parametrize("page,G", [(16, 4), (64, 16), (32, 1)])
+@pytest.mark.parametrize("page,G", [(16, 4), (64, 16), (32, 1), (16, 8), (32, 2)])
 def test_sparse_decode_attn_kv4(page, G):
     """Attention over KV4 pages against the oracle's attention over the decoded rows of the
     selected pages (ragged requests, a short last page)."""
