@@ -735,7 +735,9 @@ __global__ void __launch_bounds__(kSThreads, 1)
     // software-pipelined: while chunk A's pages are issued, the page-table entries of chunk B and
     // the selections of chunk C are already in flight.
     DSA_STAMP_DIRECT(g_trace_stream, 13, kSW * 32 + (n_units == -12345));
-    const int NL = min(kIssueLanes, S);  // a group of NL pages uses NL distinct stages
+    // a group of NL pages uses NL distinct stages; a quantised page is a single copy, so a group
+    // issues more of them (their pages are small: the ring turns over faster)
+    const int NL = min(QNT ? 4 * kIssueLanes : kIssueLanes, S);
     int i = 0;                           // ring position
     bool stopped = false;
     // First pages, straight-line.  The general loop below is long code that every CTA runs cold at
@@ -766,39 +768,54 @@ __global__ void __launch_bounds__(kSThreads, 1)
                   a.q + (static_cast<size_t>(b0) * kv.Hq + static_cast<size_t>(h0) * G) * kHeadDim,
                   static_cast<uint32_t>(G) * kHeadDim * 2, full);
       }
-      const int F = max(0, min(min(end - beg, S), 16));  // ring positions 0..F-1: no waits
+      // ring positions 0..F-1 need no waits: up to 32 quantised pages (a lane each), 16 bf16 ones
+      // (two lanes each)
+      const int F = max(0, min(min(end - beg, S), QNT ? 32 : 16));
       const int pos = lane < F ? selv : -1;
       const bool in = lane < F && pos >= 0 && pos < (len + page - 1) / page;
       const int raw = in ? kv.page_table[static_cast<size_t>(b0) * kv.max_pages + pos] : -1;
       const bool ok = in && raw >= 0 && raw < kv.num_phys;
       if (in && !ok) raise_status(kv.status, DSA_STATUS_BAD_PAGE);
       DSA_STAMP_DIRECT(g_trace_stream, 12, kSW * 32 + (raw == -12345));
-      // issue: lane 2q (K) and lane 2q + 1 (V) take page q, so that the copies go out page by
-      // page (F <= kStreamMaxStages = 16 pages; a quantised page block is one copy, from lane 2q)
-      const int q = lane >> 1;
-      const int pos_q = __shfl_sync(0xffffffffu, pos, q);
-      const int raw_q = __shfl_sync(0xffffffffu, raw, q);
-      const bool ok_q = __shfl_sync(0xffffffffu, ok ? 1 : 0, q) != 0;
-      if (q < F) {
-        const uint32_t full = smem_u32(&bars[q]);
-        const uint32_t dst = smem_base + q * stage_bytes;
-        const int rowk = (raw_q * kv.Hkv + h0) * page;
-        if ((lane & 1) == 0) {
-          stage_pos[q] = pos_q;
-          stage_ok[q] = ok_q ? 1 : 0;  // both published by the arrive below
-          if (!ok_q) {
+      if constexpr (QNT) {  // lane q issues page q's block: one bulk copy
+        if (lane < F) {
+          const uint32_t full = smem_u32(&bars[lane]);
+          stage_pos[lane] = pos;
+          stage_ok[lane] = ok ? 1 : 0;  // both published by the arrive below
+          if (!ok) {
             mbar_arrive(full);  // nothing to load: complete the phase with a plain arrival
           } else {
             mbar_arrive_expect_tx(full, stage_tx);
-            if (QNT) bulk_load(dst, a.qkv + static_cast<size_t>(rowk) * kBpt, kBpt * page, full);
+            bulk_load(smem_base + lane * stage_bytes,
+                      a.qkv + static_cast<size_t>((raw * kv.Hkv + h0) * page) * kBpt, kBpt * page,
+                      full);
           }
         }
-        __syncwarp(0xffffffffu >> (32 - 2 * F));  // the byte count is posted before any copy lands
-        if (!QNT && ok_q) {
-          if ((lane & 1) == 0)
-            tma_load_page(dst, &tmK, rowk, full);
-          else
-            tma_load_page(dst + 2 * page * 128, &tmV, rowk, full);
+      } else {
+        // lane 2q (K) and lane 2q + 1 (V) take page q, so that the copies go out page by page
+        const int q = lane >> 1;
+        const int pos_q = __shfl_sync(0xffffffffu, pos, q);
+        const int raw_q = __shfl_sync(0xffffffffu, raw, q);
+        const bool ok_q = __shfl_sync(0xffffffffu, ok ? 1 : 0, q) != 0;
+        if (q < F) {
+          const uint32_t full = smem_u32(&bars[q]);
+          const uint32_t dst = smem_base + q * stage_bytes;
+          const int rowk = (raw_q * kv.Hkv + h0) * page;
+          if ((lane & 1) == 0) {
+            stage_pos[q] = pos_q;
+            stage_ok[q] = ok_q ? 1 : 0;  // both published by the arrive below
+            if (!ok_q)
+              mbar_arrive(full);  // nothing to load: complete the phase with a plain arrival
+            else
+              mbar_arrive_expect_tx(full, stage_tx);
+          }
+          __syncwarp(0xffffffffu >> (32 - 2 * F));  // the byte count is posted before any copy
+          if (ok_q) {
+            if ((lane & 1) == 0)
+              tma_load_page(dst, &tmK, rowk, full);
+            else
+              tma_load_page(dst + 2 * page * 128, &tmV, rowk, full);
+          }
         }
       }
       if (lane == 0) *issued = F;
