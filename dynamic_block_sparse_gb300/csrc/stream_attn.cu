@@ -161,6 +161,15 @@ DSA_DEV uint32_t kv4_pair(uint32_t w, int a, int b) {
   return *reinterpret_cast<const uint32_t*>(&h);
 }
 
+// The same for the nibbles at bits a and a + 16 of w: one shift and one mask-and-or.
+DSA_DEV uint32_t kv4_pair16(uint32_t w, int a) {
+  const uint32_t bits = ((w >> a) & 0x000f000fu) | 0x64006400u;
+  const uint32_t off = 0x64086408u;
+  const __half2 h = __hsub2(*reinterpret_cast<const __half2*>(&bits),
+                            *reinterpret_cast<const __half2*>(&off));
+  return *reinterpret_cast<const uint32_t*>(&h);
+}
+
 // S = Q . codes^T for the 16 code rows at kc (the tile's rows of a KV4 page block).  Lane column
 // tig reads dims 32 tig .. +31 of its token: 16 bytes, k-step ks taking the nibbles of dims
 // 32 tig + 4 ks .. +3 (one 16-bit half of word ks / 2).
@@ -215,7 +224,7 @@ DSA_DEV void tile_pv_kv4(WarpSoftmaxState& st, const uint32_t (&pa)[4], const ui
 #pragma unroll
       for (int n = 0; n < 4; ++n) {
         const int j = 8 * half + 4 * quad + n;
-        mma_f16(st.o[j], pa, kv4_pair(x01, 4 * n, 16 + 4 * n), kv4_pair(x23, 4 * n, 16 + 4 * n));
+        mma_f16(st.o[j], pa, kv4_pair16(x01, 4 * n), kv4_pair16(x23, 4 * n));
       }
     }
   }
@@ -379,6 +388,20 @@ DSA_DEV void load_qT_frags(const __nv_bfloat16* sQ, uint32_t (&qb)[8][4]) {
   }
 }
 
+// The same for the KV4 transposed scores: k-step ks = 2 i + s takes dims 32 tig + 8 i + 2 s,
+// + 2 s + 4 (qb[ks][0]) and + 2 s + 1, + 2 s + 5 (qb[ks][1]).
+DSA_DEV void load_qT_frags_kv4(const __nv_bfloat16* sQ, uint32_t (&qb)[8][4]) {
+  const int lane = threadIdx.x & 31;
+  const int g = lane >> 2, tig = lane & 3;
+  const __nv_bfloat16* row = sQ + g * kHeadDim + 32 * tig;
+#pragma unroll
+  for (int ks = 0; ks < 8; ++ks) {
+    const int d = 8 * (ks >> 1) + 2 * (ks & 1);
+    qb[ks][0] = pack_f16(__bfloat162float(row[d]), __bfloat162float(row[d + 4]));
+    qb[ks][1] = pack_f16(__bfloat162float(row[d + 1]), __bfloat162float(row[d + 5]));
+  }
+}
+
 // S^T for the tile's 16 code rows at kc: sc[0], sc[1] = token g, heads 2 tig, 2 tig + 1;
 // sc[2], sc[3] = token g + 8, the same heads.
 template <int FMT>
@@ -407,16 +430,18 @@ DSA_DEV void tileT_scores(const uint32_t (&qb)[8][4], const uint8_t* kc, float (
       mma_f16(acc[ks & 1], af, qb[ks][0], qb[ks][1]);
     }
   } else {
+    // k-step ks = 2 i + s of lane tig: word i of its 16 bytes (dims 32 tig + 8 i .. + 7), the
+    // dims at nibbles 2 s, 2 s + 4 (k = 2 tig, 2 tig + 1) and 2 s + 1, 2 s + 5 (k = 2 tig + 8, + 9):
+    // each pair 16 bits apart (the query fragments take the same dims, load_qT_frags_kv4)
     const uint4 a4 = *reinterpret_cast<const uint4*>(kc + kv4_row(g) * 64 + 16 * tig);
     const uint4 b4 = *reinterpret_cast<const uint4*>(kc + kv4_row(g + 8) * 64 + 16 * tig);
     const uint32_t wa[4] = {a4.x, a4.y, a4.z, a4.w};
     const uint32_t wb[4] = {b4.x, b4.y, b4.z, b4.w};
 #pragma unroll
     for (int ks = 0; ks < 8; ++ks) {
-      const int h = 16 * (ks & 1);
-      const uint32_t af[4] = {kv4_pair(wa[ks >> 1], h, h + 4), kv4_pair(wb[ks >> 1], h, h + 4),
-                              kv4_pair(wa[ks >> 1], h + 8, h + 12),
-                              kv4_pair(wb[ks >> 1], h + 8, h + 12)};
+      const int sh = 8 * (ks & 1);
+      const uint32_t af[4] = {kv4_pair16(wa[ks >> 1], sh), kv4_pair16(wb[ks >> 1], sh),
+                              kv4_pair16(wa[ks >> 1], sh + 4), kv4_pair16(wb[ks >> 1], sh + 4)};
       mma_f16(acc[ks & 1], af, qb[ks][0], qb[ks][1]);
     }
   }
@@ -518,10 +543,8 @@ DSA_DEV void tileT_softmax_pv(WarpStateT& st, const float (&sc)[4], float scale_
         const uint32_t x01 = __byte_perm(w0, w1, sel), x23 = __byte_perm(w2, w3, sel);
 #pragma unroll
         for (int n = 0; n < 2; ++n) {  // dims + 2 n (rows g) and + 2 n + 1 (rows g + 8)
-          const uint32_t fa[4] = {kv4_pair(x01, 8 * n, 16 + 8 * n),
-                                  kv4_pair(x01, 8 * n + 4, 16 + 8 * n + 4),
-                                  kv4_pair(x23, 8 * n, 16 + 8 * n),
-                                  kv4_pair(x23, 8 * n + 4, 16 + 8 * n + 4)};
+          const uint32_t fa[4] = {kv4_pair16(x01, 8 * n), kv4_pair16(x01, 8 * n + 4),
+                                  kv4_pair16(x23, 8 * n), kv4_pair16(x23, 8 * n + 4)};
           mma_f16(st.o[4 * half + 2 * quad + n], fa, b0, b1);
         }
       }
@@ -1047,7 +1070,9 @@ __global__ void __launch_bounds__(kSThreads, 1)
     const int di = d_first + u;
     uint32_t qa[8][4] = {};
     if (!dry) {
-      if (TR)
+      if (TR && KV4)
+        load_qT_frags_kv4(sQ + slot * 16 * kHeadDim, qa);
+      else if (TR)
         load_qT_frags(sQ + slot * 16 * kHeadDim, qa);
       else if (QNT)
         load_q_frags_kv8(sQ + slot * 16 * kHeadDim, qa);
