@@ -845,7 +845,7 @@ def test_select_threshold(tau, cap, nleft, G):
 
 @pytest.mark.parametrize("bad", ["negative", "too_large"])
 @pytest.mark.parametrize("path", ["meta", "score", "persistent", "splits", "page_partials",
-                                  "streaming"])
+                                  "streaming", "kv8", "kv4"])
 def test_bad_page_id_raises_status_without_fault(bad, path):
     """One bad page-table entry inside a request (negative, or past the pool) per call: the call
     raises DSA_STATUS_BAD_PAGE, skips the page and leaves finite outputs."""
@@ -870,6 +870,16 @@ def test_bad_page_id_raises_status_without_fault(bad, path):
         assert torch.isinf(scores[1, :, 0]).all() and (scores[1, :, 0] < 0).all()
     elif path == "streaming":
         B.dsa_streaming_head_attn(kv, inp["q"][0], 16, 32, 0.1, out, m, l)
+    elif path in ("kv8", "kv4"):  # quantised blocks of the whole pool; the bad entry is read
+        blocks = cache.kv8() if path == "kv8" else cache.kv4()
+        if path == "kv8":
+            ws = torch.zeros(max(16, B.dsa_sparse_decode_attn_kv8_workspace_size(kv, 2)),
+                             dtype=torch.uint8, device="cuda")
+            B.dsa_sparse_decode_attn_kv8(kv, blocks, inp["q"][0], idx, cnt, 0.1, out, m, l, ws)
+        else:
+            ws = torch.zeros(max(16, B.dsa_sparse_decode_attn_kv4_workspace_size(kv, 2)),
+                             dtype=torch.uint8, device="cuda")
+            B.dsa_sparse_decode_attn_kv4(kv, blocks, inp["q"][0], idx, cnt, 0.1, out, m, l, ws)
     else:
         splits = {"persistent": 0, "splits": 2, "page_partials": 1}[path]
         parts = None
