@@ -14,7 +14,8 @@ of a model's layers do: each step reads what the 31 steps before it did not touc
 later, far past the 129 MB L2, so its inputs come from HBM while the kernel's code stays warm.
 Exactly --steps steps are timed with CUDA events.  The single-step figure with L2 flushed before
 each step (a 256 MiB write, then a 256 MiB read of another buffer, outside the timed window;
-this also evicts the kernel's code) is reported beside it as cold_step.
+this also evicts the kernel's code) is reported beside it as cold_step, and the step replayed on
+one layer's caches (data and code warm in L2) as warm_step.
 
 value = algorithmic bytes of the step / device time of the step (GB/s): metadata read by scoring
 + K/V of every page attended (P and A \\ P) + auxiliary state (query, scores, EMA level/trend,
@@ -376,6 +377,22 @@ def bench_prr(args, w, dev, rank):
     cold_ms = timed_replay(single, n_cold, qi0=4)
     dec.t += n_cold
 
+    # ---- 32 steps of one layer in one graph, replayed back to back: the layer's ~14 MB stay in
+    # L2 (data and code warm), launched like the rotation
+    warm_graph = capture([dec] * 32, static_q, parity_steps=1)[0]
+    n_warm_rep = max(4, min(32, args.steps // 32))
+    for _ in range(2):
+        warm_graph.replay()
+    torch.cuda.synchronize()
+    w_ev = [torch.cuda.Event(enable_timing=True) for _ in range(2)]
+    w_ev[0].record(stream)
+    for _ in range(n_warm_rep):
+        warm_graph.replay()
+    w_ev[1].record(stream)
+    torch.cuda.synchronize()
+    warm_ms = w_ev[0].elapsed_time(w_ev[1]) / (32 * n_warm_rep)
+    dec.t += 32 * (n_warm_rep + 2)
+
     # ---- stages of the step as separate launches (layer 0, L2 flushed before each)
     stage_graphs = {}
     for name, fn in (("score_pages", lambda: dec.stage_score(static_q)),
@@ -432,6 +449,9 @@ def bench_prr(args, w, dev, rank):
                  cold_step={"us": cold_mean * 1e3, "us_p50": statistics.median(cold_ms) * 1e3,
                             "gbs": bytes_step / (cold_mean * 1e6),
                             "note": "one step alone, L2 flushed before it (code and data cold)"},
+                 warm_step={"us": warm_ms * 1e3, "gbs": bytes_step / (warm_ms * 1e6),
+                            "note": "32 steps of one layer per graph, replayed back to back with "
+                                    "one query: the layer's data and code stay in L2"},
                  meta_build_ms=meta_build_ms,
                  meta_build_gbs=(rows * n_valid * w.page_size * w.head_dim * 2
                                  + rows * n_valid * 512) / (meta_build_ms * 1e6),
