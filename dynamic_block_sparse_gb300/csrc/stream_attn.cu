@@ -8,16 +8,19 @@
 // one partial record per CTA (at most two per CTA: its first and its last row), and the CTA that
 // takes the row's last ticket merges them in CTA order.  No CTA ever waits for another.
 //
-// Inside a CTA, warp 8 is a TMA producer: it resolves 32 page-table entries at a time and streams
-// whole K/V pages (one 3-D tensor load per pool) through a ring of about 128 KB, several lanes
-// issuing at once.  Warps 0..7 attend with the mma core.  Every (stage, 16-token tile) slot of the
-// ring belongs to one consumer warp for the whole launch, so a warp waits only for the pages it
-// computes on, it waits on every phase of its stages in order (a phase-parity wait is only
-// unambiguous for a waiter that never skips a phase), and each stage is released by exactly the
-// warps that read it.  The producer also
-// publishes each unit (its row, selected slots and request length, and the row's G query vectors
-// by a 1-D bulk copy) through a two-slot mailbox, so the consumers never touch global memory
-// before their epilogues.
+// Inside a CTA, warp 8 is a TMA producer: it sets up the barriers alone and, before its general
+// loop, issues the first unit's first pages from a short straight-line path; the loop then
+// resolves 32 page-table entries at a time and streams whole pages through a ring (bf16: two 3-D
+// tensor loads per page into about 128 KB; quantised blocks: one bulk copy each, up to 64 stages
+// in 160 KB), several lanes issuing at once.  Warps 0..7 attend with the mma core.  Every (stage,
+// 16-token tile) slot of the ring belongs to one consumer warp for the whole launch, so a warp
+// waits only for the pages it computes on, it waits on every phase of its stages in order (a
+// phase-parity wait is only unambiguous for a waiter that never skips a phase), and each stage is
+// released by exactly the warps that read it.  The producer also publishes each unit (its row,
+// selected slots and request length, and the row's G query vectors by a 1-D bulk copy) through a
+// two-slot mailbox, so the consumers never touch global memory before their epilogues.
+// The page format (bf16, KV8, KV4) is a template parameter, and so is the tile orientation of the
+// quantised formats (transposed for query groups of at most 8).
 #include "attn_core.cuh"
 #include <cuda_fp8.h>
 
