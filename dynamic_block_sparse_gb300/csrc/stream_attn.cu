@@ -555,6 +555,104 @@ DSA_DEV void tileT_softmax_pv(WarpStateT& st, const float (&sc)[4], float scale_
   }
 }
 
+// ---- Transposed tiles over bf16 pages (query groups of at most 8): the K tile is the A operand
+// as it lies in the 128-byte-swizzled stage (ldmatrix), the V tile is V^T through a transposing
+// ldmatrix, and O^T's m-tile mt holds dims 16 mt .. + 15 in order (rows g and g + 8).
+
+// B fragments of Q^T in natural dim order: qb[ks][0] = head g's dims 16 ks + 2 tig, + 1 and
+// qb[ks][1] its dims 16 ks + 2 tig + 8, + 9 (bf16 pairs).
+DSA_DEV void load_qT_frags_bf16(const __nv_bfloat16* sQ, uint32_t (&qb)[8][4]) {
+  const int lane = threadIdx.x & 31;
+  const int g = lane >> 2, tig = lane & 3;
+#pragma unroll
+  for (int ks = 0; ks < 8; ++ks) {
+    qb[ks][0] = *reinterpret_cast<const uint32_t*>(sQ + g * kHeadDim + 16 * ks + 2 * tig);
+    qb[ks][1] = *reinterpret_cast<const uint32_t*>(sQ + g * kHeadDim + 16 * ks + 2 * tig + 8);
+  }
+}
+
+// S^T for tokens [row0, row0 + 16) of a staged page (kbase: the K box of dims 0..63; dims 64..127
+// follow at + page * 128): sc as in tileT_scores.
+DSA_DEV void tileT_scores_bf16(const uint32_t (&qb)[8][4], uint32_t kbase, int page, int row0,
+                               float (&sc)[4]) {
+  const int lane = threadIdx.x & 31;
+  const int mi = lane >> 3;
+  const uint32_t tok = static_cast<uint32_t>(row0 + (mi & 1) * 8 + (lane & 7));
+  const uint32_t half_stride = static_cast<uint32_t>(page * 128);
+  float acc[2][4];
+#pragma unroll
+  for (int c = 0; c < 2; ++c)
+#pragma unroll
+    for (int e = 0; e < 4; ++e) acc[c][e] = 0.f;
+#pragma unroll
+  for (int ks = 0; ks < 8; ++ks) {
+    const uint32_t chunk = static_cast<uint32_t>(2 * ks + (mi >> 1));
+    uint32_t af[4];
+    ldsm_x4(kbase + (chunk >> 3) * half_stride + sw128(tok, chunk & 7u), af[0], af[1], af[2],
+            af[3]);
+    mma_bf16(acc[ks & 1], af, qb[ks][0], qb[ks][1]);
+  }
+#pragma unroll
+  for (int e = 0; e < 4; ++e) sc[e] = acc[0][e] + acc[1][e];
+}
+
+// Online-softmax update of the transposed bf16 tile, then O^T += V^T . P^T (vbase: the V box of
+// dims 0..63 of the staged page).
+DSA_DEV void tileT_softmax_pv_bf16(WarpStateT& st, const float (&sc)[4], float scale_log2,
+                                   uint32_t valid, uint32_t vbase, int page, int row0) {
+  const int lane = threadIdx.x & 31;
+  const int g = lane >> 2;
+  const bool va = (valid >> g) & 1u, vb = (valid >> (g + 8)) & 1u;
+  float x[4];
+  x[0] = va ? sc[0] * scale_log2 : -INFINITY;
+  x[1] = va ? sc[1] * scale_log2 : -INFINITY;
+  x[2] = vb ? sc[2] * scale_log2 : -INFINITY;
+  x[3] = vb ? sc[3] * scale_log2 : -INFINITY;
+  float mx[2] = {fmaxf(x[0], x[2]), fmaxf(x[1], x[3])};
+#pragma unroll
+  for (int r = 0; r < 2; ++r)
+#pragma unroll
+    for (int o = 4; o < 32; o <<= 1) mx[r] = fmaxf(mx[r], __shfl_xor_sync(0xffffffffu, mx[r], o));
+  float alpha[2], mnew[2];
+#pragma unroll
+  for (int r = 0; r < 2; ++r) {
+    mnew[r] = fmaxf(st.m[r], mx[r]);
+    alpha[r] = (mnew[r] == -INFINITY) ? 1.f : fast_exp2(st.m[r] - mnew[r]);
+  }
+  float p[4];
+#pragma unroll
+  for (int e = 0; e < 4; ++e) {
+    const int r = e & 1;
+    p[e] = (mnew[r] == -INFINITY) ? 0.f : fast_exp2(x[e] - mnew[r]);
+  }
+  st.l[0] = st.l[0] * alpha[0] + (p[0] + p[2]);
+  st.l[1] = st.l[1] * alpha[1] + (p[1] + p[3]);
+  st.m[0] = mnew[0];
+  st.m[1] = mnew[1];
+  if (!__all_sync(0xffffffffu, alpha[0] == 1.f && alpha[1] == 1.f)) {
+#pragma unroll
+    for (int j = 0; j < 8; ++j) {
+      st.o[j][0] *= alpha[0];
+      st.o[j][1] *= alpha[1];
+      st.o[j][2] *= alpha[0];
+      st.o[j][3] *= alpha[1];
+    }
+  }
+  const uint32_t b0 = movmatrix_trans(pack_bf16(p[0], p[1]));
+  const uint32_t b1 = movmatrix_trans(pack_bf16(p[2], p[3]));
+  const int mi = lane >> 3;
+  const uint32_t tok = static_cast<uint32_t>(row0 + (mi >> 1) * 8 + (lane & 7));
+  const uint32_t half_stride = static_cast<uint32_t>(page * 128);
+#pragma unroll
+  for (int mt = 0; mt < 8; ++mt) {  // dims 16 mt .. + 15
+    const uint32_t chunk = static_cast<uint32_t>(2 * mt + (mi & 1));
+    uint32_t af[4];
+    ldsm_x4_t(vbase + (chunk >> 3) * half_stride + sw128(tok, chunk & 7u), af[0], af[1], af[2],
+              af[3]);
+    mma_bf16(st.o[mt], af, b0, b1);
+  }
+}
+
 // Shared position of output dim d of query head r in the KV8 path's merge area: the pieces of 16
 // dims are XOR-permuted by the writer's column pair and row, so that the fragment stores of a warp
 // spread over the banks.
@@ -1075,8 +1173,10 @@ __global__ void __launch_bounds__(kSThreads, 1)
     if (!dry) {
       if (TR && KV4)
         load_qT_frags_kv4(sQ + slot * 16 * kHeadDim, qa);
-      else if (TR)
+      else if (TR && KV8)
         load_qT_frags(sQ + slot * 16 * kHeadDim, qa);
+      else if (TR)
+        load_qT_frags_bf16(sQ + slot * 16 * kHeadDim, qa);
       else if (QNT)
         load_q_frags_kv8(sQ + slot * 16 * kHeadDim, qa);
       else
@@ -1118,7 +1218,15 @@ __global__ void __launch_bounds__(kSThreads, 1)
         const bool in = tok < L && (tok < lo_end || tok >= hi_beg);
         const uint32_t vm = __ballot_sync(0xffffffffu, in) & 0xffffu;
         if (vm == 0u) continue;
-        if constexpr (TR) {
+        if constexpr (TR && !QNT) {
+          if (vm != 0xffffu)
+            wrote |=
+                zero_invalid_v_rows(vm, smem + s * stage_bytes + 2 * page * 128, page, t * 16);
+          float sc4[4];
+          tileT_scores_bf16(qa, kb, page, t * 16, sc4);
+          tileT_softmax_pv_bf16(st, sc4, a.scale_log2, vm, vb, page, t * 16);
+          continue;
+        } else if constexpr (TR) {
           const uint8_t* blk = smem + s * stage_bytes;  // the page's quantised block
           const int rowb = KV8 ? 128 : 64;  // bytes per code row
           const float* ksc = reinterpret_cast<const float*>(blk + 2 * rowb * page) + t * 16;
@@ -1161,17 +1269,30 @@ __global__ void __launch_bounds__(kSThreads, 1)
     state_finish(st);
 
     // ---- unit epilogue: merge the warps' states of the G query heads
-    if constexpr (TR) {  // lane (g, tig): dims 16 g + 2 mt, + 1 of heads 2 tig, 2 tig + 1
+    if constexpr (TR) {
       const int g8 = lane >> 2, q0 = (lane & 3) * 2;
       float* wO = sO + warp * G * kHeadDim;
 #pragma unroll
       for (int mt = 0; mt < 8; ++mt) {
-        const int d = 16 * g8 + 2 * mt;
-        if (q0 < G)
-          *reinterpret_cast<float2*>(wO + q0 * kHeadDim + d) = make_float2(st.o[mt][0], st.o[mt][2]);
-        if (q0 + 1 < G)
-          *reinterpret_cast<float2*>(wO + (q0 + 1) * kHeadDim + d) =
-              make_float2(st.o[mt][1], st.o[mt][3]);
+        if constexpr (QNT) {  // lane (g, tig): dims 16 g + 2 mt, + 1 of heads 2 tig, 2 tig + 1
+          const int d = 16 * g8 + 2 * mt;
+          if (q0 < G)
+            *reinterpret_cast<float2*>(wO + q0 * kHeadDim + d) =
+                make_float2(st.o[mt][0], st.o[mt][2]);
+          if (q0 + 1 < G)
+            *reinterpret_cast<float2*>(wO + (q0 + 1) * kHeadDim + d) =
+                make_float2(st.o[mt][1], st.o[mt][3]);
+        } else {  // lane (g, tig): dims 16 mt + g, + 8 of heads 2 tig, 2 tig + 1
+          const int d = 16 * mt + g8;
+          if (q0 < G) {
+            wO[q0 * kHeadDim + d] = st.o[mt][0];
+            wO[q0 * kHeadDim + d + 8] = st.o[mt][2];
+          }
+          if (q0 + 1 < G) {
+            wO[(q0 + 1) * kHeadDim + d] = st.o[mt][1];
+            wO[(q0 + 1) * kHeadDim + d + 8] = st.o[mt][3];
+          }
+        }
       }
       if (g8 == 0) {
         if (q0 < G) {
@@ -1394,14 +1515,15 @@ cudaError_t launch_stream_attn(const CUtensorMap& tmK, const CUtensorMap& tmV,
     if (e != cudaSuccess) return e;
     return launch_pdl(kernel, grid, kSThreads, bytes, s, tmK, tmV, a);
   };
-  // quantised pages: the transposed tiles when the query group fits their n8 columns
+  // the transposed tiles when the query group fits their n8 columns
   const bool tr = a.kv.G <= 8;
   if (fmt == kFmtKv8)
     return tr ? go(stream_attn_kernel<false, kFmtKv8, true>) : go(stream_attn_kernel<false, kFmtKv8>);
   if (fmt == kFmtKv4)
     return tr ? go(stream_attn_kernel<false, kFmtKv4, true>) : go(stream_attn_kernel<false, kFmtKv4>);
-  return a.stream_stride > 0 ? go(stream_attn_kernel<true, kFmtBf16>)
-                             : go(stream_attn_kernel<false, kFmtBf16>);
+  if (a.stream_stride > 0)
+    return tr ? go(stream_attn_kernel<true, kFmtBf16, true>) : go(stream_attn_kernel<true, kFmtBf16>);
+  return tr ? go(stream_attn_kernel<false, kFmtBf16, true>) : go(stream_attn_kernel<false, kFmtBf16>);
 }
 
 }  // namespace dsa
