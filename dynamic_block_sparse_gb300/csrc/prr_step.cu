@@ -142,8 +142,10 @@ DSA_DEV unsigned ld_acquire(const unsigned* p) {
   return v;
 }
 
-// One thread: waits until *ctr reaches target (compared as a sequence number).  Bounded: gives up
-// after kWaitLimitNs, raising DSA_STATUS_TIMEOUT and the CTA's abort flag.
+// One thread: waits until *ctr reaches target (compared as a sequence number).  Each poll is one
+// L2 round trip and there is no sleep between polls, so the count is seen complete about one
+// round trip after its last increment; one thread per CTA polls.  Bounded: gives up after
+// kWaitLimitNs, raising DSA_STATUS_TIMEOUT and the CTA's abort flag.
 DSA_DEV void wait_count(const unsigned* ctr, unsigned target, volatile int* abort,
                         int32_t* status) {
   if (*abort || static_cast<int>(ld_acquire(ctr) - target) >= 0) return;
@@ -154,7 +156,6 @@ DSA_DEV void wait_count(const unsigned* ctr, unsigned target, volatile int* abor
       raise_status(status, DSA_STATUS_TIMEOUT);
       return;
     }
-    __nanosleep(32);
   }
 }
 
@@ -829,6 +830,17 @@ __global__ void __launch_bounds__(kThreads, 1)
     return cntP;
   };
 
+  // The counters go back to zero once every CTA has arrived at the exit count: the last to
+  // arrive resets them.  A CTA arrives after its last wait on a counter; every increment of the
+  // counters has then been seen by a wait of some CTA that arrived before it, so none is in flight.
+  auto reset_counters = [&]() {
+    for (int r = 0; r < rows; ++r) {
+      W.done[r] = 0u;
+      W.sdone[r] = 0u;
+    }
+    *W.exit = 0u;
+  };
+  bool arrived = false;  // (uniform) the CTA has arrived at the exit count
   for (int task = split ? (cta < n_tasks ? cta : n_tasks) : cta; task < n_tasks;
        task += split ? n_tasks : grid) {
     __syncthreads();  // the previous task's shared data are no longer read
@@ -878,6 +890,13 @@ __global__ void __launch_bounds__(kThreads, 1)
     __syncthreads();
     if (*abort_flag) break;
     DSA_STAMP(8);  // task: ranked
+    // with the records on chip the waits on the row's counters are behind this CTA: in its last
+    // task the issue warp arrives at the exit count now and reads the ticket once it has issued
+    // the missed pages, which takes the arrival off the launch's tail
+    const bool early_exit = a.rec_smem && task + (split ? n_tasks : grid) >= n_tasks;
+    unsigned exit_ticket = 0u;
+    if (early_exit && warp == kW && lane == 0) exit_ticket = atomicAdd(W.exit, 1u);
+    arrived = early_exit;
     cntA = s_red[3];
     const bool bits_ok = cntA >= 0;  // the A_t and P_t bitmaps hold
     if (cntA == -1) {  // the keys are in place: P_t's bound over them, else every key
@@ -969,9 +988,11 @@ __global__ void __launch_bounds__(kThreads, 1)
     // state and leaves query head g's part of it (unnormalised O, max in log2 units, sum) in
     // wst[w]
     if (warp == kW) {
-      if (lane == 0)
+      if (lane == 0) {
         for (int i = 0; i < n_miss; ++i)
           if (!issue(ring + i, row, mlist[i], true, npos)) break;
+        if (early_exit && exit_ticket == gridDim.x - 1) reset_counters();
+      }
       __syncwarp();
     } else {
       float* ws = wst + warp * kWs;
@@ -1122,17 +1143,10 @@ __global__ void __launch_bounds__(kThreads, 1)
     return;
   }
 
-  // ---- the last CTA out sets the counters back to zero for the next call
-  if (tid == 0) {
+  // ---- the CTAs that have not arrived yet (workers, selections) arrive on their way out
+  if (tid == 0 && !arrived) {
     __threadfence();
-    if (atomicAdd(W.exit, 1u) == gridDim.x - 1) {
-      for (int r = 0; r < rows; ++r) {
-        W.done[r] = 0u;
-        W.sdone[r] = 0u;
-      }
-      *W.exit = 0u;
-      __threadfence();
-    }
+    if (atomicAdd(W.exit, 1u) == gridDim.x - 1) reset_counters();
   }
   DSA_STAMP(13);  // end
   DSA_TRACE_END(g_trace_prr);
