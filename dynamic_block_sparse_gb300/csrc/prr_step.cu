@@ -208,6 +208,7 @@ __global__ void __launch_bounds__(kThreads, 1)
   __shared__ unsigned s_t0, s_hint, s_kmid, s_klow;
   __shared__ int s_wlo, s_whi;  // the workers whose shares meet a task's row
   __shared__ int s_ccnt;  // a worker's candidates of the current segment
+  __shared__ int s_cntp;  // |P_t| of a task prepared during the worker phase
   const KvView& kv = a.kv;
   const Ws& W = a.ws;
   const int page = kv.p, G = kv.G, tiles = page / 16, S = a.stages;
@@ -232,6 +233,43 @@ __global__ void __launch_bounds__(kThreads, 1)
   const long long s_end = wk < 0 ? 0 : static_cast<long long>(wk + 1) * T / workers;
   const int n_items = rows * kp;
   const int my_items = cta < n_items ? (n_items - 1 - cta) / grid + 1 : 0;
+
+  // a merge task's first steps need neither the row's scores nor the ring (compute warps): its
+  // bitmaps cleared and P_t's positions (in pl) marked, the workers whose shares meet its row
+  // found.  A barrier of the compute warps must follow before these are read.
+  TopkScratch& ts = sel.small;
+  int32_t* pl = reinterpret_cast<int32_t*>(smem + lay.pl_off);  // P_t's positions
+  auto merge_prep = [&](int row, int cntP) {
+    const int nwords = (n + 31) >> 5;
+    uint32_t* abits = ts.bits;
+    uint32_t* pbits = ts.bits + kBitsMax / 32;
+    if (n <= kBitsMax)
+      for (int w = tid; w < nwords; w += kCT) abits[w] = pbits[w] = 0u;
+    if (tid == 0) {
+      s_hint = 0u;
+      ts.n_cand = 0;
+    }
+    if (tid == 32) {
+      // the workers whose shares [w T / workers, (w + 1) T / workers) meet [r0, r1): from the
+      // one holding slot r0 to the one holding slot r1 - 1
+      const long long r0 = static_cast<long long>(row) * n, r1 = r0 + n;
+      auto holder = [&](long long x) {
+        int w = static_cast<int>(min(static_cast<long long>(workers - 1), x * workers / T));
+        while (w > 0 && static_cast<long long>(w) * T / workers > x) --w;
+        while (w + 1 < workers && static_cast<long long>(w + 1) * T / workers <= x) ++w;
+        return w;
+      };
+      s_wlo = holder(r0);
+      s_whi = holder(r1 - 1);
+    }
+    named_barrier(1, kCT);
+    if (n <= kBitsMax)
+      for (int i = tid; i < cntP; i += kCT)
+        if (pl[i] >= 0 && pl[i] < n) atomicOr(&pbits[pl[i] >> 5], 1u << (pl[i] & 31));
+  };
+  // in split mode a merge-task CTA has one task, known now: its compute warps, idle while the issue
+  // warp attends the CTA's page of P_t, take the task's first steps meanwhile
+  const bool pre = split && cta < rows * G;
 
   volatile int* stage_ok = s_ctl;  // -1 nothing, 0 empty part, 1 page loaded
   volatile int* stage_pos = s_ctl + S;
@@ -497,6 +535,14 @@ __global__ void __launch_bounds__(kThreads, 1)
     DSA_STAMP(2);  // worker: its share scored and published
 
     DSA_STAMP(3);  // the compute warps' part is over (thread 0)
+    if (pre) {
+      const int row = cta / G;
+      const int cntP = min(max(a.spec_count[row], 0), kp);
+      for (int i = tid; i < cntP; i += kCT) pl[i] = a.spec_idx[static_cast<size_t>(row) * kp + i];
+      if (tid == 0) s_cntp = cntP;
+      named_barrier(1, kCT);  // pl written
+      merge_prep(row, cntP);
+    }
   }
   __syncthreads();
   DSA_STAMP(4);  // the CTA's worker part is over
@@ -509,10 +555,8 @@ __global__ void __launch_bounds__(kThreads, 1)
   // (row, query head) merges first, then one P_{t+1} selection per row.  In a merge the seven
   // compute warps select A_t while the TMA issue warp brings the speculative records of the task's
   // query head on chip.
-  TopkScratch& ts = sel.small;
   uint32_t* keys = reinterpret_cast<uint32_t*>(smem + lay.keys_off);  // a row's keys
   float* srec = reinterpret_cast<float*>(smem + lay.rec_off);  // P_t's records of one head
-  int32_t* pl = reinterpret_cast<int32_t*>(smem + lay.pl_off);  // P_t's positions
   uint32_t* pk = reinterpret_cast<uint32_t*>(smem + lay.pk_off);  // their keys
   int32_t* sA = reinterpret_cast<int32_t*>(smem + lay.sa_off);
   int32_t* mlist = reinterpret_cast<int32_t*>(smem + lay.list_off);  // missed positions
@@ -688,32 +732,11 @@ __global__ void __launch_bounds__(kThreads, 1)
   // kCandCap candidates) returns -1 with the row's keys in place for the caller's full selection.
   // -2 after a timeout.  Bitmaps (rows of at most kBitsMax pages): ts.bits[0, w) A_t,
   // ts.bits[kBitsMax / 32, +w) P_t, the latter marked while the workers still score the row.
-  auto select_merge = [&](int row, int kk, int cntP, int32_t* out) -> int {
+  auto select_merge = [&](int row, int kk, int cntP, int32_t* out, bool prepared) -> int {
     const int nwords = (n + 31) >> 5;
     uint32_t* abits = ts.bits;
-    uint32_t* pbits = ts.bits + kBitsMax / 32;
     unsigned long long* cv = reinterpret_cast<unsigned long long*>(ts.hist);
-    if (n <= kBitsMax)
-      for (int w = tid; w < nwords; w += kCT) abits[w] = pbits[w] = 0u;
-    if (tid == 0) {
-      s_hint = 0u;
-      ts.n_cand = 0;
-      // the workers whose shares [w T / workers, (w + 1) T / workers) meet [r0, r1): from the
-      // one holding slot r0 to the one holding slot r1 - 1
-      const long long r0 = static_cast<long long>(row) * n, r1 = r0 + n;
-      auto holder = [&](long long x) {
-        int w = static_cast<int>(min(static_cast<long long>(workers - 1), x * workers / T));
-        while (w > 0 && static_cast<long long>(w) * T / workers > x) --w;
-        while (w + 1 < workers && static_cast<long long>(w + 1) * T / workers <= x) ++w;
-        return w;
-      };
-      s_wlo = holder(r0);
-      s_whi = holder(r1 - 1);
-    }
-    named_barrier(1, kCT);
-    if (n <= kBitsMax)
-      for (int i = tid; i < cntP; i += kCT)
-        if (pl[i] >= 0 && pl[i] < n) atomicOr(&pbits[pl[i] >> 5], 1u << (pl[i] & 31));
+    if (!prepared) merge_prep(row, cntP);
     if (tid == 0) wait_count(W.done + row, static_cast<unsigned>(n), abort_flag, kv.status);
     DSA_STAMP(6);  // task: the row's scores are complete
     if (named_barrier_or(1, kCT, *abort_flag)) return -2;
@@ -862,8 +885,9 @@ __global__ void __launch_bounds__(kThreads, 1)
     const int L = request_len(kv, b);
     const int npos = (L + page - 1) / page;
     const size_t qhead = static_cast<size_t>(b) * kv.Hq + static_cast<size_t>(row % kv.Hkv) * G + g;
-    const int cntP = load_plist(row);
-    __syncthreads();
+    const bool prepared = pre && task == cta;  // its first steps taken in the worker phase
+    const int cntP = prepared ? s_cntp : load_plist(row);
+    if (!prepared) __syncthreads();
     DSA_STAMP(5);  // task (merge): start
     const float* recs = a.partials + static_cast<size_t>(row) * kp * G * kRecordFloats;
     // the issue warp: once the row's records are written, query head g's of them on chip
@@ -884,7 +908,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     if (warp == kW) {
       fetch_records();
     } else {
-      const int got = select_merge(row, a.k, cntP, sA);
+      const int got = select_merge(row, a.k, cntP, sA, prepared);
       if (tid == 0) s_red[3] = got;
     }
     __syncthreads();
