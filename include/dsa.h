@@ -412,9 +412,10 @@ size_t dsa_calibrate_ema_workspace_size(int32_t steps, int32_t rows, int32_t n, 
  * long while it runs; its waits are bounded and raise DSA_STATUS_TIMEOUT), launched as a
  * programmatic dependent of the previous kernel in the stream: its CTAs are scheduled while that
  * kernel finishes and wait for it before reading global memory.  No CTA waits for the whole grid:
- * every CTA scores an equal
- * share of the (request, KV head, page) slots beside its pages of P_t, and the selections, the
- * repair and the merges wait only for their own row's counters.
+ * the worker CTAs (all CTAs but the task CTAs when the grid holds at least four CTAs per task,
+ * else every CTA) score equal shares of the (request, KV head, page) slots, every CTA attends its
+ * pages of P_t, and the selections, the repair and the merges wait only for their own row's
+ * counters.
  *   args->q            : bf16 [B][Hq][D], 16-byte aligned.  Device memory, or page-locked host
  *                        memory mapped for the device (cudaHostAlloc / cudaHostRegister): the
  *                        kernel then reads the query over the host link itself, no copy needed.
