@@ -3,8 +3,9 @@
 // of the missed pages and the merge), organised so that no CTA ever waits for the whole grid.
 //
 // Roles.  With few (row, query head) tasks (at most a quarter of the grid), the first CTAs only run
-// tasks and the others (the workers) score; otherwise every CTA is a worker first and then takes
-// tasks round robin.
+// tasks and the others (the workers) score; a task CTA's compute warps take its task's first steps
+// (the P_t list, the bitmaps, the row's workers) while its eighth warp attends its pages of P_t.
+// Otherwise every CTA is a worker first and then takes tasks round robin.
 //   scoring  each worker scores an equal share of the (row, page) slots with the scoring kernel's
 //            arithmetic (every page-table entry, length, EMA state and query load of a round in
 //            flight at once, then the metadata records), updates the EMA state of those pages at
@@ -30,8 +31,9 @@
 //            one more task ranks P_{t+1} from the new predictions with T0's counterpart (the
 //            k_pred-th largest prediction over P_t).
 // Each wait is on a per-row counter that only work done before any wait advances, so every wait
-// ends; all are bounded (DSA_STATUS_TIMEOUT after 2 s).  The last CTA out sets the counters back
-// to zero.
+// ends; all are bounded (DSA_STATUS_TIMEOUT after 2 s).  Every CTA arrives at an exit count after
+// its last wait (a merge task's eighth warp in mid-task, the other CTAs on their way out); the
+// last to arrive sets the counters back to zero.
 #include "attn_core.cuh"
 #include "internal.h"
 #include "score_core.cuh"
