@@ -522,6 +522,90 @@ def test_pins_catch_planted_mistakes(monkeypatch):
     assert swapped[0].tolist() != kv4["bytes"]
 
 
+
+def _plant(mp, name, fn):
+    """Replaces one oracle routine (package and module names alike) for the context's duration."""
+    mp.setattr(O, name, fn)
+    mp.setattr(OD, name, fn)
+
+
+def _pin_fails(pin, *cases):
+    """True when the pin raises on at least one of its cases."""
+    for args in cases:
+        try:
+            pin(*args)
+        except AssertionError:
+            return True
+    return False
+
+
+def test_pins_catch_planted_mistakes_in_metadata_selection_and_merge(monkeypatch):
+    """More plausible mistakes, each planted in the oracle (on the CPU): the pin named beside each
+    must fail with it in place (and passes without it, as the pins above show)."""
+    orig_repair = OD.spec_repair
+
+    def merge_wrong_sign(parts):  # the rescale exponents taken the wrong way round
+        parts = list(parts)
+        G, D = parts[0][0].shape
+        Om, m, l = np.zeros((G, D)), np.full(G, -np.inf), np.zeros(G)
+        for (Op, mp_, lp) in parts:
+            for g in range(G):
+                if lp[g] == 0.0:
+                    continue
+                if l[g] == 0.0:
+                    Om[g], m[g], l[g] = Op[g], mp_[g], lp[g]
+                    continue
+                m_new = max(m[g], mp_[g])
+                a = math.exp(m_new - m[g]) * l[g]
+                b = math.exp(m_new - mp_[g]) * lp[g]
+                Om[g] = (a * Om[g] + b * Op[g]) / (a + b)
+                m[g], l[g] = m_new, a + b
+        return Om, m, l
+
+    plants = [
+        # LServe §4.2: a physical page's importance is the max of its logical pages, not the mean
+        ("physical_scores",
+         lambda s, g: np.array([np.asarray(s, dtype=np.float64)[p * g:(p + 1) * g].mean()
+                                for p in range(-(-len(s) // g))]),
+         test_hier_matches_brute_force_over_physical_pages, [(i,) for i in range(20)]),
+        # PSA §5: a ragged last block averages over its valid tokens, not the full block size
+        ("page_meta_mean",
+         lambda K, b: np.stack([K[j * b:(j + 1) * b].sum(axis=0) / b for j in range(-(-len(K) // b))]),
+         test_mean_meta_closed_forms, [()]),
+        # LServe §4.2: the max is taken per channel, not once over two whole dot products
+        ("score_pages_minmax",
+         lambda qb, kmax, kmin: np.maximum(kmax @ qb, kmin @ qb),
+         test_quest_score_is_maximum_over_box_corners, [(i,) for i in range(3)]),
+        # PRR §3.3: the running maximum rescales both parts by exp(m_old - m_new)
+        ("merge_partials", merge_wrong_sign,
+         test_merge_of_disjoint_parts_equals_attention_over_union, [(i,) for i in range(4)]),
+        # LServe §4.1: the local window ends at the current token
+        ("streaming_token_ids",
+         lambda L, sink, local: np.asarray(sorted(set(range(min(sink, L))) |
+                                                  set(range(max(0, L - local - 1), L - 1))),
+                                           dtype=np.int64),
+         test_streaming_window_matches_lambda_mask, [()]),
+        # PRR §3.1: the prediction scales the trend by gamma, not the level
+        ("ema_predict",
+         lambda ell, v, gamma: gamma * np.asarray(ell, dtype=np.float64) + np.asarray(v),
+         test_ema_hand_sequence, [()]),
+        # PRR §5: the group's representative query is the mean of its heads, not the sum
+        ("representative_query",
+         lambda qg: OD.to_f64(qg).sum(axis=0),
+         test_representative_query_is_group_mean, [()]),
+        # PRR §3.3 exact mode: speculative parts of pages outside A are dropped, not merged
+        ("spec_repair",
+         lambda *a, superset=False, **kw: orig_repair(*a, superset=True, **kw),
+         test_spec_plus_repair_equals_attention_over_true_set, [("random",), ("disjoint",)]),
+    ]
+    for name, wrong, pin, cases in plants:
+        with monkeypatch.context() as mp:
+            _plant(mp, name, wrong)
+            assert _pin_fails(pin, *cases), f"{pin.__name__} does not catch a wrong {name}"
+    for name, _, pin, cases in plants:  # and every pin passes on the oracle as it stands
+        assert not _pin_fails(pin, *cases), f"{pin.__name__} fails on the unchanged oracle"
+
+
 # ------------------------------------------------------------------------------------ KV8
 
 def test_kv8_codes_match_the_e4m3_format():
