@@ -604,6 +604,11 @@ def test_pins_catch_planted_mistakes_in_metadata_selection_and_merge(monkeypatch
             assert _pin_fails(pin, *cases), f"{pin.__name__} does not catch a wrong {name}"
     for name, _, pin, cases in plants:  # and every pin passes on the oracle as it stands
         assert not _pin_fails(pin, *cases), f"{pin.__name__} fails on the unchanged oracle"
+    # PSA §3.2: the stop rule compares against the smallest block mass seen, not the largest
+    with monkeypatch.context() as mp:
+        mp.setattr(OD.np, "minimum", np.maximum)
+        assert _pin_fails(test_psa_stop_count_matches_zipf_closed_form, ())
+    assert not _pin_fails(test_psa_stop_count_matches_zipf_closed_form, ())
 
 
 # ------------------------------------------------------------------------------------ KV8
