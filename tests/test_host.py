@@ -326,6 +326,31 @@ def test_bench_rows_only_rejects_unknown_workload():
     assert r.returncode != 0 and "no rows for prr_512k" in r.stderr
 
 
+def test_bench_reference_arm_prints_the_contract_line():
+    """``bench.py --impl reference`` times the oracle on the host cores and prints one JSON line
+    with the GPU arm's metric, unit and workload, its own cpu_baseline and an e2e equal to its
+    value; under a launcher's rank other than 0 it exits 0 without output."""
+    cmd = [sys.executable, os.path.join(ROOT, "bench.py"), "--impl", "reference", "--steps", "1",
+           "--warmup", "0"]
+    r = subprocess.run(cmd, capture_output=True, text=True, timeout=600)
+    assert r.returncode == 0, r.stderr[-2000:]
+    line = json.loads(r.stdout.strip().splitlines()[-1])
+    sys.path.insert(0, ROOT)
+    import bench
+    assert line["impl"] == "reference" and line["metric"] == bench.METRIC
+    assert line["unit"] == "GB/s" and line["higher_is_better"] is True
+    assert line["value"] > 0 and line["steps"] == 1 and line["n_gpus"] == 1
+    assert line["config"]["workload"].startswith("prr_512k:")
+    cb = line["cpu_baseline"]
+    assert cb["kind"] == "oracle" and cb["cores"] >= 1 and cb["value"] == line["value"] and cb["sample"]
+    e2e = line["e2e"]
+    assert e2e["value"] == line["value"] and e2e["unit"] == line["unit"]
+    assert e2e["h2d_bytes_per_step"] == 0 and e2e["d2h_bytes_per_step"] == 0
+    env = dict(os.environ, RANK="1", WORLD_SIZE="2", LOCAL_RANK="1")
+    r1 = subprocess.run(cmd, capture_output=True, text=True, timeout=600, env=env)
+    assert r1.returncode == 0 and r1.stdout.strip() == ""
+
+
 def test_stream_k_cut_geometry():
     """The persistent attention's stream-K bookkeeping, restated: CTA c of n holds the slots
     [c T / n, (c + 1) T / n) of T, and slot x belongs to CTA ((x + 1) n - 1) / T.  A row (unit) is
